@@ -1,0 +1,378 @@
+/*
+ * moe_oracle.c -- plain, slow CPU statement of the local Mixture-of-Experts
+ * FFN forward (softmax top-k routing, compact dispatch, bias-free SwiGLU
+ * experts, weighted combine, residual Add + RMSNorm).
+ *
+ * TEST INFRASTRUCTURE. Only the test suite, the smoke check and the timed CPU
+ * baseline of the benchmark load this file's library. It shares no code,
+ * header, table or helper with the CUDA path, and the CUDA path never calls it.
+ *
+ * Sources (page title, section):
+ *   [ruDNN-4]  ruDNN user guide, section 4 "Routing contract" (German and
+ *              Chinese editions): FP32 softmax over all E experts before
+ *              top-k; ties favour the lower expert id; optional
+ *              renormalisation of the selected weights, then a cast to the
+ *              logits dtype; rows holding NaN or +inf, or only -inf, keep NaN
+ *              weights; indices are U32 of shape [T, top_k].
+ *   [ruDNN-5]  ruDNN user guide, section 5 "Expert weights and dispatch":
+ *              x [T,H], gate/up [E,I,H], down [E,H,I], one float dtype;
+ *              dispatch drops nothing; order inside an expert is unspecified;
+ *              a saved map restores token order.
+ *   [ruDNN-3]  ruDNN user guide, section 3 "MoE workflow": logits ->
+ *              softmax/top-k -> compact dispatch -> SwiGLU experts ->
+ *              weighted combine; bias-free experts.
+ *   [ruDNN-7]  ruDNN user guide, section 7 "LayerNorm, RMSNorm and Softmax":
+ *              last-axis RMSNorm, epsilon finite and > 0, FP32 statistics,
+ *              output in the input dtype.
+ *   [Ascend-CARN] aclnnMoeDistributeCombineAddRmsNormV2, "Function" formula:
+ *              combineOut = sum_k(expertScales * expert output),
+ *              x = combineOut + residualX,
+ *              y = x / sqrt(mean(x^2) + normEps) * gamma; outputs yOut, xOut
+ *              (residual dtype) and rstdOut (FP32, one per token).
+ *   [aclnnFFN] aclnnFFN, "Formula": y = activation(x W1 + b1) W2 + b2; the
+ *              experts here are its bias-free, SwiGLU-activated case.
+ *
+ * Precision. Routing follows [ruDNN-4] literally: the softmax is computed in
+ * float (FP32) with libm expf. Everything the pages leave open (expert GEMMs,
+ * combine, norm statistics) is computed in double and left unrounded unless
+ * the pages name an output dtype.
+ *
+ * Readings taken where the pages are silent (each is listed in the design
+ * notes of the repository):
+ *   - selection ranks experts by their FP32 logit, highest first, lower id on
+ *     equal logits; softmax is strictly increasing in the logit, so this is
+ *     the top-k of the exact softmax;
+ *   - the k outputs of a row are written in selection order;
+ *   - an invalid row (NaN, +inf, or all -inf) gets indices 0..k-1 (every key
+ *     ties, so the lower ids win) and NaN weights; it is still dispatched;
+ *   - weights are cast to the logits dtype with or without renormalisation;
+ *   - order inside an expert segment is the assignment order t*k+j here;
+ *     any order is valid, so tests compare per-expert sets;
+ *   - an expert index >= E handed to dispatch gets no row (row_of = -1) and
+ *     makes the token's combined output NaN;
+ *   - RMSNorm statistics are taken on x after it is rounded to the output
+ *     dtype, so the fused op equals RMSNorm applied to xOut.
+ *
+ * Element type codes: 0 = f32, 1 = bf16, 2 = f16 (both stored as raw 16-bit
+ * words), 3 = f64 (oracle-internal arrays only).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { OR_F32 = 0, OR_BF16 = 1, OR_F16 = 2, OR_F64 = 3 };
+
+/* ---- element conversions (IEEE 754 binary32 / bfloat16 / binary16) ----- */
+
+/* bfloat16 is the top half of a binary32 word, so the upcast is exact. */
+static float bf16_bits_to_float(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* binary32 -> bfloat16, round to nearest, ties to even; NaN stays NaN. */
+static uint16_t float_to_bf16_bits(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7fffffffu) > 0x7f800000u)
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t keep_lsb = (u >> 16) & 1u;
+    u += 0x7fffu + keep_lsb;
+    return (uint16_t)(u >> 16);
+}
+
+/* binary16 conversions go through the compiler's IEEE _Float16 type. */
+static float f16_bits_to_float(uint16_t b)
+{
+    _Float16 h;
+    memcpy(&h, &b, sizeof h);
+    return (float)h;
+}
+
+static uint16_t float_to_f16_bits(float f)
+{
+    _Float16 h = (_Float16)f;
+    uint16_t b;
+    memcpy(&b, &h, sizeof b);
+    return b;
+}
+
+static double load_elem(const void *p, int dt, int64_t i)
+{
+    switch (dt) {
+    case OR_F32: return (double)((const float *)p)[i];
+    case OR_BF16: return (double)bf16_bits_to_float(((const uint16_t *)p)[i]);
+    case OR_F16: return (double)f16_bits_to_float(((const uint16_t *)p)[i]);
+    default: return ((const double *)p)[i];
+    }
+}
+
+/* Store v rounded once to dtype dt. For the 16-bit types the value is first
+ * rounded to binary32; doubles that reach this point are already float-exact
+ * (routing weights) or the double rounding is inside every stated tolerance. */
+static void store_elem(void *p, int dt, int64_t i, double v)
+{
+    switch (dt) {
+    case OR_F32: ((float *)p)[i] = (float)v; break;
+    case OR_BF16: ((uint16_t *)p)[i] = float_to_bf16_bits((float)v); break;
+    case OR_F16: ((uint16_t *)p)[i] = float_to_f16_bits((float)v); break;
+    default: ((double *)p)[i] = v; break;
+    }
+}
+
+/* Exposed so tests can pin the conversions against library routines. */
+void oracle_convert(const void *src, int sdt, void *dst, int ddt, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        store_elem(dst, ddt, i, load_elem(src, sdt, i));
+}
+
+/* ---- routing [ruDNN-4] -------------------------------------------------- */
+
+/*
+ * For every token t: upcast the E logits to FP32; classify the row; FP32
+ * softmax over all E (max-subtracted, summed in ascending expert order);
+ * pick top_k experts one at a time, each pick the highest remaining FP32
+ * logit with the lower id kept on equal logits; optionally divide the picked
+ * probabilities by their FP32 sum (taken in slot order); cast to the logits
+ * dtype. Returns the number of invalid rows, or -1 on bad arguments.
+ */
+int64_t oracle_route(const void *logits, int ldt, int64_t T, int64_t E,
+                     int64_t top_k, int renormalize, uint32_t *idx, void *w)
+{
+    if (T < 0 || E < 1 || top_k < 1 || top_k > E)
+        return -1;
+    float *l = (float *)malloc((size_t)E * sizeof(float));
+    float *p = (float *)malloc((size_t)E * sizeof(float));
+    float *sel = (float *)malloc((size_t)top_k * sizeof(float));
+    unsigned char *taken = (unsigned char *)malloc((size_t)E);
+    int64_t invalid_rows = 0;
+
+    for (int64_t t = 0; t < T; ++t) {
+        int has_nan_or_pinf = 0, all_ninf = 1;
+        for (int64_t e = 0; e < E; ++e) {
+            l[e] = (float)load_elem(logits, ldt, t * E + e);
+            if (isnan(l[e]) || (isinf(l[e]) && l[e] > 0.0f))
+                has_nan_or_pinf = 1;
+            if (!(isinf(l[e]) && l[e] < 0.0f))
+                all_ninf = 0;
+        }
+        if (has_nan_or_pinf || all_ninf) {
+            for (int64_t j = 0; j < top_k; ++j) {
+                idx[t * top_k + j] = (uint32_t)j;
+                store_elem(w, ldt, t * top_k + j, (double)NAN);
+            }
+            ++invalid_rows;
+            continue;
+        }
+
+        float m = l[0];
+        for (int64_t e = 1; e < E; ++e)
+            if (l[e] > m) m = l[e];
+        float s = 0.0f;
+        for (int64_t e = 0; e < E; ++e)
+            s += expf(l[e] - m);
+        for (int64_t e = 0; e < E; ++e)
+            p[e] = expf(l[e] - m) / s;
+
+        memset(taken, 0, (size_t)E);
+        for (int64_t j = 0; j < top_k; ++j) {
+            int64_t best = -1;
+            for (int64_t e = 0; e < E; ++e) {
+                if (taken[e]) continue;
+                if (best < 0 || l[e] > l[best]) best = e;
+            }
+            taken[best] = 1;
+            idx[t * top_k + j] = (uint32_t)best;
+            sel[j] = p[best];
+        }
+        if (renormalize) {
+            float z = 0.0f;
+            for (int64_t j = 0; j < top_k; ++j) z += sel[j];
+            for (int64_t j = 0; j < top_k; ++j) sel[j] = sel[j] / z;
+        }
+        for (int64_t j = 0; j < top_k; ++j)
+            store_elem(w, ldt, t * top_k + j, (double)sel[j]);
+    }
+    free(l); free(p); free(sel); free(taken);
+    return invalid_rows;
+}
+
+/* ---- dispatch [ruDNN-5] ------------------------------------------------- */
+
+/*
+ * Count assignments per expert, take the exclusive prefix sum, and give each
+ * assignment a = t*top_k + j the next free row of its expert's segment, in
+ * ascending a. row_of[a] is that row; src_of[row] = a is its inverse. An
+ * index >= E gets no row (row_of = -1). src_of entries past the last row are
+ * set to -1. Returns the number of such bad indices, or -1 on bad arguments.
+ */
+int64_t oracle_dispatch(const uint32_t *idx, int64_t T, int64_t top_k, int64_t E,
+                        int32_t *counts, int32_t *offsets, int32_t *row_of,
+                        int32_t *src_of)
+{
+    if (T < 0 || E < 1 || top_k < 1)
+        return -1;
+    int64_t A = T * top_k, bad = 0;
+    int64_t *next = (int64_t *)malloc((size_t)E * sizeof(int64_t));
+    for (int64_t e = 0; e < E; ++e) counts[e] = 0;
+    for (int64_t a = 0; a < A; ++a) {
+        if ((int64_t)idx[a] >= E) ++bad;
+        else ++counts[idx[a]];
+    }
+    offsets[0] = 0;
+    for (int64_t e = 0; e < E; ++e) {
+        offsets[e + 1] = offsets[e] + counts[e];
+        next[e] = offsets[e];
+    }
+    for (int64_t r = 0; r < A; ++r) src_of[r] = -1;
+    for (int64_t a = 0; a < A; ++a) {
+        int64_t e = (int64_t)idx[a];
+        if (e >= E) { row_of[a] = -1; continue; }
+        int64_t r = next[e]++;
+        row_of[a] = (int32_t)r;
+        src_of[r] = (int32_t)a;
+    }
+    free(next);
+    return bad;
+}
+
+/* x_disp[r, :] = x[src_of[r] / top_k, :] for every row r < rows; rows with
+ * src_of < 0 are left untouched. Same dtype on both sides (a copy). */
+void oracle_gather(const void *x, int dt, int64_t H, int64_t top_k,
+                   const int32_t *src_of, int64_t rows, void *x_disp)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        if (src_of[r] < 0) continue;
+        int64_t t = src_of[r] / top_k;
+        for (int64_t h = 0; h < H; ++h)
+            store_elem(x_disp, dt, r * H + h, load_elem(x, dt, t * H + h));
+    }
+}
+
+/* ---- experts [ruDNN-3], [ruDNN-5], [aclnnFFN] --------------------------- */
+
+/*
+ * For each of nrows input rows x_r with expert e = expert_of_row[r]:
+ *   g = Wg[e] x_r, u = Wu[e] x_r          (Wg, Wu are [E, I, H]; length I)
+ *   h = SiLU(g) * u, SiLU(z) = z / (1 + exp(-z))
+ *   out_r = Wd[e] h                       (Wd is [E, H, I]; length H)
+ * in double, unrounded. x and the weights share dtype dt.
+ * Returns 0, or -1 when an expert id is out of range.
+ */
+int oracle_swiglu_rows(const void *xrows, int dt, int64_t nrows,
+                       const int32_t *expert_of_row, const void *gate,
+                       const void *up, const void *down, int64_t E, int64_t H,
+                       int64_t I, double *out)
+{
+    double *xr = (double *)malloc((size_t)H * sizeof(double));
+    double *hv = (double *)malloc((size_t)I * sizeof(double));
+    int rc = 0;
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t e = expert_of_row[r];
+        if (e < 0 || e >= E) { rc = -1; break; }
+        for (int64_t k = 0; k < H; ++k) xr[k] = load_elem(xrows, dt, r * H + k);
+        for (int64_t i = 0; i < I; ++i) {
+            double g = 0.0, u = 0.0;
+            int64_t wrow = (e * I + i) * H;
+            for (int64_t k = 0; k < H; ++k) {
+                g += load_elem(gate, dt, wrow + k) * xr[k];
+                u += load_elem(up, dt, wrow + k) * xr[k];
+            }
+            hv[i] = g / (1.0 + exp(-g)) * u;
+        }
+        for (int64_t o = 0; o < H; ++o) {
+            double acc = 0.0;
+            int64_t wrow = (e * H + o) * I;
+            for (int64_t i = 0; i < I; ++i)
+                acc += load_elem(down, dt, wrow + i) * hv[i];
+            out[r * H + o] = acc;
+        }
+    }
+    free(xr); free(hv);
+    return rc;
+}
+
+/* The dispatched form: rows [offsets[e], offsets[e+1]) belong to expert e. */
+int oracle_experts_dispatched(const void *x_disp, int dt, const int32_t *offsets,
+                              int64_t E, const void *gate, const void *up,
+                              const void *down, int64_t H, int64_t I, double *out)
+{
+    int64_t rows = offsets[E];
+    int32_t *owner = (int32_t *)malloc((size_t)(rows > 0 ? rows : 1) * sizeof(int32_t));
+    for (int64_t e = 0; e < E; ++e)
+        for (int64_t r = offsets[e]; r < offsets[e + 1]; ++r) owner[r] = (int32_t)e;
+    int rc = oracle_swiglu_rows(x_disp, dt, rows, owner, gate, up, down, E, H, I, out);
+    free(owner);
+    return rc;
+}
+
+/* ---- combine [ruDNN-3], [Ascend-CARN] ----------------------------------- */
+
+/*
+ * y[t, :] = sum over slots j < top_k, in slot order, of
+ *           w[t, j] * out_disp[row_of[t*top_k + j], :]
+ * in double, unrounded. A slot with row_of < 0 makes the whole row NaN.
+ */
+void oracle_combine(const void *out_disp, int odt, const void *w, int wdt,
+                    const int32_t *row_of, int64_t T, int64_t top_k, int64_t H,
+                    double *y)
+{
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t h = 0; h < H; ++h) {
+            double acc = 0.0;
+            for (int64_t j = 0; j < top_k; ++j) {
+                int64_t r = row_of[t * top_k + j];
+                if (r < 0) { acc = NAN; break; }
+                acc += load_elem(w, wdt, t * top_k + j) * load_elem(out_disp, odt, r * H + h);
+            }
+            y[t * H + h] = acc;
+        }
+    }
+}
+
+/* ---- RMSNorm [ruDNN-7], Add + RMSNorm [Ascend-CARN] --------------------- */
+
+/* y = x / sqrt(mean over H of x^2 + eps) * gamma, rstd = 1/sqrt(mean + eps).
+ * Returns -1 when eps is not finite and positive. */
+int oracle_rmsnorm(const void *x, int xdt, const void *gamma, int gdt, float eps,
+                   int64_t T, int64_t H, void *y, int ydt, float *rstd)
+{
+    if (!(isfinite(eps) && eps > 0.0f)) return -1;
+    for (int64_t t = 0; t < T; ++t) {
+        double ss = 0.0;
+        for (int64_t h = 0; h < H; ++h) {
+            double v = load_elem(x, xdt, t * H + h);
+            ss += v * v;
+        }
+        double r = 1.0 / sqrt(ss / (double)H + (double)eps);
+        if (rstd) rstd[t] = (float)r;
+        for (int64_t h = 0; h < H; ++h)
+            store_elem(y, ydt, t * H + h,
+                       load_elem(x, xdt, t * H + h) * r * load_elem(gamma, gdt, h));
+    }
+    return 0;
+}
+
+/*
+ * x = combine + residual, rounded to the residual dtype -> x_out;
+ * rstd = 1/sqrt(mean(x_out^2) + eps) -> rstd (FP32);
+ * y = x_out * rstd * gamma -> y (residual dtype).
+ * combine is the unrounded double result of oracle_combine.
+ */
+int oracle_add_rmsnorm(const double *combine, const void *residual, int rdt,
+                       const void *gamma, int gdt, float eps, int64_t T,
+                       int64_t H, void *y, void *x_out, float *rstd)
+{
+    if (!(isfinite(eps) && eps > 0.0f)) return -1;
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t h = 0; h < H; ++h)
+            store_elem(x_out, rdt, t * H + h,
+                       combine[t * H + h] + load_elem(residual, rdt, t * H + h));
+    return oracle_rmsnorm(x_out, rdt, gamma, gdt, eps, T, H, y, rdt, rstd);
+}

@@ -1,0 +1,84 @@
+"""Plant plausible mistakes in a copy of the oracle (on the CPU) and check
+that the pins catch every one of them.
+
+Each mutant is a one-place edit of ``oracle/moe_oracle.c`` built into a
+temporary library; at least one ``check_*`` in ``oracle_pins.py`` must fail on
+it. This shows the pins constrain each step of the oracle (routing, dispatch,
+gather, experts, combine, norm, dtype rounding), not only its happy path.
+"""
+
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from oracle_pins import ALL_CHECKS
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "moe_oracle.c")
+
+# (name, text in moe_oracle.c, replacement)
+MUTANTS = [
+    ("tie_to_higher_id", "if (best < 0 || l[e] > l[best]) best = e;",
+     "if (best < 0 || l[e] >= l[best]) best = e;"),
+    ("no_renormalise", "sel[j] = sel[j] / z;", "sel[j] = sel[j];"),
+    ("softmax_no_denominator", "p[e] = expf(l[e] - m) / s;",
+     "p[e] = expf(l[e] - m);"),
+    ("all_ninf_row_valid", "if (has_nan_or_pinf || all_ninf) {",
+     "if (has_nan_or_pinf) {"),
+    ("pinf_row_valid", "if (isnan(l[e]) || (isinf(l[e]) && l[e] > 0.0f))",
+     "if (isnan(l[e]))"),
+    ("silu_wrong_sign", "hv[i] = g / (1.0 + exp(-g)) * u;",
+     "hv[i] = g / (1.0 + exp(g)) * u;"),
+    ("gate_up_swapped", "hv[i] = g / (1.0 + exp(-g)) * u;",
+     "hv[i] = u / (1.0 + exp(-u)) * g;"),
+    ("silu_dropped_gate", "hv[i] = g / (1.0 + exp(-g)) * u;",
+     "hv[i] = 1.0 / (1.0 + exp(-g)) * u;"),
+    ("gate_transposed", "g += load_elem(gate, dt, wrow + k) * xr[k];",
+     "g += load_elem(gate, dt, (e * H + k) * I + i) * xr[k];"),
+    ("down_transposed", "acc += load_elem(down, dt, wrow + i) * hv[i];",
+     "acc += load_elem(down, dt, (e * I + i) * H + o) * hv[i];"),
+    ("combine_drops_first_slot",
+     "for (int64_t j = 0; j < top_k; ++j) {\n                int64_t r",
+     "for (int64_t j = 1; j < top_k; ++j) {\n                int64_t r"),
+    ("combine_ignores_weight",
+     "acc += load_elem(w, wdt, t * top_k + j) * load_elem(out_disp",
+     "acc += 1.0 * load_elem(out_disp"),
+    ("dispatch_src_is_token", "src_of[r] = (int32_t)a;",
+     "src_of[r] = (int32_t)(a / top_k);"),
+    ("gather_wrong_token", "int64_t t = src_of[r] / top_k;",
+     "int64_t t = src_of[r] % top_k;"),
+    ("offsets_inclusive", "offsets[e + 1] = offsets[e] + counts[e];\n        next[e] = offsets[e];",
+     "offsets[e + 1] = offsets[e] + counts[e];\n        next[e] = offsets[e + 1] - counts[e] + (e > 0);"),
+    ("rms_mean_off_by_one", "ss / (double)H + (double)eps", "ss / (double)(H + 1) + (double)eps"),
+    ("rms_eps_dropped", "ss / (double)H + (double)eps", "ss / (double)H"),
+    ("rms_not_reciprocal", "double r = 1.0 / sqrt(", "double r = sqrt("),
+    ("add_residual_dropped",
+     "combine[t * H + h] + load_elem(residual, rdt, t * H + h)",
+     "combine[t * H + h]"),
+    ("bf16_truncates", "u += 0x7fffu + keep_lsb;", "u += 0u * keep_lsb;"),
+]
+
+
+def _build(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not unique"
+    c = tmp_path / f"{name}.c"
+    c.write_text(src.replace(old, new))
+    so = tmp_path / f"lib{name}.so"
+    subprocess.run(["gcc", "-std=c11", "-O2", "-fPIC", "-shared", str(c), "-o",
+                    str(so), "-lm"], check=True)
+    return oracle.load_library(str(so))
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(tmp_path, name, old, new):
+    lib = _build(tmp_path, name, old, new)
+    caught = []
+    for check in ALL_CHECKS:
+        try:
+            check(lib)
+        except (AssertionError, ValueError, IndexError):
+            caught.append(check.__name__)
+    assert caught, f"no pin catches mutant {name}"
