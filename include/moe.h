@@ -1,0 +1,240 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) local Mixture-of-Experts FFN forward.
+ *
+ * The computation, following the ruDNN user guide (sections 3-7) and the
+ * aclnnMoeDistributeCombineAddRmsNormV2 "Function" formula:
+ *
+ *   logits [T,E] --route--> expert indices [T,k] (U32), weights [T,k]
+ *     --dispatch--> rows grouped by expert (no token dropped) + saved map
+ *     --experts--> per row of expert e: (SiLU(x Wg[e]^T) * (x Wu[e]^T)) Wd[e]^T
+ *     --combine--> y[t] = sum_j w[t,j] * expert_out[row of (t,j)]
+ *     (--optional--> x = y + residual, out = x / sqrt(mean(x^2) + eps) * gamma)
+ *
+ * Conventions shared by every call:
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller (for
+ *     example a torch tensor's data_ptr()); tensors are dense, row-major,
+ *     with the shapes given below. The library never allocates, frees or
+ *     retains memory: scratch space is a caller-provided workspace whose size
+ *     the matching *_workspace_size() returns (0 means none is needed).
+ *   - Tensor and workspace pointers must be 16-byte aligned (the workspace
+ *     256-byte aligned); otherwise MOE_ERR_ALIGN / MOE_ERR_WORKSPACE.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Every
+ *     compute call only enqueues kernels on it and returns without waiting;
+ *     outputs are valid once the stream reaches that point.
+ *   - Arguments are validated on the host before anything is enqueued. A
+ *     call that returns an error has enqueued nothing and left every output
+ *     untouched. T == 0 is valid and enqueues nothing.
+ *   - Errors found on the device (an expert index >= E handed to
+ *     moe_dispatch; a bounded wait inside a kernel that ran out) do not stop
+ *     the stream: the affected output rows become NaN and a per-device status
+ *     word records the error; read it with moe_device_status().
+ *
+ * Element types: expert weights, x, intermediate and output activations share
+ * one dtype (ruDNN user guide section 5: "same floating-point dtype"). FP32
+ * runs on CUDA cores in true FP32; BF16 and F16 run on the tcgen05 tensor
+ * cores with FP32 accumulation. Logits may be F32, BF16 or F16 on their own
+ * (ruDNN user guide section 4).
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types. */
+typedef enum moe_dtype {
+    MOE_F32 = 0,
+    MOE_BF16 = 1,
+    MOE_F16 = 2
+} moe_dtype;
+
+/* Status codes (every entry point returns one as an int). */
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_NULL = 1,           /* a required pointer is NULL */
+    MOE_ERR_SHAPE = 2,          /* a size is out of range or inconsistent */
+    MOE_ERR_DTYPE = 3,          /* unsupported dtype or dtype combination */
+    MOE_ERR_VALUE = 4,          /* a scalar argument is invalid (eps) */
+    MOE_ERR_ALIGN = 5,          /* a tensor pointer is not 16-byte aligned */
+    MOE_ERR_WORKSPACE = 6,      /* workspace too small or misaligned */
+    MOE_ERR_CUDA = 7,           /* the CUDA runtime reported an error */
+    MOE_ERR_DEVICE_TIMEOUT = 8, /* device status: a bounded wait gave up */
+    MOE_ERR_BAD_INDEX = 9       /* device status: an expert index >= E */
+} moe_status;
+
+/* Human-readable text of a status code; never NULL. */
+const char *moe_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int moe_abi_version(void);
+
+/* Text describing the last error returned on the calling thread (which
+ * argument or which CUDA call failed); "" if none. Never NULL. */
+const char *moe_last_error_detail(void);
+
+/*
+ * moe_route -- softmax top-k routing.
+ * ruDNN user guide, section 4 "Routing contract".
+ *
+ *   logits          [T, E], dtype logits_dtype (F32/BF16/F16), read only.
+ *   T >= 0, 1 <= E <= 1024, 1 <= top_k <= E.
+ *   expert_indices  [T, top_k] uint32, written.
+ *   weights         [T, top_k] in logits_dtype, written.
+ *
+ * Per token: FP32 softmax over all E logits; the top_k experts by FP32
+ * logit, highest first, the lower expert id first among equal logits (the
+ * softmax is strictly increasing, so this is its top-k); if renormalize != 0
+ * the selected probabilities are divided by their FP32 sum; the result is
+ * rounded once to logits_dtype. A row holding NaN or +inf, or holding only
+ * -inf, gets indices 0..top_k-1 and NaN weights (it is not replaced by a
+ * uniform distribution). A -inf logit in an otherwise valid row has weight 0.
+ * Errors: MOE_ERR_NULL, MOE_ERR_SHAPE, MOE_ERR_DTYPE, MOE_ERR_ALIGN,
+ * MOE_ERR_CUDA.
+ */
+int moe_route(const void *logits, int logits_dtype, int64_t T, int64_t E,
+              int top_k, int renormalize, uint32_t *expert_indices,
+              void *weights, void *stream);
+
+/*
+ * moe_dispatch -- compact dispatch with a saved map; nothing is dropped.
+ * ruDNN user guide, section 5 "Expert weights and dispatch".
+ *
+ *   expert_indices  [T, top_k] uint32 (as written by moe_route), read only.
+ *   x               [T, H] in x_dtype, read only. H >= 1.
+ *   counts          [E] int32, written: assignments per expert.
+ *   offsets         [E + 1] int32, written: exclusive prefix sum of counts;
+ *                   the rows of expert e are [offsets[e], offsets[e+1]).
+ *   row_of          [T * top_k] int32, written: row_of[t*top_k + j] is the
+ *                   dispatched row of assignment (t, j).
+ *   src_of          [T * top_k] int32, written: the inverse map,
+ *                   src_of[row] = t*top_k + j.
+ *   x_disp          [T * top_k, H] in x_dtype, written: x_disp[row] = x[t].
+ *   workspace       moe_dispatch_workspace_size(T, top_k, E) bytes.
+ *
+ * Rows inside one expert's segment follow the assignment order t*top_k + j
+ * (the pages leave this order unspecified; this build makes it
+ * deterministic). An index >= E gets no row: row_of = -1, the status word
+ * records MOE_ERR_BAD_INDEX, src_of/x_disp rows past offsets[E] are -1 /
+ * untouched. Errors: MOE_ERR_NULL, MOE_ERR_SHAPE, MOE_ERR_DTYPE,
+ * MOE_ERR_ALIGN, MOE_ERR_WORKSPACE, MOE_ERR_CUDA.
+ */
+size_t moe_dispatch_workspace_size(int64_t T, int top_k, int64_t E);
+int moe_dispatch(const uint32_t *expert_indices, int64_t T, int top_k,
+                 int64_t E, const void *x, int x_dtype, int64_t H,
+                 int32_t *counts, int32_t *offsets, int32_t *row_of,
+                 int32_t *src_of, void *x_disp, void *workspace,
+                 size_t workspace_bytes, void *stream);
+
+/*
+ * moe_experts_forward -- bias-free SwiGLU experts on dispatched rows.
+ * ruDNN user guide, sections 3 and 5 (SwiGluExperts::forward_dispatched);
+ * aclnnFFN "Formula" with no bias and a SwiGLU activation.
+ *
+ *   x_disp    [rows, H] in dtype, read only.
+ *   offsets   [E + 1] int32 (device), read only: rows of expert e are
+ *             [offsets[e], offsets[e+1]); offsets[E] <= rows.
+ *   gate, up  [E, I, H] in dtype;  down [E, H, I] in dtype.
+ *   out_disp  [rows, H] in dtype, written for rows < offsets[E].
+ *   workspace moe_experts_workspace_size(...) bytes (holds h [rows, I]).
+ *
+ * For each row r of expert e: g = Wg[e] x_r, u = Wu[e] x_r,
+ * h = SiLU(g) * u with SiLU(z) = z / (1 + exp(-z)), out_r = Wd[e] h.
+ * BF16/F16: tcgen05 tensor cores, FP32 accumulation, h rounded to dtype
+ * between the two GEMMs. F32: CUDA cores, FP32 throughout.
+ * Constraints: BF16/F16 need H % 8 == 0 and I % 8 == 0; F32 needs
+ * H % 4 == 0 and I % 4 == 0; 1 <= E <= 1024.
+ * Errors: MOE_ERR_NULL, MOE_ERR_SHAPE, MOE_ERR_DTYPE, MOE_ERR_ALIGN,
+ * MOE_ERR_WORKSPACE, MOE_ERR_CUDA.
+ */
+size_t moe_experts_workspace_size(int64_t rows, int64_t E, int64_t H,
+                                  int64_t I, int dtype);
+int moe_experts_forward(const void *x_disp, const int32_t *offsets,
+                        int64_t rows, const void *gate, const void *up,
+                        const void *down, int64_t E, int64_t H, int64_t I,
+                        int dtype, void *out_disp, void *workspace,
+                        size_t workspace_bytes, void *stream);
+
+/*
+ * moe_combine -- restore token order and sum the weighted expert outputs.
+ * ruDNN user guide, sections 3 and 6 (DispatchedTokens::combine).
+ *
+ *   out_disp  [T * top_k, H] in dtype, read only.
+ *   weights   [T, top_k] in weights_dtype (F32 or dtype), read only.
+ *   row_of    [T * top_k] int32, read only (from moe_dispatch).
+ *   y         [T, H] in dtype, written.
+ *
+ * y[t] = sum over j < top_k, in slot order, of weights[t,j] *
+ * out_disp[row_of[t*top_k + j]], accumulated in FP32, rounded once to dtype.
+ * A slot with row_of < 0 makes the token's row NaN.
+ * Errors: MOE_ERR_NULL, MOE_ERR_SHAPE, MOE_ERR_DTYPE, MOE_ERR_ALIGN,
+ * MOE_ERR_CUDA.
+ */
+int moe_combine(const void *out_disp, int dtype, const void *weights,
+                int weights_dtype, const int32_t *row_of, int64_t T, int top_k,
+                int64_t H, void *y, void *stream);
+
+/*
+ * moe_combine_add_rmsnorm -- combine, residual Add and RMSNorm in one pass.
+ * aclnnMoeDistributeCombineAddRmsNormV2, "Function" formula, without its
+ * ReduceScatterV / AlltoAllV exchange (this library is single-GPU):
+ *   x = combine + residual,  y = x / sqrt(mean(x^2) + eps) * gamma.
+ * ruDNN user guide section 7: eps finite and > 0, FP32 statistics.
+ *
+ *   out_disp, weights, row_of, T, top_k, H as for moe_combine.
+ *   residual  [T, H] in dtype, read only.
+ *   gamma     [H] in gamma_dtype (F32 or dtype), read only.
+ *   y         [T, H] in dtype, written (normalised output, yOut).
+ *   x_out     [T, H] in dtype, written (the pre-norm sum, xOut).
+ *   rstd      [T] float, written: 1 / sqrt(mean(x_out^2) + eps) (rstdOut).
+ *
+ * The statistics are taken on x_out after it is rounded to dtype, so y
+ * equals RMSNorm applied to x_out. Errors: MOE_ERR_NULL, MOE_ERR_SHAPE,
+ * MOE_ERR_DTYPE, MOE_ERR_VALUE, MOE_ERR_ALIGN, MOE_ERR_CUDA.
+ */
+int moe_combine_add_rmsnorm(const void *out_disp, int dtype,
+                            const void *weights, int weights_dtype,
+                            const int32_t *row_of, const void *residual,
+                            const void *gamma, int gamma_dtype, float eps,
+                            int64_t T, int top_k, int64_t H, void *y,
+                            void *x_out, float *rstd, void *stream);
+
+/*
+ * moe_forward -- the whole local forward in one call: route, dispatch,
+ * experts, combine. ruDNN user guide, section 6 (SwiGluExperts::forward):
+ * takes precomputed logits (no gate projection, no weight loading).
+ *
+ *   x       [T, H] in dtype;   logits [T, E] in logits_dtype.
+ *   gate, up [E, I, H];  down [E, H, I], in dtype.
+ *   y       [T, H] in dtype, written.
+ *   workspace moe_forward_workspace_size(...) bytes; it holds the routing
+ *           plan, the dispatch map and the dispatched activations.
+ * Same rules and errors as the staged calls; the result equals
+ * moe_route -> moe_dispatch -> moe_experts_forward -> moe_combine.
+ */
+size_t moe_forward_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E,
+                                  int top_k, int dtype, int logits_dtype);
+int moe_forward(const void *x, int dtype, const void *logits,
+                int logits_dtype, const void *gate, const void *up,
+                const void *down, int64_t T, int64_t H, int64_t I, int64_t E,
+                int top_k, int renormalize, void *y, void *workspace,
+                size_t workspace_bytes, void *stream);
+
+/*
+ * moe_device_status -- read the current device's status word.
+ * Synchronises `stream`, then returns MOE_OK, MOE_ERR_BAD_INDEX or
+ * MOE_ERR_DEVICE_TIMEOUT (the latter wins when both are set). If clear != 0
+ * the word is reset to zero afterwards. MOE_ERR_CUDA if the read fails.
+ * (Router training in the ruDNN user guide, section 12, fixes the same rule
+ * for illegal indices: NaN rows, no out-of-bounds read, no host sync.)
+ */
+int moe_device_status(void *stream, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,1 +1,289 @@
-"""GB300-native local Mixture-of-Experts FFN forward (placeholder binding)."""
+"""GB300-native local Mixture-of-Experts FFN forward.
+
+A thin ctypes binding of the C ABI in ``include/moe.h``: every function here
+has the name of the C entry point it calls and only marshals arguments
+(torch tensors -> device pointers and sizes, the current CUDA stream). All
+compute runs in the hand-written sm_103a kernels of ``_lib/libmoe_gb300.so``;
+there is no fallback: if the library is missing the call raises.
+
+Tensors must be contiguous CUDA tensors. Expert indices are U32 in the ABI;
+the binding stores them in ``torch.int32`` tensors (same bits, values < 1024).
+Outputs may be passed in (``out=``-style keyword arguments) to reuse memory;
+otherwise they are allocated with torch on the input's device. Workspaces are
+torch ``uint8`` tensors sized by the matching ``*_workspace_size`` call.
+
+Sources: ruDNN user guide sections 3-7 (routing, dispatch, SwiGLU experts,
+combine, RMSNorm); aclnnMoeDistributeCombineAddRmsNormV2 "Function" formula.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libmoe_gb300.so")
+
+MOE_F32, MOE_BF16, MOE_F16 = 0, 1, 2
+DTYPE_CODES = {torch.float32: MOE_F32, torch.bfloat16: MOE_BF16,
+               torch.float16: MOE_F16}
+
+STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_NULL", 2: "MOE_ERR_SHAPE",
+                3: "MOE_ERR_DTYPE", 4: "MOE_ERR_VALUE", 5: "MOE_ERR_ALIGN",
+                6: "MOE_ERR_WORKSPACE", 7: "MOE_ERR_CUDA",
+                8: "MOE_ERR_DEVICE_TIMEOUT", 9: "MOE_ERR_BAD_INDEX"}
+
+EXPORTED = ["moe_status_string", "moe_abi_version", "moe_last_error_detail",
+            "moe_route", "moe_dispatch_workspace_size", "moe_dispatch",
+            "moe_experts_workspace_size", "moe_experts_forward", "moe_combine",
+            "moe_combine_add_rmsnorm", "moe_forward_workspace_size",
+            "moe_forward", "moe_device_status"]
+
+_lock = threading.Lock()
+_lib = None
+
+_P, _I64, _INT, _SZ, _F = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+                           ctypes.c_size_t, ctypes.c_float)
+
+
+class MoeError(RuntimeError):
+    """A non-zero status returned by the C ABI."""
+
+    def __init__(self, code: int, fn: str, detail: str = ""):
+        self.code = code
+        self.name = STATUS_NAMES.get(code, str(code))
+        super().__init__(f"{fn}: {self.name}" + (f" ({detail})" if detail else ""))
+
+
+def _bind(lib):
+    sig = {
+        "moe_status_string": ([_INT], ctypes.c_char_p),
+        "moe_abi_version": ([], _INT),
+        "moe_last_error_detail": ([], ctypes.c_char_p),
+        "moe_route": ([_P, _INT, _I64, _I64, _INT, _INT, _P, _P, _P], _INT),
+        "moe_dispatch_workspace_size": ([_I64, _INT, _I64], _SZ),
+        "moe_dispatch": ([_P, _I64, _INT, _I64, _P, _INT, _I64, _P, _P, _P, _P,
+                          _P, _P, _SZ, _P], _INT),
+        "moe_experts_workspace_size": ([_I64, _I64, _I64, _I64, _INT], _SZ),
+        "moe_experts_forward": ([_P, _P, _I64, _P, _P, _P, _I64, _I64, _I64,
+                                 _INT, _P, _P, _SZ, _P], _INT),
+        "moe_combine": ([_P, _INT, _P, _INT, _P, _I64, _INT, _I64, _P, _P], _INT),
+        "moe_combine_add_rmsnorm": ([_P, _INT, _P, _INT, _P, _P, _P, _INT, _F,
+                                     _I64, _INT, _I64, _P, _P, _P, _P], _INT),
+        "moe_forward_workspace_size": ([_I64, _I64, _I64, _I64, _INT, _INT,
+                                        _INT], _SZ),
+        "moe_forward": ([_P, _INT, _P, _INT, _P, _P, _P, _I64, _I64, _I64, _I64,
+                         _INT, _INT, _P, _P, _SZ, _P], _INT),
+        "moe_device_status": ([_P, _INT], _INT),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+    return lib
+
+
+def load_library(path: str | None = None):
+    """Load the extension. Raises if it has not been built (no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is None or path is not None:
+            p = path or LIB_PATH
+            if not os.path.exists(p):
+                raise RuntimeError(
+                    f"CUDA extension not built: {p} is missing; run "
+                    "mixture_experts_ffn_topk_gb300.build.build()")
+            lib = _bind(ctypes.CDLL(p))
+            if path is not None:
+                return lib
+            _lib = lib
+    return _lib
+
+
+def _check(rc: int, fn: str):
+    if rc != 0:
+        detail = load_library().moe_last_error_detail().decode(errors="replace")
+        raise MoeError(rc, fn, detail)
+
+
+def _code(dtype: torch.dtype) -> int:
+    if dtype not in DTYPE_CODES:
+        raise TypeError(f"unsupported dtype {dtype}; use float32, bfloat16 or float16")
+    return DTYPE_CODES[dtype]
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ptr(t: torch.Tensor | None) -> ctypes.c_void_p:
+    if t is None:
+        return ctypes.c_void_p(None)
+    if not t.is_cuda:
+        raise ValueError("tensors passed to the C ABI must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the C ABI must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _workspace(nbytes: int, device, given: torch.Tensor | None) -> torch.Tensor | None:
+    if given is not None:
+        return given
+    if nbytes == 0:
+        return None
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def _nbytes(t: torch.Tensor | None) -> int:
+    return 0 if t is None else t.numel() * t.element_size()
+
+
+# ----------------------------------------------------------------- entry points
+
+def moe_status_string(status: int) -> str:
+    return load_library().moe_status_string(int(status)).decode()
+
+
+def moe_abi_version() -> int:
+    return load_library().moe_abi_version()
+
+
+def moe_route(logits: torch.Tensor, top_k: int, renormalize: bool,
+              expert_indices: torch.Tensor | None = None,
+              weights: torch.Tensor | None = None, stream=None):
+    """Softmax top-k routing. Returns ``(expert_indices int32 [T,k],
+    weights [T,k] in logits.dtype)``."""
+    T, E = logits.shape
+    dev = logits.device
+    if expert_indices is None:
+        expert_indices = torch.empty((T, top_k), dtype=torch.int32, device=dev)
+    if weights is None:
+        weights = torch.empty((T, top_k), dtype=logits.dtype, device=dev)
+    rc = load_library().moe_route(_ptr(logits), _code(logits.dtype), T, E,
+                                  int(top_k), int(bool(renormalize)),
+                                  _ptr(expert_indices), _ptr(weights),
+                                  _stream(stream))
+    _check(rc, "moe_route")
+    return expert_indices, weights
+
+
+def moe_dispatch_workspace_size(T: int, top_k: int, E: int) -> int:
+    return int(load_library().moe_dispatch_workspace_size(T, top_k, E))
+
+
+def moe_dispatch(expert_indices: torch.Tensor, x: torch.Tensor, E: int,
+                 counts=None, offsets=None, row_of=None, src_of=None,
+                 x_disp=None, workspace=None, stream=None) -> dict:
+    """Compact no-drop dispatch. Returns a dict with ``counts [E]``,
+    ``offsets [E+1]``, ``row_of [T*k]``, ``src_of [T*k]`` (int32) and
+    ``x_disp [T*k, H]``."""
+    T, k = expert_indices.shape
+    H = x.shape[1]
+    dev = x.device
+    A = T * k
+    counts = counts if counts is not None else torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = offsets if offsets is not None else torch.empty(E + 1, dtype=torch.int32, device=dev)
+    row_of = row_of if row_of is not None else torch.empty(A, dtype=torch.int32, device=dev)
+    src_of = src_of if src_of is not None else torch.empty(A, dtype=torch.int32, device=dev)
+    x_disp = x_disp if x_disp is not None else torch.empty((A, H), dtype=x.dtype, device=dev)
+    ws = _workspace(moe_dispatch_workspace_size(T, k, E), dev, workspace)
+    rc = load_library().moe_dispatch(
+        _ptr(expert_indices), T, k, E, _ptr(x), _code(x.dtype), H, _ptr(counts),
+        _ptr(offsets), _ptr(row_of), _ptr(src_of), _ptr(x_disp), _ptr(ws),
+        _nbytes(ws), _stream(stream))
+    _check(rc, "moe_dispatch")
+    return {"counts": counts, "offsets": offsets, "row_of": row_of,
+            "src_of": src_of, "x_disp": x_disp}
+
+
+def moe_experts_workspace_size(rows: int, E: int, H: int, I: int,
+                               dtype: torch.dtype) -> int:
+    return int(load_library().moe_experts_workspace_size(rows, E, H, I, _code(dtype)))
+
+
+def moe_experts_forward(x_disp: torch.Tensor, offsets: torch.Tensor,
+                        gate: torch.Tensor, up: torch.Tensor,
+                        down: torch.Tensor, out_disp=None, workspace=None,
+                        stream=None) -> torch.Tensor:
+    """Bias-free SwiGLU experts on dispatched rows; returns ``out_disp``."""
+    rows, H = x_disp.shape
+    E, I, _ = gate.shape
+    dev = x_disp.device
+    out_disp = out_disp if out_disp is not None else torch.empty((rows, H), dtype=x_disp.dtype, device=dev)
+    ws = _workspace(moe_experts_workspace_size(rows, E, H, I, x_disp.dtype), dev, workspace)
+    rc = load_library().moe_experts_forward(
+        _ptr(x_disp), _ptr(offsets), rows, _ptr(gate), _ptr(up), _ptr(down), E,
+        H, I, _code(x_disp.dtype), _ptr(out_disp), _ptr(ws), _nbytes(ws),
+        _stream(stream))
+    _check(rc, "moe_experts_forward")
+    return out_disp
+
+
+def moe_combine(out_disp: torch.Tensor, weights: torch.Tensor,
+                row_of: torch.Tensor, y=None, stream=None) -> torch.Tensor:
+    """Weighted combine back to token order; returns ``y [T, H]``."""
+    T, k = weights.shape
+    H = out_disp.shape[1]
+    y = y if y is not None else torch.empty((T, H), dtype=out_disp.dtype, device=out_disp.device)
+    rc = load_library().moe_combine(
+        _ptr(out_disp), _code(out_disp.dtype), _ptr(weights),
+        _code(weights.dtype), _ptr(row_of), T, k, H, _ptr(y), _stream(stream))
+    _check(rc, "moe_combine")
+    return y
+
+
+def moe_combine_add_rmsnorm(out_disp: torch.Tensor, weights: torch.Tensor,
+                            row_of: torch.Tensor, residual: torch.Tensor,
+                            gamma: torch.Tensor, eps: float, y=None,
+                            x_out=None, rstd=None, stream=None):
+    """Combine + residual Add + RMSNorm; returns ``(y, x_out, rstd)``."""
+    T, k = weights.shape
+    H = out_disp.shape[1]
+    dev = out_disp.device
+    y = y if y is not None else torch.empty((T, H), dtype=out_disp.dtype, device=dev)
+    x_out = x_out if x_out is not None else torch.empty((T, H), dtype=out_disp.dtype, device=dev)
+    rstd = rstd if rstd is not None else torch.empty(T, dtype=torch.float32, device=dev)
+    rc = load_library().moe_combine_add_rmsnorm(
+        _ptr(out_disp), _code(out_disp.dtype), _ptr(weights),
+        _code(weights.dtype), _ptr(row_of), _ptr(residual), _ptr(gamma),
+        _code(gamma.dtype), float(eps), T, k, H, _ptr(y), _ptr(x_out),
+        _ptr(rstd), _stream(stream))
+    _check(rc, "moe_combine_add_rmsnorm")
+    return y, x_out, rstd
+
+
+def moe_forward_workspace_size(T: int, H: int, I: int, E: int, top_k: int,
+                               dtype: torch.dtype, logits_dtype: torch.dtype) -> int:
+    return int(load_library().moe_forward_workspace_size(
+        T, H, I, E, top_k, _code(dtype), _code(logits_dtype)))
+
+
+def moe_forward(x: torch.Tensor, logits: torch.Tensor, gate: torch.Tensor,
+                up: torch.Tensor, down: torch.Tensor, top_k: int,
+                renormalize: bool, y=None, workspace=None,
+                stream=None) -> torch.Tensor:
+    """The whole local forward (route, dispatch, experts, combine)."""
+    T, H = x.shape
+    E, I, _ = gate.shape
+    dev = x.device
+    y = y if y is not None else torch.empty((T, H), dtype=x.dtype, device=dev)
+    ws = _workspace(moe_forward_workspace_size(T, H, I, E, top_k, x.dtype, logits.dtype),
+                    dev, workspace)
+    rc = load_library().moe_forward(
+        _ptr(x), _code(x.dtype), _ptr(logits), _code(logits.dtype), _ptr(gate),
+        _ptr(up), _ptr(down), T, H, I, E, int(top_k), int(bool(renormalize)),
+        _ptr(y), _ptr(ws), _nbytes(ws), _stream(stream))
+    _check(rc, "moe_forward")
+    return y
+
+
+def moe_device_status(stream=None, clear: bool = True) -> int:
+    """Synchronise ``stream`` and return the device status code (0 = OK)."""
+    return int(load_library().moe_device_status(_stream(stream), int(bool(clear))))

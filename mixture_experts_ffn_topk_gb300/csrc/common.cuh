@@ -1,0 +1,90 @@
+// common.cuh -- device helpers shared by the kernels of the GB300 MoE path.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+enum : int { DT_F32 = 0, DT_BF16 = 1, DT_F16 = 2 };
+
+// Bits of the per-device status word (see moe_device_status in moe.h).
+enum : unsigned { ST_BAD_INDEX = 1u, ST_TIMEOUT = 2u };
+
+// Element access by dtype code. 16-bit types are loaded as raw words.
+template <int DT> struct Elem;
+
+template <> struct Elem<DT_F32> {
+    using T = float;
+    static __device__ __forceinline__ float to_f(T v) { return v; }
+    static __device__ __forceinline__ T from_f(float v) { return v; }
+};
+template <> struct Elem<DT_BF16> {
+    using T = __nv_bfloat16;
+    static __device__ __forceinline__ float to_f(T v) { return __bfloat162float(v); }
+    static __device__ __forceinline__ T from_f(float v) { return __float2bfloat16_rn(v); }
+};
+template <> struct Elem<DT_F16> {
+    using T = __half;
+    static __device__ __forceinline__ float to_f(T v) { return __half2float(v); }
+    static __device__ __forceinline__ T from_f(float v) { return __float2half_rn(v); }
+};
+
+// Load element i of a buffer whose dtype is only known at run time.
+__device__ __forceinline__ float load_as_float(const void *p, int dt, int64_t i)
+{
+    if (dt == DT_F32) return static_cast<const float *>(p)[i];
+    if (dt == DT_BF16) return __bfloat162float(static_cast<const __nv_bfloat16 *>(p)[i]);
+    return __half2float(static_cast<const __half *>(p)[i]);
+}
+
+__device__ __forceinline__ void store_from_float(void *p, int dt, int64_t i, float v)
+{
+    if (dt == DT_F32) static_cast<float *>(p)[i] = v;
+    else if (dt == DT_BF16) static_cast<__nv_bfloat16 *>(p)[i] = __float2bfloat16_rn(v);
+    else static_cast<__half *>(p)[i] = __float2half_rn(v);
+}
+
+// Eight 16-bit elements (or four floats) travel as one 16-byte vector; the
+// 16-bit pairs are reinterpreted from the 32-bit words w[].
+union Vec16 {
+    uint4 u;
+    float f[4];
+    uint32_t w[4];
+};
+
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w)
+{
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w));
+}
+__device__ __forceinline__ float2 f16x2_to_float2(uint32_t w)
+{
+    return __half22float2(*reinterpret_cast<const __half2 *>(&w));
+}
+__device__ __forceinline__ uint32_t float2_to_bf16x2(float a, float b)
+{
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+__device__ __forceinline__ uint32_t float2_to_f16x2(float a, float b)
+{
+    const __half2 v = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+__device__ __forceinline__ unsigned lane_id() { return threadIdx.x & 31u; }
+
+__device__ __forceinline__ uint64_t global_timer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Every spin-wait in this library gives up after this long, sets
+// ST_TIMEOUT in the status word and lets the kernel wind down.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+}  // namespace moe

@@ -1,0 +1,573 @@
+// experts_tc.cu -- BF16/F16 bias-free SwiGLU experts on tcgen05 tensor cores.
+//
+// ruDNN user guide, sections 3 and 5: per dispatched row r of expert e,
+//   h_r = SiLU(x_r Wg[e]^T) * (x_r Wu[e]^T),   out_r = h_r Wd[e]^T,
+// gate/up [E,I,H], down [E,H,I] (aclnnFFN "Formula" with no bias and a SwiGLU
+// activation). Inputs BF16 or F16, FP32 accumulation in tensor memory, h
+// rounded to the input dtype between the two GEMMs.
+//
+// Two launches of one persistent, warp-specialised grouped GEMM:
+//   GEMM1 (SWIGLU):  B tile = 128 gate rows stacked on 128 up rows of the
+//                    same output columns; one 128x256x16 MMA computes both;
+//                    the epilogue forms SiLU(g)*u for 128 columns of h.
+//   GEMM2:           B tile = 256 rows of down; the epilogue rounds to dtype.
+// Per CTA (one per SM, 192 threads):
+//   warp 0  TMA producer: x tile [128 rows x 64 k] and weight tile
+//           [256 rows x 64 k] per stage, 128-byte swizzle, 4 stages;
+//   warp 1  MMA issuer: tcgen05.mma.cta_group::1.kind::f16, M=128 N=256 K=16,
+//           accumulators double-buffered in TMEM (2 x 256 columns);
+//   warps 2-5  epilogue: tcgen05.ld 32 lanes x 32 columns, math, stores.
+// Tiles: each expert's row segment [offsets[e], offsets[e+1]) is cut into
+// 128-row M-tiles; linear tile ids run over (expert, n-tile, m-tile) with the
+// m-tile fastest, so CTAs working at the same time share weight tiles in L2.
+// The schedule is computed per CTA from the device-side offsets: no host
+// synchronisation. Rows of a tile past the segment end belong to the next
+// expert (or are TMA zero-fill past the last row); they are computed and not
+// stored. TMA zero-fills the K and N edges.
+//
+// Every wait is bounded (kWaitLimitNs); on expiry the kernel sets ST_TIMEOUT,
+// stops issuing work, drains its own TMA copies and MMAs, frees TMEM and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int BM = 128;                      // rows per tile (UMMA M)
+constexpr int BK = 64;                       // K per stage: 128 bytes of 16-bit
+constexpr int UK = 16;                       // K per tcgen05.mma kind::f16
+constexpr int BN = 256;                      // B rows per stage (UMMA N)
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;         // 16 KiB
+constexpr int B_BYTES = BN * BK * 2;         // 32 KiB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int ACC_COLS = 256;                // fp32 columns per accumulator
+constexpr int TMEM_COLS = 2 * ACC_COLS;
+constexpr int THREADS = 192;
+constexpr int MAX_E = 1024;
+constexpr uint64_t kDrainLimitNs = 100000000ull;   // 100 ms per teardown drain
+
+struct __align__(1024) SharedStorage {
+    uint8_t stage[STAGES][STAGE_BYTES];      // each stage 1024-byte aligned
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+    int prefix[MAX_E + 1];
+    int offs[MAX_E + 1];
+};
+
+constexpr size_t kSmemBytes = sizeof(SharedStorage) + 1024;  // + alignment slack
+
+// ---- PTX wrappers ---------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete. Gives up (false) when
+// another role raised the abort flag, or after limit_ns, which sets ST_TIMEOUT
+// and raises the abort. With abort_flag == nullptr (teardown drains) the wait
+// ignores the flag and only records a timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          volatile int *abort_flag,
+                                          unsigned *status, uint64_t limit_ns)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (abort_flag != nullptr && *abort_flag) return false;
+        if (global_timer_ns() - t0 > limit_ns) {
+            atomicOr(status, ST_TIMEOUT);
+            if (abort_flag != nullptr) *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int c0, int c1)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int c0, int c1, int c2)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A[smem] * B[smem]^T, both K-major, M=128, N=256, K=16.
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on an mbarrier once every tcgen05 op issued so far by this thread
+// has completed.
+__device__ __forceinline__ void umma_commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// 32 TMEM lanes (one per thread of the warp) x 32 consecutive fp32 columns.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+}
+
+// Wait for this thread's tcgen05.ld results; the empty asm after it ties the
+// registers to the wait so no use of them is scheduled earlier.
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]),
+                   "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]),
+                   "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, rows of 128
+// bytes, 8-row groups 1024 bytes apart (stride byte offset), version 1.
+__device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);        // start address
+    d |= (uint64_t)1 << 16;                          // leading byte offset (unused here)
+    d |= (uint64_t)(1024 >> 4) << 32;                // stride byte offset
+    d |= (uint64_t)1 << 46;                          // descriptor version
+    d |= (uint64_t)2 << 61;                          // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: FP32 accumulator, A/B BF16 (1) or F16 (0),
+// both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+template <int DT>
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N)
+{
+    return (1u << 4) | ((DT == DT_BF16 ? 1u : 0u) << 7) | ((DT == DT_BF16 ? 1u : 0u) << 10) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void decode_tile(const SharedStorage &S, int E, int tile,
+                                            int &e, int &n, int &m)
+{
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (S.prefix[mid] <= tile) lo = mid; else hi = mid - 1;
+    }
+    e = lo;
+    const int mt = (S.offs[e + 1] - S.offs[e] + BM - 1) / BM;
+    const int local = tile - S.prefix[e];
+    n = local / mt;
+    m = local % mt;
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t pack2(float a, float b)
+{
+    if constexpr (DT == DT_BF16) return float2_to_bf16x2(a, b);
+    else return float2_to_f16x2(a, b);
+}
+
+// ---- the kernel -------------------------------------------------------------
+
+template <int DT, bool SWIGLU>
+__global__ void __launch_bounds__(THREADS, 1)
+grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                       const __grid_constant__ CUtensorMap tmB0,
+                       const __grid_constant__ CUtensorMap tmB1,
+                       const int32_t *__restrict__ offsets, int E, int N, int K,
+                       int n_tiles, void *__restrict__ out, unsigned *status)
+{
+    extern __shared__ uint8_t smem_raw[];
+    SharedStorage &S = *reinterpret_cast<SharedStorage *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int N_OUT = SWIGLU ? BN / 2 : BN;      // output columns per tile
+    const int num_kb = (K + BK - 1) / BK;
+
+    for (int i = threadIdx.x; i <= E; i += THREADS) S.offs[i] = offsets[i];
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) { mbar_init(&S.full[s], 1); mbar_init(&S.empty[s], 1); }
+        for (int a = 0; a < 2; ++a) { mbar_init(&S.acc_full[a], 1); mbar_init(&S.acc_empty[a], 4); }
+        mbar_init(&S.drain, 1);
+        S.abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        tmem_alloc(&S.tmem_base, TMEM_COLS);
+        tmem_relinquish();
+    }
+    __syncthreads();
+    if (warp == 0) {
+        // prefix[e] = tiles of experts < e; lane l owns a contiguous run of experts
+        const int per = (E + 31) / 32, e0 = lane * per;
+        int local = 0;
+        for (int e = e0; e < e0 + per && e < E; ++e)
+            local += (S.offs[e + 1] - S.offs[e] + BM - 1) / BM * n_tiles;
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int run = incl - local;
+        for (int e = e0; e < e0 + per && e < E; ++e) {
+            S.prefix[e] = run;
+            run += (S.offs[e + 1] - S.offs[e] + BM - 1) / BM * n_tiles;
+        }
+        if (lane == 31) S.prefix[E] = incl;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    const uint32_t tmem_base = S.tmem_base;
+    const int total_tiles = S.prefix[E];
+    volatile int *abort_flag = &S.abort;
+
+    // producer bookkeeping for a safe drain on abort
+    uint32_t filled_mask = 0, filled_parity = 0;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------------ TMA producer
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+            int e, n, m;
+            decode_tile(S, E, tile, e, n, m);
+            const int row0 = S.offs[e] + m * BM;
+            bool ok = true;
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if (!mbar_wait(&S.empty[stage], phase ^ 1u, abort_flag, status, kWaitLimitNs)) { ok = false; break; }
+                mbar_arrive_expect_tx(&S.full[stage], STAGE_BYTES);
+                uint8_t *sa = S.stage[stage];
+                uint8_t *sb = sa + A_BYTES;
+                tma_load_2d(sa, &tmA, &S.full[stage], kb * BK, row0);
+                if (SWIGLU) {
+                    tma_load_3d(sb, &tmB0, &S.full[stage], kb * BK, n * (BN / 2), e);
+                    tma_load_3d(sb + B_BYTES / 2, &tmB1, &S.full[stage], kb * BK, n * (BN / 2), e);
+                } else {
+                    tma_load_3d(sb, &tmB0, &S.full[stage], kb * BK, n * BN, e);
+                }
+                filled_mask |= 1u << stage;
+                filled_parity = (filled_parity & ~(1u << stage)) | (phase << stage);
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+            if (!ok) break;
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------------ MMA issuer
+        constexpr uint32_t idesc = idesc_f16<DT>(BM, BN);
+        int stage = 0;
+        uint32_t phase = 0;
+        int it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++it) {
+            const int acc = it & 1;
+            const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+            if (!mbar_wait(&S.acc_empty[acc], acc_phase ^ 1u, abort_flag, status, kWaitLimitNs)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t d = tmem_base + (uint32_t)(acc * ACC_COLS);
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if (!mbar_wait(&S.full[stage], phase, abort_flag, status, kWaitLimitNs)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t a0 = smem_u32(S.stage[stage]);
+                const uint32_t b0 = a0 + A_BYTES;
+#pragma unroll
+                for (int k = 0; k < BK / UK; ++k)
+                    umma_f16(d, sdesc_k_sw128(a0 + k * UK * 2), sdesc_k_sw128(b0 + k * UK * 2),
+                             idesc, (kb | k) != 0 ? 1u : 0u);
+                umma_commit(&S.empty[stage]);
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+            if (ok) umma_commit(&S.acc_full[acc]);
+        }
+        if (*abort_flag) {
+            // every MMA issued so far must finish before TMEM is released
+            umma_commit(&S.drain);
+            mbar_wait(&S.drain, 0, nullptr, status, kDrainLimitNs);
+        }
+    } else if (warp >= 2) {
+        // ------------------------------------------------------ epilogue
+        const int q = warp & 3;            // TMEM lane quadrant of this warp
+        int it = 0;
+        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++it) {
+            int e, n, m;
+            decode_tile(S, E, tile, e, n, m);
+            const int seg_rows = S.offs[e + 1] - S.offs[e];
+            const int r_in_seg = m * BM + q * 32 + lane;
+            const bool row_ok = r_in_seg < seg_rows;
+            const int64_t row = (int64_t)S.offs[e] + r_in_seg;
+            const int acc = it & 1;
+            const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+            // every lane waits; the warp leaves together if any lane gave up,
+            // since tcgen05.ld below needs the whole warp converged
+            const bool ready = mbar_wait(&S.acc_full[acc], acc_phase, abort_flag, status, kWaitLimitNs);
+            if (!__all_sync(0xffffffffu, ready)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
+            using ET = typename Elem<DT>::T;
+            ET *orow = static_cast<ET *>(out) + row * (int64_t)N;
+#pragma unroll 1
+            for (int c = 0; c < N_OUT / 32; ++c) {
+                uint32_t g[32];
+                tmem_ld32(tbase + c * 32, g);
+                uint4 v[4];
+                uint32_t *pv = reinterpret_cast<uint32_t *>(v);
+                if (SWIGLU) {
+                    uint32_t u[32];
+                    tmem_ld32(tbase + BN / 2 + c * 32, u);
+                    tmem_ld_wait(g);
+                    tmem_ld_wait(u);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
+                        const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
+                        const float h0 = g0 / (1.0f + __expf(-g0)) * u0;
+                        const float h1 = g1 / (1.0f + __expf(-g1)) * u1;
+                        pv[i] = pack2<DT>(h0, h1);
+                    }
+                } else {
+                    tmem_ld_wait(g);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        pv[i] = pack2<DT>(__uint_as_float(g[2 * i]), __uint_as_float(g[2 * i + 1]));
+                }
+                const int col0 = n * N_OUT + c * 32;
+                if (row_ok) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (col0 + 8 * j < N)
+                            *reinterpret_cast<uint4 *>(orow + col0 + 8 * j) = v[j];
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.acc_empty[acc]);
+        }
+    }
+
+    // ------------------------------------------------------------ teardown
+    __syncthreads();
+    if (*abort_flag && warp == 0 && lane == 0) {
+        // let this CTA's outstanding TMA copies land before shared memory goes
+        for (int s = 0; s < STAGES; ++s)
+            if (filled_mask >> s & 1u)
+                mbar_wait(&S.full[s], filled_parity >> s & 1u, nullptr, status, kDrainLimitNs);
+    }
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ---- host side ---------------------------------------------------------------
+
+using EncodeTiledFn = PFN_cuTensorMapEncodeTiled_v12000;
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Row-major [outer, inner] 16-bit matrix; box = box_outer rows x box_inner
+// elements (box_inner * 2 == 128 bytes, the swizzle span).
+bool encode_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner,
+               uint64_t outer, uint32_t box_inner, uint32_t box_outer)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Row-major [d2, d1, d0] 16-bit tensor (expert, row, k); box = one expert,
+// box1 rows, box0 elements of k.
+bool encode_3d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t d0,
+               uint64_t d1, uint64_t d2, uint32_t box0, uint32_t box1)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+    cuuint32_t box[3] = {box0, box1, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, dt, 3, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The dynamic shared-memory opt-in is per device and per kernel instance.
+template <int DT, bool SWIGLU>
+cudaError_t ensure_smem_attr()
+{
+    static std::atomic<uint64_t> done_mask{0};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (done_mask.load() & bit) return cudaSuccess;
+    err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<DT, SWIGLU>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (err == cudaSuccess) done_mask.fetch_or(bit);
+    return err;
+}
+
+int64_t tc_tile_upper_bound(int64_t rows, int E, int64_t n_tiles)
+{
+    const int64_t mt = rows / BM + (rows < E ? rows : E);
+    return mt * n_tiles;
+}
+
+template <int DT>
+cudaError_t launch_tc_dt(const void *x_disp, const int32_t *offsets, int64_t rows,
+                         const void *gate, const void *up, const void *down, int E,
+                         int64_t H, int64_t I, void *h_ws, void *out_disp,
+                         unsigned *status, cudaStream_t s)
+{
+    const CUtensorMapDataType tdt =
+        DT == DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUtensorMap mx, mg, mu, mh, md;
+    if (!encode_2d(&mx, tdt, x_disp, (uint64_t)H, (uint64_t)rows, BK, BM) ||
+        !encode_3d(&mg, tdt, gate, (uint64_t)H, (uint64_t)I, (uint64_t)E, BK, BN / 2) ||
+        !encode_3d(&mu, tdt, up, (uint64_t)H, (uint64_t)I, (uint64_t)E, BK, BN / 2) ||
+        !encode_2d(&mh, tdt, h_ws, (uint64_t)I, (uint64_t)rows, BK, BM) ||
+        !encode_3d(&md, tdt, down, (uint64_t)I, (uint64_t)H, (uint64_t)E, BK, BN))
+        return cudaErrorInvalidValue;
+    cudaError_t err = ensure_smem_attr<DT, true>();
+    if (err == cudaSuccess) err = ensure_smem_attr<DT, false>();
+    if (err != cudaSuccess) return err;
+    const int64_t sms = device_sm_count();
+    const int nt1 = (int)((I + BN / 2 - 1) / (BN / 2));
+    const int nt2 = (int)((H + BN - 1) / BN);
+    int64_t g1 = tc_tile_upper_bound(rows, E, nt1);
+    int64_t g2 = tc_tile_upper_bound(rows, E, nt2);
+    if (g1 > sms) g1 = sms;
+    if (g2 > sms) g2 = sms;
+    grouped_gemm_tc_kernel<DT, true><<<(unsigned)g1, THREADS, kSmemBytes, s>>>(
+        mx, mg, mu, offsets, E, (int)I, (int)H, nt1, h_ws, status);
+    grouped_gemm_tc_kernel<DT, false><<<(unsigned)g2, THREADS, kSmemBytes, s>>>(
+        mh, md, md, offsets, E, (int)H, (int)I, nt2, out_disp, status);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_experts_tc(int dt, const void *x_disp, const int32_t *offsets,
+                              int64_t rows, const void *gate, const void *up,
+                              const void *down, int E, int64_t H, int64_t I,
+                              void *h_ws, void *out_disp, unsigned *status,
+                              cudaStream_t s)
+{
+    if (rows == 0) return cudaSuccess;
+    if (dt == DT_BF16)
+        return launch_tc_dt<DT_BF16>(x_disp, offsets, rows, gate, up, down, E, H, I, h_ws, out_disp, status, s);
+    return launch_tc_dt<DT_F16>(x_disp, offsets, rows, gate, up, down, E, H, I, h_ws, out_disp, status, s);
+}
+
+}  // namespace moe

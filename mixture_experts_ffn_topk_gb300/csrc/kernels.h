@@ -1,0 +1,51 @@
+// kernels.h -- host-side launchers of the GB300 MoE kernels (internal).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+// Streaming multiprocessors of the current device (cached per device).
+int device_sm_count();
+
+// Softmax top-k routing, warp per token. E <= 1024.
+cudaError_t launch_route(const void *logits, int ldt, int64_t T, int E,
+                         int top_k, int renormalize, uint32_t *idx, void *w,
+                         cudaStream_t s);
+
+// Dispatch: per-chunk histograms, a scan, a stable rank/scatter, a row gather.
+size_t dispatch_workspace_bytes(int64_t A, int E);
+cudaError_t launch_dispatch(const uint32_t *idx, int64_t T, int top_k, int E,
+                            const void *x, int xdt, int64_t H, int32_t *counts,
+                            int32_t *offsets, int32_t *row_of, int32_t *src_of,
+                            void *x_disp, void *ws, unsigned *status,
+                            cudaStream_t s);
+
+// Weighted combine, optionally followed by residual Add + RMSNorm.
+int combine_max_h(int dt, bool norm);
+cudaError_t launch_combine(const void *out_disp, int dt, const void *w, int wdt,
+                           const int32_t *row_of, const void *residual,
+                           const void *gamma, int gdt, float eps, int64_t T,
+                           int top_k, int64_t H, void *y, void *x_out,
+                           float *rstd, cudaStream_t s);
+
+// FP32 SwiGLU experts on CUDA cores. h_ws holds [rows, I] floats.
+cudaError_t launch_experts_simt(const float *x_disp, const int32_t *offsets,
+                                int64_t rows, const float *gate,
+                                const float *up, const float *down, int E,
+                                int64_t H, int64_t I, float *h_ws,
+                                float *out_disp, cudaStream_t s);
+
+// BF16/F16 SwiGLU experts on tcgen05 tensor cores (TMA + TMEM).
+// h_ws holds [rows, I] elements of dt. Returns cudaErrorInvalidValue when a
+// TMA descriptor cannot be encoded for the given shapes/pointers.
+cudaError_t launch_experts_tc(int dt, const void *x_disp,
+                              const int32_t *offsets, int64_t rows,
+                              const void *gate, const void *up,
+                              const void *down, int E, int64_t H, int64_t I,
+                              void *h_ws, void *out_disp, unsigned *status,
+                              cudaStream_t s);
+
+}  // namespace moe

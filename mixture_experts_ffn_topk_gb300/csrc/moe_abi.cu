@@ -1,0 +1,356 @@
+// moe_abi.cu -- the extern "C" boundary declared in include/moe.h: host-side
+// argument validation, workspace carving and kernel launches. Nothing here
+// allocates device memory; nothing here synchronises except
+// moe_device_status().
+#include <math.h>
+#include <stdio.h>
+
+#include <atomic>
+
+#include "../../include/moe.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+// Per-device status word (ST_* bits); see moe_device_status().
+__device__ unsigned g_moe_status = 0u;
+
+int device_sm_count()
+{
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    const int slot = dev & 63;
+    int v = cache[slot].load();
+    if (v > 0) return v;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+        v = 1;
+    cache[slot].store(v);
+    return v;
+}
+
+namespace {
+
+thread_local char g_detail[256] = "";
+
+int fail(int code, const char *what)
+{
+    snprintf(g_detail, sizeof g_detail, "%s", what);
+    return code;
+}
+
+int cuda_fail(cudaError_t err, const char *where)
+{
+    snprintf(g_detail, sizeof g_detail, "%s: %s", where, cudaGetErrorString(err));
+    return MOE_ERR_CUDA;
+}
+
+unsigned *status_ptr()
+{
+    static std::atomic<unsigned *> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    unsigned *p = cache[dev & 63].load();
+    if (p != nullptr) return p;
+    void *q = nullptr;
+    if (cudaGetSymbolAddress(&q, g_moe_status) != cudaSuccess) return nullptr;
+    cache[dev & 63].store(static_cast<unsigned *>(q));
+    return static_cast<unsigned *>(q);
+}
+
+bool valid_dtype(int dt) { return dt == MOE_F32 || dt == MOE_BF16 || dt == MOE_F16; }
+size_t elem_bytes(int dt) { return dt == MOE_F32 ? 4 : 2; }
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+constexpr int64_t kMaxE = 1024;
+constexpr int64_t kMaxRows = 0x7fffffff;   // dispatched rows are int32
+
+// Vector width rule shared by the experts and combine kernels: rows are moved
+// in 16-byte vectors and TMA strides are 16-byte multiples.
+bool vec_dim_ok(int64_t n, int dt) { return n >= 1 && (n * (int64_t)elem_bytes(dt)) % 16 == 0; }
+
+int check_route_args(const void *logits, int ldt, int64_t T, int64_t E, int top_k,
+                     const uint32_t *idx, const void *w)
+{
+    if (!valid_dtype(ldt)) return fail(MOE_ERR_DTYPE, "logits dtype must be F32, BF16 or F16");
+    if (T < 0 || E < 1 || E > kMaxE) return fail(MOE_ERR_SHAPE, "need T >= 0 and 1 <= E <= 1024");
+    if (top_k < 1 || top_k > E) return fail(MOE_ERR_SHAPE, "need 1 <= top_k <= E");
+    if (T * top_k > kMaxRows) return fail(MOE_ERR_SHAPE, "T * top_k exceeds 2^31 - 1");
+    if (T == 0) return MOE_OK;
+    if (!logits || !idx || !w) return fail(MOE_ERR_NULL, "moe_route: NULL tensor");
+    if (!aligned16(logits) || !aligned16(idx) || !aligned16(w))
+        return fail(MOE_ERR_ALIGN, "moe_route: tensors must be 16-byte aligned");
+    return MOE_OK;
+}
+
+int check_experts_args(int64_t rows, int64_t E, int64_t H, int64_t I, int dt)
+{
+    if (!valid_dtype(dt)) return fail(MOE_ERR_DTYPE, "expert dtype must be F32, BF16 or F16");
+    if (rows < 0 || rows > kMaxRows || E < 1 || E > kMaxE)
+        return fail(MOE_ERR_SHAPE, "need 0 <= rows < 2^31 and 1 <= E <= 1024");
+    if (!vec_dim_ok(H, dt) || !vec_dim_ok(I, dt))
+        return fail(MOE_ERR_SHAPE, "H and I must be >= 1 with H*elem and I*elem multiples of 16 bytes");
+    if (H > 0x7fffffff || I > 0x7fffffff) return fail(MOE_ERR_SHAPE, "H and I must fit int32");
+    return MOE_OK;
+}
+
+int check_combine_args(int dt, int wdt, int64_t T, int top_k, int64_t H, bool norm)
+{
+    if (!valid_dtype(dt) || !valid_dtype(wdt)) return fail(MOE_ERR_DTYPE, "dtype must be F32, BF16 or F16");
+    if (T < 0 || top_k < 1 || T * top_k > kMaxRows) return fail(MOE_ERR_SHAPE, "need T >= 0, top_k >= 1, T*top_k < 2^31");
+    if (!vec_dim_ok(H, dt)) return fail(MOE_ERR_SHAPE, "H*elem must be a positive multiple of 16 bytes");
+    if (H > combine_max_h(dt, norm)) return fail(MOE_ERR_SHAPE, "H too large for the fused norm (one pass per row)");
+    return MOE_OK;
+}
+
+struct ForwardLayout {
+    size_t idx, w, counts, offsets, row_of, src_of, disp_ws, x_disp, h, out_disp, total;
+};
+
+ForwardLayout forward_layout(int64_t T, int64_t H, int64_t I, int64_t E, int top_k,
+                             int dt, int ldt)
+{
+    const size_t A = (size_t)(T * top_k), eb = elem_bytes(dt);
+    ForwardLayout L;
+    size_t off = 0;
+    auto take = [&](size_t bytes) { const size_t at = off; off = round_up(off + bytes, 256); return at; };
+    L.idx = take(A * 4);
+    L.w = take(A * elem_bytes(ldt));
+    L.counts = take((size_t)E * 4);
+    L.offsets = take((size_t)(E + 1) * 4);
+    L.row_of = take(A * 4);
+    L.src_of = take(A * 4);
+    L.disp_ws = take(dispatch_workspace_bytes((int64_t)A, (int)E));
+    L.x_disp = take(A * (size_t)H * eb);
+    L.h = take(A * (size_t)I * eb);
+    L.out_disp = take(A * (size_t)H * eb);
+    L.total = off;
+    return L;
+}
+
+int run_experts(const void *x_disp, const int32_t *offsets, int64_t rows, const void *gate,
+                const void *up, const void *down, int64_t E, int64_t H, int64_t I, int dt,
+                void *h_ws, void *out_disp, cudaStream_t s)
+{
+    cudaError_t err;
+    if (dt == MOE_F32) {
+        err = launch_experts_simt(static_cast<const float *>(x_disp), offsets, rows,
+                                  static_cast<const float *>(gate), static_cast<const float *>(up),
+                                  static_cast<const float *>(down), (int)E, H, I,
+                                  static_cast<float *>(h_ws), static_cast<float *>(out_disp), s);
+    } else {
+        unsigned *st = status_ptr();
+        if (!st) return fail(MOE_ERR_CUDA, "cannot resolve the device status word");
+        err = launch_experts_tc(dt, x_disp, offsets, rows, gate, up, down, (int)E, H, I, h_ws,
+                                out_disp, st, s);
+        if (err == cudaErrorInvalidValue)
+            return fail(MOE_ERR_ALIGN, "TMA descriptor rejected (pointer alignment or shape)");
+    }
+    if (err != cudaSuccess) return cuda_fail(err, "experts launch");
+    return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char *moe_status_string(int status)
+{
+    switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_NULL: return "a required pointer is NULL";
+    case MOE_ERR_SHAPE: return "a size is out of range or inconsistent";
+    case MOE_ERR_DTYPE: return "unsupported dtype or dtype combination";
+    case MOE_ERR_VALUE: return "invalid scalar argument";
+    case MOE_ERR_ALIGN: return "a tensor pointer is not 16-byte aligned";
+    case MOE_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_DEVICE_TIMEOUT: return "a bounded device wait gave up";
+    case MOE_ERR_BAD_INDEX: return "an expert index >= E reached dispatch";
+    default: return "unknown status";
+    }
+}
+
+int moe_abi_version(void) { return 100; }
+
+const char *moe_last_error_detail(void) { return g_detail; }
+
+int moe_route(const void *logits, int logits_dtype, int64_t T, int64_t E, int top_k,
+              int renormalize, uint32_t *expert_indices, void *weights, void *stream)
+{
+    int rc = check_route_args(logits, logits_dtype, T, E, top_k, expert_indices, weights);
+    if (rc != MOE_OK || T == 0) return rc;
+    cudaError_t err = launch_route(logits, logits_dtype, T, (int)E, top_k, renormalize,
+                                   expert_indices, weights, static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_route");
+}
+
+size_t moe_dispatch_workspace_size(int64_t T, int top_k, int64_t E)
+{
+    if (T <= 0 || top_k < 1 || E < 1 || E > kMaxE) return 0;
+    return round_up(dispatch_workspace_bytes(T * top_k, (int)E), 256);
+}
+
+int moe_dispatch(const uint32_t *expert_indices, int64_t T, int top_k, int64_t E,
+                 const void *x, int x_dtype, int64_t H, int32_t *counts, int32_t *offsets,
+                 int32_t *row_of, int32_t *src_of, void *x_disp, void *workspace,
+                 size_t workspace_bytes, void *stream)
+{
+    if (!valid_dtype(x_dtype)) return fail(MOE_ERR_DTYPE, "x dtype must be F32, BF16 or F16");
+    if (T < 0 || E < 1 || E > kMaxE || top_k < 1 || H < 1 || T * top_k > kMaxRows)
+        return fail(MOE_ERR_SHAPE, "need T >= 0, 1 <= E <= 1024, top_k >= 1, H >= 1");
+    if (T == 0) return MOE_OK;
+    if (!expert_indices || !x || !counts || !offsets || !row_of || !src_of || !x_disp)
+        return fail(MOE_ERR_NULL, "moe_dispatch: NULL tensor");
+    if (!aligned16(expert_indices) || !aligned16(x) || !aligned16(counts) || !aligned16(offsets) ||
+        !aligned16(row_of) || !aligned16(src_of) || !aligned16(x_disp))
+        return fail(MOE_ERR_ALIGN, "moe_dispatch: tensors must be 16-byte aligned");
+    const size_t need = moe_dispatch_workspace_size(T, top_k, E);
+    if (workspace_bytes < need || (need && !workspace) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return fail(MOE_ERR_WORKSPACE, "moe_dispatch: workspace too small or not 256-byte aligned");
+    unsigned *st = status_ptr();
+    if (!st) return fail(MOE_ERR_CUDA, "cannot resolve the device status word");
+    cudaError_t err = launch_dispatch(expert_indices, T, top_k, (int)E, x, x_dtype, H, counts,
+                                      offsets, row_of, src_of, x_disp, workspace, st,
+                                      static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_dispatch");
+}
+
+size_t moe_experts_workspace_size(int64_t rows, int64_t E, int64_t H, int64_t I, int dtype)
+{
+    (void)E;
+    (void)H;
+    if (rows <= 0 || I <= 0 || !valid_dtype(dtype)) return 0;
+    return round_up((size_t)rows * (size_t)I * elem_bytes(dtype), 256);
+}
+
+int moe_experts_forward(const void *x_disp, const int32_t *offsets, int64_t rows,
+                        const void *gate, const void *up, const void *down, int64_t E,
+                        int64_t H, int64_t I, int dtype, void *out_disp, void *workspace,
+                        size_t workspace_bytes, void *stream)
+{
+    int rc = check_experts_args(rows, E, H, I, dtype);
+    if (rc != MOE_OK || rows == 0) return rc;
+    if (!x_disp || !offsets || !gate || !up || !down || !out_disp)
+        return fail(MOE_ERR_NULL, "moe_experts_forward: NULL tensor");
+    if (!aligned16(x_disp) || !aligned16(offsets) || !aligned16(gate) || !aligned16(up) ||
+        !aligned16(down) || !aligned16(out_disp))
+        return fail(MOE_ERR_ALIGN, "moe_experts_forward: tensors must be 16-byte aligned");
+    const size_t need = moe_experts_workspace_size(rows, E, H, I, dtype);
+    if (workspace_bytes < need || !workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return fail(MOE_ERR_WORKSPACE, "moe_experts_forward: workspace too small or not 256-byte aligned");
+    return run_experts(x_disp, offsets, rows, gate, up, down, E, H, I, dtype, workspace,
+                       out_disp, static_cast<cudaStream_t>(stream));
+}
+
+int moe_combine(const void *out_disp, int dtype, const void *weights, int weights_dtype,
+                const int32_t *row_of, int64_t T, int top_k, int64_t H, void *y, void *stream)
+{
+    int rc = check_combine_args(dtype, weights_dtype, T, top_k, H, false);
+    if (rc != MOE_OK || T == 0) return rc;
+    if (!out_disp || !weights || !row_of || !y) return fail(MOE_ERR_NULL, "moe_combine: NULL tensor");
+    if (!aligned16(out_disp) || !aligned16(weights) || !aligned16(row_of) || !aligned16(y))
+        return fail(MOE_ERR_ALIGN, "moe_combine: tensors must be 16-byte aligned");
+    cudaError_t err = launch_combine(out_disp, dtype, weights, weights_dtype, row_of, nullptr,
+                                     nullptr, MOE_F32, 1.0f, T, top_k, H, y, nullptr, nullptr,
+                                     static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_combine");
+}
+
+int moe_combine_add_rmsnorm(const void *out_disp, int dtype, const void *weights,
+                            int weights_dtype, const int32_t *row_of, const void *residual,
+                            const void *gamma, int gamma_dtype, float eps, int64_t T, int top_k,
+                            int64_t H, void *y, void *x_out, float *rstd, void *stream)
+{
+    int rc = check_combine_args(dtype, weights_dtype, T, top_k, H, true);
+    if (rc != MOE_OK) return rc;
+    if (!valid_dtype(gamma_dtype)) return fail(MOE_ERR_DTYPE, "gamma dtype must be F32, BF16 or F16");
+    if (!(isfinite(eps) && eps > 0.0f)) return fail(MOE_ERR_VALUE, "eps must be finite and > 0");
+    if (T == 0) return MOE_OK;
+    if (!out_disp || !weights || !row_of || !residual || !gamma || !y || !x_out || !rstd)
+        return fail(MOE_ERR_NULL, "moe_combine_add_rmsnorm: NULL tensor");
+    if (!aligned16(out_disp) || !aligned16(weights) || !aligned16(row_of) || !aligned16(residual) ||
+        !aligned16(gamma) || !aligned16(y) || !aligned16(x_out) || !aligned16(rstd))
+        return fail(MOE_ERR_ALIGN, "moe_combine_add_rmsnorm: tensors must be 16-byte aligned");
+    cudaError_t err = launch_combine(out_disp, dtype, weights, weights_dtype, row_of, residual,
+                                     gamma, gamma_dtype, eps, T, top_k, H, y, x_out, rstd,
+                                     static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_combine_add_rmsnorm");
+}
+
+size_t moe_forward_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E, int top_k,
+                                  int dtype, int logits_dtype)
+{
+    if (T <= 0 || H < 1 || I < 1 || E < 1 || E > kMaxE || top_k < 1 || top_k > E ||
+        !valid_dtype(dtype) || !valid_dtype(logits_dtype))
+        return 0;
+    return forward_layout(T, H, I, E, top_k, dtype, logits_dtype).total;
+}
+
+int moe_forward(const void *x, int dtype, const void *logits, int logits_dtype, const void *gate,
+                const void *up, const void *down, int64_t T, int64_t H, int64_t I, int64_t E,
+                int top_k, int renormalize, void *y, void *workspace, size_t workspace_bytes,
+                void *stream)
+{
+    if (!valid_dtype(logits_dtype)) return fail(MOE_ERR_DTYPE, "logits dtype must be F32, BF16 or F16");
+    int rc = check_experts_args(T * (int64_t)(top_k > 0 ? top_k : 1), E, H, I, dtype);
+    if (rc != MOE_OK) return rc;
+    if (T < 0 || top_k < 1 || top_k > E || T * top_k > kMaxRows)
+        return fail(MOE_ERR_SHAPE, "need T >= 0 and 1 <= top_k <= E");
+    if (T == 0) return MOE_OK;
+    if (!x || !logits || !gate || !up || !down || !y) return fail(MOE_ERR_NULL, "moe_forward: NULL tensor");
+    if (!aligned16(x) || !aligned16(logits) || !aligned16(gate) || !aligned16(up) ||
+        !aligned16(down) || !aligned16(y))
+        return fail(MOE_ERR_ALIGN, "moe_forward: tensors must be 16-byte aligned");
+    const ForwardLayout L = forward_layout(T, H, I, E, top_k, dtype, logits_dtype);
+    if (workspace_bytes < L.total || !workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return fail(MOE_ERR_WORKSPACE, "moe_forward: workspace too small or not 256-byte aligned");
+    unsigned *st = status_ptr();
+    if (!st) return fail(MOE_ERR_CUDA, "cannot resolve the device status word");
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    uint32_t *idx = reinterpret_cast<uint32_t *>(ws + L.idx);
+    void *w = ws + L.w;
+    int32_t *counts = reinterpret_cast<int32_t *>(ws + L.counts);
+    int32_t *offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
+    int32_t *row_of = reinterpret_cast<int32_t *>(ws + L.row_of);
+    int32_t *src_of = reinterpret_cast<int32_t *>(ws + L.src_of);
+    void *x_disp = ws + L.x_disp, *h = ws + L.h, *out_disp = ws + L.out_disp;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t A = T * top_k;
+
+    cudaError_t err = launch_route(logits, logits_dtype, T, (int)E, top_k, renormalize, idx, w, s);
+    if (err != cudaSuccess) return cuda_fail(err, "moe_forward/route");
+    err = launch_dispatch(idx, T, top_k, (int)E, x, dtype, H, counts, offsets, row_of, src_of,
+                          x_disp, ws + L.disp_ws, st, s);
+    if (err != cudaSuccess) return cuda_fail(err, "moe_forward/dispatch");
+    rc = run_experts(x_disp, offsets, A, gate, up, down, E, H, I, dtype, h, out_disp, s);
+    if (rc != MOE_OK) return rc;
+    err = launch_combine(out_disp, dtype, w, logits_dtype, row_of, nullptr, nullptr, MOE_F32, 1.0f,
+                         T, top_k, H, y, nullptr, nullptr, s);
+    return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_forward/combine");
+}
+
+int moe_device_status(void *stream, int clear)
+{
+    cudaError_t err = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess) return cuda_fail(err, "moe_device_status/sync");
+    unsigned v = 0;
+    err = cudaMemcpyFromSymbol(&v, g_moe_status, sizeof v);
+    if (err != cudaSuccess) return cuda_fail(err, "moe_device_status/read");
+    if (clear) {
+        const unsigned zero = 0;
+        err = cudaMemcpyToSymbol(g_moe_status, &zero, sizeof zero);
+        if (err != cudaSuccess) return cuda_fail(err, "moe_device_status/clear");
+    }
+    if (v & ST_TIMEOUT) return MOE_ERR_DEVICE_TIMEOUT;
+    if (v & ST_BAD_INDEX) return MOE_ERR_BAD_INDEX;
+    return MOE_OK;
+}
+
+}  // extern "C"

@@ -161,18 +161,27 @@ def _plant_special_rows(l: torch.Tensor, E: int) -> None:
     l[5, :] = float("-inf")
 
 
-def moe_inputs(cfg: MoeConfig, device="cpu", seed: int | None = None) -> dict:
-    """x [T,H], logits [T,E], gate/up [E,I,H], down [E,H,I] as torch tensors
-    on ``device``. The same seed and device always give the same bytes."""
-    g = _gen(cfg.seed if seed is None else seed, device)
-    logits = _logits(cfg, g, device)
-    x = _normal((cfg.T, cfg.H), g, device, dtype=cfg.dtype)
+def moe_inputs(cfg: MoeConfig, device="cpu", seed: int | None = None,
+               weights_device=None) -> dict:
+    """x [T,H], logits [T,E], gate/up [E,I,H], down [E,H,I] as torch tensors.
+
+    Logits and x are always drawn by a CPU generator (so the routing of a
+    workload is the same whatever device the tensors end up on) and moved to
+    ``device``. The expert weights are drawn by a generator on
+    ``weights_device`` (default ``device``), which lets multi-GB weights be
+    drawn in place on a GPU. Same seed and devices -> same bytes."""
+    seed = cfg.seed if seed is None else seed
+    g = _gen(seed, "cpu")
+    logits = _logits(cfg, g, "cpu").to(device)
+    x = _normal((cfg.T, cfg.H), g, "cpu", dtype=cfg.dtype).to(device)
+    wdev = device if weights_device is None else weights_device
+    gw = _gen(seed + 7919, wdev)
     rows = max(1, (1 << 24) // max(1, cfg.I * cfg.H))
-    gate = _normal((cfg.E, cfg.I, cfg.H), g, device, std=cfg.H ** -0.5,
+    gate = _normal((cfg.E, cfg.I, cfg.H), gw, wdev, std=cfg.H ** -0.5,
                    dtype=cfg.dtype, chunk_rows=rows)
-    up = _normal((cfg.E, cfg.I, cfg.H), g, device, std=cfg.H ** -0.5,
+    up = _normal((cfg.E, cfg.I, cfg.H), gw, wdev, std=cfg.H ** -0.5,
                  dtype=cfg.dtype, chunk_rows=rows)
-    down = _normal((cfg.E, cfg.H, cfg.I), g, device, std=cfg.I ** -0.5,
+    down = _normal((cfg.E, cfg.H, cfg.I), gw, wdev, std=cfg.I ** -0.5,
                    dtype=cfg.dtype, chunk_rows=rows)
     return {"x": x, "logits": logits, "gate": gate, "up": up, "down": down}
 
@@ -180,10 +189,12 @@ def moe_inputs(cfg: MoeConfig, device="cpu", seed: int | None = None) -> dict:
 def combine_norm_inputs(cfg: CombineNormConfig, device="cpu",
                         seed: int | None = None) -> dict:
     """Expert outputs ``out_disp [T*top_k, H]``, routing logits ``[T, E]``
-    (FP32), ``residual [T, H]`` and ``gamma [H]``."""
-    g = _gen(cfg.seed if seed is None else seed, device)
-    logits = torch.randn((cfg.T, cfg.E), generator=g, device=device,
-                         dtype=torch.float32)
+    (FP32, drawn on the CPU), ``residual [T, H]`` and ``gamma [H]`` (drawn on
+    ``device``)."""
+    seed = cfg.seed if seed is None else seed
+    logits = torch.randn((cfg.T, cfg.E), generator=_gen(seed, "cpu"),
+                         dtype=torch.float32).to(device)
+    g = _gen(seed + 7919, device)
     rows = max(1, (1 << 24) // cfg.H)
     out_disp = _normal((cfg.T * cfg.top_k, cfg.H), g, device, dtype=cfg.dtype,
                        chunk_rows=rows)

@@ -1,0 +1,169 @@
+"""The C ABI library on a machine without a GPU: it builds, loads, exports
+every entry point include/moe.h declares, sizes workspaces, and rejects bad
+arguments on the host before any CUDA call (no compute is launched here)."""
+
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+import mixture_experts_ffn_topk_gb300 as moe
+from mixture_experts_ffn_topk_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+OK, NULL, SHAPE, DTYPE, VALUE, ALIGN, WORKSPACE = 0, 1, 2, 3, 4, 5, 6
+F32, BF16, F16 = 0, 1, 2
+FAKE = 0x7f0000000000          # 16-byte aligned, never dereferenced
+FAKE_ODD = FAKE + 8
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return moe.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    for n in ["moe_route", "moe_dispatch", "moe_experts_forward", "moe_combine",
+              "moe_combine_add_rmsnorm", "moe_forward", "moe_device_status"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(moe.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(raw, name), f"{name} declared in moe.h but not exported"
+    assert sorted(moe.EXPORTED) == declared_functions()
+
+
+def test_status_strings(lib):
+    for code in range(10):
+        assert moe.moe_status_string(code)
+    assert moe.moe_status_string(99) == "unknown status"
+    assert moe.moe_abi_version() == 100
+
+
+def P(v):
+    return ctypes.c_void_p(v)
+
+
+def test_route_validation(lib):
+    s = P(None)
+    assert lib.moe_route(P(FAKE), 7, 4, 8, 2, 1, P(FAKE), P(FAKE), s) == DTYPE
+    assert lib.moe_route(P(FAKE), F32, 4, 0, 1, 1, P(FAKE), P(FAKE), s) == SHAPE
+    assert lib.moe_route(P(FAKE), F32, 4, 1025, 1, 1, P(FAKE), P(FAKE), s) == SHAPE
+    assert lib.moe_route(P(FAKE), F32, 4, 8, 0, 1, P(FAKE), P(FAKE), s) == SHAPE
+    assert lib.moe_route(P(FAKE), F32, 4, 8, 9, 1, P(FAKE), P(FAKE), s) == SHAPE
+    assert lib.moe_route(P(FAKE), F32, -1, 8, 2, 1, P(FAKE), P(FAKE), s) == SHAPE
+    assert lib.moe_route(P(None), F32, 4, 8, 2, 1, P(FAKE), P(FAKE), s) == NULL
+    assert lib.moe_route(P(FAKE_ODD), F32, 4, 8, 2, 1, P(FAKE), P(FAKE), s) == ALIGN
+    # T == 0 is a valid no-op even with NULL tensors
+    assert lib.moe_route(P(None), BF16, 0, 8, 2, 1, P(None), P(None), s) == OK
+    lib.moe_route(P(FAKE), F32, 4, 8, 9, 1, P(FAKE), P(FAKE), s)
+    assert b"top_k" in lib.moe_last_error_detail()
+
+
+def test_dispatch_validation(lib):
+    s = P(None)
+    args = lambda **kw: [kw.get("idx", P(FAKE)), kw.get("T", 16), kw.get("k", 2),
+                         kw.get("E", 8), kw.get("x", P(FAKE)), kw.get("xdt", BF16),
+                         kw.get("H", 64), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE),
+                         kw.get("ws", P(FAKE)), kw.get("wsb", 1 << 20), s]
+    assert lib.moe_dispatch(*args(xdt=5)) == DTYPE
+    assert lib.moe_dispatch(*args(E=0)) == SHAPE
+    assert lib.moe_dispatch(*args(H=0)) == SHAPE
+    assert lib.moe_dispatch(*args(idx=P(None))) == NULL
+    assert lib.moe_dispatch(*args(x=P(FAKE_ODD))) == ALIGN
+    assert lib.moe_dispatch(*args(wsb=0)) == WORKSPACE
+    assert lib.moe_dispatch(*args(ws=P(FAKE + 16))) == WORKSPACE
+    assert lib.moe_dispatch(*args(T=0, idx=P(None))) == OK
+
+
+def test_workspace_sizes(lib):
+    assert lib.moe_dispatch_workspace_size(0, 2, 8) == 0
+    ws = lib.moe_dispatch_workspace_size(4096, 6, 64)
+    assert ws > 0 and ws % 256 == 0
+    assert lib.moe_experts_workspace_size(100, 8, 64, 40, BF16) >= 100 * 40 * 2
+    assert lib.moe_experts_workspace_size(100, 8, 64, 40, F32) >= 100 * 40 * 4
+    fw = lib.moe_forward_workspace_size(4096, 2048, 1408, 64, 6, BF16, BF16)
+    A = 4096 * 6
+    assert fw >= A * (2048 * 2 * 2 + 1408 * 2) + A * (4 + 2 + 4 + 4)
+    assert lib.moe_forward_workspace_size(4096, 2048, 1408, 64, 65, BF16, BF16) == 0
+
+
+def test_experts_validation(lib):
+    s = P(None)
+    base = dict(x=P(FAKE), off=P(FAKE), rows=64, g=P(FAKE), u=P(FAKE), d=P(FAKE),
+                E=4, H=64, I=32, dt=BF16, out=P(FAKE), ws=P(FAKE), wsb=1 << 20)
+
+    def call(**kw):
+        a = dict(base, **kw)
+        return lib.moe_experts_forward(a["x"], a["off"], a["rows"], a["g"], a["u"],
+                                       a["d"], a["E"], a["H"], a["I"], a["dt"],
+                                       a["out"], a["ws"], a["wsb"], s)
+    assert call(dt=9) == DTYPE
+    assert call(H=60) == SHAPE          # 60 * 2 bytes is not a 16-byte multiple
+    assert call(I=6, dt=F32) == SHAPE   # 24 bytes
+    assert call(E=2000) == SHAPE
+    assert call(g=P(None)) == NULL
+    assert call(d=P(FAKE_ODD)) == ALIGN
+    assert call(wsb=16) == WORKSPACE
+    assert call(rows=0, x=P(None)) == OK
+
+
+def test_combine_validation(lib):
+    s = P(None)
+    assert lib.moe_combine(P(FAKE), BF16, P(FAKE), F32, P(FAKE), 8, 2, 60, P(FAKE), s) == SHAPE
+    assert lib.moe_combine(P(FAKE), 4, P(FAKE), F32, P(FAKE), 8, 2, 64, P(FAKE), s) == DTYPE
+    assert lib.moe_combine(P(None), BF16, P(FAKE), F32, P(FAKE), 8, 2, 64, P(FAKE), s) == NULL
+    assert lib.moe_combine(P(FAKE), BF16, P(FAKE), F32, P(FAKE), 0, 2, 64, P(None), s) == OK
+    for eps in (0.0, -1e-6, math.inf, math.nan):
+        rc = lib.moe_combine_add_rmsnorm(P(FAKE), BF16, P(FAKE), F32, P(FAKE), P(FAKE),
+                                         P(FAKE), BF16, eps, 8, 2, 64, P(FAKE), P(FAKE),
+                                         P(FAKE), s)
+        assert rc == VALUE, eps
+    big = 8 * 256 * 8 + 8
+    assert lib.moe_combine_add_rmsnorm(P(FAKE), BF16, P(FAKE), F32, P(FAKE), P(FAKE),
+                                       P(FAKE), BF16, 1e-6, 8, 2, big, P(FAKE), P(FAKE),
+                                       P(FAKE), s) == SHAPE
+
+
+def test_forward_validation(lib):
+    s = P(None)
+
+    def call(**kw):
+        a = dict(x=P(FAKE), dt=BF16, lg=P(FAKE), ldt=BF16, T=32, H=64, I=32, E=8, k=2,
+                 y=P(FAKE), ws=P(FAKE), wsb=1 << 30)
+        a.update(kw)
+        return lib.moe_forward(a["x"], a["dt"], a["lg"], a["ldt"], P(FAKE), P(FAKE),
+                               P(FAKE), a["T"], a["H"], a["I"], a["E"], a["k"], 1,
+                               a["y"], a["ws"], a["wsb"], s)
+    assert call(ldt=3) == DTYPE
+    assert call(k=9) == SHAPE
+    assert call(k=0) == SHAPE
+    assert call(lg=P(None)) == NULL
+    assert call(y=P(FAKE_ODD)) == ALIGN
+    assert call(wsb=100) == WORKSPACE
+    assert call(T=0, x=P(None), lg=P(None), y=P(None)) == OK
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    with pytest.raises(ValueError):
+        moe.moe_route(torch.zeros(4, 8), 2, True, stream=0)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError, match="not built"):
+        moe.load_library(str(tmp_path / "nope.so"))

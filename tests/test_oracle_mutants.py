@@ -5,6 +5,8 @@ Each mutant is a one-place edit of ``oracle/moe_oracle.c`` built into a
 temporary library; at least one ``check_*`` in ``oracle_pins.py`` must fail on
 it. This shows the pins constrain each step of the oracle (routing, dispatch,
 gather, experts, combine, norm, dtype rounding), not only its happy path.
+Every mutant keeps all memory accesses in bounds: mutants run inside the test
+process, so one that wrote out of bounds could corrupt it.
 """
 
 import ctypes
@@ -49,8 +51,10 @@ MUTANTS = [
      "src_of[r] = (int32_t)(a / top_k);"),
     ("gather_wrong_token", "int64_t t = src_of[r] / top_k;",
      "int64_t t = src_of[r] % top_k;"),
-    ("offsets_inclusive", "offsets[e + 1] = offsets[e] + counts[e];\n        next[e] = offsets[e];",
-     "offsets[e + 1] = offsets[e] + counts[e];\n        next[e] = offsets[e + 1] - counts[e] + (e > 0);"),
+    ("offsets_short_by_one", "offsets[e + 1] = offsets[e] + counts[e];\n        next[e] = offsets[e];",
+     "offsets[e + 1] = offsets[e] + counts[e] - (e + 1 == E);\n        next[e] = offsets[e];"),
+    ("rows_reversed_in_expert", "int64_t r = next[e]++;",
+     "int64_t r = offsets[e + 1] - 1 - (next[e]++ - offsets[e]);"),
     ("rms_mean_off_by_one", "ss / (double)H + (double)eps", "ss / (double)(H + 1) + (double)eps"),
     ("rms_eps_dropped", "ss / (double)H + (double)eps", "ss / (double)H"),
     ("rms_not_reciprocal", "double r = 1.0 / sqrt(", "double r = sqrt("),

@@ -1,0 +1,379 @@
+"""CUDA path vs the CPU oracle, element by element, through the C ABI.
+
+Every input is seeded and synthetic (``workloads``); every expected value
+comes from ``oracle/`` on the same bytes. Sizes span several 128-row tiles,
+ragged K/N/M edges, empty experts and the degenerate cases (E=1, top_k=E,
+invalid rows, T=0). Full-size workloads are checked in
+``test_parity_full_gpu.py``.
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import mixture_experts_ffn_topk_gb300 as moe
+from mixture_experts_ffn_topk_gb300 import workloads as W
+from parity import TORCH_TO_NAME, assert_close, np_of, per_expert_sets, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from mixture_experts_ffn_topk_gb300 import build
+    build.build()
+    moe.load_library()
+    return torch.device("cuda:0")
+
+
+def cfg_small(name, **kw):
+    return W.MoeConfig(name, 90, **kw)
+
+
+# (name, T, H, I, E, k, renorm, dtype, logits dtype, bias, bias param)
+SMALL = [
+    cfg_small("multi_tile_bf16", T=300, H=320, I=200, E=6, top_k=2, renormalize=True,
+              dtype="bf16", logits_dtype="f32", logit_bias="normal", bias_param=1.0),
+    cfg_small("many_experts_bf16", T=256, H=256, I=136, E=64, top_k=6,
+              renormalize=False, dtype="bf16", logits_dtype="bf16"),
+    cfg_small("single_expert_bf16", T=150, H=192, I=264, E=1, top_k=1,
+              renormalize=True, dtype="bf16", logits_dtype="bf16"),
+    cfg_small("topk_equals_e_f16", T=70, H=128, I=64, E=4, top_k=4, renormalize=True,
+              dtype="f16", logits_dtype="f16"),
+    cfg_small("hot_expert_bf16", T=400, H=128, I=128, E=8, top_k=2, renormalize=True,
+              dtype="bf16", logits_dtype="f32", logit_bias="zipf", bias_param=3.0),
+    cfg_small("multi_tile_f32", T=200, H=192, I=136, E=5, top_k=2, renormalize=False,
+              dtype="f32", logits_dtype="f32", logit_bias="normal", bias_param=0.5),
+    W.CONFIGS["tiny_fp32"],
+]
+
+
+def oracle_inputs(d):
+    return {k: np_of(v) for k, v in d.items()}
+
+
+def inputs_on(cfg, dev):
+    cpu = W.moe_inputs(cfg, device="cpu")
+    return cpu, {k: v.to(dev) for k, v in cpu.items()}
+
+
+# ---------------------------------------------------------------- routing
+
+ROUTE_CASES = [
+    # (T, E, k, renorm, logits dtype, generator)
+    (1000, 64, 6, False, "bf16", "normal"),
+    (1000, 8, 2, True, "f32", "normal"),
+    (333, 256, 8, True, "f32", "normal"),
+    (257, 33, 5, True, "f16", "normal"),
+    (64, 1, 1, False, "f32", "normal"),
+    (64, 1, 1, True, "bf16", "normal"),
+    (50, 7, 7, True, "f32", "normal"),
+    (40, 1024, 16, True, "f32", "normal"),
+    (12, 1024, 1024, False, "f32", "normal"),
+    (500, 16, 4, True, "f32", "ties"),
+    (500, 40, 3, False, "bf16", "ties"),
+    (300, 24, 4, True, "f32", "specials"),
+]
+
+
+def _route_logits(T, E, ldt, kind, seed):
+    g = torch.Generator().manual_seed(seed)
+    if kind == "ties":
+        l = torch.randint(-2, 3, (T, E), generator=g).float() * 0.5
+    else:
+        l = torch.randn((T, E), generator=g)
+    if kind == "specials":
+        l[0, 3] = float("nan")
+        l[1, :] = float("-inf")
+        l[2, 5] = float("inf")
+        l[3, ::2] = float("-inf")           # valid: finite and -inf mixed
+        l[4, :] = float("-inf")
+        l[4, E - 1] = 0.0                    # one finite entry, k > 1
+        l[5, 0] = float("-inf")
+        l[5, 1] = float("inf")
+        l[6, :] = 0.0                        # all tied
+        l[7, :] = -0.0
+        l[7, 2] = 0.0                        # +0 and -0 tie
+    return l.to(W.TORCH_DTYPES[ldt])
+
+
+@pytest.mark.parametrize("T,E,k,renorm,ldt,kind", ROUTE_CASES)
+def test_route_parity(dev, T, E, k, renorm, ldt, kind):
+    logits = _route_logits(T, E, ldt, kind, seed=T * 131 + E)
+    idx_ref, w_ref, _ = oracle.route(np_of(logits), ldt, k, renorm)
+    idx, w = moe.moe_route(logits.to(dev), k, renorm)
+    torch.cuda.synchronize()
+    assert np.array_equal(idx.cpu().numpy().view(np.uint32), idx_ref), "expert ids differ"
+    assert_close(to_f64(w), oracle.to_f64(w_ref, ldt), ldt if ldt != "f32" else "f32", "weights")
+
+
+def test_route_workload_logits(dev):
+    for cfg in list(W.CONFIGS.values()):
+        logits = W.moe_inputs(cfg.scaled(I=8, H=8), device="cpu")["logits"]
+        idx_ref, w_ref, inval = oracle.route(np_of(logits), cfg.logits_dtype, cfg.top_k,
+                                             cfg.renormalize)
+        idx, w = moe.moe_route(logits.to(dev), cfg.top_k, cfg.renormalize)
+        torch.cuda.synchronize()
+        assert np.array_equal(idx.cpu().numpy().view(np.uint32), idx_ref), cfg.name
+        assert_close(to_f64(w), oracle.to_f64(w_ref, cfg.logits_dtype), cfg.logits_dtype,
+                     cfg.name)
+    cn = W.COMBINE_NORM
+    logits = W.combine_norm_inputs(cn.scaled(T=cn.T, H=8), device="cpu")["logits"]
+    idx_ref, w_ref, _ = oracle.route(np_of(logits), "f32", cn.top_k, True)
+    idx, w = moe.moe_route(logits.to(dev), cn.top_k, True)
+    torch.cuda.synchronize()
+    assert np.array_equal(idx.cpu().numpy().view(np.uint32), idx_ref)
+    assert_close(to_f64(w), w_ref.astype(np.float64), "f32", "combine-norm routing")
+
+
+def test_route_empty(dev):
+    idx, w = moe.moe_route(torch.empty((0, 8), device=dev), 2, True)
+    assert idx.shape == (0, 2) and w.shape == (0, 2)
+
+
+# ---------------------------------------------------------------- dispatch
+
+def _check_dispatch(d, idx_np, x_np, E, k, dt):
+    counts, offsets, row_of, src_of, bad = oracle.dispatch(idx_np, E)
+    g_counts = d["counts"].cpu().numpy()
+    g_offsets = d["offsets"].cpu().numpy()
+    g_row = d["row_of"].cpu().numpy()
+    g_src = d["src_of"].cpu().numpy()
+    assert np.array_equal(g_counts, counts) and np.array_equal(g_offsets, offsets)
+    rows = int(offsets[E])
+    assert per_expert_sets(g_src[:rows], offsets) == per_expert_sets(src_of[:rows], offsets)
+    valid = row_of >= 0
+    assert np.array_equal(g_row < 0, ~valid)
+    assert np.array_equal(g_src[g_row[valid]], np.nonzero(valid)[0])
+    # this implementation is stable: rows follow the assignment order
+    assert np.array_equal(g_row, row_of) and np.array_equal(g_src[:rows], src_of[:rows])
+    xd = np_of(d["x_disp"])[:rows]
+    assert np.array_equal(xd, oracle.gather(x_np, dt, k, src_of, rows))
+
+
+DISPATCH_CASES = [(4096, 6, 64, 2048, "bf16"), (8192, 8, 256, 64, "bf16"),
+                  (16384, 2, 8, 64, "f32"), (128, 8, 256, 7168, "bf16"),
+                  (37, 3, 5, 24, "f16"), (1, 1, 1, 8, "f32"), (500, 4, 1024, 8, "bf16"),
+                  (3000, 1, 4, 40, "bf16")]
+
+
+@pytest.mark.parametrize("T,k,E,H,dt", DISPATCH_CASES)
+def test_dispatch_parity(dev, T, k, E, H, dt):
+    g = torch.Generator().manual_seed(T + k * 7 + E)
+    if E > 1 and T == 3000:
+        idx = torch.zeros((T, k), dtype=torch.int32)          # every token to expert 0
+    else:
+        idx = torch.stack([torch.randperm(E, generator=g)[:k] if k <= E else
+                           torch.randint(0, E, (k,), generator=g) for _ in range(T)]).int()
+    x = (torch.randn((T, H), generator=g)).to(W.TORCH_DTYPES[dt])
+    d = moe.moe_dispatch(idx.to(dev), x.to(dev), E)
+    torch.cuda.synchronize()
+    _check_dispatch(d, idx.numpy().view(np.uint32), np_of(x), E, k, dt)
+    assert moe.moe_device_status() == 0
+
+
+def test_dispatch_bad_index_flags_and_nans(dev):
+    T, k, E, H = 40, 2, 4, 16
+    g = torch.Generator().manual_seed(5)
+    idx = torch.randint(0, E, (T, k), generator=g).int()
+    idx[3, 1] = 7
+    idx[10, 0] = 2 ** 31 - 1
+    x = torch.randn((T, H), generator=g).to(torch.bfloat16)
+    assert moe.moe_device_status(clear=True) == 0
+    d = moe.moe_dispatch(idx.to(dev), x.to(dev), E)
+    assert moe.moe_device_status(clear=True) == 9        # MOE_ERR_BAD_INDEX
+    assert moe.moe_device_status(clear=True) == 0        # cleared
+    _check_dispatch(d, idx.numpy().view(np.uint32), np_of(x), E, k, "bf16")
+    w = torch.full((T, k), 0.5, device=dev)
+    out = torch.randn((T * k, H), device=dev).to(torch.bfloat16)
+    y = moe.moe_combine(out, w, d["row_of"])
+    torch.cuda.synchronize()
+    nan_rows = torch.isnan(y.float()).all(dim=1).cpu().numpy()
+    assert nan_rows[3] and nan_rows[10] and nan_rows.sum() == 2
+
+
+# ---------------------------------------------------------------- experts
+
+@pytest.mark.parametrize("cfg", SMALL, ids=lambda c: c.name)
+def test_experts_parity(dev, cfg):
+    cpu, g = inputs_on(cfg, dev)
+    o = oracle_inputs(cpu)
+    idx, _, _ = oracle.route(o["logits"], cfg.logits_dtype, cfg.top_k, cfg.renormalize)
+    _, offsets, _, src_of, _ = oracle.dispatch(idx, cfg.E)
+    rows = int(offsets[cfg.E])
+    x_disp = oracle.gather(o["x"], cfg.dtype, cfg.top_k, src_of, rows)
+    ref = oracle.experts_dispatched(x_disp, cfg.dtype, offsets, o["gate"], o["up"], o["down"])
+    xd = W.from_numpy(x_disp, cfg.dtype, dev)
+    out = moe.moe_experts_forward(xd, torch.from_numpy(offsets).to(dev), g["gate"],
+                                  g["up"], g["down"])
+    torch.cuda.synchronize()
+    assert moe.moe_device_status() == 0
+    assert_close(to_f64(out), ref, cfg.dtype, f"{cfg.name} expert outputs")
+
+
+def test_experts_rows_beyond_offsets_untouched(dev):
+    """offsets[E] < rows: rows past the last segment are not written."""
+    cfg = SMALL[0]
+    cpu, g = inputs_on(cfg, dev)
+    o = oracle_inputs(cpu)
+    idx, _, _ = oracle.route(o["logits"], cfg.logits_dtype, cfg.top_k, cfg.renormalize)
+    _, offsets, _, src_of, _ = oracle.dispatch(idx, cfg.E)
+    rows = int(offsets[cfg.E])
+    x_disp = oracle.gather(o["x"], cfg.dtype, cfg.top_k, src_of, rows)
+    pad = np.zeros((rows + 77, cfg.H), np.uint16)
+    pad[:rows] = x_disp
+    xd = W.from_numpy(pad, cfg.dtype, dev)
+    out = torch.full((rows + 77, cfg.H), 3.0, dtype=torch.bfloat16, device=dev)
+    moe.moe_experts_forward(xd, torch.from_numpy(offsets).to(dev), g["gate"], g["up"],
+                            g["down"], out_disp=out)
+    torch.cuda.synchronize()
+    assert torch.all(out[rows:].float() == 3.0)
+    ref = oracle.experts_dispatched(x_disp, cfg.dtype, offsets, o["gate"], o["up"], o["down"])
+    assert_close(to_f64(out[:rows]), ref, cfg.dtype, "prefix rows")
+
+
+def test_experts_exact_small_integers(dev):
+    """Integer-valued BF16 inputs with gate = 0 rows make SiLU exact (h = 0
+    where g = 0); up/down chosen so every product and FP32 sum is exact."""
+    E, I, H, T = 3, 128, 64, 200
+    g = torch.Generator().manual_seed(3)
+    x = torch.randint(-3, 4, (T, H), generator=g).to(torch.bfloat16)
+    gate = torch.zeros((E, I, H), dtype=torch.bfloat16)
+    up = torch.randint(-2, 3, (E, I, H), generator=g).to(torch.bfloat16)
+    down = torch.randint(-2, 3, (E, H, I), generator=g).to(torch.bfloat16)
+    offsets = torch.tensor([0, 50, 50, T], dtype=torch.int32)
+    out = moe.moe_experts_forward(x.to(dev), offsets.to(dev), gate.to(dev), up.to(dev),
+                                  down.to(dev))
+    torch.cuda.synchronize()
+    assert torch.all(out.cpu().float() == 0.0)
+
+
+# ---------------------------------------------------------------- combine
+
+COMBINE_CASES = [(300, 2, 320, "bf16", "f32"), (4096, 6, 2048, "bf16", "bf16"),
+                 (64, 2, 128, "f32", "f32"), (129, 8, 7168, "bf16", "f32"),
+                 (77, 3, 264, "f16", "f16"), (5, 1, 16384, "bf16", "f32")]
+
+
+def _routing_for(T, k, E, seed):
+    g = torch.Generator().manual_seed(seed)
+    logits = torch.randn((T, E), generator=g)
+    logits[1 % T, 0] = float("nan")
+    idx, w, _ = oracle.route(logits.numpy(), "f32", k, True)
+    _, _, row_of, _, _ = oracle.dispatch(idx, E)
+    return w, row_of
+
+
+@pytest.mark.parametrize("T,k,H,dt,wdt", COMBINE_CASES)
+def test_combine_parity(dev, T, k, H, dt, wdt):
+    E = max(k, 16)
+    w, row_of = _routing_for(T, k, E, seed=T + H)
+    wt = torch.from_numpy(w)
+    if wdt != "f32":
+        wt = wt.to(W.TORCH_DTYPES[wdt])
+    g = torch.Generator().manual_seed(H)
+    out = torch.randn((T * k, H), generator=g).to(W.TORCH_DTYPES[dt])
+    ref = oracle.combine(np_of(out), dt, np_of(wt), wdt, row_of, k)
+    y = moe.moe_combine(out.to(dev), wt.to(dev), torch.from_numpy(row_of).to(dev))
+    torch.cuda.synchronize()
+    assert_close(to_f64(y), ref, dt, "combine")
+
+
+@pytest.mark.parametrize("T,k,H,dt,wdt", COMBINE_CASES)
+@pytest.mark.parametrize("gdt", ["same", "f32"])
+def test_combine_add_rmsnorm_parity(dev, T, k, H, dt, wdt, gdt):
+    E = max(k, 16)
+    w, row_of = _routing_for(T, k, E, seed=T * 3 + H)
+    wt = torch.from_numpy(w)
+    if wdt != "f32":
+        wt = wt.to(W.TORCH_DTYPES[wdt])
+    g = torch.Generator().manual_seed(H + 1)
+    tdt = W.TORCH_DTYPES[dt]
+    out = torch.randn((T * k, H), generator=g).to(tdt)
+    res = torch.randn((T, H), generator=g).to(tdt)
+    gdt_name = dt if gdt == "same" else "f32"
+    gamma = (1 + math.sqrt(0.1) * torch.randn(H, generator=g)).to(W.TORCH_DTYPES[gdt_name])
+    eps = 1e-6
+    comb = oracle.combine(np_of(out), dt, np_of(wt), wdt, row_of, k)
+    y_ref, x_ref, rstd_ref = oracle.add_rmsnorm(comb, np_of(res), dt, np_of(gamma),
+                                                gdt_name, eps)
+    y, x_out, rstd = moe.moe_combine_add_rmsnorm(
+        out.to(dev), wt.to(dev), torch.from_numpy(row_of).to(dev), res.to(dev),
+        gamma.to(dev), eps)
+    torch.cuda.synchronize()
+    assert_close(to_f64(x_out), oracle.to_f64(x_ref, dt), dt, "x_out")
+    assert_close(to_f64(y), oracle.to_f64(y_ref, dt), dt, "y")
+    assert_close(rstd.cpu().numpy().astype(np.float64), rstd_ref.astype(np.float64),
+                 "f32", "rstd")
+
+
+def test_combine_one_hot_is_exact_gather(dev):
+    T, k, H = 100, 4, 256
+    g = torch.Generator().manual_seed(9)
+    out = torch.randn((T * k, H), generator=g).to(torch.bfloat16)
+    row_of = torch.randperm(T * k, generator=g).int()
+    pick = torch.randint(0, k, (T,), generator=g)
+    w = torch.zeros((T, k))
+    w[torch.arange(T), pick] = 1.0
+    y = moe.moe_combine(out.to(dev), w.to(dev), row_of.to(dev)).cpu()
+    want = out[row_of.view(T, k)[torch.arange(T), pick].long()]
+    assert torch.equal(y, want)
+
+
+# ---------------------------------------------------------------- forward
+
+@pytest.mark.parametrize("cfg", SMALL, ids=lambda c: c.name)
+def test_forward_parity(dev, cfg):
+    cpu, g = inputs_on(cfg, dev)
+    o = oracle_inputs(cpu)
+    ref = oracle.forward(o["x"], cfg.dtype, o["logits"], cfg.logits_dtype, o["gate"],
+                         o["up"], o["down"], cfg.top_k, cfg.renormalize)
+    y = moe.moe_forward(g["x"], g["logits"], g["gate"], g["up"], g["down"], cfg.top_k,
+                        cfg.renormalize)
+    torch.cuda.synchronize()
+    assert moe.moe_device_status() == 0
+    assert_close(to_f64(y), ref["y"], cfg.dtype, f"{cfg.name} y")
+    # the staged calls give the same result bit for bit
+    idx, w = moe.moe_route(g["logits"], cfg.top_k, cfg.renormalize)
+    d = moe.moe_dispatch(idx, g["x"], cfg.E)
+    out = moe.moe_experts_forward(d["x_disp"], d["offsets"], g["gate"], g["up"], g["down"])
+    y2 = moe.moe_combine(out, w, d["row_of"])
+    torch.cuda.synchronize()
+    assert torch.equal(torch.isnan(y), torch.isnan(y2))
+    assert torch.equal(torch.nan_to_num(y), torch.nan_to_num(y2))
+
+
+def test_forward_tiny_fp32_special_rows(dev):
+    cfg = W.CONFIGS["tiny_fp32"]
+    cpu, g = inputs_on(cfg, dev)
+    y = moe.moe_forward(g["x"], g["logits"], g["gate"], g["up"], g["down"], 2, True).cpu()
+    nan_rows = torch.isnan(y).all(dim=1)
+    assert nan_rows[4] and nan_rows[5] and int(nan_rows.sum()) == 2
+
+
+def test_forward_deterministic_and_stream(dev):
+    cfg = SMALL[1]
+    _, g = inputs_on(cfg, dev)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        y1 = moe.moe_forward(g["x"], g["logits"], g["gate"], g["up"], g["down"],
+                             cfg.top_k, cfg.renormalize, stream=s)
+        y2 = moe.moe_forward(g["x"], g["logits"], g["gate"], g["up"], g["down"],
+                             cfg.top_k, cfg.renormalize, stream=s)
+    s.synchronize()
+    assert torch.equal(y1, y2)
+
+
+def test_forward_empty_batch(dev):
+    cfg = SMALL[0]
+    _, g = inputs_on(cfg, dev)
+    y = moe.moe_forward(g["x"][:0], g["logits"][:0], g["gate"], g["up"], g["down"],
+                        cfg.top_k, cfg.renormalize)
+    assert y.shape == (0, cfg.H)
