@@ -1,0 +1,473 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 local MoE FFN forward.
+
+One step = one pass of the whole path (route -> dispatch -> SwiGLU experts
+-> combine) over one batch of the fine-grained prefill workload (T=4096
+tokens, H=2048, I=1408, E=64 experts, top_k=6, BF16) with inputs resident in
+HBM. Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME]
+
+* ``value``: tokens/s of the whole job (all ranks), device time from CUDA
+  events on the launching stream, L2 flushed (256 MiB write) between steps.
+* ``e2e``: the same metric through the one-call C ABI (``moe_forward``) with
+  pinned HOST buffers: each step copies x and logits in and y out.
+* ``roofline``: the expert grouped GEMM (the dominant kernels), algorithmic
+  FLOPs (6*H*I per assignment) over its measured duration, against the
+  measured dense BF16 peak; ``kernels`` gives every stage.
+* ``cpu_baseline`` (rank 0, N=1): the CPU oracle on a bounded token sample.
+* ``--impl reference``: the CPU oracle as the reference arm (rank 0 only).
+
+Multi-GPU (torchrun): every rank runs an independent replica on its own GPU
+(no collective on the data path); the step time is the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "MoE fwd tokens/s; expert GEMM TFLOP/s and combine GB/s as % of GB300 peak"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d["bf16_tflops_sustained"]),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def load_traffic(workload, kernel):
+    """Per-launch DRAM bytes from the committed ncu summary, if it still
+    matches the current kernel build (see profiles/)."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            d = json.load(f)
+        return d.get(workload, {}).get(kernel)
+    except (OSError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------- distributed
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        return rank, world, local, dist
+    return 0, 1, 0, None
+
+
+def barrier(dist, device):
+    if dist is not None:
+        if device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def reduce_max(dist, value, device):
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(step_s_max: float, tokens_per_rank: int, world: int) -> float:
+    """Whole-job tokens/s: all ranks' tokens over the slowest rank's step."""
+    return tokens_per_rank * world / step_s_max
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.out.close()
+
+    def summary(self):
+        if self.proc is None or self.path is None:
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r)
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local, dist):
+    import mixture_experts_ffn_topk_gb300 as moe
+    from mixture_experts_ffn_topk_gb300 import build, workloads as W
+
+    build.build()
+    moe.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    if args.workload == W.COMBINE_NORM.name:
+        return run_combine_norm(args, rank, world, local, dist, dev, peaks, flush)
+
+    cfg = W.CONFIGS[args.workload]
+    d = W.moe_inputs(cfg, device=dev, seed=cfg.seed + 1000 * rank)
+    T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.top_k
+    A = T * k
+    x, logits = d["x"], d["logits"]
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, k), dtype=logits.dtype, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    row_of = torch.empty(A, dtype=torch.int32, device=dev)
+    src_of = torch.empty(A, dtype=torch.int32, device=dev)
+    x_disp = torch.empty((A, H), dtype=x.dtype, device=dev)
+    out_disp = torch.empty((A, H), dtype=torch.float32, device=dev)   # unrounded
+    y = torch.empty((T, H), dtype=x.dtype, device=dev)
+    ws_d = torch.empty(max(1, moe.moe_dispatch_workspace_size(T, k, E)), dtype=torch.uint8,
+                       device=dev)
+    ws_e = torch.empty(moe.moe_experts_workspace_size(A, E, H, I, x.dtype),
+                       dtype=torch.uint8, device=dev)
+    ws_f = torch.empty(moe.moe_forward_workspace_size(T, H, I, E, k, x.dtype, logits.dtype),
+                       dtype=torch.uint8, device=dev)
+
+    def step(ev=None):
+        if ev: ev[0].record(stream)
+        moe.moe_route(logits, k, cfg.renormalize, expert_indices=idx, weights=w)
+        if ev: ev[1].record(stream)
+        moe.moe_dispatch(idx, x, E, counts=counts, offsets=offsets, row_of=row_of,
+                         src_of=src_of, x_disp=x_disp, workspace=ws_d)
+        if ev: ev[2].record(stream)
+        moe.moe_experts_forward(x_disp, offsets, d["gate"], d["up"], d["down"],
+                                out_disp=out_disp, workspace=ws_e)
+        if ev: ev[3].record(stream)
+        moe.moe_combine(out_disp, w, row_of, y=y)
+        if ev: ev[4].record(stream)
+
+    launches_per_step = 1 + 4 + 2 + 1
+    for _ in range(args.warmup):
+        step()
+        flush.fill_(1)
+    torch.cuda.synchronize(dev)
+    if moe.moe_device_status() != 0:
+        raise RuntimeError("device status error during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    barrier(dist, dev)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clk:
+        for i in range(args.steps):
+            step(evs[i])
+            flush.fill_(1)   # untimed: between the events of consecutive steps
+        torch.cuda.synchronize(dev)
+    barrier(dist, dev)
+    stage_ms = {name: [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)]
+                for j, name in enumerate(["route", "dispatch", "experts", "combine"])}
+    step_ms = [evs[i][0].elapsed_time(evs[i][4]) for i in range(args.steps)]
+    ms = statistics.mean(step_ms)
+    ms_max = reduce_max(dist, ms, dev)
+    value = aggregate(ms_max / 1e3, T, world)
+
+    # one-call API on device buffers (cross-check) and end to end from host
+    def fwd():
+        moe.moe_forward(x, logits, d["gate"], d["up"], d["down"], k, cfg.renormalize,
+                        y=y, workspace=ws_f)
+    api_ms = timed_loop(fwd, args, stream, flush)
+    x_h = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    x_h.copy_(x)
+    l_h = torch.empty(logits.shape, dtype=logits.dtype, pin_memory=True)
+    l_h.copy_(logits)
+    y_h = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    x_in = torch.empty_like(x)
+    l_in = torch.empty_like(logits)
+
+    def e2e():
+        x_in.copy_(x_h, non_blocking=True)
+        l_in.copy_(l_h, non_blocking=True)
+        moe.moe_forward(x_in, l_in, d["gate"], d["up"], d["down"], k, cfg.renormalize,
+                        y=y, workspace=ws_f)
+        y_h.copy_(y, non_blocking=True)
+    e2e_ms = timed_loop(e2e, args, stream, flush)
+    e2e_ms_max = reduce_max(dist, e2e_ms, dev)
+    if moe.moe_device_status() != 0:
+        raise RuntimeError("device status error in the timed region")
+
+    flops = 6.0 * H * I * A
+    exp_ms = statistics.mean(stage_ms["experts"])
+    achieved = flops / (exp_ms / 1e3) / 1e12
+    comb_ms = statistics.mean(stage_ms["combine"])
+    eb = x.element_size()
+    comb_bytes = A * H * 4 + A * (w.element_size() + 4) + T * H * eb
+    disp_bytes = A * 12 + E * 8 + T * H * eb + A * H * eb + A * H * eb
+    route_bytes = T * E * logits.element_size() + A * (4 + w.element_size())
+    hbm = peaks["hbm_gbs"]
+    kernels = {
+        "route": {"ms": statistics.mean(stage_ms["route"]), "bytes": route_bytes},
+        "dispatch": {"ms": statistics.mean(stage_ms["dispatch"]), "bytes": disp_bytes},
+        "experts": {"ms": exp_ms, "flops": flops, "tflops": achieved,
+                    "frac_bf16_peak": achieved / peaks["bf16_tflops"]},
+        "combine": {"ms": comb_ms, "bytes": comb_bytes},
+    }
+    for kname in ("route", "dispatch", "combine"):
+        kk = kernels[kname]
+        kk["gbs"] = kk["bytes"] / (kk["ms"] / 1e3) / 1e9
+        kk["frac_hbm"] = kk["gbs"] / hbm
+    traffic = load_traffic(args.workload, "experts")
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if cfg.dtype == "bf16" else cfg.dtype,
+        "data": "synthetic (seeded; random-init expert weights)",
+        "config": {"workload": cfg.name, "T": T, "H": H, "I": I, "E": E, "top_k": k,
+                   "renormalize": cfg.renormalize, "logits_dtype": cfg.logits_dtype,
+                   "global_batch": T * world, "parallelism": f"replicas x{world}",
+                   "l2": "flushed between steps (256 MiB write)"},
+        "e2e": {"value": aggregate(e2e_ms_max / 1e3, T, world), "unit": UNIT,
+                "h2d_bytes_per_step": x.numel() * eb + logits.numel() * logits.element_size(),
+                "d2h_bytes_per_step": y.numel() * eb},
+        "forward_api_ms": api_ms,
+        "roofline": {"bound": "tensor", "kernel": "grouped SwiGLU GEMM (GEMM1 + GEMM2)",
+                     "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": achieved / peaks["bf16_tflops"],
+                     "peak_source": peaks["source"] + " burst bf16", "traffic": traffic},
+        "kernels": kernels,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, d, args.cpu_seconds)
+    return line
+
+
+def timed_loop(fn, args, stream, flush):
+    for _ in range(max(1, args.warmup)):
+        fn()
+        flush.fill_(1)
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for a, b in pairs:
+        a.record(stream)
+        fn()
+        b.record(stream)
+        flush.fill_(1)
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in pairs)
+
+
+def run_combine_norm(args, rank, world, local, dist, dev, peaks, flush):
+    import oracle
+    import mixture_experts_ffn_topk_gb300 as moe
+    from mixture_experts_ffn_topk_gb300 import workloads as W
+    cfg = W.COMBINE_NORM
+    d = W.combine_norm_inputs(cfg, device=dev, seed=cfg.seed + 1000 * rank)
+    T, H, k = cfg.T, cfg.H, cfg.top_k
+    idx, w = moe.moe_route(d["logits"], k, True)
+    disp = moe.moe_dispatch(idx, torch.zeros((T, 8), dtype=torch.bfloat16, device=dev), cfg.E)
+    row_of = disp["row_of"]
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    xo = torch.empty_like(y)
+    rstd = torch.empty(T, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def fn():
+        moe.moe_combine_add_rmsnorm(d["out_disp"], w, row_of, d["residual"], d["gamma"],
+                                    cfg.eps, y=y, x_out=xo, rstd=rstd)
+    with ClockSampler(dev.index) as clk:
+        ms = timed_loop(fn, args, stream, flush)
+    ms_max = reduce_max(dist, ms, dev)
+    nbytes = (T * k * H * 2 + T * k * (4 + 4) + T * H * 2 + H * 2 + 2 * T * H * 2 + T * 4)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"metric": METRIC, "value": aggregate(ms_max / 1e3, T, world), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded)",
+            "config": {"workload": cfg.name, "T": T, "H": H, "E": cfg.E, "top_k": k,
+                       "l2": "flushed between steps (256 MiB write)"},
+            "roofline": {"bound": "hbm", "kernel": "combine + Add + RMSNorm", "achieved": gbs,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                         "peak_source": peaks["source"],
+                         "traffic": load_traffic(cfg.name, "combine_add_rmsnorm")},
+            "gpu_launches": args.steps, "clocks": clk.summary()}
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_token_rate(cfg, host, seconds, max_threads=None):
+    """Oracle throughput (tokens/s) on a bounded token sample, split over
+    host threads (the C oracle releases the GIL through ctypes)."""
+    import concurrent.futures as cf
+    import numpy as np
+    import oracle
+    lib = oracle.load_library()
+    threads = max_threads or os.cpu_count() or 1
+    T = cfg.T
+
+    def run(tokens):
+        oracle.forward_tokens(tokens, host["x"], cfg.dtype, host["logits"], cfg.logits_dtype,
+                              host["gate"], host["up"], host["down"], cfg.top_k,
+                              cfg.renormalize, lib)
+    t0 = time.perf_counter()
+    run(np.array([0]))
+    one = max(time.perf_counter() - t0, 1e-4)
+    n = int(max(threads, min(T, seconds * threads / one)))
+    n = max(threads, n // threads * threads)
+    rng = np.random.default_rng(cfg.seed)
+    tokens = rng.choice(T, size=min(n, T), replace=False)
+    chunks = np.array_split(tokens, threads)
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(run, chunks))
+    wall = time.perf_counter() - t0
+    return tokens.size / wall, tokens.size, threads, wall
+
+
+def host_inputs(cfg, d):
+    from mixture_experts_ffn_topk_gb300 import workloads as W
+    return {k: W.to_numpy(v) for k, v in d.items()}
+
+
+def cpu_baseline(cfg, d, seconds):
+    host = host_inputs(cfg, d)
+    rate, n, threads, wall = oracle_token_rate(cfg, host, seconds)
+    return {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{n} of {cfg.T} tokens of {cfg.name}, full forward per token "
+                      f"(route, k experts, combine) in {wall:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm: each step is a bounded token
+    sample of the same workload."""
+    if rank != 0:
+        return None
+    import numpy as np
+    from mixture_experts_ffn_topk_gb300 import workloads as W
+    cfg = W.CONFIGS[args.workload] if args.workload in W.CONFIGS else W.CONFIGS["fine_prefill_bf16"]
+    d = W.moe_inputs(cfg, device="cpu")
+    host = host_inputs(cfg, d)
+    per_step = max(1.0, args.cpu_seconds * 4 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_token_rate(cfg, host, per_step / 4)
+    rates, sizes, walls = [], [], []
+    threads = os.cpu_count() or 1
+    for _ in range(args.steps):
+        r, n, threads, wall = oracle_token_rate(cfg, host, per_step)
+        rates.append(r)
+        sizes.append(n)
+        walls.append(wall)
+    value = sum(sizes) / sum(walls)
+    ms = 1e3 * cfg.T / value
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": cfg.dtype, "data": "synthetic (seeded; random-init expert weights)",
+            "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E,
+                       "top_k": cfg.top_k, "renormalize": cfg.renormalize},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": f"{sum(sizes)} tokens over {args.steps} steps"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="fine_prefill_bf16")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU seconds of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local, dist = dist_setup(args.gpus)
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ours(args, rank, world, local, dist)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

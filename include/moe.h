@@ -138,15 +138,17 @@ int moe_dispatch(const uint32_t *expert_indices, int64_t T, int top_k,
  *   offsets   [E + 1] int32 (device), read only: rows of expert e are
  *             [offsets[e], offsets[e+1]); offsets[E] <= rows.
  *   gate, up  [E, I, H] in dtype;  down [E, H, I] in dtype.
- *   out_disp  [rows, H] in dtype, written for rows < offsets[E].
+ *   out_disp  [rows, H] in out_dtype (dtype or MOE_F32), written for rows
+ *             < offsets[E]; rows past offsets[E] are left untouched.
  *   workspace moe_experts_workspace_size(...) bytes (holds h [rows, I]).
  *
  * For each row r of expert e: g = Wg[e] x_r, u = Wu[e] x_r,
  * h = SiLU(g) * u with SiLU(z) = z / (1 + exp(-z)), out_r = Wd[e] h.
  * BF16/F16: tcgen05 tensor cores, FP32 accumulation, h rounded to dtype
- * between the two GEMMs. F32: CUDA cores, FP32 throughout.
- * Constraints: BF16/F16 need H % 8 == 0 and I % 8 == 0; F32 needs
- * H % 4 == 0 and I % 4 == 0; 1 <= E <= 1024.
+ * between the two GEMMs; out_dtype MOE_F32 keeps the expert outputs
+ * unrounded for a following combine. F32: CUDA cores, FP32 throughout.
+ * Constraints: H*elem and I*elem multiples of 16 bytes (BF16/F16: H % 8 and
+ * I % 8 == 0; F32: H % 4 and I % 4 == 0); 1 <= E <= 1024.
  * Errors: MOE_ERR_NULL, MOE_ERR_SHAPE, MOE_ERR_DTYPE, MOE_ERR_ALIGN,
  * MOE_ERR_WORKSPACE, MOE_ERR_CUDA.
  */
@@ -155,27 +157,27 @@ size_t moe_experts_workspace_size(int64_t rows, int64_t E, int64_t H,
 int moe_experts_forward(const void *x_disp, const int32_t *offsets,
                         int64_t rows, const void *gate, const void *up,
                         const void *down, int64_t E, int64_t H, int64_t I,
-                        int dtype, void *out_disp, void *workspace,
-                        size_t workspace_bytes, void *stream);
+                        int dtype, void *out_disp, int out_dtype,
+                        void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * moe_combine -- restore token order and sum the weighted expert outputs.
  * ruDNN user guide, sections 3 and 6 (DispatchedTokens::combine).
  *
- *   out_disp  [T * top_k, H] in dtype, read only.
- *   weights   [T, top_k] in weights_dtype (F32 or dtype), read only.
+ *   out_disp  [T * top_k, H] in out_dtype (dtype or MOE_F32), read only.
+ *   weights   [T, top_k] in weights_dtype (F32, BF16 or F16), read only.
  *   row_of    [T * top_k] int32, read only (from moe_dispatch).
  *   y         [T, H] in dtype, written.
  *
  * y[t] = sum over j < top_k, in slot order, of weights[t,j] *
  * out_disp[row_of[t*top_k + j]], accumulated in FP32, rounded once to dtype.
- * A slot with row_of < 0 makes the token's row NaN.
+ * A slot with row_of < 0 makes the token's row NaN. Needs H % 8 == 0.
  * Errors: MOE_ERR_NULL, MOE_ERR_SHAPE, MOE_ERR_DTYPE, MOE_ERR_ALIGN,
  * MOE_ERR_CUDA.
  */
-int moe_combine(const void *out_disp, int dtype, const void *weights,
+int moe_combine(const void *out_disp, int out_dtype, const void *weights,
                 int weights_dtype, const int32_t *row_of, int64_t T, int top_k,
-                int64_t H, void *y, void *stream);
+                int64_t H, void *y, int dtype, void *stream);
 
 /*
  * moe_combine_add_rmsnorm -- combine, residual Add and RMSNorm in one pass.
@@ -184,23 +186,24 @@ int moe_combine(const void *out_disp, int dtype, const void *weights,
  *   x = combine + residual,  y = x / sqrt(mean(x^2) + eps) * gamma.
  * ruDNN user guide section 7: eps finite and > 0, FP32 statistics.
  *
- *   out_disp, weights, row_of, T, top_k, H as for moe_combine.
+ *   out_disp, out_dtype, weights, row_of, T, top_k, H as for moe_combine.
  *   residual  [T, H] in dtype, read only.
- *   gamma     [H] in gamma_dtype (F32 or dtype), read only.
+ *   gamma     [H] in gamma_dtype (F32, BF16 or F16), read only.
  *   y         [T, H] in dtype, written (normalised output, yOut).
  *   x_out     [T, H] in dtype, written (the pre-norm sum, xOut).
  *   rstd      [T] float, written: 1 / sqrt(mean(x_out^2) + eps) (rstdOut).
  *
  * The statistics are taken on x_out after it is rounded to dtype, so y
- * equals RMSNorm applied to x_out. Errors: MOE_ERR_NULL, MOE_ERR_SHAPE,
- * MOE_ERR_DTYPE, MOE_ERR_VALUE, MOE_ERR_ALIGN, MOE_ERR_CUDA.
+ * equals RMSNorm applied to x_out. Needs H % 8 == 0 and H <= 16384 (a row
+ * is normalised in one pass from registers). Errors: MOE_ERR_NULL,
+ * MOE_ERR_SHAPE, MOE_ERR_DTYPE, MOE_ERR_VALUE, MOE_ERR_ALIGN, MOE_ERR_CUDA.
  */
-int moe_combine_add_rmsnorm(const void *out_disp, int dtype,
+int moe_combine_add_rmsnorm(const void *out_disp, int out_dtype,
                             const void *weights, int weights_dtype,
                             const int32_t *row_of, const void *residual,
-                            const void *gamma, int gamma_dtype, float eps,
-                            int64_t T, int top_k, int64_t H, void *y,
-                            void *x_out, float *rstd, void *stream);
+                            int dtype, const void *gamma, int gamma_dtype,
+                            float eps, int64_t T, int top_k, int64_t H,
+                            void *y, void *x_out, float *rstd, void *stream);
 
 /*
  * moe_forward -- the whole local forward in one call: route, dispatch,
@@ -213,7 +216,8 @@ int moe_combine_add_rmsnorm(const void *out_disp, int dtype,
  *   workspace moe_forward_workspace_size(...) bytes; it holds the routing
  *           plan, the dispatch map and the dispatched activations.
  * Same rules and errors as the staged calls; the result equals
- * moe_route -> moe_dispatch -> moe_experts_forward -> moe_combine.
+ * moe_route -> moe_dispatch -> moe_experts_forward (out_dtype MOE_F32) ->
+ * moe_combine: expert outputs reach the combine unrounded. Needs H % 8 == 0.
  */
 size_t moe_forward_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E,
                                   int top_k, int dtype, int logits_dtype);

@@ -69,10 +69,10 @@ def _bind(lib):
                           _P, _P, _SZ, _P], _INT),
         "moe_experts_workspace_size": ([_I64, _I64, _I64, _I64, _INT], _SZ),
         "moe_experts_forward": ([_P, _P, _I64, _P, _P, _P, _I64, _I64, _I64,
-                                 _INT, _P, _P, _SZ, _P], _INT),
-        "moe_combine": ([_P, _INT, _P, _INT, _P, _I64, _INT, _I64, _P, _P], _INT),
-        "moe_combine_add_rmsnorm": ([_P, _INT, _P, _INT, _P, _P, _P, _INT, _F,
-                                     _I64, _INT, _I64, _P, _P, _P, _P], _INT),
+                                 _INT, _P, _INT, _P, _SZ, _P], _INT),
+        "moe_combine": ([_P, _INT, _P, _INT, _P, _I64, _INT, _I64, _P, _INT, _P], _INT),
+        "moe_combine_add_rmsnorm": ([_P, _INT, _P, _INT, _P, _P, _INT, _P, _INT,
+                                     _F, _I64, _INT, _I64, _P, _P, _P, _P], _INT),
         "moe_forward_workspace_size": ([_I64, _I64, _I64, _I64, _INT, _INT,
                                         _INT], _SZ),
         "moe_forward": ([_P, _INT, _P, _INT, _P, _P, _P, _I64, _I64, _I64, _I64,
@@ -211,30 +211,44 @@ def moe_experts_workspace_size(rows: int, E: int, H: int, I: int,
 def moe_experts_forward(x_disp: torch.Tensor, offsets: torch.Tensor,
                         gate: torch.Tensor, up: torch.Tensor,
                         down: torch.Tensor, out_disp=None, workspace=None,
+                        out_dtype: torch.dtype | None = None,
                         stream=None) -> torch.Tensor:
-    """Bias-free SwiGLU experts on dispatched rows; returns ``out_disp``."""
+    """Bias-free SwiGLU experts on dispatched rows; returns ``out_disp`` in
+    ``out_dtype`` (default: the activation dtype; ``torch.float32`` keeps the
+    expert outputs unrounded)."""
     rows, H = x_disp.shape
     E, I, _ = gate.shape
     dev = x_disp.device
-    out_disp = out_disp if out_disp is not None else torch.empty((rows, H), dtype=x_disp.dtype, device=dev)
+    if out_disp is not None:
+        out_dtype = out_disp.dtype
+    out_dtype = out_dtype or x_disp.dtype
+    if out_disp is None:
+        out_disp = torch.empty((rows, H), dtype=out_dtype, device=dev)
     ws = _workspace(moe_experts_workspace_size(rows, E, H, I, x_disp.dtype), dev, workspace)
     rc = load_library().moe_experts_forward(
         _ptr(x_disp), _ptr(offsets), rows, _ptr(gate), _ptr(up), _ptr(down), E,
-        H, I, _code(x_disp.dtype), _ptr(out_disp), _ptr(ws), _nbytes(ws),
-        _stream(stream))
+        H, I, _code(x_disp.dtype), _ptr(out_disp), _code(out_dtype), _ptr(ws),
+        _nbytes(ws), _stream(stream))
     _check(rc, "moe_experts_forward")
     return out_disp
 
 
 def moe_combine(out_disp: torch.Tensor, weights: torch.Tensor,
-                row_of: torch.Tensor, y=None, stream=None) -> torch.Tensor:
-    """Weighted combine back to token order; returns ``y [T, H]``."""
+                row_of: torch.Tensor, y=None, dtype: torch.dtype | None = None,
+                stream=None) -> torch.Tensor:
+    """Weighted combine back to token order; returns ``y [T, H]`` in
+    ``dtype`` (default: ``y.dtype`` if given, else ``out_disp.dtype``)."""
     T, k = weights.shape
     H = out_disp.shape[1]
-    y = y if y is not None else torch.empty((T, H), dtype=out_disp.dtype, device=out_disp.device)
+    if y is not None:
+        dtype = y.dtype
+    dtype = dtype or out_disp.dtype
+    if y is None:
+        y = torch.empty((T, H), dtype=dtype, device=out_disp.device)
     rc = load_library().moe_combine(
         _ptr(out_disp), _code(out_disp.dtype), _ptr(weights),
-        _code(weights.dtype), _ptr(row_of), T, k, H, _ptr(y), _stream(stream))
+        _code(weights.dtype), _ptr(row_of), T, k, H, _ptr(y), _code(dtype),
+        _stream(stream))
     _check(rc, "moe_combine")
     return y
 
@@ -243,16 +257,18 @@ def moe_combine_add_rmsnorm(out_disp: torch.Tensor, weights: torch.Tensor,
                             row_of: torch.Tensor, residual: torch.Tensor,
                             gamma: torch.Tensor, eps: float, y=None,
                             x_out=None, rstd=None, stream=None):
-    """Combine + residual Add + RMSNorm; returns ``(y, x_out, rstd)``."""
+    """Combine + residual Add + RMSNorm; returns ``(y, x_out, rstd)`` with y
+    and x_out in ``residual.dtype``."""
     T, k = weights.shape
     H = out_disp.shape[1]
     dev = out_disp.device
-    y = y if y is not None else torch.empty((T, H), dtype=out_disp.dtype, device=dev)
-    x_out = x_out if x_out is not None else torch.empty((T, H), dtype=out_disp.dtype, device=dev)
+    dt = residual.dtype
+    y = y if y is not None else torch.empty((T, H), dtype=dt, device=dev)
+    x_out = x_out if x_out is not None else torch.empty((T, H), dtype=dt, device=dev)
     rstd = rstd if rstd is not None else torch.empty(T, dtype=torch.float32, device=dev)
     rc = load_library().moe_combine_add_rmsnorm(
         _ptr(out_disp), _code(out_disp.dtype), _ptr(weights),
-        _code(weights.dtype), _ptr(row_of), _ptr(residual), _ptr(gamma),
+        _code(weights.dtype), _ptr(row_of), _ptr(residual), _code(dt), _ptr(gamma),
         _code(gamma.dtype), float(eps), T, k, H, _ptr(y), _ptr(x_out),
         _ptr(rstd), _stream(stream))
     _check(rc, "moe_combine_add_rmsnorm")

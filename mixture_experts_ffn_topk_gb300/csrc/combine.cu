@@ -8,12 +8,15 @@
 // with rstdOut = 1 / sqrt(mean(x^2) + eps) in FP32; ruDNN user guide section 7
 // (FP32 statistics, output in the input dtype).
 //
-// One CTA per token (grid-stride). Each thread owns V 16-byte vectors of the
-// row; for every slot j it issues V independent 16-byte loads of expert output
-// row row_of[t*k+j], so a CTA keeps k*V loads in flight. The sum runs in FP32
-// in slot order. With the norm, x is rounded to the output dtype first and the
-// statistics are taken on the rounded x (so y == RMSNorm(x_out)); x stays in
-// registers between the two passes. HBM-bound.
+// One CTA per token (grid-stride). A row is moved in groups of 8 elements (one
+// 16-byte vector of a 16-bit type, two of FP32). Each thread owns V groups; for
+// every slot j it issues V independent loads of expert-output row
+// row_of[t*k+j], so a CTA keeps k*V loads in flight. The sum runs in FP32 in
+// slot order. Expert outputs may be FP32 (the one-call forward keeps them
+// unrounded) or the activation dtype. With the norm, x is rounded to the
+// activation dtype first and the statistics are taken on the rounded x (so
+// y == RMSNorm(x_out)); x stays in registers between the two passes.
+// HBM-bound.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -21,90 +24,98 @@ namespace moe {
 
 namespace {
 
-template <int DT> struct VecTraits;
-template <> struct VecTraits<DT_F32> { static constexpr int N = 4; };
-template <> struct VecTraits<DT_BF16> { static constexpr int N = 8; };
-template <> struct VecTraits<DT_F16> { static constexpr int N = 8; };
+constexpr int kMaxV = 8;          // groups per thread
+constexpr int kMaxThreads = 256;
 
 template <int DT>
-__device__ __forceinline__ void unpack(const Vec16 &v, float (&f)[VecTraits<DT>::N])
+__device__ __forceinline__ void load8(const void *base, int64_t g, float (&f)[8])
 {
     if constexpr (DT == DT_F32) {
+        const uint4 *p = static_cast<const uint4 *>(base) + 2 * g;
+        Vec16 a, b;
+        a.u = __ldg(p);
+        b.u = __ldg(p + 1);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) f[i] = v.f[i];
-    } else if constexpr (DT == DT_BF16) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 p = bf16x2_to_float2(v.w[i]);
-            f[2 * i] = p.x;
-            f[2 * i + 1] = p.y;
-        }
+        for (int i = 0; i < 4; ++i) { f[i] = a.f[i]; f[4 + i] = b.f[i]; }
     } else {
+        Vec16 a;
+        a.u = __ldg(static_cast<const uint4 *>(base) + g);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const float2 p = f16x2_to_float2(v.w[i]);
+            const float2 p = DT == DT_BF16 ? bf16x2_to_float2(a.w[i]) : f16x2_to_float2(a.w[i]);
             f[2 * i] = p.x;
             f[2 * i + 1] = p.y;
         }
     }
 }
 
+// Round to DT; f is replaced by the rounded values.
 template <int DT>
-__device__ __forceinline__ Vec16 pack(const float (&f)[VecTraits<DT>::N])
+__device__ __forceinline__ void store8(void *base, int64_t g, float (&f)[8])
 {
-    Vec16 v;
     if constexpr (DT == DT_F32) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) v.f[i] = f[i];
-    } else if constexpr (DT == DT_BF16) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) v.w[i] = float2_to_bf16x2(f[2 * i], f[2 * i + 1]);
+        uint4 *p = static_cast<uint4 *>(base) + 2 * g;
+        p[0] = make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                          __float_as_uint(f[3]));
+        p[1] = make_uint4(__float_as_uint(f[4]), __float_as_uint(f[5]), __float_as_uint(f[6]),
+                          __float_as_uint(f[7]));
     } else {
+        Vec16 a;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) v.w[i] = float2_to_f16x2(f[2 * i], f[2 * i + 1]);
+        for (int i = 0; i < 4; ++i) {
+            a.w[i] = DT == DT_BF16 ? float2_to_bf16x2(f[2 * i], f[2 * i + 1])
+                                   : float2_to_f16x2(f[2 * i], f[2 * i + 1]);
+            const float2 p = DT == DT_BF16 ? bf16x2_to_float2(a.w[i]) : f16x2_to_float2(a.w[i]);
+            f[2 * i] = p.x;
+            f[2 * i + 1] = p.y;
+        }
+        static_cast<uint4 *>(base)[g] = a.u;
     }
-    return v;
 }
 
-template <int DT, int V, bool NORM>
-__global__ void __launch_bounds__(256)
-combine_kernel(const uint4 *__restrict__ out_disp, const void *__restrict__ w,
-               int wdt, const int32_t *__restrict__ row_of,
-               const uint4 *__restrict__ residual, const void *__restrict__ gamma,
-               int gdt, float eps, int64_t T, int top_k, int64_t H,
-               uint4 *__restrict__ y, uint4 *__restrict__ x_out,
+__device__ __forceinline__ void load8_rt(const void *base, int dt, int64_t g, float (&f)[8])
+{
+    if (dt == DT_F32) load8<DT_F32>(base, g, f);
+    else if (dt == DT_BF16) load8<DT_BF16>(base, g, f);
+    else load8<DT_F16>(base, g, f);
+}
+
+template <int ODT, int YDT, int V, bool NORM>
+__global__ void __launch_bounds__(kMaxThreads)
+combine_kernel(const void *__restrict__ out_disp, const void *__restrict__ w, int wdt,
+               const int32_t *__restrict__ row_of, const void *__restrict__ residual,
+               const void *__restrict__ gamma, int gdt, float eps, int64_t T, int top_k,
+               int64_t H, void *__restrict__ y, void *__restrict__ x_out,
                float *__restrict__ rstd)
 {
-    constexpr int N = VecTraits<DT>::N;
-    const int64_t nvec = H / N;
-    __shared__ float red[8];
+    const int64_t ng = H / 8;
+    __shared__ float red[kMaxThreads / 32];
     __shared__ float s_rstd;
+    const int64_t elem_o = ODT == DT_F32 ? 4 : 2;
 
     for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
-        // rows handled in passes of V * blockDim vectors (one pass when NORM)
-        for (int64_t base = 0; base < nvec; base += (int64_t)V * blockDim.x) {
-            float acc[V][N];
+        // groups handled in passes of V * blockDim (a single pass with NORM)
+        for (int64_t base = 0; base < ng; base += (int64_t)V * blockDim.x) {
+            float acc[V][8];
 #pragma unroll
             for (int v = 0; v < V; ++v)
 #pragma unroll
-                for (int i = 0; i < N; ++i) acc[v][i] = 0.0f;
+                for (int i = 0; i < 8; ++i) acc[v][i] = 0.0f;
             bool nan_row = false;
 #pragma unroll 2
             for (int j = 0; j < top_k; ++j) {
                 const int32_t r = row_of[t * top_k + j];
                 const float wj = load_as_float(w, wdt, t * top_k + j);
                 if (r < 0) { nan_row = true; continue; }
-                const uint4 *src = out_disp + (int64_t)r * nvec;
+                const void *src = static_cast<const uint8_t *>(out_disp) + (int64_t)r * H * elem_o;
 #pragma unroll
                 for (int v = 0; v < V; ++v) {
                     const int64_t c = base + threadIdx.x + (int64_t)v * blockDim.x;
-                    if (c < nvec) {
-                        Vec16 q;
-                        q.u = __ldg(src + c);
-                        float f[N];
-                        unpack<DT>(q, f);
+                    if (c < ng) {
+                        float f[8];
+                        load8<ODT>(src, c, f);
 #pragma unroll
-                        for (int i = 0; i < N; ++i) acc[v][i] = fmaf(wj, f[i], acc[v][i]);
+                        for (int i = 0; i < 8; ++i) acc[v][i] = fmaf(wj, f[i], acc[v][i]);
                     }
                 }
             }
@@ -112,32 +123,29 @@ combine_kernel(const uint4 *__restrict__ out_disp, const void *__restrict__ w,
 #pragma unroll
                 for (int v = 0; v < V; ++v)
 #pragma unroll
-                    for (int i = 0; i < N; ++i) acc[v][i] = __int_as_float(0x7fc00000);
+                    for (int i = 0; i < 8; ++i) acc[v][i] = __int_as_float(0x7fc00000);
             }
             if constexpr (!NORM) {
 #pragma unroll
                 for (int v = 0; v < V; ++v) {
                     const int64_t c = base + threadIdx.x + (int64_t)v * blockDim.x;
-                    if (c < nvec) y[t * nvec + c] = pack<DT>(acc[v]).u;
+                    if (c < ng) store8<YDT>(y, t * ng + c, acc[v]);
                 }
             } else {
-                // x = acc + residual, rounded to dtype; sum of squares of it
+                // x = acc + residual, rounded to the activation dtype; sum of
+                // squares of the rounded x
                 float ss = 0.0f;
 #pragma unroll
                 for (int v = 0; v < V; ++v) {
                     const int64_t c = base + threadIdx.x + (int64_t)v * blockDim.x;
-                    if (c < nvec) {
-                        Vec16 q;
-                        q.u = __ldg(residual + t * nvec + c);
-                        float f[N];
-                        unpack<DT>(q, f);
+                    if (c < ng) {
+                        float f[8];
+                        load8<YDT>(residual, t * ng + c, f);
 #pragma unroll
-                        for (int i = 0; i < N; ++i) acc[v][i] += f[i];
-                        const Vec16 xr = pack<DT>(acc[v]);
-                        x_out[t * nvec + c] = xr.u;
-                        unpack<DT>(xr, acc[v]);
+                        for (int i = 0; i < 8; ++i) acc[v][i] += f[i];
+                        store8<YDT>(x_out, t * ng + c, acc[v]);
 #pragma unroll
-                        for (int i = 0; i < N; ++i) ss = fmaf(acc[v][i], acc[v][i], ss);
+                        for (int i = 0; i < 8; ++i) ss = fmaf(acc[v][i], acc[v][i], ss);
                     }
                 }
 #pragma unroll
@@ -156,12 +164,12 @@ combine_kernel(const uint4 *__restrict__ out_disp, const void *__restrict__ w,
 #pragma unroll
                 for (int v = 0; v < V; ++v) {
                     const int64_t c = base + threadIdx.x + (int64_t)v * blockDim.x;
-                    if (c < nvec) {
-                        float f[N];
+                    if (c < ng) {
+                        float gm[8];
+                        load8_rt(gamma, gdt, c, gm);
 #pragma unroll
-                        for (int i = 0; i < N; ++i)
-                            f[i] = acc[v][i] * r * load_as_float(gamma, gdt, c * N + i);
-                        y[t * nvec + c] = pack<DT>(f).u;
+                        for (int i = 0; i < 8; ++i) acc[v][i] = acc[v][i] * r * gm[i];
+                        store8<YDT>(y, t * ng + c, acc[v]);
                     }
                 }
             }
@@ -169,31 +177,25 @@ combine_kernel(const uint4 *__restrict__ out_disp, const void *__restrict__ w,
     }
 }
 
-template <int DT, bool NORM>
-cudaError_t launch_combine_dt(const void *out_disp, const void *w, int wdt,
-                              const int32_t *row_of, const void *residual,
-                              const void *gamma, int gdt, float eps, int64_t T,
-                              int top_k, int64_t H, void *y, void *x_out,
-                              float *rstd, cudaStream_t s)
+template <int ODT, int YDT, bool NORM>
+cudaError_t launch_typed(const void *out_disp, const void *w, int wdt, const int32_t *row_of,
+                         const void *residual, const void *gamma, int gdt, float eps,
+                         int64_t T, int top_k, int64_t H, void *y, void *x_out, float *rstd,
+                         cudaStream_t s)
 {
-    constexpr int N = VecTraits<DT>::N;
-    const int64_t nvec = H / N;
+    const int64_t ng = H / 8;
     int V = 1;
-    while (V < 8 && nvec > (int64_t)V * 256) V *= 2;
-    int64_t threads = (nvec + V - 1) / V;
+    while (V < kMaxV && ng > (int64_t)V * kMaxThreads) V *= 2;
+    int64_t threads = (ng + V - 1) / V;
     threads = (threads + 31) / 32 * 32;
-    if (threads > 256) threads = 256;
+    if (threads > kMaxThreads) threads = kMaxThreads;
     if (threads < 32) threads = 32;
     int64_t blocks = T;
     const int64_t cap = (int64_t)device_sm_count() * 32;
     if (blocks > cap) blocks = cap;
-    const uint4 *od = static_cast<const uint4 *>(out_disp);
-    const uint4 *res = static_cast<const uint4 *>(residual);
-    uint4 *yv = static_cast<uint4 *>(y);
-    uint4 *xv = static_cast<uint4 *>(x_out);
-#define MOE_COMBINE_LAUNCH(VV)                                                  \
-    combine_kernel<DT, VV, NORM><<<(unsigned)blocks, (unsigned)threads, 0, s>>>( \
-        od, w, wdt, row_of, res, gamma, gdt, eps, T, top_k, H, yv, xv, rstd)
+#define MOE_COMBINE_LAUNCH(VV)                                                             \
+    combine_kernel<ODT, YDT, VV, NORM><<<(unsigned)blocks, (unsigned)threads, 0, s>>>(     \
+        out_disp, w, wdt, row_of, residual, gamma, gdt, eps, T, top_k, H, y, x_out, rstd)
     switch (V) {
     case 1: MOE_COMBINE_LAUNCH(1); break;
     case 2: MOE_COMBINE_LAUNCH(2); break;
@@ -205,42 +207,45 @@ cudaError_t launch_combine_dt(const void *out_disp, const void *w, int wdt,
 }
 
 template <bool NORM>
-cudaError_t launch_combine_norm(int dt, const void *out_disp, const void *w,
-                                int wdt, const int32_t *row_of,
-                                const void *residual, const void *gamma,
-                                int gdt, float eps, int64_t T, int top_k,
-                                int64_t H, void *y, void *x_out, float *rstd,
-                                cudaStream_t s)
+cudaError_t launch_norm(const void *out_disp, int odt, const void *w, int wdt,
+                        const int32_t *row_of, const void *residual, const void *gamma,
+                        int gdt, float eps, int64_t T, int top_k, int64_t H, void *y, int ydt,
+                        void *x_out, float *rstd, cudaStream_t s)
 {
-    switch (dt) {
-    case DT_F32:
-        return launch_combine_dt<DT_F32, NORM>(out_disp, w, wdt, row_of, residual, gamma, gdt, eps, T, top_k, H, y, x_out, rstd, s);
-    case DT_BF16:
-        return launch_combine_dt<DT_BF16, NORM>(out_disp, w, wdt, row_of, residual, gamma, gdt, eps, T, top_k, H, y, x_out, rstd, s);
-    default:
-        return launch_combine_dt<DT_F16, NORM>(out_disp, w, wdt, row_of, residual, gamma, gdt, eps, T, top_k, H, y, x_out, rstd, s);
+#define MOE_TYPED(O, Y)                                                                   \
+    return launch_typed<O, Y, NORM>(out_disp, w, wdt, row_of, residual, gamma, gdt, eps, T, \
+                                    top_k, H, y, x_out, rstd, s)
+    if (ydt == DT_F32) MOE_TYPED(DT_F32, DT_F32);
+    if (ydt == DT_BF16) {
+        if (odt == DT_F32) MOE_TYPED(DT_F32, DT_BF16);
+        MOE_TYPED(DT_BF16, DT_BF16);
     }
+    if (odt == DT_F32) MOE_TYPED(DT_F32, DT_F16);
+    MOE_TYPED(DT_F16, DT_F16);
+#undef MOE_TYPED
 }
 
 }  // namespace
 
-// With the norm the whole row must fit one pass: 8 vectors x 256 threads.
-int combine_max_h(int dt, bool norm)
+// With the norm the whole row must fit one pass: 8 groups x 256 threads.
+int combine_max_h(bool norm)
 {
     if (!norm) return 1 << 30;
-    return 8 * 256 * (dt == DT_F32 ? 4 : 8);
+    return kMaxV * kMaxThreads * 8;
 }
 
-cudaError_t launch_combine(const void *out_disp, int dt, const void *w, int wdt,
+cudaError_t launch_combine(const void *out_disp, int odt, const void *w, int wdt,
                            const int32_t *row_of, const void *residual,
                            const void *gamma, int gdt, float eps, int64_t T,
-                           int top_k, int64_t H, void *y, void *x_out,
+                           int top_k, int64_t H, void *y, int ydt, void *x_out,
                            float *rstd, cudaStream_t s)
 {
     if (T == 0) return cudaSuccess;
     if (residual != nullptr)
-        return launch_combine_norm<true>(dt, out_disp, w, wdt, row_of, residual, gamma, gdt, eps, T, top_k, H, y, x_out, rstd, s);
-    return launch_combine_norm<false>(dt, out_disp, w, wdt, row_of, residual, gamma, gdt, eps, T, top_k, H, y, x_out, rstd, s);
+        return launch_norm<true>(out_disp, odt, w, wdt, row_of, residual, gamma, gdt, eps, T,
+                                 top_k, H, y, ydt, x_out, rstd, s);
+    return launch_norm<false>(out_disp, odt, w, wdt, row_of, residual, gamma, gdt, eps, T,
+                              top_k, H, y, ydt, x_out, rstd, s);
 }
 
 }  // namespace moe

@@ -10,7 +10,8 @@
 //   GEMM1 (SWIGLU):  B tile = 128 gate rows stacked on 128 up rows of the
 //                    same output columns; one 128x256x16 MMA computes both;
 //                    the epilogue forms SiLU(g)*u for 128 columns of h.
-//   GEMM2:           B tile = 256 rows of down; the epilogue rounds to dtype.
+//   GEMM2:           B tile = 256 rows of down; the epilogue writes FP32 or
+//                    rounds to dtype (the caller's choice of output type).
 // Per CTA (one per SM, 192 threads):
 //   warp 0  TMA producer: x tile [128 rows x 64 k] and weight tile
 //           [256 rows x 64 k] per stage, 128-byte swizzle, 4 stages;
@@ -258,7 +259,7 @@ __device__ __forceinline__ uint32_t pack2(float a, float b)
 
 // ---- the kernel -------------------------------------------------------------
 
-template <int DT, bool SWIGLU>
+template <int DT, bool SWIGLU, bool OUT_F32>
 __global__ void __launch_bounds__(THREADS, 1)
 grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB0,
@@ -394,19 +395,18 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             if (!__all_sync(0xffffffffu, ready)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
-            using ET = typename Elem<DT>::T;
-            ET *orow = static_cast<ET *>(out) + row * (int64_t)N;
 #pragma unroll 1
             for (int c = 0; c < N_OUT / 32; ++c) {
                 uint32_t g[32];
                 tmem_ld32(tbase + c * 32, g);
-                uint4 v[4];
-                uint32_t *pv = reinterpret_cast<uint32_t *>(v);
-                if (SWIGLU) {
+                const int col0 = n * N_OUT + c * 32;
+                if constexpr (SWIGLU) {
                     uint32_t u[32];
                     tmem_ld32(tbase + BN / 2 + c * 32, u);
                     tmem_ld_wait(g);
                     tmem_ld_wait(u);
+                    uint4 v[4];
+                    uint32_t *pv = reinterpret_cast<uint32_t *>(v);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
@@ -415,18 +415,37 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                         const float h1 = g1 / (1.0f + __expf(-g1)) * u1;
                         pv[i] = pack2<DT>(h0, h1);
                     }
+                    uint16_t *orow = static_cast<uint16_t *>(out) + row * (int64_t)N;
+                    if (row_ok) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            if (col0 + 8 * j < N)
+                                *reinterpret_cast<uint4 *>(orow + col0 + 8 * j) = v[j];
+                    }
+                } else if constexpr (OUT_F32) {
+                    tmem_ld_wait(g);
+                    float *orow = static_cast<float *>(out) + row * (int64_t)N;
+                    if (row_ok) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            if (col0 + 4 * j < N)
+                                *reinterpret_cast<uint4 *>(orow + col0 + 4 * j) =
+                                    make_uint4(g[4 * j], g[4 * j + 1], g[4 * j + 2], g[4 * j + 3]);
+                    }
                 } else {
                     tmem_ld_wait(g);
+                    uint4 v[4];
+                    uint32_t *pv = reinterpret_cast<uint32_t *>(v);
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         pv[i] = pack2<DT>(__uint_as_float(g[2 * i]), __uint_as_float(g[2 * i + 1]));
-                }
-                const int col0 = n * N_OUT + c * 32;
-                if (row_ok) {
+                    uint16_t *orow = static_cast<uint16_t *>(out) + row * (int64_t)N;
+                    if (row_ok) {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        if (col0 + 8 * j < N)
-                            *reinterpret_cast<uint4 *>(orow + col0 + 8 * j) = v[j];
+                        for (int j = 0; j < 4; ++j)
+                            if (col0 + 8 * j < N)
+                                *reinterpret_cast<uint4 *>(orow + col0 + 8 * j) = v[j];
+                    }
                 }
             }
             tc_fence_before();
@@ -503,7 +522,7 @@ bool encode_3d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_
 }
 
 // The dynamic shared-memory opt-in is per device and per kernel instance.
-template <int DT, bool SWIGLU>
+template <int DT, bool SWIGLU, bool OUT_F32>
 cudaError_t ensure_smem_attr()
 {
     static std::atomic<uint64_t> done_mask{0};
@@ -512,7 +531,7 @@ cudaError_t ensure_smem_attr()
     if (err != cudaSuccess) return err;
     const uint64_t bit = 1ull << (dev & 63);
     if (done_mask.load() & bit) return cudaSuccess;
-    err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<DT, SWIGLU>,
+    err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<DT, SWIGLU, OUT_F32>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (err == cudaSuccess) done_mask.fetch_or(bit);
     return err;
@@ -527,7 +546,7 @@ int64_t tc_tile_upper_bound(int64_t rows, int E, int64_t n_tiles)
 template <int DT>
 cudaError_t launch_tc_dt(const void *x_disp, const int32_t *offsets, int64_t rows,
                          const void *gate, const void *up, const void *down, int E,
-                         int64_t H, int64_t I, void *h_ws, void *out_disp,
+                         int64_t H, int64_t I, void *h_ws, void *out_disp, bool out_f32,
                          unsigned *status, cudaStream_t s)
 {
     const CUtensorMapDataType tdt =
@@ -539,8 +558,9 @@ cudaError_t launch_tc_dt(const void *x_disp, const int32_t *offsets, int64_t row
         !encode_2d(&mh, tdt, h_ws, (uint64_t)I, (uint64_t)rows, BK, BM) ||
         !encode_3d(&md, tdt, down, (uint64_t)I, (uint64_t)H, (uint64_t)E, BK, BN))
         return cudaErrorInvalidValue;
-    cudaError_t err = ensure_smem_attr<DT, true>();
-    if (err == cudaSuccess) err = ensure_smem_attr<DT, false>();
+    cudaError_t err = ensure_smem_attr<DT, true, false>();
+    if (err == cudaSuccess)
+        err = out_f32 ? ensure_smem_attr<DT, false, true>() : ensure_smem_attr<DT, false, false>();
     if (err != cudaSuccess) return err;
     const int64_t sms = device_sm_count();
     const int nt1 = (int)((I + BN / 2 - 1) / (BN / 2));
@@ -549,10 +569,14 @@ cudaError_t launch_tc_dt(const void *x_disp, const int32_t *offsets, int64_t row
     int64_t g2 = tc_tile_upper_bound(rows, E, nt2);
     if (g1 > sms) g1 = sms;
     if (g2 > sms) g2 = sms;
-    grouped_gemm_tc_kernel<DT, true><<<(unsigned)g1, THREADS, kSmemBytes, s>>>(
+    grouped_gemm_tc_kernel<DT, true, false><<<(unsigned)g1, THREADS, kSmemBytes, s>>>(
         mx, mg, mu, offsets, E, (int)I, (int)H, nt1, h_ws, status);
-    grouped_gemm_tc_kernel<DT, false><<<(unsigned)g2, THREADS, kSmemBytes, s>>>(
-        mh, md, md, offsets, E, (int)H, (int)I, nt2, out_disp, status);
+    if (out_f32)
+        grouped_gemm_tc_kernel<DT, false, true><<<(unsigned)g2, THREADS, kSmemBytes, s>>>(
+            mh, md, md, offsets, E, (int)H, (int)I, nt2, out_disp, status);
+    else
+        grouped_gemm_tc_kernel<DT, false, false><<<(unsigned)g2, THREADS, kSmemBytes, s>>>(
+            mh, md, md, offsets, E, (int)H, (int)I, nt2, out_disp, status);
     return cudaGetLastError();
 }
 
@@ -561,13 +585,15 @@ cudaError_t launch_tc_dt(const void *x_disp, const int32_t *offsets, int64_t row
 cudaError_t launch_experts_tc(int dt, const void *x_disp, const int32_t *offsets,
                               int64_t rows, const void *gate, const void *up,
                               const void *down, int E, int64_t H, int64_t I,
-                              void *h_ws, void *out_disp, unsigned *status,
+                              void *h_ws, void *out_disp, bool out_f32, unsigned *status,
                               cudaStream_t s)
 {
     if (rows == 0) return cudaSuccess;
     if (dt == DT_BF16)
-        return launch_tc_dt<DT_BF16>(x_disp, offsets, rows, gate, up, down, E, H, I, h_ws, out_disp, status, s);
-    return launch_tc_dt<DT_F16>(x_disp, offsets, rows, gate, up, down, E, H, I, h_ws, out_disp, status, s);
+        return launch_tc_dt<DT_BF16>(x_disp, offsets, rows, gate, up, down, E, H, I, h_ws,
+                                     out_disp, out_f32, status, s);
+    return launch_tc_dt<DT_F16>(x_disp, offsets, rows, gate, up, down, E, H, I, h_ws,
+                                out_disp, out_f32, status, s);
 }
 
 }  // namespace moe

@@ -24,11 +24,12 @@ cudaError_t launch_dispatch(const uint32_t *idx, int64_t T, int top_k, int E,
                             cudaStream_t s);
 
 // Weighted combine, optionally followed by residual Add + RMSNorm.
-int combine_max_h(int dt, bool norm);
-cudaError_t launch_combine(const void *out_disp, int dt, const void *w, int wdt,
+// out_disp in odt; y, residual and x_out in ydt; H % 8 == 0.
+int combine_max_h(bool norm);
+cudaError_t launch_combine(const void *out_disp, int odt, const void *w, int wdt,
                            const int32_t *row_of, const void *residual,
                            const void *gamma, int gdt, float eps, int64_t T,
-                           int top_k, int64_t H, void *y, void *x_out,
+                           int top_k, int64_t H, void *y, int ydt, void *x_out,
                            float *rstd, cudaStream_t s);
 
 // FP32 SwiGLU experts on CUDA cores. h_ws holds [rows, I] floats.
@@ -39,13 +40,14 @@ cudaError_t launch_experts_simt(const float *x_disp, const int32_t *offsets,
                                 float *out_disp, cudaStream_t s);
 
 // BF16/F16 SwiGLU experts on tcgen05 tensor cores (TMA + TMEM).
-// h_ws holds [rows, I] elements of dt. Returns cudaErrorInvalidValue when a
-// TMA descriptor cannot be encoded for the given shapes/pointers.
+// h_ws holds [rows, I] elements of dt; out_disp is FP32 when out_f32, else dt.
+// Returns cudaErrorInvalidValue when a TMA descriptor cannot be encoded for
+// the given shapes/pointers.
 cudaError_t launch_experts_tc(int dt, const void *x_disp,
                               const int32_t *offsets, int64_t rows,
                               const void *gate, const void *up,
                               const void *down, int E, int64_t H, int64_t I,
-                              void *h_ws, void *out_disp, unsigned *status,
-                              cudaStream_t s);
+                              void *h_ws, void *out_disp, bool out_f32,
+                              unsigned *status, cudaStream_t s);
 
 }  // namespace moe

@@ -96,12 +96,15 @@ int check_experts_args(int64_t rows, int64_t E, int64_t H, int64_t I, int dt)
     return MOE_OK;
 }
 
-int check_combine_args(int dt, int wdt, int64_t T, int top_k, int64_t H, bool norm)
+int check_combine_args(int odt, int wdt, int dt, int64_t T, int top_k, int64_t H, bool norm)
 {
-    if (!valid_dtype(dt) || !valid_dtype(wdt)) return fail(MOE_ERR_DTYPE, "dtype must be F32, BF16 or F16");
+    if (!valid_dtype(odt) || !valid_dtype(wdt) || !valid_dtype(dt))
+        return fail(MOE_ERR_DTYPE, "dtype must be F32, BF16 or F16");
+    if (odt != dt && odt != MOE_F32)
+        return fail(MOE_ERR_DTYPE, "expert outputs must be in the activation dtype or F32");
     if (T < 0 || top_k < 1 || T * top_k > kMaxRows) return fail(MOE_ERR_SHAPE, "need T >= 0, top_k >= 1, T*top_k < 2^31");
-    if (!vec_dim_ok(H, dt)) return fail(MOE_ERR_SHAPE, "H*elem must be a positive multiple of 16 bytes");
-    if (H > combine_max_h(dt, norm)) return fail(MOE_ERR_SHAPE, "H too large for the fused norm (one pass per row)");
+    if (H < 1 || H % 8 != 0) return fail(MOE_ERR_SHAPE, "H must be a positive multiple of 8");
+    if (H > combine_max_h(norm)) return fail(MOE_ERR_SHAPE, "H too large for the fused norm (one pass per row)");
     return MOE_OK;
 }
 
@@ -125,14 +128,14 @@ ForwardLayout forward_layout(int64_t T, int64_t H, int64_t I, int64_t E, int top
     L.disp_ws = take(dispatch_workspace_bytes((int64_t)A, (int)E));
     L.x_disp = take(A * (size_t)H * eb);
     L.h = take(A * (size_t)I * eb);
-    L.out_disp = take(A * (size_t)H * eb);
+    L.out_disp = take(A * (size_t)H * 4);   // expert outputs stay FP32
     L.total = off;
     return L;
 }
 
 int run_experts(const void *x_disp, const int32_t *offsets, int64_t rows, const void *gate,
                 const void *up, const void *down, int64_t E, int64_t H, int64_t I, int dt,
-                void *h_ws, void *out_disp, cudaStream_t s)
+                void *h_ws, void *out_disp, int odt, cudaStream_t s)
 {
     cudaError_t err;
     if (dt == MOE_F32) {
@@ -144,7 +147,7 @@ int run_experts(const void *x_disp, const int32_t *offsets, int64_t rows, const 
         unsigned *st = status_ptr();
         if (!st) return fail(MOE_ERR_CUDA, "cannot resolve the device status word");
         err = launch_experts_tc(dt, x_disp, offsets, rows, gate, up, down, (int)E, H, I, h_ws,
-                                out_disp, st, s);
+                                out_disp, odt == MOE_F32, st, s);
         if (err == cudaErrorInvalidValue)
             return fail(MOE_ERR_ALIGN, "TMA descriptor rejected (pointer alignment or shape)");
     }
@@ -232,11 +235,14 @@ size_t moe_experts_workspace_size(int64_t rows, int64_t E, int64_t H, int64_t I,
 
 int moe_experts_forward(const void *x_disp, const int32_t *offsets, int64_t rows,
                         const void *gate, const void *up, const void *down, int64_t E,
-                        int64_t H, int64_t I, int dtype, void *out_disp, void *workspace,
-                        size_t workspace_bytes, void *stream)
+                        int64_t H, int64_t I, int dtype, void *out_disp, int out_dtype,
+                        void *workspace, size_t workspace_bytes, void *stream)
 {
     int rc = check_experts_args(rows, E, H, I, dtype);
-    if (rc != MOE_OK || rows == 0) return rc;
+    if (rc != MOE_OK) return rc;
+    if (out_dtype != dtype && out_dtype != MOE_F32)
+        return fail(MOE_ERR_DTYPE, "out_dtype must be the expert dtype or F32");
+    if (rows == 0) return MOE_OK;
     if (!x_disp || !offsets || !gate || !up || !down || !out_disp)
         return fail(MOE_ERR_NULL, "moe_experts_forward: NULL tensor");
     if (!aligned16(x_disp) || !aligned16(offsets) || !aligned16(gate) || !aligned16(up) ||
@@ -246,29 +252,31 @@ int moe_experts_forward(const void *x_disp, const int32_t *offsets, int64_t rows
     if (workspace_bytes < need || !workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return fail(MOE_ERR_WORKSPACE, "moe_experts_forward: workspace too small or not 256-byte aligned");
     return run_experts(x_disp, offsets, rows, gate, up, down, E, H, I, dtype, workspace,
-                       out_disp, static_cast<cudaStream_t>(stream));
+                       out_disp, out_dtype, static_cast<cudaStream_t>(stream));
 }
 
-int moe_combine(const void *out_disp, int dtype, const void *weights, int weights_dtype,
-                const int32_t *row_of, int64_t T, int top_k, int64_t H, void *y, void *stream)
+int moe_combine(const void *out_disp, int out_dtype, const void *weights, int weights_dtype,
+                const int32_t *row_of, int64_t T, int top_k, int64_t H, void *y, int dtype,
+                void *stream)
 {
-    int rc = check_combine_args(dtype, weights_dtype, T, top_k, H, false);
+    int rc = check_combine_args(out_dtype, weights_dtype, dtype, T, top_k, H, false);
     if (rc != MOE_OK || T == 0) return rc;
     if (!out_disp || !weights || !row_of || !y) return fail(MOE_ERR_NULL, "moe_combine: NULL tensor");
     if (!aligned16(out_disp) || !aligned16(weights) || !aligned16(row_of) || !aligned16(y))
         return fail(MOE_ERR_ALIGN, "moe_combine: tensors must be 16-byte aligned");
-    cudaError_t err = launch_combine(out_disp, dtype, weights, weights_dtype, row_of, nullptr,
-                                     nullptr, MOE_F32, 1.0f, T, top_k, H, y, nullptr, nullptr,
-                                     static_cast<cudaStream_t>(stream));
+    cudaError_t err = launch_combine(out_disp, out_dtype, weights, weights_dtype, row_of, nullptr,
+                                     nullptr, MOE_F32, 1.0f, T, top_k, H, y, dtype, nullptr,
+                                     nullptr, static_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_combine");
 }
 
-int moe_combine_add_rmsnorm(const void *out_disp, int dtype, const void *weights,
+int moe_combine_add_rmsnorm(const void *out_disp, int out_dtype, const void *weights,
                             int weights_dtype, const int32_t *row_of, const void *residual,
-                            const void *gamma, int gamma_dtype, float eps, int64_t T, int top_k,
-                            int64_t H, void *y, void *x_out, float *rstd, void *stream)
+                            int dtype, const void *gamma, int gamma_dtype, float eps, int64_t T,
+                            int top_k, int64_t H, void *y, void *x_out, float *rstd,
+                            void *stream)
 {
-    int rc = check_combine_args(dtype, weights_dtype, T, top_k, H, true);
+    int rc = check_combine_args(out_dtype, weights_dtype, dtype, T, top_k, H, true);
     if (rc != MOE_OK) return rc;
     if (!valid_dtype(gamma_dtype)) return fail(MOE_ERR_DTYPE, "gamma dtype must be F32, BF16 or F16");
     if (!(isfinite(eps) && eps > 0.0f)) return fail(MOE_ERR_VALUE, "eps must be finite and > 0");
@@ -278,8 +286,8 @@ int moe_combine_add_rmsnorm(const void *out_disp, int dtype, const void *weights
     if (!aligned16(out_disp) || !aligned16(weights) || !aligned16(row_of) || !aligned16(residual) ||
         !aligned16(gamma) || !aligned16(y) || !aligned16(x_out) || !aligned16(rstd))
         return fail(MOE_ERR_ALIGN, "moe_combine_add_rmsnorm: tensors must be 16-byte aligned");
-    cudaError_t err = launch_combine(out_disp, dtype, weights, weights_dtype, row_of, residual,
-                                     gamma, gamma_dtype, eps, T, top_k, H, y, x_out, rstd,
+    cudaError_t err = launch_combine(out_disp, out_dtype, weights, weights_dtype, row_of, residual,
+                                     gamma, gamma_dtype, eps, T, top_k, H, y, dtype, x_out, rstd,
                                      static_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_combine_add_rmsnorm");
 }
@@ -303,6 +311,7 @@ int moe_forward(const void *x, int dtype, const void *logits, int logits_dtype, 
     if (rc != MOE_OK) return rc;
     if (T < 0 || top_k < 1 || top_k > E || T * top_k > kMaxRows)
         return fail(MOE_ERR_SHAPE, "need T >= 0 and 1 <= top_k <= E");
+    if (H % 8 != 0) return fail(MOE_ERR_SHAPE, "H must be a multiple of 8");
     if (T == 0) return MOE_OK;
     if (!x || !logits || !gate || !up || !down || !y) return fail(MOE_ERR_NULL, "moe_forward: NULL tensor");
     if (!aligned16(x) || !aligned16(logits) || !aligned16(gate) || !aligned16(up) ||
@@ -329,10 +338,10 @@ int moe_forward(const void *x, int dtype, const void *logits, int logits_dtype, 
     err = launch_dispatch(idx, T, top_k, (int)E, x, dtype, H, counts, offsets, row_of, src_of,
                           x_disp, ws + L.disp_ws, st, s);
     if (err != cudaSuccess) return cuda_fail(err, "moe_forward/dispatch");
-    rc = run_experts(x_disp, offsets, A, gate, up, down, E, H, I, dtype, h, out_disp, s);
+    rc = run_experts(x_disp, offsets, A, gate, up, down, E, H, I, dtype, h, out_disp, MOE_F32, s);
     if (rc != MOE_OK) return rc;
-    err = launch_combine(out_disp, dtype, w, logits_dtype, row_of, nullptr, nullptr, MOE_F32, 1.0f,
-                         T, top_k, H, y, nullptr, nullptr, s);
+    err = launch_combine(out_disp, MOE_F32, w, logits_dtype, row_of, nullptr, nullptr, MOE_F32,
+                         1.0f, T, top_k, H, y, dtype, nullptr, nullptr, s);
     return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_forward/combine");
 }
 

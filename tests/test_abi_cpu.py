@@ -111,8 +111,9 @@ def test_experts_validation(lib):
         a = dict(base, **kw)
         return lib.moe_experts_forward(a["x"], a["off"], a["rows"], a["g"], a["u"],
                                        a["d"], a["E"], a["H"], a["I"], a["dt"],
-                                       a["out"], a["ws"], a["wsb"], s)
+                                       a["out"], a.get("odt", a["dt"]), a["ws"], a["wsb"], s)
     assert call(dt=9) == DTYPE
+    assert call(odt=F16) == DTYPE       # output must be the expert dtype or F32
     assert call(H=60) == SHAPE          # 60 * 2 bytes is not a 16-byte multiple
     assert call(I=6, dt=F32) == SHAPE   # 24 bytes
     assert call(E=2000) == SHAPE
@@ -124,17 +125,19 @@ def test_experts_validation(lib):
 
 def test_combine_validation(lib):
     s = P(None)
-    assert lib.moe_combine(P(FAKE), BF16, P(FAKE), F32, P(FAKE), 8, 2, 60, P(FAKE), s) == SHAPE
-    assert lib.moe_combine(P(FAKE), 4, P(FAKE), F32, P(FAKE), 8, 2, 64, P(FAKE), s) == DTYPE
-    assert lib.moe_combine(P(None), BF16, P(FAKE), F32, P(FAKE), 8, 2, 64, P(FAKE), s) == NULL
-    assert lib.moe_combine(P(FAKE), BF16, P(FAKE), F32, P(FAKE), 0, 2, 64, P(None), s) == OK
+    assert lib.moe_combine(P(FAKE), BF16, P(FAKE), F32, P(FAKE), 8, 2, 60, P(FAKE), BF16, s) == SHAPE
+    assert lib.moe_combine(P(FAKE), 4, P(FAKE), F32, P(FAKE), 8, 2, 64, P(FAKE), BF16, s) == DTYPE
+    assert lib.moe_combine(P(FAKE), F16, P(FAKE), F32, P(FAKE), 8, 2, 64, P(FAKE), BF16, s) == DTYPE
+    assert lib.moe_combine(P(None), BF16, P(FAKE), F32, P(FAKE), 8, 2, 64, P(FAKE), BF16, s) == NULL
+    assert lib.moe_combine(P(FAKE), F32, P(FAKE), F32, P(FAKE), 8, 2, 64, P(FAKE_ODD), BF16, s) == ALIGN
+    assert lib.moe_combine(P(FAKE), BF16, P(FAKE), F32, P(FAKE), 0, 2, 64, P(None), BF16, s) == OK
     for eps in (0.0, -1e-6, math.inf, math.nan):
-        rc = lib.moe_combine_add_rmsnorm(P(FAKE), BF16, P(FAKE), F32, P(FAKE), P(FAKE),
+        rc = lib.moe_combine_add_rmsnorm(P(FAKE), BF16, P(FAKE), F32, P(FAKE), P(FAKE), BF16,
                                          P(FAKE), BF16, eps, 8, 2, 64, P(FAKE), P(FAKE),
                                          P(FAKE), s)
         assert rc == VALUE, eps
     big = 8 * 256 * 8 + 8
-    assert lib.moe_combine_add_rmsnorm(P(FAKE), BF16, P(FAKE), F32, P(FAKE), P(FAKE),
+    assert lib.moe_combine_add_rmsnorm(P(FAKE), BF16, P(FAKE), F32, P(FAKE), P(FAKE), BF16,
                                        P(FAKE), BF16, 1e-6, 8, 2, big, P(FAKE), P(FAKE),
                                        P(FAKE), s) == SHAPE
 

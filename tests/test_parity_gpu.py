@@ -202,7 +202,10 @@ def test_dispatch_bad_index_flags_and_nans(dev):
 # ---------------------------------------------------------------- experts
 
 @pytest.mark.parametrize("cfg", SMALL, ids=lambda c: c.name)
-def test_experts_parity(dev, cfg):
+@pytest.mark.parametrize("out_f32", [False, True], ids=["out_dtype", "out_f32"])
+def test_experts_parity(dev, cfg, out_f32):
+    if out_f32 and cfg.dtype == "f32":
+        pytest.skip("FP32 experts always write FP32")
     cpu, g = inputs_on(cfg, dev)
     o = oracle_inputs(cpu)
     idx, _, _ = oracle.route(o["logits"], cfg.logits_dtype, cfg.top_k, cfg.renormalize)
@@ -212,9 +215,12 @@ def test_experts_parity(dev, cfg):
     ref = oracle.experts_dispatched(x_disp, cfg.dtype, offsets, o["gate"], o["up"], o["down"])
     xd = W.from_numpy(x_disp, cfg.dtype, dev)
     out = moe.moe_experts_forward(xd, torch.from_numpy(offsets).to(dev), g["gate"],
-                                  g["up"], g["down"])
+                                  g["up"], g["down"],
+                                  out_dtype=torch.float32 if out_f32 else None)
     torch.cuda.synchronize()
     assert moe.moe_device_status() == 0
+    # FP32 outputs of BF16/F16 experts still carry the rounding of h to the
+    # input dtype between the GEMMs, so they are held to the input dtype's bar
     assert_close(to_f64(out), ref, cfg.dtype, f"{cfg.name} expert outputs")
 
 
@@ -257,9 +263,11 @@ def test_experts_exact_small_integers(dev):
 
 # ---------------------------------------------------------------- combine
 
-COMBINE_CASES = [(300, 2, 320, "bf16", "f32"), (4096, 6, 2048, "bf16", "bf16"),
-                 (64, 2, 128, "f32", "f32"), (129, 8, 7168, "bf16", "f32"),
-                 (77, 3, 264, "f16", "f16"), (5, 1, 16384, "bf16", "f32")]
+# (T, k, H, expert-output dtype, weight dtype, activation dtype)
+COMBINE_CASES = [(300, 2, 320, "bf16", "f32", "bf16"), (4096, 6, 2048, "bf16", "bf16", "bf16"),
+                 (64, 2, 128, "f32", "f32", "f32"), (129, 8, 7168, "bf16", "f32", "bf16"),
+                 (77, 3, 264, "f16", "f16", "f16"), (5, 1, 16384, "bf16", "f32", "bf16"),
+                 (300, 6, 2048, "f32", "bf16", "bf16"), (90, 4, 520, "f32", "f32", "f16")]
 
 
 def _routing_for(T, k, E, seed):
@@ -271,24 +279,26 @@ def _routing_for(T, k, E, seed):
     return w, row_of
 
 
-@pytest.mark.parametrize("T,k,H,dt,wdt", COMBINE_CASES)
-def test_combine_parity(dev, T, k, H, dt, wdt):
+@pytest.mark.parametrize("T,k,H,odt,wdt,dt", COMBINE_CASES)
+def test_combine_parity(dev, T, k, H, odt, wdt, dt):
     E = max(k, 16)
     w, row_of = _routing_for(T, k, E, seed=T + H)
     wt = torch.from_numpy(w)
     if wdt != "f32":
         wt = wt.to(W.TORCH_DTYPES[wdt])
     g = torch.Generator().manual_seed(H)
-    out = torch.randn((T * k, H), generator=g).to(W.TORCH_DTYPES[dt])
-    ref = oracle.combine(np_of(out), dt, np_of(wt), wdt, row_of, k)
-    y = moe.moe_combine(out.to(dev), wt.to(dev), torch.from_numpy(row_of).to(dev))
+    out = torch.randn((T * k, H), generator=g).to(W.TORCH_DTYPES[odt])
+    ref = oracle.combine(np_of(out), odt, np_of(wt), wdt, row_of, k)
+    y = moe.moe_combine(out.to(dev), wt.to(dev), torch.from_numpy(row_of).to(dev),
+                        dtype=W.TORCH_DTYPES[dt])
     torch.cuda.synchronize()
+    assert y.dtype == W.TORCH_DTYPES[dt]
     assert_close(to_f64(y), ref, dt, "combine")
 
 
-@pytest.mark.parametrize("T,k,H,dt,wdt", COMBINE_CASES)
+@pytest.mark.parametrize("T,k,H,odt,wdt,dt", COMBINE_CASES)
 @pytest.mark.parametrize("gdt", ["same", "f32"])
-def test_combine_add_rmsnorm_parity(dev, T, k, H, dt, wdt, gdt):
+def test_combine_add_rmsnorm_parity(dev, T, k, H, odt, wdt, dt, gdt):
     E = max(k, 16)
     w, row_of = _routing_for(T, k, E, seed=T * 3 + H)
     wt = torch.from_numpy(w)
@@ -296,12 +306,12 @@ def test_combine_add_rmsnorm_parity(dev, T, k, H, dt, wdt, gdt):
         wt = wt.to(W.TORCH_DTYPES[wdt])
     g = torch.Generator().manual_seed(H + 1)
     tdt = W.TORCH_DTYPES[dt]
-    out = torch.randn((T * k, H), generator=g).to(tdt)
+    out = torch.randn((T * k, H), generator=g).to(W.TORCH_DTYPES[odt])
     res = torch.randn((T, H), generator=g).to(tdt)
     gdt_name = dt if gdt == "same" else "f32"
     gamma = (1 + math.sqrt(0.1) * torch.randn(H, generator=g)).to(W.TORCH_DTYPES[gdt_name])
     eps = 1e-6
-    comb = oracle.combine(np_of(out), dt, np_of(wt), wdt, row_of, k)
+    comb = oracle.combine(np_of(out), odt, np_of(wt), wdt, row_of, k)
     y_ref, x_ref, rstd_ref = oracle.add_rmsnorm(comb, np_of(res), dt, np_of(gamma),
                                                 gdt_name, eps)
     y, x_out, rstd = moe.moe_combine_add_rmsnorm(
@@ -343,8 +353,9 @@ def test_forward_parity(dev, cfg):
     # the staged calls give the same result bit for bit
     idx, w = moe.moe_route(g["logits"], cfg.top_k, cfg.renormalize)
     d = moe.moe_dispatch(idx, g["x"], cfg.E)
-    out = moe.moe_experts_forward(d["x_disp"], d["offsets"], g["gate"], g["up"], g["down"])
-    y2 = moe.moe_combine(out, w, d["row_of"])
+    out = moe.moe_experts_forward(d["x_disp"], d["offsets"], g["gate"], g["up"], g["down"],
+                                  out_dtype=torch.float32)
+    y2 = moe.moe_combine(out, w, d["row_of"], dtype=g["x"].dtype)
     torch.cuda.synchronize()
     assert torch.equal(torch.isnan(y), torch.isnan(y2))
     assert torch.equal(torch.nan_to_num(y), torch.nan_to_num(y2))
