@@ -29,9 +29,7 @@ import argparse
 import json
 import os
 import statistics
-import subprocess
 import sys
-import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -110,61 +108,76 @@ def aggregate(step_s_max: float, tokens_per_rank: int, world: int) -> float:
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+    """Samples the SM clock and clock-event (throttle) reasons of one GPU while
+    the timed region runs: a background thread reads NVML through ctypes
+    every millisecond (read-only queries). Falls back to nothing if NVML is
+    unavailable."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
-        self.path = None
+    def __init__(self, device: torch.device):
+        self.device = device
+        self.samples = []
+        self.max_mhz = None
+        self._stop = None
+        self._thread = None
+
+    def _handle(self):
+        import ctypes
+        nvml = ctypes.CDLL("libnvidia-ml.so.1")
+        if nvml.nvmlInit_v2() != 0:
+            return None, None
+        h = ctypes.c_void_p()
+        uuid = getattr(torch.cuda.get_device_properties(self.device), "uuid", None)
+        ok = False
+        if uuid is not None:
+            ok = nvml.nvmlDeviceGetHandleByUUID(("GPU-" + str(uuid)).encode(), ctypes.byref(h)) == 0
+        if not ok:
+            ok = nvml.nvmlDeviceGetHandleByIndex_v2(self.device.index or 0, ctypes.byref(h)) == 0
+        return (nvml, h) if ok else (None, None)
 
     def __enter__(self):
+        import ctypes
+        import threading
         try:
-            fd, self.path = tempfile.mkstemp(suffix=".csv")
-            os.close(fd)
-            self.out = open(self.path, "w")
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=self.out, stderr=subprocess.DEVNULL)
+            nvml, h = self._handle()
         except OSError:
-            self.proc = None
+            nvml, h = None, None
+        if nvml is None:
+            return self
+        mx = ctypes.c_uint()
+        if nvml.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+            self.max_mhz = mx.value
+        reasons_fn = getattr(nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        self._stop = threading.Event()
+
+        def poll():
+            clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+            while not self._stop.is_set():
+                if nvml.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and \
+                        reasons_fn(h, ctypes.byref(rs)) == 0:
+                    self.samples.append((clk.value, rs.value))
+                time.sleep(0.001)
+        self._thread = threading.Thread(target=poll, daemon=True)
+        self._thread.start()
+        time.sleep(0.01)
         return self
 
     def __exit__(self, *exc):
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
-            self.out.close()
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=5)
 
     def summary(self):
-        if self.proc is None or self.path is None:
+        if not self.samples:
             return None
-        rows = []
-        with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
-                except ValueError:
-                    continue
-        os.unlink(self.path)
-        if not rows:
-            return None
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r)
-                          if v.lower() == "active"})
-        return {"sm_mhz": statistics.median(r[0] for r in rows),
-                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
-                "samples": len(rows)}
+        reasons = sorted({name for _, r in self.samples for bit, name in self.REASONS.items()
+                          if r & bit})
+        return {"sm_mhz": statistics.median(c for c, _ in self.samples),
+                "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(self.samples), "source": "NVML, 1 ms polling"}
 
 
 # ---------------------------------------------------------------- our arm
@@ -229,7 +242,7 @@ def run_ours(args, rank, world, local, dist):
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     barrier(dist, dev)
     torch.cuda.synchronize(dev)
-    with ClockSampler(dev.index) as clk:
+    with ClockSampler(dev) as clk:
         for i in range(args.steps):
             step(evs[i])
             flush.fill_(1)   # untimed: between the events of consecutive steps
@@ -348,7 +361,7 @@ def run_combine_norm(args, rank, world, local, dist, dev, peaks, flush):
     def fn():
         moe.moe_combine_add_rmsnorm(d["out_disp"], w, row_of, d["residual"], d["gamma"],
                                     cfg.eps, y=y, x_out=xo, rstd=rstd)
-    with ClockSampler(dev.index) as clk:
+    with ClockSampler(dev) as clk:
         ms = timed_loop(fn, args, stream, flush)
     ms_max = reduce_max(dist, ms, dev)
     nbytes = (T * k * H * 2 + T * k * (4 + 4) + T * H * 2 + H * 2 + 2 * T * H * 2 + T * 4)
@@ -448,7 +461,7 @@ def run_reference(args, rank, world):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="fine_prefill_bf16")
