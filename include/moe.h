@@ -130,6 +130,34 @@ int moe_dispatch(const uint32_t *expert_indices, int64_t T, int top_k,
                  size_t workspace_bytes, void *stream);
 
 /*
+ * moe_dispatch_noalloc -- moe_dispatch for callers that cannot allocate.
+ * The source pages have no counterpart to this call; it exists for callers
+ * that cannot supply device scratch memory: code whose device memory belongs
+ * to a pool that permits no allocation after start-up (for example a serving
+ * engine that reserves HBM up front, or a plugin whose host framework gives
+ * it no scratch in its enqueue step), and code that cannot pay for the
+ * device-wide synchronisation cudaMalloc / cudaFree bring on a latency-
+ * critical path.
+ *
+ * Arguments, outputs, ordering and errors are those of moe_dispatch, minus
+ * the workspace: the scratch lives in a 256 KiB array that the library owns
+ * on each device (kept until the process exits). It fits the per-chunk
+ * histograms when ceil(T*top_k / chunk) * E <= 65536 counters, i.e. any
+ * T*top_k with E <= 512, and E up to 1024 while T*top_k <= 16384; larger
+ * problems return MOE_ERR_WORKSPACE before anything is enqueued.
+ * The library allocates nothing for this call. The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress) and caches it;
+ * make that first call before any stream capture. Every call on a device
+ * shares the one array: calls whose kernels overlap on the GPU (different
+ * streams without ordering between them) race on it. Nothing in the array
+ * has to start at zero: each call writes every counter it reads.
+ */
+int moe_dispatch_noalloc(const uint32_t *expert_indices, int64_t T, int top_k,
+                         int64_t E, const void *x, int x_dtype, int64_t H,
+                         int32_t *counts, int32_t *offsets, int32_t *row_of,
+                         int32_t *src_of, void *x_disp, void *stream);
+
+/*
  * moe_experts_forward -- bias-free SwiGLU experts on dispatched rows.
  * ruDNN user guide, sections 3 and 5 (SwiGluExperts::forward_dispatched);
  * aclnnFFN "Formula" with no bias and a SwiGLU activation.

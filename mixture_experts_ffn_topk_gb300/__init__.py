@@ -38,6 +38,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_NULL", 2: "MOE_ERR_SHAPE",
 
 EXPORTED = ["moe_status_string", "moe_abi_version", "moe_last_error_detail",
             "moe_route", "moe_dispatch_workspace_size", "moe_dispatch",
+            "moe_dispatch_noalloc",
             "moe_experts_workspace_size", "moe_experts_forward", "moe_combine",
             "moe_combine_add_rmsnorm", "moe_forward_workspace_size",
             "moe_forward", "moe_device_status"]
@@ -67,6 +68,8 @@ def _bind(lib):
         "moe_dispatch_workspace_size": ([_I64, _INT, _I64], _SZ),
         "moe_dispatch": ([_P, _I64, _INT, _I64, _P, _INT, _I64, _P, _P, _P, _P,
                           _P, _P, _SZ, _P], _INT),
+        "moe_dispatch_noalloc": ([_P, _I64, _INT, _I64, _P, _INT, _I64, _P, _P, _P,
+                                  _P, _P, _P], _INT),
         "moe_experts_workspace_size": ([_I64, _I64, _I64, _I64, _INT], _SZ),
         "moe_experts_forward": ([_P, _P, _I64, _P, _P, _P, _I64, _I64, _I64,
                                  _INT, _P, _INT, _P, _SZ, _P], _INT),
@@ -199,6 +202,29 @@ def moe_dispatch(expert_indices: torch.Tensor, x: torch.Tensor, E: int,
         _ptr(offsets), _ptr(row_of), _ptr(src_of), _ptr(x_disp), _ptr(ws),
         _nbytes(ws), _stream(stream))
     _check(rc, "moe_dispatch")
+    return {"counts": counts, "offsets": offsets, "row_of": row_of,
+            "src_of": src_of, "x_disp": x_disp}
+
+
+def moe_dispatch_noalloc(expert_indices: torch.Tensor, x: torch.Tensor, E: int,
+                         counts=None, offsets=None, row_of=None, src_of=None,
+                         x_disp=None, stream=None) -> dict:
+    """``moe_dispatch`` without a workspace, for callers that cannot allocate
+    device scratch: the library keeps the scratch in a fixed 256 KiB array per
+    device (see ``include/moe.h``). Same outputs as :func:`moe_dispatch`."""
+    T, k = expert_indices.shape
+    H = x.shape[1]
+    dev = x.device
+    A = T * k
+    counts = counts if counts is not None else torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = offsets if offsets is not None else torch.empty(E + 1, dtype=torch.int32, device=dev)
+    row_of = row_of if row_of is not None else torch.empty(A, dtype=torch.int32, device=dev)
+    src_of = src_of if src_of is not None else torch.empty(A, dtype=torch.int32, device=dev)
+    x_disp = x_disp if x_disp is not None else torch.empty((A, H), dtype=x.dtype, device=dev)
+    rc = load_library().moe_dispatch_noalloc(
+        _ptr(expert_indices), T, k, E, _ptr(x), _code(x.dtype), H, _ptr(counts),
+        _ptr(offsets), _ptr(row_of), _ptr(src_of), _ptr(x_disp), _stream(stream))
+    _check(rc, "moe_dispatch_noalloc")
     return {"counts": counts, "offsets": offsets, "row_of": row_of,
             "src_of": src_of, "x_disp": x_disp}
 

@@ -1,0 +1,73 @@
+// dispatch_noalloc.cu -- moe_dispatch for callers that cannot allocate.
+//
+// moe_dispatch needs a small caller-provided scratch buffer (the per-chunk,
+// per-expert histograms of its first pass). Some callers cannot hand one
+// over: their device memory is owned by a pool that allows no allocation
+// after start-up (a serving engine that reserves all of HBM up front, or a
+// plugin whose host framework gives it no scratch space in its enqueue
+// step), or they cannot afford the device-wide synchronisation that
+// cudaMalloc / cudaFree imply on a latency-critical path. This entry point
+// takes the same inputs and outputs as moe_dispatch and keeps that scratch in
+// a fixed array that the library itself owns on every device.
+#include <atomic>
+#include <mutex>
+
+#include "../../include/moe.h"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+// The built-in scratch: 256 KiB, i.e. nchunks * E <= 65536 histogram
+// counters. Every GPU on which the library is loaded holds this array until
+// the process exits.
+constexpr size_t kNoAllocScratchBytes = 256u * 1024u;
+static __device__ __align__(256) unsigned char g_dispatch_scratch[kNoAllocScratchBytes];
+
+// In host code g_dispatch_scratch names a host-side stand-in, not device
+// memory, so the device address is looked up once per device (with that
+// device current) and cached.
+void *scratch_device_address(cudaError_t *err)
+{
+    static std::atomic<void *> cache[64];
+    static std::mutex mu;
+    int dev = 0;
+    *err = cudaGetDevice(&dev);
+    if (*err != cudaSuccess) return nullptr;
+    void *p = cache[dev & 63].load();
+    if (p != nullptr) return p;
+    std::lock_guard<std::mutex> lock(mu);
+    p = cache[dev & 63].load();
+    if (p != nullptr) return p;
+    *err = cudaGetSymbolAddress(&p, g_dispatch_scratch);
+    if (*err != cudaSuccess) return nullptr;
+    cache[dev & 63].store(p);
+    return p;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" int moe_dispatch_noalloc(const uint32_t *expert_indices, int64_t T, int top_k,
+                                    int64_t E, const void *x, int x_dtype, int64_t H,
+                                    int32_t *counts, int32_t *offsets, int32_t *row_of,
+                                    int32_t *src_of, void *x_disp, void *stream)
+{
+    // Sizes beyond the built-in array are refused before anything else runs.
+    const size_t need = moe_dispatch_workspace_size(T, top_k, E);
+    if (need > moe::kNoAllocScratchBytes)
+        return moe::report_error(MOE_ERR_WORKSPACE,
+                                 "moe_dispatch_noalloc: this T*top_k and E need more than the "
+                                 "256 KiB built-in scratch (chunks x E x 4 bytes); use "
+                                 "moe_dispatch with a workspace");
+    if (need == 0)   // T == 0 or invalid T/top_k/E: moe_dispatch validates and returns
+        return moe_dispatch(expert_indices, T, top_k, E, x, x_dtype, H, counts, offsets,
+                            row_of, src_of, x_disp, nullptr, 0, stream);
+    cudaError_t err = cudaSuccess;
+    void *scratch = moe::scratch_device_address(&err);
+    if (scratch == nullptr)
+        return moe::report_error(MOE_ERR_CUDA,
+                                 "moe_dispatch_noalloc: cannot resolve the scratch address");
+    return moe_dispatch(expert_indices, T, top_k, E, x, x_dtype, H, counts, offsets, row_of,
+                        src_of, x_disp, scratch, moe::kNoAllocScratchBytes, stream);
+}

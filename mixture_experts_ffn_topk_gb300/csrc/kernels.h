@@ -10,6 +10,10 @@ namespace moe {
 // Streaming multiprocessors of the current device (cached per device).
 int device_sm_count();
 
+// Records `what` as the text moe_last_error_detail() returns on this thread
+// and returns `code`.
+int report_error(int code, const char *what);
+
 // Softmax top-k routing, warp per token. E <= 1024.
 cudaError_t launch_route(const void *logits, int ldt, int64_t T, int E,
                          int top_k, int renormalize, uint32_t *idx, void *w,

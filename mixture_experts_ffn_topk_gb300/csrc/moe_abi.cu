@@ -156,6 +156,9 @@ int run_experts(const void *x_disp, const int32_t *offsets, int64_t rows, const 
 }
 
 }  // namespace
+
+int report_error(int code, const char *what) { return fail(code, what); }
+
 }  // namespace moe
 
 using namespace moe;
