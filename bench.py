@@ -57,14 +57,30 @@ def load_peaks():
         return dict(FALLBACK_PEAKS, source="fallback")
 
 
+KERNEL_SOURCES = {"experts": ["experts_tc.cu", "common.cuh"],
+                  "combine_add_rmsnorm": ["combine.cu", "common.cuh"]}
+
+
+def source_digest(kernel):
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "mixture_experts_ffn_topk_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def load_traffic(workload, kernel):
-    """Per-launch DRAM bytes from the committed ncu summary, if it still
-    matches the current kernel build (see profiles/)."""
+    """Per-launch DRAM bytes from the committed ncu summary, or None when
+    the kernel's sources changed since the counters were taken."""
     try:
         with open(PROFILE_TRAFFIC) as f:
             d = json.load(f)
-        return d.get(workload, {}).get(kernel)
-    except (OSError, ValueError):
+        entry = d.get(workload, {}).get(kernel)
+        if not entry or entry.get("source") != source_digest(kernel):
+            return None
+        return entry["bytes"]
+    except (OSError, ValueError, KeyError):
         return None
 
 
