@@ -17,7 +17,8 @@
 //           [256 rows x 64 k] per stage, 128-byte swizzle, 4 stages;
 //   warp 1  MMA issuer: tcgen05.mma.cta_group::1.kind::f16, M=128 N=256 K=16,
 //           accumulators double-buffered in TMEM (2 x 256 columns);
-//   warps 2-5  epilogue: tcgen05.ld 32 lanes x 32 columns, math, stores.
+//   warps 2-5  epilogue: tcgen05.ld 32 lanes x 32 columns, math, then a
+//           swizzled shared-memory hop so every store writes whole lines.
 // Tiles: each expert's row segment [offsets[e], offsets[e+1]) is cut into
 // 128-row M-tiles; linear tile ids run over (expert, n-tile, m-tile) with the
 // m-tile fastest, so CTAs working at the same time share weight tiles in L2.
@@ -55,8 +56,11 @@ constexpr int THREADS = 192;
 constexpr int MAX_E = 1024;
 constexpr uint64_t kDrainLimitNs = 100000000ull;   // 100 ms per teardown drain
 
+constexpr int EPI_ROW_BYTES = 128;           // epilogue staging: 32 rows x 128 B per warp
+
 struct __align__(1024) SharedStorage {
     uint8_t stage[STAGES][STAGE_BYTES];      // each stage 1024-byte aligned
+    uint8_t epi[4][32 * EPI_ROW_BYTES];      // per epilogue warp, 16-byte chunks swizzled
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
     uint64_t acc_full[2];
@@ -378,15 +382,26 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         }
     } else if (warp >= 2) {
         // ------------------------------------------------------ epilogue
+        // Each warp owns 32 accumulator rows (its TMEM lane quadrant). Per
+        // round it turns 128 output bytes of each row into its staging rows
+        // (thread = row; 16-byte chunk p stored at p ^ (row & 7) so the 32
+        // writes of one instruction spread over all banks), then copies the
+        // 32 x 128 bytes out with each store instruction writing four whole
+        // rows' 128-byte lines, masked to the expert's rows and to N.
         const int q = warp & 3;            // TMEM lane quadrant of this warp
+        uint8_t *stg = S.epi[warp - 2];
+        constexpr int ESZ = (OUT_F32 && !SWIGLU) ? 4 : 2;       // output element bytes
+        constexpr int RCOLS = EPI_ROW_BYTES / ESZ;              // columns per round
+        constexpr int ROUNDS = N_OUT / RCOLS;
+        const int64_t out_row_bytes = (int64_t)N * ESZ;
+        const int cch = lane & 7;                               // chunk this lane copies out
         int it = 0;
         for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++it) {
             int e, n, m;
             decode_tile(S, E, tile, e, n, m);
             const int seg_rows = S.offs[e + 1] - S.offs[e];
-            const int r_in_seg = m * BM + q * 32 + lane;
-            const bool row_ok = r_in_seg < seg_rows;
-            const int64_t row = (int64_t)S.offs[e] + r_in_seg;
+            const int r_base = m * BM + q * 32;                 // this warp's first row in the segment
+            uint8_t *out_base = static_cast<uint8_t *>(out) + ((int64_t)S.offs[e] + r_base) * out_row_bytes;
             const int acc = it & 1;
             const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
             // every lane waits; the warp leaves together if any lane gave up,
@@ -396,57 +411,54 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
 #pragma unroll 1
-            for (int c = 0; c < N_OUT / 32; ++c) {
-                uint32_t g[32];
-                tmem_ld32(tbase + c * 32, g);
-                const int col0 = n * N_OUT + c * 32;
-                if constexpr (SWIGLU) {
-                    uint32_t u[32];
-                    tmem_ld32(tbase + BN / 2 + c * 32, u);
-                    tmem_ld_wait(g);
-                    tmem_ld_wait(u);
-                    uint4 v[4];
-                    uint32_t *pv = reinterpret_cast<uint32_t *>(v);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
-                        const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
-                        const float h0 = g0 / (1.0f + __expf(-g0)) * u0;
-                        const float h1 = g1 / (1.0f + __expf(-g1)) * u1;
-                        pv[i] = pack2<DT>(h0, h1);
-                    }
-                    uint16_t *orow = static_cast<uint16_t *>(out) + row * (int64_t)N;
-                    if (row_ok) {
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            if (col0 + 8 * j < N)
-                                *reinterpret_cast<uint4 *>(orow + col0 + 8 * j) = v[j];
-                    }
-                } else if constexpr (OUT_F32) {
-                    tmem_ld_wait(g);
-                    float *orow = static_cast<float *>(out) + row * (int64_t)N;
-                    if (row_ok) {
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            if (col0 + 4 * j < N)
-                                *reinterpret_cast<uint4 *>(orow + col0 + 4 * j) =
-                                    make_uint4(g[4 * j], g[4 * j + 1], g[4 * j + 2], g[4 * j + 3]);
-                    }
+            for (int rd = 0; rd < ROUNDS; ++rd) {
+                uint32_t w[32];                                 // this row's 128 output bytes
+                if constexpr (OUT_F32 && !SWIGLU) {
+                    tmem_ld32(tbase + rd * 32, w);
+                    tmem_ld_wait(w);
                 } else {
-                    tmem_ld_wait(g);
-                    uint4 v[4];
-                    uint32_t *pv = reinterpret_cast<uint32_t *>(v);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        pv[i] = pack2<DT>(__uint_as_float(g[2 * i]), __uint_as_float(g[2 * i + 1]));
-                    uint16_t *orow = static_cast<uint16_t *>(out) + row * (int64_t)N;
-                    if (row_ok) {
+                    for (int half = 0; half < 2; ++half) {
+                        const int c = rd * 2 + half;            // 32-column TMEM chunk
+                        uint32_t g[32];
+                        tmem_ld32(tbase + c * 32, g);
+                        if constexpr (SWIGLU) {
+                            uint32_t u[32];
+                            tmem_ld32(tbase + BN / 2 + c * 32, u);
+                            tmem_ld_wait(g);
+                            tmem_ld_wait(u);
 #pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            if (col0 + 8 * j < N)
-                                *reinterpret_cast<uint4 *>(orow + col0 + 8 * j) = v[j];
+                            for (int i = 0; i < 16; ++i) {
+                                const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
+                                const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
+                                const float h0 = g0 / (1.0f + __expf(-g0)) * u0;
+                                const float h1 = g1 / (1.0f + __expf(-g1)) * u1;
+                                w[half * 16 + i] = pack2<DT>(h0, h1);
+                            }
+                        } else {
+                            tmem_ld_wait(g);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                w[half * 16 + i] = pack2<DT>(__uint_as_float(g[2 * i]),
+                                                             __uint_as_float(g[2 * i + 1]));
+                        }
                     }
                 }
+#pragma unroll
+                for (int p = 0; p < 8; ++p)
+                    *reinterpret_cast<uint4 *>(stg + lane * EPI_ROW_BYTES + ((p ^ (lane & 7)) << 4)) =
+                        make_uint4(w[4 * p], w[4 * p + 1], w[4 * p + 2], w[4 * p + 3]);
+                __syncwarp();
+                const int64_t col_byte = (int64_t)(n * N_OUT + rd * RCOLS) * ESZ + cch * 16;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int rr = 4 * j + (lane >> 3);
+                    const uint4 v = *reinterpret_cast<const uint4 *>(
+                        stg + rr * EPI_ROW_BYTES + ((cch ^ (rr & 7)) << 4));
+                    if (r_base + rr < seg_rows && col_byte < out_row_bytes)
+                        *reinterpret_cast<uint4 *>(out_base + rr * out_row_bytes + col_byte) = v;
+                }
+                __syncwarp();
             }
             tc_fence_before();
             __syncwarp();
