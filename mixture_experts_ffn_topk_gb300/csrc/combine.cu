@@ -92,6 +92,8 @@ combine_kernel(const void *__restrict__ out_disp, const void *__restrict__ w, in
     __shared__ float red[kMaxThreads / 32];
     __shared__ float s_rstd;
     const int64_t elem_o = ODT == DT_F32 ? 4 : 2;
+    pdl_wait();
+    pdl_launch_dependents();
 
     for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
         // groups handled in passes of V * blockDim (a single pass with NORM)
@@ -194,16 +196,16 @@ cudaError_t launch_typed(const void *out_disp, const void *w, int wdt, const int
     const int64_t cap = (int64_t)device_sm_count() * 32;
     if (blocks > cap) blocks = cap;
 #define MOE_COMBINE_LAUNCH(VV)                                                             \
-    combine_kernel<ODT, YDT, VV, NORM><<<(unsigned)blocks, (unsigned)threads, 0, s>>>(     \
-        out_disp, w, wdt, row_of, residual, gamma, gdt, eps, T, top_k, H, y, x_out, rstd)
+    return launch_pdl(combine_kernel<ODT, YDT, VV, NORM>, dim3((unsigned)blocks),           \
+                      dim3((unsigned)threads), 0, s, out_disp, w, wdt, row_of, residual,    \
+                      gamma, gdt, eps, T, top_k, H, y, x_out, rstd)
     switch (V) {
-    case 1: MOE_COMBINE_LAUNCH(1); break;
-    case 2: MOE_COMBINE_LAUNCH(2); break;
-    case 4: MOE_COMBINE_LAUNCH(4); break;
-    default: MOE_COMBINE_LAUNCH(8); break;
+    case 1: MOE_COMBINE_LAUNCH(1);
+    case 2: MOE_COMBINE_LAUNCH(2);
+    case 4: MOE_COMBINE_LAUNCH(4);
+    default: MOE_COMBINE_LAUNCH(8);
     }
 #undef MOE_COMBINE_LAUNCH
-    return cudaGetLastError();
 }
 
 template <bool NORM>

@@ -83,6 +83,35 @@ __device__ __forceinline__ uint64_t global_timer_ns()
     return t;
 }
 
+// Programmatic dependent launch. Every kernel of the library is launched with
+// programmatic stream serialisation allowed, so it may start while the
+// previous kernel on the stream drains; it calls pdl_wait() before its first
+// global-memory access (which returns once the previous grid has completed and
+// its writes are visible) and pdl_launch_dependents() to let the next kernel
+// start early in turn. Launched without the attribute, both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Every spin-wait in this library gives up after this long, sets
 // ST_TIMEOUT in the status word and lets the kernel wind down.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s

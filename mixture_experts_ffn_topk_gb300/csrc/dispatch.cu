@@ -49,6 +49,8 @@ dispatch_count_kernel(const uint32_t *__restrict__ idx, int64_t A, int E,
                       unsigned *status)
 {
     extern __shared__ int hist[];
+    pdl_wait();
+    pdl_launch_dependents();
     const int w = threadIdx.x / 32, lane = (int)lane_id();
     const int c = blockIdx.x * kChunkWarps + w;
     int *h = hist + (size_t)w * E;
@@ -76,6 +78,8 @@ dispatch_scan_kernel(int *__restrict__ chunk_counts, int nchunks, int E,
 {
     __shared__ int warp_tot[32];
     __shared__ int total_rows;
+    pdl_wait();
+    pdl_launch_dependents();
     const int e = threadIdx.x, lane = e & 31, w = e >> 5;
     int total = 0;
     if (e < E) {
@@ -124,6 +128,8 @@ dispatch_rank_kernel(const uint32_t *__restrict__ idx, int64_t A, int E,
                      int32_t *__restrict__ row_of, int32_t *__restrict__ src_of)
 {
     extern __shared__ int base[];
+    pdl_wait();
+    pdl_launch_dependents();
     const int w = threadIdx.x / 32, lane = (int)lane_id();
     const int c = blockIdx.x * kChunkWarps + w;
     if (c >= nchunks) return;
@@ -162,6 +168,8 @@ dispatch_gather_kernel(const uint8_t *__restrict__ x, int64_t rows,
 {
     const int lane = (int)lane_id();
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
+    pdl_wait();
+    pdl_launch_dependents();
     for (int64_t r = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
          r < rows; r += warps) {
         const int32_t a = src_of[r];
@@ -202,12 +210,15 @@ cudaError_t launch_dispatch(const uint32_t *idx, int64_t T, int top_k, int E,
     int *chunk = static_cast<int *>(ws);
     const int blocks = (p.nchunks + kChunkWarps - 1) / kChunkWarps;
     const size_t hist_bytes = (size_t)kChunkWarps * E * sizeof(int);
-    dispatch_count_kernel<<<blocks, kChunkWarps * 32, hist_bytes, s>>>(
-        idx, A, E, p.chunk, p.nchunks, chunk, status);
-    dispatch_scan_kernel<<<1, 1024, 0, s>>>(chunk, p.nchunks, E, A, counts,
-                                           offsets, src_of);
-    dispatch_rank_kernel<<<blocks, kChunkWarps * 32, hist_bytes, s>>>(
-        idx, A, E, p.chunk, p.nchunks, chunk, row_of, src_of);
+    cudaError_t err = launch_pdl(dispatch_count_kernel, dim3(blocks), dim3(kChunkWarps * 32),
+                                 hist_bytes, s, idx, A, E, p.chunk, p.nchunks, chunk, status);
+    if (err != cudaSuccess) return err;
+    err = launch_pdl(dispatch_scan_kernel, dim3(1), dim3(1024), 0, s, chunk, p.nchunks, E, A,
+                     counts, offsets, src_of);
+    if (err != cudaSuccess) return err;
+    err = launch_pdl(dispatch_rank_kernel, dim3(blocks), dim3(kChunkWarps * 32), hist_bytes, s,
+                     idx, A, E, p.chunk, p.nchunks, (const int *)chunk, row_of, src_of);
+    if (err != cudaSuccess) return err;
     const int64_t row_bytes = H * (xdt == DT_F32 ? 4 : 2);
     int64_t gblocks = (A + 7) / 8;
     const int64_t cap = (int64_t)device_sm_count() * 16;
@@ -215,14 +226,15 @@ cudaError_t launch_dispatch(const uint32_t *idx, int64_t T, int top_k, int E,
     const bool vec = (row_bytes % 16 == 0) &&
                      (reinterpret_cast<uintptr_t>(x) % 16 == 0) &&
                      (reinterpret_cast<uintptr_t>(x_disp) % 16 == 0);
+    const uint8_t *xb = static_cast<const uint8_t *>(x);
+    uint8_t *xd = static_cast<uint8_t *>(x_disp);
     if (vec)
-        dispatch_gather_kernel<true><<<(unsigned)gblocks, 256, 0, s>>>(
-            static_cast<const uint8_t *>(x), A, row_bytes, top_k, src_of,
-            static_cast<uint8_t *>(x_disp));
+        err = launch_pdl(dispatch_gather_kernel<true>, dim3((unsigned)gblocks), dim3(256), 0, s,
+                         xb, A, row_bytes, top_k, (const int32_t *)src_of, xd);
     else
-        dispatch_gather_kernel<false><<<(unsigned)gblocks, 256, 0, s>>>(
-            static_cast<const uint8_t *>(x), A, row_bytes, top_k, src_of,
-            static_cast<uint8_t *>(x_disp));
+        err = launch_pdl(dispatch_gather_kernel<false>, dim3((unsigned)gblocks), dim3(256), 0, s,
+                         xb, A, row_bytes, top_k, (const int32_t *)src_of, xd);
+    if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
 

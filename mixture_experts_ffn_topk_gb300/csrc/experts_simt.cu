@@ -31,6 +31,8 @@ experts_simt_kernel(const float *__restrict__ A, const int32_t *__restrict__ off
     __shared__ float As[SBK][SBM + 4];
     __shared__ float Bs[SBK][SBN + 4];
     __shared__ float Us[SWIGLU ? SBK : 1][SWIGLU ? SBN + 4 : 1];
+    pdl_wait();
+    pdl_launch_dependents();
 
     // prefix[e] = number of tiles of experts < e (block scan over experts)
     const int per = (E + STHREADS - 1) / STHREADS;
@@ -151,14 +153,15 @@ cudaError_t launch_experts_simt(const float *x_disp, const int32_t *offsets,
     const int nt1 = (int)((I + SBN - 1) / SBN);
     int64_t g1 = tile_upper_bound(rows, E, nt1);
     if (g1 > cap) g1 = cap;
-    experts_simt_kernel<true><<<(unsigned)g1, STHREADS, 0, s>>>(
-        x_disp, offsets, E, gate, up, (int)I, (int)H, nt1, h_ws);
+    cudaError_t err = launch_pdl(experts_simt_kernel<true>, dim3((unsigned)g1), dim3(STHREADS), 0,
+                                 s, x_disp, offsets, E, gate, up, (int)I, (int)H, nt1, h_ws);
+    if (err != cudaSuccess) return err;
     const int nt2 = (int)((H + SBN - 1) / SBN);
     int64_t g2 = tile_upper_bound(rows, E, nt2);
     if (g2 > cap) g2 = cap;
-    experts_simt_kernel<false><<<(unsigned)g2, STHREADS, 0, s>>>(
-        h_ws, offsets, E, down, nullptr, (int)H, (int)I, nt2, out_disp);
-    return cudaGetLastError();
+    return launch_pdl(experts_simt_kernel<false>, dim3((unsigned)g2), dim3(STHREADS), 0, s,
+                      (const float *)h_ws, offsets, E, down, (const float *)nullptr, (int)H,
+                      (int)I, nt2, out_disp);
 }
 
 }  // namespace moe

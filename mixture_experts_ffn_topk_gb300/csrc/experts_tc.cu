@@ -278,7 +278,6 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     constexpr int N_OUT = SWIGLU ? BN / 2 : BN;      // output columns per tile
     const int num_kb = (K + BK - 1) / BK;
 
-    for (int i = threadIdx.x; i <= E; i += THREADS) S.offs[i] = offsets[i];
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) { mbar_init(&S.full[s], 1); mbar_init(&S.empty[s], 1); }
         for (int a = 0; a < 2; ++a) { mbar_init(&S.acc_full[a], 1); mbar_init(&S.acc_empty[a], 4); }
@@ -290,6 +289,11 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         tmem_alloc(&S.tmem_base, TMEM_COLS);
         tmem_relinquish();
     }
+    // everything above is CTA-local; the offsets and operands come from the
+    // previous kernels on the stream
+    pdl_wait();
+    pdl_launch_dependents();
+    for (int i = threadIdx.x; i <= E; i += THREADS) S.offs[i] = offsets[i];
     __syncthreads();
     if (warp == 0) {
         // prefix[e] = tiles of experts < e; lane l owns a contiguous run of experts
@@ -581,14 +585,18 @@ cudaError_t launch_tc_dt(const void *x_disp, const int32_t *offsets, int64_t row
     int64_t g2 = tc_tile_upper_bound(rows, E, nt2);
     if (g1 > sms) g1 = sms;
     if (g2 > sms) g2 = sms;
-    grouped_gemm_tc_kernel<DT, true, false><<<(unsigned)g1, THREADS, kSmemBytes, s>>>(
-        mx, mg, mu, offsets, E, (int)I, (int)H, nt1, h_ws, status);
+    err = launch_pdl(grouped_gemm_tc_kernel<DT, true, false>, dim3((unsigned)g1), dim3(THREADS),
+                     kSmemBytes, s, mx, mg, mu, offsets, E, (int)I, (int)H, nt1, h_ws, status);
+    if (err != cudaSuccess) return err;
     if (out_f32)
-        grouped_gemm_tc_kernel<DT, false, true><<<(unsigned)g2, THREADS, kSmemBytes, s>>>(
-            mh, md, md, offsets, E, (int)H, (int)I, nt2, out_disp, status);
+        err = launch_pdl(grouped_gemm_tc_kernel<DT, false, true>, dim3((unsigned)g2),
+                         dim3(THREADS), kSmemBytes, s, mh, md, md, offsets, E, (int)H, (int)I,
+                         nt2, out_disp, status);
     else
-        grouped_gemm_tc_kernel<DT, false, false><<<(unsigned)g2, THREADS, kSmemBytes, s>>>(
-            mh, md, md, offsets, E, (int)H, (int)I, nt2, out_disp, status);
+        err = launch_pdl(grouped_gemm_tc_kernel<DT, false, false>, dim3((unsigned)g2),
+                         dim3(THREADS), kSmemBytes, s, mh, md, md, offsets, E, (int)H, (int)I,
+                         nt2, out_disp, status);
+    if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
 

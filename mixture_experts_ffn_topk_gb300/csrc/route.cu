@@ -41,6 +41,8 @@ route_kernel(const void *__restrict__ logits, int64_t T, int E, int top_k,
     ET *W = static_cast<ET *>(w_out);
     const int lane = (int)lane_id();
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
+    pdl_wait();
+    pdl_launch_dependents();
 
     for (int64_t t = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
          t < T; t += warps) {
@@ -138,13 +140,12 @@ cudaError_t launch_route_dt(const void *logits, int64_t T, int E, int top_k,
     if (blocks > cap) blocks = cap;
     const dim3 grid((unsigned)blocks), block(kRouteThreads);
     const int epl = (E + 31) / 32;
-    if (epl <= 1) route_kernel<1, LDT><<<grid, block, 0, s>>>(logits, T, E, top_k, renorm, idx, w);
-    else if (epl <= 2) route_kernel<2, LDT><<<grid, block, 0, s>>>(logits, T, E, top_k, renorm, idx, w);
-    else if (epl <= 4) route_kernel<4, LDT><<<grid, block, 0, s>>>(logits, T, E, top_k, renorm, idx, w);
-    else if (epl <= 8) route_kernel<8, LDT><<<grid, block, 0, s>>>(logits, T, E, top_k, renorm, idx, w);
-    else if (epl <= 16) route_kernel<16, LDT><<<grid, block, 0, s>>>(logits, T, E, top_k, renorm, idx, w);
-    else route_kernel<32, LDT><<<grid, block, 0, s>>>(logits, T, E, top_k, renorm, idx, w);
-    return cudaGetLastError();
+    if (epl <= 1) return launch_pdl(route_kernel<1, LDT>, grid, block, 0, s, logits, T, E, top_k, renorm, idx, w);
+    else if (epl <= 2) return launch_pdl(route_kernel<2, LDT>, grid, block, 0, s, logits, T, E, top_k, renorm, idx, w);
+    else if (epl <= 4) return launch_pdl(route_kernel<4, LDT>, grid, block, 0, s, logits, T, E, top_k, renorm, idx, w);
+    else if (epl <= 8) return launch_pdl(route_kernel<8, LDT>, grid, block, 0, s, logits, T, E, top_k, renorm, idx, w);
+    else if (epl <= 16) return launch_pdl(route_kernel<16, LDT>, grid, block, 0, s, logits, T, E, top_k, renorm, idx, w);
+    return launch_pdl(route_kernel<32, LDT>, grid, block, 0, s, logits, T, E, top_k, renorm, idx, w);
 }
 
 }  // namespace
