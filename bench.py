@@ -212,6 +212,8 @@ def run_ours(args, rank, world, local, dist):
 
     if args.workload == W.COMBINE_NORM.name:
         return run_combine_norm(args, rank, world, local, dist, dev, peaks, flush)
+    if args.workload == "routing_sweep":
+        return run_routing_sweep(args, world, dist, dev, peaks, flush)
 
     cfg = W.CONFIGS[args.workload]
     d = W.moe_inputs(cfg, device=dev, seed=cfg.seed + 1000 * rank)
@@ -381,6 +383,63 @@ def timed_loop(fn, args, stream, flush):
         flush.fill_(1)
     torch.cuda.synchronize()
     return statistics.mean(a.elapsed_time(b) for a, b in pairs)
+
+
+def run_routing_sweep(args, world, dist, dev, peaks, flush):
+    """Route and dispatch alone, on the fine prefill's routing shape (E=64,
+    top_k=6, BF16 logits N(0,1)) at growing T, to show where they leave the
+    launch-bound regime. Dispatch carries 8-element rows so its gather is
+    small; its algorithmic bytes are the indices read once, the two maps
+    written, and the gathered rows."""
+    import mixture_experts_ffn_topk_gb300 as moe
+    from mixture_experts_ffn_topk_gb300 import workloads as W
+    base = W.CONFIGS["fine_prefill_bf16"]
+    stream = torch.cuda.current_stream(dev)
+    E, k, Hs = base.E, base.top_k, 8
+    rows = []
+    with ClockSampler(dev) as clk:
+        for T in (4096, 65536, 1 << 20):
+            cfg = base.scaled(T=T, H=Hs, I=8)
+            d = W.moe_inputs(cfg, device=dev)
+            logits, x = d["logits"], d["x"]
+            idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+            w = torch.empty((T, k), dtype=logits.dtype, device=dev)
+            A = T * k
+            bufs = {"counts": torch.empty(E, dtype=torch.int32, device=dev),
+                    "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
+                    "row_of": torch.empty(A, dtype=torch.int32, device=dev),
+                    "src_of": torch.empty(A, dtype=torch.int32, device=dev),
+                    "x_disp": torch.empty((A, Hs), dtype=x.dtype, device=dev),
+                    "workspace": torch.empty(moe.moe_dispatch_workspace_size(T, k, E),
+                                             dtype=torch.uint8, device=dev)}
+            r_ms = timed_loop(lambda: moe.moe_route(logits, k, False, expert_indices=idx,
+                                                    weights=w), args, stream, flush)
+            d_ms = timed_loop(lambda: moe.moe_dispatch(idx, x, E, **bufs), args, stream, flush)
+            r_bytes = T * E * 2 + A * (4 + 2)
+            d_bytes = A * 12 + E * 8 + T * Hs * 2 + A * Hs * 2
+            rows.append({"T": T, "route_us": r_ms * 1e3,
+                         "route_frac_hbm": r_bytes / (r_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                         "dispatch_us": d_ms * 1e3,
+                         "dispatch_frac_hbm": d_bytes / (d_ms / 1e3) / 1e9 / peaks["hbm_gbs"]})
+    if moe.moe_device_status() != 0:
+        raise RuntimeError("device status error in the routing sweep")
+    big = rows[-1]
+    T = big["T"]
+    return {"metric": METRIC, "value": T * world / (big["route_us"] + big["dispatch_us"]) * 1e6,
+            "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": (big["route_us"] + big["dispatch_us"]) / 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded)",
+            "config": {"workload": "routing_sweep", "E": E, "top_k": k, "logits_dtype": "bf16",
+                       "l2": "flushed between steps (256 MiB write)"},
+            "sweep": rows,
+            "roofline": {"bound": "hbm", "kernel": "route (T = 2^20)",
+                         "achieved": big["route_frac_hbm"] * peaks["hbm_gbs"],
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": big["route_frac_hbm"], "peak_source": peaks["source"],
+                         "traffic": None},
+            "gpu_launches": 5 * len(rows) * (args.steps + max(1, args.warmup)),
+            "clocks": clk.summary()}
 
 
 def run_combine_norm(args, rank, world, local, dist, dev, peaks, flush):

@@ -141,10 +141,11 @@ int moe_dispatch(const uint32_t *expert_indices, int64_t T, int top_k,
  *
  * Arguments, outputs, ordering and errors are those of moe_dispatch, minus
  * the workspace: the scratch lives in a 256 KiB array that the library owns
- * on each device (kept until the process exits). It fits the per-chunk
- * histograms when ceil(T*top_k / chunk) * E <= 65536 counters, i.e. any
- * T*top_k with E <= 512, and E up to 1024 while T*top_k <= 16384; larger
- * problems return MOE_ERR_WORKSPACE before anything is enqueued.
+ * on each device (kept until the process exits). It serves every problem
+ * whose moe_dispatch_workspace_size(T, top_k, E) is at most 256 KiB (on a
+ * 152-SM GB300 that covers, for example, every T*top_k <= 65536 with
+ * E <= 256 and every T*top_k <= 16384 with E <= 1024); larger problems
+ * return MOE_ERR_WORKSPACE before anything is enqueued.
  * The library allocates nothing for this call. The first call on a device
  * looks up the array's device address (cudaGetSymbolAddress) and caches it;
  * make that first call before any stream capture. Every call on a device

@@ -18,8 +18,8 @@
 namespace moe {
 namespace {
 
-// The built-in scratch: 256 KiB, i.e. nchunks * E <= 65536 histogram
-// counters. Every GPU on which the library is loaded holds this array until
+// The built-in scratch: 256 KiB of per-chunk histogram counters (the size
+// moe_dispatch_workspace_size reports must not exceed it). Every GPU on which the library is loaded holds this array until
 // the process exits.
 constexpr size_t kNoAllocScratchBytes = 256u * 1024u;
 static __device__ __align__(256) unsigned char g_dispatch_scratch[kNoAllocScratchBytes];
@@ -58,7 +58,7 @@ extern "C" int moe_dispatch_noalloc(const uint32_t *expert_indices, int64_t T, i
     if (need > moe::kNoAllocScratchBytes)
         return moe::report_error(MOE_ERR_WORKSPACE,
                                  "moe_dispatch_noalloc: this T*top_k and E need more than the "
-                                 "256 KiB built-in scratch (chunks x E x 4 bytes); use "
+                                 "256 KiB built-in scratch (moe_dispatch_workspace_size); use "
                                  "moe_dispatch with a workspace");
     if (need == 0)   // T == 0 or invalid T/top_k/E: moe_dispatch validates and returns
         return moe_dispatch(expert_indices, T, top_k, E, x, x_dtype, H, counts, offsets,

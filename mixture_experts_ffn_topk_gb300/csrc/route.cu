@@ -5,11 +5,14 @@
 // renormalisation, then a cast to the logits dtype; rows holding NaN, +inf or
 // only -inf keep NaN weights.
 //
-// Each lane keeps EPL = ceil(E/32) logits in registers (expert e lives in lane
-// e % 32, slot e / 32). The softmax max and sum are warp reductions. The k
-// selections are k rounds of a warp-wide argmax over (logit desc, id asc):
-// ranking by the FP32 logit is ranking by the exact softmax, and it makes the
-// chosen ids independent of exp rounding. Weights are summed in slot order.
+// A group of G lanes (G = 1..32, a power of two) routes one token, so a warp
+// routes 32/G tokens at once; lane r of a group holds logits r*EPL ..
+// r*EPL+EPL-1 in registers (G*EPL >= E, EPL <= 32), so a group reads one
+// contiguous row. The softmax max and sum are shuffle reductions inside the
+// group. The k selections are k rounds of a group-wide argmax over
+// (logit desc, id asc): ranking by the FP32 logit is ranking by the exact
+// softmax, and it makes the chosen ids independent of exp rounding. Weights are
+// summed in slot order. G is picked so that EPL <= 8 where E allows it.
 #include <limits.h>
 
 #include "common.cuh"
@@ -30,7 +33,23 @@ __device__ __forceinline__ bool ranks_before(float la, int ea, float lb, int eb)
     return la > lb || (la == lb && ea < eb);
 }
 
-template <int EPL, int LDT>
+// OR / AND / max / sum over the G lanes of a group (xor offsets < G stay in it).
+template <int G>
+__device__ __forceinline__ int group_or(int v)
+{
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) v |= __shfl_xor_sync(kFull, v, o);
+    return v;
+}
+template <int G>
+__device__ __forceinline__ int group_and(int v)
+{
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) v &= __shfl_xor_sync(kFull, v, o);
+    return v;
+}
+
+template <int G, int EPL, int LDT>
 __global__ void __launch_bounds__(kRouteThreads)
 route_kernel(const void *__restrict__ logits, int64_t T, int E, int top_k,
              int renormalize, uint32_t *__restrict__ idx_out,
@@ -39,19 +58,28 @@ route_kernel(const void *__restrict__ logits, int64_t T, int E, int top_k,
     using ET = typename Elem<LDT>::T;
     const ET *L = static_cast<const ET *>(logits);
     ET *W = static_cast<ET *>(w_out);
+    constexpr int TPW = 32 / G;                          // tokens per warp
+    // per warp: TPW tokens x (G*EPL >= top_k) selected probabilities
+    __shared__ float sp[kRouteThreads / 32][32 * EPL];
     const int lane = (int)lane_id();
-    const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
+    const int r = lane % G, gbase = lane - r;            // lane in group, group's first lane
+    const int64_t slots = (int64_t)gridDim.x * (blockDim.x / 32) * TPW;
     pdl_wait();
     pdl_launch_dependents();
 
-    for (int64_t t = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-         t < T; t += warps) {
+    // the loop is uniform across the warp: groups past T work on a clamped
+    // token and store nothing, so every shuffle sees the full warp
+    for (int64_t t0 = ((int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32) * TPW;
+         t0 < T; t0 += slots) {
+        const int64_t t_raw = t0 + lane / G;
+        const bool live = t_raw < T;
+        const int64_t t = live ? t_raw : T - 1;
         float l[EPL];
-        unsigned avail = 0;  // bit i: expert lane + 32 i exists, not yet taken
-        bool bad = false, all_ninf = true;
+        unsigned avail = 0;  // bit i: expert r*EPL + i exists, not yet taken
+        int bad = 0, all_ninf = 1;
 #pragma unroll
         for (int i = 0; i < EPL; ++i) {
-            const int e = lane + 32 * i;
+            const int e = r * EPL + i;
             l[i] = -INFINITY;
             if (e < E) {
                 l[i] = Elem<LDT>::to_f(L[t * E + e]);
@@ -60,36 +88,35 @@ route_kernel(const void *__restrict__ logits, int64_t T, int E, int top_k,
                 all_ninf &= (l[i] == -INFINITY);
             }
         }
-        bad = __any_sync(kFull, bad);
-        all_ninf = __all_sync(kFull, all_ninf);
-        if (bad || all_ninf) {
-            for (int j = lane; j < top_k; j += 32) {
-                idx_out[t * top_k + j] = (uint32_t)j;
-                W[t * top_k + j] = Elem<LDT>::from_f(__int_as_float(0x7fc00000));
-            }
-            continue;
-        }
+        // both group votes run on every lane: a short-circuit here would let
+        // part of the warp skip a full-mask shuffle
+        const int any_bad = group_or<G>(bad);
+        const int every_ninf = group_and<G>(all_ninf);
+        const bool invalid = any_bad || every_ninf;
 
-        // FP32 softmax statistics over all E experts.
+        // FP32 softmax over all E experts: exp(l - max) once per expert (as
+        // exp2 of the scaled difference), kept for the selected ones
         float m = -INFINITY;
 #pragma unroll
         for (int i = 0; i < EPL; ++i)
             if (avail >> i & 1u) m = fmaxf(m, l[i]);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+        for (int o = G / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+        constexpr float kLog2e = 1.4426950408889634f;
+        float ex[EPL];
         float s = 0.0f;
 #pragma unroll
-        for (int i = 0; i < EPL; ++i)
-            if (avail >> i & 1u) s += expf(l[i] - m);
+        for (int i = 0; i < EPL; ++i) {
+            ex[i] = (avail >> i & 1u) ? exp2f((l[i] - m) * kLog2e) : 0.0f;
+            s += ex[i];
+        }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
+        for (int o = G / 2; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
+        const float inv_s = 1.0f / s;
 
-        // k rounds of warp argmax. Slot j of the output lives in lane j % 32,
-        // register j / 32.
-        int sel_e[EPL];
-        float sel_p[EPL];
-#pragma unroll
-        for (int i = 0; i < EPL; ++i) { sel_e[i] = 0; sel_p[i] = 0.0f; }
+        // k rounds of a group argmax; ids go straight to the output, the
+        // selected probabilities wait in shared memory for their sum
+        float *pw = sp[threadIdx.x / 32] + (lane / G) * (G * EPL);
         float z = 0.0f;
         for (int j = 0; j < top_k; ++j) {
             float bl = -INFINITY;
@@ -98,54 +125,72 @@ route_kernel(const void *__restrict__ logits, int64_t T, int E, int top_k,
             for (int i = 0; i < EPL; ++i)
                 if ((avail >> i & 1u) && (be == INT_MAX || l[i] > bl)) {
                     bl = l[i];
-                    be = lane + 32 * i;
+                    be = r * EPL + i;
                 }
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
+            for (int o = G / 2; o > 0; o >>= 1) {
                 const float ol = __shfl_xor_sync(kFull, bl, o);
                 const int oe = __shfl_xor_sync(kFull, be, o);
                 if (ranks_before(ol, oe, bl, be)) { bl = ol; be = oe; }
             }
-            const int owner = be & 31, slot = be >> 5;
+            // an invalid row may have no candidate left; its results are
+            // replaced below, so any in-range owner will do
+            const int eb = be == INT_MAX ? 0 : be;
+            const int owner = eb / EPL, slot = eb % EPL;
             float mine = 0.0f;
-            if (lane == owner) {
+            if (r == owner) {
                 avail &= ~(1u << slot);
-                mine = expf(bl - m) / s;
+#pragma unroll
+                for (int i = 0; i < EPL; ++i)
+                    if (i == slot) mine = ex[i] * inv_s;
             }
-            const float p = __shfl_sync(kFull, mine, owner);
+            const float p = __shfl_sync(kFull, mine, gbase + owner);
             z += p;
-#pragma unroll
-            for (int i = 0; i < EPL; ++i)
-                if ((j >> 5) == i && (j & 31) == lane) { sel_e[i] = be; sel_p[i] = p; }
-        }
-#pragma unroll
-        for (int i = 0; i < EPL; ++i) {
-            const int j = lane + 32 * i;
-            if (j < top_k) {
-                idx_out[t * top_k + j] = (uint32_t)sel_e[i];
-                const float w = renormalize ? sel_p[i] / z : sel_p[i];
-                W[t * top_k + j] = Elem<LDT>::from_f(w);
+            if (r == j % G) {
+                pw[j] = p;
+                if (live && !invalid) idx_out[t * top_k + j] = (uint32_t)eb;
             }
         }
+        __syncwarp();
+        if (live) {
+            for (int j = r; j < top_k; j += G) {
+                if (invalid) {
+                    idx_out[t * top_k + j] = (uint32_t)j;
+                    W[t * top_k + j] = Elem<LDT>::from_f(__int_as_float(0x7fc00000));
+                } else {
+                    const float w = renormalize ? pw[j] / z : pw[j];
+                    W[t * top_k + j] = Elem<LDT>::from_f(w);
+                }
+            }
+        }
+        __syncwarp();   // pw is reused by the next token of this group
     }
+}
+
+template <int G, int EPL, int LDT>
+cudaError_t launch_route_cfg(const void *logits, int64_t T, int E, int top_k, int renorm,
+                             uint32_t *idx, void *w, cudaStream_t s)
+{
+    const int64_t tokens_per_block = (kRouteThreads / 32) * (32 / G);
+    int64_t blocks = (T + tokens_per_block - 1) / tokens_per_block;
+    const int64_t cap = (int64_t)device_sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    return launch_pdl(route_kernel<G, EPL, LDT>, dim3((unsigned)blocks), dim3(kRouteThreads), 0,
+                      s, logits, T, E, top_k, renorm, idx, w);
 }
 
 template <int LDT>
 cudaError_t launch_route_dt(const void *logits, int64_t T, int E, int top_k,
                             int renorm, uint32_t *idx, void *w, cudaStream_t s)
 {
-    const int warps_per_block = kRouteThreads / 32;
-    int64_t blocks = (T + warps_per_block - 1) / warps_per_block;
-    const int64_t cap = (int64_t)device_sm_count() * 8;
-    if (blocks > cap) blocks = cap;
-    const dim3 grid((unsigned)blocks), block(kRouteThreads);
-    const int epl = (E + 31) / 32;
-    if (epl <= 1) return launch_pdl(route_kernel<1, LDT>, grid, block, 0, s, logits, T, E, top_k, renorm, idx, w);
-    else if (epl <= 2) return launch_pdl(route_kernel<2, LDT>, grid, block, 0, s, logits, T, E, top_k, renorm, idx, w);
-    else if (epl <= 4) return launch_pdl(route_kernel<4, LDT>, grid, block, 0, s, logits, T, E, top_k, renorm, idx, w);
-    else if (epl <= 8) return launch_pdl(route_kernel<8, LDT>, grid, block, 0, s, logits, T, E, top_k, renorm, idx, w);
-    else if (epl <= 16) return launch_pdl(route_kernel<16, LDT>, grid, block, 0, s, logits, T, E, top_k, renorm, idx, w);
-    return launch_pdl(route_kernel<32, LDT>, grid, block, 0, s, logits, T, E, top_k, renorm, idx, w);
+    if (E <= 8) return launch_route_cfg<1, 8, LDT>(logits, T, E, top_k, renorm, idx, w, s);
+    if (E <= 16) return launch_route_cfg<2, 8, LDT>(logits, T, E, top_k, renorm, idx, w, s);
+    if (E <= 32) return launch_route_cfg<4, 8, LDT>(logits, T, E, top_k, renorm, idx, w, s);
+    if (E <= 64) return launch_route_cfg<8, 8, LDT>(logits, T, E, top_k, renorm, idx, w, s);
+    if (E <= 128) return launch_route_cfg<16, 8, LDT>(logits, T, E, top_k, renorm, idx, w, s);
+    if (E <= 256) return launch_route_cfg<32, 8, LDT>(logits, T, E, top_k, renorm, idx, w, s);
+    if (E <= 512) return launch_route_cfg<32, 16, LDT>(logits, T, E, top_k, renorm, idx, w, s);
+    return launch_route_cfg<32, 32, LDT>(logits, T, E, top_k, renorm, idx, w, s);
 }
 
 }  // namespace

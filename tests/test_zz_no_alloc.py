@@ -83,7 +83,7 @@ def test_noalloc_matches_dispatch_on_two_calls(lib):
 
 def test_noalloc_refuses_sizes_beyond_its_scratch(lib):
     dev = torch.device("cuda:0")
-    T, k, E, H = 8192, 8, 1024, 8       # 128 chunks x 1024 experts > 65536 counters
+    T, k, E, H = 32768, 8, 1024, 8      # 128 chunks x 1024 experts > 65536 counters
     idx = torch.zeros((T, k), dtype=torch.int32, device=dev)
     x = torch.zeros((T, H), dtype=torch.bfloat16, device=dev)
     out = _outputs(T, k, E, H, x.dtype, dev)
