@@ -244,9 +244,15 @@ int moe_combine_add_rmsnorm(const void *out_disp, int out_dtype,
  *   y       [T, H] in dtype, written.
  *   workspace moe_forward_workspace_size(...) bytes; it holds the routing
  *           plan, the dispatch map and the dispatched activations.
- * Same rules and errors as the staged calls; the result equals
+ * Same rules and errors as the staged calls, and the same arithmetic as
  * moe_route -> moe_dispatch -> moe_experts_forward (out_dtype MOE_F32) ->
- * moe_combine: expert outputs reach the combine unrounded. Needs H % 8 == 0.
+ * moe_combine: expert outputs reach the combine unrounded. For BF16/F16 with
+ * T*H*4 <= 64 MiB (an accumulator that stays in L2) the combine runs inside
+ * the second expert GEMM, which adds each weighted row into an FP32 [T, H]
+ * accumulator with reductions whose order varies from run to run, so
+ * repeated calls may differ by one unit in the last place of an output.
+ * Otherwise, for FP32 runs, and for the staged calls the result is
+ * bit-reproducible. Needs H % 8 == 0.
  */
 size_t moe_forward_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E,
                                   int top_k, int dtype, int logits_dtype);

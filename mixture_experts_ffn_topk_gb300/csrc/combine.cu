@@ -227,7 +227,40 @@ cudaError_t launch_norm(const void *out_disp, int odt, const void *w, int wdt,
 #undef MOE_TYPED
 }
 
+// y = y_acc (FP32) rounded to YDT, 8 elements per thread and step.
+template <int YDT>
+__global__ void __launch_bounds__(256)
+finalize_kernel(const float *__restrict__ y_acc, int64_t groups, void *__restrict__ y)
+{
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < groups; g += stride) {
+        float f[8];
+        load8<DT_F32>(y_acc, g, f);
+        store8<YDT>(y, g, f);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_finalize(const float *y_acc, int64_t T, int64_t H, void *y, int ydt,
+                            cudaStream_t s)
+{
+    const int64_t groups = T * H / 8;
+    if (groups == 0) return cudaSuccess;
+    int64_t blocks = (groups + 255) / 256;
+    const int64_t cap = (int64_t)device_sm_count() * 16;
+    if (blocks > cap) blocks = cap;
+    if (ydt == DT_BF16)
+        return launch_pdl(finalize_kernel<DT_BF16>, dim3((unsigned)blocks), dim3(256), 0, s,
+                          y_acc, groups, y);
+    if (ydt == DT_F16)
+        return launch_pdl(finalize_kernel<DT_F16>, dim3((unsigned)blocks), dim3(256), 0, s,
+                          y_acc, groups, y);
+    return launch_pdl(finalize_kernel<DT_F32>, dim3((unsigned)blocks), dim3(256), 0, s, y_acc,
+                      groups, y);
+}
 
 // With the norm the whole row must fit one pass: 8 groups x 256 threads.
 int combine_max_h(bool norm)

@@ -88,7 +88,9 @@ __device__ __forceinline__ uint64_t global_timer_ns()
 // previous kernel on the stream drains; it calls pdl_wait() before its first
 // global-memory access (which returns once the previous grid has completed and
 // its writes are visible) and pdl_launch_dependents() to let the next kernel
-// start early in turn. Launched without the attribute, both are no-ops.
+// start early in turn -- at entry for short kernels, after the main loop for
+// bandwidth-heavy ones whose occupancy the next kernel's resident CTAs would
+// cut. Launched without the attribute, both are no-ops.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents()
 {

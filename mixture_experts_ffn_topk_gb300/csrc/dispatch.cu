@@ -213,8 +213,9 @@ dispatch_gather_rows_kernel(const uint4 *__restrict__ x, int64_t rows, int64_t p
                             int top_k, const int32_t *__restrict__ src_of,
                             uint4 *__restrict__ x_disp)
 {
+    // the next kernel (the first expert GEMM) is not let in before this
+    // copy ends: its resident CTAs would take registers from the copy
     pdl_wait();
-    pdl_launch_dependents();
     const int lane = (int)lane_id();
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
     for (int64_t r = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; r < rows;
@@ -226,6 +227,7 @@ dispatch_gather_rows_kernel(const uint4 *__restrict__ x, int64_t rows, int64_t p
 #pragma unroll 4
         for (int64_t v = lane; v < per_row; v += 32) dst[v] = __ldg(src + v);
     }
+    pdl_launch_dependents();
 }
 
 template <bool VEC>
@@ -236,7 +238,6 @@ dispatch_gather_kernel(const uint8_t *__restrict__ x, int64_t rows,
                        uint8_t *__restrict__ x_disp)
 {
     pdl_wait();
-    pdl_launch_dependents();
     const int64_t unit = VEC ? 16 : 1;
     const int64_t per_row = row_bytes / unit;
     const int64_t n = rows * per_row;
@@ -252,6 +253,7 @@ dispatch_gather_kernel(const uint8_t *__restrict__ x, int64_t rows,
         else
             x_disp[r * row_bytes + v] = x[t * row_bytes + v];
     }
+    pdl_launch_dependents();
 }
 
 }  // namespace

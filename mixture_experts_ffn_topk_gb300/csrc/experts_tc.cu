@@ -11,7 +11,10 @@
 //                    same output columns; one 128x256x16 MMA computes both;
 //                    the epilogue forms SiLU(g)*u for 128 columns of h.
 //   GEMM2:           B tile = 256 rows of down; the epilogue writes FP32 or
-//                    rounds to dtype (the caller's choice of output type).
+//                    rounds to dtype (the caller's choice of output type), or,
+//                    in the one-call forward, multiplies each row by its
+//                    routing weight and reduces it in FP32 into its token's
+//                    row of y_acc [T, H] (red.global.add.v4.f32; the combine).
 // Per CTA (one per SM, 192 threads):
 //   warp 0  TMA producer: x tile [128 rows x 64 k] and weight tile
 //           [256 rows x 64 k] per stage, 128-byte swizzle, 4 stages;
@@ -57,6 +60,22 @@ constexpr int MAX_E = 1024;
 constexpr uint64_t kDrainLimitNs = 100000000ull;   // 100 ms per teardown drain
 
 constexpr int EPI_ROW_BYTES = 128;           // epilogue staging: 32 rows x 128 B per warp
+
+// What the epilogue does with the accumulator tile.
+enum OutMode : int {
+    kOutDtype = 0,     // rows in the input dtype (h of GEMM1, or expert outputs)
+    kOutF32 = 1,       // rows in FP32 (unrounded expert outputs)
+    kOutCombine = 2,   // routing weight x row, reduced in FP32 into y_acc [T, N]
+};
+
+// kOutCombine: dispatched row r belongs to assignment a = src_of[r], token
+// a / top_k, weight w[a] (dtype wdt).
+struct CombineInto {
+    const int32_t *src_of;
+    const void *w;
+    int wdt;
+    int top_k;
+};
 
 struct __align__(1024) SharedStorage {
     uint8_t stage[STAGES][STAGE_BYTES];      // each stage 1024-byte aligned
@@ -263,13 +282,14 @@ __device__ __forceinline__ uint32_t pack2(float a, float b)
 
 // ---- the kernel -------------------------------------------------------------
 
-template <int DT, bool SWIGLU, bool OUT_F32>
+template <int DT, bool SWIGLU, int OUT>
 __global__ void __launch_bounds__(THREADS, 1)
 grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB0,
                        const __grid_constant__ CUtensorMap tmB1,
                        const int32_t *__restrict__ offsets, int E, int N, int K,
-                       int n_tiles, void *__restrict__ out, unsigned *status)
+                       int n_tiles, void *__restrict__ out, unsigned *status,
+                       CombineInto comb)
 {
     extern __shared__ uint8_t smem_raw[];
     SharedStorage &S = *reinterpret_cast<SharedStorage *>(
@@ -394,7 +414,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         // rows' 128-byte lines, masked to the expert's rows and to N.
         const int q = warp & 3;            // TMEM lane quadrant of this warp
         uint8_t *stg = S.epi[warp - 2];
-        constexpr int ESZ = (OUT_F32 && !SWIGLU) ? 4 : 2;       // output element bytes
+        constexpr bool F32ACC = !SWIGLU && OUT != kOutDtype;   // FP32 values leave the tile
+        constexpr int ESZ = F32ACC ? 4 : 2;                     // output element bytes
         constexpr int RCOLS = EPI_ROW_BYTES / ESZ;              // columns per round
         constexpr int ROUNDS = N_OUT / RCOLS;
         const int64_t out_row_bytes = (int64_t)N * ESZ;
@@ -406,6 +427,16 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             const int seg_rows = S.offs[e + 1] - S.offs[e];
             const int r_base = m * BM + q * 32;                 // this warp's first row in the segment
             uint8_t *out_base = static_cast<uint8_t *>(out) + ((int64_t)S.offs[e] + r_base) * out_row_bytes;
+            // kOutCombine: token and routing weight of this lane's row
+            int row_tok = -1;
+            float row_w = 0.0f;
+            if constexpr (OUT == kOutCombine) {
+                if (r_base + lane < seg_rows) {
+                    const int a = comb.src_of[S.offs[e] + r_base + lane];
+                    row_tok = a / comb.top_k;
+                    row_w = load_as_float(comb.w, comb.wdt, a);
+                }
+            }
             const int acc = it & 1;
             const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
             // every lane waits; the warp leaves together if any lane gave up,
@@ -417,9 +448,14 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll 1
             for (int rd = 0; rd < ROUNDS; ++rd) {
                 uint32_t w[32];                                 // this row's 128 output bytes
-                if constexpr (OUT_F32 && !SWIGLU) {
+                if constexpr (F32ACC) {
                     tmem_ld32(tbase + rd * 32, w);
                     tmem_ld_wait(w);
+                    if constexpr (OUT == kOutCombine) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            w[i] = __float_as_uint(__uint_as_float(w[i]) * row_w);
+                    }
                 } else {
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
@@ -459,8 +495,20 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                     const int rr = 4 * j + (lane >> 3);
                     const uint4 v = *reinterpret_cast<const uint4 *>(
                         stg + rr * EPI_ROW_BYTES + ((cch ^ (rr & 7)) << 4));
-                    if (r_base + rr < seg_rows && col_byte < out_row_bytes)
-                        *reinterpret_cast<uint4 *>(out_base + rr * out_row_bytes + col_byte) = v;
+                    if constexpr (OUT == kOutCombine) {
+                        const int tk = __shfl_sync(0xffffffffu, row_tok, rr);
+                        if (tk >= 0 && col_byte < out_row_bytes) {
+                            float *dst = reinterpret_cast<float *>(
+                                static_cast<uint8_t *>(out) + (int64_t)tk * out_row_bytes + col_byte);
+                            asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst),
+                                         "f"(__uint_as_float(v.x)), "f"(__uint_as_float(v.y)),
+                                         "f"(__uint_as_float(v.z)), "f"(__uint_as_float(v.w))
+                                         : "memory");
+                        }
+                    } else {
+                        if (r_base + rr < seg_rows && col_byte < out_row_bytes)
+                            *reinterpret_cast<uint4 *>(out_base + rr * out_row_bytes + col_byte) = v;
+                    }
                 }
                 __syncwarp();
             }
@@ -538,7 +586,7 @@ bool encode_3d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_
 }
 
 // The dynamic shared-memory opt-in is per device and per kernel instance.
-template <int DT, bool SWIGLU, bool OUT_F32>
+template <int DT, bool SWIGLU, int OUT>
 cudaError_t ensure_smem_attr()
 {
     static std::atomic<uint64_t> done_mask{0};
@@ -547,7 +595,7 @@ cudaError_t ensure_smem_attr()
     if (err != cudaSuccess) return err;
     const uint64_t bit = 1ull << (dev & 63);
     if (done_mask.load() & bit) return cudaSuccess;
-    err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<DT, SWIGLU, OUT_F32>,
+    err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<DT, SWIGLU, OUT>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (err == cudaSuccess) done_mask.fetch_or(bit);
     return err;
@@ -562,8 +610,8 @@ int64_t tc_tile_upper_bound(int64_t rows, int E, int64_t n_tiles)
 template <int DT>
 cudaError_t launch_tc_dt(const void *x_disp, const int32_t *offsets, int64_t rows,
                          const void *gate, const void *up, const void *down, int E,
-                         int64_t H, int64_t I, void *h_ws, void *out_disp, bool out_f32,
-                         unsigned *status, cudaStream_t s)
+                         int64_t H, int64_t I, void *h_ws, void *out, int out_mode,
+                         const CombineInto &comb, unsigned *status, cudaStream_t s)
 {
     const CUtensorMapDataType tdt =
         DT == DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -574,9 +622,12 @@ cudaError_t launch_tc_dt(const void *x_disp, const int32_t *offsets, int64_t row
         !encode_2d(&mh, tdt, h_ws, (uint64_t)I, (uint64_t)rows, BK, BM) ||
         !encode_3d(&md, tdt, down, (uint64_t)I, (uint64_t)H, (uint64_t)E, BK, BN))
         return cudaErrorInvalidValue;
-    cudaError_t err = ensure_smem_attr<DT, true, false>();
-    if (err == cudaSuccess)
-        err = out_f32 ? ensure_smem_attr<DT, false, true>() : ensure_smem_attr<DT, false, false>();
+    cudaError_t err = ensure_smem_attr<DT, true, kOutDtype>();
+    if (err == cudaSuccess) {
+        if (out_mode == kOutF32) err = ensure_smem_attr<DT, false, kOutF32>();
+        else if (out_mode == kOutCombine) err = ensure_smem_attr<DT, false, kOutCombine>();
+        else err = ensure_smem_attr<DT, false, kOutDtype>();
+    }
     if (err != cudaSuccess) return err;
     const int64_t sms = device_sm_count();
     const int nt1 = (int)((I + BN / 2 - 1) / (BN / 2));
@@ -585,19 +636,23 @@ cudaError_t launch_tc_dt(const void *x_disp, const int32_t *offsets, int64_t row
     int64_t g2 = tc_tile_upper_bound(rows, E, nt2);
     if (g1 > sms) g1 = sms;
     if (g2 > sms) g2 = sms;
-    err = launch_pdl(grouped_gemm_tc_kernel<DT, true, false>, dim3((unsigned)g1), dim3(THREADS),
-                     kSmemBytes, s, mx, mg, mu, offsets, E, (int)I, (int)H, nt1, h_ws, status);
+    err = launch_pdl(grouped_gemm_tc_kernel<DT, true, kOutDtype>, dim3((unsigned)g1),
+                     dim3(THREADS), kSmemBytes, s, mx, mg, mu, offsets, E, (int)I, (int)H, nt1,
+                     h_ws, status, comb);
     if (err != cudaSuccess) return err;
-    if (out_f32)
-        err = launch_pdl(grouped_gemm_tc_kernel<DT, false, true>, dim3((unsigned)g2),
+    if (out_mode == kOutF32)
+        err = launch_pdl(grouped_gemm_tc_kernel<DT, false, kOutF32>, dim3((unsigned)g2),
                          dim3(THREADS), kSmemBytes, s, mh, md, md, offsets, E, (int)H, (int)I,
-                         nt2, out_disp, status);
+                         nt2, out, status, comb);
+    else if (out_mode == kOutCombine)
+        err = launch_pdl(grouped_gemm_tc_kernel<DT, false, kOutCombine>, dim3((unsigned)g2),
+                         dim3(THREADS), kSmemBytes, s, mh, md, md, offsets, E, (int)H, (int)I,
+                         nt2, out, status, comb);
     else
-        err = launch_pdl(grouped_gemm_tc_kernel<DT, false, false>, dim3((unsigned)g2),
+        err = launch_pdl(grouped_gemm_tc_kernel<DT, false, kOutDtype>, dim3((unsigned)g2),
                          dim3(THREADS), kSmemBytes, s, mh, md, md, offsets, E, (int)H, (int)I,
-                         nt2, out_disp, status);
-    if (err != cudaSuccess) return err;
-    return cudaGetLastError();
+                         nt2, out, status, comb);
+    return err;
 }
 
 }  // namespace
@@ -609,11 +664,29 @@ cudaError_t launch_experts_tc(int dt, const void *x_disp, const int32_t *offsets
                               cudaStream_t s)
 {
     if (rows == 0) return cudaSuccess;
+    const CombineInto none{nullptr, nullptr, DT_F32, 1};
+    const int mode = out_f32 ? kOutF32 : kOutDtype;
     if (dt == DT_BF16)
         return launch_tc_dt<DT_BF16>(x_disp, offsets, rows, gate, up, down, E, H, I, h_ws,
-                                     out_disp, out_f32, status, s);
-    return launch_tc_dt<DT_F16>(x_disp, offsets, rows, gate, up, down, E, H, I, h_ws,
-                                out_disp, out_f32, status, s);
+                                     out_disp, mode, none, status, s);
+    return launch_tc_dt<DT_F16>(x_disp, offsets, rows, gate, up, down, E, H, I, h_ws, out_disp,
+                                mode, none, status, s);
+}
+
+cudaError_t launch_experts_tc_combine(int dt, const void *x_disp, const int32_t *offsets,
+                                      int64_t rows, const void *gate, const void *up,
+                                      const void *down, int E, int64_t H, int64_t I,
+                                      void *h_ws, const int32_t *src_of, const void *w,
+                                      int wdt, int top_k, float *y_acc, unsigned *status,
+                                      cudaStream_t s)
+{
+    if (rows == 0) return cudaSuccess;
+    const CombineInto comb{src_of, w, wdt, top_k};
+    if (dt == DT_BF16)
+        return launch_tc_dt<DT_BF16>(x_disp, offsets, rows, gate, up, down, E, H, I, h_ws,
+                                     y_acc, kOutCombine, comb, status, s);
+    return launch_tc_dt<DT_F16>(x_disp, offsets, rows, gate, up, down, E, H, I, h_ws, y_acc,
+                                kOutCombine, comb, status, s);
 }
 
 }  // namespace moe

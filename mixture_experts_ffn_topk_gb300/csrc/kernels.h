@@ -54,4 +54,19 @@ cudaError_t launch_experts_tc(int dt, const void *x_disp,
                               void *h_ws, void *out_disp, bool out_f32,
                               unsigned *status, cudaStream_t s);
 
+// Same GEMMs, with the weighted combine folded into GEMM2: every dispatched
+// row r adds w[src_of[r]] * out_r into y_acc[src_of[r] / top_k] (FP32 [T, H],
+// zeroed by the caller), in an order that varies from run to run.
+cudaError_t launch_experts_tc_combine(int dt, const void *x_disp,
+                                      const int32_t *offsets, int64_t rows,
+                                      const void *gate, const void *up,
+                                      const void *down, int E, int64_t H, int64_t I,
+                                      void *h_ws, const int32_t *src_of,
+                                      const void *w, int wdt, int top_k,
+                                      float *y_acc, unsigned *status, cudaStream_t s);
+
+// y = y_acc rounded to ydt ([T, H], H % 8 == 0).
+cudaError_t launch_finalize(const float *y_acc, int64_t T, int64_t H, void *y, int ydt,
+                            cudaStream_t s);
+
 }  // namespace moe

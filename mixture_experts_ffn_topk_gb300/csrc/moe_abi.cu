@@ -108,6 +108,17 @@ int check_combine_args(int odt, int wdt, int dt, int64_t T, int top_k, int64_t H
     return MOE_OK;
 }
 
+// The one-call forward folds the combine into the second expert GEMM (FP32
+// reductions into y_acc [T, H]) when y_acc stays well inside the 129 MB L2;
+// a larger y_acc would turn every reduction into an HBM read-modify-write, so
+// then the expert outputs go to HBM in FP32 and the combine kernel sums them.
+constexpr size_t kFoldCombineMaxBytes = 64u << 20;
+
+bool fold_combine(int64_t T, int64_t H, int dt)
+{
+    return dt != MOE_F32 && (size_t)T * (size_t)H * 4 <= kFoldCombineMaxBytes;
+}
+
 struct ForwardLayout {
     size_t idx, w, counts, offsets, row_of, src_of, disp_ws, x_disp, h, out_disp, total;
 };
@@ -128,7 +139,9 @@ ForwardLayout forward_layout(int64_t T, int64_t H, int64_t I, int64_t E, int top
     L.disp_ws = take(dispatch_workspace_bytes((int64_t)A, (int)E));
     L.x_disp = take(A * (size_t)H * eb);
     L.h = take(A * (size_t)I * eb);
-    L.out_disp = take(A * (size_t)H * 4);   // expert outputs stay FP32
+    // FP32 expert outputs [A, H] for the combine kernel, or y_acc [T, H]
+    // when the combine is folded into the second GEMM
+    L.out_disp = take(fold_combine(T, H, dt) ? (size_t)T * (size_t)H * 4 : A * (size_t)H * 4);
     L.total = off;
     return L;
 }
@@ -336,11 +349,27 @@ int moe_forward(const void *x, int dtype, const void *logits, int logits_dtype, 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t A = T * top_k;
 
-    cudaError_t err = launch_route(logits, logits_dtype, T, (int)E, top_k, renormalize, idx, w, s);
+    const bool fused_combine = fold_combine(T, H, dtype);
+    cudaError_t err = cudaSuccess;
+    if (fused_combine) {
+        err = cudaMemsetAsync(out_disp, 0, (size_t)T * (size_t)H * 4, s);
+        if (err != cudaSuccess) return cuda_fail(err, "moe_forward/zero");
+    }
+    err = launch_route(logits, logits_dtype, T, (int)E, top_k, renormalize, idx, w, s);
     if (err != cudaSuccess) return cuda_fail(err, "moe_forward/route");
     err = launch_dispatch(idx, T, top_k, (int)E, x, dtype, H, counts, offsets, row_of, src_of,
                           x_disp, ws + L.disp_ws, st, s);
     if (err != cudaSuccess) return cuda_fail(err, "moe_forward/dispatch");
+    if (fused_combine) {
+        err = launch_experts_tc_combine(dtype, x_disp, offsets, A, gate, up, down, (int)E, H, I,
+                                        h, src_of, w, logits_dtype, top_k,
+                                        static_cast<float *>(out_disp), st, s);
+        if (err == cudaErrorInvalidValue)
+            return fail(MOE_ERR_ALIGN, "TMA descriptor rejected (pointer alignment or shape)");
+        if (err != cudaSuccess) return cuda_fail(err, "moe_forward/experts");
+        err = launch_finalize(static_cast<const float *>(out_disp), T, H, y, dtype, s);
+        return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_forward/finalize");
+    }
     rc = run_experts(x_disp, offsets, A, gate, up, down, E, H, I, dtype, h, out_disp, MOE_F32, s);
     if (rc != MOE_OK) return rc;
     err = launch_combine(out_disp, MOE_F32, w, logits_dtype, row_of, nullptr, nullptr, MOE_F32,

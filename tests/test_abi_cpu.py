@@ -96,9 +96,14 @@ def test_workspace_sizes(lib):
     assert ws > 0 and ws % 256 == 0
     assert lib.moe_experts_workspace_size(100, 8, 64, 40, BF16) >= 100 * 40 * 2
     assert lib.moe_experts_workspace_size(100, 8, 64, 40, F32) >= 100 * 40 * 4
+    # fine prefill: x_disp and h in BF16, the FP32 [T, H] combine accumulator
     fw = lib.moe_forward_workspace_size(4096, 2048, 1408, 64, 6, BF16, BF16)
     A = 4096 * 6
-    assert fw >= A * (2048 * 2 * 2 + 1408 * 2) + A * (4 + 2 + 4 + 4)
+    assert fw >= A * (2048 * 2 + 1408 * 2) + 4096 * 2048 * 4 + A * (4 + 2 + 4 + 4)
+    # coarse prefill (accumulator past 64 MiB): FP32 expert outputs [T*k, H]
+    fw = lib.moe_forward_workspace_size(16384, 4096, 14336, 8, 2, BF16, F32)
+    A = 16384 * 2
+    assert fw >= A * (4096 * 2 + 14336 * 2 + 4096 * 4)
     assert lib.moe_forward_workspace_size(4096, 2048, 1408, 64, 65, BF16, BF16) == 0
 
 
