@@ -249,9 +249,11 @@ int moe_combine_add_rmsnorm(const void *out_disp, int out_dtype,
  * moe_combine: expert outputs reach the combine unrounded. For BF16/F16 with
  * T*H*4 <= 64 MiB (an accumulator that stays in L2) the combine runs inside
  * the second expert GEMM, which adds each weighted row into an FP32 [T, H]
- * accumulator with reductions whose order varies from run to run, so
- * repeated calls may differ by one unit in the last place of an output.
- * Otherwise, for FP32 runs, and for the staged calls the result is
+ * accumulator with reductions whose order varies from run to run: each FP32
+ * sum is within k * 2^-24 * sum_j |w_j * o_j| of the exact sum, so repeated
+ * calls may differ by that much plus one unit in the last place of the
+ * output dtype (usually at most the one unit; more only where the k terms
+ * cancel). Otherwise, for FP32 runs, and for the staged calls the result is
  * bit-reproducible. Needs H % 8 == 0.
  */
 size_t moe_forward_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E,

@@ -22,6 +22,15 @@
 //           accumulators double-buffered in TMEM (2 x 256 columns);
 //   warps 2-5  epilogue: tcgen05.ld 32 lanes x 32 columns, math, then a
 //           swizzled shared-memory hop so every store writes whole lines.
+// Paired form (CG = 2, a cluster of two CTAs on two SMs): the pair computes
+// a 256 x 256 tile with tcgen05.mma.cta_group::2 (M=256): each CTA holds its
+// own 128 x rows and HALF of the 256 weight rows (the MMA reads the other
+// half from the peer's shared memory), so a stage is 32 KiB per CTA instead
+// of 48 and six stages fit: the load pipeline covers 2.5x more MMA time,
+// which the load-latency-bound prefill GEMMs need. The even CTA issues the
+// MMAs and commits them to both CTAs' barriers; both CTAs' TMA copies
+// complete on the even CTA's stage barrier; both CTAs' epilogues read their
+// own TMEM and release the accumulator on the even CTA's barrier.
 // Tiles: each expert's row segment [offsets[e], offsets[e+1]) is cut into
 // 128-row M-tiles; linear tile ids run over (expert, n-tile, m-tile) with the
 // m-tile fastest, so CTAs working at the same time share weight tiles in L2.
@@ -48,11 +57,17 @@ namespace {
 constexpr int BM = 128;                      // rows per tile (UMMA M)
 constexpr int BK = 64;                       // K per stage: 128 bytes of 16-bit
 constexpr int UK = 16;                       // K per tcgen05.mma kind::f16
-constexpr int BN = 256;                      // B rows per stage (UMMA N)
-constexpr int STAGES = 4;
+constexpr int BN = 256;                      // B rows per tile (UMMA N)
 constexpr int A_BYTES = BM * BK * 2;         // 16 KiB
-constexpr int B_BYTES = BN * BK * 2;         // 32 KiB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+
+// Per-CTA pipeline shape for one CTA per tile (CG = 1) or a CTA pair (CG = 2).
+template <int CG>
+struct Pipe {
+    static constexpr int B_ROWS = BN / CG;                     // weight rows this CTA loads
+    static constexpr int B_BYTES = B_ROWS * BK * 2;            // 32 / 16 KiB
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;      // 48 / 32 KiB
+    static constexpr int STAGES = CG == 2 ? 6 : 4;
+};
 constexpr int ACC_COLS = 256;                // fp32 columns per accumulator
 constexpr int TMEM_COLS = 2 * ACC_COLS;
 constexpr int THREADS = 192;
@@ -77,11 +92,12 @@ struct CombineInto {
     int top_k;
 };
 
+template <int CG>
 struct __align__(1024) SharedStorage {
-    uint8_t stage[STAGES][STAGE_BYTES];      // each stage 1024-byte aligned
+    uint8_t stage[Pipe<CG>::STAGES][Pipe<CG>::STAGE_BYTES];   // each stage 1024-byte aligned
     uint8_t epi[4][32 * EPI_ROW_BYTES];      // per epilogue warp, 16-byte chunks swizzled
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
+    uint64_t full[Pipe<CG>::STAGES];
+    uint64_t empty[Pipe<CG>::STAGES];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t drain;
@@ -91,7 +107,8 @@ struct __align__(1024) SharedStorage {
     int offs[MAX_E + 1];
 };
 
-constexpr size_t kSmemBytes = sizeof(SharedStorage) + 1024;  // + alignment slack
+template <int CG>
+constexpr size_t kSmemBytes = sizeof(SharedStorage<CG>) + 1024;  // + alignment slack
 
 // ---- PTX wrappers ---------------------------------------------------------
 
@@ -128,18 +145,64 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// Same wait with cluster-scope acquire: orders this thread after arrivals
+// released by the peer CTA of a pair.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Address of the same shared-memory variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+// Arrive on an mbarrier that may live in another CTA of the cluster.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// All threads of both CTAs of the cluster.
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
 // Wait for the phase with the given parity to complete. Gives up (false) when
 // another role raised the abort flag, or after limit_ns, which sets ST_TIMEOUT
 // and raises the abort. With abort_flag == nullptr (teardown drains) the wait
 // ignores the flag and only records a timeout.
+template <int CG = 1>
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
                                           volatile int *abort_flag,
                                           unsigned *status, uint64_t limit_ns)
 {
-    if (mbar_try_wait(bar, parity)) return true;
+    auto try_once = [&] {
+        return CG == 2 ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+    };
+    if (try_once()) return true;
     const uint64_t t0 = global_timer_ns();
     for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (try_once()) return true;
         if (abort_flag != nullptr && *abort_flag) return false;
         if (global_timer_ns() - t0 > limit_ns) {
             atomicOr(status, ST_TIMEOUT);
@@ -169,41 +232,102 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
+// TMA copy into this CTA's shared memory that completes on an mbarrier of
+// either CTA of the pair (cluster address of the barrier).
+__device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *map,
+                                                 uint32_t bar_cluster, int c0, int c1)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_pair(void *dst, const CUtensorMap *map,
+                                                 uint32_t bar_cluster, int c0, int c1, int c2)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+// Tensor-memory allocation; with CG = 2 one warp of each CTA of the pair
+// performs it together, and both CTAs get the same columns.
+template <int CG>
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols)
 {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols) : "memory");
+    if constexpr (CG == 2)
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols) : "memory");
+    else
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols) : "memory");
 }
 
+template <int CG>
 __device__ __forceinline__ void tmem_relinquish()
 {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if constexpr (CG == 2)
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    else
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
 
+template <int CG>
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
 {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+    if constexpr (CG == 2)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+    else
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, both K-major, M=128, N=256, K=16.
+// D[tmem] (+)= A[smem] * B[smem]^T, both K-major, K=16; M=128 N=256 on one
+// CTA, or M=256 N=256 over a CTA pair (each CTA: 128 rows of A, 128 rows of
+// B at the same shared-memory offsets, 128 rows of D in its own TMEM).
+template <int CG>
 __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                          uint32_t idesc, uint32_t accumulate)
 {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
+    if constexpr (CG == 2)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+            : "memory");
 }
 
-// Arrive on an mbarrier once every tcgen05 op issued so far by this thread
-// has completed.
+// Arrive on an mbarrier of this CTA once every tcgen05 op issued so far by
+// this thread has completed.
+template <int CG>
 __device__ __forceinline__ void umma_commit(uint64_t *bar)
 {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+    if constexpr (CG == 2)
+        asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+    else
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// The same, arriving on the barrier at this offset in both CTAs of the pair.
+__device__ __forceinline__ void umma_commit_pair(uint64_t *bar)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"((uint16_t)0x3)
+        : "memory");
 }
 
 // 32 TMEM lanes (one per thread of the warp) x 32 consecutive fp32 columns.
@@ -258,7 +382,18 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N)
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void decode_tile(const SharedStorage &S, int E, int tile,
+// M-tile units of one expert: 128-row tiles, or pairs of them (CG = 2).
+template <int CG>
+__device__ __forceinline__ int m_units(int seg_rows)
+{
+    return (seg_rows + BM * CG - 1) / (BM * CG);
+}
+
+// Unit id -> (expert, n-tile, m-tile of this CTA). With CG = 2 the pair's
+// CTAs take m-tiles 2u and 2u+1 of the unit; the second may lie past the
+// expert's rows (computed, never stored).
+template <int CG, typename SS>
+__device__ __forceinline__ void decode_tile(const SS &S, int E, int tile, int rank,
                                             int &e, int &n, int &m)
 {
     int lo = 0, hi = E - 1;
@@ -267,10 +402,10 @@ __device__ __forceinline__ void decode_tile(const SharedStorage &S, int E, int t
         if (S.prefix[mid] <= tile) lo = mid; else hi = mid - 1;
     }
     e = lo;
-    const int mt = (S.offs[e + 1] - S.offs[e] + BM - 1) / BM;
+    const int mu = m_units<CG>(S.offs[e + 1] - S.offs[e]);
     const int local = tile - S.prefix[e];
-    n = local / mt;
-    m = local % mt;
+    n = local / mu;
+    m = (local % mu) * CG + rank;
 }
 
 template <int DT>
@@ -282,7 +417,7 @@ __device__ __forceinline__ uint32_t pack2(float a, float b)
 
 // ---- the kernel -------------------------------------------------------------
 
-template <int DT, bool SWIGLU, int OUT>
+template <int DT, bool SWIGLU, int OUT, int CG>
 __global__ void __launch_bounds__(THREADS, 1)
 grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB0,
@@ -291,23 +426,30 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                        int n_tiles, void *__restrict__ out, unsigned *status,
                        CombineInto comb)
 {
+    using P = Pipe<CG>;
+    constexpr int STAGES = P::STAGES;
     extern __shared__ uint8_t smem_raw[];
-    SharedStorage &S = *reinterpret_cast<SharedStorage *>(
+    SharedStorage<CG> &S = *reinterpret_cast<SharedStorage<CG> *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr int N_OUT = SWIGLU ? BN / 2 : BN;      // output columns per tile
     const int num_kb = (K + BK - 1) / BK;
+    // CTA pair: rank 0 issues the MMAs and owns the stage and accumulator
+    // barriers that both CTAs' copies and epilogues signal
+    const int rank = CG == 2 ? (int)cluster_ctarank() : 0;
+    const bool leader = rank == 0;
+    const int unit0 = (int)blockIdx.x / CG, unit_step = (int)gridDim.x / CG;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) { mbar_init(&S.full[s], 1); mbar_init(&S.empty[s], 1); }
-        for (int a = 0; a < 2; ++a) { mbar_init(&S.acc_full[a], 1); mbar_init(&S.acc_empty[a], 4); }
+        for (int a = 0; a < 2; ++a) { mbar_init(&S.acc_full[a], 1); mbar_init(&S.acc_empty[a], 4 * CG); }
         mbar_init(&S.drain, 1);
         S.abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
-        tmem_alloc(&S.tmem_base, TMEM_COLS);
-        tmem_relinquish();
+        tmem_alloc<CG>(&S.tmem_base, TMEM_COLS);
+        tmem_relinquish<CG>();
     }
     // everything above is CTA-local; the offsets and operands come from the
     // previous kernels on the stream
@@ -320,7 +462,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         const int per = (E + 31) / 32, e0 = lane * per;
         int local = 0;
         for (int e = e0; e < e0 + per && e < E; ++e)
-            local += (S.offs[e + 1] - S.offs[e] + BM - 1) / BM * n_tiles;
+            local += m_units<CG>(S.offs[e + 1] - S.offs[e]) * n_tiles;
         int incl = local;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -330,12 +472,15 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         int run = incl - local;
         for (int e = e0; e < e0 + per && e < E; ++e) {
             S.prefix[e] = run;
-            run += (S.offs[e + 1] - S.offs[e] + BM - 1) / BM * n_tiles;
+            run += m_units<CG>(S.offs[e + 1] - S.offs[e]) * n_tiles;
         }
         if (lane == 31) S.prefix[E] = incl;
     }
     tc_fence_before();
-    __syncthreads();
+    // a pair also makes each CTA's barrier initialisation visible to the
+    // other before any copy or arrival targets it
+    if constexpr (CG == 2) cluster_sync();
+    else __syncthreads();
     tc_fence_after();
 
     const uint32_t tmem_base = S.tmem_base;
@@ -349,22 +494,35 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         // ------------------------------------------------------ TMA producer
         int stage = 0;
         uint32_t phase = 0;
-        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+        for (int tile = unit0; tile < total_tiles; tile += unit_step) {
             int e, n, m;
-            decode_tile(S, E, tile, e, n, m);
+            decode_tile<CG>(S, E, tile, rank, e, n, m);
             const int row0 = S.offs[e] + m * BM;
             bool ok = true;
             for (int kb = 0; kb < num_kb; ++kb) {
-                if (!mbar_wait(&S.empty[stage], phase ^ 1u, abort_flag, status, kWaitLimitNs)) { ok = false; break; }
-                mbar_arrive_expect_tx(&S.full[stage], STAGE_BYTES);
+                if (!mbar_wait<CG>(&S.empty[stage], phase ^ 1u, abort_flag, status, kWaitLimitNs)) { ok = false; break; }
                 uint8_t *sa = S.stage[stage];
                 uint8_t *sb = sa + A_BYTES;
-                tma_load_2d(sa, &tmA, &S.full[stage], kb * BK, row0);
-                if (SWIGLU) {
-                    tma_load_3d(sb, &tmB0, &S.full[stage], kb * BK, n * (BN / 2), e);
-                    tma_load_3d(sb + B_BYTES / 2, &tmB1, &S.full[stage], kb * BK, n * (BN / 2), e);
+                if constexpr (CG == 2) {
+                    // the leader's barrier expects both CTAs' bytes; a peer's
+                    // copy may land before the leader arms it (the phase
+                    // cannot complete while the leader's arrival is pending)
+                    if (leader) mbar_arrive_expect_tx(&S.full[stage], 2 * P::STAGE_BYTES);
+                    const uint32_t bar = mapa_shared(smem_u32(&S.full[stage]), 0);
+                    tma_load_2d_pair(sa, &tmA, bar, kb * BK, row0);
+                    if (SWIGLU)      // CTA 0 holds the gate rows, CTA 1 the up rows
+                        tma_load_3d_pair(sb, rank == 0 ? &tmB0 : &tmB1, bar, kb * BK, n * (BN / 2), e);
+                    else
+                        tma_load_3d_pair(sb, &tmB0, bar, kb * BK, n * BN + rank * (BN / 2), e);
                 } else {
-                    tma_load_3d(sb, &tmB0, &S.full[stage], kb * BK, n * BN, e);
+                    mbar_arrive_expect_tx(&S.full[stage], P::STAGE_BYTES);
+                    tma_load_2d(sa, &tmA, &S.full[stage], kb * BK, row0);
+                    if (SWIGLU) {
+                        tma_load_3d(sb, &tmB0, &S.full[stage], kb * BK, n * (BN / 2), e);
+                        tma_load_3d(sb + P::B_BYTES / 2, &tmB1, &S.full[stage], kb * BK, n * (BN / 2), e);
+                    } else {
+                        tma_load_3d(sb, &tmB0, &S.full[stage], kb * BK, n * BN, e);
+                    }
                 }
                 filled_mask |= 1u << stage;
                 filled_parity = (filled_parity & ~(1u << stage)) | (phase << stage);
@@ -372,36 +530,40 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             }
             if (!ok) break;
         }
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1 && lane == 0 && leader) {
         // ------------------------------------------------------ MMA issuer
-        constexpr uint32_t idesc = idesc_f16<DT>(BM, BN);
+        constexpr uint32_t idesc = idesc_f16<DT>(BM * CG, BN);
         int stage = 0;
         uint32_t phase = 0;
         int it = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++it) {
+        for (int tile = unit0; tile < total_tiles && ok; tile += unit_step, ++it) {
             const int acc = it & 1;
             const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
-            if (!mbar_wait(&S.acc_empty[acc], acc_phase ^ 1u, abort_flag, status, kWaitLimitNs)) { ok = false; break; }
+            if (!mbar_wait<CG>(&S.acc_empty[acc], acc_phase ^ 1u, abort_flag, status, kWaitLimitNs)) { ok = false; break; }
             tc_fence_after();
             const uint32_t d = tmem_base + (uint32_t)(acc * ACC_COLS);
             for (int kb = 0; kb < num_kb; ++kb) {
-                if (!mbar_wait(&S.full[stage], phase, abort_flag, status, kWaitLimitNs)) { ok = false; break; }
+                if (!mbar_wait<CG>(&S.full[stage], phase, abort_flag, status, kWaitLimitNs)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t a0 = smem_u32(S.stage[stage]);
                 const uint32_t b0 = a0 + A_BYTES;
 #pragma unroll
                 for (int k = 0; k < BK / UK; ++k)
-                    umma_f16(d, sdesc_k_sw128(a0 + k * UK * 2), sdesc_k_sw128(b0 + k * UK * 2),
-                             idesc, (kb | k) != 0 ? 1u : 0u);
-                umma_commit(&S.empty[stage]);
+                    umma_f16<CG>(d, sdesc_k_sw128(a0 + k * UK * 2), sdesc_k_sw128(b0 + k * UK * 2),
+                                 idesc, (kb | k) != 0 ? 1u : 0u);
+                if constexpr (CG == 2) umma_commit_pair(&S.empty[stage]);
+                else umma_commit<CG>(&S.empty[stage]);
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
-            if (ok) umma_commit(&S.acc_full[acc]);
+            if (ok) {
+                if constexpr (CG == 2) umma_commit_pair(&S.acc_full[acc]);
+                else umma_commit<CG>(&S.acc_full[acc]);
+            }
         }
         if (*abort_flag) {
             // every MMA issued so far must finish before TMEM is released
-            umma_commit(&S.drain);
+            umma_commit<CG>(&S.drain);
             mbar_wait(&S.drain, 0, nullptr, status, kDrainLimitNs);
         }
     } else if (warp >= 2) {
@@ -421,9 +583,9 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         const int64_t out_row_bytes = (int64_t)N * ESZ;
         const int cch = lane & 7;                               // chunk this lane copies out
         int it = 0;
-        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++it) {
+        for (int tile = unit0; tile < total_tiles; tile += unit_step, ++it) {
             int e, n, m;
-            decode_tile(S, E, tile, e, n, m);
+            decode_tile<CG>(S, E, tile, rank, e, n, m);
             const int seg_rows = S.offs[e + 1] - S.offs[e];
             const int r_base = m * BM + q * 32;                 // this warp's first row in the segment
             uint8_t *out_base = static_cast<uint8_t *>(out) + ((int64_t)S.offs[e] + r_base) * out_row_bytes;
@@ -441,7 +603,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
             // every lane waits; the warp leaves together if any lane gave up,
             // since tcgen05.ld below needs the whole warp converged
-            const bool ready = mbar_wait(&S.acc_full[acc], acc_phase, abort_flag, status, kWaitLimitNs);
+            const bool ready = mbar_wait<CG>(&S.acc_full[acc], acc_phase, abort_flag, status, kWaitLimitNs);
             if (!__all_sync(0xffffffffu, ready)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
@@ -514,23 +676,36 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&S.acc_empty[acc]);
+            if (lane == 0) {
+                if (CG == 2 && !leader) mbar_arrive_cluster(mapa_shared(smem_u32(&S.acc_empty[acc]), 0));
+                else mbar_arrive(&S.acc_empty[acc]);
+            }
         }
     }
 
     // ------------------------------------------------------------ teardown
     __syncthreads();
     if (*abort_flag && warp == 0 && lane == 0) {
-        // let this CTA's outstanding TMA copies land before shared memory goes
-        for (int s = 0; s < STAGES; ++s)
-            if (filled_mask >> s & 1u)
-                mbar_wait(&S.full[s], filled_parity >> s & 1u, nullptr, status, kDrainLimitNs);
+        if (CG == 1 || leader) {
+            // let the outstanding TMA copies land before shared memory goes
+            for (int s = 0; s < STAGES; ++s)
+                if (filled_mask >> s & 1u)
+                    mbar_wait(&S.full[s], filled_parity >> s & 1u, nullptr, status, kDrainLimitNs);
+        } else {
+            // a peer's copies complete on the leader's barriers, which it
+            // cannot wait on: give them the same bounded time to land
+            const uint64_t t0 = global_timer_ns();
+            while (global_timer_ns() - t0 < kDrainLimitNs) { }
+        }
     }
-    __syncthreads();
+    // a pair keeps both CTAs (their shared memory is read by the leader's
+    // MMAs and signalled by its commits) until both are done
+    if constexpr (CG == 2) cluster_sync();
+    else __syncthreads();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        tmem_dealloc<CG>(tmem_base, TMEM_COLS);
     }
 }
 
@@ -586,7 +761,7 @@ bool encode_3d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_
 }
 
 // The dynamic shared-memory opt-in is per device and per kernel instance.
-template <int DT, bool SWIGLU, int OUT>
+template <int DT, bool SWIGLU, int OUT, int CG>
 cudaError_t ensure_smem_attr()
 {
     static std::atomic<uint64_t> done_mask{0};
@@ -595,20 +770,94 @@ cudaError_t ensure_smem_attr()
     if (err != cudaSuccess) return err;
     const uint64_t bit = 1ull << (dev & 63);
     if (done_mask.load() & bit) return cudaSuccess;
-    err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<DT, SWIGLU, OUT>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<DT, SWIGLU, OUT, CG>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes<CG>);
     if (err == cudaSuccess) done_mask.fetch_or(bit);
     return err;
 }
 
-int64_t tc_tile_upper_bound(int64_t rows, int E, int64_t n_tiles)
+// Upper bound on the tile units of a grouped GEMM: every expert adds at most
+// one partial unit.
+int64_t tc_unit_upper_bound(int64_t rows, int E, int64_t n_tiles, int cg)
 {
-    const int64_t mt = rows / BM + (rows < E ? rows : E);
-    return mt * n_tiles;
+    const int64_t per = (int64_t)BM * cg;
+    const int64_t mu = rows / per + (rows < E ? rows : E);
+    return mu * n_tiles;
 }
 
-template <int DT>
-cudaError_t launch_tc_dt(const void *x_disp, const int32_t *offsets, int64_t rows,
+// CTAs to launch: one per SM for CG = 1; for CG = 2 twice the number of
+// pairs the GPU holds at once (cluster placement can leave SMs unpaired), so
+// the persistent grid is always a single wave.
+template <int DT, bool SWIGLU, int OUT, int CG>
+cudaError_t grid_size(int64_t units, int *grid)
+{
+    const int64_t sms = device_sm_count();
+    if constexpr (CG == 1) {
+        *grid = (int)(units < sms ? units : sms);
+        return cudaSuccess;
+    } else {
+        static std::atomic<int> cached[64];
+        int dev = 0;
+        cudaError_t err = cudaGetDevice(&dev);
+        if (err != cudaSuccess) return err;
+        int pairs = cached[dev & 63].load();
+        if (pairs == 0) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)(sms & ~int64_t(1)));
+            cfg.blockDim = dim3(THREADS);
+            cfg.dynamicSmemBytes = kSmemBytes<CG>;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            err = cudaOccupancyMaxActiveClusters(&pairs, grouped_gemm_tc_kernel<DT, SWIGLU, OUT, CG>, &cfg);
+            if (err != cudaSuccess) return err;
+            if (pairs < 1) return cudaErrorInvalidConfiguration;
+            cached[dev & 63].store(pairs);
+        }
+        *grid = 2 * (int)(units < pairs ? units : pairs);
+        return cudaSuccess;
+    }
+}
+
+// Programmatic dependent launch, in clusters of CG CTAs.
+template <int DT, bool SWIGLU, int OUT, int CG>
+cudaError_t launch_gemm(int64_t units, cudaStream_t s, const CUtensorMap &ta, const CUtensorMap &tb0,
+                        const CUtensorMap &tb1, const int32_t *offsets, int E, int N, int K,
+                        int n_tiles, void *out, unsigned *status, const CombineInto &comb)
+{
+    cudaError_t err = ensure_smem_attr<DT, SWIGLU, OUT, CG>();
+    if (err != cudaSuccess) return err;
+    int grid = 0;
+    err = grid_size<DT, SWIGLU, OUT, CG>(units, &grid);
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = kSmemBytes<CG>;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = CG;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = CG == 2 ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<DT, SWIGLU, OUT, CG>, ta, tb0, tb1,
+                              offsets, E, N, K, n_tiles, out, status, comb);
+}
+
+// CTA pairs pay when experts average at least two M-tiles: a pair's second
+// M-tile past an expert's rows is computed for nothing.
+constexpr int64_t kPairMinRowsPerExpert = 2 * BM;
+
+template <int DT, int CG>
+cudaError_t launch_tc_cg(const void *x_disp, const int32_t *offsets, int64_t rows,
                          const void *gate, const void *up, const void *down, int E,
                          int64_t H, int64_t I, void *h_ws, void *out, int out_mode,
                          const CombineInto &comb, unsigned *status, cudaStream_t s)
@@ -620,39 +869,36 @@ cudaError_t launch_tc_dt(const void *x_disp, const int32_t *offsets, int64_t row
         !encode_3d(&mg, tdt, gate, (uint64_t)H, (uint64_t)I, (uint64_t)E, BK, BN / 2) ||
         !encode_3d(&mu, tdt, up, (uint64_t)H, (uint64_t)I, (uint64_t)E, BK, BN / 2) ||
         !encode_2d(&mh, tdt, h_ws, (uint64_t)I, (uint64_t)rows, BK, BM) ||
-        !encode_3d(&md, tdt, down, (uint64_t)I, (uint64_t)H, (uint64_t)E, BK, BN))
+        !encode_3d(&md, tdt, down, (uint64_t)I, (uint64_t)H, (uint64_t)E, BK, BN / CG))
         return cudaErrorInvalidValue;
-    cudaError_t err = ensure_smem_attr<DT, true, kOutDtype>();
-    if (err == cudaSuccess) {
-        if (out_mode == kOutF32) err = ensure_smem_attr<DT, false, kOutF32>();
-        else if (out_mode == kOutCombine) err = ensure_smem_attr<DT, false, kOutCombine>();
-        else err = ensure_smem_attr<DT, false, kOutDtype>();
-    }
-    if (err != cudaSuccess) return err;
-    const int64_t sms = device_sm_count();
     const int nt1 = (int)((I + BN / 2 - 1) / (BN / 2));
     const int nt2 = (int)((H + BN - 1) / BN);
-    int64_t g1 = tc_tile_upper_bound(rows, E, nt1);
-    int64_t g2 = tc_tile_upper_bound(rows, E, nt2);
-    if (g1 > sms) g1 = sms;
-    if (g2 > sms) g2 = sms;
-    err = launch_pdl(grouped_gemm_tc_kernel<DT, true, kOutDtype>, dim3((unsigned)g1),
-                     dim3(THREADS), kSmemBytes, s, mx, mg, mu, offsets, E, (int)I, (int)H, nt1,
-                     h_ws, status, comb);
+    const int64_t u1 = tc_unit_upper_bound(rows, E, nt1, CG);
+    const int64_t u2 = tc_unit_upper_bound(rows, E, nt2, CG);
+    cudaError_t err = launch_gemm<DT, true, kOutDtype, CG>(u1, s, mx, mg, mu, offsets, E, (int)I,
+                                                           (int)H, nt1, h_ws, status, comb);
     if (err != cudaSuccess) return err;
     if (out_mode == kOutF32)
-        err = launch_pdl(grouped_gemm_tc_kernel<DT, false, kOutF32>, dim3((unsigned)g2),
-                         dim3(THREADS), kSmemBytes, s, mh, md, md, offsets, E, (int)H, (int)I,
-                         nt2, out, status, comb);
-    else if (out_mode == kOutCombine)
-        err = launch_pdl(grouped_gemm_tc_kernel<DT, false, kOutCombine>, dim3((unsigned)g2),
-                         dim3(THREADS), kSmemBytes, s, mh, md, md, offsets, E, (int)H, (int)I,
-                         nt2, out, status, comb);
-    else
-        err = launch_pdl(grouped_gemm_tc_kernel<DT, false, kOutDtype>, dim3((unsigned)g2),
-                         dim3(THREADS), kSmemBytes, s, mh, md, md, offsets, E, (int)H, (int)I,
-                         nt2, out, status, comb);
-    return err;
+        return launch_gemm<DT, false, kOutF32, CG>(u2, s, mh, md, md, offsets, E, (int)H, (int)I,
+                                                   nt2, out, status, comb);
+    if (out_mode == kOutCombine)
+        return launch_gemm<DT, false, kOutCombine, CG>(u2, s, mh, md, md, offsets, E, (int)H,
+                                                       (int)I, nt2, out, status, comb);
+    return launch_gemm<DT, false, kOutDtype, CG>(u2, s, mh, md, md, offsets, E, (int)H, (int)I,
+                                                 nt2, out, status, comb);
+}
+
+template <int DT>
+cudaError_t launch_tc_dt(const void *x_disp, const int32_t *offsets, int64_t rows,
+                         const void *gate, const void *up, const void *down, int E,
+                         int64_t H, int64_t I, void *h_ws, void *out, int out_mode,
+                         const CombineInto &comb, unsigned *status, cudaStream_t s)
+{
+    if (rows >= kPairMinRowsPerExpert * E)
+        return launch_tc_cg<DT, 2>(x_disp, offsets, rows, gate, up, down, E, H, I, h_ws, out,
+                                   out_mode, comb, status, s);
+    return launch_tc_cg<DT, 1>(x_disp, offsets, rows, gate, up, down, E, H, I, h_ws, out,
+                               out_mode, comb, status, s);
 }
 
 }  // namespace
