@@ -5,6 +5,13 @@
 // renormalisation, then a cast to the logits dtype; rows holding NaN, +inf or
 // only -inf keep NaN weights.
 //
+// Two kernels. At large T (E <= 64, top_k <= 8) one thread routes one token:
+// the E logits sit in its registers, each of the k selections is a scan for
+// the first maximum (so among equal logits the lower id wins), and the k
+// weights stay in registers until their slot-order sum is known -- no
+// communication between lanes, the fewest instructions per token. Below that
+// T, too few threads would be in flight, and a group of lanes shares a token:
+//
 // A group of G lanes (G = 1..32, a power of two) routes one token, so a warp
 // routes 32/G tokens at once; lane r of a group holds logits r*EPL ..
 // r*EPL+EPL-1 in registers (G*EPL >= E, EPL <= 32), so a group reads one
@@ -167,6 +174,132 @@ route_kernel(const void *__restrict__ logits, int64_t T, int E, int top_k,
     }
 }
 
+// ---- one thread per token ----------------------------------------------------
+
+constexpr int kMaxThreadTopK = 8;
+
+template <int EPL, int LDT>
+__global__ void __launch_bounds__(kRouteThreads)
+route_thread_kernel(const void *__restrict__ logits, int64_t T, int E, int top_k,
+                    int renormalize, int vec_rows, uint32_t *__restrict__ idx_out,
+                    void *__restrict__ w_out)
+{
+    using ET = typename Elem<LDT>::T;
+    constexpr int VEC = 16 / (int)sizeof(ET);          // elements per 16-byte load
+    static_assert(EPL % VEC == 0, "rows are read in 16-byte pieces");
+    const ET *L = static_cast<const ET *>(logits);
+    ET *W = static_cast<ET *>(w_out);
+    pdl_wait();
+    pdl_launch_dependents();
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < T;
+         t += (int64_t)gridDim.x * blockDim.x) {
+        float l[EPL];
+        const ET *row = L + t * E;
+        if (vec_rows) {
+            // E * sizeof(ET) is a multiple of 16 and the buffer 16-byte aligned
+#pragma unroll
+            for (int c = 0; c < EPL; c += VEC) {
+                if (c < E) {
+                    Vec16 v;
+                    v.u = *reinterpret_cast<const uint4 *>(row + c);
+#pragma unroll
+                    for (int i = 0; i < VEC; ++i) {
+                        if constexpr (LDT == DT_F32) l[c + i] = v.f[i];
+                        else {
+                            const float2 f = LDT == DT_BF16 ? bf16x2_to_float2(v.w[i / 2])
+                                                            : f16x2_to_float2(v.w[i / 2]);
+                            l[c + i] = (i & 1) ? f.y : f.x;
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < VEC; ++i) l[c + i] = -INFINITY;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) l[i] = i < E ? Elem<LDT>::to_f(row[i]) : -INFINITY;
+        }
+        int bad = 0, all_ninf = 1;
+        float m = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i)
+            if (i < E) {
+                bad |= isnan(l[i]) || l[i] == INFINITY;
+                all_ninf &= (l[i] == -INFINITY);
+                m = fmaxf(m, l[i]);
+            }
+        const bool invalid = bad || all_ninf;
+
+        // FP32 softmax over all E experts, exp(l - max) as exp2 of the scaled
+        // difference; the selected ones are recomputed below (same value)
+        constexpr float kLog2e = 1.4426950408889634f;
+        float s = 0.0f;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i)
+            if (i < E) s += exp2f((l[i] - m) * kLog2e);
+        const float inv_s = 1.0f / s;
+
+        uint64_t avail = E >= 64 ? ~0ull : ((1ull << E) - 1ull);
+        float p[kMaxThreadTopK];
+        int id[kMaxThreadTopK];
+        float z = 0.0f;
+#pragma unroll
+        for (int j = 0; j < kMaxThreadTopK; ++j) {
+            p[j] = 0.0f;
+            id[j] = j;
+            if (j < top_k) {
+                float bl = -INFINITY;
+                int be = -1;
+#pragma unroll
+                for (int i = 0; i < EPL; ++i)
+                    if ((avail >> i & 1ull) && (be < 0 || l[i] > bl)) {
+                        bl = l[i];
+                        be = i;
+                    }
+                if (be >= 0) {
+                    avail &= ~(1ull << be);
+                    id[j] = be;
+                    p[j] = exp2f((bl - m) * kLog2e) * inv_s;
+                    z += p[j];
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kMaxThreadTopK; ++j) {
+            if (j < top_k) {
+                if (invalid) {
+                    idx_out[t * top_k + j] = (uint32_t)j;
+                    W[t * top_k + j] = Elem<LDT>::from_f(__int_as_float(0x7fc00000));
+                } else {
+                    idx_out[t * top_k + j] = (uint32_t)id[j];
+                    W[t * top_k + j] = Elem<LDT>::from_f(renormalize ? p[j] / z : p[j]);
+                }
+            }
+        }
+    }
+}
+
+template <int EPL, int LDT>
+cudaError_t launch_route_thread(const void *logits, int64_t T, int E, int top_k, int renorm,
+                                uint32_t *idx, void *w, cudaStream_t s)
+{
+    using ET = typename Elem<LDT>::T;
+    const int vec_rows = ((int64_t)E * (int64_t)sizeof(ET)) % 16 == 0 &&
+                         reinterpret_cast<uintptr_t>(logits) % 16 == 0;
+    int64_t blocks = (T + kRouteThreads - 1) / kRouteThreads;
+    const int64_t cap = (int64_t)device_sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    return launch_pdl(route_thread_kernel<EPL, LDT>, dim3((unsigned)blocks), dim3(kRouteThreads),
+                      0, s, logits, T, E, top_k, renorm, vec_rows, idx, w);
+}
+
+// One thread per token once there are at least two warps of tokens per SM.
+bool thread_route_fits(int64_t T, int E, int top_k)
+{
+    return E <= 64 && top_k <= kMaxThreadTopK && T >= (int64_t)device_sm_count() * 64;
+}
+
 template <int G, int EPL, int LDT>
 cudaError_t launch_route_cfg(const void *logits, int64_t T, int E, int top_k, int renorm,
                              uint32_t *idx, void *w, cudaStream_t s)
@@ -183,6 +316,12 @@ template <int LDT>
 cudaError_t launch_route_dt(const void *logits, int64_t T, int E, int top_k,
                             int renorm, uint32_t *idx, void *w, cudaStream_t s)
 {
+    if (thread_route_fits(T, E, top_k)) {
+        if (E <= 8) return launch_route_thread<8, LDT>(logits, T, E, top_k, renorm, idx, w, s);
+        if (E <= 16) return launch_route_thread<16, LDT>(logits, T, E, top_k, renorm, idx, w, s);
+        if (E <= 32) return launch_route_thread<32, LDT>(logits, T, E, top_k, renorm, idx, w, s);
+        return launch_route_thread<64, LDT>(logits, T, E, top_k, renorm, idx, w, s);
+    }
     if (E <= 8) return launch_route_cfg<1, 8, LDT>(logits, T, E, top_k, renorm, idx, w, s);
     if (E <= 16) return launch_route_cfg<2, 8, LDT>(logits, T, E, top_k, renorm, idx, w, s);
     if (E <= 32) return launch_route_cfg<4, 8, LDT>(logits, T, E, top_k, renorm, idx, w, s);

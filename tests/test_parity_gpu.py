@@ -89,6 +89,14 @@ ROUTE_CASES = [
     (500, 16, 4, True, "f32", "ties"),
     (500, 40, 3, False, "bf16", "ties"),
     (300, 24, 4, True, "f32", "specials"),
+    # T >= 64 tokens per SM: one thread routes one token (E <= 64, k <= 8);
+    # 16-byte row loads where E * dtype size % 16 == 0
+    (100000, 64, 6, False, "bf16", "normal"),
+    (90000, 8, 2, True, "f32", "ties"),
+    (80000, 33, 5, True, "f16", "specials"),
+    (80000, 24, 8, True, "bf16", "ties"),
+    (100000, 64, 8, True, "f32", "specials"),
+    (12000, 40, 3, False, "bf16", "ties"),
 ]
 
 
