@@ -77,6 +77,9 @@ def _bind(lib):
     lib.oracle_convert.restype = None
     lib.oracle_route.argtypes = [_P, _INT, _I64, _I64, _I64, _INT, _P, _P]
     lib.oracle_route.restype = _I64
+    lib.oracle_route_sigmoid_grouped.argtypes = [_P, _INT, _I64, _I64, _P, _I64, _I64,
+                                                  _I64, _INT, _INT, _F, _P, _P]
+    lib.oracle_route_sigmoid_grouped.restype = _I64
     lib.oracle_dispatch.argtypes = [_P, _I64, _I64, _I64, _P, _P, _P, _P]
     lib.oracle_dispatch.restype = _I64
     lib.oracle_gather.argtypes = [_P, _INT, _I64, _I64, _P, _I64, _P]
@@ -146,6 +149,31 @@ def route(logits, ldt: str, top_k: int, renormalize: bool, lib=None):
                          int(bool(renormalize)), _ptr(idx), _ptr(w))
     if n < 0:
         raise ValueError("oracle_route: bad arguments")
+    return idx, w, int(n)
+
+
+def route_sigmoid_grouped(logits, ldt: str, bias, top_k: int, groups: int,
+                          selected_groups: int, group_top_two: bool, renormalize: bool,
+                          scale: float, lib=None):
+    """Group-limited sigmoid routing (ruDNN user guide, section 10).
+
+    ``bias`` is a float32 ``[E]`` correction or None. Returns ``(idx uint32
+    [T,k], w [T,k] in ldt storage, invalid_rows)``.
+    """
+    lib = lib or load_library()
+    logits = _arr(logits, ldt)
+    T, E = logits.shape
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    if b is not None and b.shape != (E,):
+        raise ValueError("bias must have shape [E]")
+    idx = np.empty((T, top_k), dtype=np.uint32)
+    w = np.empty((T, top_k), dtype=_storage(ldt))
+    n = lib.oracle_route_sigmoid_grouped(
+        _ptr(logits), DTYPE_CODES[ldt], T, E, None if b is None else _ptr(b), top_k, groups,
+        selected_groups, int(bool(group_top_two)), int(bool(renormalize)), float(scale),
+        _ptr(idx), _ptr(w))
+    if n < 0:
+        raise ValueError("oracle_route_sigmoid_grouped: arguments outside the limits")
     return idx, w, int(n)
 
 

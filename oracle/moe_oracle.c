@@ -21,6 +21,15 @@
  *   [ruDNN-3]  ruDNN user guide, section 3 "MoE workflow": logits ->
  *              softmax/top-k -> compact dispatch -> SwiGLU experts ->
  *              weighted combine; bias-free experts.
+ *   [ruDNN-10] ruDNN user guide, section 10 "Group-limited sigmoid MoE
+ *              routing" (Chinese edition): sigmoid scores; an optional FP32
+ *              correction bias that only affects the selection; experts in
+ *              equal consecutive groups; a group scored by its best (or two
+ *              best) corrected scores; selected_groups groups kept, top_k
+ *              experts picked inside them; weights are the raw scores,
+ *              optionally renormalised, times a finite positive scale; equal
+ *              scores favour the lower id; limits E 1..1024, groups 1..128,
+ *              top_k 1..64.
  *   [ruDNN-7]  ruDNN user guide, section 7 "LayerNorm, RMSNorm and Softmax":
  *              last-axis RMSNorm, epsilon finite and > 0, FP32 statistics,
  *              output in the input dtype.
@@ -200,6 +209,109 @@ int64_t oracle_route(const void *logits, int ldt, int64_t T, int64_t E,
             store_elem(w, ldt, t * top_k + j, (double)sel[j]);
     }
     free(l); free(p); free(sel); free(taken);
+    return invalid_rows;
+}
+
+/* ---- grouped sigmoid routing [ruDNN-10] --------------------------------- */
+
+/* Sigmoid of a binary32 value, correctly rounded to binary32: evaluated in
+ * double (whose error is far below half a binary32 ulp) and rounded once. */
+static float sigmoid_f32(float x)
+{
+    return (float)(1.0 / (1.0 + exp(-(double)x)));
+}
+
+/*
+ * For every token t, in the order the section gives:
+ *   s_e = sigmoid(l_e) as an FP32 score; c_e = s_e + bias_e (FP32; the bias
+ *   only steers the selection);
+ *   the E experts form `groups` groups of E/groups consecutive experts; a
+ *   group's score is its largest c, or the FP32 sum of its two largest c when
+ *   group_top_two is set;
+ *   the `selected_groups` best groups are kept (higher score first, lower
+ *   group id on equal scores);
+ *   top_k experts of the kept groups are picked by c (higher first, lower id
+ *   on equal scores);
+ *   their weights are the raw scores s, divided by their FP32 sum (slot
+ *   order) when renormalize is set, times `scale`, cast to the logits dtype.
+ * A row whose corrected scores hold a NaN (a NaN logit or bias) gets indices
+ * 0..k-1 and NaN weights, as in the softmax contract. bias may be NULL
+ * (all zero). Returns the number of such rows, or -1 on arguments outside
+ * the section's limits.
+ */
+int64_t oracle_route_sigmoid_grouped(const void *logits, int ldt, int64_t T, int64_t E,
+                                     const float *bias, int64_t top_k, int64_t groups,
+                                     int64_t selected_groups, int group_top_two,
+                                     int renormalize, float scale, uint32_t *idx, void *w)
+{
+    if (T < 0 || E < 1 || E > 1024 || groups < 1 || groups > 128 || E % groups != 0 ||
+        selected_groups < 1 || selected_groups > groups || top_k < 1 || top_k > 64 ||
+        top_k > selected_groups * (E / groups) || (group_top_two && E / groups < 2) ||
+        !isfinite(scale) || !(scale > 0.0f))
+        return -1;
+    const int64_t gs = E / groups;
+    float *sc = (float *)malloc((size_t)E * sizeof(float));
+    float *c = (float *)malloc((size_t)E * sizeof(float));
+    float *gscore = (float *)malloc((size_t)groups * sizeof(float));
+    unsigned char *gkept = (unsigned char *)malloc((size_t)groups);
+    unsigned char *taken = (unsigned char *)malloc((size_t)E);
+    float *pick = (float *)malloc((size_t)top_k * sizeof(float));
+    int64_t invalid_rows = 0;
+
+    for (int64_t t = 0; t < T; ++t) {
+        int has_nan = 0;
+        for (int64_t e = 0; e < E; ++e) {
+            sc[e] = sigmoid_f32((float)load_elem(logits, ldt, t * E + e));
+            c[e] = sc[e] + (bias ? bias[e] : 0.0f);
+            if (isnan(c[e])) has_nan = 1;
+        }
+        if (has_nan) {
+            for (int64_t j = 0; j < top_k; ++j) {
+                idx[t * top_k + j] = (uint32_t)j;
+                store_elem(w, ldt, t * top_k + j, (double)NAN);
+            }
+            ++invalid_rows;
+            continue;
+        }
+
+        for (int64_t g = 0; g < groups; ++g) {
+            float first = -INFINITY, second = -INFINITY;
+            for (int64_t e = g * gs; e < (g + 1) * gs; ++e) {
+                if (c[e] > first) { second = first; first = c[e]; }
+                else if (c[e] > second) second = c[e];
+            }
+            gscore[g] = group_top_two ? first + second : first;
+        }
+        memset(gkept, 0, (size_t)groups);
+        for (int64_t n = 0; n < selected_groups; ++n) {
+            int64_t best = -1;
+            for (int64_t g = 0; g < groups; ++g) {
+                if (gkept[g]) continue;
+                if (best < 0 || gscore[g] > gscore[best]) best = g;
+            }
+            gkept[best] = 1;
+        }
+
+        memset(taken, 0, (size_t)E);
+        for (int64_t j = 0; j < top_k; ++j) {
+            int64_t best = -1;
+            for (int64_t e = 0; e < E; ++e) {
+                if (taken[e] || !gkept[e / gs]) continue;
+                if (best < 0 || c[e] > c[best]) best = e;
+            }
+            taken[best] = 1;
+            idx[t * top_k + j] = (uint32_t)best;
+            pick[j] = sc[best];
+        }
+        if (renormalize) {
+            float zsum = 0.0f;
+            for (int64_t j = 0; j < top_k; ++j) zsum += pick[j];
+            for (int64_t j = 0; j < top_k; ++j) pick[j] = pick[j] / zsum;
+        }
+        for (int64_t j = 0; j < top_k; ++j)
+            store_elem(w, ldt, t * top_k + j, (double)(pick[j] * scale));
+    }
+    free(sc); free(c); free(gscore); free(gkept); free(taken); free(pick);
     return invalid_rows;
 }
 

@@ -147,6 +147,110 @@ def check_route_full_softmax(lib):
                 assert np.all(np.diff(ref[t, idx[t]]) <= 1e-12)
 
 
+def _sg_case(fields):
+    E, G, S, k, two, ren = (int(v) for v in fields[0].split()[:6])
+    scale = float(Fraction(fields[0].split()[6]))
+    def tok(v):
+        return -_logit(v[1:]) if v.startswith("-ln:") else _logit(v)
+    logits = np.array([[tok(v) for v in fields[1].split()]], np.float32)
+    bias = None if fields[2] == "none" else np.array(
+        [float(Fraction(v)) if v != "nan" else math.nan for v in fields[2].split()], np.float32)
+    return E, G, S, k, two, ren, scale, logits, bias
+
+
+def check_sigmoid_grouped_golden(lib):
+    """Hand-derived group-limited sigmoid routing cases (ruDNN user guide,
+    section 10)."""
+    n = 0
+    for fields in _lines("sigmoid_grouped_cases.txt"):
+        E, G, S, k, two, ren, scale, logits, bias = _sg_case(fields)
+        assert logits.shape == (1, E)
+        idx, w, _ = oracle.route_sigmoid_grouped(logits, "f32", bias, k, G, S, bool(two),
+                                                 bool(ren), scale, lib)
+        want_idx = [int(v) for v in fields[3].split()]
+        assert list(idx[0]) == want_idx, (fields, idx)
+        for got, want in zip(w[0], fields[4].split()):
+            if want == "nan":
+                assert math.isnan(got), (fields, w)
+            else:
+                assert _f32_close(float(got), float(Fraction(want)), 1e-6), (fields, w)
+        n += 1
+    assert n >= 12
+
+
+def _group_scores(c, G, two):
+    per = np.sort(c.reshape(G, -1), axis=1)[:, ::-1]
+    return per[:, 0] + per[:, 1] if two else per[:, 0]
+
+
+def check_sigmoid_grouped_optimality(lib):
+    """Random rows against the selection rule stated as order conditions
+    (checked with sorts, not the oracle's scans): every kept group ranks
+    before every dropped one on (score desc, id asc); the picked experts lie
+    in kept groups and rank before every unpicked expert of those groups on
+    (corrected score desc, id asc), in pick order; weights are the closed-form
+    sigmoid of the picked logits, renormalised and scaled."""
+    rng = np.random.default_rng(41)
+    for trial in range(60):
+        G = int(rng.choice([1, 2, 4, 8]))
+        gs = int(rng.choice([2, 3, 4]))
+        E = G * gs
+        S = int(rng.integers(1, G + 1))
+        k = int(rng.integers(1, S * gs + 1))
+        two, ren = bool(trial % 2), bool(trial % 3 == 0)
+        scale = float(rng.choice([1.0, 2.5]))
+        T = 7
+        logits = np.round(rng.standard_normal((T, E)) * 2, 1).astype(np.float32)  # ties happen
+        bias = (np.round(rng.standard_normal(E), 1) * 0.2).astype(np.float32) if trial % 4 else None
+        idx, w, bad = oracle.route_sigmoid_grouped(logits, "f32", bias, k, G, S, two, ren,
+                                                   scale, lib)
+        assert bad == 0
+        for t in range(T):
+            s = (1.0 / (1.0 + np.exp(-logits[t].astype(np.float64)))).astype(np.float32)
+            c = s + (bias if bias is not None else np.float32(0))
+            gsc = _group_scores(c, G, two)
+            order_g = np.lexsort((np.arange(G), -gsc.astype(np.float64)))
+            kept = set(order_g[:S].tolist())
+            cand = [e for e in range(E) if e // gs in kept]
+            order_e = sorted(cand, key=lambda e: (-float(c[e]), e))
+            assert idx[t].tolist() == order_e[:k], (trial, t)
+            sel = s[idx[t]].astype(np.float64)
+            if ren:
+                sel = sel / sel.sum()
+            assert np.allclose(w[t], sel * scale, rtol=2e-6, atol=0), (trial, t)
+
+
+def check_sigmoid_grouped_reduces_to_softmax_order(lib):
+    """One group, no bias: sigmoid is increasing, so the picks are the top-k
+    logits -- the same ids as the (separately pinned) softmax routing, for
+    logits far from sigmoid saturation."""
+    rng = np.random.default_rng(43)
+    logits = (rng.standard_normal((50, 40)) * 2).astype(np.float32)
+    for k in (1, 5, 40):
+        ids, _, _ = oracle.route_sigmoid_grouped(logits, "f32", None, k, 1, 1, False, False,
+                                                 1.0, lib)
+        ref, _, _ = oracle.route(logits, "f32", k, False, lib)
+        assert np.array_equal(ids, ref)
+
+
+def check_sigmoid_grouped_arguments(lib):
+    """Limits the section states are rejected."""
+    lg = np.zeros((1, 8), np.float32)
+    bad = [dict(k=1, G=3, S=1), dict(k=1, G=2, S=3), dict(k=9, G=1, S=1),
+           dict(k=5, G=4, S=2), dict(k=1, G=8, S=1, two=True), dict(k=1, G=1, S=1, scale=0.0),
+           dict(k=1, G=1, S=1, scale=math.inf), dict(k=65, G=1, S=1)]
+    for a in bad:
+        width = 128 if a["k"] == 65 else 8
+        try:
+            oracle.route_sigmoid_grouped(np.zeros((1, width), np.float32), "f32", None, a["k"],
+                                         a["G"], a["S"], a.get("two", False), False,
+                                         a.get("scale", 1.0), lib)
+        except ValueError:
+            continue
+        raise AssertionError(f"accepted {a}")
+    oracle.route_sigmoid_grouped(lg, "f32", None, 4, 4, 2, True, True, 1.0, lib)
+
+
 def check_route_selection_sort(lib):
     """Brute force over heavy-tie rows: the selection equals a stable sort
     by (logit descending, id ascending) done by numpy."""

@@ -62,6 +62,25 @@ MUTANTS = [
      "combine[t * H + h] + load_elem(residual, rdt, t * H + h)",
      "combine[t * H + h]"),
     ("bf16_truncates", "u += 0x7fffu + keep_lsb;", "u += 0u * keep_lsb;"),
+    # group-limited sigmoid routing
+    ("sg_weight_uses_corrected_score", "pick[j] = sc[best];", "pick[j] = c[best];"),
+    ("sg_bias_subtracted", "c[e] = sc[e] + (bias ? bias[e] : 0.0f);",
+     "c[e] = sc[e] - (bias ? bias[e] : 0.0f);"),
+    ("sg_top_two_ignored", "gscore[g] = group_top_two ? first + second : first;",
+     "gscore[g] = first;"),
+    ("sg_top_two_always", "gscore[g] = group_top_two ? first + second : first;",
+     "gscore[g] = first + second;"),
+    ("sg_second_best_missed", "else if (c[e] > second) second = c[e];", "else second = second;"),
+    ("sg_group_tie_to_higher_id", "if (best < 0 || gscore[g] > gscore[best]) best = g;",
+     "if (best < 0 || gscore[g] >= gscore[best]) best = g;"),
+    ("sg_expert_tie_to_higher_id", "if (best < 0 || c[e] > c[best]) best = e;",
+     "if (best < 0 || c[e] >= c[best]) best = e;"),
+    ("sg_groups_ignored", "if (taken[e] || !gkept[e / gs]) continue;", "if (taken[e]) continue;"),
+    ("sg_scale_dropped", "(double)(pick[j] * scale)", "(double)(pick[j])"),
+    ("sg_no_renormalise", "pick[j] = pick[j] / zsum;", "pick[j] = pick[j];"),
+    ("sg_nan_row_valid", "if (isnan(c[e])) has_nan = 1;", "if (isnan(c[e])) has_nan = 0;"),
+    ("sg_sigmoid_wrong_sign", "return (float)(1.0 / (1.0 + exp(-(double)x)));",
+     "return (float)(1.0 / (1.0 + exp((double)x)));"),
 ]
 
 
