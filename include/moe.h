@@ -100,6 +100,40 @@ int moe_route(const void *logits, int logits_dtype, int64_t T, int64_t E,
               void *weights, void *stream);
 
 /*
+ * moe_route_sigmoid_grouped -- group-limited sigmoid routing.
+ * ruDNN user guide, section 10 "Group-limited sigmoid MoE routing".
+ *
+ *   logits          [T, E], dtype logits_dtype (F32/BF16/F16), read only.
+ *   bias            [E] FP32 correction, read only; NULL means all zero.
+ *   T >= 0, 1 <= E <= 1024, 1 <= groups <= 128 with E % groups == 0,
+ *   1 <= selected_groups <= groups, 1 <= top_k <= 64 and
+ *   top_k <= selected_groups * (E / groups); group_top_two needs
+ *   E / groups >= 2; scale finite and > 0.
+ *   expert_indices  [T, top_k] uint32, written.
+ *   weights         [T, top_k] in logits_dtype, written.
+ *
+ * Per token: FP32 scores s_e = 1 / (1 + exp(-l_e)); selection scores
+ * c_e = s_e + bias_e (FP32; the bias affects the selection only); groups
+ * are the E/groups consecutive experts starting at g*(E/groups), each scored
+ * by its largest c, or by the FP32 sum of its two largest c when
+ * group_top_two != 0; the selected_groups best groups are kept (higher score
+ * first, lower group id among equal scores); top_k experts of the kept
+ * groups are picked by c, highest first, lower id among equal c; their
+ * weights are the scores s, divided by their FP32 sum (in pick order) when
+ * renormalize != 0, then multiplied by scale and rounded once to
+ * logits_dtype. A row whose corrected scores hold a NaN (a NaN logit or bias)
+ * gets indices 0..top_k-1 and NaN weights. +inf and -inf logits are valid
+ * (scores 1 and 0).
+ * Errors: MOE_ERR_NULL, MOE_ERR_SHAPE, MOE_ERR_DTYPE, MOE_ERR_VALUE (scale),
+ * MOE_ERR_ALIGN (logits, indices, weights and a non-NULL bias must be
+ * 16-byte aligned), MOE_ERR_CUDA.
+ */
+int moe_route_sigmoid_grouped(const void *logits, int logits_dtype, int64_t T, int64_t E,
+                              const float *bias, int top_k, int groups, int selected_groups,
+                              int group_top_two, int renormalize, float scale,
+                              uint32_t *expert_indices, void *weights, void *stream);
+
+/*
  * moe_dispatch -- compact dispatch with a saved map; nothing is dropped.
  * ruDNN user guide, section 5 "Expert weights and dispatch".
  *
@@ -263,6 +297,23 @@ int moe_forward(const void *x, int dtype, const void *logits,
                 const void *down, int64_t T, int64_t H, int64_t I, int64_t E,
                 int top_k, int renormalize, void *y, void *workspace,
                 size_t workspace_bytes, void *stream);
+
+/*
+ * moe_forward_sigmoid_grouped -- the one-call forward of moe_forward with
+ * group-limited sigmoid routing in place of softmax top-k routing
+ * (ruDNN user guide, section 10, SwiGluExperts::forward_sigmoid_grouped):
+ * moe_route_sigmoid_grouped -> dispatch -> SwiGLU experts -> weighted
+ * combine. Arguments are those of moe_forward plus the routing arguments of
+ * moe_route_sigmoid_grouped (same limits and errors); the workspace is
+ * moe_forward_workspace_size(T, H, I, E, top_k, dtype, logits_dtype) bytes.
+ * The routing weights enter the combine as they are (with scale applied).
+ */
+int moe_forward_sigmoid_grouped(const void *x, int dtype, const void *logits, int logits_dtype,
+                                const float *bias, const void *gate, const void *up,
+                                const void *down, int64_t T, int64_t H, int64_t I, int64_t E,
+                                int top_k, int groups, int selected_groups, int group_top_two,
+                                int renormalize, float scale, void *y, void *workspace,
+                                size_t workspace_bytes, void *stream);
 
 /*
  * moe_device_status -- read the current device's status word.

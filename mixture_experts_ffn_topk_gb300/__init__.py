@@ -37,11 +37,12 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_NULL", 2: "MOE_ERR_SHAPE",
                 8: "MOE_ERR_DEVICE_TIMEOUT", 9: "MOE_ERR_BAD_INDEX"}
 
 EXPORTED = ["moe_status_string", "moe_abi_version", "moe_last_error_detail",
-            "moe_route", "moe_dispatch_workspace_size", "moe_dispatch",
+            "moe_route", "moe_route_sigmoid_grouped", "moe_dispatch_workspace_size",
+            "moe_dispatch",
             "moe_dispatch_noalloc",
             "moe_experts_workspace_size", "moe_experts_forward", "moe_combine",
             "moe_combine_add_rmsnorm", "moe_forward_workspace_size",
-            "moe_forward", "moe_device_status"]
+            "moe_forward", "moe_forward_sigmoid_grouped", "moe_device_status"]
 
 _lock = threading.Lock()
 _lib = None
@@ -65,6 +66,8 @@ def _bind(lib):
         "moe_abi_version": ([], _INT),
         "moe_last_error_detail": ([], ctypes.c_char_p),
         "moe_route": ([_P, _INT, _I64, _I64, _INT, _INT, _P, _P, _P], _INT),
+        "moe_route_sigmoid_grouped": ([_P, _INT, _I64, _I64, _P, _INT, _INT, _INT, _INT,
+                                       _INT, _F, _P, _P, _P], _INT),
         "moe_dispatch_workspace_size": ([_I64, _INT, _I64], _SZ),
         "moe_dispatch": ([_P, _I64, _INT, _I64, _P, _INT, _I64, _P, _P, _P, _P,
                           _P, _P, _SZ, _P], _INT),
@@ -80,6 +83,9 @@ def _bind(lib):
                                         _INT], _SZ),
         "moe_forward": ([_P, _INT, _P, _INT, _P, _P, _P, _I64, _I64, _I64, _I64,
                          _INT, _INT, _P, _P, _SZ, _P], _INT),
+        "moe_forward_sigmoid_grouped": ([_P, _INT, _P, _INT, _P, _P, _P, _P, _I64, _I64,
+                                         _I64, _I64, _INT, _INT, _INT, _INT, _INT, _F, _P,
+                                         _P, _SZ, _P], _INT),
         "moe_device_status": ([_P, _INT], _INT),
     }
     for name, (args, res) in sig.items():
@@ -174,6 +180,31 @@ def moe_route(logits: torch.Tensor, top_k: int, renormalize: bool,
                                   _ptr(expert_indices), _ptr(weights),
                                   _stream(stream))
     _check(rc, "moe_route")
+    return expert_indices, weights
+
+
+def moe_route_sigmoid_grouped(logits: torch.Tensor, bias: torch.Tensor | None, top_k: int,
+                              groups: int, selected_groups: int, group_top_two: bool,
+                              renormalize: bool, scale: float = 1.0,
+                              expert_indices: torch.Tensor | None = None,
+                              weights: torch.Tensor | None = None, stream=None):
+    """Group-limited sigmoid routing; ``bias`` is an FP32 ``[E]`` correction
+    or None. Returns ``(expert_indices int32 [T,k], weights [T,k] in
+    logits.dtype)``."""
+    T, E = logits.shape
+    dev = logits.device
+    if bias is not None and (bias.dtype != torch.float32 or tuple(bias.shape) != (E,)):
+        raise ValueError("bias must be float32 of shape [E]")
+    if expert_indices is None:
+        expert_indices = torch.empty((T, top_k), dtype=torch.int32, device=dev)
+    if weights is None:
+        weights = torch.empty((T, top_k), dtype=logits.dtype, device=dev)
+    rc = load_library().moe_route_sigmoid_grouped(
+        _ptr(logits), _code(logits.dtype), T, E, None if bias is None else _ptr(bias),
+        int(top_k), int(groups), int(selected_groups), int(bool(group_top_two)),
+        int(bool(renormalize)), float(scale), _ptr(expert_indices), _ptr(weights),
+        _stream(stream))
+    _check(rc, "moe_route_sigmoid_grouped")
     return expert_indices, weights
 
 
@@ -323,6 +354,29 @@ def moe_forward(x: torch.Tensor, logits: torch.Tensor, gate: torch.Tensor,
         _ptr(up), _ptr(down), T, H, I, E, int(top_k), int(bool(renormalize)),
         _ptr(y), _ptr(ws), _nbytes(ws), _stream(stream))
     _check(rc, "moe_forward")
+    return y
+
+
+def moe_forward_sigmoid_grouped(x: torch.Tensor, logits: torch.Tensor, bias: torch.Tensor | None,
+                                gate: torch.Tensor, up: torch.Tensor, down: torch.Tensor,
+                                top_k: int, groups: int, selected_groups: int,
+                                group_top_two: bool, renormalize: bool, scale: float = 1.0,
+                                y=None, workspace=None, stream=None) -> torch.Tensor:
+    """The whole local forward with group-limited sigmoid routing."""
+    T, H = x.shape
+    E, I, _ = gate.shape
+    dev = x.device
+    if bias is not None and (bias.dtype != torch.float32 or tuple(bias.shape) != (E,)):
+        raise ValueError("bias must be float32 of shape [E]")
+    y = y if y is not None else torch.empty((T, H), dtype=x.dtype, device=dev)
+    ws = _workspace(moe_forward_workspace_size(T, H, I, E, top_k, x.dtype, logits.dtype),
+                    dev, workspace)
+    rc = load_library().moe_forward_sigmoid_grouped(
+        _ptr(x), _code(x.dtype), _ptr(logits), _code(logits.dtype),
+        None if bias is None else _ptr(bias), _ptr(gate), _ptr(up), _ptr(down), T, H, I, E,
+        int(top_k), int(groups), int(selected_groups), int(bool(group_top_two)),
+        int(bool(renormalize)), float(scale), _ptr(y), _ptr(ws), _nbytes(ws), _stream(stream))
+    _check(rc, "moe_forward_sigmoid_grouped")
     return y
 
 

@@ -19,6 +19,16 @@ cudaError_t launch_route(const void *logits, int ldt, int64_t T, int E,
                          int top_k, int renormalize, uint32_t *idx, void *w,
                          cudaStream_t s);
 
+// Group-limited sigmoid routing (one warp per token); the limits are the
+// caller's to check. Largest top_k and group count the kernel supports.
+cudaError_t launch_route_sigmoid_grouped(const void *logits, int ldt, int64_t T, int E,
+                                         const float *bias, int top_k, int groups,
+                                         int selected_groups, int group_top_two,
+                                         int renormalize, float scale, uint32_t *idx, void *w,
+                                         cudaStream_t s);
+int sigmoid_route_max_top_k();
+int sigmoid_route_max_groups();
+
 // Dispatch: per-chunk histograms, a scan, a stable rank/scatter, a row gather.
 size_t dispatch_workspace_bytes(int64_t A, int E);
 cudaError_t launch_dispatch(const uint32_t *idx, int64_t T, int top_k, int E,

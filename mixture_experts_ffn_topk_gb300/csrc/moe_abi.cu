@@ -3,6 +3,8 @@
 // allocates device memory; nothing here synchronises except
 // moe_device_status().
 #include <math.h>
+
+#include <cmath>
 #include <stdio.h>
 
 #include <atomic>
@@ -82,6 +84,24 @@ int check_route_args(const void *logits, int ldt, int64_t T, int64_t E, int top_
     if (!logits || !idx || !w) return fail(MOE_ERR_NULL, "moe_route: NULL tensor");
     if (!aligned16(logits) || !aligned16(idx) || !aligned16(w))
         return fail(MOE_ERR_ALIGN, "moe_route: tensors must be 16-byte aligned");
+    return MOE_OK;
+}
+
+// Limits of ruDNN section 10 on top of the shared routing checks.
+int check_sigmoid_grouped_args(int64_t E, const float *bias, int top_k, int groups,
+                               int selected_groups, int group_top_two, float scale)
+{
+    if (groups < 1 || groups > sigmoid_route_max_groups() || E % groups != 0)
+        return fail(MOE_ERR_SHAPE, "need 1 <= groups <= 128 dividing E");
+    if (selected_groups < 1 || selected_groups > groups)
+        return fail(MOE_ERR_SHAPE, "need 1 <= selected_groups <= groups");
+    if (top_k > sigmoid_route_max_top_k() || (int64_t)top_k > (int64_t)selected_groups * (E / groups))
+        return fail(MOE_ERR_SHAPE, "need top_k <= 64 and top_k <= selected_groups * E / groups");
+    if (group_top_two && E / groups < 2)
+        return fail(MOE_ERR_SHAPE, "group_top_two needs at least two experts per group");
+    if (!std::isfinite(scale) || !(scale > 0.0f))
+        return fail(MOE_ERR_VALUE, "scale must be finite and > 0");
+    if (bias != nullptr && !aligned16(bias)) return fail(MOE_ERR_ALIGN, "bias must be 16-byte aligned");
     return MOE_OK;
 }
 
@@ -168,6 +188,69 @@ int run_experts(const void *x_disp, const int32_t *offsets, int64_t rows, const 
     return MOE_OK;
 }
 
+// The one-call forward after its routing step: dispatch, experts, combine.
+// route(idx, w, stream) enqueues the routing into the workspace's idx / w.
+template <typename RouteFn>
+int forward_impl(const char *name, const void *x, int dtype, const void *logits,
+                 int logits_dtype, const void *gate, const void *up, const void *down,
+                 int64_t T, int64_t H, int64_t I, int64_t E, int top_k, void *y,
+                 void *workspace, size_t workspace_bytes, void *stream, RouteFn route)
+{
+    if (!valid_dtype(logits_dtype)) return fail(MOE_ERR_DTYPE, "logits dtype must be F32, BF16 or F16");
+    int rc = check_experts_args(T * (int64_t)(top_k > 0 ? top_k : 1), E, H, I, dtype);
+    if (rc != MOE_OK) return rc;
+    if (T < 0 || top_k < 1 || top_k > E || T * top_k > kMaxRows)
+        return fail(MOE_ERR_SHAPE, "need T >= 0 and 1 <= top_k <= E");
+    if (H % 8 != 0) return fail(MOE_ERR_SHAPE, "H must be a multiple of 8");
+    if (T == 0) return MOE_OK;
+    if (!x || !logits || !gate || !up || !down || !y) return fail(MOE_ERR_NULL, name);
+    if (!aligned16(x) || !aligned16(logits) || !aligned16(gate) || !aligned16(up) ||
+        !aligned16(down) || !aligned16(y))
+        return fail(MOE_ERR_ALIGN, "tensors must be 16-byte aligned");
+    const ForwardLayout L = forward_layout(T, H, I, E, top_k, dtype, logits_dtype);
+    if (workspace_bytes < L.total || !workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return fail(MOE_ERR_WORKSPACE, "workspace too small or not 256-byte aligned");
+    unsigned *st = status_ptr();
+    if (!st) return fail(MOE_ERR_CUDA, "cannot resolve the device status word");
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    uint32_t *idx = reinterpret_cast<uint32_t *>(ws + L.idx);
+    void *w = ws + L.w;
+    int32_t *counts = reinterpret_cast<int32_t *>(ws + L.counts);
+    int32_t *offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
+    int32_t *row_of = reinterpret_cast<int32_t *>(ws + L.row_of);
+    int32_t *src_of = reinterpret_cast<int32_t *>(ws + L.src_of);
+    void *x_disp = ws + L.x_disp, *h = ws + L.h, *out_disp = ws + L.out_disp;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t A = T * top_k;
+
+    const bool fused_combine = fold_combine(T, H, dtype);
+    cudaError_t err = cudaSuccess;
+    if (fused_combine) {
+        err = cudaMemsetAsync(out_disp, 0, (size_t)T * (size_t)H * 4, s);
+        if (err != cudaSuccess) return cuda_fail(err, "forward/zero");
+    }
+    err = route(idx, w, s);
+    if (err != cudaSuccess) return cuda_fail(err, "forward/route");
+    err = launch_dispatch(idx, T, top_k, (int)E, x, dtype, H, counts, offsets, row_of, src_of,
+                          x_disp, ws + L.disp_ws, st, s);
+    if (err != cudaSuccess) return cuda_fail(err, "forward/dispatch");
+    if (fused_combine) {
+        err = launch_experts_tc_combine(dtype, x_disp, offsets, A, gate, up, down, (int)E, H, I,
+                                        h, src_of, w, logits_dtype, top_k,
+                                        static_cast<float *>(out_disp), st, s);
+        if (err == cudaErrorInvalidValue)
+            return fail(MOE_ERR_ALIGN, "TMA descriptor rejected (pointer alignment or shape)");
+        if (err != cudaSuccess) return cuda_fail(err, "forward/experts");
+        err = launch_finalize(static_cast<const float *>(out_disp), T, H, y, dtype, s);
+        return err == cudaSuccess ? MOE_OK : cuda_fail(err, "forward/finalize");
+    }
+    rc = run_experts(x_disp, offsets, A, gate, up, down, E, H, I, dtype, h, out_disp, MOE_F32, s);
+    if (rc != MOE_OK) return rc;
+    err = launch_combine(out_disp, MOE_F32, w, logits_dtype, row_of, nullptr, nullptr, MOE_F32,
+                         1.0f, T, top_k, H, y, dtype, nullptr, nullptr, s);
+    return err == cudaSuccess ? MOE_OK : cuda_fail(err, "forward/combine");
+}
+
 }  // namespace
 
 int report_error(int code, const char *what) { return fail(code, what); }
@@ -207,6 +290,22 @@ int moe_route(const void *logits, int logits_dtype, int64_t T, int64_t E, int to
     cudaError_t err = launch_route(logits, logits_dtype, T, (int)E, top_k, renormalize,
                                    expert_indices, weights, static_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_route");
+}
+
+int moe_route_sigmoid_grouped(const void *logits, int logits_dtype, int64_t T, int64_t E,
+                              const float *bias, int top_k, int groups, int selected_groups,
+                              int group_top_two, int renormalize, float scale,
+                              uint32_t *expert_indices, void *weights, void *stream)
+{
+    int rc = check_route_args(logits, logits_dtype, T, E, top_k, expert_indices, weights);
+    if (rc != MOE_OK) return rc;
+    rc = check_sigmoid_grouped_args(E, bias, top_k, groups, selected_groups, group_top_two, scale);
+    if (rc != MOE_OK || T == 0) return rc;
+    cudaError_t err = launch_route_sigmoid_grouped(logits, logits_dtype, T, (int)E, bias, top_k,
+                                                   groups, selected_groups, group_top_two,
+                                                   renormalize, scale, expert_indices, weights,
+                                                   static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_route_sigmoid_grouped");
 }
 
 size_t moe_dispatch_workspace_size(int64_t T, int top_k, int64_t E)
@@ -322,59 +421,33 @@ int moe_forward(const void *x, int dtype, const void *logits, int logits_dtype, 
                 int top_k, int renormalize, void *y, void *workspace, size_t workspace_bytes,
                 void *stream)
 {
-    if (!valid_dtype(logits_dtype)) return fail(MOE_ERR_DTYPE, "logits dtype must be F32, BF16 or F16");
-    int rc = check_experts_args(T * (int64_t)(top_k > 0 ? top_k : 1), E, H, I, dtype);
-    if (rc != MOE_OK) return rc;
-    if (T < 0 || top_k < 1 || top_k > E || T * top_k > kMaxRows)
-        return fail(MOE_ERR_SHAPE, "need T >= 0 and 1 <= top_k <= E");
-    if (H % 8 != 0) return fail(MOE_ERR_SHAPE, "H must be a multiple of 8");
-    if (T == 0) return MOE_OK;
-    if (!x || !logits || !gate || !up || !down || !y) return fail(MOE_ERR_NULL, "moe_forward: NULL tensor");
-    if (!aligned16(x) || !aligned16(logits) || !aligned16(gate) || !aligned16(up) ||
-        !aligned16(down) || !aligned16(y))
-        return fail(MOE_ERR_ALIGN, "moe_forward: tensors must be 16-byte aligned");
-    const ForwardLayout L = forward_layout(T, H, I, E, top_k, dtype, logits_dtype);
-    if (workspace_bytes < L.total || !workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-        return fail(MOE_ERR_WORKSPACE, "moe_forward: workspace too small or not 256-byte aligned");
-    unsigned *st = status_ptr();
-    if (!st) return fail(MOE_ERR_CUDA, "cannot resolve the device status word");
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
-    uint32_t *idx = reinterpret_cast<uint32_t *>(ws + L.idx);
-    void *w = ws + L.w;
-    int32_t *counts = reinterpret_cast<int32_t *>(ws + L.counts);
-    int32_t *offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
-    int32_t *row_of = reinterpret_cast<int32_t *>(ws + L.row_of);
-    int32_t *src_of = reinterpret_cast<int32_t *>(ws + L.src_of);
-    void *x_disp = ws + L.x_disp, *h = ws + L.h, *out_disp = ws + L.out_disp;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int64_t A = T * top_k;
+    return forward_impl("moe_forward: NULL tensor", x, dtype, logits, logits_dtype, gate, up,
+                        down, T, H, I, E, top_k, y, workspace, workspace_bytes, stream,
+                        [&](uint32_t *idx, void *w, cudaStream_t s) {
+                            return launch_route(logits, logits_dtype, T, (int)E, top_k,
+                                                renormalize, idx, w, s);
+                        });
+}
 
-    const bool fused_combine = fold_combine(T, H, dtype);
-    cudaError_t err = cudaSuccess;
-    if (fused_combine) {
-        err = cudaMemsetAsync(out_disp, 0, (size_t)T * (size_t)H * 4, s);
-        if (err != cudaSuccess) return cuda_fail(err, "moe_forward/zero");
+int moe_forward_sigmoid_grouped(const void *x, int dtype, const void *logits, int logits_dtype,
+                                const float *bias, const void *gate, const void *up,
+                                const void *down, int64_t T, int64_t H, int64_t I, int64_t E,
+                                int top_k, int groups, int selected_groups, int group_top_two,
+                                int renormalize, float scale, void *y, void *workspace,
+                                size_t workspace_bytes, void *stream)
+{
+    if (E >= 1 && E <= kMaxE && top_k >= 1) {
+        const int rc = check_sigmoid_grouped_args(E, bias, top_k, groups, selected_groups,
+                                                  group_top_two, scale);
+        if (rc != MOE_OK) return rc;
     }
-    err = launch_route(logits, logits_dtype, T, (int)E, top_k, renormalize, idx, w, s);
-    if (err != cudaSuccess) return cuda_fail(err, "moe_forward/route");
-    err = launch_dispatch(idx, T, top_k, (int)E, x, dtype, H, counts, offsets, row_of, src_of,
-                          x_disp, ws + L.disp_ws, st, s);
-    if (err != cudaSuccess) return cuda_fail(err, "moe_forward/dispatch");
-    if (fused_combine) {
-        err = launch_experts_tc_combine(dtype, x_disp, offsets, A, gate, up, down, (int)E, H, I,
-                                        h, src_of, w, logits_dtype, top_k,
-                                        static_cast<float *>(out_disp), st, s);
-        if (err == cudaErrorInvalidValue)
-            return fail(MOE_ERR_ALIGN, "TMA descriptor rejected (pointer alignment or shape)");
-        if (err != cudaSuccess) return cuda_fail(err, "moe_forward/experts");
-        err = launch_finalize(static_cast<const float *>(out_disp), T, H, y, dtype, s);
-        return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_forward/finalize");
-    }
-    rc = run_experts(x_disp, offsets, A, gate, up, down, E, H, I, dtype, h, out_disp, MOE_F32, s);
-    if (rc != MOE_OK) return rc;
-    err = launch_combine(out_disp, MOE_F32, w, logits_dtype, row_of, nullptr, nullptr, MOE_F32,
-                         1.0f, T, top_k, H, y, dtype, nullptr, nullptr, s);
-    return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_forward/combine");
+    return forward_impl("moe_forward_sigmoid_grouped: NULL tensor", x, dtype, logits,
+                        logits_dtype, gate, up, down, T, H, I, E, top_k, y, workspace,
+                        workspace_bytes, stream, [&](uint32_t *idx, void *w, cudaStream_t s) {
+                            return launch_route_sigmoid_grouped(
+                                logits, logits_dtype, T, (int)E, bias, top_k, groups,
+                                selected_groups, group_top_two, renormalize, scale, idx, w, s);
+                        });
 }
 
 int moe_device_status(void *stream, int clear)

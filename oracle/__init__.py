@@ -307,6 +307,22 @@ def forward(x, dt: str, logits, ldt: str, gate, up, down, top_k: int,
     is the unrounded float64 output ``[T, H]``."""
     lib = lib or load_library()
     idx, w, invalid = route(logits, ldt, top_k, renormalize, lib)
+    return _forward_routed(x, dt, idx, w, ldt, invalid, gate, up, down, lib)
+
+
+def forward_sigmoid_grouped(x, dt: str, logits, ldt: str, bias, gate, up, down, top_k: int,
+                            groups: int, selected_groups: int, group_top_two: bool,
+                            renormalize: bool, scale: float, lib=None):
+    """The same chain with group-limited sigmoid routing (ruDNN user guide,
+    section 10, forward_sigmoid_grouped)."""
+    lib = lib or load_library()
+    idx, w, invalid = route_sigmoid_grouped(logits, ldt, bias, top_k, groups, selected_groups,
+                                            group_top_two, renormalize, scale, lib)
+    return _forward_routed(x, dt, idx, w, ldt, invalid, gate, up, down, lib)
+
+
+def _forward_routed(x, dt, idx, w, ldt, invalid, gate, up, down, lib):
+    top_k = idx.shape[1]
     E = np.asarray(gate).shape[0]
     counts, offsets, row_of, src_of, bad = dispatch(idx, E, lib)
     rows = int(offsets[E])

@@ -74,6 +74,58 @@ def test_route_validation(lib):
     assert b"top_k" in lib.moe_last_error_detail()
 
 
+def test_route_sigmoid_grouped_validation(lib):
+    """ruDNN section 10 limits, checked on the host before any launch."""
+    s = P(None)
+
+    def call(**kw):
+        a = dict(lg=P(FAKE), ldt=BF16, T=4, E=16, bias=P(FAKE), k=2, G=4, S=2, two=1, ren=1,
+                 scale=2.5, idx=P(FAKE), w=P(FAKE))
+        a.update(kw)
+        return lib.moe_route_sigmoid_grouped(a["lg"], a["ldt"], a["T"], a["E"], a["bias"],
+                                             a["k"], a["G"], a["S"], a["two"], a["ren"],
+                                             a["scale"], a["idx"], a["w"], s)
+    assert call(ldt=7) == DTYPE
+    assert call(E=0) == SHAPE
+    assert call(E=1025) == SHAPE
+    assert call(G=0) == SHAPE
+    assert call(G=3) == SHAPE                  # 16 % 3 != 0
+    assert call(E=256, G=256) == SHAPE         # more than 128 groups
+    assert call(S=0) == SHAPE
+    assert call(S=5) == SHAPE                  # more than groups
+    assert call(k=9) == SHAPE                  # more than S * E / G = 8
+    assert call(E=128, G=1, S=1, k=65) == SHAPE    # top_k <= 64
+    assert call(E=8, G=8, S=4, k=2, two=1) == SHAPE   # one expert per group
+    assert call(scale=0.0) == VALUE
+    assert call(scale=-1.0) == VALUE
+    assert call(scale=math.inf) == VALUE
+    assert call(scale=math.nan) == VALUE
+    assert call(bias=P(FAKE_ODD)) == ALIGN
+    assert call(lg=P(None)) == NULL
+    assert call(T=0, lg=P(None), idx=P(None), w=P(None)) == OK
+    call(k=9)
+    assert b"top_k" in lib.moe_last_error_detail()
+
+
+def test_forward_sigmoid_grouped_validation(lib):
+    s = P(None)
+
+    def call(**kw):
+        a = dict(x=P(FAKE), lg=P(FAKE), bias=P(None), T=32, H=64, I=32, E=16, k=2, G=4, S=2,
+                 two=0, scale=1.0, y=P(FAKE), wsb=1 << 30)
+        a.update(kw)
+        return lib.moe_forward_sigmoid_grouped(
+            a["x"], BF16, a["lg"], BF16, a["bias"], P(FAKE), P(FAKE), P(FAKE), a["T"], a["H"],
+            a["I"], a["E"], a["k"], a["G"], a["S"], a["two"], 1, a["scale"], a["y"], P(FAKE),
+            a["wsb"], s)
+    assert call(G=5) == SHAPE
+    assert call(k=9) == SHAPE
+    assert call(scale=0.0) == VALUE
+    assert call(y=P(FAKE_ODD)) == ALIGN
+    assert call(wsb=100) == WORKSPACE
+    assert call(T=0, x=P(None), lg=P(None), y=P(None)) == OK
+
+
 def test_dispatch_validation(lib):
     s = P(None)
     args = lambda **kw: [kw.get("idx", P(FAKE)), kw.get("T", 16), kw.get("k", 2),
