@@ -236,11 +236,31 @@ def run_ours(args, rank, world, local, dist):
     ws_f = torch.empty(moe.moe_forward_workspace_size(T, H, I, E, k, x.dtype, logits.dtype),
                        dtype=torch.uint8, device=dev)
 
+    sigmoid = cfg.routing == "sigmoid_grouped"
+    bias = d.get("bias")
+
+    def route_into(lg):
+        if sigmoid:
+            moe.moe_route_sigmoid_grouped(lg, bias, k, cfg.groups, cfg.selected_groups,
+                                          cfg.group_top_two, cfg.renormalize, cfg.scale,
+                                          expert_indices=idx, weights=w)
+        else:
+            moe.moe_route(lg, k, cfg.renormalize, expert_indices=idx, weights=w)
+
+    def forward(x_, lg):
+        if sigmoid:
+            moe.moe_forward_sigmoid_grouped(x_, lg, bias, d["gate"], d["up"], d["down"], k,
+                                            cfg.groups, cfg.selected_groups, cfg.group_top_two,
+                                            cfg.renormalize, cfg.scale, y=y, workspace=ws_f)
+        else:
+            moe.moe_forward(x_, lg, d["gate"], d["up"], d["down"], k, cfg.renormalize,
+                            y=y, workspace=ws_f)
+
     def step(ev=None):
         # events only at the step boundaries and around the expert GEMMs: an
         # event between two kernels stops the next one from starting early
         if ev: ev[0].record(stream)
-        moe.moe_route(logits, k, cfg.renormalize, expert_indices=idx, weights=w)
+        route_into(logits)
         moe.moe_dispatch(idx, x, E, counts=counts, offsets=offsets, row_of=row_of,
                          src_of=src_of, x_disp=x_disp, workspace=ws_d)
         if ev: ev[1].record(stream)
@@ -261,8 +281,7 @@ def run_ours(args, rank, world, local, dist):
     # Timed region 1 (the headline): K passes of the one-call forward, events
     # only at step boundaries so every kernel may start early (PDL).
     def fwd():
-        moe.moe_forward(x, logits, d["gate"], d["up"], d["down"], k, cfg.renormalize,
-                        y=y, workspace=ws_f)
+        forward(x, logits)
     for _ in range(args.warmup):
         fwd()
         flush.fill_(1)
@@ -304,8 +323,7 @@ def run_ours(args, rank, world, local, dist):
     def e2e():
         x_in.copy_(x_h, non_blocking=True)
         l_in.copy_(l_h, non_blocking=True)
-        moe.moe_forward(x_in, l_in, d["gate"], d["up"], d["down"], k, cfg.renormalize,
-                        y=y, workspace=ws_f)
+        forward(x_in, l_in)
         y_h.copy_(y, non_blocking=True)
     e2e_ms = timed_loop(e2e, args, stream, flush)
     e2e_ms_max = reduce_max(dist, e2e_ms, dev)
@@ -326,7 +344,8 @@ def run_ours(args, rank, world, local, dist):
     eb = x.element_size()
     comb_bytes = A * H * 4 + A * (w.element_size() + 4) + T * H * eb
     disp_bytes = A * 12 + E * 8 + T * H * eb + A * H * eb + A * H * eb
-    route_bytes = T * E * logits.element_size() + A * (4 + w.element_size())
+    route_bytes = (T * E * logits.element_size() + A * (4 + w.element_size())
+                   + (E * 4 if bias is not None else 0))
     hbm = peaks["hbm_gbs"]
     kernels = {
         "route+dispatch": {"ms": statistics.mean(stage_ms["route+dispatch"]),
@@ -348,10 +367,10 @@ def run_ours(args, rank, world, local, dist):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if cfg.dtype == "bf16" else cfg.dtype,
         "data": "synthetic (seeded; random-init expert weights)",
-        "config": {"workload": cfg.name, "T": T, "H": H, "I": I, "E": E, "top_k": k,
-                   "renormalize": cfg.renormalize, "logits_dtype": cfg.logits_dtype,
-                   "global_batch": T * world, "parallelism": f"replicas x{world}",
-                   "l2": "flushed between steps (256 MiB write)"},
+        "config": dict({"workload": cfg.name, "T": T, "H": H, "I": I, "E": E, "top_k": k,
+                        "renormalize": cfg.renormalize, "logits_dtype": cfg.logits_dtype,
+                        "global_batch": T * world, "parallelism": f"replicas x{world}",
+                        "l2": "flushed between steps (256 MiB write)"}, **routing_config(cfg)),
         "e2e": {"value": aggregate(e2e_ms_max / 1e3, T, world), "unit": UNIT,
                 "h2d_bytes_per_step": x.numel() * eb + logits.numel() * logits.element_size(),
                 "d2h_bytes_per_step": y.numel() * eb},
@@ -364,6 +383,15 @@ def run_ours(args, rank, world, local, dist):
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, d, args.cpu_seconds)
     return line
+
+
+def routing_config(cfg):
+    """Config keys naming the routing of a workload."""
+    if cfg.routing != "sigmoid_grouped":
+        return {"routing": "softmax"}
+    return {"routing": "sigmoid_grouped", "groups": cfg.groups,
+            "selected_groups": cfg.selected_groups, "group_top_two": cfg.group_top_two,
+            "scale": cfg.scale, "correction_bias_var": cfg.correction_var}
 
 
 def roofline_entry(tflops, gbs, nbytes, flops, peaks, traffic):
@@ -504,10 +532,16 @@ def oracle_token_rate(cfg, host, seconds, max_threads=None):
     threads = max_threads or os.cpu_count() or 1
     T = cfg.T
 
+    sg = None
+    if cfg.routing == "sigmoid_grouped":
+        sg = {"bias": host.get("bias"), "groups": cfg.groups,
+              "selected_groups": cfg.selected_groups, "group_top_two": cfg.group_top_two,
+              "scale": cfg.scale}
+
     def run(tokens):
         oracle.forward_tokens(tokens, host["x"], cfg.dtype, host["logits"], cfg.logits_dtype,
                               host["gate"], host["up"], host["down"], cfg.top_k,
-                              cfg.renormalize, lib)
+                              cfg.renormalize, lib, sigmoid_grouped=sg)
     t0 = time.perf_counter()
     run(np.array([0]))
     one = max(time.perf_counter() - t0, 1e-4)
@@ -562,8 +596,9 @@ def run_reference(args, rank, world):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": cfg.dtype, "data": "synthetic (seeded; random-init expert weights)",
-            "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E,
-                       "top_k": cfg.top_k, "renormalize": cfg.renormalize},
+            "config": dict({"workload": cfg.name, "T": cfg.T, "H": cfg.H, "I": cfg.I,
+                            "E": cfg.E, "top_k": cfg.top_k, "renormalize": cfg.renormalize},
+                           **routing_config(cfg)),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                              "sample": f"{sum(sizes)} tokens over {args.steps} steps"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,

@@ -20,6 +20,10 @@ method is measured on:
 * ``combine_norm_bf16``    combine + residual Add + RMSNorm, T=8192 H=7168
   top_k=8 E=256: expert outputs [T*8, H] N(0,1) BF16, FP32 logits N(0,1) to
   route with, residual N(0,1) BF16, gamma N(1, 0.1) BF16, eps 1e-6.
+* ``sigmoid_grouped_decode_bf16``  the decode shapes routed by group-limited
+  sigmoid routing: 8 groups of 32 experts, 4 kept, each scored by its two
+  best corrected scores, top_k=8, renormalised, scale 2.5; FP32 logits
+  N(0,1) and an FP32 correction bias N(0, 0.01) drawn by its own generator.
 
 N(m, v) names the variance v; expert weights are N(0, 1/fan_in). BF16 inputs
 are FP32 draws rounded to nearest-even by torch's dtype cast. Seeds are
@@ -49,6 +53,14 @@ class MoeConfig:
     logit_bias: str = "none"   # "none" | "normal" | "zipf"
     bias_param: float = 0.0    # variance of the normal bias, or Zipf s
     special_rows: bool = False
+    # routing: "softmax" (top-k of the softmax) or "sigmoid_grouped"
+    # (group-limited sigmoid routing with the fields below)
+    routing: str = "softmax"
+    groups: int = 1
+    selected_groups: int = 1
+    group_top_two: bool = False
+    scale: float = 1.0
+    correction_var: float = 0.0   # variance of the FP32 correction bias (0: none)
 
     @property
     def seed(self) -> int:
@@ -97,6 +109,10 @@ CONFIGS = {
                              top_k=8, renormalize=True, dtype="bf16",
                              logits_dtype="f32", logit_bias="zipf",
                              bias_param=1.1),
+    "sigmoid_grouped_decode_bf16": MoeConfig(
+        "sigmoid_grouped_decode_bf16", 6, T=128, H=7168, I=2048, E=256, top_k=8,
+        renormalize=True, dtype="bf16", logits_dtype="f32", routing="sigmoid_grouped",
+        groups=8, selected_groups=4, group_top_two=True, scale=2.5, correction_var=0.01),
 }
 
 COMBINE_NORM = CombineNormConfig("combine_norm_bf16", 5, T=8192, H=7168, E=256,
@@ -183,7 +199,23 @@ def moe_inputs(cfg: MoeConfig, device="cpu", seed: int | None = None,
                  dtype=cfg.dtype, chunk_rows=rows)
     down = _normal((cfg.E, cfg.H, cfg.I), gw, wdev, std=cfg.I ** -0.5,
                    dtype=cfg.dtype, chunk_rows=rows)
-    return {"x": x, "logits": logits, "gate": gate, "up": up, "down": down}
+    out = {"x": x, "logits": logits, "gate": gate, "up": up, "down": down}
+    if cfg.routing == "sigmoid_grouped":
+        b = correction_bias(cfg, device, seed)
+        if b is not None:
+            out["bias"] = b
+    return out
+
+
+def correction_bias(cfg: MoeConfig, device="cpu", seed: int | None = None):
+    """FP32 [E] correction bias N(0, correction_var) for sigmoid routing, or
+    None; drawn by a generator of its own (seed + 31) on the CPU."""
+    if cfg.correction_var <= 0.0:
+        return None
+    seed = cfg.seed if seed is None else seed
+    g = _gen(seed + 31, "cpu")
+    b = torch.randn((cfg.E,), generator=g, dtype=torch.float32) * math.sqrt(cfg.correction_var)
+    return b.to(device)
 
 
 def combine_norm_inputs(cfg: CombineNormConfig, device="cpu",

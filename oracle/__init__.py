@@ -335,16 +335,24 @@ def _forward_routed(x, dt, idx, w, ldt, invalid, gate, up, down, lib):
 
 
 def forward_tokens(tokens, x, dt: str, logits, ldt: str, gate, up, down,
-                   top_k: int, renormalize: bool, lib=None):
+                   top_k: int, renormalize: bool, lib=None, sigmoid_grouped=None):
     """The same chain evaluated for a subset of tokens only (used to sample
     full-size workloads). A token's output depends only on its own row of x
-    and logits, so this equals rows ``tokens`` of :func:`forward`. Returns
-    ``(idx, w, y)`` for those tokens."""
+    and logits, so this equals rows ``tokens`` of :func:`forward`. With
+    ``sigmoid_grouped`` a dict of :func:`route_sigmoid_grouped`'s arguments
+    (bias, groups, selected_groups, group_top_two, scale), the tokens are
+    routed that way instead. Returns ``(idx, w, y)`` for those tokens."""
     lib = lib or load_library()
     tokens = np.asarray(tokens, dtype=np.int64)
     lg = _arr(logits, ldt)[tokens]
     xs = _arr(x, dt)[tokens]
-    idx, w, _ = route(lg, ldt, top_k, renormalize, lib)
+    if sigmoid_grouped is None:
+        idx, w, _ = route(lg, ldt, top_k, renormalize, lib)
+    else:
+        sg = sigmoid_grouped
+        idx, w, _ = route_sigmoid_grouped(lg, ldt, sg["bias"], top_k, sg["groups"],
+                                          sg["selected_groups"], sg["group_top_two"],
+                                          renormalize, sg["scale"], lib)
     n = tokens.size
     rows = np.repeat(xs, top_k, axis=0)
     out = swiglu_rows(rows, dt, idx.reshape(-1).astype(np.int32), gate, up,

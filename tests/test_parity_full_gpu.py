@@ -107,3 +107,55 @@ def test_full_combine_add_rmsnorm(dev):
                  "rstd")
     del d, y, x_out
     _free()
+
+
+def test_full_forward_sigmoid_grouped_sampled(dev):
+    """The decode shapes with group-limited sigmoid routing (ruDNN user guide,
+    section 10), through moe_forward_sigmoid_grouped: routing in full (ids
+    exact outside near-ties, see test_sigmoid_grouped_gpu), y on sampled
+    tokens."""
+    from test_sigmoid_grouped_gpu import near_tie_rows
+    cfg = W.CONFIGS["sigmoid_grouped_decode_bf16"]
+    d = W.moe_inputs(cfg, device=dev)
+    T, k, E = cfg.T, cfg.top_k, cfg.E
+    bias = d.get("bias")
+    y = moe.moe_forward_sigmoid_grouped(d["x"], d["logits"], bias, d["gate"], d["up"],
+                                        d["down"], k, cfg.groups, cfg.selected_groups,
+                                        cfg.group_top_two, cfg.renormalize, cfg.scale)
+    idx, w = moe.moe_route_sigmoid_grouped(d["logits"], bias, k, cfg.groups,
+                                           cfg.selected_groups, cfg.group_top_two,
+                                           cfg.renormalize, cfg.scale)
+    torch.cuda.synchronize()
+    assert moe.moe_device_status() == 0
+    logits_np, x_np = np_of(d["logits"]), np_of(d["x"])
+    bias_np = None if bias is None else bias.cpu().numpy()
+    idx_ref, w_ref, _ = oracle.route_sigmoid_grouped(logits_np, cfg.logits_dtype, bias_np, k,
+                                                     cfg.groups, cfg.selected_groups,
+                                                     cfg.group_top_two, cfg.renormalize,
+                                                     cfg.scale)
+    skip = set(near_tie_rows(logits_np.astype(np.float32), bias_np, k, cfg.groups,
+                             cfg.selected_groups, cfg.group_top_two))
+    assert len(skip) <= 2
+    keep = np.array([t for t in range(T) if t not in skip])
+    assert np.array_equal(idx.cpu().numpy().view(np.uint32)[keep], idx_ref[keep])
+    assert_close(to_f64(w)[keep], oracle.to_f64(w_ref, cfg.logits_dtype)[keep],
+                 cfg.logits_dtype, "w")
+
+    rng = np.random.default_rng(cfg.seed)
+    tokens = np.array(sorted(set(rng.choice(keep, 8, replace=False).tolist()) | {int(keep[0])}))
+    sel = idx_ref[tokens]
+    experts = np.unique(sel)
+    remap = {int(e): i for i, e in enumerate(experts)}
+    ex_t = torch.from_numpy(experts.astype(np.int64)).to(dev)
+    gate = np_of(d["gate"].index_select(0, ex_t))
+    up = np_of(d["up"].index_select(0, ex_t))
+    down = np_of(d["down"].index_select(0, ex_t))
+    rows = np.repeat(x_np[tokens], k, axis=0)
+    eor = np.array([remap[int(e)] for e in sel.reshape(-1)], np.int32)
+    out = oracle.swiglu_rows(rows, cfg.dtype, eor, gate, up, down)
+    y_ref = oracle.combine(out, "f64", w_ref[tokens], cfg.logits_dtype,
+                           np.arange(tokens.size * k, dtype=np.int32), k)
+    assert_close(to_f64(y[torch.from_numpy(tokens).to(dev)]), y_ref, cfg.dtype,
+                 "sigmoid-routed sampled y")
+    del d, y
+    _free()
