@@ -92,6 +92,9 @@ def _bind(lib):
     lib.oracle_experts_dispatched.restype = _INT
     lib.oracle_combine.argtypes = [_P, _INT, _P, _INT, _P, _I64, _I64, _I64, _P]
     lib.oracle_combine.restype = None
+    lib.oracle_combine_v2.argtypes = [_P, _INT, _P, _INT, _P, _P, _I64, _I64, _I64, _I64,
+                                      _P, _P, _P, _P, _P, _P, _INT, _INT, _I64, _I64, _I64, _P]
+    lib.oracle_combine_v2.restype = _INT
     lib.oracle_rmsnorm.argtypes = [_P, _INT, _P, _INT, _F, _I64, _I64, _P,
                                    _INT, _P]
     lib.oracle_rmsnorm.restype = _INT
@@ -257,6 +260,39 @@ def combine(out_disp, odt: str, w, wdt: str, row_of, top_k: int, lib=None):
     y = np.empty((T, H), dtype=np.float64)
     lib.oracle_combine(_ptr(out_disp), DTYPE_CODES[odt], _ptr(w),
                        DTYPE_CODES[wdt], _ptr(row_of), T, top_k, H, _ptr(y))
+    return y
+
+
+def combine_v2(out_disp, odt: str, w, wdt: str, row_of, top_k: int, xdt: str, ids=None,
+               E: int = 0, zero: int = 0, copy: int = 0, const: int = 0, ori_x=None,
+               alpha1=None, alpha2=None, const_v=None, shared_x=None, mask=None, lib=None):
+    """Combine of aclnnMoeDistributeCombineAddRmsNormV2 (special experts,
+    shared expert, active mask). ``mask`` is None, bool [T] or bool [T, k];
+    ``ori_x``, ``alpha1``, ``alpha2``, ``const_v``, ``shared_x`` in ``xdt``
+    storage. Returns the unrounded float64 ``[T, H]``."""
+    lib = lib or load_library()
+    out_disp = _arr(out_disp, odt)
+    w = _arr(w, wdt)
+    T = w.shape[0]
+    H = out_disp.shape[1]
+    row_of = np.ascontiguousarray(row_of, dtype=np.int32)
+    ids_a = None if ids is None else np.ascontiguousarray(ids, dtype=np.uint32)
+    opt = {n: (None if v is None else _arr(v, xdt)) for n, v in
+           dict(ori_x=ori_x, alpha1=alpha1, alpha2=alpha2, const_v=const_v,
+                shared_x=shared_x).items()}
+    mask_a = None if mask is None else np.ascontiguousarray(mask, dtype=np.uint8)
+    mdims = 0 if mask_a is None else mask_a.ndim
+    y = np.empty((T, H), dtype=np.float64)
+    p = lambda a: None if a is None else _ptr(a)
+    rc = lib.oracle_combine_v2(_ptr(out_disp), DTYPE_CODES[odt], _ptr(w), DTYPE_CODES[wdt],
+                               _ptr(row_of), p(ids_a), E, zero, copy, const, p(opt["ori_x"]),
+                               p(opt["alpha1"]), p(opt["alpha2"]), p(opt["const_v"]),
+                               p(opt["shared_x"]), p(mask_a), mdims, DTYPE_CODES[xdt], T,
+                               top_k, H, _ptr(y))
+    if rc == -2:
+        raise ValueError("oracle_combine_v2: a 1-D active mask must keep its tokens first")
+    if rc != 0:
+        raise ValueError("oracle_combine_v2: missing inputs for the configured experts or mask")
     return y
 
 

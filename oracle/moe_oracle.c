@@ -38,6 +38,12 @@
  *              x = combineOut + residualX,
  *              y = x / sqrt(mean(x^2) + normEps) * gamma; outputs yOut, xOut
  *              (residual dtype) and rstdOut (FP32, one per token).
+ *   [Ascend-CARN-V2] the same operator's formula and parameter list:
+ *              combineOut = Sum(expertScales * ataOut + expertScales *
+ *              sharedExpertX); special experts by id range after the
+ *              moeExpertNum routed experts: zero (output 0), copy (output
+ *              oriX), const (alpha1 * oriX + alpha2 * V); xActiveMask 1-D
+ *              [BS] (kept tokens first) or 2-D [BS, K].
  *   [aclnnFFN] aclnnFFN, "Formula": y = activation(x W1 + b1) W2 + b2; the
  *              experts here are its bias-free, SwiGLU-activated case.
  *
@@ -446,6 +452,80 @@ void oracle_combine(const void *out_disp, int odt, const void *w, int wdt,
             y[t * H + h] = acc;
         }
     }
+}
+
+/* ---- combine with special experts, shared expert, active mask
+ *      [Ascend-CARN-V2] -------------------------------------------------- */
+
+/*
+ * The combine of aclnnMoeDistributeCombineAddRmsNormV2 on one device. For
+ * each token t and each slot j that the active mask keeps (mask_dims 0: all;
+ * 1: mask[t] keeps or drops the token's every slot; 2: mask[t*k+j]), with
+ * id = ids[t*k+j] and scale s = w[t*k+j]:
+ *   id < E                        o = the dispatched row out_disp[row_of[.]]
+ *   E <= id < E+zero              o = 0                      (zero expert)
+ *   ... < E+zero+copy             o = ori_x[t]               (copy expert)
+ *   ... < E+zero+copy+const_n     o = alpha1[c]*ori_x[t] + alpha2[c]*V[c],
+ *                                 c = id - E - zero - copy   (const expert)
+ * and combineOut[t] = sum_j (s*o + s*shared_x[t]), the formula's shared term
+ * taken as printed (one per kept slot, scaled like it; no term without
+ * shared_x). ids may be NULL when no special experts are configured (every
+ * slot is then a dispatched expert). A slot with a dispatched id but no row
+ * (row_of < 0), or an id past the last special expert, makes the token's
+ * output NaN. ori_x, alpha1/2, V and shared_x are in dtype xdt. Sums in
+ * double. Returns -1 on missing inputs for the configured special experts or
+ * a bad mask_dims, -2 if a 1-D mask keeps a token after dropping one (the
+ * operator requires the kept tokens first), else 0.
+ */
+int oracle_combine_v2(const void *out_disp, int odt, const void *w, int wdt,
+                      const int32_t *row_of, const uint32_t *ids, int64_t E, int64_t zero_n,
+                      int64_t copy_n, int64_t const_n, const void *ori_x,
+                      const void *alpha1, const void *alpha2, const void *const_v,
+                      const void *shared_x, const uint8_t *mask, int mask_dims, int xdt,
+                      int64_t T, int64_t top_k, int64_t H, double *y)
+{
+    const int64_t special = zero_n + copy_n + const_n;
+    if (zero_n < 0 || copy_n < 0 || const_n < 0 || mask_dims < 0 || mask_dims > 2 ||
+        (mask_dims && !mask) || (special > 0 && !ids) ||
+        ((copy_n > 0 || const_n > 0) && !ori_x) ||
+        (const_n > 0 && (!alpha1 || !alpha2 || !const_v)))
+        return -1;
+    if (mask_dims == 1)
+        for (int64_t t = 1; t < T; ++t)
+            if (mask[t] && !mask[t - 1]) return -2;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t h = 0; h < H; ++h) {
+            double acc = 0.0;
+            for (int64_t j = 0; j < top_k; ++j) {
+                const int64_t a = t * top_k + j;
+                if (mask_dims == 1 && !mask[t]) continue;
+                if (mask_dims == 2 && !mask[a]) continue;
+                const int64_t id = ids ? (int64_t)ids[a] : 0;
+                const double sc = load_elem(w, wdt, a);
+                double o;
+                if (!ids || id < E) {
+                    const int64_t r = row_of[a];
+                    if (r < 0) { acc = NAN; break; }
+                    o = load_elem(out_disp, odt, r * H + h);
+                } else if (id < E + zero_n) {
+                    o = 0.0;
+                } else if (id < E + zero_n + copy_n) {
+                    o = load_elem(ori_x, xdt, t * H + h);
+                } else if (id < E + special) {
+                    const int64_t c = id - E - zero_n - copy_n;
+                    o = load_elem(alpha1, xdt, c) * load_elem(ori_x, xdt, t * H + h) +
+                        load_elem(alpha2, xdt, c) * load_elem(const_v, xdt, c * H + h);
+                } else {
+                    acc = NAN;
+                    break;
+                }
+                acc += sc * o;
+                if (shared_x) acc += sc * load_elem(shared_x, xdt, t * H + h);
+            }
+            y[t * H + h] = acc;
+        }
+    }
+    return 0;
 }
 
 /* ---- RMSNorm [ruDNN-7], Add + RMSNorm [Ascend-CARN] --------------------- */

@@ -472,6 +472,87 @@ def check_combine_weighted(lib):
 
 # -------------------------------------------------------------------- rmsnorm
 
+def check_combine_v2_hand_cases(lib):
+    """aclnnMoeDistributeCombineAddRmsNormV2 (formula and parameter list):
+    special experts by id range after the E routed experts, the shared-expert
+    term inside the sum over slots, and the active mask. Each case is worked
+    by hand (H = 2)."""
+    f = np.float32
+    cv = lambda out, w, rows, k, **kw: oracle.combine_v2(
+        np.array(out, f), "f32", np.array(w, f), "f32", np.array(rows, np.int32), k, "f32",
+        lib=lib, **{n: (np.array(v, f) if n in ("ori_x", "alpha1", "alpha2", "const_v",
+                                                  "shared_x") else v) for n, v in kw.items()})
+    out = [[1, 2], [0, 1]]
+    # zero expert (id 2 with E=2, zero=1): 0.5*[1,2] + 0.5*0
+    y = cv(out, [[0.5, 0.5]], [0, -1], 2, ids=[[0, 2]], E=2, zero=1)
+    assert y.tolist() == [[0.5, 1.0]]
+    # copy expert (E=2, zero=1, copy=1 -> id 3): 0.25 * oriX
+    y = cv(out, [[0.25]], [-1], 1, ids=[[3]], E=2, zero=1, copy=1, ori_x=[[4, -2]])
+    assert y.tolist() == [[1.0, -0.5]]
+    # const expert c = 1 (E=2, const=2 -> ids 2, 3): 0.5*(2*[1,2] + 3*[1,1])
+    y = cv(out, [[0.5]], [-1], 1, ids=[[3]], E=2, const=2, ori_x=[[1, 2]], alpha1=[7, 2],
+           alpha2=[5, 3], const_v=[[9, 9], [1, 1]])
+    assert y.tolist() == [[2.5, 3.5]]
+    # shared expert, weights summing to 1/2: [0.25,0.25] + (0.25+0.25)*[8,4]
+    y = cv([[1, 0], [0, 1]], [[0.25, 0.25]], [0, 1], 2, shared_x=[[8, 4]])
+    assert y.tolist() == [[4.25, 2.25]]
+    # 2-D mask keeps slot 0 only, shared term included for it: 0.25*[1,0] + 0.25*[8,4]
+    y = cv([[1, 0], [0, 1]], [[0.25, 0.75]], [0, 1], 2, shared_x=[[8, 4]],
+           mask=np.array([[True, False]]))
+    assert y.tolist() == [[2.25, 1.0]]
+    # 1-D mask drops token 1 entirely (no shared term either)
+    y = cv([[1, 0], [0, 1]], [[1.0], [1.0]], [0, 1], 1, shared_x=[[8, 4], [8, 4]],
+           mask=np.array([True, False]))
+    assert y.tolist() == [[9.0, 4.0], [0.0, 0.0]]
+    # an id past the last special expert, or a routed id without a row: NaN
+    y = cv(out, [[1.0]], [0], 1, ids=[[5]], E=2, zero=1, copy=1, ori_x=[[3, 3]])
+    assert np.isnan(y).all()
+    y = cv(out, [[1.0]], [-1], 1, ids=[[1]], E=2, zero=1)
+    assert np.isnan(y).all()
+    # a 1-D mask that keeps a token after a dropped one is rejected
+    try:
+        cv(out, [[1.0], [1.0]], [0, 1], 1, mask=np.array([False, True]))
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("1-D mask order not enforced")
+
+
+def check_combine_v2_invariants(lib):
+    """Random inputs: with no extras it is the (separately pinned) combine;
+    a const expert with alpha = (1, 0) is a copy expert; a masked slot is a
+    slot of weight 0; with weights renormalised to 1 the shared expert adds
+    its row once."""
+    rng = np.random.default_rng(17)
+    T, k, H, E = 9, 3, 12, 4
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    idx, w, _ = oracle.route(logits, "f32", k, True, lib)
+    _, _, row_of, _, _ = oracle.dispatch(idx, E, lib)
+    out = rng.standard_normal((T * k, H)).astype(np.float32)
+    base = oracle.combine(out, "f32", w, "f32", row_of, k, lib)
+    y = oracle.combine_v2(out, "f32", w, "f32", row_of, k, "f32", lib=lib)
+    assert np.array_equal(y, base)
+    shared = rng.standard_normal((T, H)).astype(np.float32)
+    y = oracle.combine_v2(out, "f32", w, "f32", row_of, k, "f32", shared_x=shared, lib=lib)
+    assert np.allclose(y, base + shared.astype(np.float64), rtol=1e-6, atol=1e-6)
+    mask = rng.random((T, k)) < 0.6
+    y = oracle.combine_v2(out, "f32", w, "f32", row_of, k, "f32", mask=mask, lib=lib)
+    w0 = np.where(mask, w, np.float32(0))
+    assert np.allclose(y, oracle.combine(out, "f32", w0, "f32", row_of, k, lib), rtol=1e-12,
+                       atol=1e-12)
+    ori = rng.standard_normal((T, H)).astype(np.float32)
+    ids = idx.copy()
+    ids[:, 1] = E + 1                      # copy expert (zero=1, copy=1) vs const with (1, 0)
+    a = oracle.combine_v2(out, "f32", w, "f32", row_of, k, "f32", ids=ids, E=E, zero=1,
+                          copy=1, ori_x=ori, lib=lib)
+    ids[:, 1] = E + 1                      # const expert 0 (zero=1, copy=0)
+    b = oracle.combine_v2(out, "f32", w, "f32", row_of, k, "f32", ids=ids, E=E, zero=1,
+                          const=1, ori_x=ori, alpha1=np.ones(1, np.float32),
+                          alpha2=np.zeros(1, np.float32), const_v=np.full((1, H), 7, np.float32),
+                          lib=lib)
+    assert np.array_equal(a, b)
+
+
 def check_rmsnorm_golden(lib):
     for fields in _lines("rmsnorm_cases.txt"):
         H = int(fields[0].split()[0])

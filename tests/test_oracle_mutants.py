@@ -79,6 +79,22 @@ MUTANTS = [
     ("sg_scale_dropped", "(double)(pick[j] * scale)", "(double)(pick[j])"),
     ("sg_no_renormalise", "pick[j] = pick[j] / zsum;", "pick[j] = pick[j];"),
     ("sg_nan_row_valid", "if (isnan(c[e])) has_nan = 1;", "if (isnan(c[e])) has_nan = 0;"),
+    # combine with special experts, shared expert and active mask
+    ("cv2_zero_is_copy", "        } else if (id < E + zero_n) {\n                    o = 0.0;",
+     "        } else if (id < E + zero_n) {\n                    o = load_elem(ori_x ? ori_x : out_disp, ori_x ? xdt : odt, t * H + h);"),
+    ("cv2_copy_is_zero", "o = load_elem(ori_x, xdt, t * H + h);\n                } else if",
+     "o = 0.0;\n                } else if"),
+    ("cv2_const_alphas_swapped",
+     "o = load_elem(alpha1, xdt, c) * load_elem(ori_x, xdt, t * H + h) +\n                        load_elem(alpha2, xdt, c)",
+     "o = load_elem(alpha2, xdt, c) * load_elem(ori_x, xdt, t * H + h) +\n                        load_elem(alpha1, xdt, c)"),
+    ("cv2_const_index_off", "const int64_t c = id - E - zero_n - copy_n;",
+     "const int64_t c = (id - E - zero_n - copy_n + 1) % const_n;"),
+    ("cv2_shared_unscaled", "if (shared_x) acc += sc * load_elem(shared_x, xdt, t * H + h);",
+     "if (shared_x && j == 0) acc += load_elem(shared_x, xdt, t * H + h);"),
+    ("cv2_mask2_ignored", "if (mask_dims == 2 && !mask[a]) continue;", "if (mask_dims == 3) continue;"),
+    ("cv2_mask1_ignored", "if (mask_dims == 1 && !mask[t]) continue;", "if (mask_dims == 3) continue;"),
+    ("cv2_invalid_id_is_zero", "                } else {\n                    acc = NAN;\n                    break;\n                }",
+     "                } else {\n                    o = 0.0;\n                }"),
     ("sg_sigmoid_wrong_sign", "return (float)(1.0 / (1.0 + exp(-(double)x)));",
      "return (float)(1.0 / (1.0 + exp((double)x)));"),
 ]
