@@ -164,6 +164,20 @@ int moe_dispatch(const uint32_t *expert_indices, int64_t T, int top_k,
                  size_t workspace_bytes, void *stream);
 
 /*
+ * moe_dispatch_special -- moe_dispatch for routing that also names special
+ * experts (aclnnMoeDistributeCombineAddRmsNormV2, parameter list: zero, copy
+ * and const experts take the ids after the E routed experts). Ids in
+ * [E, E + special_experts) get no dispatched row (row_of = -1) and are not
+ * reported as bad indices; moe_combine_v2 computes their contribution. Ids
+ * >= E + special_experts are bad indices as in moe_dispatch. Arguments,
+ * workspace and errors are those of moe_dispatch; special_experts >= 0.
+ */
+int moe_dispatch_special(const uint32_t *expert_indices, int64_t T, int top_k, int64_t E,
+                         int64_t special_experts, const void *x, int x_dtype, int64_t H,
+                         int32_t *counts, int32_t *offsets, int32_t *row_of, int32_t *src_of,
+                         void *x_disp, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * moe_dispatch_noalloc -- moe_dispatch for callers that cannot allocate.
  * The source pages have no counterpart to this call; it exists for callers
  * that cannot supply device scratch memory: code whose device memory belongs
@@ -267,6 +281,82 @@ int moe_combine_add_rmsnorm(const void *out_disp, int out_dtype,
                             int dtype, const void *gamma, int gamma_dtype,
                             float eps, int64_t T, int top_k, int64_t H,
                             void *y, void *x_out, float *rstd, void *stream);
+
+/*
+ * Optional inputs of moe_combine_v2 (aclnnMoeDistributeCombineAddRmsNormV2,
+ * formula and parameter list). All pointers are device pointers owned by the
+ * caller; a NULL pointer or zero count turns the feature off.
+ *   expert_indices   [T, top_k] uint32 ids the tokens were routed to; needed
+ *                    when any special experts are configured.
+ *   num_experts      E: ids below E are routed experts (rows via row_of).
+ *   zero_experts     ids [E, E+zero) contribute 0 (zero experts).
+ *   copy_experts     the next copy_experts ids contribute ori_x[t].
+ *   const_experts    the next const_experts ids, c = id - E - zero - copy,
+ *                    contribute const_alpha1[c] * ori_x[t]
+ *                    + const_alpha2[c] * const_v[c].
+ *   ori_x            [T, H] in the activation dtype: the tokens before the
+ *                    FFN (needed for copy or const experts; 16-byte aligned).
+ *   const_alpha1/2   [const_experts] in the activation dtype.
+ *   const_v          [const_experts, H] in the activation dtype (aligned).
+ *   shared_expert_x  [T, H] in the activation dtype, or NULL: the shared
+ *                    expert's output, added once per kept slot scaled by
+ *                    that slot's weight, as the formula prints it.
+ *   active_mask      NULL, [T] (active_mask_dims 1) or [T, top_k] (2) bytes,
+ *                    nonzero = kept. A dropped token (1-D) or slot (2-D)
+ *                    contributes nothing. The operator requires a 1-D mask to
+ *                    keep its tokens first; here each token follows its flag.
+ */
+typedef struct moe_combine_extras {
+    const uint32_t *expert_indices;
+    int64_t num_experts;
+    int64_t zero_experts;
+    int64_t copy_experts;
+    int64_t const_experts;
+    const void *ori_x;
+    const void *const_alpha1;
+    const void *const_alpha2;
+    const void *const_v;
+    const void *shared_expert_x;
+    const uint8_t *active_mask;
+    int active_mask_dims;
+} moe_combine_extras;
+
+/*
+ * moe_combine_v2 -- the local math of aclnnMoeDistributeCombineAddRmsNormV2:
+ * combineOut[t] = sum over kept slots j of (w[t,j] * o_j + w[t,j] * sharedX[t])
+ * with o_j the routed expert's row out_disp[row_of[t*top_k+j]] or the
+ * special expert's output (see moe_combine_extras); then, when residual is
+ * not NULL, x = combineOut + residual (x_out, rounded to dtype), rstd and
+ * y = x / sqrt(mean(x^2) + eps) * gamma exactly as moe_combine_add_rmsnorm;
+ * when residual is NULL, y = combineOut rounded to dtype and gamma, eps,
+ * x_out, rstd are unused. extras may be NULL (then this is moe_combine or
+ * moe_combine_add_rmsnorm). A routed slot without a row, or an id past the
+ * last special expert, makes the token's row NaN. Arguments and errors as
+ * moe_combine / moe_combine_add_rmsnorm, plus MOE_ERR_NULL / MOE_ERR_ALIGN /
+ * MOE_ERR_SHAPE for inconsistent extras.
+ */
+int moe_combine_v2(const void *out_disp, int out_dtype, const void *weights, int weights_dtype,
+                   const int32_t *row_of, const moe_combine_extras *extras,
+                   const void *residual, const void *gamma, int gamma_dtype, float eps,
+                   int64_t T, int top_k, int64_t H, void *y, int dtype, void *x_out,
+                   float *rstd, void *stream);
+
+/*
+ * moe_rmsnorm -- RMSNorm over the last axis.
+ * ruDNN user guide, section 7 "LayerNorm, RMSNorm and Softmax".
+ *
+ *   x      [rows, H] in dtype (F32/BF16/F16), read only; H % 8 == 0,
+ *          1 <= H <= 16384.
+ *   gamma  [H] in gamma_dtype (F32, or dtype).
+ *   eps    finite and > 0.
+ *   y      [rows, H] in dtype, written: x / sqrt(mean(x^2) + eps) * gamma.
+ *   rstd   [rows] FP32, written when not NULL: 1 / sqrt(mean(x^2) + eps).
+ * Statistics and the affine step in FP32, output rounded once to dtype.
+ * Errors: MOE_ERR_NULL, MOE_ERR_SHAPE, MOE_ERR_DTYPE, MOE_ERR_VALUE (eps),
+ * MOE_ERR_ALIGN, MOE_ERR_CUDA.
+ */
+int moe_rmsnorm(const void *x, int dtype, const void *gamma, int gamma_dtype, float eps,
+                int64_t rows, int64_t H, void *y, float *rstd, void *stream);
 
 /*
  * moe_forward -- the whole local forward in one call: route, dispatch,

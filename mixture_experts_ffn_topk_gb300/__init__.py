@@ -38,7 +38,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_NULL", 2: "MOE_ERR_SHAPE",
 
 EXPORTED = ["moe_status_string", "moe_abi_version", "moe_last_error_detail",
             "moe_route", "moe_route_sigmoid_grouped", "moe_dispatch_workspace_size",
-            "moe_dispatch",
+            "moe_dispatch", "moe_dispatch_special", "moe_combine_v2", "moe_rmsnorm",
             "moe_dispatch_noalloc",
             "moe_experts_workspace_size", "moe_experts_forward", "moe_combine",
             "moe_combine_add_rmsnorm", "moe_forward_workspace_size",
@@ -49,6 +49,16 @@ _lib = None
 
 _P, _I64, _INT, _SZ, _F = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
                            ctypes.c_size_t, ctypes.c_float)
+
+
+class CombineExtras(ctypes.Structure):
+    """Mirror of ``moe_combine_extras`` (include/moe.h)."""
+    _fields_ = [("expert_indices", ctypes.c_void_p), ("num_experts", ctypes.c_int64),
+                ("zero_experts", ctypes.c_int64), ("copy_experts", ctypes.c_int64),
+                ("const_experts", ctypes.c_int64), ("ori_x", ctypes.c_void_p),
+                ("const_alpha1", ctypes.c_void_p), ("const_alpha2", ctypes.c_void_p),
+                ("const_v", ctypes.c_void_p), ("shared_expert_x", ctypes.c_void_p),
+                ("active_mask", ctypes.c_void_p), ("active_mask_dims", ctypes.c_int)]
 
 
 class MoeError(RuntimeError):
@@ -73,6 +83,11 @@ def _bind(lib):
                           _P, _P, _SZ, _P], _INT),
         "moe_dispatch_noalloc": ([_P, _I64, _INT, _I64, _P, _INT, _I64, _P, _P, _P,
                                   _P, _P, _P], _INT),
+        "moe_dispatch_special": ([_P, _I64, _INT, _I64, _I64, _P, _INT, _I64, _P, _P, _P,
+                                  _P, _P, _P, _SZ, _P], _INT),
+        "moe_combine_v2": ([_P, _INT, _P, _INT, _P, ctypes.POINTER(CombineExtras), _P, _P,
+                            _INT, _F, _I64, _INT, _I64, _P, _INT, _P, _P, _P], _INT),
+        "moe_rmsnorm": ([_P, _INT, _P, _INT, _F, _I64, _I64, _P, _P, _P], _INT),
         "moe_experts_workspace_size": ([_I64, _I64, _I64, _I64, _INT], _SZ),
         "moe_experts_forward": ([_P, _P, _I64, _P, _P, _P, _I64, _I64, _I64,
                                  _INT, _P, _INT, _P, _SZ, _P], _INT),
@@ -237,6 +252,30 @@ def moe_dispatch(expert_indices: torch.Tensor, x: torch.Tensor, E: int,
             "src_of": src_of, "x_disp": x_disp}
 
 
+def moe_dispatch_special(expert_indices: torch.Tensor, x: torch.Tensor, E: int,
+                         special_experts: int, counts=None, offsets=None, row_of=None,
+                         src_of=None, x_disp=None, workspace=None, stream=None) -> dict:
+    """:func:`moe_dispatch` where ids in ``[E, E + special_experts)`` name
+    special experts: no dispatched row, not a bad index."""
+    T, k = expert_indices.shape
+    H = x.shape[1]
+    dev = x.device
+    A = T * k
+    counts = counts if counts is not None else torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = offsets if offsets is not None else torch.empty(E + 1, dtype=torch.int32, device=dev)
+    row_of = row_of if row_of is not None else torch.empty(A, dtype=torch.int32, device=dev)
+    src_of = src_of if src_of is not None else torch.empty(A, dtype=torch.int32, device=dev)
+    x_disp = x_disp if x_disp is not None else torch.empty((A, H), dtype=x.dtype, device=dev)
+    ws = _workspace(moe_dispatch_workspace_size(T, k, E), dev, workspace)
+    rc = load_library().moe_dispatch_special(
+        _ptr(expert_indices), T, k, E, int(special_experts), _ptr(x), _code(x.dtype), H,
+        _ptr(counts), _ptr(offsets), _ptr(row_of), _ptr(src_of), _ptr(x_disp), _ptr(ws),
+        _nbytes(ws), _stream(stream))
+    _check(rc, "moe_dispatch_special")
+    return {"counts": counts, "offsets": offsets, "row_of": row_of,
+            "src_of": src_of, "x_disp": x_disp}
+
+
 def moe_dispatch_noalloc(expert_indices: torch.Tensor, x: torch.Tensor, E: int,
                          counts=None, offsets=None, row_of=None, src_of=None,
                          x_disp=None, stream=None) -> dict:
@@ -330,6 +369,48 @@ def moe_combine_add_rmsnorm(out_disp: torch.Tensor, weights: torch.Tensor,
         _ptr(rstd), _stream(stream))
     _check(rc, "moe_combine_add_rmsnorm")
     return y, x_out, rstd
+
+
+def moe_combine_v2(out_disp: torch.Tensor, weights: torch.Tensor, row_of: torch.Tensor,
+                   dtype: torch.dtype, expert_indices=None, num_experts: int = 1,
+                   zero_experts: int = 0, copy_experts: int = 0, const_experts: int = 0,
+                   ori_x=None, const_alpha1=None, const_alpha2=None, const_v=None,
+                   shared_expert_x=None, active_mask=None, residual=None, gamma=None,
+                   eps: float = 1e-6, y=None, x_out=None, rstd=None, stream=None):
+    """Combine with special experts, a shared expert and an active mask
+    (bool [T] or [T, k]); with ``residual`` also Add + RMSNorm. Returns ``y``,
+    or ``(y, x_out, rstd)`` with a residual."""
+    T, k = weights.shape
+    H = out_disp.shape[1]
+    dev = out_disp.device
+    y = y if y is not None else torch.empty((T, H), dtype=dtype, device=dev)
+    mask = None if active_mask is None else active_mask.to(torch.uint8).contiguous()
+    ex = CombineExtras(_ptr(expert_indices), int(num_experts), int(zero_experts),
+                       int(copy_experts), int(const_experts), _ptr(ori_x), _ptr(const_alpha1),
+                       _ptr(const_alpha2), _ptr(const_v), _ptr(shared_expert_x), _ptr(mask),
+                       0 if mask is None else mask.dim())
+    if residual is not None:
+        x_out = x_out if x_out is not None else torch.empty((T, H), dtype=dtype, device=dev)
+        rstd = rstd if rstd is not None else torch.empty(T, dtype=torch.float32, device=dev)
+    rc = load_library().moe_combine_v2(
+        _ptr(out_disp), _code(out_disp.dtype), _ptr(weights), _code(weights.dtype),
+        _ptr(row_of), ctypes.byref(ex), _ptr(residual), _ptr(gamma),
+        _code(gamma.dtype) if gamma is not None else 0, float(eps), T, k, H, _ptr(y),
+        _code(dtype), _ptr(x_out), _ptr(rstd), _stream(stream))
+    _check(rc, "moe_combine_v2")
+    return y if residual is None else (y, x_out, rstd)
+
+
+def moe_rmsnorm(x: torch.Tensor, gamma: torch.Tensor, eps: float, y=None, rstd=None,
+                stream=None):
+    """RMSNorm over the last axis of ``x [rows, H]``; returns ``(y, rstd)``."""
+    rows, H = x.shape
+    y = y if y is not None else torch.empty_like(x)
+    rstd = rstd if rstd is not None else torch.empty(rows, dtype=torch.float32, device=x.device)
+    rc = load_library().moe_rmsnorm(_ptr(x), _code(x.dtype), _ptr(gamma), _code(gamma.dtype),
+                                    float(eps), rows, H, _ptr(y), _ptr(rstd), _stream(stream))
+    _check(rc, "moe_rmsnorm")
+    return y, rstd
 
 
 def moe_forward_workspace_size(T: int, H: int, I: int, E: int, top_k: int,

@@ -17,6 +17,17 @@
 // activation dtype first and the statistics are taken on the rounded x (so
 // y == RMSNorm(x_out)); x stays in registers between the two passes.
 // HBM-bound.
+//
+// With extras (aclnnMoeDistributeCombineAddRmsNormV2, formula and parameter
+// list): a slot the active mask drops contributes nothing; an expert id
+// past the E routed experts names a special expert -- zero (contributes 0),
+// copy (the token's original row oriX) or const (alpha1[c] * oriX + alpha2[c]
+// * V[c]); and a shared-expert row is added once per kept slot, scaled like
+// it, i.e. (sum of the kept weights) * sharedX.
+//
+// rmsnorm_kernel is the standalone RMSNorm of ruDNN user guide section 7:
+// y = x / sqrt(mean(x^2) + eps) * gamma per row, FP32 statistics, output in
+// the input dtype.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -80,13 +91,16 @@ __device__ __forceinline__ void load8_rt(const void *base, int dt, int64_t g, fl
     else load8<DT_F16>(base, g, f);
 }
 
-template <int ODT, int YDT, int V, bool NORM>
+// Sources of a slot other than a dispatched expert row (see the header).
+enum SlotKind : int { kRouted = 0, kZero = 1, kCopy = 2, kConst = 3, kBad = 4 };
+
+template <int ODT, int YDT, int V, bool NORM, bool EXTRAS>
 __global__ void __launch_bounds__(kMaxThreads)
 combine_kernel(const void *__restrict__ out_disp, const void *__restrict__ w, int wdt,
                const int32_t *__restrict__ row_of, const void *__restrict__ residual,
                const void *__restrict__ gamma, int gdt, float eps, int64_t T, int top_k,
                int64_t H, void *__restrict__ y, void *__restrict__ x_out,
-               float *__restrict__ rstd)
+               float *__restrict__ rstd, CombineExtras ex)
 {
     const int64_t ng = H / 8;
     __shared__ float red[kMaxThreads / 32];
@@ -104,20 +118,75 @@ combine_kernel(const void *__restrict__ out_disp, const void *__restrict__ w, in
 #pragma unroll
                 for (int i = 0; i < 8; ++i) acc[v][i] = 0.0f;
             bool nan_row = false;
+            float wkept = 0.0f;                 // sum of the kept slots' weights (shared term)
 #pragma unroll 2
             for (int j = 0; j < top_k; ++j) {
-                const int32_t r = row_of[t * top_k + j];
-                const float wj = load_as_float(w, wdt, t * top_k + j);
-                if (r < 0) { nan_row = true; continue; }
-                const void *src = static_cast<const uint8_t *>(out_disp) + (int64_t)r * H * elem_o;
+                const int64_t a = t * top_k + j;
+                int kind = kRouted;
+                int64_t cidx = 0;
+                if constexpr (EXTRAS) {
+                    if (ex.mask_dims == 1 && !ex.mask[t]) continue;
+                    if (ex.mask_dims == 2 && !ex.mask[a]) continue;
+                    if (ex.ids != nullptr) {
+                        const int64_t id = ex.ids[a];
+                        if (id >= ex.E) {
+                            const int64_t sp = id - ex.E;
+                            kind = sp < ex.zero_n ? kZero
+                                 : sp < ex.zero_n + ex.copy_n ? kCopy
+                                 : sp < ex.zero_n + ex.copy_n + ex.const_n ? kConst : kBad;
+                            cidx = sp - ex.zero_n - ex.copy_n;
+                        }
+                    }
+                }
+                const float wj = load_as_float(w, wdt, a);
+                if (kind == kBad) { nan_row = true; continue; }
+                const void *src = nullptr;
+                if (kind == kRouted) {
+                    const int32_t r = row_of[a];
+                    if (r < 0) { nan_row = true; continue; }
+                    src = static_cast<const uint8_t *>(out_disp) + (int64_t)r * H * elem_o;
+                }
+                if constexpr (EXTRAS) wkept += wj;
+                if (kind == kZero) continue;
+                float a1 = 0.0f, a2 = 0.0f;
+                if constexpr (EXTRAS) {
+                    if (kind == kConst) {
+                        a1 = load_as_float(ex.alpha1, YDT, cidx);
+                        a2 = load_as_float(ex.alpha2, YDT, cidx);
+                    }
+                }
 #pragma unroll
                 for (int v = 0; v < V; ++v) {
                     const int64_t c = base + threadIdx.x + (int64_t)v * blockDim.x;
                     if (c < ng) {
                         float f[8];
-                        load8<ODT>(src, c, f);
+                        if (!EXTRAS || kind == kRouted) {
+                            load8<ODT>(src, c, f);
+                        } else {
+                            load8<YDT>(ex.ori_x, t * ng + c, f);
+                            if (kind == kConst) {
+                                float cv[8];
+                                load8<YDT>(ex.const_v, cidx * ng + c, cv);
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) f[i] = a1 * f[i] + a2 * cv[i];
+                            }
+                        }
 #pragma unroll
                         for (int i = 0; i < 8; ++i) acc[v][i] = fmaf(wj, f[i], acc[v][i]);
+                    }
+                }
+            }
+            if constexpr (EXTRAS) {
+                if (ex.shared_x != nullptr && !nan_row) {
+#pragma unroll
+                    for (int v = 0; v < V; ++v) {
+                        const int64_t c = base + threadIdx.x + (int64_t)v * blockDim.x;
+                        if (c < ng) {
+                            float f[8];
+                            load8<YDT>(ex.shared_x, t * ng + c, f);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) acc[v][i] = fmaf(wkept, f[i], acc[v][i]);
+                        }
                     }
                 }
             }
@@ -179,11 +248,11 @@ combine_kernel(const void *__restrict__ out_disp, const void *__restrict__ w, in
     }
 }
 
-template <int ODT, int YDT, bool NORM>
+template <int ODT, int YDT, bool NORM, bool EXTRAS>
 cudaError_t launch_typed(const void *out_disp, const void *w, int wdt, const int32_t *row_of,
                          const void *residual, const void *gamma, int gdt, float eps,
                          int64_t T, int top_k, int64_t H, void *y, void *x_out, float *rstd,
-                         cudaStream_t s)
+                         const CombineExtras &ex, cudaStream_t s)
 {
     const int64_t ng = H / 8;
     int V = 1;
@@ -196,9 +265,9 @@ cudaError_t launch_typed(const void *out_disp, const void *w, int wdt, const int
     const int64_t cap = (int64_t)device_sm_count() * 32;
     if (blocks > cap) blocks = cap;
 #define MOE_COMBINE_LAUNCH(VV)                                                             \
-    return launch_pdl(combine_kernel<ODT, YDT, VV, NORM>, dim3((unsigned)blocks),           \
+    return launch_pdl(combine_kernel<ODT, YDT, VV, NORM, EXTRAS>, dim3((unsigned)blocks),   \
                       dim3((unsigned)threads), 0, s, out_disp, w, wdt, row_of, residual,    \
-                      gamma, gdt, eps, T, top_k, H, y, x_out, rstd)
+                      gamma, gdt, eps, T, top_k, H, y, x_out, rstd, ex)
     switch (V) {
     case 1: MOE_COMBINE_LAUNCH(1);
     case 2: MOE_COMBINE_LAUNCH(2);
@@ -208,15 +277,15 @@ cudaError_t launch_typed(const void *out_disp, const void *w, int wdt, const int
 #undef MOE_COMBINE_LAUNCH
 }
 
-template <bool NORM>
+template <bool NORM, bool EXTRAS>
 cudaError_t launch_norm(const void *out_disp, int odt, const void *w, int wdt,
                         const int32_t *row_of, const void *residual, const void *gamma,
                         int gdt, float eps, int64_t T, int top_k, int64_t H, void *y, int ydt,
-                        void *x_out, float *rstd, cudaStream_t s)
+                        void *x_out, float *rstd, const CombineExtras &ex, cudaStream_t s)
 {
-#define MOE_TYPED(O, Y)                                                                   \
-    return launch_typed<O, Y, NORM>(out_disp, w, wdt, row_of, residual, gamma, gdt, eps, T, \
-                                    top_k, H, y, x_out, rstd, s)
+#define MOE_TYPED(O, Y)                                                                     \
+    return launch_typed<O, Y, NORM, EXTRAS>(out_disp, w, wdt, row_of, residual, gamma, gdt, \
+                                            eps, T, top_k, H, y, x_out, rstd, ex, s)
     if (ydt == DT_F32) MOE_TYPED(DT_F32, DT_F32);
     if (ydt == DT_BF16) {
         if (odt == DT_F32) MOE_TYPED(DT_F32, DT_BF16);
@@ -225,6 +294,83 @@ cudaError_t launch_norm(const void *out_disp, int odt, const void *w, int wdt,
     if (odt == DT_F32) MOE_TYPED(DT_F32, DT_F16);
     MOE_TYPED(DT_F16, DT_F16);
 #undef MOE_TYPED
+}
+
+// Standalone RMSNorm: one CTA per row (grid-stride), the row in registers.
+template <int XDT, int V>
+__global__ void __launch_bounds__(kMaxThreads)
+rmsnorm_kernel(const void *__restrict__ x, const void *__restrict__ gamma, int gdt, float eps,
+               int64_t rows, int64_t H, void *__restrict__ y, float *__restrict__ rstd)
+{
+    const int64_t ng = H / 8;
+    __shared__ float red[kMaxThreads / 32];
+    __shared__ float s_rstd;
+    pdl_wait();
+    pdl_launch_dependents();
+    for (int64_t t = blockIdx.x; t < rows; t += gridDim.x) {
+        float f[V][8];
+        float ss = 0.0f;
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const int64_t c = threadIdx.x + (int64_t)v * blockDim.x;
+            if (c < ng) {
+                load8<XDT>(x, t * ng + c, f[v]);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) ss = fmaf(f[v][i], f[v][i], ss);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if (lane_id() == 0) red[threadIdx.x / 32] = ss;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float tot = 0.0f;
+            for (int i = 0; i < (int)(blockDim.x / 32); ++i) tot += red[i];
+            const float r = 1.0f / sqrtf(tot / (float)H + eps);
+            s_rstd = r;
+            if (rstd != nullptr) rstd[t] = r;
+        }
+        __syncthreads();
+        const float r = s_rstd;
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const int64_t c = threadIdx.x + (int64_t)v * blockDim.x;
+            if (c < ng) {
+                float gm[8];
+                load8_rt(gamma, gdt, c, gm);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) f[v][i] = f[v][i] * r * gm[i];
+                store8<XDT>(y, t * ng + c, f[v]);
+            }
+        }
+        __syncthreads();     // red / s_rstd are reused by the next row
+    }
+}
+
+template <int XDT>
+cudaError_t launch_rmsnorm_dt(const void *x, const void *gamma, int gdt, float eps, int64_t rows,
+                              int64_t H, void *y, float *rstd, cudaStream_t s)
+{
+    const int64_t ng = H / 8;
+    int V = 1;
+    while (V < kMaxV && ng > (int64_t)V * kMaxThreads) V *= 2;
+    int64_t threads = (ng + V - 1) / V;
+    threads = (threads + 31) / 32 * 32;
+    if (threads > kMaxThreads) threads = kMaxThreads;
+    if (threads < 32) threads = 32;
+    int64_t blocks = rows;
+    const int64_t cap = (int64_t)device_sm_count() * 32;
+    if (blocks > cap) blocks = cap;
+#define MOE_RMS(VV)                                                                        \
+    return launch_pdl(rmsnorm_kernel<XDT, VV>, dim3((unsigned)blocks), dim3((unsigned)threads), \
+                      0, s, x, gamma, gdt, eps, rows, H, y, rstd)
+    switch (V) {
+    case 1: MOE_RMS(1);
+    case 2: MOE_RMS(2);
+    case 4: MOE_RMS(4);
+    default: MOE_RMS(8);
+    }
+#undef MOE_RMS
 }
 
 // y = y_acc (FP32) rounded to YDT, 8 elements per thread and step.
@@ -273,14 +419,31 @@ cudaError_t launch_combine(const void *out_disp, int odt, const void *w, int wdt
                            const int32_t *row_of, const void *residual,
                            const void *gamma, int gdt, float eps, int64_t T,
                            int top_k, int64_t H, void *y, int ydt, void *x_out,
-                           float *rstd, cudaStream_t s)
+                           float *rstd, cudaStream_t s, const CombineExtras *ex)
 {
     if (T == 0) return cudaSuccess;
+    const CombineExtras none{};
+    if (ex != nullptr) {
+        if (residual != nullptr)
+            return launch_norm<true, true>(out_disp, odt, w, wdt, row_of, residual, gamma, gdt,
+                                           eps, T, top_k, H, y, ydt, x_out, rstd, *ex, s);
+        return launch_norm<false, true>(out_disp, odt, w, wdt, row_of, residual, gamma, gdt, eps,
+                                        T, top_k, H, y, ydt, x_out, rstd, *ex, s);
+    }
     if (residual != nullptr)
-        return launch_norm<true>(out_disp, odt, w, wdt, row_of, residual, gamma, gdt, eps, T,
-                                 top_k, H, y, ydt, x_out, rstd, s);
-    return launch_norm<false>(out_disp, odt, w, wdt, row_of, residual, gamma, gdt, eps, T,
-                              top_k, H, y, ydt, x_out, rstd, s);
+        return launch_norm<true, false>(out_disp, odt, w, wdt, row_of, residual, gamma, gdt, eps,
+                                        T, top_k, H, y, ydt, x_out, rstd, none, s);
+    return launch_norm<false, false>(out_disp, odt, w, wdt, row_of, residual, gamma, gdt, eps, T,
+                                     top_k, H, y, ydt, x_out, rstd, none, s);
+}
+
+cudaError_t launch_rmsnorm(const void *x, int xdt, const void *gamma, int gdt, float eps,
+                           int64_t rows, int64_t H, void *y, float *rstd, cudaStream_t s)
+{
+    if (rows == 0) return cudaSuccess;
+    if (xdt == DT_BF16) return launch_rmsnorm_dt<DT_BF16>(x, gamma, gdt, eps, rows, H, y, rstd, s);
+    if (xdt == DT_F16) return launch_rmsnorm_dt<DT_F16>(x, gamma, gdt, eps, rows, H, y, rstd, s);
+    return launch_rmsnorm_dt<DT_F32>(x, gamma, gdt, eps, rows, H, y, rstd, s);
 }
 
 }  // namespace moe

@@ -46,8 +46,9 @@ int64_t chunk_size(int64_t A)
 int64_t num_chunks(int64_t A) { return (A + chunk_size(A) - 1) / chunk_size(A); }
 
 __global__ void __launch_bounds__(kChunkWarps * 32)
-dispatch_count_kernel(const uint32_t *__restrict__ idx, int64_t A, int E, int64_t chunk,
-                      int64_t nchunks, int *__restrict__ chunk_counts, unsigned *status)
+dispatch_count_kernel(const uint32_t *__restrict__ idx, int64_t A, int E, int64_t special,
+                      int64_t chunk, int64_t nchunks, int *__restrict__ chunk_counts,
+                      unsigned *status)
 {
     extern __shared__ int hist[];
     pdl_wait();
@@ -72,7 +73,8 @@ dispatch_count_kernel(const uint32_t *__restrict__ idx, int64_t A, int E, int64_
         for (int b = 0; b < kBatch; ++b) {
             const bool act = s0 + 32 * b + lane < a1;
             const bool ok = act && ev[b] < (uint32_t)E;
-            saw_bad |= act && !ok;
+            // ids in [E, E + special) name special experts: no row, not bad
+            saw_bad |= act && !ok && (uint64_t)ev[b] >= (uint64_t)E + (uint64_t)special;
             const unsigned peers = __match_any_sync(kFull, ok ? ev[b] : 0xffffffffu);
             if (ok && lane == __ffs(peers) - 1) atomicAdd(&h[ev[b]], __popc(peers));
         }
@@ -264,7 +266,7 @@ size_t dispatch_workspace_bytes(int64_t A, int E)
     return (size_t)num_chunks(A) * (size_t)E * sizeof(int);
 }
 
-cudaError_t launch_dispatch(const uint32_t *idx, int64_t T, int top_k, int E,
+cudaError_t launch_dispatch(const uint32_t *idx, int64_t T, int top_k, int E, int64_t special,
                             const void *x, int xdt, int64_t H, int32_t *counts,
                             int32_t *offsets, int32_t *row_of, int32_t *src_of,
                             void *x_disp, void *ws, unsigned *status,
@@ -278,7 +280,8 @@ cudaError_t launch_dispatch(const uint32_t *idx, int64_t T, int top_k, int E,
     const unsigned blocks = (unsigned)((nchunks + kChunkWarps - 1) / kChunkWarps);
     const size_t hist_bytes = (size_t)kChunkWarps * E * sizeof(int);
     cudaError_t err = launch_pdl(dispatch_count_kernel, dim3(blocks), dim3(kChunkWarps * 32),
-                                 hist_bytes, s, idx, A, E, chunk_len, nchunks, chunk, status);
+                                 hist_bytes, s, idx, A, E, special, chunk_len, nchunks, chunk,
+                                 status);
     if (err != cudaSuccess) return err;
     err = launch_pdl(dispatch_scan_kernel, dim3((unsigned)((E + 31) / 32)), dim3(kScanThreads),
                      0, s, chunk, nchunks, E, counts);

@@ -31,7 +31,9 @@ int sigmoid_route_max_groups();
 
 // Dispatch: per-chunk histograms, a scan, a stable rank/scatter, a row gather.
 size_t dispatch_workspace_bytes(int64_t A, int E);
-cudaError_t launch_dispatch(const uint32_t *idx, int64_t T, int top_k, int E,
+// Expert ids in [E, E + special) are special experts (see CombineExtras):
+// they get no row and are not reported as bad indices.
+cudaError_t launch_dispatch(const uint32_t *idx, int64_t T, int top_k, int E, int64_t special,
                             const void *x, int xdt, int64_t H, int32_t *counts,
                             int32_t *offsets, int32_t *row_of, int32_t *src_of,
                             void *x_disp, void *ws, unsigned *status,
@@ -40,11 +42,27 @@ cudaError_t launch_dispatch(const uint32_t *idx, int64_t T, int top_k, int E,
 // Weighted combine, optionally followed by residual Add + RMSNorm.
 // out_disp in odt; y, residual and x_out in ydt; H % 8 == 0.
 int combine_max_h(bool norm);
+// Special experts, shared expert and active mask of the combine (all zero /
+// NULL: none). ori_x, alpha1/2, const_v and shared_x are in the activation
+// dtype; ids may be NULL when no special experts are configured.
+struct CombineExtras {
+    const uint32_t *ids;
+    int64_t E, zero_n, copy_n, const_n;
+    const void *ori_x, *alpha1, *alpha2, *const_v, *shared_x;
+    const uint8_t *mask;
+    int mask_dims;                // 0, 1 ([T]) or 2 ([T, top_k])
+};
+
 cudaError_t launch_combine(const void *out_disp, int odt, const void *w, int wdt,
                            const int32_t *row_of, const void *residual,
                            const void *gamma, int gdt, float eps, int64_t T,
                            int top_k, int64_t H, void *y, int ydt, void *x_out,
-                           float *rstd, cudaStream_t s);
+                           float *rstd, cudaStream_t s,
+                           const CombineExtras *extras = nullptr);
+
+// Standalone RMSNorm of rows x [rows, H] (H % 8 == 0, H <= combine_max_h(true)).
+cudaError_t launch_rmsnorm(const void *x, int xdt, const void *gamma, int gdt, float eps,
+                           int64_t rows, int64_t H, void *y, float *rstd, cudaStream_t s);
 
 // FP32 SwiGLU experts on CUDA cores. h_ws holds [rows, I] floats.
 cudaError_t launch_experts_simt(const float *x_disp, const int32_t *offsets,

@@ -231,7 +231,7 @@ int forward_impl(const char *name, const void *x, int dtype, const void *logits,
     }
     err = route(idx, w, s);
     if (err != cudaSuccess) return cuda_fail(err, "forward/route");
-    err = launch_dispatch(idx, T, top_k, (int)E, x, dtype, H, counts, offsets, row_of, src_of,
+    err = launch_dispatch(idx, T, top_k, (int)E, 0, x, dtype, H, counts, offsets, row_of, src_of,
                           x_disp, ws + L.disp_ws, st, s);
     if (err != cudaSuccess) return cuda_fail(err, "forward/dispatch");
     if (fused_combine) {
@@ -314,7 +314,8 @@ size_t moe_dispatch_workspace_size(int64_t T, int top_k, int64_t E)
     return round_up(dispatch_workspace_bytes(T * top_k, (int)E), 256);
 }
 
-int moe_dispatch(const uint32_t *expert_indices, int64_t T, int top_k, int64_t E,
+int moe_dispatch_special(const uint32_t *expert_indices, int64_t T, int top_k, int64_t E,
+                         int64_t special_experts,
                  const void *x, int x_dtype, int64_t H, int32_t *counts, int32_t *offsets,
                  int32_t *row_of, int32_t *src_of, void *x_disp, void *workspace,
                  size_t workspace_bytes, void *stream)
@@ -322,6 +323,8 @@ int moe_dispatch(const uint32_t *expert_indices, int64_t T, int top_k, int64_t E
     if (!valid_dtype(x_dtype)) return fail(MOE_ERR_DTYPE, "x dtype must be F32, BF16 or F16");
     if (T < 0 || E < 1 || E > kMaxE || top_k < 1 || H < 1 || T * top_k > kMaxRows)
         return fail(MOE_ERR_SHAPE, "need T >= 0, 1 <= E <= 1024, top_k >= 1, H >= 1");
+    if (special_experts < 0 || special_experts > 0x7fffffff - E)
+        return fail(MOE_ERR_SHAPE, "need 0 <= special_experts and E + special_experts < 2^31");
     if (T == 0) return MOE_OK;
     if (!expert_indices || !x || !counts || !offsets || !row_of || !src_of || !x_disp)
         return fail(MOE_ERR_NULL, "moe_dispatch: NULL tensor");
@@ -334,10 +337,19 @@ int moe_dispatch(const uint32_t *expert_indices, int64_t T, int top_k, int64_t E
         return fail(MOE_ERR_WORKSPACE, "moe_dispatch: workspace too small or not 256-byte aligned");
     unsigned *st = status_ptr();
     if (!st) return fail(MOE_ERR_CUDA, "cannot resolve the device status word");
-    cudaError_t err = launch_dispatch(expert_indices, T, top_k, (int)E, x, x_dtype, H, counts,
+    cudaError_t err = launch_dispatch(expert_indices, T, top_k, (int)E, special_experts, x, x_dtype, H, counts,
                                       offsets, row_of, src_of, x_disp, workspace, st,
                                       static_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_dispatch");
+}
+
+int moe_dispatch(const uint32_t *expert_indices, int64_t T, int top_k, int64_t E,
+                 const void *x, int x_dtype, int64_t H, int32_t *counts, int32_t *offsets,
+                 int32_t *row_of, int32_t *src_of, void *x_disp, void *workspace,
+                 size_t workspace_bytes, void *stream)
+{
+    return moe_dispatch_special(expert_indices, T, top_k, E, 0, x, x_dtype, H, counts, offsets,
+                                row_of, src_of, x_disp, workspace, workspace_bytes, stream);
 }
 
 size_t moe_experts_workspace_size(int64_t rows, int64_t E, int64_t H, int64_t I, int dtype)
@@ -405,6 +417,82 @@ int moe_combine_add_rmsnorm(const void *out_disp, int out_dtype, const void *wei
                                      gamma, gamma_dtype, eps, T, top_k, H, y, dtype, x_out, rstd,
                                      static_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_combine_add_rmsnorm");
+}
+
+int moe_combine_v2(const void *out_disp, int out_dtype, const void *weights, int weights_dtype,
+                   const int32_t *row_of, const moe_combine_extras *extras,
+                   const void *residual, const void *gamma, int gamma_dtype, float eps,
+                   int64_t T, int top_k, int64_t H, void *y, int dtype, void *x_out,
+                   float *rstd, void *stream)
+{
+    const bool norm = residual != nullptr;
+    int rc = check_combine_args(out_dtype, weights_dtype, dtype, T, top_k, H, norm);
+    if (rc != MOE_OK) return rc;
+    if (norm) {
+        if (!valid_dtype(gamma_dtype)) return fail(MOE_ERR_DTYPE, "gamma dtype must be F32, BF16 or F16");
+        if (!(isfinite(eps) && eps > 0.0f)) return fail(MOE_ERR_VALUE, "eps must be finite and > 0");
+    }
+    CombineExtras ex{};
+    if (extras != nullptr) {
+        const moe_combine_extras &e = *extras;
+        const int64_t special = e.zero_experts + e.copy_experts + e.const_experts;
+        if (e.num_experts < 1 || e.zero_experts < 0 || e.copy_experts < 0 || e.const_experts < 0 ||
+            special > 0x7fffffff - e.num_experts)
+            return fail(MOE_ERR_SHAPE, "moe_combine_v2: need num_experts >= 1 and special expert counts >= 0");
+        if (e.active_mask_dims < 0 || e.active_mask_dims > 2)
+            return fail(MOE_ERR_SHAPE, "moe_combine_v2: active_mask_dims must be 0, 1 or 2");
+        if (T > 0) {
+            if ((special > 0 && !e.expert_indices) ||
+                ((e.copy_experts > 0 || e.const_experts > 0) && !e.ori_x) ||
+                (e.const_experts > 0 && (!e.const_alpha1 || !e.const_alpha2 || !e.const_v)) ||
+                (e.active_mask_dims > 0 && !e.active_mask))
+                return fail(MOE_ERR_NULL, "moe_combine_v2: an input its configured experts or mask need is NULL");
+            if ((e.ori_x && !aligned16(e.ori_x)) || (e.const_v && !aligned16(e.const_v)) ||
+                (e.shared_expert_x && !aligned16(e.shared_expert_x)))
+                return fail(MOE_ERR_ALIGN, "moe_combine_v2: ori_x, const_v and shared_expert_x must be 16-byte aligned");
+        }
+        ex.ids = e.expert_indices;
+        ex.E = e.num_experts;
+        ex.zero_n = e.zero_experts;
+        ex.copy_n = e.copy_experts;
+        ex.const_n = e.const_experts;
+        ex.ori_x = e.ori_x;
+        ex.alpha1 = e.const_alpha1;
+        ex.alpha2 = e.const_alpha2;
+        ex.const_v = e.const_v;
+        ex.shared_x = e.shared_expert_x;
+        ex.mask = e.active_mask;
+        ex.mask_dims = e.active_mask_dims;
+    }
+    if (T == 0) return MOE_OK;
+    if (!out_disp || !weights || !row_of || !y || (norm && (!gamma || !x_out || !rstd)))
+        return fail(MOE_ERR_NULL, "moe_combine_v2: NULL tensor");
+    if (!aligned16(out_disp) || !aligned16(weights) || !aligned16(row_of) || !aligned16(y) ||
+        (norm && (!aligned16(residual) || !aligned16(gamma) || !aligned16(x_out) || !aligned16(rstd))))
+        return fail(MOE_ERR_ALIGN, "moe_combine_v2: tensors must be 16-byte aligned");
+    cudaError_t err = launch_combine(out_disp, out_dtype, weights, weights_dtype, row_of, residual,
+                                     gamma, gamma_dtype, eps, T, top_k, H, y, dtype, x_out, rstd,
+                                     static_cast<cudaStream_t>(stream),
+                                     extras != nullptr ? &ex : nullptr);
+    return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_combine_v2");
+}
+
+int moe_rmsnorm(const void *x, int dtype, const void *gamma, int gamma_dtype, float eps,
+                int64_t rows, int64_t H, void *y, float *rstd, void *stream)
+{
+    if (!valid_dtype(dtype)) return fail(MOE_ERR_DTYPE, "x dtype must be F32, BF16 or F16");
+    if (gamma_dtype != MOE_F32 && gamma_dtype != dtype)
+        return fail(MOE_ERR_DTYPE, "gamma dtype must be F32 or the input dtype");
+    if (rows < 0 || H < 1 || H % 8 != 0 || H > combine_max_h(true))
+        return fail(MOE_ERR_SHAPE, "need rows >= 0 and H a multiple of 8 in [8, 16384]");
+    if (!(isfinite(eps) && eps > 0.0f)) return fail(MOE_ERR_VALUE, "eps must be finite and > 0");
+    if (rows == 0) return MOE_OK;
+    if (!x || !gamma || !y) return fail(MOE_ERR_NULL, "moe_rmsnorm: NULL tensor");
+    if (!aligned16(x) || !aligned16(gamma) || !aligned16(y) || (rstd && !aligned16(rstd)))
+        return fail(MOE_ERR_ALIGN, "moe_rmsnorm: tensors must be 16-byte aligned");
+    cudaError_t err = launch_rmsnorm(x, dtype, gamma, gamma_dtype, eps, rows, H, y, rstd,
+                                     static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_rmsnorm");
 }
 
 size_t moe_forward_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E, int top_k,

@@ -30,7 +30,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_abi():
@@ -124,6 +124,92 @@ def test_forward_sigmoid_grouped_validation(lib):
     assert call(y=P(FAKE_ODD)) == ALIGN
     assert call(wsb=100) == WORKSPACE
     assert call(T=0, x=P(None), lg=P(None), y=P(None)) == OK
+
+
+def test_combine_extras_layout_matches_header(tmp_path):
+    """The binding's moe_combine_extras mirror has the C header's layout
+    (field offsets and size as the C compiler lays them out)."""
+    import subprocess
+    fields = [f[0] for f in moe.CombineExtras._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "moe.h"\n'
+                   "int main(void) {\n"
+                   '    printf("%zu\\n", sizeof(moe_combine_extras));\n'
+                   + "".join(f'    printf("%zu\\n", offsetof(moe_combine_extras, {n}));\n'
+                             for n in fields) + "    return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o",
+                    str(exe)], check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], check=True, capture_output=True,
+                                          text=True).stdout.split()]
+    assert got[0] == ctypes.sizeof(moe.CombineExtras)
+    assert got[1:] == [getattr(moe.CombineExtras, n).offset for n in fields]
+
+
+def test_combine_v2_validation(lib):
+    s = P(None)
+
+    def call(ex=None, **kw):
+        a = dict(out=P(FAKE), odt=F32, w=P(FAKE), wdt=F32, rows=P(FAKE), res=P(None),
+                 gamma=P(None), gdt=F32, eps=1e-6, T=8, k=2, H=64, y=P(FAKE), dt=BF16,
+                 xo=P(None), rstd=P(None))
+        a.update(kw)
+        return lib.moe_combine_v2(a["out"], a["odt"], a["w"], a["wdt"], a["rows"],
+                                  None if ex is None else ctypes.byref(ex), a["res"], a["gamma"],
+                                  a["gdt"], a["eps"], a["T"], a["k"], a["H"], a["y"], a["dt"],
+                                  a["xo"], a["rstd"], s)
+
+    def extras(**kw):
+        a = dict(ids=None, E=4, zero=0, copy=0, const=0, ori=None, a1=None, a2=None, v=None,
+                 shared=None, mask=None, mdims=0)
+        a.update(kw)
+        return moe.CombineExtras(a["ids"], a["E"], a["zero"], a["copy"], a["const"], a["ori"],
+                                 a["a1"], a["a2"], a["v"], a["shared"], a["mask"], a["mdims"])
+    assert call(H=60) == SHAPE
+    assert call(extras(E=0)) == SHAPE
+    assert call(extras(zero=-1)) == SHAPE
+    assert call(extras(mdims=3)) == SHAPE
+    assert call(extras(zero=1)) == NULL                     # special experts need ids
+    assert call(extras(ids=FAKE, copy=1)) == NULL           # copy needs ori_x
+    assert call(extras(ids=FAKE, const=1, ori=FAKE)) == NULL  # const needs alpha1/2 and V
+    assert call(extras(mdims=2)) == NULL                    # mask dims without a mask
+    assert call(extras(shared=FAKE_ODD)) == ALIGN
+    assert call(extras(ids=FAKE, copy=1, ori=FAKE_ODD)) == ALIGN
+    assert call(extras(), res=P(FAKE), gamma=P(FAKE), eps=0.0) == VALUE
+    assert call(extras(), res=P(FAKE), gamma=P(FAKE)) == NULL    # norm needs x_out, rstd
+    assert call(extras(), T=0, out=P(None), w=P(None), rows=P(None), y=P(None)) == OK
+    assert call(None, T=0, out=P(None), w=P(None), rows=P(None), y=P(None)) == OK
+
+
+def test_dispatch_special_validation(lib):
+    s = P(None)
+    assert lib.moe_dispatch_special(P(FAKE), 4, 2, 8, -1, P(FAKE), BF16, 64, P(FAKE), P(FAKE),
+                                    P(FAKE), P(FAKE), P(FAKE), P(FAKE), 1 << 20, s) == SHAPE
+    assert lib.moe_dispatch_special(P(FAKE), 4, 2, 8, 1 << 31, P(FAKE), BF16, 64, P(FAKE),
+                                    P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), 1 << 20,
+                                    s) == SHAPE
+    assert lib.moe_dispatch_special(P(None), 0, 2, 8, 3, P(None), BF16, 64, P(None), P(None),
+                                    P(None), P(None), P(None), P(None), 0, s) == OK
+
+
+def test_rmsnorm_validation(lib):
+    s = P(None)
+
+    def call(**kw):
+        a = dict(x=P(FAKE), dt=BF16, g=P(FAKE), gdt=F32, eps=1e-6, rows=4, H=64, y=P(FAKE),
+                 r=P(None))
+        a.update(kw)
+        return lib.moe_rmsnorm(a["x"], a["dt"], a["g"], a["gdt"], a["eps"], a["rows"], a["H"],
+                               a["y"], a["r"], s)
+    assert call(dt=9) == DTYPE
+    assert call(gdt=F16) == DTYPE                 # gamma F32 or the input dtype
+    assert call(H=60) == SHAPE
+    assert call(H=16392) == SHAPE
+    assert call(eps=0.0) == VALUE
+    assert call(eps=math.nan) == VALUE
+    assert call(x=P(None)) == NULL
+    assert call(y=P(FAKE_ODD)) == ALIGN
+    assert call(rows=0, x=P(None), y=P(None)) == OK
 
 
 def test_dispatch_validation(lib):
