@@ -15,7 +15,8 @@ Arrays: f32 data is ``np.float32``; bf16 and f16 data are raw 16-bit words in
 
 Sources, by page title and section:
   ruDNN user guide, sections 3-7 (MoE workflow, routing contract, expert
-  weights and dispatch, calling MoE, RMSNorm); aclnnMoeDistributeCombine-
+  weights and dispatch, calling MoE, RMSNorm), section 10 (grouped sigmoid
+  routing) and section 12 (MoE first-order training); aclnnMoeDistributeCombine-
   AddRmsNormV2, "Function" formula (combine, Add, RMSNorm, rstdOut);
   aclnnFFN, "Formula" (the FFN the experts instantiate).
 """
@@ -101,6 +102,21 @@ def _bind(lib):
     lib.oracle_add_rmsnorm.argtypes = [_P, _P, _INT, _P, _INT, _F, _I64, _I64,
                                        _P, _P, _P]
     lib.oracle_add_rmsnorm.restype = _INT
+    _D = ctypes.c_double
+    lib.oracle_router_weights.argtypes = [_P, _INT, _I64, _I64, _P, _I64, _INT, _INT, _D,
+                                          _P, _INT]
+    lib.oracle_router_weights.restype = _I64
+    lib.oracle_router_backward.argtypes = [_P, _INT, _I64, _I64, _P, _I64, _P, _INT, _INT,
+                                           _INT, _D, _P, _INT]
+    lib.oracle_router_backward.restype = _I64
+    lib.oracle_combine_backward.argtypes = [_P, _INT, _P, _INT, _P, _P, _INT, _I64, _I64,
+                                            _I64, _I64, _P, _P]
+    lib.oracle_combine_backward.restype = None
+    lib.oracle_swiglu_backward_rows.argtypes = [_P, _INT, _I64, _P, _P, _P, _P, _I64, _I64,
+                                                _I64, _P, _INT, _P, _P, _P, _P]
+    lib.oracle_swiglu_backward_rows.restype = _INT
+    lib.oracle_dispatch_backward.argtypes = [_P, _INT, _P, _I64, _I64, _I64, _P]
+    lib.oracle_dispatch_backward.restype = None
     return lib
 
 
@@ -396,3 +412,126 @@ def forward_tokens(tokens, x, dt: str, logits, ldt: str, gate, up, down,
     row_of = np.arange(n * top_k, dtype=np.int32)
     y = combine(out, "f64", w, ldt, row_of, top_k, lib)
     return idx, w, y
+
+
+# ---- first-order training (ruDNN user guide, section 12) -----------------
+
+SCORING = {"softmax": 0, "sigmoid": 1}
+
+
+def _idx64(idx):
+    """Selection indices as int64 (U32, I32 and I64 are all accepted)."""
+    a = np.asarray(idx)
+    if a.dtype == np.uint32 or a.dtype == np.uint64:
+        a = a.astype(np.uint64)
+        a = np.where(a > np.uint64(2**62), np.uint64(2**62), a).astype(np.int64)
+    return np.ascontiguousarray(a, dtype=np.int64)
+
+
+def router_weights(logits, ldt: str, idx, scoring: str = "softmax",
+                   renormalize: bool = False, scale: float = 1.0, out_dt: str = "f32",
+                   lib=None):
+    """Weights of a fixed selection (selected_router_weights). Returns
+    ``(w [T,k] in out_dt storage, nan_rows)``."""
+    lib = lib or load_library()
+    logits = _arr(logits, ldt)
+    T, E = logits.shape
+    idx = _idx64(idx)
+    k = idx.shape[1]
+    w = np.empty((T, k), dtype=_storage(out_dt))
+    n = lib.oracle_router_weights(_ptr(logits), DTYPE_CODES[ldt], T, E, _ptr(idx), k,
+                                  SCORING[scoring], int(bool(renormalize)), float(scale),
+                                  _ptr(w), DTYPE_CODES[out_dt])
+    if n < 0:
+        raise ValueError("oracle_router_weights: bad arguments")
+    return w, int(n)
+
+
+def router_backward(logits, ldt: str, idx, grad_w, gwdt: str = "f32",
+                    scoring: str = "softmax", renormalize: bool = False, scale: float = 1.0,
+                    out_dt: str | None = None, lib=None):
+    """Logits gradient of :func:`router_weights` (selected_router_backward).
+    Returns ``(dlogits [T,E] in out_dt storage (default the logits dtype),
+    nan_rows)``."""
+    lib = lib or load_library()
+    out_dt = out_dt or ldt
+    logits = _arr(logits, ldt)
+    T, E = logits.shape
+    idx = _idx64(idx)
+    k = idx.shape[1]
+    gw = _arr(grad_w, gwdt)
+    dl = np.empty((T, E), dtype=_storage(out_dt))
+    n = lib.oracle_router_backward(_ptr(logits), DTYPE_CODES[ldt], T, E, _ptr(idx), k,
+                                   _ptr(gw), DTYPE_CODES[gwdt], SCORING[scoring],
+                                   int(bool(renormalize)), float(scale), _ptr(dl),
+                                   DTYPE_CODES[out_dt])
+    if n < 0:
+        raise ValueError("oracle_router_backward: bad arguments")
+    return dl, int(n)
+
+
+def combine_backward(out_disp, odt: str, w, wdt: str, row_of, grad_y, gdt: str, top_k: int,
+                     lib=None):
+    """Backward of the weighted combine. Returns float64 ``(dexpert [rows,H],
+    dw [T,k])``."""
+    lib = lib or load_library()
+    out_disp = _arr(out_disp, odt)
+    w = _arr(w, wdt)
+    gy = _arr(grad_y, gdt)
+    row_of = np.ascontiguousarray(row_of, dtype=np.int32)
+    T, H = gy.shape
+    rows = out_disp.shape[0]
+    dexp = np.empty((rows, H), dtype=np.float64)
+    dw = np.empty((T, top_k), dtype=np.float64)
+    lib.oracle_combine_backward(_ptr(out_disp), DTYPE_CODES[odt], _ptr(w), DTYPE_CODES[wdt],
+                                _ptr(row_of), _ptr(gy), DTYPE_CODES[gdt], T, top_k, H, rows,
+                                _ptr(dexp), _ptr(dw))
+    return dexp, dw
+
+
+def swiglu_backward_rows(xrows, dt: str, expert_of_row, gate, up, down, dout, ddt: str,
+                         lib=None):
+    """Backward of the SwiGLU experts on (row, expert) pairs, in double.
+    Returns ``(dx [n,H], dgate [E,I,H], dup [E,I,H], ddown [E,H,I])``."""
+    lib = lib or load_library()
+    xrows = _arr(xrows, dt)
+    gate, up, down = _arr(gate, dt), _arr(up, dt), _arr(down, dt)
+    dout = _arr(dout, ddt)
+    E, I, H = gate.shape
+    n = xrows.shape[0]
+    eor = np.ascontiguousarray(expert_of_row, dtype=np.int32)
+    dx = np.empty((n, H), dtype=np.float64)
+    dg = np.empty((E, I, H), dtype=np.float64)
+    du = np.empty((E, I, H), dtype=np.float64)
+    dd = np.empty((E, H, I), dtype=np.float64)
+    rc = lib.oracle_swiglu_backward_rows(_ptr(xrows), DTYPE_CODES[dt], n, _ptr(eor),
+                                         _ptr(gate), _ptr(up), _ptr(down), E, H, I,
+                                         _ptr(dout), DTYPE_CODES[ddt], _ptr(dx), _ptr(dg),
+                                         _ptr(du), _ptr(dd))
+    if rc != 0:
+        raise ValueError("oracle_swiglu_backward_rows: expert id out of range")
+    return dx, dg, du, dd
+
+
+def experts_backward_dispatched(x_disp, dt: str, offsets, gate, up, down, dout, ddt: str,
+                                lib=None):
+    """:func:`swiglu_backward_rows` on dispatched rows (rows of expert e are
+    ``[offsets[e], offsets[e+1])``)."""
+    offsets = np.asarray(offsets, dtype=np.int64)
+    E = np.asarray(gate).shape[0]
+    owner = np.repeat(np.arange(E, dtype=np.int32), np.diff(offsets))
+    return swiglu_backward_rows(x_disp, dt, owner, gate, up, down, dout, ddt, lib)
+
+
+def dispatch_backward(dinput, dt: str, row_of, top_k: int, lib=None):
+    """Backward of the dispatch gather: the selected rows summed back to their
+    token (no routing weight). Returns float64 ``[T,H]``."""
+    lib = lib or load_library()
+    d = _arr(dinput, dt)
+    row_of = np.ascontiguousarray(row_of, dtype=np.int32)
+    T = row_of.size // top_k
+    H = d.shape[1]
+    dx = np.empty((T, H), dtype=np.float64)
+    lib.oracle_dispatch_backward(_ptr(d), DTYPE_CODES[dt], _ptr(row_of), T, top_k, H,
+                                 _ptr(dx))
+    return dx

@@ -46,6 +46,17 @@
  *              [BS] (kept tokens first) or 2-D [BS, K].
  *   [aclnnFFN] aclnnFFN, "Formula": y = activation(x W1 + b1) W2 + b2; the
  *              experts here are its bias-free, SwiGLU-activated case.
+ *   [ruDNN-12] ruDNN user guide, section 12 "MoE first-order training"
+ *              (Chinese edition): FP32 weights of a fixed selection
+ *              (softmax or sigmoid scoring, optional renormalisation of the
+ *              selected weights, then a finite positive scale) and their
+ *              logits gradient; repeated indices act as a gather; an illegal
+ *              index makes the whole row NaN; no derivative through the
+ *              selection. Backward order: combine backward (expert-output
+ *              gradient and FP32 weight gradient), expert backward (input
+ *              rows and FP32 gate/up/down gradients), dispatch backward (the
+ *              selected rows summed back to their token without the routing
+ *              weight), then the router backward.
  *
  * Precision. Routing follows [ruDNN-4] literally: the softmax is computed in
  * float (FP32) with libm expf. Everything the pages leave open (expert GEMMs,
@@ -567,4 +578,261 @@ int oracle_add_rmsnorm(const double *combine, const void *residual, int rdt,
             store_elem(x_out, rdt, t * H + h,
                        combine[t * H + h] + load_elem(residual, rdt, t * H + h));
     return oracle_rmsnorm(x_out, rdt, gamma, gdt, eps, T, H, y, rdt, rstd);
+}
+
+/* ---- first-order training [ruDNN-12] ------------------------------------ */
+
+/*
+ * Score of every expert of row t under a fixed selection: softmax over all E
+ * logits (scoring 0) or the element-wise sigmoid (scoring 1), in double.
+ * Returns 0 when the softmax row is invalid under the routing contract (a NaN
+ * or +inf logit, or every logit -inf), else 1. For the sigmoid, scores of
+ * NaN logits are NaN and +-inf give 1 and 0.
+ */
+static int row_scores(const void *logits, int ldt, int64_t t, int64_t E, int scoring,
+                      double *p)
+{
+    if (scoring == 1) {
+        for (int64_t e = 0; e < E; ++e)
+            p[e] = 1.0 / (1.0 + exp(-load_elem(logits, ldt, t * E + e)));
+        return 1;
+    }
+    int bad = 0, all_ninf = 1;
+    double m = -INFINITY;
+    for (int64_t e = 0; e < E; ++e) {
+        double l = load_elem(logits, ldt, t * E + e);
+        if (isnan(l) || (isinf(l) && l > 0.0)) bad = 1;
+        if (!(isinf(l) && l < 0.0)) all_ninf = 0;
+        if (l > m) m = l;
+    }
+    if (bad || all_ninf) return 0;
+    double s = 0.0;
+    for (int64_t e = 0; e < E; ++e) {
+        p[e] = exp(load_elem(logits, ldt, t * E + e) - m);
+        s += p[e];
+    }
+    for (int64_t e = 0; e < E; ++e) p[e] /= s;
+    return 1;
+}
+
+/*
+ * Weights of a fixed selection: for slot j of token t, s_j = score of expert
+ * idx[t,j] (a repeated id is gathered again); with renormalize, s_j / sum_i s_i
+ * (the sum over the k slots); times scale; rounded once to wdt (FP32 in the
+ * section; f64 for derivative checks). A slot id outside [0, E) makes the
+ * row NaN, and so does an invalid softmax row. Returns the number of NaN
+ * rows so made, or -1 on bad arguments.
+ */
+int64_t oracle_router_weights(const void *logits, int ldt, int64_t T, int64_t E,
+                              const int64_t *idx, int64_t top_k, int scoring,
+                              int renormalize, double scale, void *w, int wdt)
+{
+    if (T < 0 || E < 1 || top_k < 1 || top_k > E || top_k > 64 ||
+        (scoring != 0 && scoring != 1) || !isfinite(scale) || !(scale > 0.0))
+        return -1;
+    double *p = (double *)malloc((size_t)E * sizeof(double));
+    double sel[64];
+    int64_t nan_rows = 0;
+    for (int64_t t = 0; t < T; ++t) {
+        int ok = row_scores(logits, ldt, t, E, scoring, p);
+        for (int64_t j = 0; j < top_k; ++j) {
+            int64_t e = idx[t * top_k + j];
+            if (e < 0 || e >= E) ok = 0;
+            else sel[j] = p[e];
+        }
+        if (!ok) {
+            for (int64_t j = 0; j < top_k; ++j) store_elem(w, wdt, t * top_k + j, (double)NAN);
+            ++nan_rows;
+            continue;
+        }
+        double z = 0.0;
+        for (int64_t j = 0; j < top_k; ++j) z += sel[j];
+        for (int64_t j = 0; j < top_k; ++j) {
+            double v = renormalize ? sel[j] / z : sel[j];
+            store_elem(w, wdt, t * top_k + j, v * scale);
+        }
+    }
+    free(p);
+    return nan_rows;
+}
+
+/*
+ * Logits gradient of the weights above for an upstream gradient gw [T,k]
+ * (FP32 in the section), by the chain rule in double:
+ *   ds_j = scale * gw_j                                  without renormalize,
+ *   ds_j = scale * (gw_j - sum_i gw_i s_i / Z) / Z,  Z = sum_i s_i, with it;
+ *   G_e  = sum of ds_j over the slots j that hold expert e (gather adjoint);
+ *   softmax: dl_e = p_e * (G_e - sum_f p_f G_f);
+ *   sigmoid: dl_e = G_e * sigma_e * (1 - sigma_e).
+ * Rounded once to dldt (the logits dtype in the section). Rows that the
+ * forward makes NaN (illegal id, invalid softmax row) are NaN. Returns the
+ * number of such rows, or -1 on bad arguments.
+ */
+int64_t oracle_router_backward(const void *logits, int ldt, int64_t T, int64_t E,
+                               const int64_t *idx, int64_t top_k, const void *gw, int gwdt,
+                               int scoring, int renormalize, double scale, void *dl,
+                               int dldt)
+{
+    if (T < 0 || E < 1 || top_k < 1 || top_k > E || top_k > 64 ||
+        (scoring != 0 && scoring != 1) || !isfinite(scale) || !(scale > 0.0))
+        return -1;
+    double *p = (double *)malloc((size_t)E * sizeof(double));
+    double *G = (double *)malloc((size_t)E * sizeof(double));
+    double sel[64], ds[64];
+    int64_t nan_rows = 0;
+    for (int64_t t = 0; t < T; ++t) {
+        int ok = row_scores(logits, ldt, t, E, scoring, p);
+        for (int64_t j = 0; j < top_k; ++j) {
+            int64_t e = idx[t * top_k + j];
+            if (e < 0 || e >= E) ok = 0;
+            else sel[j] = p[e];
+        }
+        if (!ok) {
+            for (int64_t e = 0; e < E; ++e) store_elem(dl, dldt, t * E + e, (double)NAN);
+            ++nan_rows;
+            continue;
+        }
+        if (renormalize) {
+            double z = 0.0, gbar = 0.0;
+            for (int64_t j = 0; j < top_k; ++j) z += sel[j];
+            for (int64_t j = 0; j < top_k; ++j)
+                gbar += load_elem(gw, gwdt, t * top_k + j) * sel[j];
+            gbar /= z;
+            for (int64_t j = 0; j < top_k; ++j)
+                ds[j] = scale * (load_elem(gw, gwdt, t * top_k + j) - gbar) / z;
+        } else {
+            for (int64_t j = 0; j < top_k; ++j)
+                ds[j] = scale * load_elem(gw, gwdt, t * top_k + j);
+        }
+        for (int64_t e = 0; e < E; ++e) G[e] = 0.0;
+        for (int64_t j = 0; j < top_k; ++j) G[idx[t * top_k + j]] += ds[j];
+        if (scoring == 0) {
+            double c = 0.0;
+            for (int64_t e = 0; e < E; ++e) c += p[e] * G[e];
+            for (int64_t e = 0; e < E; ++e) store_elem(dl, dldt, t * E + e, p[e] * (G[e] - c));
+        } else {
+            for (int64_t e = 0; e < E; ++e)
+                store_elem(dl, dldt, t * E + e, G[e] * p[e] * (1.0 - p[e]));
+        }
+    }
+    free(p); free(G);
+    return nan_rows;
+}
+
+/*
+ * Backward of the combine y[t] = sum_j w[t,j] * out_disp[row_of[t*k+j]]:
+ *   dexpert[row_of[t*k+j]] = w[t,j] * gy[t]          (the routing weight
+ *                                                     scales the gradient)
+ *   dw[t,j] = sum_h gy[t,h] * out_disp[row_of[t*k+j], h]
+ * in double. A slot with no row (row_of < 0) writes no dexpert row and gets
+ * dw = NaN. dexpert rows no slot names stay 0.
+ */
+void oracle_combine_backward(const void *out_disp, int odt, const void *w, int wdt,
+                             const int32_t *row_of, const void *gy, int gdt, int64_t T,
+                             int64_t top_k, int64_t H, int64_t rows, double *dexpert,
+                             double *dw)
+{
+    for (int64_t i = 0; i < rows * H; ++i) dexpert[i] = 0.0;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t j = 0; j < top_k; ++j) {
+            const int64_t a = t * top_k + j;
+            const int64_t r = row_of[a];
+            if (r < 0) { dw[a] = NAN; continue; }
+            const double wj = load_elem(w, wdt, a);
+            double acc = 0.0;
+            for (int64_t h = 0; h < H; ++h) {
+                const double g = load_elem(gy, gdt, t * H + h);
+                dexpert[r * H + h] = wj * g;
+                acc += g * load_elem(out_disp, odt, r * H + h);
+            }
+            dw[a] = acc;
+        }
+    }
+}
+
+/*
+ * Backward of the bias-free SwiGLU expert o = Wd (silu(Wg x) * (Wu x)) for
+ * every dispatched row r of expert e, given do = dout[r]:
+ *   g = Wg x, u = Wu x, s = sigmoid(g), h = g s u      (recomputed)
+ *   dh    = Wd^T do
+ *   dg    = dh * u * s * (1 + g (1 - s))               (d silu / dg)
+ *   du    = dh * g * s
+ *   dx    = Wg^T dg + Wu^T du
+ *   dWd  += do h^T,  dWg += dg x^T,  dWu += du x^T
+ * All in double. dx is [nrows,H]; dgate, dup are [E,I,H] and ddown [E,H,I],
+ * zeroed here and summed over every row of the expert. Returns -1 on an
+ * expert id out of range.
+ */
+int oracle_swiglu_backward_rows(const void *xrows, int dt, int64_t nrows,
+                                const int32_t *expert_of_row, const void *gate,
+                                const void *up, const void *down, int64_t E, int64_t H,
+                                int64_t I, const void *dout, int ddt, double *dx,
+                                double *dgate, double *dup, double *ddown)
+{
+    for (int64_t i = 0; i < E * I * H; ++i) { dgate[i] = 0.0; dup[i] = 0.0; ddown[i] = 0.0; }
+    double *xr = (double *)malloc((size_t)H * sizeof(double));
+    double *dor = (double *)malloc((size_t)H * sizeof(double));
+    double *hv = (double *)malloc((size_t)I * sizeof(double));
+    double *dgv = (double *)malloc((size_t)I * sizeof(double));
+    double *duv = (double *)malloc((size_t)I * sizeof(double));
+    int rc = 0;
+    for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t e = expert_of_row[r];
+        if (e < 0 || e >= E) { rc = -1; break; }
+        for (int64_t k = 0; k < H; ++k) {
+            xr[k] = load_elem(xrows, dt, r * H + k);
+            dor[k] = load_elem(dout, ddt, r * H + k);
+        }
+        for (int64_t i = 0; i < I; ++i) {
+            double g = 0.0, u = 0.0, dh = 0.0;
+            const int64_t wrow = (e * I + i) * H;
+            for (int64_t k = 0; k < H; ++k) {
+                g += load_elem(gate, dt, wrow + k) * xr[k];
+                u += load_elem(up, dt, wrow + k) * xr[k];
+            }
+            for (int64_t o = 0; o < H; ++o)
+                dh += load_elem(down, dt, (e * H + o) * I + i) * dor[o];
+            const double s = 1.0 / (1.0 + exp(-g));
+            hv[i] = g * s * u;
+            dgv[i] = dh * u * s * (1.0 + g * (1.0 - s));
+            duv[i] = dh * g * s;
+        }
+        for (int64_t o = 0; o < H; ++o)
+            for (int64_t i = 0; i < I; ++i)
+                ddown[(e * H + o) * I + i] += dor[o] * hv[i];
+        for (int64_t i = 0; i < I; ++i)
+            for (int64_t k = 0; k < H; ++k) {
+                dgate[(e * I + i) * H + k] += dgv[i] * xr[k];
+                dup[(e * I + i) * H + k] += duv[i] * xr[k];
+            }
+        for (int64_t k = 0; k < H; ++k) {
+            double acc = 0.0;
+            for (int64_t i = 0; i < I; ++i)
+                acc += load_elem(gate, dt, (e * I + i) * H + k) * dgv[i] +
+                       load_elem(up, dt, (e * I + i) * H + k) * duv[i];
+            dx[r * H + k] = acc;
+        }
+    }
+    free(xr); free(dor); free(hv); free(dgv); free(duv);
+    return rc;
+}
+
+/*
+ * Backward of the dispatch gather: dx[t] = sum over slots j (slot order) of
+ * dinput[row_of[t*k+j]], in double, without the routing weight (the combine
+ * backward already applied it). A slot with no row contributes nothing (the
+ * gather never copied x for it).
+ */
+void oracle_dispatch_backward(const void *dinput, int dt, const int32_t *row_of, int64_t T,
+                              int64_t top_k, int64_t H, double *dx)
+{
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t h = 0; h < H; ++h) {
+            double acc = 0.0;
+            for (int64_t j = 0; j < top_k; ++j) {
+                const int64_t r = row_of[t * top_k + j];
+                if (r >= 0) acc += load_elem(dinput, dt, r * H + h);
+            }
+            dx[t * H + h] = acc;
+        }
 }

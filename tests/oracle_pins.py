@@ -612,4 +612,6 @@ def check_rmsnorm_eps_validation(lib):
         raise AssertionError(f"eps={eps} must be rejected")
 
 
+from oracle_pins_training import *  # noqa: E402,F401,F403  (the training pins)
+
 ALL_CHECKS = [v for k, v in sorted(globals().items()) if k.startswith("check_")]

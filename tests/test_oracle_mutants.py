@@ -97,6 +97,46 @@ MUTANTS = [
      "                } else {\n                    o = 0.0;\n                }"),
     ("sg_sigmoid_wrong_sign", "return (float)(1.0 / (1.0 + exp(-(double)x)));",
      "return (float)(1.0 / (1.0 + exp((double)x)));"),
+    # first-order training
+    ("rw_renorm_dropped", "double v = renormalize ? sel[j] / z : sel[j];", "double v = sel[j];"),
+    ("rw_scale_dropped", "store_elem(w, wdt, t * top_k + j, v * scale);",
+     "store_elem(w, wdt, t * top_k + j, v);"),
+    ("rw_illegal_id_ignored",
+     "if (e < 0 || e >= E) ok = 0;\n            else sel[j] = p[e];\n        }\n        if (!ok) {\n"
+     "            for (int64_t j = 0; j < top_k; ++j) store_elem(w,",
+     "if (e < 0 || e >= E) sel[j] = 0.0;\n            else sel[j] = p[e];\n        }\n        if (!ok) {\n"
+     "            for (int64_t j = 0; j < top_k; ++j) store_elem(w,"),
+    ("rw_sigmoid_wrong_sign", "p[e] = 1.0 / (1.0 + exp(-load_elem(logits, ldt, t * E + e)));",
+     "p[e] = 1.0 / (1.0 + exp(load_elem(logits, ldt, t * E + e)));"),
+    ("rw_softmax_unnormalised", "for (int64_t e = 0; e < E; ++e) p[e] /= s;",
+     "for (int64_t e = 0; e < E; ++e) p[e] /= 1.0;"),
+    ("rb_softmax_not_centred", "store_elem(dl, dldt, t * E + e, p[e] * (G[e] - c));",
+     "store_elem(dl, dldt, t * E + e, p[e] * G[e]);"),
+    ("rb_renorm_mean_dropped", "ds[j] = scale * (load_elem(gw, gwdt, t * top_k + j) - gbar) / z;",
+     "ds[j] = scale * load_elem(gw, gwdt, t * top_k + j) / z;"),
+    ("rb_renorm_not_divided", "ds[j] = scale * (load_elem(gw, gwdt, t * top_k + j) - gbar) / z;",
+     "ds[j] = scale * (load_elem(gw, gwdt, t * top_k + j) - gbar);"),
+    ("rb_sigmoid_derivative_short", "store_elem(dl, dldt, t * E + e, G[e] * p[e] * (1.0 - p[e]));",
+     "store_elem(dl, dldt, t * E + e, G[e] * p[e]);"),
+    ("rb_scale_dropped", "ds[j] = scale * load_elem(gw, gwdt, t * top_k + j);",
+     "ds[j] = load_elem(gw, gwdt, t * top_k + j);"),
+    ("rb_repeat_overwrites", "G[idx[t * top_k + j]] += ds[j];", "G[idx[t * top_k + j]] = ds[j];"),
+    ("cb_dw_uses_weight", "acc += g * load_elem(out_disp, odt, r * H + h);", "acc += g * wj;"),
+    ("cb_dexpert_unweighted", "dexpert[r * H + h] = wj * g;", "dexpert[r * H + h] = g;"),
+    ("sb_dsilu_short", "dgv[i] = dh * u * s * (1.0 + g * (1.0 - s));", "dgv[i] = dh * u * s;"),
+    ("sb_du_sigmoid_only", "duv[i] = dh * g * s;", "duv[i] = dh * s;"),
+    ("sb_gate_up_grads_swapped", "dgate[(e * I + i) * H + k] += dgv[i] * xr[k];",
+     "dgate[(e * I + i) * H + k] += duv[i] * xr[k];"),
+    ("sb_ddown_uses_dg", "ddown[(e * H + o) * I + i] += dor[o] * hv[i];",
+     "ddown[(e * H + o) * I + i] += dor[o] * dgv[i];"),
+    ("sb_dx_up_term_dropped",
+     "acc += load_elem(gate, dt, (e * I + i) * H + k) * dgv[i] +\n"
+     "                       load_elem(up, dt, (e * I + i) * H + k) * duv[i];",
+     "acc += load_elem(gate, dt, (e * I + i) * H + k) * dgv[i];"),
+    ("sb_dh_transposed", "dh += load_elem(down, dt, (e * H + o) * I + i) * dor[o];",
+     "dh += load_elem(down, dt, ((e * H + o) * I + i + 1) % (E * H * I)) * dor[o];"),
+    ("db_last_slot_only", "if (r >= 0) acc += load_elem(dinput, dt, r * H + h);",
+     "if (r >= 0) acc = load_elem(dinput, dt, r * H + h);"),
 ]
 
 
