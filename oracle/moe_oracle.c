@@ -785,10 +785,10 @@ int oracle_swiglu_backward_rows(const void *xrows, int dt, int64_t nrows,
         }
         for (int64_t i = 0; i < I; ++i) {
             double g = 0.0, u = 0.0, dh = 0.0;
-            const int64_t wrow = (e * I + i) * H;
+            const int64_t wr = (e * I + i) * H;
             for (int64_t k = 0; k < H; ++k) {
-                g += load_elem(gate, dt, wrow + k) * xr[k];
-                u += load_elem(up, dt, wrow + k) * xr[k];
+                g += load_elem(gate, dt, wr + k) * xr[k];
+                u += load_elem(up, dt, wr + k) * xr[k];
             }
             for (int64_t o = 0; o < H; ++o)
                 dh += load_elem(down, dt, (e * H + o) * I + i) * dor[o];
