@@ -663,7 +663,8 @@ int64_t oracle_router_weights(const void *logits, int ldt, int64_t T, int64_t E,
  *   ds_j = scale * (gw_j - sum_i gw_i s_i / Z) / Z,  Z = sum_i s_i, with it;
  *   G_e  = sum of ds_j over the slots j that hold expert e (gather adjoint);
  *   softmax: dl_e = p_e * (G_e - sum_f p_f G_f);
- *   sigmoid: dl_e = G_e * sigma_e * (1 - sigma_e).
+ *   sigmoid: dl_e = G_e * sigma_e * (1 - sigma_e) for the selected experts,
+ *            0 for the others.
  * Rounded once to dldt (the logits dtype in the section). Rows that the
  * forward makes NaN (illegal id, invalid softmax row) are NaN. Returns the
  * number of such rows, or -1 on bad arguments.
@@ -711,8 +712,13 @@ int64_t oracle_router_backward(const void *logits, int ldt, int64_t T, int64_t E
             for (int64_t e = 0; e < E; ++e) c += p[e] * G[e];
             for (int64_t e = 0; e < E; ++e) store_elem(dl, dldt, t * E + e, p[e] * (G[e] - c));
         } else {
-            for (int64_t e = 0; e < E; ++e)
+            /* only the selected logits move a sigmoid weight: the others get an
+             * exact 0, even where their own logit is NaN */
+            for (int64_t e = 0; e < E; ++e) store_elem(dl, dldt, t * E + e, 0.0);
+            for (int64_t j = 0; j < top_k; ++j) {
+                const int64_t e = idx[t * top_k + j];
                 store_elem(dl, dldt, t * E + e, G[e] * p[e] * (1.0 - p[e]));
+            }
         }
     }
     free(p); free(G);

@@ -178,6 +178,13 @@ def check_router_backward_invariants(lib):
         dl, _ = oracle.router_backward(logits, "f32", idx, gw, "f32", "sigmoid", renorm, 1.0,
                                        "f64", lib)
         assert np.all(dl[unsel] == 0.0) and np.all(dl[~unsel] != 0.0)
+    # a NaN logit outside a sigmoid selection leaves the gradient untouched
+    lg = logits.copy(); lg[0, unsel[0].nonzero()[0][0]] = np.nan
+    d_nan, n = oracle.router_backward(lg, "f32", idx, gw, "f32", "sigmoid", True, 1.0, "f64",
+                                      lib)
+    d_ref, _ = oracle.router_backward(logits, "f32", idx, gw, "f32", "sigmoid", True, 1.0,
+                                      "f64", lib)
+    assert n == 0 and np.array_equal(d_nan, d_ref)
     # linear in the scale, with and without renormalisation
     for scoring in ("softmax", "sigmoid"):
         for renorm in (False, True):

@@ -118,6 +118,8 @@ MUTANTS = [
      "ds[j] = scale * (load_elem(gw, gwdt, t * top_k + j) - gbar);"),
     ("rb_sigmoid_derivative_short", "store_elem(dl, dldt, t * E + e, G[e] * p[e] * (1.0 - p[e]));",
      "store_elem(dl, dldt, t * E + e, G[e] * p[e]);"),
+    ("rb_sigmoid_unselected_nan", "for (int64_t e = 0; e < E; ++e) store_elem(dl, dldt, t * E + e, 0.0);",
+     "for (int64_t e = 0; e < E; ++e) store_elem(dl, dldt, t * E + e, 0.0 * p[e]);"),
     ("rb_scale_dropped", "ds[j] = scale * load_elem(gw, gwdt, t * top_k + j);",
      "ds[j] = load_elem(gw, gwdt, t * top_k + j);"),
     ("rb_repeat_overwrites", "G[idx[t * top_k + j]] += ds[j];", "G[idx[t * top_k + j]] = ds[j];"),
