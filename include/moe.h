@@ -405,6 +405,160 @@ int moe_forward_sigmoid_grouped(const void *x, int dtype, const void *logits, in
                                 int renormalize, float scale, void *y, void *workspace,
                                 size_t workspace_bytes, void *stream);
 
+/* ======================================================================
+ * First-order training.
+ * ruDNN user guide, section 12 "MoE first-order training": the weights of a
+ * fixed selection and their logits gradient; expert training in the order
+ *   combine backward -> expert backward -> dispatch backward -> router
+ *   backward,
+ * with FP32 routing-weight and expert-weight gradients. Nothing is
+ * differentiated through the top-k / group selection or a correction bias.
+ * ====================================================================== */
+
+/* Scoring of the training weights. */
+typedef enum moe_router_scoring {
+    MOE_SCORING_SOFTMAX = 0,
+    MOE_SCORING_SIGMOID = 1
+} moe_router_scoring;
+
+/* Element type of a selection's expert ids (the section accepts U32, I32,
+ * I64). */
+typedef enum moe_index_dtype {
+    MOE_INDEX_U32 = 0,
+    MOE_INDEX_I32 = 1,
+    MOE_INDEX_I64 = 2
+} moe_index_dtype;
+
+/*
+ * moe_router_weights -- weights of a fixed selection (selected_router_weights).
+ *
+ *   logits   [T, E] in logits_dtype (F32/BF16/F16), read only.
+ *   indices  [T, top_k] expert ids in index_dtype, read only.
+ *   T >= 0, 1 <= E <= 1024, 1 <= top_k <= min(E, 64); scale finite and > 0.
+ *   weights  [T, top_k] FP32, written.
+ *
+ * Slot j of token t scores s_j = softmax(logits[t])[id] (MOE_SCORING_SOFTMAX,
+ * over all E logits) or sigmoid(logits[t, id]) (MOE_SCORING_SIGMOID), with
+ * id = indices[t, j]; a repeated id is gathered again. With renormalize != 0
+ * each s_j is divided by the sum over the k slots; every weight is then
+ * multiplied by scale. FP32 arithmetic. An id outside [0, E) (negative, or
+ * >= E) makes the token's row NaN, reads nothing out of bounds and sets
+ * MOE_ERR_BAD_INDEX in the device status word; a softmax row holding NaN or
+ * +inf, or only -inf, is NaN too (as in moe_route).
+ * Errors: MOE_ERR_NULL, MOE_ERR_SHAPE, MOE_ERR_DTYPE (logits or index dtype,
+ * scoring), MOE_ERR_VALUE (scale), MOE_ERR_ALIGN, MOE_ERR_CUDA.
+ */
+int moe_router_weights(const void *logits, int logits_dtype, int64_t T, int64_t E,
+                       const void *indices, int index_dtype, int top_k, int scoring,
+                       int renormalize, float scale, float *weights, void *stream);
+
+/*
+ * moe_router_backward -- logits gradient of moe_router_weights
+ * (selected_router_backward), for the same arguments and an upstream
+ * gradient grad_weights [T, top_k] FP32.
+ *
+ *   grad_logits  [T, E] in logits_dtype, written.
+ *
+ * With ds_j = scale * g_j (no renormalisation) or
+ * ds_j = scale * (g_j - sum_i g_i s_i / Z) / Z, Z = sum_i s_i, and G_e the
+ * sum of ds_j over the slots holding expert e:
+ *   softmax: d logit_e = p_e * (G_e - sum_f p_f G_f)  (every expert);
+ *   sigmoid: d logit_e = G_e * s_e * (1 - s_e) for selected experts, 0 else.
+ * FP32 arithmetic, rounded once to logits_dtype. Rows that
+ * moe_router_weights makes NaN are NaN here. Errors as moe_router_weights.
+ */
+int moe_router_backward(const void *logits, int logits_dtype, int64_t T, int64_t E,
+                        const void *indices, int index_dtype, int top_k,
+                        const float *grad_weights, int scoring, int renormalize, float scale,
+                        void *grad_logits, void *stream);
+
+/*
+ * moe_combine_backward -- backward of moe_combine
+ * (DispatchedTokens::combine_backward).
+ *
+ *   out_disp   [T * top_k, H] expert outputs of the forward, out_dtype (dtype
+ *              or F32), read only.
+ *   weights    [T, top_k] routing weights in weights_dtype, read only.
+ *   row_of     [T * top_k] int32 (from moe_dispatch), read only.
+ *   grad_y     [T, H] in dtype, read only: the gradient of the combine output.
+ *   grad_out_disp [T * top_k, H] in dtype, written for every row some slot
+ *              names: grad_out_disp[row_of[t*k + j]] = weights[t, j] * grad_y[t].
+ *   grad_weights  [T, top_k] FP32, written:
+ *              sum over h of grad_y[t, h] * out_disp[row_of[t*k + j], h].
+ *
+ * FP32 arithmetic. A slot with row_of < 0 writes no row and gets a NaN
+ * weight gradient. Needs H % 8 == 0. Errors: MOE_ERR_NULL, MOE_ERR_SHAPE,
+ * MOE_ERR_DTYPE, MOE_ERR_ALIGN, MOE_ERR_CUDA.
+ */
+int moe_combine_backward(const void *out_disp, int out_dtype, const void *weights,
+                         int weights_dtype, const int32_t *row_of, const void *grad_y,
+                         int64_t T, int top_k, int64_t H, int dtype, void *grad_out_disp,
+                         float *grad_weights, void *stream);
+
+/*
+ * moe_dispatch_backward -- backward of the dispatch gather
+ * (DispatchedTokens::dispatch_backward).
+ *
+ *   grad_x_disp [T * top_k, H] in dtype, read only (from moe_experts_backward).
+ *   row_of      [T * top_k] int32 (from moe_dispatch), read only.
+ *   grad_x      [T, H] in dtype, written: sum over slots j, in slot order, of
+ *               grad_x_disp[row_of[t*k + j]]; FP32 sum rounded once. The
+ *               routing weight is not applied again. Slots with row_of < 0
+ *               add nothing.
+ * Needs H % 8 == 0. Errors: MOE_ERR_NULL, MOE_ERR_SHAPE, MOE_ERR_DTYPE,
+ * MOE_ERR_ALIGN, MOE_ERR_CUDA.
+ */
+int moe_dispatch_backward(const void *grad_x_disp, int dtype, const int32_t *row_of,
+                          int64_t T, int top_k, int64_t H, void *grad_x, void *stream);
+
+/*
+ * moe_experts_forward_training -- moe_experts_forward that also keeps what
+ * the backward needs (SwiGluExperts::forward_dispatched_training).
+ *
+ *   Arguments as moe_experts_forward, except that the cache replaces the
+ *   workspace:
+ *   cache  moe_experts_training_cache_size(rows, I, dtype) bytes, 256-byte
+ *          aligned, written: h [rows, I] in dtype, then g = x Wg^T and
+ *          u = x Wu^T of every row as two [rows, I] FP32 arrays (kept in FP32
+ *          so the backward's SiLU derivative starts from unrounded values).
+ *          Keep it, unchanged, for moe_experts_backward.
+ * out_disp matches moe_experts_forward with the same arguments.
+ */
+size_t moe_experts_training_cache_size(int64_t rows, int64_t I, int dtype);
+int moe_experts_forward_training(const void *x_disp, const int32_t *offsets, int64_t rows,
+                                 const void *gate, const void *up, const void *down, int64_t E,
+                                 int64_t H, int64_t I, int dtype, void *out_disp, int out_dtype,
+                                 void *cache, size_t cache_bytes, void *stream);
+
+/*
+ * moe_experts_backward -- backward of the SwiGLU experts (cache.backward).
+ *
+ *   x_disp, offsets, rows, gate, up, down, E, H, I, dtype: as given to
+ *          moe_experts_forward_training; cache: what it wrote.
+ *   grad_out     [rows, H] in dtype, read only: gradient of the expert
+ *                outputs (grad_out_disp of moe_combine_backward).
+ *   grad_x_disp  [rows, H] in dtype, written (rows < offsets[E]).
+ *   grad_gate, grad_up [E, I, H] FP32, grad_down [E, H, I] FP32, written in
+ *                full (experts without rows get zeros).
+ *   workspace    moe_experts_backward_workspace_size(...) bytes.
+ *
+ * Per row of expert e (s = sigmoid(g)): dh = do Wd[e],
+ * dg = dh * u * s * (1 + g (1 - s)), du = dh * g * s, dx = dg Wg[e] + du Wu[e];
+ * dWd[e] = sum do^T h, dWg[e] = sum dg^T x, dWu[e] = sum du^T x over the
+ * expert's rows. BF16/F16 run on tcgen05 tensor cores with FP32
+ * accumulation (dg and du rounded to dtype between the GEMMs; h as cached);
+ * F32 runs in FP32 on CUDA cores. Constraints and errors as
+ * moe_experts_forward.
+ */
+size_t moe_experts_backward_workspace_size(int64_t rows, int64_t E, int64_t H, int64_t I,
+                                           int dtype);
+int moe_experts_backward(const void *x_disp, const int32_t *offsets, int64_t rows,
+                         const void *gate, const void *up, const void *down, int64_t E,
+                         int64_t H, int64_t I, int dtype, const void *cache,
+                         const void *grad_out, void *grad_x_disp, float *grad_gate,
+                         float *grad_up, float *grad_down, void *workspace,
+                         size_t workspace_bytes, void *stream);
+
 /*
  * moe_device_status -- read the current device's status word.
  * Synchronises `stream`, then returns MOE_OK, MOE_ERR_BAD_INDEX or

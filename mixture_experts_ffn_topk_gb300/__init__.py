@@ -13,7 +13,9 @@ otherwise they are allocated with torch on the input's device. Workspaces are
 torch ``uint8`` tensors sized by the matching ``*_workspace_size`` call.
 
 Sources: ruDNN user guide sections 3-7 (routing, dispatch, SwiGLU experts,
-combine, RMSNorm); aclnnMoeDistributeCombineAddRmsNormV2 "Function" formula.
+combine, RMSNorm), section 10 (grouped sigmoid routing) and section 12
+(first-order MoE training); aclnnMoeDistributeCombineAddRmsNormV2 "Function"
+formula.
 """
 
 from __future__ import annotations
@@ -42,7 +44,17 @@ EXPORTED = ["moe_status_string", "moe_abi_version", "moe_last_error_detail",
             "moe_dispatch_noalloc",
             "moe_experts_workspace_size", "moe_experts_forward", "moe_combine",
             "moe_combine_add_rmsnorm", "moe_forward_workspace_size",
-            "moe_forward", "moe_forward_sigmoid_grouped", "moe_device_status"]
+            "moe_forward", "moe_forward_sigmoid_grouped", "moe_device_status",
+            "moe_router_weights", "moe_router_backward", "moe_combine_backward",
+            "moe_dispatch_backward", "moe_experts_training_cache_size",
+            "moe_experts_forward_training", "moe_experts_backward_workspace_size",
+            "moe_experts_backward"]
+
+MOE_SCORING_SOFTMAX, MOE_SCORING_SIGMOID = 0, 1
+SCORING_CODES = {"softmax": MOE_SCORING_SOFTMAX, "sigmoid": MOE_SCORING_SIGMOID}
+INDEX_CODES = {torch.int32: 1, torch.int64: 2}
+if hasattr(torch, "uint32"):
+    INDEX_CODES[torch.uint32] = 0
 
 _lock = threading.Lock()
 _lib = None
@@ -102,6 +114,19 @@ def _bind(lib):
                                          _I64, _I64, _INT, _INT, _INT, _INT, _INT, _F, _P,
                                          _P, _SZ, _P], _INT),
         "moe_device_status": ([_P, _INT], _INT),
+        "moe_router_weights": ([_P, _INT, _I64, _I64, _P, _INT, _INT, _INT, _INT, _F, _P,
+                                _P], _INT),
+        "moe_router_backward": ([_P, _INT, _I64, _I64, _P, _INT, _INT, _P, _INT, _INT, _F,
+                                 _P, _P], _INT),
+        "moe_combine_backward": ([_P, _INT, _P, _INT, _P, _P, _I64, _INT, _I64, _INT, _P, _P,
+                                  _P], _INT),
+        "moe_dispatch_backward": ([_P, _INT, _P, _I64, _INT, _I64, _P, _P], _INT),
+        "moe_experts_training_cache_size": ([_I64, _I64, _INT], _SZ),
+        "moe_experts_forward_training": ([_P, _P, _I64, _P, _P, _P, _I64, _I64, _I64, _INT,
+                                          _P, _INT, _P, _SZ, _P], _INT),
+        "moe_experts_backward_workspace_size": ([_I64, _I64, _I64, _I64, _INT], _SZ),
+        "moe_experts_backward": ([_P, _P, _I64, _P, _P, _P, _I64, _I64, _I64, _INT, _P, _P,
+                                  _P, _P, _P, _P, _P, _SZ, _P], _INT),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -464,3 +489,134 @@ def moe_forward_sigmoid_grouped(x: torch.Tensor, logits: torch.Tensor, bias: tor
 def moe_device_status(stream=None, clear: bool = True) -> int:
     """Synchronise ``stream`` and return the device status code (0 = OK)."""
     return int(load_library().moe_device_status(_stream(stream), int(bool(clear))))
+
+
+# ---- first-order training (ruDNN user guide, section 12) -------------------
+
+def _index_code(indices: torch.Tensor) -> int:
+    if indices.dtype not in INDEX_CODES:
+        raise TypeError("expert ids must be int32, int64 or uint32")
+    return INDEX_CODES[indices.dtype]
+
+
+def moe_router_weights(logits: torch.Tensor, indices: torch.Tensor, scoring: str = "softmax",
+                       renormalize: bool = False, scale: float = 1.0, weights=None,
+                       stream=None) -> torch.Tensor:
+    """FP32 weights ``[T, k]`` of the fixed selection ``indices``
+    (selected_router_weights)."""
+    T, E = logits.shape
+    k = indices.shape[1]
+    weights = weights if weights is not None else torch.empty(
+        (T, k), dtype=torch.float32, device=logits.device)
+    rc = load_library().moe_router_weights(
+        _ptr(logits), _code(logits.dtype), T, E, _ptr(indices), _index_code(indices), k,
+        SCORING_CODES[scoring], int(bool(renormalize)), float(scale), _ptr(weights),
+        _stream(stream))
+    _check(rc, "moe_router_weights")
+    return weights
+
+
+def moe_router_backward(logits: torch.Tensor, indices: torch.Tensor, grad_weights: torch.Tensor,
+                        scoring: str = "softmax", renormalize: bool = False, scale: float = 1.0,
+                        grad_logits=None, stream=None) -> torch.Tensor:
+    """Logits gradient ``[T, E]`` (logits dtype) of :func:`moe_router_weights`
+    for the FP32 upstream gradient ``grad_weights [T, k]``."""
+    T, E = logits.shape
+    k = indices.shape[1]
+    grad_logits = grad_logits if grad_logits is not None else torch.empty_like(logits)
+    rc = load_library().moe_router_backward(
+        _ptr(logits), _code(logits.dtype), T, E, _ptr(indices), _index_code(indices), k,
+        _ptr(grad_weights), SCORING_CODES[scoring], int(bool(renormalize)), float(scale),
+        _ptr(grad_logits), _stream(stream))
+    _check(rc, "moe_router_backward")
+    return grad_logits
+
+
+def moe_combine_backward(out_disp: torch.Tensor, weights: torch.Tensor, row_of: torch.Tensor,
+                         grad_y: torch.Tensor, grad_out_disp=None, grad_weights=None,
+                         stream=None):
+    """Backward of :func:`moe_combine`. Returns ``(grad_out_disp [T*k, H] in
+    grad_y.dtype, grad_weights [T, k] FP32)``."""
+    T, k = weights.shape
+    H = grad_y.shape[1]
+    dev = grad_y.device
+    grad_out_disp = grad_out_disp if grad_out_disp is not None else torch.empty(
+        (out_disp.shape[0], H), dtype=grad_y.dtype, device=dev)
+    grad_weights = grad_weights if grad_weights is not None else torch.empty(
+        (T, k), dtype=torch.float32, device=dev)
+    rc = load_library().moe_combine_backward(
+        _ptr(out_disp), _code(out_disp.dtype), _ptr(weights), _code(weights.dtype),
+        _ptr(row_of), _ptr(grad_y), T, k, H, _code(grad_y.dtype), _ptr(grad_out_disp),
+        _ptr(grad_weights), _stream(stream))
+    _check(rc, "moe_combine_backward")
+    return grad_out_disp, grad_weights
+
+
+def moe_dispatch_backward(grad_x_disp: torch.Tensor, row_of: torch.Tensor, T: int, top_k: int,
+                          grad_x=None, stream=None) -> torch.Tensor:
+    """Sum every token's dispatched gradient rows back to ``grad_x [T, H]``."""
+    H = grad_x_disp.shape[1]
+    grad_x = grad_x if grad_x is not None else torch.empty(
+        (T, H), dtype=grad_x_disp.dtype, device=grad_x_disp.device)
+    rc = load_library().moe_dispatch_backward(
+        _ptr(grad_x_disp), _code(grad_x_disp.dtype), _ptr(row_of), T, int(top_k), H,
+        _ptr(grad_x), _stream(stream))
+    _check(rc, "moe_dispatch_backward")
+    return grad_x
+
+
+def moe_experts_training_cache_size(rows: int, I: int, dtype: torch.dtype) -> int:
+    return int(load_library().moe_experts_training_cache_size(rows, I, _code(dtype)))
+
+
+def moe_experts_forward_training(x_disp: torch.Tensor, offsets: torch.Tensor,
+                                 gate: torch.Tensor, up: torch.Tensor, down: torch.Tensor,
+                                 out_dtype: torch.dtype | None = None, out_disp=None,
+                                 cache=None, stream=None):
+    """SwiGLU experts that keep the backward's cache. Returns ``(out_disp,
+    cache)``; ``cache`` (uint8) holds h, g, u as three ``[rows, I]`` planes."""
+    rows, H = x_disp.shape
+    E, I, _ = gate.shape
+    dev = x_disp.device
+    if out_disp is not None:
+        out_dtype = out_disp.dtype
+    out_dtype = out_dtype or x_disp.dtype
+    if out_disp is None:
+        out_disp = torch.empty((rows, H), dtype=out_dtype, device=dev)
+    cache = _workspace(moe_experts_training_cache_size(rows, I, x_disp.dtype), dev, cache)
+    rc = load_library().moe_experts_forward_training(
+        _ptr(x_disp), _ptr(offsets), rows, _ptr(gate), _ptr(up), _ptr(down), E, H, I,
+        _code(x_disp.dtype), _ptr(out_disp), _code(out_dtype), _ptr(cache), _nbytes(cache),
+        _stream(stream))
+    _check(rc, "moe_experts_forward_training")
+    return out_disp, cache
+
+
+def moe_experts_backward_workspace_size(rows: int, E: int, H: int, I: int,
+                                        dtype: torch.dtype) -> int:
+    return int(load_library().moe_experts_backward_workspace_size(rows, E, H, I, _code(dtype)))
+
+
+def moe_experts_backward(x_disp: torch.Tensor, offsets: torch.Tensor, gate: torch.Tensor,
+                         up: torch.Tensor, down: torch.Tensor, cache: torch.Tensor,
+                         grad_out: torch.Tensor, grad_x_disp=None, grad_gate=None,
+                         grad_up=None, grad_down=None, workspace=None, stream=None):
+    """Backward of the SwiGLU experts. Returns ``(grad_x_disp [rows, H],
+    grad_gate [E, I, H], grad_up [E, I, H], grad_down [E, H, I])``, the
+    weight gradients in FP32."""
+    rows, H = x_disp.shape
+    E, I, _ = gate.shape
+    dev = x_disp.device
+    f32 = torch.float32
+    grad_x_disp = grad_x_disp if grad_x_disp is not None else torch.empty_like(x_disp)
+    grad_gate = grad_gate if grad_gate is not None else torch.empty((E, I, H), dtype=f32, device=dev)
+    grad_up = grad_up if grad_up is not None else torch.empty((E, I, H), dtype=f32, device=dev)
+    grad_down = grad_down if grad_down is not None else torch.empty((E, H, I), dtype=f32, device=dev)
+    ws = _workspace(moe_experts_backward_workspace_size(rows, E, H, I, x_disp.dtype), dev,
+                    workspace)
+    rc = load_library().moe_experts_backward(
+        _ptr(x_disp), _ptr(offsets), rows, _ptr(gate), _ptr(up), _ptr(down), E, H, I,
+        _code(x_disp.dtype), _ptr(cache), _ptr(grad_out), _ptr(grad_x_disp), _ptr(grad_gate),
+        _ptr(grad_up), _ptr(grad_down), _ptr(ws), _nbytes(ws), _stream(stream))
+    _check(rc, "moe_experts_backward")
+    return grad_x_disp, grad_gate, grad_up, grad_down

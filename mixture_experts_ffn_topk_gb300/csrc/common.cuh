@@ -10,6 +10,9 @@ namespace moe {
 
 enum : int { DT_F32 = 0, DT_BF16 = 1, DT_F16 = 2 };
 
+// Index element types of the training calls (moe_index_dtype in moe.h).
+enum : int { IDX_U32 = 0, IDX_I32 = 1, IDX_I64 = 2 };
+
 // Bits of the per-device status word (see moe_device_status in moe.h).
 enum : unsigned { ST_BAD_INDEX = 1u, ST_TIMEOUT = 2u };
 

@@ -19,12 +19,15 @@ namespace {
 
 constexpr int SBM = 64, SBN = 64, SBK = 16, STHREADS = 256, SMAX_E = 1024;
 
+// SWIGLU: C = SiLU(A B0^T) * (A B1^T); with pre-activation outputs g_out /
+// u_out (training) the two products are stored there too. Otherwise C = A B0^T.
 template <bool SWIGLU>
 __global__ void __launch_bounds__(STHREADS)
 experts_simt_kernel(const float *__restrict__ A, const int32_t *__restrict__ offsets,
                     int E, const float *__restrict__ B0,
                     const float *__restrict__ B1, int N, int K, int n_tiles,
-                    float *__restrict__ C)
+                    float *__restrict__ C, float *__restrict__ g_out = nullptr,
+                    float *__restrict__ u_out = nullptr)
 {
     __shared__ int prefix[SMAX_E + 1];
     __shared__ int warp_sum[STHREADS / 32];
@@ -127,7 +130,13 @@ experts_simt_kernel(const float *__restrict__ A, const int32_t *__restrict__ off
                 const int gn = col0 + tc * 4 + j;
                 if (gn >= N) continue;
                 float v = accg[i][j];
-                if (SWIGLU) v = v / (1.0f + expf(-v)) * accu[i][j];
+                if (SWIGLU) {
+                    if (g_out != nullptr) {
+                        g_out[(int64_t)gr * N + gn] = v;
+                        u_out[(int64_t)gr * N + gn] = accu[i][j];
+                    }
+                    v = v / (1.0f + expf(-v)) * accu[i][j];
+                }
                 C[(int64_t)gr * N + gn] = v;
             }
         }
@@ -146,7 +155,7 @@ cudaError_t launch_experts_simt(const float *x_disp, const int32_t *offsets,
                                 int64_t rows, const float *gate,
                                 const float *up, const float *down, int E,
                                 int64_t H, int64_t I, float *h_ws,
-                                float *out_disp, cudaStream_t s)
+                                float *out_disp, cudaStream_t s, float *g_out, float *u_out)
 {
     if (rows == 0) return cudaSuccess;
     const int64_t cap = (int64_t)device_sm_count() * 8;
@@ -154,14 +163,15 @@ cudaError_t launch_experts_simt(const float *x_disp, const int32_t *offsets,
     int64_t g1 = tile_upper_bound(rows, E, nt1);
     if (g1 > cap) g1 = cap;
     cudaError_t err = launch_pdl(experts_simt_kernel<true>, dim3((unsigned)g1), dim3(STHREADS), 0,
-                                 s, x_disp, offsets, E, gate, up, (int)I, (int)H, nt1, h_ws);
+                                 s, x_disp, offsets, E, gate, up, (int)I, (int)H, nt1, h_ws,
+                                 g_out, u_out);
     if (err != cudaSuccess) return err;
     const int nt2 = (int)((H + SBN - 1) / SBN);
     int64_t g2 = tile_upper_bound(rows, E, nt2);
     if (g2 > cap) g2 = cap;
     return launch_pdl(experts_simt_kernel<false>, dim3((unsigned)g2), dim3(STHREADS), 0, s,
                       (const float *)h_ws, offsets, E, down, (const float *)nullptr, (int)H,
-                      (int)I, nt2, out_disp);
+                      (int)I, nt2, out_disp, (float *)nullptr, (float *)nullptr);
 }
 
 }  // namespace moe

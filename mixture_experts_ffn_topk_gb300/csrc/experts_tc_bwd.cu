@@ -1,0 +1,617 @@
+// experts_tc_bwd.cu -- BF16/F16 SwiGLU expert backward on tcgen05 tensor cores.
+//
+// ruDNN user guide, section 12 "MoE first-order training" (cache.backward of
+// SwiGluExperts::forward_dispatched_training). Per dispatched row r of
+// expert e, with the forward's cached g = x Wg[e]^T, u = x Wu[e]^T and
+// h = SiLU(g) * u, and the expert-output gradient do:
+//   DH  dh = do Wd[e]        [rows x I], K = H; the epilogue reads the cached
+//                             FP32 g and u and forms
+//                             dg = dh * u * s * (1 + g (1 - s)) and
+//                             du = dh * g * s (s = sigmoid(g)) into
+//                             dgu [rows, 2I] (dg | du) in the input dtype;
+//   DX  dx = dg Wg[e] + du Wu[e]   [rows x H], K = 2I;
+//   WG  dWd[e] = do^T h  [H x I],  dWg[e] = dg^T x, dWu[e] = du^T x  [I x H],
+//       K = the expert's rows; FP32 outputs, zeros for experts without rows.
+// Inputs BF16 or F16, FP32 accumulation in tensor memory.
+//
+// One persistent, warp-specialised kernel per step (one CTA per SM):
+//   warp 0     TMA producer, 4 stages of 48 KiB (A 128 x 64, B 256 x 64);
+//   warp 1     tcgen05.mma issuer, M=128 N=256 K=16, two TMEM accumulators;
+//   warps 2-5  epilogue (tcgen05.ld, math, swizzled staging, line stores);
+//   warp 6     (WG only) tail fixer, see below.
+// Operand layouts: the activation rows of DH and DX are K-major (rows of the
+// dispatched matrices, as in the forward). The weights read across their rows
+// (Wd as [H][I] for dh, Wg/Wu as [I][H] for dx) and both WG operands (columns
+// of row-major activations, reduced over rows) are MN-major: TMA boxes of
+// 64 M/N elements (128 bytes) by 64 k-rows with 128-byte swizzle, described
+// to the MMA with MN-major shared-memory descriptors (64-element groups 8 KiB
+// apart) and the transpose bits of the instruction descriptor.
+// WG reduces over an expert's row segment, which starts and ends anywhere:
+// the last 64-row block of a segment also holds rows of the next expert. The
+// producer lands that block on a separate barrier; the fixer warp zeroes the
+// rows past the segment in every box of the stage, makes the writes visible
+// to the tensor core (fence.proxy.async) and only then releases the stage to
+// the MMA. (Zeroing both operands keeps a NaN row of another expert out.)
+//
+// Every wait is bounded (kWaitLimitNs); on expiry the kernel sets ST_TIMEOUT,
+// stops issuing work, drains its own copies and MMAs, frees TMEM and exits.
+#include <atomic>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int BM = 128;                  // UMMA M: rows (DH, DX) or weight rows (WG)
+constexpr int BN = 256;                  // UMMA N
+constexpr int BK = 64;                   // k per stage
+constexpr int UK = 16;                   // k per tcgen05.mma kind::f16
+constexpr int BOX = 64;                  // MN-major box: 64 elements x 64 k-rows
+constexpr int BOX_BYTES = BOX * BK * 2;  // 8 KiB
+constexpr int A_BYTES = BM * BK * 2;     // 16 KiB
+constexpr int B_BYTES = BN * BK * 2;     // 32 KiB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int STAGES = 4;
+constexpr int ACC_COLS = 256;
+constexpr int TMEM_COLS = 2 * ACC_COLS;
+constexpr int MAX_E = 1024;
+constexpr int EPI_ROW_BYTES = 128;
+constexpr uint64_t kDrainLimitNs = 100000000ull;
+
+enum Mode : int { kDH = 0, kDX = 1, kWG = 2 };
+
+template <int MODE>
+__host__ __device__ constexpr int threads_of() { return MODE == kWG ? 224 : 192; }
+
+struct __align__(1024) BwdSmem {
+    uint8_t stage[STAGES][STAGE_BYTES];
+    uint8_t epi[4][32 * EPI_ROW_BYTES];
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t tail_full[2];
+    uint64_t tail_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+    int prefix[MAX_E + 1];
+    int offs[MAX_E + 1];
+};
+constexpr size_t kBwdSmemBytes = sizeof(BwdSmem) + 1024;
+
+struct BwdParams {
+    const int32_t *offsets;
+    int E;
+    int n_tiles;      // N tiles of 256
+    int num_k;        // DH: H; DX: I (each half); WG: unused
+    int N;            // output columns (DH: I, DX: H, WG: weight columns)
+    int M;            // WG: weight rows
+    int nprob;        // WG: problems in this launch (1: dWd; 2: dWg, dWu)
+    const float *g_plane, *u_plane;     // DH: the cached FP32 g and u [rows, I]
+    uint8_t *out0, *out1;               // DH: dgu; DX: dx; WG: W of problem 0 / 1
+    int64_t out_row_bytes;              // bytes per output row
+    int64_t du_col_bytes;               // DH: byte offset of du inside a dgu row
+    unsigned *status;
+};
+
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Tile id -> (expert, m, n, problem). DH / DX: m-tiles of an expert's rows,
+// m fastest (weight tiles shared through L2). WG: expert slowest, then
+// weight-row tile m, then column tile n.
+template <int MODE>
+__device__ __forceinline__ void decode(const BwdSmem &S, const BwdParams &p, int tile, int &e,
+                                       int &m, int &n, int &prob)
+{
+    if constexpr (MODE == kWG) {
+        const int mt = (p.M + BM - 1) / BM, per = mt * p.n_tiles;
+        prob = tile / (p.E * per);
+        const int rem = tile - prob * p.E * per;
+        e = rem / per;
+        const int loc = rem - e * per;
+        m = loc / p.n_tiles;
+        n = loc - m * p.n_tiles;
+    } else {
+        int lo = 0, hi = p.E - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (S.prefix[mid] <= tile) lo = mid; else hi = mid - 1;
+        }
+        e = lo;
+        const int mu = (S.offs[e + 1] - S.offs[e] + BM - 1) / BM;
+        const int local = tile - S.prefix[e];
+        n = local / mu;
+        m = local - n * mu;
+        prob = 0;
+    }
+}
+
+template <int MODE>
+__device__ __forceinline__ int k_blocks(const BwdSmem &S, const BwdParams &p, int e)
+{
+    if constexpr (MODE == kDH) return (p.num_k + BK - 1) / BK;
+    else if constexpr (MODE == kDX) return 2 * ((p.num_k + BK - 1) / BK);
+    else return (S.offs[e + 1] - S.offs[e] + BK - 1) / BK;
+}
+
+// Rows of the last k-block that belong to the segment (WG), 0 if it is full.
+__device__ __forceinline__ int tail_rows(const BwdSmem &S, int e)
+{
+    return (S.offs[e + 1] - S.offs[e]) % BK;
+}
+
+// Writes 32 rows x 128 bytes (this lane's row in v[]) through the warp's
+// swizzled staging buffer so that each store instruction covers four whole
+// 128-byte row segments. Row rr goes to base + rr * row_bytes + col_byte when
+// rr < rows_valid and the column is below col_limit (bytes).
+__device__ __forceinline__ void emit_rows(uint8_t *stg, const uint32_t (&v)[32], uint8_t *base,
+                                          int64_t row_bytes, int64_t col_byte,
+                                          int64_t col_limit, int rows_valid)
+{
+    const int lane = threadIdx.x & 31, cch = lane & 7;
+#pragma unroll
+    for (int p = 0; p < 8; ++p)
+        *reinterpret_cast<uint4 *>(stg + lane * EPI_ROW_BYTES + ((p ^ (lane & 7)) << 4)) =
+            make_uint4(v[4 * p], v[4 * p + 1], v[4 * p + 2], v[4 * p + 3]);
+    __syncwarp();
+    const int64_t cb = col_byte + cch * 16;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int rr = 4 * j + (lane >> 3);
+        const uint4 q = *reinterpret_cast<const uint4 *>(stg + rr * EPI_ROW_BYTES +
+                                                         ((cch ^ (rr & 7)) << 4));
+        if (rr < rows_valid && cb < col_limit)
+            *reinterpret_cast<uint4 *>(base + rr * row_bytes + cb) = q;
+    }
+    __syncwarp();
+}
+
+template <int DT, int MODE>
+__global__ void __launch_bounds__(threads_of<MODE>(), 1)
+bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+                const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
+                const BwdParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    BwdSmem &S = *reinterpret_cast<BwdSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    unsigned *status = p.status;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) { mbar_init(&S.full[s], 1); mbar_init(&S.empty[s], 1); }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&S.acc_full[a], 1);
+            mbar_init(&S.acc_empty[a], 4);
+            mbar_init(&S.tail_full[a], 1);
+            mbar_init(&S.tail_empty[a], 1);
+        }
+        mbar_init(&S.drain, 1);
+        S.abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        tmem_alloc<1>(&S.tmem_base, TMEM_COLS);
+        tmem_relinquish<1>();
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+    for (int i = threadIdx.x; i <= p.E; i += threads_of<MODE>()) S.offs[i] = p.offsets[i];
+    __syncthreads();
+    if (MODE != kWG && warp == 0) {
+        // prefix[e] = tiles of experts < e (lane l owns a contiguous run)
+        const int per = (p.E + 31) / 32, e0 = lane * per;
+        int local = 0;
+        for (int e = e0; e < e0 + per && e < p.E; ++e)
+            local += (S.offs[e + 1] - S.offs[e] + BM - 1) / BM * p.n_tiles;
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int run = incl - local;
+        for (int e = e0; e < e0 + per && e < p.E; ++e) {
+            S.prefix[e] = run;
+            run += (S.offs[e + 1] - S.offs[e] + BM - 1) / BM * p.n_tiles;
+        }
+        if (lane == 31) S.prefix[p.E] = incl;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    const uint32_t tmem_base = S.tmem_base;
+    const int total_tiles = MODE == kWG ? p.nprob * p.E * ((p.M + BM - 1) / BM) * p.n_tiles
+                                        : S.prefix[p.E];
+    volatile int *abort_flag = &S.abort;
+    uint32_t filled_mask = 0, filled_parity = 0;       // producer: stages in flight
+    uint32_t tail_mask = 0, tail_parity = 0;           // producer: tail copies in flight
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------------ TMA producer
+        int stage = 0, tb = 0;
+        uint32_t phase = 0, tphase = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+            int e, m, n, prob;
+            decode<MODE>(S, p, tile, e, m, n, prob);
+            const int nkb = k_blocks<MODE>(S, p, e);
+            const int tail = MODE == kWG ? tail_rows(S, e) : 0;
+            const int seg0 = S.offs[e];
+            for (int kb = 0; kb < nkb; ++kb) {
+                if (!mbar_wait(&S.empty[stage], phase ^ 1u, abort_flag, status, kWaitLimitNs)) { ok = false; break; }
+                const bool is_tail = MODE == kWG && tail != 0 && kb == nkb - 1;
+                uint64_t *bar = &S.full[stage];
+                if (is_tail) {
+                    if (!mbar_wait(&S.tail_empty[tb], tphase ^ 1u, abort_flag, status, kWaitLimitNs)) { ok = false; break; }
+                    bar = &S.tail_full[tb];
+                }
+                uint8_t *sa = S.stage[stage];
+                uint8_t *sb = sa + A_BYTES;
+                mbar_arrive_expect_tx(bar, STAGE_BYTES);
+                if constexpr (MODE == kDH) {
+                    const int row0 = seg0 + m * BM;
+                    tma_load_2d(sa, &tmA0, bar, kb * BK, row0);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        tma_load_3d(sb + j * BOX_BYTES, &tmB0, bar, n * BN + j * BOX, kb * BK, e);
+                } else if constexpr (MODE == kDX) {
+                    const int row0 = seg0 + m * BM;
+                    const int half = (p.num_k + BK - 1) / BK;
+                    const bool second = kb >= half;
+                    const int kk = (second ? kb - half : kb) * BK;
+                    tma_load_2d(sa, second ? &tmA1 : &tmA0, bar, kk, row0);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        tma_load_3d(sb + j * BOX_BYTES, second ? &tmB1 : &tmB0, bar, n * BN + j * BOX, kk, e);
+                } else {
+                    const int r0 = seg0 + kb * BK;
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+                        tma_load_2d(sa + j * BOX_BYTES, prob ? &tmA1 : &tmA0, bar, m * BM + j * BOX, r0);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        tma_load_2d(sb + j * BOX_BYTES, &tmB0, bar, n * BN + j * BOX, r0);
+                }
+                if (is_tail) {
+                    tail_mask |= 1u << tb;
+                    tail_parity = (tail_parity & ~(1u << tb)) | (tphase << tb);
+                    if (++tb == 2) { tb = 0; tphase ^= 1u; }
+                } else {
+                    filled_mask |= 1u << stage;
+                    filled_parity = (filled_parity & ~(1u << stage)) | (phase << stage);
+                }
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------------ MMA issuer
+        constexpr uint32_t idesc = idesc_f16_major<DT>(BM, BN, MODE == kWG, true);
+        int stage = 0;
+        uint32_t phase = 0;
+        int it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++it) {
+            int e, m, n, prob;
+            decode<MODE>(S, p, tile, e, m, n, prob);
+            const int nkb = k_blocks<MODE>(S, p, e);
+            const int acc = it & 1;
+            const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+            if (!mbar_wait(&S.acc_empty[acc], acc_phase ^ 1u, abort_flag, status, kWaitLimitNs)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t d = tmem_base + (uint32_t)(acc * ACC_COLS);
+            for (int kb = 0; kb < nkb; ++kb) {
+                if (!mbar_wait(&S.full[stage], phase, abort_flag, status, kWaitLimitNs)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t a0 = smem_u32(S.stage[stage]);
+                const uint32_t b0 = a0 + A_BYTES;
+#pragma unroll
+                for (int k = 0; k < BK / UK; ++k) {
+                    const uint64_t ad = MODE == kWG ? sdesc_mn_sw128(a0 + k * UK * 128, BOX_BYTES)
+                                                    : sdesc_k_sw128(a0 + k * UK * 2);
+                    const uint64_t bd = sdesc_mn_sw128(b0 + k * UK * 128, BOX_BYTES);
+                    umma_f16<1>(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                }
+                umma_commit<1>(&S.empty[stage]);
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+            if (ok) umma_commit<1>(&S.acc_full[acc]);
+        }
+        if (*abort_flag) {
+            umma_commit<1>(&S.drain);
+            mbar_wait(&S.drain, 0, nullptr, status, kDrainLimitNs);
+        }
+    } else if (MODE == kWG && warp == 6) {
+        // ------------------------------------------------------ tail fixer
+        int stage = 0, tb = 0;
+        uint32_t tphase = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+            int e, m, n, prob;
+            decode<MODE>(S, p, tile, e, m, n, prob);
+            const int nkb = k_blocks<MODE>(S, p, e);
+            const int tail = tail_rows(S, e);
+            for (int kb = 0; kb < nkb; ++kb) {
+                if (tail != 0 && kb == nkb - 1) {
+                    const bool ready = mbar_wait(&S.tail_full[tb], tphase, abort_flag, status, kWaitLimitNs);
+                    if (!__all_sync(0xffffffffu, ready)) { ok = false; break; }
+                    // rows [tail, 64) of the six 64-row boxes (2 of A, 4 of B)
+                    const int zrows = BK - tail;
+                    const int per_box = zrows * (EPI_ROW_BYTES / 16);
+                    uint8_t *base = S.stage[stage];
+                    for (int i = lane; i < 6 * per_box; i += 32) {
+                        const int box = i / per_box, rem = i - box * per_box;
+                        const int row = tail + rem / 8, chunk = rem % 8;
+                        *reinterpret_cast<uint4 *>(base + box * BOX_BYTES + row * 128 + chunk * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&S.full[stage]);
+                        mbar_arrive(&S.tail_empty[tb]);
+                    }
+                    if (++tb == 2) { tb = 0; tphase ^= 1u; }
+                }
+                if (++stage == STAGES) stage = 0;
+            }
+        }
+    } else if (warp >= 2 && warp < 6) {
+        // ------------------------------------------------------ epilogue
+        const int q = warp & 3;                    // TMEM lane quadrant
+        uint8_t *stg = S.epi[warp - 2];
+        int it = 0;
+        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++it) {
+            int e, m, n, prob;
+            decode<MODE>(S, p, tile, e, m, n, prob);
+            const int acc = it & 1;
+            const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+            const bool ready = mbar_wait(&S.acc_full[acc], acc_phase, abort_flag, status, kWaitLimitNs);
+            if (!__all_sync(0xffffffffu, ready)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
+            if constexpr (MODE == kWG) {
+                // rows: weight rows m*128 + q*32 + r; FP32, 32 columns per round
+                const int row0 = m * BM + q * 32;
+                const int rows_valid = p.M - row0;
+                const bool empty_expert = S.offs[e + 1] == S.offs[e];
+                uint8_t *W = (prob ? p.out1 : p.out0) + ((int64_t)e * p.M + row0) * p.out_row_bytes;
+#pragma unroll 1
+                for (int rd = 0; rd < BN / 32; ++rd) {
+                    uint32_t v[32];
+                    if (empty_expert) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = 0u;
+                    } else {
+                        tmem_ld32(tbase + rd * 32, v);
+                        tmem_ld_wait(v);
+                    }
+                    emit_rows(stg, v, W, p.out_row_bytes, (int64_t)(n * BN + rd * 32) * 4,
+                              p.out_row_bytes, rows_valid);
+                }
+            } else {
+                const int seg_rows = S.offs[e + 1] - S.offs[e];
+                const int r_seg = m * BM + q * 32;                      // warp's first row in the segment
+                const int rows_valid = seg_rows - r_seg;
+                const int64_t grow0 = (int64_t)S.offs[e] + r_seg;       // its dispatched row
+                uint8_t *ob = p.out0 + grow0 * p.out_row_bytes;
+                const int64_t col_limit = (int64_t)p.N * 2;
+#pragma unroll 1
+                for (int rd = 0; rd < BN / 64; ++rd) {
+                    uint32_t v0[32];
+                    if constexpr (MODE == kDX) {
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            uint32_t d[32];
+                            tmem_ld32(tbase + (rd * 2 + half) * 32, d);
+                            tmem_ld_wait(d);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                v0[half * 16 + i] = pack2<DT>(__uint_as_float(d[2 * i]),
+                                                              __uint_as_float(d[2 * i + 1]));
+                        }
+                        emit_rows(stg, v0, ob, p.out_row_bytes, (int64_t)(n * BN + rd * 64) * 2,
+                                  col_limit, rows_valid);
+                    } else {
+                        uint32_t v1[32];
+                        const bool row_ok = lane < rows_valid;
+                        const int64_t grow = grow0 + lane;
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            const int col0 = n * BN + (rd * 2 + half) * 32;
+                            uint32_t d[32];
+                            tmem_ld32(tbase + (rd * 2 + half) * 32, d);
+                            // the cached FP32 g and u of these 32 columns of this lane's row
+                            float4 gv[8], uv[8];
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) {
+                                if (row_ok && col0 + 4 * c < p.N) {
+                                    const int64_t off = grow * p.N + col0 + 4 * c;
+                                    gv[c] = *reinterpret_cast<const float4 *>(p.g_plane + off);
+                                    uv[c] = *reinterpret_cast<const float4 *>(p.u_plane + off);
+                                } else {
+                                    gv[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                                    uv[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                                }
+                            }
+                            tmem_ld_wait(d);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                const float4 g4 = gv[i / 2], u4 = uv[i / 2];
+                                const float2 g = (i & 1) ? make_float2(g4.z, g4.w) : make_float2(g4.x, g4.y);
+                                const float2 u = (i & 1) ? make_float2(u4.z, u4.w) : make_float2(u4.x, u4.y);
+                                const float dh0 = __uint_as_float(d[2 * i]);
+                                const float dh1 = __uint_as_float(d[2 * i + 1]);
+                                const float s0 = 1.0f / (1.0f + __expf(-g.x));
+                                const float s1 = 1.0f / (1.0f + __expf(-g.y));
+                                v0[half * 16 + i] = pack2<DT>(dh0 * u.x * s0 * (1.0f + g.x * (1.0f - s0)),
+                                                              dh1 * u.y * s1 * (1.0f + g.y * (1.0f - s1)));
+                                v1[half * 16 + i] = pack2<DT>(dh0 * g.x * s0, dh1 * g.y * s1);
+                            }
+                        }
+                        const int64_t cb = (int64_t)(n * BN + rd * 64) * 2;
+                        emit_rows(stg, v0, ob, p.out_row_bytes, cb, col_limit, rows_valid);
+                        emit_rows(stg, v1, ob + p.du_col_bytes, p.out_row_bytes, cb, col_limit,
+                                  rows_valid);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.acc_empty[acc]);
+        }
+    }
+
+    // ------------------------------------------------------------ teardown
+    __syncthreads();
+    if (*abort_flag && warp == 0 && lane == 0) {
+        for (int s = 0; s < STAGES; ++s)
+            if (filled_mask >> s & 1u)
+                mbar_wait(&S.full[s], filled_parity >> s & 1u, nullptr, status, kDrainLimitNs);
+        for (int t = 0; t < 2; ++t)
+            if (tail_mask >> t & 1u)
+                mbar_wait(&S.tail_full[t], tail_parity >> t & 1u, nullptr, status, kDrainLimitNs);
+    }
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc<1>(tmem_base, TMEM_COLS);
+    }
+}
+
+// ---- host side ---------------------------------------------------------------
+
+template <int DT, int MODE>
+cudaError_t launch_step(int64_t units, const CUtensorMap &a0, const CUtensorMap &a1,
+                        const CUtensorMap &b0, const CUtensorMap &b1, const BwdParams &p,
+                        cudaStream_t s)
+{
+    static std::atomic<uint64_t> done_mask{0};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(done_mask.load() & bit)) {
+        err = cudaFuncSetAttribute(bwd_gemm_kernel<DT, MODE>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBwdSmemBytes);
+        if (err != cudaSuccess) return err;
+        done_mask.fetch_or(bit);
+    }
+    const int64_t sms = device_sm_count();
+    const int grid = (int)(units < sms ? (units < 1 ? 1 : units) : sms);
+    return launch_pdl(bwd_gemm_kernel<DT, MODE>, dim3((unsigned)grid), dim3(threads_of<MODE>()),
+                      kBwdSmemBytes, s, a0, a1, b0, b1, p);
+}
+
+template <int DT>
+cudaError_t launch_backward(const void *x_disp, const int32_t *offsets, int64_t rows,
+                            const void *gate, const void *up, const void *down, int E, int64_t H,
+                            int64_t I, const void *cache, const void *dout, void *dgu, void *dx,
+                            float *dgate, float *dup, float *ddown, unsigned *status,
+                            cudaStream_t s)
+{
+    const CUtensorMapDataType tdt =
+        DT == DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const uint64_t R = (uint64_t)(rows > 0 ? rows : 1);
+    if (rows == 0) {
+        // no activation rows: only the zero weight gradients are written and no
+        // tensor map below is ever read; gate stands in for the absent pointers
+        dout = cache = x_disp = gate;
+        dgu = const_cast<void *>(gate);
+    }
+    const uint8_t *cb = static_cast<const uint8_t *>(cache);
+    const float *g_plane = reinterpret_cast<const float *>(cb + rows * I * 2);
+    const uint8_t *dgu_b = static_cast<const uint8_t *>(dgu);
+    // DH: dout rows (K-major) x Wd[e] read as [H][I] (MN-major)
+    // DX: dg / du column views of dgu (K-major) x Wg[e], Wu[e] read as [I][H]
+    // WG: columns of do / dg / du (MN-major) x columns of h / x (MN-major)
+    CUtensorMap dh_a, dh_b, dx_a0, dx_a1, dx_b0, dx_b1, wd_a, wd_b, wgu_a0, wgu_a1, wgu_b;
+    if (!encode_2d(&dh_a, tdt, dout, (uint64_t)H, R, BK, BM) ||
+        !encode_3d(&dh_b, tdt, down, (uint64_t)I, (uint64_t)H, (uint64_t)E, BOX, BK) ||
+        !encode_2d_strided(&dx_a0, tdt, dgu_b, (uint64_t)I, R, (uint64_t)(4 * I), BK, BM) ||
+        !encode_2d_strided(&dx_a1, tdt, dgu_b + 2 * I, (uint64_t)I, R, (uint64_t)(4 * I), BK, BM) ||
+        !encode_3d(&dx_b0, tdt, gate, (uint64_t)H, (uint64_t)I, (uint64_t)E, BOX, BK) ||
+        !encode_3d(&dx_b1, tdt, up, (uint64_t)H, (uint64_t)I, (uint64_t)E, BOX, BK) ||
+        !encode_2d(&wd_a, tdt, dout, (uint64_t)H, R, BOX, BK) ||
+        !encode_2d(&wd_b, tdt, cb, (uint64_t)I, R, BOX, BK) ||
+        !encode_2d_strided(&wgu_a0, tdt, dgu_b, (uint64_t)I, R, (uint64_t)(4 * I), BOX, BK) ||
+        !encode_2d_strided(&wgu_a1, tdt, dgu_b + 2 * I, (uint64_t)I, R, (uint64_t)(4 * I), BOX, BK) ||
+        !encode_2d(&wgu_b, tdt, x_disp, (uint64_t)H, R, BOX, BK))
+        return cudaErrorInvalidValue;
+
+    BwdParams p{};
+    p.offsets = offsets;
+    p.E = E;
+    p.status = status;
+    cudaError_t err;
+    if (rows > 0) {
+        const int64_t mt = rows / BM + (rows < E ? rows : E);     // M-tiles, upper bound
+        // DH: dh, then dg / du into dgu
+        p.n_tiles = (int)((I + BN - 1) / BN);
+        p.num_k = (int)H;
+        p.N = (int)I;
+        p.g_plane = g_plane;
+        p.u_plane = g_plane + rows * I;
+        p.out0 = static_cast<uint8_t *>(dgu);
+        p.out_row_bytes = 4 * I;
+        p.du_col_bytes = 2 * I;
+        err = launch_step<DT, kDH>(mt * p.n_tiles, dh_a, dh_a, dh_b, dh_b, p, s);
+        if (err != cudaSuccess) return err;
+        // DX
+        p.n_tiles = (int)((H + BN - 1) / BN);
+        p.num_k = (int)I;
+        p.N = (int)H;
+        p.out0 = static_cast<uint8_t *>(dx);
+        p.out_row_bytes = 2 * H;
+        err = launch_step<DT, kDX>(mt * p.n_tiles, dx_a0, dx_a1, dx_b0, dx_b1, p, s);
+        if (err != cudaSuccess) return err;
+    }
+    // WG: dWd (M = H rows of Wd, N = I)
+    p.M = (int)H;
+    p.N = (int)I;
+    p.n_tiles = (int)((I + BN - 1) / BN);
+    p.nprob = 1;
+    p.out0 = reinterpret_cast<uint8_t *>(ddown);
+    p.out1 = nullptr;
+    p.out_row_bytes = 4 * I;
+    err = launch_step<DT, kWG>((int64_t)E * ((H + BM - 1) / BM) * p.n_tiles, wd_a, wd_a, wd_b,
+                               wd_b, p, s);
+    if (err != cudaSuccess) return err;
+    // WG: dWg, dWu (M = I rows, N = H)
+    p.M = (int)I;
+    p.N = (int)H;
+    p.n_tiles = (int)((H + BN - 1) / BN);
+    p.nprob = 2;
+    p.out0 = reinterpret_cast<uint8_t *>(dgate);
+    p.out1 = reinterpret_cast<uint8_t *>(dup);
+    p.out_row_bytes = 4 * H;
+    return launch_step<DT, kWG>(2 * (int64_t)E * ((I + BM - 1) / BM) * p.n_tiles, wgu_a0, wgu_a1,
+                                wgu_b, wgu_b, p, s);
+}
+
+}  // namespace
+
+cudaError_t launch_experts_tc_backward(int dt, const void *x_disp, const int32_t *offsets,
+                                       int64_t rows, const void *gate, const void *up,
+                                       const void *down, int E, int64_t H, int64_t I,
+                                       const void *cache, const void *dout, void *dgu_ws,
+                                       void *dx, float *dgate, float *dup, float *ddown,
+                                       unsigned *status, cudaStream_t s)
+{
+    if (dt == DT_BF16)
+        return launch_backward<DT_BF16>(x_disp, offsets, rows, gate, up, down, E, H, I, cache,
+                                        dout, dgu_ws, dx, dgate, dup, ddown, status, s);
+    return launch_backward<DT_F16>(x_disp, offsets, rows, gate, up, down, E, H, I, cache, dout,
+                                   dgu_ws, dx, dgate, dup, ddown, status, s);
+}
+
+}  // namespace moe

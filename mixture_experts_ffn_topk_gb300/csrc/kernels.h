@@ -64,12 +64,50 @@ cudaError_t launch_combine(const void *out_disp, int odt, const void *w, int wdt
 cudaError_t launch_rmsnorm(const void *x, int xdt, const void *gamma, int gdt, float eps,
                            int64_t rows, int64_t H, void *y, float *rstd, cudaStream_t s);
 
-// FP32 SwiGLU experts on CUDA cores. h_ws holds [rows, I] floats.
+// FP32 SwiGLU experts on CUDA cores. h_ws holds [rows, I] floats. With
+// g_out / u_out (training) the gate and up products [rows, I] are kept too.
 cudaError_t launch_experts_simt(const float *x_disp, const int32_t *offsets,
                                 int64_t rows, const float *gate,
                                 const float *up, const float *down, int E,
                                 int64_t H, int64_t I, float *h_ws,
-                                float *out_disp, cudaStream_t s);
+                                float *out_disp, cudaStream_t s, float *g_out = nullptr,
+                                float *u_out = nullptr);
+
+// FP32 SwiGLU expert backward on CUDA cores, in three steps:
+//   dgu [rows, 2I]: per row, dg = dh * u * s * (1 + g (1 - s)) in columns
+//                   [0, I) and du = dh * g * s in [I, 2I), dh = dout Wd[e]
+//                   (s = sigmoid(g); g, u from the forward's cache);
+//   dx  [rows, H] = dg Wg[e] + du Wu[e];
+//   dgate/dup [E, I, H] and ddown [E, H, I] (FP32): sums over each expert's
+//   rows of dg x^T, du x^T and dout h^T; experts without rows get zeros.
+// cache holds h, g, u as three [rows, I] arrays.
+cudaError_t launch_experts_simt_backward(const float *x_disp, const int32_t *offsets,
+                                         int64_t rows, const float *gate, const float *up,
+                                         const float *down, int E, int64_t H, int64_t I,
+                                         const float *cache, const float *dout, float *dgu,
+                                         float *dx, float *dgate, float *dup, float *ddown,
+                                         cudaStream_t s);
+
+// ---- first-order training (ruDNN user guide, section 12) ----
+int router_train_max_top_k();
+// FP32 weights [T, k] of a fixed selection (idt: IDX_*); sigmoid selects the
+// scoring; ids outside [0, E) NaN the row and set ST_BAD_INDEX.
+cudaError_t launch_router_weights(const void *logits, int ldt, int64_t T, int E, const void *idx,
+                                  int idt, int k, int sigmoid, int renorm, float scale,
+                                  float *w_out, unsigned *status, cudaStream_t s);
+// Logits gradient [T, E] in ldt for the FP32 weight gradient gw [T, k].
+cudaError_t launch_router_backward(const void *logits, int ldt, int64_t T, int E,
+                                   const void *idx, int idt, int k, const float *gw,
+                                   int sigmoid, int renorm, float scale, void *dl_out,
+                                   unsigned *status, cudaStream_t s);
+// dexp[row_of[a]] = w[a] * gy[a / k] (dtype dt), dw[a] = <gy, out_disp row>
+// (FP32); out_disp in odt (dt or F32); H % 8 == 0.
+cudaError_t launch_combine_backward(const void *out_disp, int odt, const void *w, int wdt,
+                                    const int32_t *row_of, const void *gy, int dt, int64_t T,
+                                    int k, int64_t H, void *dexp, float *dw, cudaStream_t s);
+// dx[t] = sum_j d[row_of[t*k + j]] (rows with row_of < 0 skipped); H % 8 == 0.
+cudaError_t launch_dispatch_backward(const void *d, int dt, const int32_t *row_of, int64_t T,
+                                     int k, int64_t H, void *dx, cudaStream_t s);
 
 // BF16/F16 SwiGLU experts on tcgen05 tensor cores (TMA + TMEM).
 // h_ws holds [rows, I] elements of dt; out_disp is FP32 when out_f32, else dt.
@@ -92,6 +130,23 @@ cudaError_t launch_experts_tc_combine(int dt, const void *x_disp,
                                       void *h_ws, const int32_t *src_of,
                                       const void *w, int wdt, int top_k,
                                       float *y_acc, unsigned *status, cudaStream_t s);
+
+// Training forward: launch_experts_tc with g and u kept. cache holds h, g, u
+// as three [rows, I] arrays of dt (h feeds the second GEMM).
+cudaError_t launch_experts_tc_training(int dt, const void *x_disp, const int32_t *offsets,
+                                       int64_t rows, const void *gate, const void *up,
+                                       const void *down, int E, int64_t H, int64_t I,
+                                       void *cache, void *out_disp, bool out_f32,
+                                       unsigned *status, cudaStream_t s);
+
+// Expert backward on tcgen05 (see launch_experts_simt_backward for the
+// math); dgu_ws holds [rows, 2I] of dt.
+cudaError_t launch_experts_tc_backward(int dt, const void *x_disp, const int32_t *offsets,
+                                       int64_t rows, const void *gate, const void *up,
+                                       const void *down, int E, int64_t H, int64_t I,
+                                       const void *cache, const void *dout, void *dgu_ws,
+                                       void *dx, float *dgate, float *dup, float *ddown,
+                                       unsigned *status, cudaStream_t s);
 
 // y = y_acc rounded to ydt ([T, H], H % 8 == 0).
 cudaError_t launch_finalize(const float *y_acc, int64_t T, int64_t H, void *y, int ydt,

@@ -8,6 +8,7 @@
 #include <stdio.h>
 
 #include <atomic>
+#include <initializer_list>
 
 #include "../../include/moe.h"
 #include "common.cuh"
@@ -536,6 +537,215 @@ int moe_forward_sigmoid_grouped(const void *x, int dtype, const void *logits, in
                                 logits, logits_dtype, T, (int)E, bias, top_k, groups,
                                 selected_groups, group_top_two, renormalize, scale, idx, w, s);
                         });
+}
+
+// ---- first-order training (ruDNN user guide, section 12) ------------------
+
+namespace {
+
+int check_router_train_args(const void *logits, int ldt, int64_t T, int64_t E, const void *idx,
+                            int idt, int top_k, int scoring, float scale, const void *in2,
+                            const void *out)
+{
+    if (!valid_dtype(ldt)) return fail(MOE_ERR_DTYPE, "logits dtype must be F32, BF16 or F16");
+    if (idt != MOE_INDEX_U32 && idt != MOE_INDEX_I32 && idt != MOE_INDEX_I64)
+        return fail(MOE_ERR_DTYPE, "index dtype must be U32, I32 or I64");
+    if (scoring != MOE_SCORING_SOFTMAX && scoring != MOE_SCORING_SIGMOID)
+        return fail(MOE_ERR_DTYPE, "scoring must be softmax or sigmoid");
+    if (T < 0 || E < 1 || E > kMaxE) return fail(MOE_ERR_SHAPE, "need T >= 0 and 1 <= E <= 1024");
+    if (top_k < 1 || top_k > E || top_k > router_train_max_top_k())
+        return fail(MOE_ERR_SHAPE, "need 1 <= top_k <= min(E, 64)");
+    if (T * top_k > kMaxRows) return fail(MOE_ERR_SHAPE, "T * top_k exceeds 2^31 - 1");
+    if (!std::isfinite(scale) || !(scale > 0.0f)) return fail(MOE_ERR_VALUE, "scale must be finite and > 0");
+    if (T == 0) return MOE_OK;
+    if (!logits || !idx || !in2 || !out) return fail(MOE_ERR_NULL, "router training: NULL tensor");
+    if (!aligned16(logits) || !aligned16(idx) || !aligned16(in2) || !aligned16(out))
+        return fail(MOE_ERR_ALIGN, "router training: tensors must be 16-byte aligned");
+    return MOE_OK;
+}
+
+// Training cache: h [rows, I] in the expert dtype, then g and u [rows, I] in FP32.
+size_t cache_bytes_for(int64_t rows, int64_t I, int dt)
+{
+    return round_up((size_t)rows * (size_t)I * (elem_bytes(dt) + 8), 256);
+}
+
+int check_experts_ptrs(const char *name, std::initializer_list<const void *> ptrs)
+{
+    for (const void *q : ptrs)
+        if (!q) return fail(MOE_ERR_NULL, name);
+    for (const void *q : ptrs)
+        if (!aligned16(q)) return fail(MOE_ERR_ALIGN, name);
+    return MOE_OK;
+}
+
+}  // namespace
+
+int moe_router_weights(const void *logits, int logits_dtype, int64_t T, int64_t E,
+                       const void *indices, int index_dtype, int top_k, int scoring,
+                       int renormalize, float scale, float *weights, void *stream)
+{
+    int rc = check_router_train_args(logits, logits_dtype, T, E, indices, index_dtype, top_k,
+                                     scoring, scale, weights, weights);
+    if (rc != MOE_OK || T == 0) return rc;
+    unsigned *st = status_ptr();
+    if (!st) return fail(MOE_ERR_CUDA, "cannot resolve the device status word");
+    cudaError_t err = launch_router_weights(logits, logits_dtype, T, (int)E, indices, index_dtype,
+                                            top_k, scoring == MOE_SCORING_SIGMOID, renormalize != 0,
+                                            scale, weights, st, static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_router_weights");
+}
+
+int moe_router_backward(const void *logits, int logits_dtype, int64_t T, int64_t E,
+                        const void *indices, int index_dtype, int top_k,
+                        const float *grad_weights, int scoring, int renormalize, float scale,
+                        void *grad_logits, void *stream)
+{
+    int rc = check_router_train_args(logits, logits_dtype, T, E, indices, index_dtype, top_k,
+                                     scoring, scale, grad_weights, grad_logits);
+    if (rc != MOE_OK || T == 0) return rc;
+    unsigned *st = status_ptr();
+    if (!st) return fail(MOE_ERR_CUDA, "cannot resolve the device status word");
+    cudaError_t err = launch_router_backward(logits, logits_dtype, T, (int)E, indices,
+                                             index_dtype, top_k, grad_weights,
+                                             scoring == MOE_SCORING_SIGMOID, renormalize != 0,
+                                             scale, grad_logits, st,
+                                             static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_router_backward");
+}
+
+int moe_combine_backward(const void *out_disp, int out_dtype, const void *weights,
+                         int weights_dtype, const int32_t *row_of, const void *grad_y,
+                         int64_t T, int top_k, int64_t H, int dtype, void *grad_out_disp,
+                         float *grad_weights, void *stream)
+{
+    if (!valid_dtype(out_dtype) || !valid_dtype(weights_dtype) || !valid_dtype(dtype))
+        return fail(MOE_ERR_DTYPE, "dtype must be F32, BF16 or F16");
+    if (out_dtype != dtype && out_dtype != MOE_F32)
+        return fail(MOE_ERR_DTYPE, "expert outputs must be in the activation dtype or F32");
+    if (T < 0 || top_k < 1 || T * top_k > kMaxRows)
+        return fail(MOE_ERR_SHAPE, "need T >= 0, top_k >= 1, T*top_k < 2^31");
+    if (H < 1 || H % 8 != 0) return fail(MOE_ERR_SHAPE, "H must be a positive multiple of 8");
+    if (T == 0) return MOE_OK;
+    int rc = check_experts_ptrs("moe_combine_backward: tensors must be non-NULL and 16-byte aligned",
+                                {out_disp, weights, row_of, grad_y, grad_out_disp, grad_weights});
+    if (rc != MOE_OK) return rc;
+    cudaError_t err = launch_combine_backward(out_disp, out_dtype, weights, weights_dtype, row_of,
+                                              grad_y, dtype, T, top_k, H, grad_out_disp,
+                                              grad_weights, static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_combine_backward");
+}
+
+int moe_dispatch_backward(const void *grad_x_disp, int dtype, const int32_t *row_of,
+                          int64_t T, int top_k, int64_t H, void *grad_x, void *stream)
+{
+    if (!valid_dtype(dtype)) return fail(MOE_ERR_DTYPE, "dtype must be F32, BF16 or F16");
+    if (T < 0 || top_k < 1 || T * top_k > kMaxRows)
+        return fail(MOE_ERR_SHAPE, "need T >= 0, top_k >= 1, T*top_k < 2^31");
+    if (H < 1 || H % 8 != 0) return fail(MOE_ERR_SHAPE, "H must be a positive multiple of 8");
+    if (T == 0) return MOE_OK;
+    int rc = check_experts_ptrs("moe_dispatch_backward: tensors must be non-NULL and 16-byte aligned",
+                                {grad_x_disp, row_of, grad_x});
+    if (rc != MOE_OK) return rc;
+    cudaError_t err = launch_dispatch_backward(grad_x_disp, dtype, row_of, T, top_k, H, grad_x,
+                                               static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_dispatch_backward");
+}
+
+size_t moe_experts_training_cache_size(int64_t rows, int64_t I, int dtype)
+{
+    if (rows <= 0 || I <= 0 || !valid_dtype(dtype)) return 0;
+    return cache_bytes_for(rows, I, dtype);
+}
+
+int moe_experts_forward_training(const void *x_disp, const int32_t *offsets, int64_t rows,
+                                 const void *gate, const void *up, const void *down, int64_t E,
+                                 int64_t H, int64_t I, int dtype, void *out_disp, int out_dtype,
+                                 void *cache, size_t cache_bytes, void *stream)
+{
+    int rc = check_experts_args(rows, E, H, I, dtype);
+    if (rc != MOE_OK) return rc;
+    if (out_dtype != dtype && out_dtype != MOE_F32)
+        return fail(MOE_ERR_DTYPE, "out_dtype must be the expert dtype or F32");
+    if (rows == 0) return MOE_OK;
+    rc = check_experts_ptrs("moe_experts_forward_training: tensors must be non-NULL and 16-byte aligned",
+                            {x_disp, offsets, gate, up, down, out_disp});
+    if (rc != MOE_OK) return rc;
+    if (cache_bytes < cache_bytes_for(rows, I, dtype) || !cache ||
+        (reinterpret_cast<uintptr_t>(cache) & 255u))
+        return fail(MOE_ERR_WORKSPACE, "moe_experts_forward_training: cache too small or not 256-byte aligned");
+    uint8_t *h = static_cast<uint8_t *>(cache);
+    uint8_t *g = h + (size_t)rows * (size_t)I * elem_bytes(dtype);
+    uint8_t *u = g + (size_t)rows * (size_t)I * 4;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t err;
+    if (dtype == MOE_F32) {
+        err = launch_experts_simt(static_cast<const float *>(x_disp), offsets, rows,
+                                  static_cast<const float *>(gate), static_cast<const float *>(up),
+                                  static_cast<const float *>(down), (int)E, H, I,
+                                  reinterpret_cast<float *>(h), static_cast<float *>(out_disp), s,
+                                  reinterpret_cast<float *>(g), reinterpret_cast<float *>(u));
+    } else {
+        unsigned *st = status_ptr();
+        if (!st) return fail(MOE_ERR_CUDA, "cannot resolve the device status word");
+        err = launch_experts_tc_training(dtype, x_disp, offsets, rows, gate, up, down, (int)E, H,
+                                         I, cache, out_disp, out_dtype == MOE_F32, st, s);
+        if (err == cudaErrorInvalidValue)
+            return fail(MOE_ERR_ALIGN, "TMA descriptor rejected (pointer alignment or shape)");
+    }
+    return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_experts_forward_training");
+}
+
+size_t moe_experts_backward_workspace_size(int64_t rows, int64_t E, int64_t H, int64_t I,
+                                           int dtype)
+{
+    (void)E;
+    (void)H;
+    if (rows <= 0 || I <= 0 || !valid_dtype(dtype)) return 0;
+    return round_up(2 * (size_t)rows * (size_t)I * elem_bytes(dtype), 256);
+}
+
+int moe_experts_backward(const void *x_disp, const int32_t *offsets, int64_t rows,
+                         const void *gate, const void *up, const void *down, int64_t E,
+                         int64_t H, int64_t I, int dtype, const void *cache,
+                         const void *grad_out, void *grad_x_disp, float *grad_gate,
+                         float *grad_up, float *grad_down, void *workspace,
+                         size_t workspace_bytes, void *stream)
+{
+    int rc = check_experts_args(rows, E, H, I, dtype);
+    if (rc != MOE_OK) return rc;
+    rc = check_experts_ptrs("moe_experts_backward: tensors must be non-NULL and 16-byte aligned",
+                            {offsets, gate, up, down, grad_gate, grad_up, grad_down});
+    if (rc != MOE_OK) return rc;
+    if (rows > 0) {
+        rc = check_experts_ptrs("moe_experts_backward: tensors must be non-NULL and 16-byte aligned",
+                                {x_disp, cache, grad_out, grad_x_disp});
+        if (rc != MOE_OK) return rc;
+        if ((reinterpret_cast<uintptr_t>(cache) & 255u))
+            return fail(MOE_ERR_WORKSPACE, "moe_experts_backward: cache not 256-byte aligned");
+        const size_t need = moe_experts_backward_workspace_size(rows, E, H, I, dtype);
+        if (workspace_bytes < need || !workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+            return fail(MOE_ERR_WORKSPACE, "moe_experts_backward: workspace too small or not 256-byte aligned");
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t err;
+    if (dtype == MOE_F32) {
+        err = launch_experts_simt_backward(
+            static_cast<const float *>(x_disp), offsets, rows, static_cast<const float *>(gate),
+            static_cast<const float *>(up), static_cast<const float *>(down), (int)E, H, I,
+            static_cast<const float *>(cache), static_cast<const float *>(grad_out),
+            static_cast<float *>(workspace), static_cast<float *>(grad_x_disp), grad_gate, grad_up,
+            grad_down, s);
+    } else {
+        unsigned *st = status_ptr();
+        if (!st) return fail(MOE_ERR_CUDA, "cannot resolve the device status word");
+        err = launch_experts_tc_backward(dtype, x_disp, offsets, rows, gate, up, down, (int)E, H, I,
+                                         cache, grad_out, workspace, grad_x_disp, grad_gate,
+                                         grad_up, grad_down, st, s);
+        if (err == cudaErrorInvalidValue)
+            return fail(MOE_ERR_ALIGN, "TMA descriptor rejected (pointer alignment or shape)");
+    }
+    return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_experts_backward");
 }
 
 int moe_device_status(void *stream, int clear)

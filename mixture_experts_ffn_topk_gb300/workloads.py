@@ -256,3 +256,12 @@ def from_numpy(a, dtype: str, device="cpu") -> torch.Tensor:
     else:
         t = torch.from_numpy(a)
     return t.to(device)
+
+
+def training_grad(cfg: MoeConfig, device="cpu", seed: int | None = None) -> torch.Tensor:
+    """Upstream gradient of the MoE output for a training step: N(0, 1)
+    ``[T, H]`` in the activation dtype, drawn by a CPU generator of its own
+    (seed + 101) and moved to ``device``."""
+    seed = cfg.seed if seed is None else seed
+    g = _gen(seed + 101, "cpu")
+    return _normal((cfg.T, cfg.H), g, "cpu", dtype=cfg.dtype).to(device)

@@ -115,6 +115,9 @@ def _bind(lib):
     lib.oracle_swiglu_backward_rows.argtypes = [_P, _INT, _I64, _P, _P, _P, _P, _I64, _I64,
                                                 _I64, _P, _INT, _P, _P, _P, _P]
     lib.oracle_swiglu_backward_rows.restype = _INT
+    lib.oracle_swiglu_cache_rows.argtypes = [_P, _INT, _I64, _P, _P, _P, _I64, _I64, _I64,
+                                             _P, _P, _P]
+    lib.oracle_swiglu_cache_rows.restype = _INT
     lib.oracle_dispatch_backward.argtypes = [_P, _INT, _P, _I64, _I64, _I64, _P]
     lib.oracle_dispatch_backward.restype = None
     return lib
@@ -535,3 +538,21 @@ def dispatch_backward(dinput, dt: str, row_of, top_k: int, lib=None):
     lib.oracle_dispatch_backward(_ptr(d), DTYPE_CODES[dt], _ptr(row_of), T, top_k, H,
                                  _ptr(dx))
     return dx
+
+
+def experts_cache_dispatched(x_disp, dt: str, offsets, gate, up, lib=None):
+    """The training forward's cache on dispatched rows: ``(g, u, h)``, each
+    float64 ``[offsets[E], I]``."""
+    lib = lib or load_library()
+    x_disp = _arr(x_disp, dt)
+    gate, up = _arr(gate, dt), _arr(up, dt)
+    E, I, H = gate.shape
+    offsets = np.asarray(offsets, dtype=np.int64)
+    n = int(offsets[E])
+    owner = np.ascontiguousarray(np.repeat(np.arange(E, dtype=np.int32), np.diff(offsets)))
+    g = np.empty((n, I)); u = np.empty((n, I)); h = np.empty((n, I))
+    rc = lib.oracle_swiglu_cache_rows(_ptr(x_disp), DTYPE_CODES[dt], n, _ptr(owner), _ptr(gate),
+                                      _ptr(up), E, H, I, _ptr(g), _ptr(u), _ptr(h))
+    if rc != 0:
+        raise ValueError("oracle_swiglu_cache_rows: expert id out of range")
+    return g, u, h

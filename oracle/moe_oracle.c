@@ -824,6 +824,34 @@ int oracle_swiglu_backward_rows(const void *xrows, int dt, int64_t nrows,
 }
 
 /*
+ * What the training forward keeps per dispatched row r of expert e: the gate
+ * and up products g = Wg[e] x_r and u = Wu[e] x_r, and h = SiLU(g) * u, each
+ * [nrows, I] in double. Returns -1 on an expert id out of range.
+ */
+int oracle_swiglu_cache_rows(const void *xrows, int dt, int64_t nrows,
+                             const int32_t *expert_of_row, const void *gate, const void *up,
+                             int64_t E, int64_t H, int64_t I, double *g_out, double *u_out,
+                             double *h_out)
+{
+    for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t e = expert_of_row[r];
+        if (e < 0 || e >= E) return -1;
+        for (int64_t i = 0; i < I; ++i) {
+            double gv = 0.0, uv = 0.0;
+            for (int64_t k = 0; k < H; ++k) {
+                const double xv = load_elem(xrows, dt, r * H + k);
+                gv += load_elem(gate, dt, (e * I + i) * H + k) * xv;
+                uv += load_elem(up, dt, (e * I + i) * H + k) * xv;
+            }
+            g_out[r * I + i] = gv;
+            u_out[r * I + i] = uv;
+            h_out[r * I + i] = gv / (1.0 + exp(-gv)) * uv;
+        }
+    }
+    return 0;
+}
+
+/*
  * Backward of the dispatch gather: dx[t] = sum over slots j (slot order) of
  * dinput[row_of[t*k+j]], in double, without the routing weight (the combine
  * backward already applied it). A slot with no row contributes nothing (the

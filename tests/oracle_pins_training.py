@@ -365,3 +365,26 @@ def check_training_chain_finite_differences(lib):
             ap[which][pos] += h; am[which][pos] -= h
             fd[pos] = (np.sum(gy * forward(*ap)[3]) - np.sum(gy * forward(*am)[3])) / (2 * h)
         _rel_close(grad, fd, 2e-7, f"chain operand {which}")
+
+
+def check_swiglu_cache_matches_forward(lib):
+    """The cache's h equals the forward's SwiGLU activation: pushed through a
+    down projection of ones it must give the forward's output."""
+    rng = np.random.default_rng(19)
+    E, H, I, n = 3, 8, 5, 7
+    x = rng.standard_normal((n, H))
+    gate = rng.standard_normal((E, I, H))
+    up = rng.standard_normal((E, I, H))
+    counts = np.array([2, 0, 5])
+    offsets = np.concatenate([[0], np.cumsum(counts)])
+    g, u, h = oracle.experts_cache_dispatched(x, "f64", offsets, gate, up, lib)
+    owner = np.repeat(np.arange(E), counts)
+    # g and u are the plain products (numpy matmul per row)
+    for r in range(n):
+        assert np.allclose(g[r], gate[owner[r]] @ x[r], rtol=1e-13, atol=1e-13)
+        assert np.allclose(u[r], up[owner[r]] @ x[r], rtol=1e-13, atol=1e-13)
+    # h against the forward: a down projection with unit vectors reads h back
+    for i in range(I):
+        down = np.zeros((E, H, I)); down[:, 0, i] = 1.0
+        out = oracle.experts_dispatched(x, "f64", offsets.astype(np.int32), gate, up, down, lib)
+        assert np.allclose(out[:, 0], h[:, i], rtol=1e-14, atol=0)

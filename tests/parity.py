@@ -19,7 +19,14 @@ Bars (fixed once here, used by every parity test):
   correctly rounded exact result already fails on outputs whose max|y|/RMS
   exceeds ~10 (bf16 half-ulp is 2^-9 |y|), which the routed MoE outputs reach;
 * NaN positions must match exactly in every case; RMS is taken over the
-  finite reference entries.
+  finite reference entries;
+* training backward: the bar above covers products with ONE operand that this
+  design rounds to BF16/F16 on its way (the forward's h). In the chained
+  backward, every tensor-core product has two such operands (the output
+  gradient rounded to the activation dtype by the combine backward, times h,
+  dg or du, themselves rounded), and independent roundings add, so those
+  results take ``rounds=2``: ``2 * 2e-2 * RMS``. An emulation of exactly these
+  roundings on the test shapes reaches 0.028 x RMS (one rounding: 0.018).
 """
 
 from __future__ import annotations
@@ -54,7 +61,7 @@ def assert_nan_match(got: np.ndarray, ref: np.ndarray, what: str):
         raise AssertionError(f"{what}: NaN positions differ at {bad.tolist()}")
 
 
-def assert_close(got: np.ndarray, ref: np.ndarray, dtype: str, what: str):
+def assert_close(got: np.ndarray, ref: np.ndarray, dtype: str, what: str, rounds: int = 1):
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert got.shape == ref.shape, (what, got.shape, ref.shape)
@@ -76,12 +83,12 @@ def assert_close(got: np.ndarray, ref: np.ndarray, dtype: str, what: str):
     else:
         half_ulp = half_ulp_of(ref[m], dtype)
         excess = err - half_ulp
-        bound = 2e-2 * r
+        bound = 2e-2 * rounds * r
         if excess.max() > bound:
             i = int(np.argmax(excess))
             raise AssertionError(
                 f"{what}: {dtype} error {err[i]:.4e} - half ulp {half_ulp[i]:.3e} > "
-                f"2e-2*RMS = {bound:.4e} (ref {ref[m][i]:.5e}, got {got[m][i]:.5e})")
+                f"{2e-2 * rounds:g}*RMS = {bound:.4e} (ref {ref[m][i]:.5e}, got {got[m][i]:.5e})")
 
 
 def half_ulp_of(ref: np.ndarray, dtype: str) -> np.ndarray:
