@@ -57,7 +57,8 @@ def load_peaks():
         return dict(FALLBACK_PEAKS, source="fallback")
 
 
-KERNEL_SOURCES = {"experts": ["experts_tc.cu", "common.cuh"],
+KERNEL_SOURCES = {"experts": ["experts_tc.cu", "tc_ptx.cuh", "common.cuh"],
+                  "experts_bwd": ["experts_tc_bwd.cu", "tc_ptx.cuh", "common.cuh"],
                   "combine_add_rmsnorm": ["combine.cu", "common.cuh"]}
 
 
@@ -214,6 +215,8 @@ def run_ours(args, rank, world, local, dist):
         return run_combine_norm(args, rank, world, local, dist, dev, peaks, flush)
     if args.workload == "routing_sweep":
         return run_routing_sweep(args, world, dist, dev, peaks, flush)
+    if args.workload in TRAINING_WORKLOADS:
+        return run_training(args, rank, world, local, dist, dev, peaks, flush)
 
     cfg = W.CONFIGS[args.workload]
     d = W.moe_inputs(cfg, device=dev, seed=cfg.seed + 1000 * rank)
@@ -383,6 +386,232 @@ def run_ours(args, rank, world, local, dist):
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, d, args.cpu_seconds)
     return line
+
+
+# Training step workloads: a forward that keeps the backward's cache, then
+# the four backward steps of ruDNN section 12, on a forward workload's shapes.
+TRAINING_WORKLOADS = {"train_fine_prefill_bf16": "fine_prefill_bf16",
+                      "train_coarse_prefill_bf16": "coarse_prefill_bf16"}
+
+
+def run_training(args, rank, world, local, dist, dev, peaks, flush):
+    """One step = route -> dispatch -> router weights (softmax of the fixed
+    selection) -> experts forward keeping the cache -> combine, then combine
+    backward -> expert backward -> dispatch backward -> router backward, for
+    an N(0,1) output gradient. Inputs and weights resident in HBM."""
+    import mixture_experts_ffn_topk_gb300 as moe
+    from mixture_experts_ffn_topk_gb300 import workloads as W
+    base = W.CONFIGS[TRAINING_WORKLOADS[args.workload]]
+    cfg = base
+    d = W.moe_inputs(cfg, device=dev, seed=cfg.seed + 1000 * rank)
+    gy = W.training_grad(cfg, device=dev, seed=cfg.seed + 1000 * rank)
+    T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.top_k
+    A = T * k
+    x, logits = d["x"], d["logits"]
+    dt = x.dtype
+    f32 = torch.float32
+    b = {"idx": torch.empty((T, k), dtype=torch.int32, device=dev),
+         "wr": torch.empty((T, k), dtype=logits.dtype, device=dev),
+         "counts": torch.empty(E, dtype=torch.int32, device=dev),
+         "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
+         "row_of": torch.empty(A, dtype=torch.int32, device=dev),
+         "src_of": torch.empty(A, dtype=torch.int32, device=dev),
+         "x_disp": torch.empty((A, H), dtype=dt, device=dev),
+         "w": torch.empty((T, k), dtype=f32, device=dev),
+         "out": torch.empty((A, H), dtype=f32, device=dev),
+         "cache": torch.empty(moe.moe_experts_training_cache_size(A, I, dt), dtype=torch.uint8,
+                              device=dev),
+         "y": torch.empty((T, H), dtype=dt, device=dev),
+         "dexp": torch.empty((A, H), dtype=dt, device=dev),
+         "dw": torch.empty((T, k), dtype=f32, device=dev),
+         "dxd": torch.empty((A, H), dtype=dt, device=dev),
+         "dgate": torch.empty((E, I, H), dtype=f32, device=dev),
+         "dup": torch.empty((E, I, H), dtype=f32, device=dev),
+         "ddown": torch.empty((E, H, I), dtype=f32, device=dev),
+         "dx": torch.empty((T, H), dtype=dt, device=dev),
+         "dl": torch.empty_like(logits),
+         "ws_d": torch.empty(max(1, moe.moe_dispatch_workspace_size(T, k, E)),
+                             dtype=torch.uint8, device=dev),
+         "ws_b": torch.empty(moe.moe_experts_backward_workspace_size(A, E, H, I, dt),
+                             dtype=torch.uint8, device=dev)}
+    stream = torch.cuda.current_stream(dev)
+
+    def step(x_, lg, g_, ev=None):
+        if ev: ev[0].record(stream)
+        moe.moe_route(lg, k, cfg.renormalize, expert_indices=b["idx"], weights=b["wr"])
+        moe.moe_dispatch(b["idx"], x_, E, counts=b["counts"], offsets=b["offsets"],
+                         row_of=b["row_of"], src_of=b["src_of"], x_disp=b["x_disp"],
+                         workspace=b["ws_d"])
+        moe.moe_router_weights(lg, b["idx"], "softmax", cfg.renormalize, 1.0, weights=b["w"])
+        if ev: ev[1].record(stream)
+        moe.moe_experts_forward_training(b["x_disp"], b["offsets"], d["gate"], d["up"],
+                                         d["down"], out_disp=b["out"], cache=b["cache"])
+        if ev: ev[2].record(stream)
+        moe.moe_combine(b["out"], b["w"], b["row_of"], y=b["y"])
+        moe.moe_combine_backward(b["out"], b["w"], b["row_of"], g_, grad_out_disp=b["dexp"],
+                                 grad_weights=b["dw"])
+        if ev: ev[3].record(stream)
+        moe.moe_experts_backward(b["x_disp"], b["offsets"], d["gate"], d["up"], d["down"],
+                                 b["cache"], b["dexp"], grad_x_disp=b["dxd"],
+                                 grad_gate=b["dgate"], grad_up=b["dup"], grad_down=b["ddown"],
+                                 workspace=b["ws_b"])
+        if ev: ev[4].record(stream)
+        moe.moe_dispatch_backward(b["dxd"], b["row_of"], T, k, grad_x=b["dx"])
+        moe.moe_router_backward(lg, b["idx"], b["dw"], "softmax", cfg.renormalize, 1.0,
+                                grad_logits=b["dl"])
+        if ev: ev[5].record(stream)
+
+    # route 1, dispatch 4, router weights 1, experts fwd 2, combine 1,
+    # combine bwd 1, experts bwd 4, dispatch bwd 1, router bwd 1
+    launches_per_step = 16
+    for _ in range(args.warmup):
+        step(x, logits, gy)
+        flush.fill_(1)
+    torch.cuda.synchronize(dev)
+    if moe.moe_device_status() != 0:
+        raise RuntimeError("device status error during warm-up")
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(args.steps)]
+    barrier(dist, dev)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev) as clk:
+        for a, e in pairs:
+            a.record(stream)
+            step(x, logits, gy)
+            e.record(stream)
+            flush.fill_(1)
+        torch.cuda.synchronize(dev)
+    barrier(dist, dev)
+    ms = statistics.mean(a.elapsed_time(e) for a, e in pairs)
+    ms_max = reduce_max(dist, ms, dev)
+
+    names = ["route+dispatch+weights", "experts_fwd", "combine+combine_bwd", "experts_bwd",
+             "dispatch_bwd+router_bwd"]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        step(x, logits, gy, evs[i])
+        flush.fill_(1)
+    torch.cuda.synchronize(dev)
+    stage_ms = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1])
+                                   for i in range(args.steps)) for j, n in enumerate(names)}
+
+    # end to end: x, logits and the output gradient in from pinned host
+    # memory, the input and logits gradients back out
+    hx = torch.empty(x.shape, dtype=dt, pin_memory=True); hx.copy_(x)
+    hl = torch.empty(logits.shape, dtype=logits.dtype, pin_memory=True); hl.copy_(logits)
+    hg = torch.empty(gy.shape, dtype=dt, pin_memory=True); hg.copy_(gy)
+    hdx = torch.empty(x.shape, dtype=dt, pin_memory=True)
+    hdl = torch.empty(logits.shape, dtype=logits.dtype, pin_memory=True)
+    dx_in, dl_in, dg_in = torch.empty_like(x), torch.empty_like(logits), torch.empty_like(gy)
+
+    def e2e():
+        dx_in.copy_(hx, non_blocking=True)
+        dl_in.copy_(hl, non_blocking=True)
+        dg_in.copy_(hg, non_blocking=True)
+        step(dx_in, dl_in, dg_in)
+        hdx.copy_(b["dx"], non_blocking=True)
+        hdl.copy_(b["dl"], non_blocking=True)
+    e2e_ms = timed_loop(e2e, args, stream, flush)
+    e2e_ms_max = reduce_max(dist, e2e_ms, dev)
+    if moe.moe_device_status() != 0:
+        raise RuntimeError("device status error in the timed region")
+
+    eb = x.element_size()
+    touched = int((b["counts"].cpu() > 0).sum())
+    bwd_ms = stage_ms["experts_bwd"]
+    bwd_flops = 12.0 * H * I * A
+    # algorithmic bytes of the expert backward: the touched experts' weights
+    # read (dh, dx), the FP32 weight gradients of every expert written, the
+    # activations read (do twice, x, h, g and u) and dgu written and read twice
+    bwd_bytes = (3 * touched * I * H * eb + 3 * E * I * H * 4
+                 + 2 * A * H * eb + A * H * eb + A * I * eb + 2 * A * I * 4
+                 + 3 * 2 * A * I * eb + A * H * eb)
+    tflops = bwd_flops / (bwd_ms / 1e3) / 1e12
+    gbs = bwd_bytes / (bwd_ms / 1e3) / 1e9
+    t_tensor = bwd_flops / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = bwd_bytes / (peaks["hbm_gbs"] * 1e9)
+    common = {"kernel": "expert backward (dh + dx + weight-gradient tcgen05 GEMMs)",
+              "algorithmic_flops": bwd_flops, "algorithmic_bytes": bwd_bytes,
+              "traffic": load_traffic(args.workload, "experts_bwd"),
+              "tflops": tflops, "gbs": gbs,
+              "frac_bf16_peak": tflops / peaks["bf16_tflops"], "frac_hbm": gbs / peaks["hbm_gbs"]}
+    if t_tensor >= t_hbm:
+        roof = dict(common, bound="tensor", achieved=tflops, peak=peaks["bf16_tflops"],
+                    unit="TFLOP/s", frac=tflops / peaks["bf16_tflops"],
+                    peak_source=peaks["source"] + " burst bf16")
+    else:
+        roof = dict(common, bound="hbm", achieved=gbs, peak=peaks["hbm_gbs"], unit="GB/s",
+                    frac=gbs / peaks["hbm_gbs"], peak_source=peaks["source"] + " HBM copy")
+    fwd_flops = 6.0 * H * I * A
+    line = {
+        "metric": "MoE training step (forward + first-order backward) tokens/s",
+        "value": aggregate(ms_max / 1e3, T, world), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; random-init expert weights; N(0,1) output gradient)",
+        "config": dict({"workload": args.workload, "T": T, "H": H, "I": I, "E": E, "top_k": k,
+                        "renormalize": cfg.renormalize, "router_scoring": "softmax",
+                        "global_batch": T * world, "parallelism": f"replicas x{world}",
+                        "l2": "flushed between steps (256 MiB write)"}),
+        "e2e": {"value": aggregate(e2e_ms_max / 1e3, T, world), "unit": UNIT,
+                "h2d_bytes_per_step": x.numel() * eb + logits.numel() * logits.element_size()
+                + gy.numel() * eb,
+                "d2h_bytes_per_step": x.numel() * eb + logits.numel() * logits.element_size()},
+        "roofline": roof,
+        "kernels": {n: {"ms": v} for n, v in stage_ms.items()},
+        "experts_fwd_tflops": fwd_flops / (stage_ms["experts_fwd"] / 1e3) / 1e12,
+        "experts_touched": touched,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_training_baseline(cfg, d, gy, args.cpu_seconds)
+    return line
+
+
+def cpu_training_baseline(cfg, d, gy, seconds):
+    """The oracle's training step on a bounded token sample (one thread):
+    forward with the fixed selection and router weights, then the four
+    backward steps, for the sampled tokens as a batch of their own."""
+    import numpy as np
+    import oracle
+    from mixture_experts_ffn_topk_gb300 import workloads as W
+    lib = oracle.load_library()
+    host = {kk: W.to_numpy(v) for kk, v in d.items()}
+    g_h = W.to_numpy(gy)
+    k, E = cfg.top_k, cfg.E
+
+    def run(tokens):
+        lg = host["logits"][tokens]
+        x = host["x"][tokens]
+        idx, _, _ = oracle.route(lg, cfg.logits_dtype, k, cfg.renormalize, lib)
+        counts, offsets, row_of, src_of, _ = oracle.dispatch(idx, E, lib)
+        w, _ = oracle.router_weights(lg, cfg.logits_dtype, idx, "softmax", cfg.renormalize, 1.0,
+                                     "f32", lib)
+        xd = oracle.gather(x, cfg.dtype, k, src_of, tokens.size * k, lib)
+        out = oracle.experts_dispatched(xd, cfg.dtype, offsets, host["gate"], host["up"],
+                                        host["down"], lib)
+        oracle.combine(out, "f64", w, "f32", row_of, k, lib)
+        dexp, dw = oracle.combine_backward(out, "f64", w, "f32", row_of, g_h[tokens], cfg.dtype,
+                                           k, lib)
+        dxd = oracle.experts_backward_dispatched(xd, cfg.dtype, offsets, host["gate"], host["up"],
+                                                 host["down"], dexp, "f64", lib)[0]
+        oracle.dispatch_backward(dxd, "f64", row_of, k, lib)
+        oracle.router_backward(lg, cfg.logits_dtype, idx, dw, "f64", "softmax", cfg.renormalize,
+                               1.0, "f64", lib)
+    rng = np.random.default_rng(cfg.seed)
+    t0 = time.perf_counter()
+    run(rng.choice(cfg.T, size=1, replace=False))
+    one = max(time.perf_counter() - t0, 1e-3)
+    n = int(max(1, min(cfg.T, seconds / one)))
+    tokens = rng.choice(cfg.T, size=n, replace=False)
+    t0 = time.perf_counter()
+    run(tokens)
+    wall = time.perf_counter() - t0
+    return {"value": n / wall, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} of {cfg.T} tokens of {cfg.name} as one training batch "
+                      f"(forward, combine/expert/dispatch/router backward) in {wall:.1f} s"}
 
 
 def routing_config(cfg):
