@@ -390,8 +390,12 @@ def run_ours(args, rank, world, local, dist):
 
 # Training step workloads: a forward that keeps the backward's cache, then
 # the four backward steps of ruDNN section 12, on a forward workload's shapes.
-TRAINING_WORKLOADS = {"train_fine_prefill_bf16": "fine_prefill_bf16",
-                      "train_coarse_prefill_bf16": "coarse_prefill_bf16"}
+# name -> (forward workload, overrides); the half case keeps the fine prefill's
+# rows per expert (T*k/E = 384) at half the tokens and experts, small enough
+# for full profiler captures of the backward kernels
+TRAINING_WORKLOADS = {"train_fine_prefill_bf16": ("fine_prefill_bf16", {}),
+                      "train_coarse_prefill_bf16": ("coarse_prefill_bf16", {}),
+                      "train_fine_prefill_half_bf16": ("fine_prefill_bf16", {"T": 2048, "E": 32})}
 
 
 def run_training(args, rank, world, local, dist, dev, peaks, flush):
@@ -401,8 +405,8 @@ def run_training(args, rank, world, local, dist, dev, peaks, flush):
     an N(0,1) output gradient. Inputs and weights resident in HBM."""
     import mixture_experts_ffn_topk_gb300 as moe
     from mixture_experts_ffn_topk_gb300 import workloads as W
-    base = W.CONFIGS[TRAINING_WORKLOADS[args.workload]]
-    cfg = base
+    base_name, overrides = TRAINING_WORKLOADS[args.workload]
+    cfg = W.CONFIGS[base_name].scaled(**overrides) if overrides else W.CONFIGS[base_name]
     d = W.moe_inputs(cfg, device=dev, seed=cfg.seed + 1000 * rank)
     gy = W.training_grad(cfg, device=dev, seed=cfg.seed + 1000 * rank)
     T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.top_k

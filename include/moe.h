@@ -540,7 +540,10 @@ int moe_experts_forward_training(const void *x_disp, const int32_t *offsets, int
  *   grad_x_disp  [rows, H] in dtype, written (rows < offsets[E]).
  *   grad_gate, grad_up [E, I, H] FP32, grad_down [E, H, I] FP32, written in
  *                full (experts without rows get zeros).
- *   workspace    moe_experts_backward_workspace_size(...) bytes.
+ *   workspace    moe_experts_backward_workspace_size(...) bytes, 256-byte
+ *                aligned: dg | du [rows, 2I] in dtype and, for BF16 / F16,
+ *                per-expert TMA descriptors of the weight-gradient GEMMs
+ *                (so it is needed even when rows == 0).
  *
  * Per row of expert e (s = sigmoid(g)): dh = do Wd[e],
  * dg = dh * u * s * (1 + g (1 - s)), du = dh * g * s, dx = dg Wg[e] + du Wu[e];

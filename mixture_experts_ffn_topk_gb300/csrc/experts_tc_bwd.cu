@@ -17,8 +17,7 @@
 // One persistent, warp-specialised kernel per step (one CTA per SM):
 //   warp 0     TMA producer, 4 stages of 48 KiB (A 128 x 64, B 256 x 64);
 //   warp 1     tcgen05.mma issuer, M=128 N=256 K=16, two TMEM accumulators;
-//   warps 2-5  epilogue (tcgen05.ld, math, swizzled staging, line stores);
-//   warp 6     (WG only) tail fixer, see below.
+//   warps 2-5  epilogue (tcgen05.ld, math, swizzled staging, line stores).
 // Operand layouts: the activation rows of DH and DX are K-major (rows of the
 // dispatched matrices, as in the forward). The weights read across their rows
 // (Wd as [H][I] for dh, Wg/Wu as [I][H] for dx) and both WG operands (columns
@@ -26,12 +25,13 @@
 // 64 M/N elements (128 bytes) by 64 k-rows with 128-byte swizzle, described
 // to the MMA with MN-major shared-memory descriptors (64-element groups 8 KiB
 // apart) and the transpose bits of the instruction descriptor.
-// WG reduces over an expert's row segment, which starts and ends anywhere:
-// the last 64-row block of a segment also holds rows of the next expert. The
-// producer lands that block on a separate barrier; the fixer warp zeroes the
-// rows past the segment in every box of the stage, makes the writes visible
-// to the tensor core (fence.proxy.async) and only then releases the stage to
-// the MMA. (Zeroing both operands keeps a NaN row of another expert out.)
+// WG reduces over an expert's row segment, which starts and ends anywhere, so
+// a 64-row block of the whole matrix would mix experts. Instead every expert
+// gets its own tensor maps: a small kernel copies each operand's map into the
+// workspace once per expert and rewrites its base address (the segment's first
+// row) and row count (the segment's length) with tensormap.replace; the TMA
+// then zero-fills the rows past the segment by itself, and a NaN row of
+// another expert never enters a sum.
 //
 // Every wait is bounded (kWaitLimitNs); on expiry the kernel sets ST_TIMEOUT,
 // stops issuing work, drains its own copies and MMAs, frees TMEM and exits.
@@ -59,12 +59,11 @@ constexpr int ACC_COLS = 256;
 constexpr int TMEM_COLS = 2 * ACC_COLS;
 constexpr int MAX_E = 1024;
 constexpr int EPI_ROW_BYTES = 128;
+constexpr int THREADS = 192;
+constexpr int MAP_BYTES = 128;            // one CUtensorMap
 constexpr uint64_t kDrainLimitNs = 100000000ull;
 
 enum Mode : int { kDH = 0, kDX = 1, kWG = 2 };
-
-template <int MODE>
-__host__ __device__ constexpr int threads_of() { return MODE == kWG ? 224 : 192; }
 
 struct __align__(1024) BwdSmem {
     uint8_t stage[STAGES][STAGE_BYTES];
@@ -73,8 +72,6 @@ struct __align__(1024) BwdSmem {
     uint64_t empty[STAGES];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
-    uint64_t tail_full[2];
-    uint64_t tail_empty[2];
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -95,13 +92,10 @@ struct BwdParams {
     uint8_t *out0, *out1;               // DH: dgu; DX: dx; WG: W of problem 0 / 1
     int64_t out_row_bytes;              // bytes per output row
     int64_t du_col_bytes;               // DH: byte offset of du inside a dgu row
+    const uint8_t *emaps;               // WG: per-expert tensor maps, maps_per_expert each
+    int maps_per_expert;                // WG: nprob A maps, then the B map
     unsigned *status;
 };
-
-__device__ __forceinline__ void fence_proxy_async_smem()
-{
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 
 // Tile id -> (expert, m, n, problem). DH / DX: m-tiles of an expert's rows,
 // m fastest (weight tiles shared through L2). WG: expert slowest, then
@@ -141,12 +135,6 @@ __device__ __forceinline__ int k_blocks(const BwdSmem &S, const BwdParams &p, in
     else return (S.offs[e + 1] - S.offs[e] + BK - 1) / BK;
 }
 
-// Rows of the last k-block that belong to the segment (WG), 0 if it is full.
-__device__ __forceinline__ int tail_rows(const BwdSmem &S, int e)
-{
-    return (S.offs[e + 1] - S.offs[e]) % BK;
-}
-
 // Writes 32 rows x 128 bytes (this lane's row in v[]) through the warp's
 // swizzled staging buffer so that each store instruction covers four whole
 // 128-byte row segments. Row rr goes to base + rr * row_bytes + col_byte when
@@ -173,8 +161,51 @@ __device__ __forceinline__ void emit_rows(uint8_t *stg, const uint32_t (&v)[32],
     __syncwarp();
 }
 
+// Orders this thread's later TMA copies through a tensor map in global
+// memory after the tensormap.replace writes that produced it.
+__device__ __forceinline__ void tensormap_acquire(const void *map)
+{
+    asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
+}
+
+// Per-expert tensor maps for the weight-gradient GEMMs: for expert e and map
+// j, a copy of base[j] whose base address is the expert's first row and whose
+// row count is the expert's (at least 1), at out + (e * nmaps + j) * 128.
+// One warp per expert; lanes 8j..8j+7 copy map j, lane j rewrites it.
+__global__ void __launch_bounds__(32)
+expert_maps_kernel(const __grid_constant__ CUtensorMap base0, const __grid_constant__ CUtensorMap base1,
+                   const __grid_constant__ CUtensorMap base2, uint64_t addr0, uint64_t addr1,
+                   uint64_t addr2, int64_t stride0, int64_t stride1, int64_t stride2, int nmaps,
+                   const int32_t *__restrict__ offsets, uint8_t *__restrict__ out)
+{
+    pdl_wait();
+    const int e = blockIdx.x, lane = threadIdx.x;
+    const int r0 = offsets[e], rows = offsets[e + 1] - r0;
+    uint8_t *slot = out + (size_t)e * nmaps * MAP_BYTES;
+    if (lane < 8 * nmaps) {
+        const int j = lane >> 3, c = lane & 7;
+        const CUtensorMap *src = j == 0 ? &base0 : j == 1 ? &base1 : &base2;
+        reinterpret_cast<uint4 *>(slot + j * MAP_BYTES)[c] =
+            reinterpret_cast<const uint4 *>(src)[c];
+    }
+    __syncwarp();
+    if (lane < nmaps) {
+        const uint64_t a = lane == 0 ? addr0 : lane == 1 ? addr1 : addr2;
+        const int64_t st = lane == 0 ? stride0 : lane == 1 ? stride1 : stride2;
+        uint8_t *map = slot + lane * MAP_BYTES;
+        const uint64_t first = a + (uint64_t)((int64_t)r0 * st);
+        const uint32_t n = (uint32_t)(rows > 0 ? rows : 1);
+        asm volatile("tensormap.replace.tile.global_address.global.b1024.b64 [%0], %1;"
+                     ::"l"(map), "l"(first) : "memory");
+        asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 1, %1;"
+                     ::"l"(map), "r"(n) : "memory");
+        asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+    }
+    pdl_launch_dependents();
+}
+
 template <int DT, int MODE>
-__global__ void __launch_bounds__(threads_of<MODE>(), 1)
+__global__ void __launch_bounds__(THREADS, 1)
 bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                 const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                 const BwdParams p)
@@ -190,8 +221,6 @@ bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant_
         for (int a = 0; a < 2; ++a) {
             mbar_init(&S.acc_full[a], 1);
             mbar_init(&S.acc_empty[a], 4);
-            mbar_init(&S.tail_full[a], 1);
-            mbar_init(&S.tail_empty[a], 1);
         }
         mbar_init(&S.drain, 1);
         S.abort = 0;
@@ -203,7 +232,7 @@ bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant_
     }
     pdl_wait();
     pdl_launch_dependents();
-    for (int i = threadIdx.x; i <= p.E; i += threads_of<MODE>()) S.offs[i] = p.offsets[i];
+    for (int i = threadIdx.x; i <= p.E; i += THREADS) S.offs[i] = p.offsets[i];
     __syncthreads();
     if (MODE != kWG && warp == 0) {
         // prefix[e] = tiles of experts < e (lane l owns a contiguous run)
@@ -233,27 +262,30 @@ bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant_
                                         : S.prefix[p.E];
     volatile int *abort_flag = &S.abort;
     uint32_t filled_mask = 0, filled_parity = 0;       // producer: stages in flight
-    uint32_t tail_mask = 0, tail_parity = 0;           // producer: tail copies in flight
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------------ TMA producer
-        int stage = 0, tb = 0;
-        uint32_t phase = 0, tphase = 0;
+        int stage = 0;
+        uint32_t phase = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
             int e, m, n, prob;
             decode<MODE>(S, p, tile, e, m, n, prob);
             const int nkb = k_blocks<MODE>(S, p, e);
-            const int tail = MODE == kWG ? tail_rows(S, e) : 0;
             const int seg0 = S.offs[e];
+            const CUtensorMap *wa = nullptr, *wb = nullptr;
+            if constexpr (MODE == kWG) {
+                const uint8_t *maps = p.emaps + (size_t)e * p.maps_per_expert * MAP_BYTES;
+                wa = reinterpret_cast<const CUtensorMap *>(maps + prob * MAP_BYTES);
+                wb = reinterpret_cast<const CUtensorMap *>(maps + (p.maps_per_expert - 1) * MAP_BYTES);
+                if (nkb > 0) {
+                    tensormap_acquire(wa);
+                    tensormap_acquire(wb);
+                }
+            }
             for (int kb = 0; kb < nkb; ++kb) {
                 if (!mbar_wait(&S.empty[stage], phase ^ 1u, abort_flag, status, kWaitLimitNs)) { ok = false; break; }
-                const bool is_tail = MODE == kWG && tail != 0 && kb == nkb - 1;
                 uint64_t *bar = &S.full[stage];
-                if (is_tail) {
-                    if (!mbar_wait(&S.tail_empty[tb], tphase ^ 1u, abort_flag, status, kWaitLimitNs)) { ok = false; break; }
-                    bar = &S.tail_full[tb];
-                }
                 uint8_t *sa = S.stage[stage];
                 uint8_t *sb = sa + A_BYTES;
                 mbar_arrive_expect_tx(bar, STAGE_BYTES);
@@ -273,22 +305,17 @@ bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant_
                     for (int j = 0; j < 4; ++j)
                         tma_load_3d(sb + j * BOX_BYTES, second ? &tmB1 : &tmB0, bar, n * BN + j * BOX, kk, e);
                 } else {
-                    const int r0 = seg0 + kb * BK;
+                    // rows relative to the expert's own maps: past its last row
+                    // the TMA fills zeros
 #pragma unroll
                     for (int j = 0; j < 2; ++j)
-                        tma_load_2d(sa + j * BOX_BYTES, prob ? &tmA1 : &tmA0, bar, m * BM + j * BOX, r0);
+                        tma_load_2d(sa + j * BOX_BYTES, wa, bar, m * BM + j * BOX, kb * BK);
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
-                        tma_load_2d(sb + j * BOX_BYTES, &tmB0, bar, n * BN + j * BOX, r0);
+                        tma_load_2d(sb + j * BOX_BYTES, wb, bar, n * BN + j * BOX, kb * BK);
                 }
-                if (is_tail) {
-                    tail_mask |= 1u << tb;
-                    tail_parity = (tail_parity & ~(1u << tb)) | (tphase << tb);
-                    if (++tb == 2) { tb = 0; tphase ^= 1u; }
-                } else {
-                    filled_mask |= 1u << stage;
-                    filled_parity = (filled_parity & ~(1u << stage)) | (phase << stage);
-                }
+                filled_mask |= 1u << stage;
+                filled_parity = (filled_parity & ~(1u << stage)) | (phase << stage);
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
         }
@@ -323,50 +350,16 @@ bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant_
                 umma_commit<1>(&S.empty[stage]);
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
+            // (an expert without rows commits with no MMA: its epilogue writes zeros)
             if (ok) umma_commit<1>(&S.acc_full[acc]);
         }
         if (*abort_flag) {
             umma_commit<1>(&S.drain);
             mbar_wait(&S.drain, 0, nullptr, status, kDrainLimitNs);
         }
-    } else if (MODE == kWG && warp == 6) {
-        // ------------------------------------------------------ tail fixer
-        int stage = 0, tb = 0;
-        uint32_t tphase = 0;
-        bool ok = true;
-        for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-            int e, m, n, prob;
-            decode<MODE>(S, p, tile, e, m, n, prob);
-            const int nkb = k_blocks<MODE>(S, p, e);
-            const int tail = tail_rows(S, e);
-            for (int kb = 0; kb < nkb; ++kb) {
-                if (tail != 0 && kb == nkb - 1) {
-                    const bool ready = mbar_wait(&S.tail_full[tb], tphase, abort_flag, status, kWaitLimitNs);
-                    if (!__all_sync(0xffffffffu, ready)) { ok = false; break; }
-                    // rows [tail, 64) of the six 64-row boxes (2 of A, 4 of B)
-                    const int zrows = BK - tail;
-                    const int per_box = zrows * (EPI_ROW_BYTES / 16);
-                    uint8_t *base = S.stage[stage];
-                    for (int i = lane; i < 6 * per_box; i += 32) {
-                        const int box = i / per_box, rem = i - box * per_box;
-                        const int row = tail + rem / 8, chunk = rem % 8;
-                        *reinterpret_cast<uint4 *>(base + box * BOX_BYTES + row * 128 + chunk * 16) =
-                            make_uint4(0u, 0u, 0u, 0u);
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        mbar_arrive(&S.full[stage]);
-                        mbar_arrive(&S.tail_empty[tb]);
-                    }
-                    if (++tb == 2) { tb = 0; tphase ^= 1u; }
-                }
-                if (++stage == STAGES) stage = 0;
-            }
-        }
-    } else if (warp >= 2 && warp < 6) {
+    } else if (warp >= 2) {
         // ------------------------------------------------------ epilogue
-        const int q = warp & 3;                    // TMEM lane quadrant
+        const int q = warp & 3;                    // TMEM lane quadrant (fixed by the warp id)
         uint8_t *stg = S.epi[warp - 2];
         int it = 0;
         for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++it) {
@@ -379,23 +372,34 @@ bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant_
             tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
             if constexpr (MODE == kWG) {
-                // rows: weight rows m*128 + q*32 + r; FP32, 32 columns per round
+                // rows: weight rows m*128 + q*32 + r; FP32, 32 columns per round;
+                // the next round's tensor-memory load is in flight while the
+                // current one is stored
                 const int row0 = m * BM + q * 32;
                 const int rows_valid = p.M - row0;
                 const bool empty_expert = S.offs[e + 1] == S.offs[e];
                 uint8_t *W = (prob ? p.out1 : p.out0) + ((int64_t)e * p.M + row0) * p.out_row_bytes;
-#pragma unroll 1
-                for (int rd = 0; rd < BN / 32; ++rd) {
-                    uint32_t v[32];
-                    if (empty_expert) {
+                constexpr int CHUNKS = BN / 32;
+                uint32_t v[32];
+                if (empty_expert) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = 0u;
-                    } else {
-                        tmem_ld32(tbase + rd * 32, v);
-                        tmem_ld_wait(v);
-                    }
+                    for (int i = 0; i < 32; ++i) v[i] = 0u;
+                } else {
+                    tmem_ld32(tbase, v);
+                    tmem_ld_wait(v);
+                }
+#pragma unroll 2
+                for (int rd = 0; rd < CHUNKS; ++rd) {
+                    uint32_t vn[32];
+                    const bool more = rd + 1 < CHUNKS && !empty_expert;
+                    if (more) tmem_ld32(tbase + (rd + 1) * 32, vn);
                     emit_rows(stg, v, W, p.out_row_bytes, (int64_t)(n * BN + rd * 32) * 4,
                               p.out_row_bytes, rows_valid);
+                    if (more) {
+                        tmem_ld_wait(vn);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = vn[i];
+                    }
                 }
             } else {
                 const int seg_rows = S.offs[e + 1] - S.offs[e];
@@ -476,9 +480,6 @@ bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant_
         for (int s = 0; s < STAGES; ++s)
             if (filled_mask >> s & 1u)
                 mbar_wait(&S.full[s], filled_parity >> s & 1u, nullptr, status, kDrainLimitNs);
-        for (int t = 0; t < 2; ++t)
-            if (tail_mask >> t & 1u)
-                mbar_wait(&S.tail_full[t], tail_parity >> t & 1u, nullptr, status, kDrainLimitNs);
     }
     __syncthreads();
     if (warp == 1) {
@@ -508,7 +509,7 @@ cudaError_t launch_step(int64_t units, const CUtensorMap &a0, const CUtensorMap 
     }
     const int64_t sms = device_sm_count();
     const int grid = (int)(units < sms ? (units < 1 ? 1 : units) : sms);
-    return launch_pdl(bwd_gemm_kernel<DT, MODE>, dim3((unsigned)grid), dim3(threads_of<MODE>()),
+    return launch_pdl(bwd_gemm_kernel<DT, MODE>, dim3((unsigned)grid), dim3(THREADS),
                       kBwdSmemBytes, s, a0, a1, b0, b1, p);
 }
 
@@ -516,15 +517,16 @@ template <int DT>
 cudaError_t launch_backward(const void *x_disp, const int32_t *offsets, int64_t rows,
                             const void *gate, const void *up, const void *down, int E, int64_t H,
                             int64_t I, const void *cache, const void *dout, void *dgu, void *dx,
-                            float *dgate, float *dup, float *ddown, unsigned *status,
-                            cudaStream_t s)
+                            float *dgate, float *dup, float *ddown, void *maps_ws,
+                            unsigned *status, cudaStream_t s)
 {
     const CUtensorMapDataType tdt =
         DT == DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const uint64_t R = (uint64_t)(rows > 0 ? rows : 1);
     if (rows == 0) {
         // no activation rows: only the zero weight gradients are written and no
-        // tensor map below is ever read; gate stands in for the absent pointers
+        // activation tensor map below is ever read; gate stands in for the
+        // absent pointers
         dout = cache = x_disp = gate;
         dgu = const_cast<void *>(gate);
     }
@@ -533,7 +535,8 @@ cudaError_t launch_backward(const void *x_disp, const int32_t *offsets, int64_t 
     const uint8_t *dgu_b = static_cast<const uint8_t *>(dgu);
     // DH: dout rows (K-major) x Wd[e] read as [H][I] (MN-major)
     // DX: dg / du column views of dgu (K-major) x Wg[e], Wu[e] read as [I][H]
-    // WG: columns of do / dg / du (MN-major) x columns of h / x (MN-major)
+    // WG: columns of do / dg / du (MN-major) x columns of h / x (MN-major),
+    //     per expert (the maps below are the templates the expert maps copy)
     CUtensorMap dh_a, dh_b, dx_a0, dx_a1, dx_b0, dx_b1, wd_a, wd_b, wgu_a0, wgu_a1, wgu_b;
     if (!encode_2d(&dh_a, tdt, dout, (uint64_t)H, R, BK, BM) ||
         !encode_3d(&dh_b, tdt, down, (uint64_t)I, (uint64_t)H, (uint64_t)E, BOX, BK) ||
@@ -548,11 +551,25 @@ cudaError_t launch_backward(const void *x_disp, const int32_t *offsets, int64_t 
         !encode_2d(&wgu_b, tdt, x_disp, (uint64_t)H, R, BOX, BK))
         return cudaErrorInvalidValue;
 
+    // per-expert maps: [E][2] for dWd (do, h), then [E][3] for dWg / dWu (dg, du, x)
+    uint8_t *maps_d = static_cast<uint8_t *>(maps_ws);
+    uint8_t *maps_gu = maps_d + (size_t)E * 2 * MAP_BYTES;
+    const uint64_t a_dout = reinterpret_cast<uint64_t>(dout), a_h = reinterpret_cast<uint64_t>(cb);
+    const uint64_t a_dg = reinterpret_cast<uint64_t>(dgu_b), a_du = a_dg + 2 * I;
+    const uint64_t a_x = reinterpret_cast<uint64_t>(x_disp);
+    cudaError_t err = launch_pdl(expert_maps_kernel, dim3((unsigned)E), dim3(32), 0, s, wd_a, wd_b,
+                                 wd_b, a_dout, a_h, a_h, (int64_t)(2 * H), (int64_t)(2 * I),
+                                 (int64_t)(2 * I), 2, offsets, maps_d);
+    if (err != cudaSuccess) return err;
+    err = launch_pdl(expert_maps_kernel, dim3((unsigned)E), dim3(32), 0, s, wgu_a0, wgu_a1, wgu_b,
+                     a_dg, a_du, a_x, (int64_t)(4 * I), (int64_t)(4 * I), (int64_t)(2 * H), 3,
+                     offsets, maps_gu);
+    if (err != cudaSuccess) return err;
+
     BwdParams p{};
     p.offsets = offsets;
     p.E = E;
     p.status = status;
-    cudaError_t err;
     if (rows > 0) {
         const int64_t mt = rows / BM + (rows < E ? rows : E);     // M-tiles, upper bound
         // DH: dh, then dg / du into dgu
@@ -583,6 +600,8 @@ cudaError_t launch_backward(const void *x_disp, const int32_t *offsets, int64_t 
     p.out0 = reinterpret_cast<uint8_t *>(ddown);
     p.out1 = nullptr;
     p.out_row_bytes = 4 * I;
+    p.emaps = maps_d;
+    p.maps_per_expert = 2;
     err = launch_step<DT, kWG>((int64_t)E * ((H + BM - 1) / BM) * p.n_tiles, wd_a, wd_a, wd_b,
                                wd_b, p, s);
     if (err != cudaSuccess) return err;
@@ -594,24 +613,28 @@ cudaError_t launch_backward(const void *x_disp, const int32_t *offsets, int64_t 
     p.out0 = reinterpret_cast<uint8_t *>(dgate);
     p.out1 = reinterpret_cast<uint8_t *>(dup);
     p.out_row_bytes = 4 * H;
+    p.emaps = maps_gu;
+    p.maps_per_expert = 3;
     return launch_step<DT, kWG>(2 * (int64_t)E * ((I + BM - 1) / BM) * p.n_tiles, wgu_a0, wgu_a1,
                                 wgu_b, wgu_b, p, s);
 }
 
 }  // namespace
 
+size_t experts_tc_backward_maps_bytes(int E) { return (size_t)E * 5 * MAP_BYTES; }
+
 cudaError_t launch_experts_tc_backward(int dt, const void *x_disp, const int32_t *offsets,
                                        int64_t rows, const void *gate, const void *up,
                                        const void *down, int E, int64_t H, int64_t I,
                                        const void *cache, const void *dout, void *dgu_ws,
-                                       void *dx, float *dgate, float *dup, float *ddown,
-                                       unsigned *status, cudaStream_t s)
+                                       void *maps_ws, void *dx, float *dgate, float *dup,
+                                       float *ddown, unsigned *status, cudaStream_t s)
 {
     if (dt == DT_BF16)
         return launch_backward<DT_BF16>(x_disp, offsets, rows, gate, up, down, E, H, I, cache,
-                                        dout, dgu_ws, dx, dgate, dup, ddown, status, s);
+                                        dout, dgu_ws, dx, dgate, dup, ddown, maps_ws, status, s);
     return launch_backward<DT_F16>(x_disp, offsets, rows, gate, up, down, E, H, I, cache, dout,
-                                   dgu_ws, dx, dgate, dup, ddown, status, s);
+                                   dgu_ws, dx, dgate, dup, ddown, maps_ws, status, s);
 }
 
 }  // namespace moe

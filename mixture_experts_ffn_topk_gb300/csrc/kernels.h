@@ -140,13 +140,16 @@ cudaError_t launch_experts_tc_training(int dt, const void *x_disp, const int32_t
                                        unsigned *status, cudaStream_t s);
 
 // Expert backward on tcgen05 (see launch_experts_simt_backward for the
-// math); dgu_ws holds [rows, 2I] of dt.
+// math); dgu_ws holds [rows, 2I] of dt, maps_ws the per-expert tensor maps of
+// the weight-gradient GEMMs (experts_tc_backward_maps_bytes(E), 128-byte
+// aligned).
+size_t experts_tc_backward_maps_bytes(int E);
 cudaError_t launch_experts_tc_backward(int dt, const void *x_disp, const int32_t *offsets,
                                        int64_t rows, const void *gate, const void *up,
                                        const void *down, int E, int64_t H, int64_t I,
                                        const void *cache, const void *dout, void *dgu_ws,
-                                       void *dx, float *dgate, float *dup, float *ddown,
-                                       unsigned *status, cudaStream_t s);
+                                       void *maps_ws, void *dx, float *dgate, float *dup,
+                                       float *ddown, unsigned *status, cudaStream_t s);
 
 // y = y_acc rounded to ydt ([T, H], H % 8 == 0).
 cudaError_t launch_finalize(const float *y_acc, int64_t T, int64_t H, void *y, int ydt,

@@ -696,13 +696,21 @@ int moe_experts_forward_training(const void *x_disp, const int32_t *offsets, int
     return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_experts_forward_training");
 }
 
+// Expert backward workspace: dgu [rows, 2I] in the expert dtype, then (BF16 /
+// F16) the per-expert tensor maps of the weight-gradient GEMMs.
+size_t backward_dgu_bytes(int64_t rows, int64_t I, int dtype)
+{
+    return round_up(2 * (size_t)(rows > 0 ? rows : 0) * (size_t)I * elem_bytes(dtype), 256);
+}
+
 size_t moe_experts_backward_workspace_size(int64_t rows, int64_t E, int64_t H, int64_t I,
                                            int dtype)
 {
-    (void)E;
     (void)H;
-    if (rows <= 0 || I <= 0 || !valid_dtype(dtype)) return 0;
-    return round_up(2 * (size_t)rows * (size_t)I * elem_bytes(dtype), 256);
+    if (rows < 0 || I <= 0 || E < 1 || E > kMaxE || !valid_dtype(dtype)) return 0;
+    size_t n = backward_dgu_bytes(rows, I, dtype);
+    if (dtype != MOE_F32) n += round_up(experts_tc_backward_maps_bytes((int)E), 256);
+    return n;
 }
 
 int moe_experts_backward(const void *x_disp, const int32_t *offsets, int64_t rows,
@@ -723,10 +731,11 @@ int moe_experts_backward(const void *x_disp, const int32_t *offsets, int64_t row
         if (rc != MOE_OK) return rc;
         if ((reinterpret_cast<uintptr_t>(cache) & 255u))
             return fail(MOE_ERR_WORKSPACE, "moe_experts_backward: cache not 256-byte aligned");
-        const size_t need = moe_experts_backward_workspace_size(rows, E, H, I, dtype);
-        if (workspace_bytes < need || !workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-            return fail(MOE_ERR_WORKSPACE, "moe_experts_backward: workspace too small or not 256-byte aligned");
     }
+    const size_t need = moe_experts_backward_workspace_size(rows, E, H, I, dtype);
+    if (need > 0 && (workspace_bytes < need || !workspace ||
+                     (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+        return fail(MOE_ERR_WORKSPACE, "moe_experts_backward: workspace too small or not 256-byte aligned");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t err;
     if (dtype == MOE_F32) {
@@ -739,9 +748,11 @@ int moe_experts_backward(const void *x_disp, const int32_t *offsets, int64_t row
     } else {
         unsigned *st = status_ptr();
         if (!st) return fail(MOE_ERR_CUDA, "cannot resolve the device status word");
+        uint8_t *ws = static_cast<uint8_t *>(workspace);
         err = launch_experts_tc_backward(dtype, x_disp, offsets, rows, gate, up, down, (int)E, H, I,
-                                         cache, grad_out, workspace, grad_x_disp, grad_gate,
-                                         grad_up, grad_down, st, s);
+                                         cache, grad_out, rows > 0 ? ws : nullptr,
+                                         ws + backward_dgu_bytes(rows, I, dtype), grad_x_disp,
+                                         grad_gate, grad_up, grad_down, st, s);
         if (err == cudaErrorInvalidValue)
             return fail(MOE_ERR_ALIGN, "TMA descriptor rejected (pointer alignment or shape)");
     }
