@@ -466,8 +466,8 @@ def run_training(args, rank, world, local, dist, dev, peaks, flush):
         if ev: ev[5].record(stream)
 
     # route 1, dispatch 4, router weights 1, experts fwd 2, combine 1,
-    # combine bwd 1, experts bwd 4, dispatch bwd 1, router bwd 1
-    launches_per_step = 16
+    # combine bwd 1, experts bwd 6 (2 map builds + 4 GEMMs), dispatch bwd 1, router bwd 1
+    launches_per_step = 18
     for _ in range(args.warmup):
         step(x, logits, gy)
         flush.fill_(1)

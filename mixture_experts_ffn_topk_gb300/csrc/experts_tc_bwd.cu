@@ -15,9 +15,14 @@
 // Inputs BF16 or F16, FP32 accumulation in tensor memory.
 //
 // One persistent, warp-specialised kernel per step (one CTA per SM):
-//   warp 0     TMA producer, 4 stages of 48 KiB (A 128 x 64, B 256 x 64);
+//   warp 0     TMA producer, stages of 48 KiB (A 128 x 64, B 256 x 64);
 //   warp 1     tcgen05.mma issuer, M=128 N=256 K=16, two TMEM accumulators;
 //   warps 2-5  epilogue (tcgen05.ld, math, swizzled staging, line stores).
+// DH's epilogue reads 256 KiB of cached FP32 g / u per tile, one row per lane;
+// with four warps those loads, not the MMA, set its pace, so DH runs eight
+// epilogue warps (two per TMEM lane quadrant, 128 columns each, 16 columns
+// per step to stay within the register file) and three stages to make room
+// for their staging buffers; DX and WG keep four stages and four warps.
 // Operand layouts: the activation rows of DH and DX are K-major (rows of the
 // dispatched matrices, as in the forward). The weights read across their rows
 // (Wd as [H][I] for dh, Wg/Wu as [I][H] for dx) and both WG operands (columns
@@ -54,20 +59,27 @@ constexpr int BOX_BYTES = BOX * BK * 2;  // 8 KiB
 constexpr int A_BYTES = BM * BK * 2;     // 16 KiB
 constexpr int B_BYTES = BN * BK * 2;     // 32 KiB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int STAGES = 4;
 constexpr int ACC_COLS = 256;
 constexpr int TMEM_COLS = 2 * ACC_COLS;
 constexpr int MAX_E = 1024;
 constexpr int EPI_ROW_BYTES = 128;
-constexpr int THREADS = 192;
 constexpr int MAP_BYTES = 128;            // one CUtensorMap
 constexpr uint64_t kDrainLimitNs = 100000000ull;
 
 enum Mode : int { kDH = 0, kDX = 1, kWG = 2 };
 
+template <int MODE>
+__host__ __device__ constexpr int stages_of() { return MODE == kDH ? 3 : 4; }
+template <int MODE>
+__host__ __device__ constexpr int epi_warps_of() { return MODE == kDH ? 8 : 4; }
+template <int MODE>
+__host__ __device__ constexpr int threads_of() { return 32 * (2 + epi_warps_of<MODE>()); }
+
+template <int MODE>
 struct __align__(1024) BwdSmem {
+    static constexpr int STAGES = stages_of<MODE>();
     uint8_t stage[STAGES][STAGE_BYTES];
-    uint8_t epi[4][32 * EPI_ROW_BYTES];
+    uint8_t epi[epi_warps_of<MODE>()][32 * EPI_ROW_BYTES];
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
     uint64_t acc_full[2];
@@ -78,7 +90,8 @@ struct __align__(1024) BwdSmem {
     int prefix[MAX_E + 1];
     int offs[MAX_E + 1];
 };
-constexpr size_t kBwdSmemBytes = sizeof(BwdSmem) + 1024;
+template <int MODE>
+constexpr size_t kBwdSmemBytes = sizeof(BwdSmem<MODE>) + 1024;
 
 struct BwdParams {
     const int32_t *offsets;
@@ -101,7 +114,7 @@ struct BwdParams {
 // m fastest (weight tiles shared through L2). WG: expert slowest, then
 // weight-row tile m, then column tile n.
 template <int MODE>
-__device__ __forceinline__ void decode(const BwdSmem &S, const BwdParams &p, int tile, int &e,
+__device__ __forceinline__ void decode(const BwdSmem<MODE> &S, const BwdParams &p, int tile, int &e,
                                        int &m, int &n, int &prob)
 {
     if constexpr (MODE == kWG) {
@@ -128,7 +141,7 @@ __device__ __forceinline__ void decode(const BwdSmem &S, const BwdParams &p, int
 }
 
 template <int MODE>
-__device__ __forceinline__ int k_blocks(const BwdSmem &S, const BwdParams &p, int e)
+__device__ __forceinline__ int k_blocks(const BwdSmem<MODE> &S, const BwdParams &p, int e)
 {
     if constexpr (MODE == kDH) return (p.num_k + BK - 1) / BK;
     else if constexpr (MODE == kDX) return 2 * ((p.num_k + BK - 1) / BK);
@@ -205,14 +218,17 @@ expert_maps_kernel(const __grid_constant__ CUtensorMap base0, const __grid_const
 }
 
 template <int DT, int MODE>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(threads_of<MODE>(), 1)
 bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                 const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                 const BwdParams p)
 {
+    constexpr int STAGES = stages_of<MODE>();
+    constexpr int EPI_WARPS = epi_warps_of<MODE>();
+    constexpr int THREADS = threads_of<MODE>();
     extern __shared__ uint8_t smem_raw[];
-    BwdSmem &S = *reinterpret_cast<BwdSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                              ~uintptr_t(1023));
+    BwdSmem<MODE> &S = *reinterpret_cast<BwdSmem<MODE> *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     unsigned *status = p.status;
 
@@ -220,7 +236,7 @@ bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant_
         for (int s = 0; s < STAGES; ++s) { mbar_init(&S.full[s], 1); mbar_init(&S.empty[s], 1); }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&S.acc_full[a], 1);
-            mbar_init(&S.acc_empty[a], 4);
+            mbar_init(&S.acc_empty[a], EPI_WARPS);
         }
         mbar_init(&S.drain, 1);
         S.abort = 0;
@@ -360,6 +376,7 @@ bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant_
     } else if (warp >= 2) {
         // ------------------------------------------------------ epilogue
         const int q = warp & 3;                    // TMEM lane quadrant (fixed by the warp id)
+        static_assert(MODE == kDH || EPI_WARPS == 4, "only DH splits columns over two warps");
         uint8_t *stg = S.epi[warp - 2];
         int it = 0;
         for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++it) {
@@ -425,18 +442,22 @@ bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant_
                         emit_rows(stg, v0, ob, p.out_row_bytes, (int64_t)(n * BN + rd * 64) * 2,
                                   col_limit, rows_valid);
                     } else {
+                        // this warp: 128 of the tile's 256 columns, 64 per round, 16 per step
+                        const int col_half = (warp - 2) >> 2;
+                        if (rd >= 2) break;
+                        const int cbase = col_half * 128 + rd * 64;        // column in the tile
                         uint32_t v1[32];
                         const bool row_ok = lane < rows_valid;
                         const int64_t grow = grow0 + lane;
 #pragma unroll
-                        for (int half = 0; half < 2; ++half) {
-                            const int col0 = n * BN + (rd * 2 + half) * 32;
-                            uint32_t d[32];
-                            tmem_ld32(tbase + (rd * 2 + half) * 32, d);
-                            // the cached FP32 g and u of these 32 columns of this lane's row
-                            float4 gv[8], uv[8];
+                        for (int qd = 0; qd < 4; ++qd) {
+                            const int col0 = n * BN + cbase + qd * 16;
+                            uint32_t d[16];
+                            tmem_ld16(tbase + cbase + qd * 16, d);
+                            // the cached FP32 g and u of these 16 columns of this lane's row
+                            float4 gv[4], uv[4];
 #pragma unroll
-                            for (int c = 0; c < 8; ++c) {
+                            for (int c = 0; c < 4; ++c) {
                                 if (row_ok && col0 + 4 * c < p.N) {
                                     const int64_t off = grow * p.N + col0 + 4 * c;
                                     gv[c] = *reinterpret_cast<const float4 *>(p.g_plane + off);
@@ -446,9 +467,9 @@ bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant_
                                     uv[c] = make_float4(0.f, 0.f, 0.f, 0.f);
                                 }
                             }
-                            tmem_ld_wait(d);
+                            tmem_ld_wait16(d);
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) {
+                            for (int i = 0; i < 8; ++i) {
                                 const float4 g4 = gv[i / 2], u4 = uv[i / 2];
                                 const float2 g = (i & 1) ? make_float2(g4.z, g4.w) : make_float2(g4.x, g4.y);
                                 const float2 u = (i & 1) ? make_float2(u4.z, u4.w) : make_float2(u4.x, u4.y);
@@ -456,12 +477,12 @@ bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant_
                                 const float dh1 = __uint_as_float(d[2 * i + 1]);
                                 const float s0 = 1.0f / (1.0f + __expf(-g.x));
                                 const float s1 = 1.0f / (1.0f + __expf(-g.y));
-                                v0[half * 16 + i] = pack2<DT>(dh0 * u.x * s0 * (1.0f + g.x * (1.0f - s0)),
-                                                              dh1 * u.y * s1 * (1.0f + g.y * (1.0f - s1)));
-                                v1[half * 16 + i] = pack2<DT>(dh0 * g.x * s0, dh1 * g.y * s1);
+                                v0[qd * 8 + i] = pack2<DT>(dh0 * u.x * s0 * (1.0f + g.x * (1.0f - s0)),
+                                                           dh1 * u.y * s1 * (1.0f + g.y * (1.0f - s1)));
+                                v1[qd * 8 + i] = pack2<DT>(dh0 * g.x * s0, dh1 * g.y * s1);
                             }
                         }
-                        const int64_t cb = (int64_t)(n * BN + rd * 64) * 2;
+                        const int64_t cb = (int64_t)(n * BN + cbase) * 2;
                         emit_rows(stg, v0, ob, p.out_row_bytes, cb, col_limit, rows_valid);
                         emit_rows(stg, v1, ob + p.du_col_bytes, p.out_row_bytes, cb, col_limit,
                                   rows_valid);
@@ -503,14 +524,15 @@ cudaError_t launch_step(int64_t units, const CUtensorMap &a0, const CUtensorMap 
     const uint64_t bit = 1ull << (dev & 63);
     if (!(done_mask.load() & bit)) {
         err = cudaFuncSetAttribute(bwd_gemm_kernel<DT, MODE>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBwdSmemBytes);
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)kBwdSmemBytes<MODE>);
         if (err != cudaSuccess) return err;
         done_mask.fetch_or(bit);
     }
     const int64_t sms = device_sm_count();
     const int grid = (int)(units < sms ? (units < 1 ? 1 : units) : sms);
-    return launch_pdl(bwd_gemm_kernel<DT, MODE>, dim3((unsigned)grid), dim3(THREADS),
-                      kBwdSmemBytes, s, a0, a1, b0, b1, p);
+    return launch_pdl(bwd_gemm_kernel<DT, MODE>, dim3((unsigned)grid), dim3(threads_of<MODE>()),
+                      kBwdSmemBytes<MODE>, s, a0, a1, b0, b1, p);
 }
 
 template <int DT>
