@@ -202,6 +202,11 @@ EXPERT_CASES = [
     ("single_expert_f16", 150, 192, 128, 1, 1, torch.float16, 0.0),
     ("ragged_f32", 200, 192, 136, 5, 2, torch.float32, 0.0),
     ("empty_experts_f16", 40, 256, 512, 32, 2, torch.float16, 2.0),
+    # at least 2 x 128 rows per expert: dh and dx run on CTA pairs too; skewed
+    # counts leave a pair's second M-tile past an expert's rows; H = I = 200
+    # leave K and N tails
+    ("pair_skewed_bf16", 900, 200, 200, 3, 1, torch.bfloat16, 1.0),
+    ("pair_f16", 640, 384, 320, 4, 2, torch.float16, 0.0),
 ]
 
 
