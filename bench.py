@@ -213,6 +213,8 @@ def run_ours(args, rank, world, local, dist):
 
     if args.workload == W.COMBINE_NORM.name:
         return run_combine_norm(args, rank, world, local, dist, dev, peaks, flush)
+    if args.workload == W.COMBINE_V2.name:
+        return run_combine_v2(args, rank, world, dist, dev, peaks, flush)
     if args.workload == "routing_sweep":
         return run_routing_sweep(args, world, dist, dev, peaks, flush)
     if args.workload in TRAINING_WORKLOADS:
@@ -750,6 +752,66 @@ def run_combine_norm(args, rank, world, local, dist, dev, peaks, flush):
                          "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
                          "peak_source": peaks["source"],
                          "traffic": load_traffic(cfg.name, "combine_add_rmsnorm")},
+            "gpu_launches": args.steps, "clocks": clk.summary()}
+
+
+def run_combine_v2(args, rank, world, dist, dev, peaks, flush):
+    """The local math of the Ascend V2 combine: special experts (zero, copy,
+    const), the shared-expert term, a 2-D active mask, then Add + RMSNorm,
+    on the combine + norm workload's shapes."""
+    import numpy as np
+    import mixture_experts_ffn_topk_gb300 as moe
+    from mixture_experts_ffn_topk_gb300 import workloads as W
+    cfg = W.COMBINE_V2
+    d = W.combine_v2_inputs(cfg, device=dev, seed=cfg.seed + 1000 * rank)
+    T, H, k, E = cfg.T, cfg.H, cfg.top_k, cfg.E
+    special = cfg.zero + cfg.copy + cfg.const
+    idx, w = moe.moe_route(d["logits"], k, True)
+    disp = moe.moe_dispatch_special(idx, torch.zeros((T, 8), dtype=torch.bfloat16, device=dev),
+                                    E, special)
+    row_of = disp["row_of"]
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    xo = torch.empty_like(y)
+    rstd = torch.empty(T, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    mask = d["mask"].to(torch.uint8)      # the C ABI takes bytes; no conversion per call
+
+    def fn():
+        moe.moe_combine_v2(d["out_disp"], w, row_of, torch.bfloat16, expert_indices=idx,
+                           num_experts=E, zero_experts=cfg.zero, copy_experts=cfg.copy,
+                           const_experts=cfg.const, ori_x=d["ori_x"], const_alpha1=d["alpha1"],
+                           const_alpha2=d["alpha2"], const_v=d["const_v"],
+                           shared_expert_x=d["shared_x"], active_mask=mask,
+                           residual=d["residual"], gamma=d["gamma"], eps=cfg.eps, y=y,
+                           x_out=xo, rstd=rstd)
+    with ClockSampler(dev) as clk:
+        ms = timed_loop(fn, args, stream, flush)
+    ms_max = reduce_max(dist, ms, dev)
+    if moe.moe_device_status() != 0:
+        raise RuntimeError("device status error in the timed region")
+    # algorithmic bytes: the rows of routed, kept slots; ori_x for tokens with
+    # a kept copy / const slot; per-slot ids, weights, maps and mask bytes;
+    # shared_x, residual, gamma; y, x_out and rstd written
+    ids = idx.cpu().numpy().astype(np.int64)
+    keep = mask.cpu().numpy()
+    routed_rows = int(((ids < E) & keep).sum())
+    needs_ori = ((ids >= E + cfg.zero) & (ids < E + special) & keep).any(axis=1).sum()
+    nbytes = (routed_rows * H * 2 + int(needs_ori) * H * 2 + T * k * (4 + 4 + 4 + 1)
+              + T * H * 2 * 2 + H * 2 + cfg.const * (H + 2) * 2 + 2 * T * H * 2 + T * 4)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"metric": METRIC, "value": aggregate(ms_max / 1e3, T, world), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded)",
+            "config": {"workload": cfg.name, "T": T, "H": H, "E": E, "top_k": k,
+                       "zero_experts": cfg.zero, "copy_experts": cfg.copy,
+                       "const_experts": cfg.const, "active_mask": f"2-D, keep {cfg.keep}",
+                       "shared_expert": True, "norm": "Add + RMSNorm",
+                       "l2": "flushed between steps (256 MiB write)"},
+            "roofline": {"bound": "hbm", "kernel": "combine (V2 extras) + Add + RMSNorm",
+                         "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "peak_source": peaks["source"],
+                         "algorithmic_bytes": nbytes, "traffic": None},
             "gpu_launches": args.steps, "clocks": clk.summary()}
 
 

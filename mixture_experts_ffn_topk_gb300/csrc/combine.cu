@@ -92,7 +92,7 @@ __device__ __forceinline__ void load8_rt(const void *base, int dt, int64_t g, fl
 }
 
 // Sources of a slot other than a dispatched expert row (see the header).
-enum SlotKind : int { kRouted = 0, kZero = 1, kCopy = 2, kConst = 3, kBad = 4 };
+enum SlotKind : int { kRouted = 0, kZero = 1, kCopy = 2, kConst = 3, kBad = 4, kSkip = 5 };
 
 template <int ODT, int YDT, int V, bool NORM, bool EXTRAS>
 __global__ void __launch_bounds__(kMaxThreads)
@@ -105,6 +105,10 @@ combine_kernel(const void *__restrict__ out_disp, const void *__restrict__ w, in
     const int64_t ng = H / 8;
     __shared__ float red[kMaxThreads / 32];
     __shared__ float s_rstd;
+    // EXTRAS: one chunk of classified slots (kind, weight, row offset or const index)
+    __shared__ int s_kind[EXTRAS ? kMaxThreads : 1];
+    __shared__ float s_w[EXTRAS ? kMaxThreads : 1];
+    __shared__ int64_t s_off[EXTRAS ? kMaxThreads : 1];
     const int64_t elem_o = ODT == DT_F32 ? 4 : 2;
     pdl_wait();
     pdl_launch_dependents();
@@ -119,60 +123,111 @@ combine_kernel(const void *__restrict__ out_disp, const void *__restrict__ w, in
                 for (int i = 0; i < 8; ++i) acc[v][i] = 0.0f;
             bool nan_row = false;
             float wkept = 0.0f;                 // sum of the kept slots' weights (shared term)
+            if constexpr (!EXTRAS) {
 #pragma unroll 2
-            for (int j = 0; j < top_k; ++j) {
-                const int64_t a = t * top_k + j;
-                int kind = kRouted;
-                int64_t cidx = 0;
-                if constexpr (EXTRAS) {
-                    if (ex.mask_dims == 1 && !ex.mask[t]) continue;
-                    if (ex.mask_dims == 2 && !ex.mask[a]) continue;
-                    if (ex.ids != nullptr) {
-                        const int64_t id = ex.ids[a];
-                        if (id >= ex.E) {
-                            const int64_t sp = id - ex.E;
-                            kind = sp < ex.zero_n ? kZero
-                                 : sp < ex.zero_n + ex.copy_n ? kCopy
-                                 : sp < ex.zero_n + ex.copy_n + ex.const_n ? kConst : kBad;
-                            cidx = sp - ex.zero_n - ex.copy_n;
-                        }
-                    }
-                }
-                const float wj = load_as_float(w, wdt, a);
-                if (kind == kBad) { nan_row = true; continue; }
-                const void *src = nullptr;
-                if (kind == kRouted) {
+                for (int j = 0; j < top_k; ++j) {
+                    const int64_t a = t * top_k + j;
+                    const float wj = load_as_float(w, wdt, a);
                     const int32_t r = row_of[a];
                     if (r < 0) { nan_row = true; continue; }
-                    src = static_cast<const uint8_t *>(out_disp) + (int64_t)r * H * elem_o;
-                }
-                if constexpr (EXTRAS) wkept += wj;
-                if (kind == kZero) continue;
-                float a1 = 0.0f, a2 = 0.0f;
-                if constexpr (EXTRAS) {
-                    if (kind == kConst) {
-                        a1 = load_as_float(ex.alpha1, YDT, cidx);
-                        a2 = load_as_float(ex.alpha2, YDT, cidx);
+                    const void *src = static_cast<const uint8_t *>(out_disp) + (int64_t)r * H * elem_o;
+#pragma unroll
+                    for (int v = 0; v < V; ++v) {
+                        const int64_t c = base + threadIdx.x + (int64_t)v * blockDim.x;
+                        if (c < ng) {
+                            float f[8];
+                            load8<ODT>(src, c, f);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) acc[v][i] = fmaf(wj, f[i], acc[v][i]);
+                        }
                     }
                 }
-#pragma unroll
-                for (int v = 0; v < V; ++v) {
-                    const int64_t c = base + threadIdx.x + (int64_t)v * blockDim.x;
-                    if (c < ng) {
-                        float f[8];
-                        if (!EXTRAS || kind == kRouted) {
-                            load8<ODT>(src, c, f);
+            } else {
+                // slots in chunks of blockDim: one thread per slot classifies it
+                // (mask bit, id, weight, row) into shared memory, then every thread
+                // walks the chunk with only its data loads left to wait for
+                for (int j0 = 0; j0 < top_k; j0 += blockDim.x) {
+                    const int nj = top_k - j0 < (int)blockDim.x ? top_k - j0 : (int)blockDim.x;
+                    __syncthreads();                    // the previous chunk's readers are done
+                    if ((int)threadIdx.x < nj) {
+                        const int64_t a = t * top_k + j0 + threadIdx.x;
+                        int k2 = kRouted;
+                        int64_t off = 0;
+                        float wv = 0.0f;
+                        if ((ex.mask_dims == 1 && !ex.mask[t]) || (ex.mask_dims == 2 && !ex.mask[a])) {
+                            k2 = kSkip;
                         } else {
-                            load8<YDT>(ex.ori_x, t * ng + c, f);
-                            if (kind == kConst) {
-                                float cv[8];
-                                load8<YDT>(ex.const_v, cidx * ng + c, cv);
-#pragma unroll
-                                for (int i = 0; i < 8; ++i) f[i] = a1 * f[i] + a2 * cv[i];
+                            if (ex.ids != nullptr) {
+                                const int64_t id = ex.ids[a];
+                                if (id >= ex.E) {
+                                    const int64_t sp = id - ex.E;
+                                    k2 = sp < ex.zero_n ? kZero
+                                       : sp < ex.zero_n + ex.copy_n ? kCopy
+                                       : sp < ex.zero_n + ex.copy_n + ex.const_n ? kConst : kBad;
+                                    off = sp - ex.zero_n - ex.copy_n;
+                                }
+                            }
+                            wv = load_as_float(w, wdt, a);
+                            if (k2 == kRouted) {
+                                const int32_t r = row_of[a];
+                                if (r < 0) k2 = kBad;
+                                else off = (int64_t)r * H * elem_o;
                             }
                         }
+                        s_kind[threadIdx.x] = k2;
+                        s_w[threadIdx.x] = wv;
+                        s_off[threadIdx.x] = off;
+                    }
+                    __syncthreads();
+                    // routed slots first, in the same tight loop as the plain combine
+                    // (the loads of two slots in flight together)
+#pragma unroll 2
+                    for (int jj = 0; jj < nj; ++jj) {
+                        if (s_kind[jj] != kRouted) continue;
+                        const float wj = s_w[jj];
+                        wkept += wj;
+                        const void *src = static_cast<const uint8_t *>(out_disp) + s_off[jj];
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) acc[v][i] = fmaf(wj, f[i], acc[v][i]);
+                        for (int v = 0; v < V; ++v) {
+                            const int64_t c = base + threadIdx.x + (int64_t)v * blockDim.x;
+                            if (c < ng) {
+                                float f[8];
+                                load8<ODT>(src, c, f);
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) acc[v][i] = fmaf(wj, f[i], acc[v][i]);
+                            }
+                        }
+                    }
+                    // then the rest: dropped, bad, zero, copy and const slots
+                    for (int jj = 0; jj < nj; ++jj) {
+                        const int k2 = s_kind[jj];
+                        if (k2 == kRouted || k2 == kSkip) continue;
+                        if (k2 == kBad) { nan_row = true; continue; }
+                        const float wj = s_w[jj];
+                        wkept += wj;
+                        if (k2 == kZero) continue;
+                        const int64_t off = s_off[jj];
+                        float a1 = 0.0f, a2 = 0.0f;
+                        if (k2 == kConst) {
+                            a1 = load_as_float(ex.alpha1, YDT, off);
+                            a2 = load_as_float(ex.alpha2, YDT, off);
+                        }
+#pragma unroll
+                        for (int v = 0; v < V; ++v) {
+                            const int64_t c = base + threadIdx.x + (int64_t)v * blockDim.x;
+                            if (c < ng) {
+                                float f[8];
+                                load8<YDT>(ex.ori_x, t * ng + c, f);
+                                if (k2 == kConst) {
+                                    float cv[8];
+                                    load8<YDT>(ex.const_v, off * ng + c, cv);
+#pragma unroll
+                                    for (int i = 0; i < 8; ++i) f[i] = a1 * f[i] + a2 * cv[i];
+                                }
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) acc[v][i] = fmaf(wj, f[i], acc[v][i]);
+                            }
+                        }
                     }
                 }
             }

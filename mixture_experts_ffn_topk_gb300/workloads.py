@@ -118,6 +118,32 @@ CONFIGS = {
 COMBINE_NORM = CombineNormConfig("combine_norm_bf16", 5, T=8192, H=7168, E=256,
                                  top_k=8, eps=1e-6)
 
+
+@dataclasses.dataclass(frozen=True)
+class CombineV2Config:
+    """The Ascend V2 combine's extras on the combine + norm workload's shapes:
+    special experts after the E routed ones, a shared expert, a 2-D active
+    mask keeping each slot with probability keep."""
+    name: str
+    number: int
+    T: int
+    H: int
+    E: int
+    top_k: int
+    eps: float
+    zero: int
+    copy: int
+    const: int
+    keep: float
+
+    @property
+    def seed(self) -> int:
+        return 1000 + self.number
+
+
+COMBINE_V2 = CombineV2Config("combine_v2_norm_bf16", 7, T=8192, H=7168, E=256, top_k=8,
+                             eps=1e-6, zero=2, copy=2, const=4, keep=0.9)
+
 TORCH_DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16,
                 "f16": torch.float16}
 
@@ -265,3 +291,26 @@ def training_grad(cfg: MoeConfig, device="cpu", seed: int | None = None) -> torc
     seed = cfg.seed if seed is None else seed
     g = _gen(seed + 101, "cpu")
     return _normal((cfg.T, cfg.H), g, "cpu", dtype=cfg.dtype).to(device)
+
+
+def combine_v2_inputs(cfg: CombineV2Config, device="cpu", seed: int | None = None) -> dict:
+    """Routing logits ``[T, E + special]`` FP32 and the 2-D mask (CPU
+    generator), then on ``device``: expert outputs ``[T*top_k, H]``, ori_x,
+    shared_x and residual ``[T, H]`` N(0,1), gamma N(1, 0.1), const alphas
+    U(0, 2) / U(-1, 1) and const values N(0,1) ``[const, H]``, all BF16."""
+    seed = cfg.seed if seed is None else seed
+    special = cfg.zero + cfg.copy + cfg.const
+    gc = _gen(seed, "cpu")
+    logits = torch.randn((cfg.T, cfg.E + special), generator=gc, dtype=torch.float32)
+    mask = torch.rand((cfg.T, cfg.top_k), generator=gc) < cfg.keep
+    g = _gen(seed + 7919, device)
+    rows = max(1, (1 << 24) // cfg.H)
+    n = lambda shape: _normal(shape, g, device, dtype="bf16", chunk_rows=rows)
+    out = {"logits": logits.to(device), "mask": mask.to(device),
+           "out_disp": n((cfg.T * cfg.top_k, cfg.H)), "ori_x": n((cfg.T, cfg.H)),
+           "shared_x": n((cfg.T, cfg.H)), "residual": n((cfg.T, cfg.H)),
+           "gamma": _normal((cfg.H,), g, device, std=math.sqrt(0.1), mean=1.0, dtype="bf16"),
+           "const_v": n((max(cfg.const, 1), cfg.H))}
+    out["alpha1"] = (torch.rand((max(cfg.const, 1),), generator=g, device=device) * 2).to(torch.bfloat16)
+    out["alpha2"] = (torch.rand((max(cfg.const, 1),), generator=g, device=device) * 2 - 1).to(torch.bfloat16)
+    return out
