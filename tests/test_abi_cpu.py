@@ -313,3 +313,101 @@ def test_binding_refuses_cpu_tensors(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="not built"):
         moe.load_library(str(tmp_path / "nope.so"))
+
+
+def test_training_validation(lib):
+    """First-order training entry points (ruDNN user guide, section 12):
+    every bad argument is refused on the host, before any CUDA call."""
+    P = ctypes.c_void_p
+    st = P(None)
+    U32, I32, I64 = 0, 1, 2
+
+    def rw(**kw):
+        a = dict(lg=P(FAKE), ldt=F32, T=8, E=16, idx=P(FAKE), idt=I32, k=4, sc=0, rn=1,
+                 scale=1.0, w=P(FAKE))
+        a.update(kw)
+        return lib.moe_router_weights(a["lg"], a["ldt"], a["T"], a["E"], a["idx"], a["idt"],
+                                      a["k"], a["sc"], a["rn"], a["scale"], a["w"], st)
+
+    assert rw(ldt=5) == DTYPE
+    assert rw(idt=3) == DTYPE
+    assert rw(sc=2) == DTYPE
+    assert rw(E=0) == SHAPE
+    assert rw(E=1025) == SHAPE
+    assert rw(k=17) == SHAPE                       # k > E
+    assert rw(E=100, k=65) == SHAPE                # k > 64
+    for bad in (0.0, -1.0, math.inf, math.nan):
+        assert rw(scale=bad) == VALUE
+    assert rw(lg=P(None)) == NULL
+    assert rw(w=P(FAKE_ODD)) == ALIGN
+    assert rw(T=0, lg=P(None), idx=P(None), w=P(None)) == OK
+
+    def rb(**kw):
+        a = dict(lg=P(FAKE), ldt=BF16, T=8, E=16, idx=P(FAKE), idt=I64, k=4, gw=P(FAKE), sc=1,
+                 rn=0, scale=2.0, dl=P(FAKE))
+        a.update(kw)
+        return lib.moe_router_backward(a["lg"], a["ldt"], a["T"], a["E"], a["idx"], a["idt"],
+                                       a["k"], a["gw"], a["sc"], a["rn"], a["scale"], a["dl"], st)
+
+    assert rb(idt=U32, sc=3) == DTYPE
+    assert rb(gw=P(None)) == NULL
+    assert rb(dl=P(FAKE_ODD)) == ALIGN
+    assert rb(scale=math.inf) == VALUE
+    assert rb(T=0, lg=P(None), idx=P(None), gw=P(None), dl=P(None)) == OK
+
+    def cb(**kw):
+        a = dict(out=P(FAKE), odt=F32, w=P(FAKE), wdt=F32, rows=P(FAKE), gy=P(FAKE), T=8, k=2,
+                 H=64, dt=BF16, dexp=P(FAKE), dw=P(FAKE))
+        a.update(kw)
+        return lib.moe_combine_backward(a["out"], a["odt"], a["w"], a["wdt"], a["rows"], a["gy"],
+                                        a["T"], a["k"], a["H"], a["dt"], a["dexp"], a["dw"], st)
+
+    assert cb(odt=F16) == DTYPE                    # outputs neither the dtype nor F32
+    assert cb(H=60) == SHAPE
+    assert cb(k=0) == SHAPE
+    assert cb(dw=P(None)) == NULL
+    assert cb(gy=P(FAKE_ODD)) == ALIGN
+    assert cb(T=0, out=P(None), w=P(None), rows=P(None), gy=P(None), dexp=P(None),
+              dw=P(None)) == OK
+
+    assert lib.moe_dispatch_backward(P(FAKE), 7, P(FAKE), 8, 2, 64, P(FAKE), st) == DTYPE
+    assert lib.moe_dispatch_backward(P(FAKE), BF16, P(FAKE), 8, 2, 60, P(FAKE), st) == SHAPE
+    assert lib.moe_dispatch_backward(P(None), BF16, P(FAKE), 8, 2, 64, P(FAKE), st) == NULL
+    assert lib.moe_dispatch_backward(P(None), BF16, P(None), 0, 2, 64, P(None), st) == OK
+
+    # training forward: the cache replaces the workspace
+    need = lib.moe_experts_training_cache_size(100, 64, BF16)
+    assert need == math.ceil(100 * 64 * (2 + 8) / 256) * 256
+    assert lib.moe_experts_training_cache_size(100, 64, F32) == math.ceil(100 * 64 * 12 / 256) * 256
+
+    def ft(**kw):
+        a = dict(rows=100, E=4, H=64, I=64, dt=BF16, odt=F32, cache=P(FAKE), nb=need)
+        a.update(kw)
+        return lib.moe_experts_forward_training(P(FAKE), P(FAKE), a["rows"], P(FAKE), P(FAKE),
+                                                P(FAKE), a["E"], a["H"], a["I"], a["dt"],
+                                                P(FAKE), a["odt"], a["cache"], a["nb"], st)
+
+    assert ft(odt=F16) == DTYPE
+    assert ft(H=60) == SHAPE
+    assert ft(nb=need - 256) == WORKSPACE
+    assert ft(cache=P(FAKE + 16)) == WORKSPACE       # not 256-byte aligned
+    assert ft(rows=0) == OK
+
+    # backward: dg | du [rows, 2I] and, for 16-bit types, per-expert TMA maps
+    ws = lib.moe_experts_backward_workspace_size(100, 4, 64, 64, BF16)
+    assert ws >= 2 * 100 * 64 * 2 + 4 * 5 * 128
+    assert lib.moe_experts_backward_workspace_size(100, 4, 64, 64, F32) == \
+        math.ceil(2 * 100 * 64 * 4 / 256) * 256
+    assert lib.moe_experts_backward_workspace_size(0, 4, 64, 64, BF16) > 0
+
+    def bw(**kw):
+        a = dict(rows=100, dt=BF16, ws=P(FAKE), nb=ws, gg=P(FAKE))
+        a.update(kw)
+        return lib.moe_experts_backward(P(FAKE), P(FAKE), a["rows"], P(FAKE), P(FAKE), P(FAKE),
+                                        4, 64, 64, a["dt"], P(FAKE), P(FAKE), P(FAKE), a["gg"],
+                                        P(FAKE), P(FAKE), a["ws"], a["nb"], st)
+
+    assert bw(dt=9) == DTYPE
+    assert bw(gg=P(None)) == NULL
+    assert bw(nb=ws - 256) == WORKSPACE
+    assert bw(rows=0, ws=P(None), nb=0) == WORKSPACE   # the maps are needed without rows too
