@@ -96,11 +96,13 @@ def test_training_step_full_size(dev):
     assert_close(to_f64(dl)[tokens], rdl, lname if lname != "f32" else "f32",
                  "logits gradient (sampled)")
 
-    # one expert's full weight gradients (all of its rows)
-    offsets = disp["offsets"].cpu().numpy()
-    counts = np.diff(offsets)
+    # one expert's full weight gradients (all of its rows, from the oracle's
+    # own dispatch, which the GPU's matches exactly)
+    counts, offsets, row_of, src_of, _ = oracle.dispatch(ridx, E)
+    assert np.array_equal(disp["offsets"].cpu().numpy(), offsets)
+    assert np.array_equal(disp["src_of"].cpu().numpy(), src_of)
     e = int(np.argmin(np.where(counts > 0, counts, np.iinfo(np.int32).max)))
-    src = disp["src_of"].cpu().numpy()[offsets[e]:offsets[e + 1]]
+    src = src_of[offsets[e]:offsets[e + 1]]
     toks, slots = src // k, src % k
     rw_e, _ = oracle.router_weights(np.ascontiguousarray(logits_np[toks]), lname, ridx[toks],
                                     "softmax", cfg.renormalize, 1.0, "f64")
