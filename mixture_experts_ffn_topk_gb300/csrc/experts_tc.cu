@@ -32,12 +32,16 @@
 // complete on the even CTA's stage barrier; both CTAs' epilogues read their
 // own TMEM and release the accumulator on the even CTA's barrier.
 // Tiles: each expert's row segment [offsets[e], offsets[e+1]) is cut into
-// 128-row M-tiles; linear tile ids run over (expert, n-tile, m-tile) with the
-// m-tile fastest, so CTAs working at the same time share weight tiles in L2.
-// The schedule is computed per CTA from the device-side offsets: no host
-// synchronisation. Rows of a tile past the segment end belong to the next
-// expert (or are TMA zero-fill past the last row); they are computed and not
-// stored. TMA zero-fills the K and N edges.
+// 128-row M-tiles (256-row units on a pair); linear unit ids run over
+// (expert, n-tile, m-unit) with the m-unit fastest, so CTAs working at the
+// same time share weight tiles in L2. A pair's last unit of an expert with at
+// most 128 rows left runs as an M = 128 pair MMA: each CTA loads 64 rows of A
+// (and, for SwiGLU, 64 gate rows over the same 64 up rows), and TMEM lanes
+// 0-63 / 64-127 of each CTA hold its rows against the two halves of the
+// tile's N. The schedule is computed per CTA from the device-side offsets: no
+// host synchronisation. Rows of a tile past the segment end belong to the
+// next expert (or are TMA zero-fill past the last row); they are computed and
+// not stored. TMA zero-fills the K and N edges.
 //
 // Every wait is bounded (kWaitLimitNs); on expiry the kernel sets ST_TIMEOUT,
 // stops issuing work, drains its own TMA copies and MMAs, frees TMEM and exits.
@@ -123,12 +127,13 @@ __device__ __forceinline__ int m_units(int seg_rows)
     return (seg_rows + BM * CG - 1) / (BM * CG);
 }
 
-// Unit id -> (expert, n-tile, m-tile of this CTA). With CG = 2 the pair's
-// CTAs take m-tiles 2u and 2u+1 of the unit; the second may lie past the
-// expert's rows (computed, never stored).
+// Unit id -> (expert, n-tile, m-unit j). With CG = 2 unit j covers rows
+// [256 j, 256 j + 256) of the expert's segment; when at most 128 of them
+// remain (`half`), the pair computes an M = 128 tile instead (64 rows per
+// CTA), so no CTA works on rows past the segment for nothing.
 template <int CG, typename SS>
-__device__ __forceinline__ void decode_tile(const SS &S, int E, int tile, int rank,
-                                            int &e, int &n, int &m)
+__device__ __forceinline__ void decode_unit(const SS &S, int E, int tile, int &e, int &n,
+                                            int &j, bool &half)
 {
     int lo = 0, hi = E - 1;
     while (lo < hi) {
@@ -136,10 +141,19 @@ __device__ __forceinline__ void decode_tile(const SS &S, int E, int tile, int ra
         if (S.prefix[mid] <= tile) lo = mid; else hi = mid - 1;
     }
     e = lo;
-    const int mu = m_units<CG>(S.offs[e + 1] - S.offs[e]);
+    const int seg = S.offs[e + 1] - S.offs[e];
+    const int mu = m_units<CG>(seg);
     const int local = tile - S.prefix[e];
     n = local / mu;
-    m = (local % mu) * CG + rank;
+    j = local % mu;
+    half = CG == 2 && seg - j * (BM * CG) <= BM;
+}
+
+// First row (within the expert's segment) of this CTA's A rows in unit j.
+template <int CG>
+__device__ __forceinline__ int unit_row0(int j, int rank, bool half)
+{
+    return j * (BM * CG) + rank * (half ? BM / 2 : BM);
 }
 
 
@@ -148,8 +162,11 @@ __device__ __forceinline__ void decode_tile(const SS &S, int E, int tile, int ra
 template <int DT, bool SWIGLU, int OUT, int CG>
 __global__ void __launch_bounds__(THREADS, 1)
 grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                       const __grid_constant__ CUtensorMap tmAh,
                        const __grid_constant__ CUtensorMap tmB0,
                        const __grid_constant__ CUtensorMap tmB1,
+                       const __grid_constant__ CUtensorMap tmB0h,
+                       const __grid_constant__ CUtensorMap tmB1h,
                        const int32_t *__restrict__ offsets, int E, int N, int K,
                        int n_tiles, void *__restrict__ out, unsigned *status,
                        CombineInto comb)
@@ -223,9 +240,10 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         int stage = 0;
         uint32_t phase = 0;
         for (int tile = unit0; tile < total_tiles; tile += unit_step) {
-            int e, n, m;
-            decode_tile<CG>(S, E, tile, rank, e, n, m);
-            const int row0 = S.offs[e] + m * BM;
+            int e, n, j;
+            bool half;
+            decode_unit<CG>(S, E, tile, e, n, j, half);
+            const int row0 = S.offs[e] + unit_row0<CG>(j, rank, half);
             bool ok = true;
             for (int kb = 0; kb < num_kb; ++kb) {
                 if (!mbar_wait<CG>(&S.empty[stage], phase ^ 1u, abort_flag, status, kWaitLimitNs)) { ok = false; break; }
@@ -235,14 +253,31 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                     // the leader's barrier expects both CTAs' bytes; a peer's
                     // copy may land before the leader arms it (the phase
                     // cannot complete while the leader's arrival is pending)
-                    if (leader) mbar_arrive_expect_tx(&S.full[stage], 2 * P::STAGE_BYTES);
+                    if (leader)
+                        mbar_arrive_expect_tx(&S.full[stage],
+                                              2 * (half ? P::STAGE_BYTES - A_BYTES / 2 : P::STAGE_BYTES));
                     const uint32_t bar = mapa_shared(smem_u32(&S.full[stage]), 0);
-                    tma_load_2d_pair(sa, &tmA, bar, kb * BK, row0);
-                    if (SWIGLU)      // CTA 0 holds the gate rows, CTA 1 the up rows
-                        tma_load_3d_pair(sb, rank == 0 ? &tmB0 : &tmB1, bar, kb * BK, n * (BN / 2), e);
-                    else
-                        tma_load_3d_pair(sb, &tmB0, bar, kb * BK, n * BN + rank * (BN / 2), e);
+                    if (half) {
+                        // 64 rows of A per CTA; for SwiGLU each CTA holds 64 gate
+                        // rows over the same 64 up rows, so each TMEM lane half
+                        // of the M = 128 tile sees both factors of 64 h columns
+                        tma_load_2d_pair(sa, &tmAh, bar, kb * BK, row0);
+                        if (SWIGLU) {
+                            const int c1 = n * (BN / 2) + rank * (BN / 4);
+                            tma_load_3d_pair(sb, &tmB0h, bar, kb * BK, c1, e);
+                            tma_load_3d_pair(sb + P::B_BYTES / 2, &tmB1h, bar, kb * BK, c1, e);
+                        } else {
+                            tma_load_3d_pair(sb, &tmB0, bar, kb * BK, n * BN + rank * (BN / 2), e);
+                        }
+                    } else {
+                        tma_load_2d_pair(sa, &tmA, bar, kb * BK, row0);
+                        if (SWIGLU)      // CTA 0 holds the gate rows, CTA 1 the up rows
+                            tma_load_3d_pair(sb, rank == 0 ? &tmB0 : &tmB1, bar, kb * BK, n * (BN / 2), e);
+                        else
+                            tma_load_3d_pair(sb, &tmB0, bar, kb * BK, n * BN + rank * (BN / 2), e);
+                    }
                 } else {
+                    (void)half;
                     mbar_arrive_expect_tx(&S.full[stage], P::STAGE_BYTES);
                     tma_load_2d(sa, &tmA, &S.full[stage], kb * BK, row0);
                     if (SWIGLU) {
@@ -260,7 +295,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         }
     } else if (warp == 1 && lane == 0 && leader) {
         // ------------------------------------------------------ MMA issuer
-        constexpr uint32_t idesc = idesc_f16<DT>(BM * CG, BN);
+        constexpr uint32_t idesc_full = idesc_f16<DT>(BM * CG, BN);
+        constexpr uint32_t idesc_half = idesc_f16<DT>(BM, BN);    // CG = 2 only
         int stage = 0;
         uint32_t phase = 0;
         int it = 0;
@@ -268,6 +304,10 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         for (int tile = unit0; tile < total_tiles && ok; tile += unit_step, ++it) {
             const int acc = it & 1;
             const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+            int e, n, j;
+            bool half;
+            decode_unit<CG>(S, E, tile, e, n, j, half);
+            const uint32_t idesc = half ? idesc_half : idesc_full;
             if (!mbar_wait<CG>(&S.acc_empty[acc], acc_phase ^ 1u, abort_flag, status, kWaitLimitNs)) { ok = false; break; }
             tc_fence_after();
             const uint32_t d = tmem_base + (uint32_t)(acc * ACC_COLS);
@@ -312,10 +352,18 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         const int cch = lane & 7;                               // chunk this lane copies out
         int it = 0;
         for (int tile = unit0; tile < total_tiles; tile += unit_step, ++it) {
-            int e, n, m;
-            decode_tile<CG>(S, E, tile, rank, e, n, m);
+            int e, n, j;
+            bool half;
+            decode_unit<CG>(S, E, tile, e, n, j, half);
             const int seg_rows = S.offs[e + 1] - S.offs[e];
-            const int r_base = m * BM + q * 32;                 // this warp's first row in the segment
+            // this warp's first row in the segment and first output column of
+            // the tile: an M = 128 pair tile keeps a CTA's 64 rows in lanes
+            // 0-63 against the first half of the tile's N and in lanes 64-127
+            // against the second half, each in TMEM columns [0, N / 2)
+            const int r_base = unit_row0<CG>(j, rank, half) + (half ? (q & 1) : q) * 32;
+            const int cblk = half ? (q >> 1) * (N_OUT / 2) : 0;
+            const int rounds = half ? ROUNDS / 2 : ROUNDS;
+            const int u_col = half ? BN / 4 : BN / 2;        // TMEM column of u (SwiGLU)
             uint8_t *out_base = static_cast<uint8_t *>(out) + ((int64_t)S.offs[e] + r_base) * out_row_bytes;
             // kOutCombine: token and routing weight of this lane's row
             int row_tok = -1;
@@ -358,7 +406,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             };
             (void)emit_lines;
 #pragma unroll 1
-            for (int rd = 0; rd < ROUNDS; ++rd) {
+            for (int rd = 0; rd < rounds; ++rd) {
                 uint32_t w[32];                                 // this row's 128 output bytes
                 if constexpr (F32ACC) {
                     tmem_ld32(tbase + rd * 32, w);
@@ -370,13 +418,13 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                     }
                 } else {
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        const int c = rd * 2 + half;            // 32-column TMEM chunk
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const int c = rd * 2 + hf;              // 32-column TMEM chunk
                         uint32_t g[32];
                         tmem_ld32(tbase + c * 32, g);
                         if constexpr (SWIGLU) {
                             uint32_t u[32];
-                            tmem_ld32(tbase + BN / 2 + c * 32, u);
+                            tmem_ld32(tbase + u_col + c * 32, u);
                             tmem_ld_wait(g);
                             tmem_ld_wait(u);
 #pragma unroll
@@ -385,12 +433,12 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                                 const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
                                 const float h0 = g0 / (1.0f + __expf(-g0)) * u0;
                                 const float h1 = g1 / (1.0f + __expf(-g1)) * u1;
-                                w[half * 16 + i] = pack2<DT>(h0, h1);
+                                w[hf * 16 + i] = pack2<DT>(h0, h1);
                             }
                             if constexpr (OUT == kOutSaveGU) {
                                 // the FP32 g and u of these 32 columns, as they are
                                 const int64_t gu_row = (int64_t)N * 4;
-                                const int64_t cb = (int64_t)(n * N_OUT + rd * RCOLS + half * 32) * 4;
+                                const int64_t cb = (int64_t)(n * N_OUT + cblk + rd * RCOLS + hf * 32) * 4;
                                 const int64_t r0 = (int64_t)S.offs[e] + r_base;
                                 emit_lines(g, reinterpret_cast<uint8_t *>(comb.g_out) + r0 * gu_row,
                                            gu_row, cb, gu_row);
@@ -401,12 +449,12 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                             tmem_ld_wait(g);
 #pragma unroll
                             for (int i = 0; i < 16; ++i)
-                                w[half * 16 + i] = pack2<DT>(__uint_as_float(g[2 * i]),
+                                w[hf * 16 + i] = pack2<DT>(__uint_as_float(g[2 * i]),
                                                              __uint_as_float(g[2 * i + 1]));
                         }
                     }
                 }
-                const int64_t col_byte = (int64_t)(n * N_OUT + rd * RCOLS) * ESZ + cch * 16;
+                const int64_t col_byte = (int64_t)(n * N_OUT + cblk + rd * RCOLS) * ESZ + cch * 16;
 #pragma unroll
                 for (int p = 0; p < 8; ++p)
                     *reinterpret_cast<uint4 *>(stg + lane * EPI_ROW_BYTES + ((p ^ (lane & 7)) << 4)) =
@@ -537,8 +585,9 @@ cudaError_t grid_size(int64_t units, int *grid)
 
 // Programmatic dependent launch, in clusters of CG CTAs.
 template <int DT, bool SWIGLU, int OUT, int CG>
-cudaError_t launch_gemm(int64_t units, cudaStream_t s, const CUtensorMap &ta, const CUtensorMap &tb0,
-                        const CUtensorMap &tb1, const int32_t *offsets, int E, int N, int K,
+cudaError_t launch_gemm(int64_t units, cudaStream_t s, const CUtensorMap &ta, const CUtensorMap &tah,
+                        const CUtensorMap &tb0, const CUtensorMap &tb1, const CUtensorMap &tb0h,
+                        const CUtensorMap &tb1h, const int32_t *offsets, int E, int N, int K,
                         int n_tiles, void *out, unsigned *status, const CombineInto &comb)
 {
     cudaError_t err = ensure_smem_attr<DT, SWIGLU, OUT, CG>();
@@ -560,8 +609,8 @@ cudaError_t launch_gemm(int64_t units, cudaStream_t s, const CUtensorMap &ta, co
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = CG == 2 ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<DT, SWIGLU, OUT, CG>, ta, tb0, tb1,
-                              offsets, E, N, K, n_tiles, out, status, comb);
+    return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<DT, SWIGLU, OUT, CG>, ta, tah, tb0, tb1,
+                              tb0h, tb1h, offsets, E, N, K, n_tiles, out, status, comb);
 }
 
 // CTA pairs pay when experts average at least two M-tiles: a pair's second
@@ -583,25 +632,33 @@ cudaError_t launch_tc_cg(const void *x_disp, const int32_t *offsets, int64_t row
         !encode_2d(&mh, tdt, h_ws, (uint64_t)I, (uint64_t)rows, BK, BM) ||
         !encode_3d(&md, tdt, down, (uint64_t)I, (uint64_t)H, (uint64_t)E, BK, BN / CG))
         return cudaErrorInvalidValue;
+    // M = 128 pair tiles: 64-row boxes of x / h, and of gate / up
+    CUtensorMap mxh = mx, mhh = mh, mgh = mg, muh = mu;
+    if (CG == 2 &&
+        (!encode_2d(&mxh, tdt, x_disp, (uint64_t)H, (uint64_t)rows, BK, BM / 2) ||
+         !encode_2d(&mhh, tdt, h_ws, (uint64_t)I, (uint64_t)rows, BK, BM / 2) ||
+         !encode_3d(&mgh, tdt, gate, (uint64_t)H, (uint64_t)I, (uint64_t)E, BK, BN / 4) ||
+         !encode_3d(&muh, tdt, up, (uint64_t)H, (uint64_t)I, (uint64_t)E, BK, BN / 4)))
+        return cudaErrorInvalidValue;
     const int nt1 = (int)((I + BN / 2 - 1) / (BN / 2));
     const int nt2 = (int)((H + BN - 1) / BN);
     const int64_t u1 = tc_unit_upper_bound(rows, E, nt1, CG);
     const int64_t u2 = tc_unit_upper_bound(rows, E, nt2, CG);
     cudaError_t err =
         comb.g_out != nullptr
-            ? launch_gemm<DT, true, kOutSaveGU, CG>(u1, s, mx, mg, mu, offsets, E, (int)I, (int)H,
-                                                   nt1, h_ws, status, comb)
-            : launch_gemm<DT, true, kOutDtype, CG>(u1, s, mx, mg, mu, offsets, E, (int)I, (int)H,
-                                                  nt1, h_ws, status, comb);
+            ? launch_gemm<DT, true, kOutSaveGU, CG>(u1, s, mx, mxh, mg, mu, mgh, muh, offsets, E,
+                                                   (int)I, (int)H, nt1, h_ws, status, comb)
+            : launch_gemm<DT, true, kOutDtype, CG>(u1, s, mx, mxh, mg, mu, mgh, muh, offsets, E,
+                                                  (int)I, (int)H, nt1, h_ws, status, comb);
     if (err != cudaSuccess) return err;
     if (out_mode == kOutF32)
-        return launch_gemm<DT, false, kOutF32, CG>(u2, s, mh, md, md, offsets, E, (int)H, (int)I,
-                                                   nt2, out, status, comb);
+        return launch_gemm<DT, false, kOutF32, CG>(u2, s, mh, mhh, md, md, md, md, offsets, E,
+                                                   (int)H, (int)I, nt2, out, status, comb);
     if (out_mode == kOutCombine)
-        return launch_gemm<DT, false, kOutCombine, CG>(u2, s, mh, md, md, offsets, E, (int)H,
-                                                       (int)I, nt2, out, status, comb);
-    return launch_gemm<DT, false, kOutDtype, CG>(u2, s, mh, md, md, offsets, E, (int)H, (int)I,
-                                                 nt2, out, status, comb);
+        return launch_gemm<DT, false, kOutCombine, CG>(u2, s, mh, mhh, md, md, md, md, offsets, E,
+                                                       (int)H, (int)I, nt2, out, status, comb);
+    return launch_gemm<DT, false, kOutDtype, CG>(u2, s, mh, mhh, md, md, md, md, offsets, E,
+                                                 (int)H, (int)I, nt2, out, status, comb);
 }
 
 template <int DT>

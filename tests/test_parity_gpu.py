@@ -280,6 +280,49 @@ def test_experts_exact_small_integers(dev, T, split):
     assert torch.all(out.cpu().float() == 0.0)
 
 
+# Rows per expert around the edges of the CTA-pair units (256 rows each; an
+# expert's last unit with at most 128 rows runs as an M = 128 pair tile, 64
+# rows per CTA): one full unit (256), exactly one M = 128 tile (128), a single
+# row (1), one CTA's rows only (64) and one more (65), a full unit with one row
+# on its second CTA (129), 383 / 384 / 385 around the fine prefill's average,
+# an empty expert, and a long one. 3095 rows >= 256 per expert select pairs;
+# H = 200 leaves a K tail, I = 200 partial N tiles in both GEMMs.
+PAIR_EDGE_COUNTS = [256, 128, 1, 64, 65, 129, 383, 384, 385, 0, 200, 1100]
+
+
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16], ids=["bf16", "f16"])
+def test_experts_pair_unit_edges(dev, dt):
+    E, H, I = len(PAIR_EDGE_COUNTS), 200, 200
+    offsets = np.concatenate([[0], np.cumsum(PAIR_EDGE_COUNTS)]).astype(np.int32)
+    rows = int(offsets[-1])
+    assert rows >= 256 * E
+    g = torch.Generator().manual_seed(11)
+    x = torch.randn((rows, H), generator=g).to(dt)
+    gate = (torch.randn((E, I, H), generator=g) * H ** -0.5).to(dt)
+    up = (torch.randn((E, I, H), generator=g) * H ** -0.5).to(dt)
+    down = (torch.randn((E, H, I), generator=g) * I ** -0.5).to(dt)
+    name = TORCH_TO_NAME[dt]
+    off = torch.from_numpy(offsets).to(dev)
+    on = [t.to(dev) for t in (x, gate, up, down)]
+    out16 = moe.moe_experts_forward(*on[:1], off, *on[1:])
+    out32 = moe.moe_experts_forward(*on[:1], off, *on[1:], out_dtype=torch.float32)
+    out_t, cache = moe.moe_experts_forward_training(*on[:1], off, *on[1:],
+                                                    out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert moe.moe_device_status() == 0
+    ref = oracle.experts_dispatched(np_of(x), name, offsets, np_of(gate), np_of(up), np_of(down))
+    assert_close(to_f64(out16), ref, name, "expert outputs (dtype)")
+    assert_close(to_f64(out32), ref, name, "expert outputs (FP32)")
+    assert torch.equal(out_t, out32)
+    hb = rows * I * x.element_size()
+    h_c = cache[:hb].view(dt).view(rows, I)
+    gu_c = cache[hb: hb + 2 * rows * I * 4].view(torch.float32).view(2, rows, I)
+    rg, ru, rh = oracle.experts_cache_dispatched(np_of(x), name, offsets, np_of(gate), np_of(up))
+    assert_close(to_f64(gu_c[0]), rg, name, "cached g")
+    assert_close(to_f64(gu_c[1]), ru, name, "cached u")
+    assert_close(to_f64(h_c), rh, name, "cached h")
+
+
 # ---------------------------------------------------------------- combine
 
 # (T, k, H, expert-output dtype, weight dtype, activation dtype)
