@@ -143,6 +143,26 @@ def _ptr(a):
     return a.ctypes.data_as(ctypes.c_void_p)
 
 
+def _check_index(ix, n: int, what: str, allow_negative: bool = False):
+    """Raise ValueError unless every entry of ``ix`` indexes one of ``n`` rows
+    (entries < 0 mean "no row" where ``allow_negative``). The C routines
+    trust their index arrays; this keeps a malformed one (an oracle mutant's
+    offsets, say) from reading or writing outside a buffer."""
+    ix = np.asarray(ix)
+    if ix.size == 0:
+        return
+    lo = ix.min()
+    if ix.max() >= n or (lo < 0 and not allow_negative):
+        raise ValueError(f"{what}: index outside [0, {n})")
+
+
+def _check_offsets(offsets, rows: int, what: str):
+    """Segment offsets [E+1]: non-decreasing from 0 and within ``rows`` rows."""
+    o = np.asarray(offsets, dtype=np.int64)
+    if o.size == 0 or o[0] != 0 or np.any(np.diff(o) < 0) or o[-1] > rows:
+        raise ValueError(f"{what}: offsets not a partition of at most {rows} rows")
+
+
 def convert(a, src_dt: str, dst_dt: str, lib=None):
     """Element-wise dtype conversion (exact upcast, RNE downcast)."""
     lib = lib or load_library()
@@ -225,6 +245,9 @@ def gather(x, dt: str, top_k: int, src_of, rows: int, lib=None):
     x = _arr(x, dt)
     H = x.shape[1]
     src_of = np.ascontiguousarray(src_of, dtype=np.int32)
+    if src_of.size < rows:
+        raise ValueError("gather: fewer src_of entries than rows")
+    _check_index(src_of[:rows] // top_k, x.shape[0], "gather")
     out = np.zeros((rows, H), dtype=_storage(dt))
     lib.oracle_gather(_ptr(x), DTYPE_CODES[dt], H, top_k, _ptr(src_of), rows,
                       _ptr(out))
@@ -242,6 +265,8 @@ def swiglu_rows(xrows, dt: str, expert_of_row, gate, up, down, lib=None):
     E, I, H = gate.shape
     n = xrows.shape[0]
     eor = np.ascontiguousarray(expert_of_row, dtype=np.int32)
+    if eor.size != n:
+        raise ValueError("swiglu_rows: one expert id per row")
     out = np.empty((n, H), dtype=np.float64)
     rc = lib.oracle_swiglu_rows(_ptr(xrows), DTYPE_CODES[dt], n, _ptr(eor),
                                 _ptr(gate), _ptr(up), _ptr(down), E, H, I,
@@ -259,6 +284,9 @@ def experts_dispatched(x_disp, dt: str, offsets, gate, up, down, lib=None):
     gate, up, down = _arr(gate, dt), _arr(up, dt), _arr(down, dt)
     E, I, H = gate.shape
     offsets = np.ascontiguousarray(offsets, dtype=np.int32)
+    if offsets.size != E + 1:
+        raise ValueError("experts_dispatched: offsets must have E + 1 entries")
+    _check_offsets(offsets, x_disp.shape[0], "experts_dispatched")
     out = np.empty((int(offsets[E]), H), dtype=np.float64)
     rc = lib.oracle_experts_dispatched(_ptr(x_disp), DTYPE_CODES[dt],
                                        _ptr(offsets), E, _ptr(gate), _ptr(up),
@@ -276,6 +304,9 @@ def combine(out_disp, odt: str, w, wdt: str, row_of, top_k: int, lib=None):
     row_of = np.ascontiguousarray(row_of, dtype=np.int32)
     T = row_of.size // top_k
     H = out_disp.shape[1]
+    _check_index(row_of, out_disp.shape[0], "combine", allow_negative=True)
+    if w.size < T * top_k:
+        raise ValueError("combine: fewer weights than slots")
     y = np.empty((T, H), dtype=np.float64)
     lib.oracle_combine(_ptr(out_disp), DTYPE_CODES[odt], _ptr(w),
                        DTYPE_CODES[wdt], _ptr(row_of), T, top_k, H, _ptr(y))
@@ -295,6 +326,7 @@ def combine_v2(out_disp, odt: str, w, wdt: str, row_of, top_k: int, xdt: str, id
     T = w.shape[0]
     H = out_disp.shape[1]
     row_of = np.ascontiguousarray(row_of, dtype=np.int32)
+    _check_index(row_of, out_disp.shape[0], "combine_v2", allow_negative=True)
     ids_a = None if ids is None else np.ascontiguousarray(ids, dtype=np.uint32)
     opt = {n: (None if v is None else _arr(v, xdt)) for n, v in
            dict(ori_x=ori_x, alpha1=alpha1, alpha2=alpha2, const_v=const_v,
@@ -484,6 +516,9 @@ def combine_backward(out_disp, odt: str, w, wdt: str, row_of, grad_y, gdt: str, 
     row_of = np.ascontiguousarray(row_of, dtype=np.int32)
     T, H = gy.shape
     rows = out_disp.shape[0]
+    _check_index(row_of, rows, "combine_backward", allow_negative=True)
+    if row_of.size != T * top_k or w.size < T * top_k:
+        raise ValueError("combine_backward: row_of / weights do not match [T, top_k]")
     dexp = np.empty((rows, H), dtype=np.float64)
     dw = np.empty((T, top_k), dtype=np.float64)
     lib.oracle_combine_backward(_ptr(out_disp), DTYPE_CODES[odt], _ptr(w), DTYPE_CODES[wdt],
@@ -503,6 +538,8 @@ def swiglu_backward_rows(xrows, dt: str, expert_of_row, gate, up, down, dout, dd
     E, I, H = gate.shape
     n = xrows.shape[0]
     eor = np.ascontiguousarray(expert_of_row, dtype=np.int32)
+    if eor.size != n or dout.shape[0] != n:
+        raise ValueError("swiglu_backward_rows: one expert id and one output gradient per row")
     dx = np.empty((n, H), dtype=np.float64)
     dg = np.empty((E, I, H), dtype=np.float64)
     du = np.empty((E, I, H), dtype=np.float64)
@@ -522,6 +559,9 @@ def experts_backward_dispatched(x_disp, dt: str, offsets, gate, up, down, dout, 
     ``[offsets[e], offsets[e+1])``)."""
     offsets = np.asarray(offsets, dtype=np.int64)
     E = np.asarray(gate).shape[0]
+    _check_offsets(offsets, np.asarray(x_disp).shape[0], "experts_backward_dispatched")
+    if offsets.size != E + 1 or offsets[E] != np.asarray(x_disp).shape[0]:
+        raise ValueError("experts_backward_dispatched: offsets[E] must equal the rows given")
     owner = np.repeat(np.arange(E, dtype=np.int32), np.diff(offsets))
     return swiglu_backward_rows(x_disp, dt, owner, gate, up, down, dout, ddt, lib)
 
@@ -534,6 +574,7 @@ def dispatch_backward(dinput, dt: str, row_of, top_k: int, lib=None):
     row_of = np.ascontiguousarray(row_of, dtype=np.int32)
     T = row_of.size // top_k
     H = d.shape[1]
+    _check_index(row_of, d.shape[0], "dispatch_backward", allow_negative=True)
     dx = np.empty((T, H), dtype=np.float64)
     lib.oracle_dispatch_backward(_ptr(d), DTYPE_CODES[dt], _ptr(row_of), T, top_k, H,
                                  _ptr(dx))
@@ -548,6 +589,9 @@ def experts_cache_dispatched(x_disp, dt: str, offsets, gate, up, lib=None):
     gate, up = _arr(gate, dt), _arr(up, dt)
     E, I, H = gate.shape
     offsets = np.asarray(offsets, dtype=np.int64)
+    if offsets.size != E + 1:
+        raise ValueError("experts_cache_dispatched: offsets must have E + 1 entries")
+    _check_offsets(offsets, x_disp.shape[0], "experts_cache_dispatched")
     n = int(offsets[E])
     owner = np.ascontiguousarray(np.repeat(np.arange(E, dtype=np.int32), np.diff(offsets)))
     g = np.empty((n, I)); u = np.empty((n, I)); h = np.empty((n, I))

@@ -5,8 +5,11 @@ Each mutant is a one-place edit of ``oracle/moe_oracle.c`` built into a
 temporary library; at least one ``check_*`` in ``oracle_pins.py`` must fail on
 it. This shows the pins constrain each step of the oracle (routing, dispatch,
 gather, experts, combine, norm, dtype rounding), not only its happy path.
-Every mutant keeps all memory accesses in bounds: mutants run inside the test
-process, so one that wrote out of bounds could corrupt it.
+Mutants run inside the test process, so none may touch memory outside a
+buffer: the mutated C code itself stays in bounds, and the oracle's Python
+wrappers check every index array (dispatch maps, offsets) against the buffer
+it indexes, so a mutant whose maps disagree with its offsets raises
+ValueError instead of reading or writing past a buffer.
 """
 
 import ctypes
@@ -163,3 +166,30 @@ def test_mutant_is_caught(tmp_path, name, old, new):
         except (AssertionError, ValueError, IndexError):
             caught.append(check.__name__)
     assert caught, f"no pin catches mutant {name}"
+
+
+def test_wrappers_reject_out_of_range_indices():
+    """Index arrays that point past their buffers are refused before any C
+    code runs (the shape of the short-offsets mutant's maps)."""
+    import numpy as np
+    rows, H, k = 5, 4, 2
+    out = np.zeros((rows, H))
+    w = np.full((3, k), 0.5)
+    gy = np.zeros((3, H))
+    bad_row_of = np.array([0, 1, 2, 3, 4, rows], dtype=np.int32)
+    with pytest.raises(ValueError):
+        oracle.combine(out, "f64", w, "f64", bad_row_of, k)
+    with pytest.raises(ValueError):
+        oracle.combine_backward(out, "f64", w, "f64", bad_row_of, gy, "f64", k)
+    with pytest.raises(ValueError):
+        oracle.dispatch_backward(out, "f64", bad_row_of, k)
+    with pytest.raises(ValueError):
+        oracle.gather(np.zeros((2, H), np.float32), "f32", k, np.array([0, 1, 4], np.int32), 3)
+    gate = np.zeros((2, 3, H), np.float32)
+    down = np.zeros((2, H, 3), np.float32)
+    with pytest.raises(ValueError):
+        oracle.experts_dispatched(np.zeros((4, H), np.float32), "f32",
+                                  np.array([0, 3, 5], np.int32), gate, gate, down)
+    with pytest.raises(ValueError):
+        oracle.experts_cache_dispatched(np.zeros((4, H), np.float32), "f32",
+                                        np.array([0, 3, 2], np.int32), gate, gate)
