@@ -385,7 +385,8 @@ def run_ours(args, rank, world, local, dist):
                 "d2h_bytes_per_step": y.numel() * eb,
                 "how": "moe_forward through the C ABI; per step x and logits copied in from "
                        "pinned host memory and y copied out, double-buffered so the copies "
-                       "of neighbouring steps overlap the compute; no L2 flush (each step "
+                       "of neighbouring steps (in and out on separate copy streams) overlap "
+                       "the compute; no L2 flush (each step "
                        "streams 1.1 GB of expert weights, more than L2)"},
         "staged_ms_per_step": staged_ms,
         "roofline": roofline_entry(achieved, exp_gbs, exp_bytes, flops, peaks, traffic),
@@ -572,7 +573,7 @@ def run_training(args, rank, world, local, dist, dev, peaks, flush):
                 "how": "the training step through the C ABI; per step x, logits and the output "
                        "gradient copied in from pinned host memory, the input and logits "
                        "gradients copied out, double-buffered so the copies of neighbouring "
-                       "steps overlap the compute; no L2 flush (each step streams the 1.1 GB "
+                       "steps (in and out on separate copy streams) overlap the compute; no L2 flush (each step streams the 1.1 GB "
                        "of expert weights and writes 2.2 GB of weight gradients)"},
         "roofline": roof,
         "kernels": {n: {"ms": v} for n, v in stage_ms.items()},
@@ -675,26 +676,27 @@ def timed_loop(fn, args, stream, flush):
 def pipelined_e2e(run_step, host_in, dev_in, dev_out, host_out, args, dev):
     """End-to-end steps through the C ABI with host buffers: every step copies
     its inputs from pinned host memory, computes, and copies its result back.
-    Two buffer sets and a copy stream beside the compute stream let step i+1's
-    inputs and step i-1's result cross the link while step i computes (a
-    serving loop's double buffering). host_in[j] -> dev_in[slot][j];
-    dev_out[slot][j] -> host_out[slot][j]; run_step(slot) computes on the
-    current stream. Returns milliseconds per step (first copy in to last copy
-    out, over args.steps steps, after args.warmup such steps)."""
+    Two buffer sets, an inbound and an outbound copy stream beside the compute
+    stream: step i+1's inputs and step i-1's result cross the link (each way
+    on its own copy engine) while step i computes, a serving loop's double
+    buffering. host_in[j] -> dev_in[slot][j]; dev_out[slot][j] ->
+    host_out[slot][j]; run_step(slot) computes on the current stream. Returns
+    milliseconds per step (first copy in to last copy out, over args.steps
+    steps, after args.warmup such steps)."""
     comp = torch.cuda.current_stream(dev)
-    cp = torch.cuda.Stream(dev)
+    cp_in, cp_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     h2d_done = [torch.cuda.Event(), torch.cuda.Event()]
     comp_done = [torch.cuda.Event(), torch.cuda.Event()]
     d2h_done = [torch.cuda.Event(), torch.cuda.Event()]
 
     def h2d(i):
         slot = i % 2
-        with torch.cuda.stream(cp):
+        with torch.cuda.stream(cp_in):
             if i >= 2:
-                cp.wait_event(comp_done[slot])          # the slot's last reader is done
+                cp_in.wait_event(comp_done[slot])       # the slot's last reader is done
             for src, dst in zip(host_in, dev_in[slot]):
                 dst.copy_(src, non_blocking=True)
-            h2d_done[slot].record(cp)
+            h2d_done[slot].record(cp_in)
 
     def loop(n):
         h2d(0)
@@ -707,18 +709,18 @@ def pipelined_e2e(run_step, host_in, dev_in, dev_out, host_out, args, dev):
             comp_done[slot].record(comp)
             if i + 1 < n:
                 h2d(i + 1)
-            with torch.cuda.stream(cp):
-                cp.wait_event(comp_done[slot])
+            with torch.cuda.stream(cp_out):
+                cp_out.wait_event(comp_done[slot])
                 for src, dst in zip(dev_out[slot], host_out[slot]):
                     dst.copy_(src, non_blocking=True)
-                d2h_done[slot].record(cp)
+                d2h_done[slot].record(cp_out)
 
     loop(max(2, args.warmup))
     torch.cuda.synchronize(dev)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record(cp)
+    start.record(cp_in)
     loop(args.steps)
-    end.record(cp)
+    end.record(cp_out)
     torch.cuda.synchronize(dev)
     return start.elapsed_time(end) / args.steps
 
