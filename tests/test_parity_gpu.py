@@ -482,6 +482,42 @@ def test_forward_repeatable_and_stream(dev):
     assert_same_sum(y1, y2, combine_magnitude(out, w, d["row_of"]), cfg.top_k)
 
 
+@pytest.mark.parametrize("cfg", [SMALL[0], PAIR[0]], ids=lambda c: c.name)
+def test_forward_cuda_graph_replay(dev, cfg):
+    """moe_forward captured once in a CUDA graph (its workspace memset, the
+    routing, dispatch, GEMM and finalize kernels, their programmatic-launch
+    edges) computes the forward of whatever the captured input buffers hold
+    at each replay."""
+    cpu, g = inputs_on(cfg, dev)
+    o = oracle_inputs(cpu)
+    x, logits = g["x"].clone(), g["logits"].clone()
+    ws = torch.empty(moe.moe_forward_workspace_size(cfg.T, cfg.H, cfg.I, cfg.E, cfg.top_k,
+                                                    x.dtype, logits.dtype),
+                     dtype=torch.uint8, device=dev)
+    y = torch.empty_like(x)
+
+    def fwd():
+        moe.moe_forward(x, logits, g["gate"], g["up"], g["down"], cfg.top_k, cfg.renormalize,
+                        y=y, workspace=ws)
+
+    fwd()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        fwd()
+    for seed in (5, 6):
+        gen = torch.Generator().manual_seed(seed)
+        x.copy_(torch.randn(x.shape, generator=gen).to(x.dtype))
+        logits.copy_(torch.randn(logits.shape, generator=gen).to(logits.dtype))
+        y.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert moe.moe_device_status() == 0
+        ref = oracle.forward(np_of(x), cfg.dtype, np_of(logits), cfg.logits_dtype, o["gate"],
+                             o["up"], o["down"], cfg.top_k, cfg.renormalize)
+        assert_close(to_f64(y), ref["y"], cfg.dtype, f"{cfg.name} y, graph replay {seed}")
+
+
 def test_forward_fp32_bit_reproducible(dev):
     cfg = SMALL[5]
     _, g = inputs_on(cfg, dev)
