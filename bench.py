@@ -275,7 +275,11 @@ def run_ours(args, rank, world, local, dist):
         moe.moe_combine(out_disp, w, row_of, y=y)
         if ev: ev[3].record(stream)
 
-    launches_per_step = 1 + 4 + 2 + 1   # route, dispatch x4, GEMM1+GEMM2, finalize
+    # route + dispatch: one fused route-and-count kernel, rank, gather (softmax
+    # routing at T below 64 tokens per SM), else route + count, scan, rank,
+    # gather; then GEMM1, GEMM2 and the finalize or combine kernel
+    front = 3 if (not sigmoid and fused_route_dispatch(T, E, k, dev)) else 5
+    launches_per_step = front + 2 + 1
     for _ in range(args.warmup):
         step()
         flush.fill_(1)
@@ -374,7 +378,7 @@ def run_ours(args, rank, world, local, dist):
     comb_ms = statistics.mean(stage_ms["combine"])
     eb = x.element_size()
     comb_bytes = A * H * 4 + A * (w.element_size() + 4) + T * H * eb
-    disp_bytes = A * 12 + E * 8 + T * H * eb + A * H * eb + A * H * eb
+    disp_bytes = A * 12 + E * 8 + T * H * eb + A * H * eb     # x read once, x_disp written
     route_bytes = (T * E * logits.element_size() + A * (4 + w.element_size())
                    + (E * 4 if bias is not None else 0))
     hbm = peaks["hbm_gbs"]
@@ -664,6 +668,20 @@ def routing_config(cfg):
     return {"routing": "sigmoid_grouped", "groups": cfg.groups,
             "selected_groups": cfg.selected_groups, "group_top_two": cfg.group_top_two,
             "scale": cfg.scale, "correction_bias_var": cfg.correction_var}
+
+
+def fused_route_dispatch(T, E, k, dev):
+    """Whether moe_forward routes and counts in one kernel: the library does so
+    unless it would route one token per thread (E <= 64, top_k <= 8 and at
+    least 64 tokens per SM), and when E <= 1024 and the chunk counts (chunks x
+    E) fit the 14336 the last CTA scans in shared memory."""
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    A = T * k
+    chunk = 256
+    while chunk < 2048 and chunk < A // (sms * 8):
+        chunk *= 2
+    thread_route = E <= 64 and k <= 8 and T >= sms * 64
+    return not thread_route and E <= 1024 and (A + chunk - 1) // chunk * E <= 14 * 1024
 
 
 def roofline_entry(tflops, gbs, nbytes, flops, peaks, traffic):

@@ -260,10 +260,26 @@ dispatch_gather_kernel(const uint8_t *__restrict__ x, int64_t rows,
 
 }  // namespace
 
+// Workspace: the per-chunk counts [nchunks][E]. The fused routing-and-count
+// path of the one-call forward adds (256-byte aligned) its completion counter.
 size_t dispatch_workspace_bytes(int64_t A, int E)
 {
     if (A <= 0) return 0;
     return (size_t)num_chunks(A) * (size_t)E * sizeof(int);
+}
+
+size_t route_dispatch_workspace_bytes(int64_t A, int E)
+{
+    if (A <= 0) return 0;
+    return (dispatch_workspace_bytes(A, E) + 255) / 256 * 256 + 256;
+}
+
+int64_t dispatch_chunk_len(int64_t A) { return chunk_size(A); }
+
+unsigned *dispatch_done_counter(void *ws, int64_t A, int E)
+{
+    const size_t counts = (size_t)num_chunks(A) * (size_t)E * sizeof(int);
+    return reinterpret_cast<unsigned *>(static_cast<uint8_t *>(ws) + (counts + 255) / 256 * 256);
 }
 
 cudaError_t launch_dispatch(const uint32_t *idx, int64_t T, int top_k, int E, int64_t special,
@@ -286,6 +302,22 @@ cudaError_t launch_dispatch(const uint32_t *idx, int64_t T, int top_k, int E, in
     err = launch_pdl(dispatch_scan_kernel, dim3((unsigned)((E + 31) / 32)), dim3(kScanThreads),
                      0, s, chunk, nchunks, E, counts);
     if (err != cudaSuccess) return err;
+    return launch_dispatch_rank_gather(idx, T, top_k, E, x, xdt, H, counts, offsets, row_of,
+                                       src_of, x_disp, ws, s);
+}
+
+cudaError_t launch_dispatch_rank_gather(const uint32_t *idx, int64_t T, int top_k, int E,
+                                        const void *x, int xdt, int64_t H, const int32_t *counts,
+                                        int32_t *offsets, int32_t *row_of, int32_t *src_of,
+                                        void *x_disp, void *ws, cudaStream_t s)
+{
+    const int64_t A = T * top_k;
+    if (A == 0) return cudaSuccess;
+    const int64_t chunk_len = chunk_size(A);
+    const int64_t nchunks = (A + chunk_len - 1) / chunk_len;
+    int *chunk = static_cast<int *>(ws);
+    const unsigned blocks = (unsigned)((nchunks + kChunkWarps - 1) / kChunkWarps);
+    cudaError_t err = cudaSuccess;
     const size_t rank_bytes = ((size_t)E + 1 + (size_t)kChunkWarps * E) * sizeof(int);
     err = launch_pdl(dispatch_rank_kernel, dim3(blocks), dim3(kRankThreads), rank_bytes, s, idx,
                      A, E, chunk_len, nchunks, (const int *)chunk, (const int32_t *)counts,

@@ -31,6 +31,31 @@ int sigmoid_route_max_groups();
 
 // Dispatch: per-chunk histograms, a scan, a stable rank/scatter, a row gather.
 size_t dispatch_workspace_bytes(int64_t A, int E);
+// Assignments per dispatch chunk; the workspace of launch_route_dispatch
+// (the dispatch workspace and the fused kernel's completion counter after
+// it) and where that counter sits.
+int64_t dispatch_chunk_len(int64_t A);
+size_t route_dispatch_workspace_bytes(int64_t A, int E);
+unsigned *dispatch_done_counter(void *ws, int64_t A, int E);
+// The rank/scatter and the row gather alone, once the workspace holds each
+// chunk's first row inside every expert and counts[] the expert totals.
+cudaError_t launch_dispatch_rank_gather(const uint32_t *idx, int64_t T, int top_k, int E,
+                                        const void *x, int xdt, int64_t H, const int32_t *counts,
+                                        int32_t *offsets, int32_t *row_of, int32_t *src_of,
+                                        void *x_disp, void *ws, cudaStream_t s);
+// Routing fused with the dispatch's chunk counts and their scan (one kernel:
+// each CTA routes the tokens of one assignment chunk and counts them; the
+// last CTA to finish scans the counts), then the rank/scatter and the gather:
+// three launches instead of five. Falls back to launch_route + launch_dispatch
+// where the fused kernel does not apply (one thread per token pays, E > 1024,
+// or more chunk counts than the last CTA scans in shared memory).
+// zeroed_counter: a zero word the caller has cleared on the stream for the
+// kernel's completion count (nullptr: one in ws, cleared here).
+cudaError_t launch_route_dispatch(const void *logits, int ldt, int64_t T, int E, int top_k,
+                                  int renormalize, uint32_t *idx, void *w, const void *x,
+                                  int xdt, int64_t H, int32_t *counts, int32_t *offsets,
+                                  int32_t *row_of, int32_t *src_of, void *x_disp, void *ws,
+                                  unsigned *zeroed_counter, unsigned *status, cudaStream_t s);
 // Expert ids in [E, E + special) are special experts (see CombineExtras):
 // they get no row and are not reported as bad indices.
 cudaError_t launch_dispatch(const uint32_t *idx, int64_t T, int top_k, int E, int64_t special,

@@ -140,6 +140,9 @@ bool fold_combine(int64_t T, int64_t H, int dt)
     return dt != MOE_F32 && (size_t)T * (size_t)H * 4 <= kFoldCombineMaxBytes;
 }
 
+// y_acc's bytes, rounded so the word after it stays aligned
+size_t fold_acc_bytes(int64_t T, int64_t H) { return round_up((size_t)T * (size_t)H * 4, 256); }
+
 struct ForwardLayout {
     size_t idx, w, counts, offsets, row_of, src_of, disp_ws, x_disp, h, out_disp, total;
 };
@@ -157,12 +160,14 @@ ForwardLayout forward_layout(int64_t T, int64_t H, int64_t I, int64_t E, int top
     L.offsets = take((size_t)(E + 1) * 4);
     L.row_of = take(A * 4);
     L.src_of = take(A * 4);
-    L.disp_ws = take(dispatch_workspace_bytes((int64_t)A, (int)E));
+    L.disp_ws = take(route_dispatch_workspace_bytes((int64_t)A, (int)E));
     L.x_disp = take(A * (size_t)H * eb);
     L.h = take(A * (size_t)I * eb);
     // FP32 expert outputs [A, H] for the combine kernel, or y_acc [T, H]
     // when the combine is folded into the second GEMM
-    L.out_disp = take(fold_combine(T, H, dt) ? (size_t)T * (size_t)H * 4 : A * (size_t)H * 4);
+    // (folded: y_acc, then 256 bytes whose first word counts the CTAs of the
+    // fused routing kernel; one memset clears both)
+    L.out_disp = take(fold_combine(T, H, dt) ? fold_acc_bytes(T, H) + 256 : A * (size_t)H * 4);
     L.total = off;
     return L;
 }
@@ -189,8 +194,17 @@ int run_experts(const void *x_disp, const int32_t *offsets, int64_t rows, const 
     return MOE_OK;
 }
 
-// The one-call forward after its routing step: dispatch, experts, combine.
-// route(idx, w, stream) enqueues the routing into the workspace's idx / w.
+// Where the one-call forward's routing and dispatch write.
+struct DispatchOut {
+    int32_t *counts, *offsets, *row_of, *src_of;
+    void *x_disp, *ws;
+    unsigned *zeroed;        // a word already cleared on the stream, or nullptr
+    unsigned *status;
+};
+
+// The one-call forward: route_dispatch(idx, w, d, stream) enqueues the routing
+// into the workspace's idx / w and the dispatch into d; then the experts and
+// the combine.
 template <typename RouteFn>
 int forward_impl(const char *name, const void *x, int dtype, const void *logits,
                  int logits_dtype, const void *gate, const void *up, const void *down,
@@ -226,15 +240,15 @@ int forward_impl(const char *name, const void *x, int dtype, const void *logits,
 
     const bool fused_combine = fold_combine(T, H, dtype);
     cudaError_t err = cudaSuccess;
+    unsigned *zeroed = nullptr;
     if (fused_combine) {
-        err = cudaMemsetAsync(out_disp, 0, (size_t)T * (size_t)H * 4, s);
+        zeroed = reinterpret_cast<unsigned *>(static_cast<uint8_t *>(out_disp) + fold_acc_bytes(T, H));
+        err = cudaMemsetAsync(out_disp, 0, fold_acc_bytes(T, H) + 256, s);
         if (err != cudaSuccess) return cuda_fail(err, "forward/zero");
     }
-    err = route(idx, w, s);
-    if (err != cudaSuccess) return cuda_fail(err, "forward/route");
-    err = launch_dispatch(idx, T, top_k, (int)E, 0, x, dtype, H, counts, offsets, row_of, src_of,
-                          x_disp, ws + L.disp_ws, st, s);
-    if (err != cudaSuccess) return cuda_fail(err, "forward/dispatch");
+    const DispatchOut d{counts, offsets, row_of, src_of, x_disp, ws + L.disp_ws, zeroed, st};
+    err = route(idx, w, d, s);
+    if (err != cudaSuccess) return cuda_fail(err, "forward/route+dispatch");
     if (fused_combine) {
         err = launch_experts_tc_combine(dtype, x_disp, offsets, A, gate, up, down, (int)E, H, I,
                                         h, src_of, w, logits_dtype, top_k,
@@ -512,9 +526,11 @@ int moe_forward(const void *x, int dtype, const void *logits, int logits_dtype, 
 {
     return forward_impl("moe_forward: NULL tensor", x, dtype, logits, logits_dtype, gate, up,
                         down, T, H, I, E, top_k, y, workspace, workspace_bytes, stream,
-                        [&](uint32_t *idx, void *w, cudaStream_t s) {
-                            return launch_route(logits, logits_dtype, T, (int)E, top_k,
-                                                renormalize, idx, w, s);
+                        [&](uint32_t *idx, void *w, const DispatchOut &d, cudaStream_t s) {
+                            return launch_route_dispatch(logits, logits_dtype, T, (int)E, top_k,
+                                                         renormalize, idx, w, x, dtype, H,
+                                                         d.counts, d.offsets, d.row_of, d.src_of,
+                                                         d.x_disp, d.ws, d.zeroed, d.status, s);
                         });
 }
 
@@ -532,10 +548,15 @@ int moe_forward_sigmoid_grouped(const void *x, int dtype, const void *logits, in
     }
     return forward_impl("moe_forward_sigmoid_grouped: NULL tensor", x, dtype, logits,
                         logits_dtype, gate, up, down, T, H, I, E, top_k, y, workspace,
-                        workspace_bytes, stream, [&](uint32_t *idx, void *w, cudaStream_t s) {
-                            return launch_route_sigmoid_grouped(
+                        workspace_bytes, stream,
+                        [&](uint32_t *idx, void *w, const DispatchOut &d, cudaStream_t s) {
+                            cudaError_t err = launch_route_sigmoid_grouped(
                                 logits, logits_dtype, T, (int)E, bias, top_k, groups,
                                 selected_groups, group_top_two, renormalize, scale, idx, w, s);
+                            if (err != cudaSuccess) return err;
+                            return launch_dispatch(idx, T, top_k, (int)E, 0, x, dtype, H,
+                                                   d.counts, d.offsets, d.row_of, d.src_of,
+                                                   d.x_disp, d.ws, d.status, s);
                         });
 }
 

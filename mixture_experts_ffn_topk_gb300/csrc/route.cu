@@ -22,6 +22,8 @@
 // summed in slot order. G is picked so that EPL <= 8 where E allows it.
 #include <limits.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -31,6 +33,10 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kRouteThreads = 256;
+// fused kernel: enough warps for one pass over a chunk's tokens (its
+// per-warp probability rows stay within 32 KiB of static shared memory)
+template <int EPL>
+__host__ __device__ constexpr int route_count_threads() { return EPL >= 32 ? 256 : 512; }
 
 // true if candidate (la, ea) ranks before (lb, eb); ea/eb == INT_MAX is "none".
 __device__ __forceinline__ bool ranks_before(float la, int ea, float lb, int eb)
@@ -56,28 +62,21 @@ __device__ __forceinline__ int group_and(int v)
     return v;
 }
 
+// Routes tokens t0 .. t0 + 32/G - 1 (one per group of G lanes; those past T
+// work on a clamped token and store nothing). Called by the whole warp, so
+// every shuffle sees the full mask. sp: this warp's 32 * EPL floats.
 template <int G, int EPL, int LDT>
-__global__ void __launch_bounds__(kRouteThreads)
-route_kernel(const void *__restrict__ logits, int64_t T, int E, int top_k,
-             int renormalize, uint32_t *__restrict__ idx_out,
-             void *__restrict__ w_out)
+__device__ __forceinline__ void route_group_tokens(const typename Elem<LDT>::T *__restrict__ L,
+                                                   typename Elem<LDT>::T *__restrict__ W,
+                                                   int64_t T, int E, int top_k, int renormalize,
+                                                   uint32_t *__restrict__ idx_out, int64_t t0,
+                                                   float *sp)
 {
     using ET = typename Elem<LDT>::T;
-    const ET *L = static_cast<const ET *>(logits);
-    ET *W = static_cast<ET *>(w_out);
-    constexpr int TPW = 32 / G;                          // tokens per warp
-    // per warp: TPW tokens x (G*EPL >= top_k) selected probabilities
-    __shared__ float sp[kRouteThreads / 32][32 * EPL];
+    (void)sizeof(ET);
     const int lane = (int)lane_id();
     const int r = lane % G, gbase = lane - r;            // lane in group, group's first lane
-    const int64_t slots = (int64_t)gridDim.x * (blockDim.x / 32) * TPW;
-    pdl_wait();
-    pdl_launch_dependents();
-
-    // the loop is uniform across the warp: groups past T work on a clamped
-    // token and store nothing, so every shuffle sees the full warp
-    for (int64_t t0 = ((int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32) * TPW;
-         t0 < T; t0 += slots) {
+    {
         const int64_t t_raw = t0 + lane / G;
         const bool live = t_raw < T;
         const int64_t t = live ? t_raw : T - 1;
@@ -123,7 +122,7 @@ route_kernel(const void *__restrict__ logits, int64_t T, int E, int top_k,
 
         // k rounds of a group argmax; ids go straight to the output, the
         // selected probabilities wait in shared memory for their sum
-        float *pw = sp[threadIdx.x / 32] + (lane / G) * (G * EPL);
+        float *pw = sp + (lane / G) * (G * EPL);
         float z = 0.0f;
         for (int j = 0; j < top_k; ++j) {
             float bl = -INFINITY;
@@ -172,6 +171,30 @@ route_kernel(const void *__restrict__ logits, int64_t T, int E, int top_k,
         }
         __syncwarp();   // pw is reused by the next token of this group
     }
+}
+
+template <int G, int EPL, int LDT>
+__global__ void __launch_bounds__(kRouteThreads)
+route_kernel(const void *__restrict__ logits, int64_t T, int E, int top_k,
+             int renormalize, uint32_t *__restrict__ idx_out,
+             void *__restrict__ w_out)
+{
+    using ET = typename Elem<LDT>::T;
+    const ET *L = static_cast<const ET *>(logits);
+    ET *W = static_cast<ET *>(w_out);
+    constexpr int TPW = 32 / G;                          // tokens per warp
+    // per warp: TPW tokens x (G*EPL >= top_k) selected probabilities
+    __shared__ float sp[kRouteThreads / 32][32 * EPL];
+    const int64_t slots = (int64_t)gridDim.x * (blockDim.x / 32) * TPW;
+    pdl_wait();
+    pdl_launch_dependents();
+
+    // the loop is uniform across the warp: groups past T work on a clamped
+    // token and store nothing, so every shuffle sees the full warp
+    for (int64_t t0 = ((int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32) * TPW;
+         t0 < T; t0 += slots)
+        route_group_tokens<G, EPL, LDT>(L, W, T, E, top_k, renormalize, idx_out, t0,
+                                        sp[threadIdx.x / 32]);
 }
 
 // ---- one thread per token ----------------------------------------------------
@@ -332,7 +355,148 @@ cudaError_t launch_route_dt(const void *logits, int64_t T, int E, int top_k,
     return launch_route_cfg<32, 32, LDT>(logits, T, E, top_k, renorm, idx, w, s);
 }
 
+// ---- routing fused with the dispatch counts ----------------------------------
+
+// CTA c routes the tokens of assignment chunk c ([c * chunk, (c + 1) * chunk)
+// of the A = T * top_k assignments; a token on a chunk edge is routed by both
+// neighbours, with identical results), counts the chunk's assignments per
+// expert in shared memory and stores the counts in chunk_counts[c][E]. The
+// last CTA to finish (a completion counter it resets afterwards) turns every
+// expert's column of counts into the first row each chunk may use inside the
+// expert and writes the expert totals: what the rank/scatter kernel reads.
+template <int G, int EPL, int LDT>
+__global__ void __launch_bounds__(route_count_threads<EPL>())
+route_count_kernel(const void *__restrict__ logits, int64_t T, int E, int top_k,
+                   int renormalize, uint32_t *__restrict__ idx_out, void *__restrict__ w_out,
+                   int64_t chunk, int64_t nchunks, int *__restrict__ chunk_counts,
+                   int32_t *__restrict__ counts, unsigned *__restrict__ done)
+{
+    using ET = typename Elem<LDT>::T;
+    const ET *L = static_cast<const ET *>(logits);
+    ET *W = static_cast<ET *>(w_out);
+    constexpr int TPW = 32 / G;
+    constexpr int NT = route_count_threads<EPL>();
+    constexpr int WARPS = NT / 32;
+    __shared__ float sp[WARPS][32 * EPL];
+    __shared__ int is_last;
+    extern __shared__ int hist[];                        // [E]
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t A = T * top_k;
+    const int64_t c = blockIdx.x;
+    const int64_t a0 = c * chunk, a1 = a0 + chunk < A ? a0 + chunk : A;
+    const int64_t t_lo = a0 / top_k, t_hi = (a1 - 1) / top_k;
+    const int warp = threadIdx.x / 32;
+    for (int e = threadIdx.x; e < E; e += NT) hist[e] = 0;
+    for (int64_t t0 = t_lo + (int64_t)warp * TPW; t0 <= t_hi; t0 += (int64_t)WARPS * TPW)
+        route_group_tokens<G, EPL, LDT>(L, W, T, E, top_k, renormalize, idx_out, t0, sp[warp]);
+    __syncthreads();         // this CTA's ids (all its chunk's tokens) are written
+    for (int64_t a = a0 + threadIdx.x; a < a1; a += NT) {
+        const uint32_t e = idx_out[a];
+        if (e < (uint32_t)E) atomicAdd(&hist[e], 1);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += NT) chunk_counts[c * E + e] = hist[e];
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) is_last = atomicAdd(done, 1u) == (unsigned)(nchunks - 1);
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    // every CTA's counts into shared memory with all threads' loads in flight
+    // (a column walk in global memory would wait for each load in turn), then
+    // one thread per expert scans its column there
+    int *cc = hist + E;                                // [nchunks][E]
+    const int n = (int)(nchunks * E);
+    for (int i = threadIdx.x; i < n; i += NT) cc[i] = __ldcg(chunk_counts + i);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += NT) {
+        int run = 0;
+        for (int k = 0; k < (int)nchunks; ++k) {
+            const int v = cc[k * E + e];
+            chunk_counts[(int64_t)k * E + e] = run;
+            run += v;
+        }
+        counts[e] = run;
+    }
+    if (threadIdx.x == 0) *done = 0u;                  // ready for the next launch
+}
+
+// Largest nchunks x E the last CTA scans in shared memory (with hist: 56 KiB).
+constexpr int64_t kFusedMaxCounts = 14 * 1024;
+
+template <int G, int EPL, int LDT>
+cudaError_t launch_route_count(const void *logits, int64_t T, int E, int top_k, int renorm,
+                               uint32_t *idx, void *w, int64_t chunk, int64_t nchunks,
+                               int *chunk_counts, int32_t *counts, unsigned *done, cudaStream_t s)
+{
+    const size_t smem = ((size_t)E + (size_t)nchunks * E) * sizeof(int);
+    static std::atomic<uint64_t> opted{0};       // the > 48 KiB opt-in, per device
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (!(opted.load() >> (dev & 63) & 1ull)) {
+        err = cudaFuncSetAttribute(route_count_kernel<G, EPL, LDT>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)((1024 + kFusedMaxCounts) * sizeof(int)));
+        if (err != cudaSuccess) return err;
+        opted.fetch_or(1ull << (dev & 63));
+    }
+    return launch_pdl(route_count_kernel<G, EPL, LDT>, dim3((unsigned)nchunks),
+                      dim3(route_count_threads<EPL>()), smem, s, logits, T, E, top_k, renorm, idx, w, chunk,
+                      nchunks, chunk_counts, counts, done);
+}
+
+template <int LDT>
+cudaError_t launch_route_count_dt(const void *logits, int64_t T, int E, int top_k, int renorm,
+                                  uint32_t *idx, void *w, int64_t chunk, int64_t nchunks,
+                                  int *cc, int32_t *counts, unsigned *done, cudaStream_t s)
+{
+    if (E <= 8) return launch_route_count<1, 8, LDT>(logits, T, E, top_k, renorm, idx, w, chunk, nchunks, cc, counts, done, s);
+    if (E <= 16) return launch_route_count<2, 8, LDT>(logits, T, E, top_k, renorm, idx, w, chunk, nchunks, cc, counts, done, s);
+    if (E <= 32) return launch_route_count<4, 8, LDT>(logits, T, E, top_k, renorm, idx, w, chunk, nchunks, cc, counts, done, s);
+    if (E <= 64) return launch_route_count<8, 8, LDT>(logits, T, E, top_k, renorm, idx, w, chunk, nchunks, cc, counts, done, s);
+    if (E <= 128) return launch_route_count<16, 8, LDT>(logits, T, E, top_k, renorm, idx, w, chunk, nchunks, cc, counts, done, s);
+    if (E <= 256) return launch_route_count<32, 8, LDT>(logits, T, E, top_k, renorm, idx, w, chunk, nchunks, cc, counts, done, s);
+    if (E <= 512) return launch_route_count<32, 16, LDT>(logits, T, E, top_k, renorm, idx, w, chunk, nchunks, cc, counts, done, s);
+    return launch_route_count<32, 32, LDT>(logits, T, E, top_k, renorm, idx, w, chunk, nchunks, cc, counts, done, s);
+}
+
 }  // namespace
+
+cudaError_t launch_route_dispatch(const void *logits, int ldt, int64_t T, int E, int top_k,
+                                  int renormalize, uint32_t *idx, void *w, const void *x,
+                                  int xdt, int64_t H, int32_t *counts, int32_t *offsets,
+                                  int32_t *row_of, int32_t *src_of, void *x_disp, void *ws,
+                                  unsigned *zeroed_counter, unsigned *status, cudaStream_t s)
+{
+    const int64_t A = T * top_k;
+    if (A == 0) return cudaSuccess;
+    const int64_t chunk = dispatch_chunk_len(A);
+    const int64_t nchunks = (A + chunk - 1) / chunk;
+    if (thread_route_fits(T, E, top_k) || nchunks * E > kFusedMaxCounts || E > 1024) {
+        cudaError_t err = launch_route(logits, ldt, T, E, top_k, renormalize, idx, w, s);
+        if (err != cudaSuccess) return err;
+        return launch_dispatch(idx, T, top_k, E, 0, x, xdt, H, counts, offsets, row_of, src_of,
+                               x_disp, ws, status, s);
+    }
+    unsigned *done = zeroed_counter;
+    cudaError_t err = cudaSuccess;
+    if (done == nullptr) {
+        done = dispatch_done_counter(ws, A, E);
+        err = cudaMemsetAsync(done, 0, sizeof(unsigned), s);
+        if (err != cudaSuccess) return err;
+    }
+    int *cc = static_cast<int *>(ws);
+    switch (ldt) {
+    case DT_F32: err = launch_route_count_dt<DT_F32>(logits, T, E, top_k, renormalize, idx, w, chunk, nchunks, cc, counts, done, s); break;
+    case DT_BF16: err = launch_route_count_dt<DT_BF16>(logits, T, E, top_k, renormalize, idx, w, chunk, nchunks, cc, counts, done, s); break;
+    default: err = launch_route_count_dt<DT_F16>(logits, T, E, top_k, renormalize, idx, w, chunk, nchunks, cc, counts, done, s); break;
+    }
+    if (err != cudaSuccess) return err;
+    return launch_dispatch_rank_gather(idx, T, top_k, E, x, xdt, H, counts, offsets, row_of,
+                                       src_of, x_disp, ws, s);
+}
 
 cudaError_t launch_route(const void *logits, int ldt, int64_t T, int E,
                          int top_k, int renormalize, uint32_t *idx, void *w,
