@@ -482,6 +482,38 @@ def test_forward_repeatable_and_stream(dev):
     assert_same_sum(y1, y2, combine_magnitude(out, w, d["row_of"]), cfg.top_k)
 
 
+# The one-call forward's fused routing-and-count kernel on every width it is
+# compiled for (lanes per token 16 / 32, logits per lane 8 / 16 / 32), with
+# dispatch chunks of 256 assignments whose edges split tokens (top_k 3, 6, 7).
+FUSED_FRONT = [
+    cfg_small("fused_e100_bf16", T=300, H=64, I=64, E=100, top_k=3, renormalize=True,
+              dtype="bf16", logits_dtype="bf16"),
+    cfg_small("fused_e300_bf16", T=200, H=64, I=32, E=300, top_k=7, renormalize=False,
+              dtype="bf16", logits_dtype="f32", logit_bias="zipf", bias_param=1.1),
+    cfg_small("fused_e700_f16", T=150, H=32, I=32, E=700, top_k=6, renormalize=True,
+              dtype="f16", logits_dtype="f16"),
+    cfg_small("fused_e1024_bf16", T=120, H=32, I=32, E=1024, top_k=8, renormalize=True,
+              dtype="bf16", logits_dtype="bf16"),
+]
+
+
+@pytest.mark.parametrize("cfg", FUSED_FRONT, ids=lambda c: c.name)
+def test_forward_fused_front_wide_experts(dev, cfg):
+    cpu, g = inputs_on(cfg, dev)
+    o = oracle_inputs(cpu)
+    ref = oracle.forward(o["x"], cfg.dtype, o["logits"], cfg.logits_dtype, o["gate"],
+                         o["up"], o["down"], cfg.top_k, cfg.renormalize)
+    y = moe.moe_forward(g["x"], g["logits"], g["gate"], g["up"], g["down"], cfg.top_k,
+                        cfg.renormalize)
+    torch.cuda.synchronize()
+    assert moe.moe_device_status() == 0
+    assert_close(to_f64(y), ref["y"], cfg.dtype, f"{cfg.name} y")
+    # the standalone routing computes the ids the forward used
+    idx, _ = moe.moe_route(g["logits"], cfg.top_k, cfg.renormalize)
+    torch.cuda.synchronize()
+    assert np.array_equal(idx.cpu().numpy().astype(np.uint32), ref["idx"])
+
+
 @pytest.mark.parametrize("cfg", [SMALL[0], PAIR[0]], ids=lambda c: c.name)
 def test_forward_cuda_graph_replay(dev, cfg):
     """moe_forward captured once in a CUDA graph (its workspace memset, the
