@@ -200,9 +200,13 @@ route_kernel(const void *__restrict__ logits, int64_t T, int E, int top_k,
 // ---- one thread per token ----------------------------------------------------
 
 constexpr int kMaxThreadTopK = 8;
+// one thread per token: 128 threads, so each thread's column of EPL keys
+// stays within 32 KiB of shared memory per block; a compile-time column
+// stride keeps the key addresses immediate offsets
+constexpr int kThreadRouteThreads = 128;
 
 template <int EPL, int LDT>
-__global__ void __launch_bounds__(kRouteThreads)
+__global__ void __launch_bounds__(kThreadRouteThreads)
 route_thread_kernel(const void *__restrict__ logits, int64_t T, int E, int top_k,
                     int renormalize, int vec_rows, uint32_t *__restrict__ idx_out,
                     void *__restrict__ w_out)
@@ -212,6 +216,7 @@ route_thread_kernel(const void *__restrict__ logits, int64_t T, int E, int top_k
     static_assert(EPL % VEC == 0, "rows are read in 16-byte pieces");
     const ET *L = static_cast<const ET *>(logits);
     ET *W = static_cast<ET *>(w_out);
+    extern __shared__ uint32_t keys[];               // [EPL][kThreadRouteThreads]
     pdl_wait();
     pdl_launch_dependents();
     for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < T;
@@ -263,7 +268,35 @@ route_thread_kernel(const void *__restrict__ logits, int64_t T, int E, int top_k
             if (i < E) s += exp2f((l[i] - m) * kLog2e);
         const float inv_s = 1.0f / s;
 
-        uint64_t avail = E >= 64 ? ~0ull : ((1ull << E) - 1ull);
+        // Selection on order-preserving integer keys of the logits (a larger
+        // key is a larger logit; -inf is 0x007fffff, so 0 marks a taken or
+        // absent expert; NaN and +inf rows are invalid and never reach here).
+        // The keys sit in this thread's column of shared memory, the best key
+        // of each group of 8 experts in registers: a round compares the group
+        // bests, takes the winner, and rescans only the winner's group. Every
+        // scan runs in ascending id with a strict '>', so among equal logits
+        // the lower id wins.
+        constexpr int NG = EPL / 8;
+        uint32_t *col = keys + threadIdx.x;          // key i at col[i * kThreadRouteThreads]
+        uint32_t gk[NG];
+        int gi[NG];
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+            gk[g] = 0u;
+            gi[g] = g * 8;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int i = g * 8 + q;
+                uint32_t key = 0u;
+                if (i < E) {
+                    // -0 and +0 are equal logits: one key, so the lower id wins
+                    const uint32_t b = l[i] == 0.0f ? 0u : __float_as_uint(l[i]);
+                    key = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+                }
+                col[i * kThreadRouteThreads] = key;
+                if (key > gk[g]) { gk[g] = key; gi[g] = i; }
+            }
+        }
         float p[kMaxThreadTopK];
         int id[kMaxThreadTopK];
         float z = 0.0f;
@@ -271,21 +304,28 @@ route_thread_kernel(const void *__restrict__ logits, int64_t T, int E, int top_k
         for (int j = 0; j < kMaxThreadTopK; ++j) {
             p[j] = 0.0f;
             id[j] = j;
-            if (j < top_k) {
-                float bl = -INFINITY;
-                int be = -1;
+            if (j < top_k && !invalid) {
+                uint32_t bk = gk[0];
+                int bi = gi[0], bg = 0;
 #pragma unroll
-                for (int i = 0; i < EPL; ++i)
-                    if ((avail >> i & 1ull) && (be < 0 || l[i] > bl)) {
-                        bl = l[i];
-                        be = i;
-                    }
-                if (be >= 0) {
-                    avail &= ~(1ull << be);
-                    id[j] = be;
-                    p[j] = exp2f((bl - m) * kLog2e) * inv_s;
-                    z += p[j];
+                for (int g = 1; g < NG; ++g)
+                    if (gk[g] > bk) { bk = gk[g]; bi = gi[g]; bg = g; }
+                id[j] = bi;
+                const uint32_t lb = (bk & 0x80000000u) ? (bk & 0x7fffffffu) : ~bk;
+                p[j] = exp2f((__uint_as_float(lb) - m) * kLog2e) * inv_s;
+                z += p[j];
+                // take it, and rescan its group
+                col[bi * kThreadRouteThreads] = 0u;
+                uint32_t nk = 0u;
+                int ni = bg * 8;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const uint32_t key = col[(bg * 8 + q) * kThreadRouteThreads];
+                    if (key > nk) { nk = key; ni = bg * 8 + q; }
                 }
+#pragma unroll
+                for (int g = 0; g < NG; ++g)
+                    if (g == bg) { gk[g] = nk; gi[g] = ni; }
             }
         }
 #pragma unroll
@@ -310,11 +350,13 @@ cudaError_t launch_route_thread(const void *logits, int64_t T, int E, int top_k,
     using ET = typename Elem<LDT>::T;
     const int vec_rows = ((int64_t)E * (int64_t)sizeof(ET)) % 16 == 0 &&
                          reinterpret_cast<uintptr_t>(logits) % 16 == 0;
-    int64_t blocks = (T + kRouteThreads - 1) / kRouteThreads;
-    const int64_t cap = (int64_t)device_sm_count() * 8;
+    constexpr int kThreads = kThreadRouteThreads;
+    int64_t blocks = (T + kThreads - 1) / kThreads;
+    const int64_t cap = (int64_t)device_sm_count() * 16;
     if (blocks > cap) blocks = cap;
-    return launch_pdl(route_thread_kernel<EPL, LDT>, dim3((unsigned)blocks), dim3(kRouteThreads),
-                      0, s, logits, T, E, top_k, renorm, vec_rows, idx, w);
+    return launch_pdl(route_thread_kernel<EPL, LDT>, dim3((unsigned)blocks), dim3(kThreads),
+                      (size_t)EPL * kThreads * sizeof(uint32_t), s, logits, T, E, top_k, renorm,
+                      vec_rows, idx, w);
 }
 
 // One thread per token once there are at least two warps of tokens per SM.
