@@ -150,7 +150,7 @@ int moe_route_sigmoid_grouped(const void *logits, int logits_dtype, int64_t T, i
  *   workspace       moe_dispatch_workspace_size(T, top_k, E) bytes.
  *
  * Rows inside one expert's segment follow the assignment order t*top_k + j
- * (the pages leave this order unspecified; this build makes it
+ * (the pages leave this order unspecified; the library makes it
  * deterministic). An index >= E gets no row: row_of = -1, the status word
  * records MOE_ERR_BAD_INDEX, src_of/x_disp rows past offsets[E] are -1 /
  * untouched. Errors: MOE_ERR_NULL, MOE_ERR_SHAPE, MOE_ERR_DTYPE,
