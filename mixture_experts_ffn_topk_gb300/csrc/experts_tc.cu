@@ -43,6 +43,14 @@
 // next expert (or are TMA zero-fill past the last row); they are computed and
 // not stored. TMA zero-fills the K and N edges.
 //
+// In the one-call forward GEMM2 does not wait for GEMM1 as a whole: GEMM1's
+// epilogue warps count each stored tile of h in a per-expert counter (after a
+// memory fence), and GEMM2's producers wait, before their first load of an
+// expert, until its counter covers all of the expert's tiles (acquire, then a
+// generic-to-async proxy fence for the TMA reads). GEMM2's CTAs take the SMs
+// that GEMM1's persistent CTAs leave, so they work on finished experts during
+// GEMM1's last, partly filled round of units.
+//
 // Every wait is bounded (kWaitLimitNs); on expiry the kernel sets ST_TIMEOUT,
 // stops issuing work, drains its own TMA copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
@@ -99,6 +107,13 @@ struct CombineInto {
     int wdt;
     int top_k;
     float *g_out, *u_out;
+    // Per-expert readiness of h (nullptr: off). GEMM1's epilogue warps add 1
+    // to ready[e] after storing each tile of expert e; GEMM2 does not wait
+    // for GEMM1 as a whole but, before its first load of expert e, until
+    // ready[e] counts all of that expert's tiles (nt1 n-tiles per m-unit,
+    // 4 warps per CTA): it starts on finished experts during GEMM1's tail.
+    unsigned *ready;
+    int nt1;
 };
 
 template <int CG>
@@ -157,6 +172,41 @@ __device__ __forceinline__ int unit_row0(int j, int rank, bool half)
 }
 
 
+// load_as_float through L2 (see the offsets load in the kernel's prologue)
+__device__ __forceinline__ float load_as_float_cg(const void *p, int dt, int64_t i)
+{
+    if (dt == DT_F32) return __ldcg(static_cast<const float *>(p) + i);
+    const unsigned short b = __ldcg(static_cast<const unsigned short *>(p) + i);
+    return dt == DT_BF16 ? __uint_as_float((uint32_t)b << 16)
+                         : __half2float(__ushort_as_half(b));
+}
+
+// Bounded wait until *c >= need (acquire at GPU scope); false on abort or
+// timeout (which sets ST_TIMEOUT and raises the abort flag).
+__device__ __forceinline__ bool wait_counter(const unsigned *c, unsigned need,
+                                             volatile int *abort_flag, unsigned *status,
+                                             uint64_t limit_ns)
+{
+    auto load = [&] {
+        unsigned v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
+        return v;
+    };
+    if (load() >= need) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        if (load() >= need) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > limit_ns) {
+            atomicOr(status, ST_TIMEOUT);
+            *abort_flag = 1;
+            return false;
+        }
+        __nanosleep(100);
+    }
+}
+
+
 // ---- the kernel -------------------------------------------------------------
 
 template <int DT, bool SWIGLU, int OUT, int CG>
@@ -198,9 +248,13 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     }
     // everything above is CTA-local; the offsets and operands come from the
     // previous kernels on the stream
-    pdl_wait();
+    // GEMM2 with per-expert readiness waits per expert instead (below);
+    // everything else it reads was complete before GEMM1 let it launch
+    if (SWIGLU || comb.ready == nullptr) pdl_wait();
     pdl_launch_dependents();
-    for (int i = threadIdx.x; i <= E; i += THREADS) S.offs[i] = offsets[i];
+    // read through L2 (GEMM2 with per-expert readiness runs without the
+    // grid-level wait, so no line may come from a stale L1)
+    for (int i = threadIdx.x; i <= E; i += THREADS) S.offs[i] = __ldcg(offsets + i);
     __syncthreads();
     if (warp == 0) {
         // prefix[e] = tiles of experts < e; lane l owns a contiguous run of experts
@@ -239,12 +293,21 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         // ------------------------------------------------------ TMA producer
         int stage = 0;
         uint32_t phase = 0;
+        int ready_e = -1;                        // last expert found ready
         for (int tile = unit0; tile < total_tiles; tile += unit_step) {
             int e, n, j;
             bool half;
             decode_unit<CG>(S, E, tile, e, n, j, half);
             const int row0 = S.offs[e] + unit_row0<CG>(j, rank, half);
             bool ok = true;
+            if (!SWIGLU && comb.ready != nullptr && e != ready_e) {
+                const unsigned need = (unsigned)(m_units<CG>(S.offs[e + 1] - S.offs[e]) * comb.nt1 * 4 * CG);
+                if (!wait_counter(comb.ready + e, need, abort_flag, status, kWaitLimitNs)) break;
+                // the h tiles were written through the generic proxy; the TMA
+                // reads below go through the async proxy
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                ready_e = e;
+            }
             for (int kb = 0; kb < num_kb; ++kb) {
                 if (!mbar_wait<CG>(&S.empty[stage], phase ^ 1u, abort_flag, status, kWaitLimitNs)) { ok = false; break; }
                 uint8_t *sa = S.stage[stage];
@@ -370,9 +433,9 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             float row_w = 0.0f;
             if constexpr (OUT == kOutCombine) {
                 if (r_base + lane < seg_rows) {
-                    const int a = comb.src_of[S.offs[e] + r_base + lane];
+                    const int a = __ldcg(comb.src_of + S.offs[e] + r_base + lane);
                     row_tok = a / comb.top_k;
-                    row_w = load_as_float(comb.w, comb.wdt, a);
+                    row_w = load_as_float_cg(comb.w, comb.wdt, a);
                 }
             }
             const int acc = it & 1;
@@ -481,6 +544,12 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                     }
                 }
                 __syncwarp();
+            }
+            if (SWIGLU && comb.ready != nullptr) {
+                // this warp's h rows of the tile are stored: publish them
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) atomicAdd(comb.ready + e, 1u);
             }
             tc_fence_before();
             __syncwarp();
@@ -683,7 +752,7 @@ cudaError_t launch_experts_tc(int dt, const void *x_disp, const int32_t *offsets
                               cudaStream_t s)
 {
     if (rows == 0) return cudaSuccess;
-    const CombineInto none{nullptr, nullptr, DT_F32, 1, nullptr, nullptr};
+    const CombineInto none{nullptr, nullptr, DT_F32, 1, nullptr, nullptr, nullptr, 0};
     const int mode = out_f32 ? kOutF32 : kOutDtype;
     if (dt == DT_BF16)
         return launch_tc_dt<DT_BF16>(x_disp, offsets, rows, gate, up, down, E, H, I, h_ws,
@@ -702,7 +771,7 @@ cudaError_t launch_experts_tc_training(int dt, const void *x_disp, const int32_t
     // cache: h [rows, I] in dt, then g and u [rows, I] in FP32
     uint8_t *c = static_cast<uint8_t *>(cache);
     float *g = reinterpret_cast<float *>(c + rows * I * 2);
-    const CombineInto save{nullptr, nullptr, DT_F32, 1, g, g + rows * I};
+    const CombineInto save{nullptr, nullptr, DT_F32, 1, g, g + rows * I, nullptr, 0};
     const int mode = out_f32 ? kOutF32 : kOutDtype;
     if (dt == DT_BF16)
         return launch_tc_dt<DT_BF16>(x_disp, offsets, rows, gate, up, down, E, H, I, cache,
@@ -715,11 +784,12 @@ cudaError_t launch_experts_tc_combine(int dt, const void *x_disp, const int32_t 
                                       int64_t rows, const void *gate, const void *up,
                                       const void *down, int E, int64_t H, int64_t I,
                                       void *h_ws, const int32_t *src_of, const void *w,
-                                      int wdt, int top_k, float *y_acc, unsigned *status,
-                                      cudaStream_t s)
+                                      int wdt, int top_k, float *y_acc, unsigned *ready,
+                                      unsigned *status, cudaStream_t s)
 {
     if (rows == 0) return cudaSuccess;
-    const CombineInto comb{src_of, w, wdt, top_k, nullptr, nullptr};
+    const CombineInto comb{src_of, w, wdt, top_k, nullptr, nullptr, ready,
+                           (int)((I + BN / 2 - 1) / (BN / 2))};
     if (dt == DT_BF16)
         return launch_tc_dt<DT_BF16>(x_disp, offsets, rows, gate, up, down, E, H, I, h_ws,
                                      y_acc, kOutCombine, comb, status, s);

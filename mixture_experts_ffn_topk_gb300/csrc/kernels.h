@@ -147,14 +147,17 @@ cudaError_t launch_experts_tc(int dt, const void *x_disp,
 
 // Same GEMMs, with the weighted combine folded into GEMM2: every dispatched
 // row r adds w[src_of[r]] * out_r into y_acc[src_of[r] / top_k] (FP32 [T, H],
-// zeroed by the caller), in an order that varies from run to run.
+// zeroed by the caller), in an order that varies from run to run. ready: E
+// zeroed per-expert counters through which GEMM2 starts on each expert as
+// soon as GEMM1 has stored its h rows (nullptr: GEMM2 waits for all of GEMM1).
 cudaError_t launch_experts_tc_combine(int dt, const void *x_disp,
                                       const int32_t *offsets, int64_t rows,
                                       const void *gate, const void *up,
                                       const void *down, int E, int64_t H, int64_t I,
                                       void *h_ws, const int32_t *src_of,
                                       const void *w, int wdt, int top_k,
-                                      float *y_acc, unsigned *status, cudaStream_t s);
+                                      float *y_acc, unsigned *ready, unsigned *status,
+                                      cudaStream_t s);
 
 // Training forward: launch_experts_tc with g and u kept. cache holds h, g, u
 // as three [rows, I] arrays of dt (h feeds the second GEMM).

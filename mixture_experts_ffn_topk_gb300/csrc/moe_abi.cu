@@ -166,8 +166,10 @@ ForwardLayout forward_layout(int64_t T, int64_t H, int64_t I, int64_t E, int top
     // FP32 expert outputs [A, H] for the combine kernel, or y_acc [T, H]
     // when the combine is folded into the second GEMM
     // (folded: y_acc, then 256 bytes whose first word counts the CTAs of the
-    // fused routing kernel; one memset clears both)
-    L.out_disp = take(fold_combine(T, H, dt) ? fold_acc_bytes(T, H) + 256 : A * (size_t)H * 4);
+    // fused routing kernel, then the experts' h-readiness counters [E]; one
+    // memset clears them all)
+    L.out_disp = take(fold_combine(T, H, dt) ? fold_acc_bytes(T, H) + 256 + round_up((size_t)E * 4, 256)
+                                             : A * (size_t)H * 4);
     L.total = off;
     return L;
 }
@@ -240,10 +242,12 @@ int forward_impl(const char *name, const void *x, int dtype, const void *logits,
 
     const bool fused_combine = fold_combine(T, H, dtype);
     cudaError_t err = cudaSuccess;
-    unsigned *zeroed = nullptr;
+    unsigned *zeroed = nullptr, *ready = nullptr;
     if (fused_combine) {
-        zeroed = reinterpret_cast<unsigned *>(static_cast<uint8_t *>(out_disp) + fold_acc_bytes(T, H));
-        err = cudaMemsetAsync(out_disp, 0, fold_acc_bytes(T, H) + 256, s);
+        uint8_t *tail = static_cast<uint8_t *>(out_disp) + fold_acc_bytes(T, H);
+        zeroed = reinterpret_cast<unsigned *>(tail);
+        ready = reinterpret_cast<unsigned *>(tail + 256);
+        err = cudaMemsetAsync(out_disp, 0, fold_acc_bytes(T, H) + 256 + round_up((size_t)E * 4, 256), s);
         if (err != cudaSuccess) return cuda_fail(err, "forward/zero");
     }
     const DispatchOut d{counts, offsets, row_of, src_of, x_disp, ws + L.disp_ws, zeroed, st};
@@ -252,7 +256,7 @@ int forward_impl(const char *name, const void *x, int dtype, const void *logits,
     if (fused_combine) {
         err = launch_experts_tc_combine(dtype, x_disp, offsets, A, gate, up, down, (int)E, H, I,
                                         h, src_of, w, logits_dtype, top_k,
-                                        static_cast<float *>(out_disp), st, s);
+                                        static_cast<float *>(out_disp), ready, st, s);
         if (err == cudaErrorInvalidValue)
             return fail(MOE_ERR_ALIGN, "TMA descriptor rejected (pointer alignment or shape)");
         if (err != cudaSuccess) return cuda_fail(err, "forward/experts");
