@@ -497,6 +497,29 @@ FUSED_FRONT = [
 ]
 
 
+# The smallest batches: one token, and three tokens over 16 experts (one
+# dispatch chunk; most experts get no rows, so GEMM2 starts on few experts).
+TINY_BATCH = [
+    cfg_small("one_token_bf16", T=1, H=64, I=64, E=4, top_k=2, renormalize=True,
+              dtype="bf16", logits_dtype="bf16"),
+    cfg_small("three_tokens_f16", T=3, H=128, I=96, E=16, top_k=4, renormalize=False,
+              dtype="f16", logits_dtype="f32"),
+]
+
+
+@pytest.mark.parametrize("cfg", TINY_BATCH, ids=lambda c: c.name)
+def test_forward_tiny_batches(dev, cfg):
+    cpu, g = inputs_on(cfg, dev)
+    o = oracle_inputs(cpu)
+    ref = oracle.forward(o["x"], cfg.dtype, o["logits"], cfg.logits_dtype, o["gate"],
+                         o["up"], o["down"], cfg.top_k, cfg.renormalize)
+    y = moe.moe_forward(g["x"], g["logits"], g["gate"], g["up"], g["down"], cfg.top_k,
+                        cfg.renormalize)
+    torch.cuda.synchronize()
+    assert moe.moe_device_status() == 0
+    assert_close(to_f64(y), ref["y"], cfg.dtype, f"{cfg.name} y")
+
+
 @pytest.mark.parametrize("cfg", FUSED_FRONT, ids=lambda c: c.name)
 def test_forward_fused_front_wide_experts(dev, cfg):
     cpu, g = inputs_on(cfg, dev)
