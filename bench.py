@@ -2,9 +2,10 @@
 """Benchmark of the GB300 local MoE FFN forward.
 
 One step = one pass of the whole path (route -> dispatch -> SwiGLU experts
--> combine) over one batch of the fine-grained prefill workload (T=4096
-tokens, H=2048, I=1408, E=64 experts, top_k=6, BF16) with inputs resident in
-HBM. Prints ONE JSON line (rank 0).
+-> combine) through the one-call ``moe_forward`` over one batch of the
+coarse-grained prefill workload (T=16384 tokens, H=4096, I=14336, E=8
+experts, top_k=2, BF16; the largest single-GPU workload) with inputs
+resident in HBM. Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload NAME]
@@ -13,14 +14,19 @@ HBM. Prints ONE JSON line (rank 0).
   events on the launching stream, L2 flushed (256 MiB write) between steps.
 * ``e2e``: the same metric through the one-call C ABI (``moe_forward``) with
   pinned HOST buffers: each step copies x and logits in and y out.
-* ``roofline``: the expert grouped GEMM (the dominant kernels), algorithmic
-  FLOPs (6*H*I per assignment) over its measured duration, against the
-  measured dense BF16 peak; ``kernels`` gives every stage.
+* ``roofline``: the expert grouped GEMM (GEMM1 + GEMM2, the dominant
+  kernels) inside the same one-call forward, timed by events recorded around
+  its two launches (``moe_forward_ex``), with algorithmic FLOPs (6*H*I per
+  assignment) and bytes (touched weights, x_disp, h twice, expert outputs)
+  against the measured peak of the roof its intensity hits; ``kernels``
+  gives every stage.
 * ``cpu_baseline`` (rank 0, N=1): the CPU oracle on a bounded token sample.
 * ``--impl reference``: the CPU oracle as the reference arm (rank 0 only).
 
-Multi-GPU (torchrun): every rank runs an independent replica on its own GPU
-(no collective on the data path); the step time is the max over ranks.
+Multi-GPU: every rank runs an independent replica on its own GPU (no
+collective on the data path); the step time is the max over ranks. Under
+torchrun each process is one rank; ``--gpus N`` without torchrun relaunches
+this script under torch.distributed.run with N ranks.
 """
 
 from __future__ import annotations
@@ -225,63 +231,37 @@ def run_ours(args, rank, world, local, dist):
     T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.top_k
     A = T * k
     x, logits = d["x"], d["logits"]
-    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
-    w = torch.empty((T, k), dtype=logits.dtype, device=dev)
-    counts = torch.empty(E, dtype=torch.int32, device=dev)
-    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
-    row_of = torch.empty(A, dtype=torch.int32, device=dev)
-    src_of = torch.empty(A, dtype=torch.int32, device=dev)
-    x_disp = torch.empty((A, H), dtype=x.dtype, device=dev)
-    out_disp = torch.empty((A, H), dtype=torch.float32, device=dev)   # unrounded
     y = torch.empty((T, H), dtype=x.dtype, device=dev)
-    ws_d = torch.empty(max(1, moe.moe_dispatch_workspace_size(T, k, E)), dtype=torch.uint8,
-                       device=dev)
-    ws_e = torch.empty(moe.moe_experts_workspace_size(A, E, H, I, x.dtype),
-                       dtype=torch.uint8, device=dev)
-    ws_f = torch.empty(moe.moe_forward_workspace_size(T, H, I, E, k, x.dtype, logits.dtype),
-                       dtype=torch.uint8, device=dev)
+    lay = moe.moe_forward_workspace_layout(T, H, I, E, k, x.dtype, logits.dtype)
+    ws_f = torch.empty(lay["total"], dtype=torch.uint8, device=dev)
 
     sigmoid = cfg.routing == "sigmoid_grouped"
     bias = d.get("bias")
+    sg = ({"bias": bias, "groups": cfg.groups, "selected_groups": cfg.selected_groups,
+           "group_top_two": cfg.group_top_two, "scale": cfg.scale} if sigmoid else None)
 
-    def route_into(lg):
-        if sigmoid:
-            moe.moe_route_sigmoid_grouped(lg, bias, k, cfg.groups, cfg.selected_groups,
-                                          cfg.group_top_two, cfg.renormalize, cfg.scale,
-                                          expert_indices=idx, weights=w)
-        else:
-            moe.moe_route(lg, k, cfg.renormalize, expert_indices=idx, weights=w)
-
-    def forward(x_, lg):
-        if sigmoid:
+    def forward(x_, lg, y_, ev=None):
+        # the one-call forward; with ev = (begin, end) the same call records
+        # events right before the first and right after the last expert GEMM
+        if ev is not None:
+            moe.moe_forward_ex(x_, lg, d["gate"], d["up"], d["down"], k, cfg.renormalize,
+                               sigmoid_grouped=sg, experts_begin_event=ev[0],
+                               experts_end_event=ev[1], y=y_, workspace=ws_f)
+        elif sigmoid:
             moe.moe_forward_sigmoid_grouped(x_, lg, bias, d["gate"], d["up"], d["down"], k,
                                             cfg.groups, cfg.selected_groups, cfg.group_top_two,
-                                            cfg.renormalize, cfg.scale, y=y, workspace=ws_f)
+                                            cfg.renormalize, cfg.scale, y=y_, workspace=ws_f)
         else:
             moe.moe_forward(x_, lg, d["gate"], d["up"], d["down"], k, cfg.renormalize,
-                            y=y, workspace=ws_f)
+                            y=y_, workspace=ws_f)
 
-    def step(ev=None):
-        # events only at the step boundaries and around the expert GEMMs: an
-        # event between two kernels stops the next one from starting early
-        if ev: ev[0].record(stream)
-        route_into(logits)
-        moe.moe_dispatch(idx, x, E, counts=counts, offsets=offsets, row_of=row_of,
-                         src_of=src_of, x_disp=x_disp, workspace=ws_d)
-        if ev: ev[1].record(stream)
-        moe.moe_experts_forward(x_disp, offsets, d["gate"], d["up"], d["down"],
-                                out_disp=out_disp, workspace=ws_e)
-        if ev: ev[2].record(stream)
-        moe.moe_combine(out_disp, w, row_of, y=y)
-        if ev: ev[3].record(stream)
-
-    # route + dispatch: one fused route-and-count kernel, rank, gather (softmax
-    # routing at T below 64 tokens per SM), else route + count, scan, rank,
-    # gather; then GEMM1, GEMM2 and the finalize or combine kernel
+    # kernels per forward: the front end (one fused route-and-count kernel,
+    # rank, gather for softmax routing below 64 tokens per SM; else route,
+    # count, scan, rank, gather), GEMM1, GEMM2, then the finalize or combine
     front = 3 if (not sigmoid and fused_route_dispatch(T, E, k, dev)) else 5
     launches_per_step = front + 2 + 1
     for _ in range(args.warmup):
-        step()
+        forward(x, logits, y)
         flush.fill_(1)
     torch.cuda.synchronize(dev)
     if moe.moe_device_status() != 0:
@@ -289,11 +269,6 @@ def run_ours(args, rank, world, local, dist):
 
     # Timed region 1 (the headline): K passes of the one-call forward, events
     # only at step boundaries so every kernel may start early (PDL).
-    def fwd():
-        forward(x, logits)
-    for _ in range(args.warmup):
-        fwd()
-        flush.fill_(1)
     pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
              for _ in range(args.steps)]
     barrier(dist, dev)
@@ -301,7 +276,7 @@ def run_ours(args, rank, world, local, dist):
     with ClockSampler(dev) as clk:
         for a, b in pairs:
             a.record(stream)
-            fwd()
+            forward(x, logits, y)
             b.record(stream)
             flush.fill_(1)   # untimed: between the events of consecutive steps
         torch.cuda.synchronize(dev)
@@ -309,13 +284,31 @@ def run_ours(args, rank, world, local, dist):
     ms = statistics.mean(a.elapsed_time(b) for a, b in pairs)
     ms_max = reduce_max(dist, ms, dev)
     value = aggregate(ms_max / 1e3, T, world)
+    if moe.moe_device_status() != 0:
+        raise RuntimeError("device status error in the timed region")
+
+    # Timed region 2 (the per-stage breakdown and the expert GEMMs' time):
+    # the same one-call forward (moe_forward_ex, same kernels) with events at
+    # the step boundaries and around its two expert GEMM launches.
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev) as clk2:
+        for e4 in evs:
+            e4[0].record(stream)
+            forward(x, logits, y, ev=(e4[1], e4[2]))
+            e4[3].record(stream)
+            flush.fill_(1)
+        torch.cuda.synchronize(dev)
+    stage_ms = {name: statistics.mean(e4[j].elapsed_time(e4[j + 1]) for e4 in evs)
+                for j, name in enumerate(["route+dispatch", "experts", "combine"])}
+    instrumented_ms = statistics.mean(e4[0].elapsed_time(e4[3]) for e4 in evs)
 
     # Timed region 3: the same one-call forward captured once in a CUDA graph
     # (the memset, the kernels and their programmatic-launch edges) and
     # replayed, so no host work sits between steps.
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
-        fwd()
+        forward(x, logits, y)
     for _ in range(args.warmup):
         graph.replay()
         flush.fill_(1)
@@ -329,20 +322,12 @@ def run_ours(args, rank, world, local, dist):
         flush.fill_(1)
     torch.cuda.synchronize(dev)
     graph_ms = reduce_max(dist, statistics.mean(a.elapsed_time(b) for a, b in gpairs), dev)
+    del graph
     if moe.moe_device_status() != 0:
         raise RuntimeError("device status error in the graph replays")
 
-    # Timed region 2 (the per-kernel breakdown): K passes of the staged calls
-    # (same kernels; the combine as its own kernel), events at stage bounds.
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    torch.cuda.synchronize(dev)
-    for i in range(args.steps):
-        step(evs[i])
-        flush.fill_(1)
-    torch.cuda.synchronize(dev)
-    stage_ms = {name: [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)]
-                for j, name in enumerate(["route+dispatch", "experts", "combine"])}
-    staged_ms = statistics.mean(evs[i][0].elapsed_time(evs[i][3]) for i in range(args.steps))
+    # Timed region 4 (end to end): host buffers in, y out, every step.
+    eb = x.element_size()
     x_h = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
     x_h.copy_(x)
     l_h = torch.empty(logits.shape, dtype=logits.dtype, pin_memory=True)
@@ -352,49 +337,41 @@ def run_ours(args, rank, world, local, dist):
     outs_h = [[torch.empty(y.shape, dtype=y.dtype, pin_memory=True)] for _ in range(2)]
 
     def e2e_step(slot):
-        if sigmoid:
-            moe.moe_forward_sigmoid_grouped(ins[slot][0], ins[slot][1], bias, d["gate"], d["up"],
-                                            d["down"], k, cfg.groups, cfg.selected_groups,
-                                            cfg.group_top_two, cfg.renormalize, cfg.scale,
-                                            y=outs[slot][0], workspace=ws_f)
-        else:
-            moe.moe_forward(ins[slot][0], ins[slot][1], d["gate"], d["up"], d["down"], k,
-                            cfg.renormalize, y=outs[slot][0], workspace=ws_f)
+        forward(ins[slot][0], ins[slot][1], outs[slot][0])
     e2e_ms = pipelined_e2e(e2e_step, [x_h, l_h], ins, outs, outs_h, args, dev)
     e2e_ms_max = reduce_max(dist, e2e_ms, dev)
     if moe.moe_device_status() != 0:
         raise RuntimeError("device status error in the timed region")
 
+    # Algorithmic work (per forward): 6*H*I FLOPs per assignment in the two
+    # expert GEMMs; their bytes are the touched experts' weights, x_disp read,
+    # the expert outputs written, and h written and read back.
+    counts = ws_f[lay["counts"]:lay["counts"] + 4 * E].view(torch.int32).cpu()
+    touched = int((counts > 0).sum())
     flops = 6.0 * H * I * A
-    exp_ms = statistics.mean(stage_ms["experts"])
-    achieved = flops / (exp_ms / 1e3) / 1e12
-    # HBM bytes the expert GEMMs must move: weights of the experts that got at
-    # least one token, the dispatched activations, h (written and read back)
-    # and the FP32 expert outputs (read outside the timed region)
-    touched = int((counts.cpu() > 0).sum())
-    exp_bytes = (3 * touched * I * H * x.element_size() + A * H * x.element_size()
-                 + 2 * A * I * x.element_size() + A * H * 4)
-    exp_gbs = exp_bytes / (exp_ms / 1e3) / 1e9
-    comb_ms = statistics.mean(stage_ms["combine"])
-    eb = x.element_size()
-    comb_bytes = A * H * 4 + A * (w.element_size() + 4) + T * H * eb
+    lb, wb = logits.element_size(), logits.element_size()
+    gemm_bytes = 3 * touched * I * H * eb + 2 * A * H * eb + 2 * A * I * eb
+    route_bytes = T * E * lb + A * (4 + wb) + (E * 4 if bias is not None else 0)
     disp_bytes = A * 12 + E * 8 + T * H * eb + A * H * eb     # x read once, x_disp written
-    route_bytes = (T * E * logits.element_size() + A * (4 + w.element_size())
-                   + (E * 4 if bias is not None else 0))
+    comb_bytes = A * H * eb + A * (wb + 4) + T * H * eb
+    exp_ms = stage_ms["experts"]
     hbm = peaks["hbm_gbs"]
     kernels = {
-        "route+dispatch": {"ms": statistics.mean(stage_ms["route+dispatch"]),
-                           "bytes": route_bytes + disp_bytes},
-        "experts": {"ms": exp_ms, "flops": flops, "tflops": achieved,
-                    "frac_bf16_peak": achieved / peaks["bf16_tflops"],
-                    "experts_touched": touched, "bytes": exp_bytes, "gbs": exp_gbs,
-                    "frac_hbm": exp_gbs / peaks["hbm_gbs"]},
-        "combine": {"ms": comb_ms, "bytes": comb_bytes},
+        "route+dispatch": {"ms": stage_ms["route+dispatch"], "bytes": route_bytes + disp_bytes},
+        "experts": {"ms": exp_ms, "flops": flops, "bytes": gemm_bytes,
+                    "experts_touched": touched},
+        "combine": {"ms": stage_ms["combine"], "bytes": comb_bytes,
+                    "how": "finalize of the FP32 accumulator the second GEMM reduced into"
+                           if fold_combine(T, H, x) else
+                           "slot-order combine of the FP32 expert outputs"},
     }
-    for kname in ("route+dispatch", "combine"):
-        kk = kernels[kname]
+    for kk in kernels.values():
         kk["gbs"] = kk["bytes"] / (kk["ms"] / 1e3) / 1e9
         kk["frac_hbm"] = kk["gbs"] / hbm
+    kernels["experts"]["tflops"] = flops / (exp_ms / 1e3) / 1e12
+    kernels["experts"]["frac_bf16_peak"] = kernels["experts"]["tflops"] / peaks["bf16_tflops"]
+    kernels["experts"]["frac_bf16_sustained"] = (kernels["experts"]["tflops"]
+                                                 / peaks["bf16_tflops_sustained"])
     traffic = load_traffic(args.workload, "experts")
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -407,26 +384,34 @@ def run_ours(args, rank, world, local, dist):
                         "global_batch": T * world, "parallelism": f"replicas x{world}",
                         "l2": "flushed between steps (256 MiB write)"}, **routing_config(cfg)),
         "e2e": {"value": aggregate(e2e_ms_max / 1e3, T, world), "unit": UNIT,
-                "h2d_bytes_per_step": x.numel() * eb + logits.numel() * logits.element_size(),
+                "h2d_bytes_per_step": x.numel() * eb + logits.numel() * lb,
                 "d2h_bytes_per_step": y.numel() * eb,
                 "how": "moe_forward through the C ABI; per step x and logits copied in from "
                        "pinned host memory and y copied out, double-buffered so the copies "
                        "of neighbouring steps (in and out on separate copy streams) overlap "
-                       "the compute; no L2 flush (each step "
-                       "streams 1.1 GB of expert weights, more than L2)"},
+                       "the compute; no L2 flush (each step streams "
+                       f"{3 * touched * I * H * eb / 1e9:.2f} GB of expert weights, more "
+                       "than L2)"},
         "graph": {"value": aggregate(graph_ms / 1e3, T, world), "unit": UNIT,
                   "ms_per_step": graph_ms,
                   "how": "the same moe_forward captured once in a CUDA graph and replayed; "
                          "L2 flushed between replays"},
-        "staged_ms_per_step": staged_ms,
-        "roofline": roofline_entry(achieved, exp_gbs, exp_bytes, flops, peaks, traffic),
+        "instrumented_ms_per_step": instrumented_ms,
+        "roofline": roofline_entry(flops, gemm_bytes, exp_ms, peaks, traffic),
         "kernels": kernels,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
+        "clocks_breakdown": clk2.summary(),
     }
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, d, args.cpu_seconds)
     return line
+
+
+def fold_combine(T, H, x):
+    """Whether moe_forward folds the combine into the second expert GEMM:
+    BF16/F16 with an FP32 [T, H] accumulator of at most 64 MiB."""
+    return x.dtype != torch.float32 and T * H * 4 <= 64 << 20
 
 
 # Training step workloads: a forward that keeps the backward's cache, then
@@ -684,18 +669,24 @@ def fused_route_dispatch(T, E, k, dev):
     return not thread_route and E <= 1024 and (A + chunk - 1) // chunk * E <= 14 * 1024
 
 
-def roofline_entry(tflops, gbs, nbytes, flops, peaks, traffic):
-    """The expert GEMMs are reported against the roof that binds them: the
-    BF16 tensor peak when the algorithmic FLOPs take longer at peak than the
-    algorithmic bytes at HBM speed (prefill), else HBM (decode, where the
-    touched experts' weights dominate)."""
-    t_tensor = flops / (peaks["bf16_tflops"] * 1e12)
-    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
-    common = {"kernel": "grouped SwiGLU GEMM (GEMM1 + GEMM2)", "traffic": traffic,
-              "algorithmic_bytes": nbytes, "algorithmic_flops": flops}
-    if t_tensor >= t_hbm:
+def roofline_entry(flops, nbytes, ms, peaks, traffic):
+    """The expert GEMMs (GEMM1 + GEMM2 of the one-call forward, timed by
+    events around their launches) against the roof that binds them: their
+    arithmetic intensity (algorithmic FLOPs over algorithmic bytes) against
+    the ridge of the measured peaks decides; the fraction is the achieved
+    rate over that peak."""
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    ai = flops / nbytes
+    tflops = flops / (ms / 1e3) / 1e12
+    gbs = nbytes / (ms / 1e3) / 1e9
+    common = {"kernel": "grouped SwiGLU GEMM (GEMM1 + GEMM2 of moe_forward)",
+              "ms": ms, "algorithmic_flops": flops, "algorithmic_bytes": nbytes,
+              "arithmetic_intensity": ai, "ridge": ridge, "traffic": traffic,
+              "tflops": tflops, "gbs": gbs}
+    if ai >= ridge:
         return dict(common, bound="tensor", achieved=tflops, peak=peaks["bf16_tflops"],
                     unit="TFLOP/s", frac=tflops / peaks["bf16_tflops"],
+                    frac_sustained=tflops / peaks["bf16_tflops_sustained"],
                     peak_source=peaks["source"] + " burst bf16")
     return dict(common, bound="hbm", achieved=gbs, peak=peaks["hbm_gbs"], unit="GB/s",
                 frac=gbs / peaks["hbm_gbs"], peak_source=peaks["source"] + " HBM copy")
@@ -924,16 +915,10 @@ def run_combine_v2(args, rank, world, dist, dev, peaks, flush):
 
 # ---------------------------------------------------------------- CPU oracle
 
-def oracle_token_rate(cfg, host, seconds, max_threads=None):
-    """Oracle throughput (tokens/s) on a bounded token sample, split over
-    host threads (the C oracle releases the GIL through ctypes)."""
-    import concurrent.futures as cf
-    import numpy as np
+def _oracle_runner(cfg, host):
+    """run(tokens): the oracle's whole forward for those tokens, one by one."""
     import oracle
     lib = oracle.load_library()
-    threads = max_threads or os.cpu_count() or 1
-    T = cfg.T
-
     sg = None
     if cfg.routing == "sigmoid_grouped":
         sg = {"bias": host.get("bias"), "groups": cfg.groups,
@@ -944,18 +929,41 @@ def oracle_token_rate(cfg, host, seconds, max_threads=None):
         oracle.forward_tokens(tokens, host["x"], cfg.dtype, host["logits"], cfg.logits_dtype,
                               host["gate"], host["up"], host["down"], cfg.top_k,
                               cfg.renormalize, lib, sigmoid_grouped=sg)
+    return run
+
+
+def oracle_seconds_per_token(run):
+    import numpy as np
+    run(np.array([0]))                       # first touch of the weights
     t0 = time.perf_counter()
-    run(np.array([0]))
-    one = max(time.perf_counter() - t0, 1e-4)
-    n = int(max(threads, min(T, seconds * threads / one)))
+    run(np.array([1]))
+    return max(time.perf_counter() - t0, 1e-4)
+
+
+def oracle_batch(run, tokens, threads):
+    """Wall seconds of the oracle on `tokens`, split over `threads` host
+    threads (the C oracle releases the GIL through ctypes)."""
+    import concurrent.futures as cf
+    import numpy as np
+    chunks = [c for c in np.array_split(tokens, threads) if c.size]
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=len(chunks)) as ex:
+        list(ex.map(run, chunks))
+    return time.perf_counter() - t0
+
+
+def oracle_token_rate(cfg, host, seconds, max_threads=None):
+    """Oracle throughput (tokens/s) on a bounded token sample of about
+    `seconds` of wall time, split over the host's threads."""
+    import numpy as np
+    threads = max_threads or os.cpu_count() or 1
+    run = _oracle_runner(cfg, host)
+    one = oracle_seconds_per_token(run)
+    n = int(max(threads, min(cfg.T, seconds * threads / one)))
     n = max(threads, n // threads * threads)
     rng = np.random.default_rng(cfg.seed)
-    tokens = rng.choice(T, size=min(n, T), replace=False)
-    chunks = np.array_split(tokens, threads)
-    t0 = time.perf_counter()
-    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
-        list(ex.map(run, chunks))
-    wall = time.perf_counter() - t0
+    tokens = rng.choice(cfg.T, size=min(n, cfg.T), replace=False)
+    wall = oracle_batch(run, tokens, threads)
     return tokens.size / wall, tokens.size, threads, wall
 
 
@@ -972,55 +980,102 @@ def cpu_baseline(cfg, d, seconds):
                       f"(route, k experts, combine) in {wall:.1f} s"}
 
 
+REFERENCE_BUDGET_S = 120.0      # wall seconds of oracle work over all steps of the arm
+
+
 def run_reference(args, rank, world):
-    """The CPU oracle as the reference arm: each step is a bounded token
-    sample of the same workload."""
+    """The CPU oracle as the reference arm, on this arm's workload: each of
+    the W + K steps runs the oracle's whole forward on a fresh sample of the
+    same number of tokens (all host threads); ms_per_step is the measured wall
+    time of a step and value its tokens over that time."""
     if rank != 0:
         return None
     import numpy as np
     from mixture_experts_ffn_topk_gb300 import workloads as W
-    cfg = W.CONFIGS[args.workload] if args.workload in W.CONFIGS else W.CONFIGS["fine_prefill_bf16"]
+    if args.workload not in W.CONFIGS:
+        return {"impl": "reference",
+                "unavailable": "the oracle reference arm times the one-call forward workloads "
+                               f"only, not {args.workload}"}
+    cfg = W.CONFIGS[args.workload]
     d = W.moe_inputs(cfg, device="cpu")
     host = host_inputs(cfg, d)
-    per_step = max(1.0, args.cpu_seconds * 4 / max(1, args.steps + args.warmup))
-    for _ in range(args.warmup):
-        oracle_token_rate(cfg, host, per_step / 4)
-    rates, sizes, walls = [], [], []
     threads = os.cpu_count() or 1
-    for _ in range(args.steps):
-        r, n, threads, wall = oracle_token_rate(cfg, host, per_step)
-        rates.append(r)
-        sizes.append(n)
-        walls.append(wall)
-    value = sum(sizes) / sum(walls)
-    ms = 1e3 * cfg.T / value
+    run = _oracle_runner(cfg, host)
+    one = oracle_seconds_per_token(run)
+    per_step = min(6.0, max(0.5, REFERENCE_BUDGET_S / (args.steps + args.warmup)))
+    n = int(max(threads, min(cfg.T, per_step * threads / one)))
+    n = max(threads, n // threads * threads)
+    rng = np.random.default_rng(cfg.seed)
+    for _ in range(args.warmup):
+        oracle_batch(run, rng.choice(cfg.T, size=n, replace=False), threads)
+    walls = [oracle_batch(run, rng.choice(cfg.T, size=n, replace=False), threads)
+             for _ in range(args.steps)]
+    ms = 1e3 * statistics.mean(walls)
+    value = n / (ms / 1e3)
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": cfg.dtype, "data": "synthetic (seeded; random-init expert weights)",
             "config": dict({"workload": cfg.name, "T": cfg.T, "H": cfg.H, "I": cfg.I,
-                            "E": cfg.E, "top_k": cfg.top_k, "renormalize": cfg.renormalize},
-                           **routing_config(cfg)),
+                            "E": cfg.E, "top_k": cfg.top_k, "renormalize": cfg.renormalize,
+                            "tokens_per_step": n}, **routing_config(cfg)),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                             "sample": f"{sum(sizes)} tokens over {args.steps} steps"},
+                             "sample": f"{n} of the workload's {cfg.T} tokens per step (a "
+                                       f"fresh seeded sample each step), the oracle's whole "
+                                       f"forward per token on {threads} host threads; "
+                                       f"{args.steps} timed steps of {ms / 1e3:.2f} s"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
 
 
+def launch_plan(gpus: int, env) -> str:
+    """How bench.py runs for --gpus N: "single" (N = 1, no process group),
+    "rank" (one rank of a torchrun job of N ranks) or "spawn" (N > 1 without
+    torchrun: relaunch under torch.distributed.run with N ranks). A torchrun
+    job whose WORLD_SIZE is not N is an error."""
+    world = env.get("WORLD_SIZE")
+    if world is not None and int(world) > 1:
+        if int(world) != gpus:
+            raise SystemExit(f"bench.py: --gpus {gpus} but WORLD_SIZE={world}")
+        return "rank"
+    if gpus > 1:
+        return "spawn"
+    if gpus < 1:
+        raise SystemExit("bench.py: --gpus must be >= 1")
+    return "single"
+
+
+def spawn_ranks(gpus: int, argv) -> int:
+    """Run this script as `gpus` ranks of one node (torch.distributed.run on
+    127.0.0.1); returns the launcher's exit status."""
+    import socket
+    import subprocess
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={gpus}", "--master-addr", "127.0.0.1", f"--master-port={port}",
+           os.path.abspath(__file__), *argv]
+    return subprocess.call(cmd)
+
+
 def main(argv=None):
+    argv = list(sys.argv[1:] if argv is None else argv)
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="fine_prefill_bf16")
+    ap.add_argument("--workload", default="coarse_prefill_bf16")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU seconds of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if launch_plan(args.gpus, os.environ) == "spawn":
+        return spawn_ranks(args.gpus, argv)
     rank, world, local, dist = dist_setup(args.gpus)
     if args.impl == "reference":
         line = run_reference(args, rank, world)
@@ -1030,7 +1085,8 @@ def main(argv=None):
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+    return 0
 
 
 if __name__ == "__main__":
-    main()
+    sys.exit(main())

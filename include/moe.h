@@ -69,7 +69,7 @@ typedef enum moe_status {
 /* Human-readable text of a status code; never NULL. */
 const char *moe_status_string(int status);
 
-/* Library ABI version (major * 100 + minor). */
+/* Library ABI version (major * 100 + minor): 101. */
 int moe_abi_version(void);
 
 /* Text describing the last error returned on the calling thread (which
@@ -405,6 +405,87 @@ int moe_forward_sigmoid_grouped(const void *x, int dtype, const void *logits, in
                                 int renormalize, float scale, void *y, void *workspace,
                                 size_t workspace_bytes, void *stream);
 
+/*
+ * moe_forward_ex -- moe_forward / moe_forward_sigmoid_grouped with options.
+ * Same computation, arguments and errors as moe_forward (ruDNN user guide,
+ * section 6, SwiGluExperts::forward), plus:
+ *
+ *   options  NULL, or a moe_forward_options read during the call:
+ *     flags            MOE_FORWARD_* bits; other bits give MOE_ERR_VALUE.
+ *       MOE_FORWARD_DETERMINISTIC  the combine always runs as its own kernel
+ *                      in slot order over FP32 expert outputs (as in the
+ *                      staged calls), so repeated calls on the same inputs
+ *                      give bit-identical y; without it BF16/F16 forwards
+ *                      whose T*H*4 <= 64 MiB fold the combine into the second
+ *                      expert GEMM (see moe_forward). It needs the larger
+ *                      workspace moe_forward_workspace_size_ex(..., flags).
+ *     sigmoid_grouped  NULL: softmax top-k routing (moe_route); else the
+ *                      group-limited sigmoid routing of
+ *                      moe_route_sigmoid_grouped with these arguments (ruDNN
+ *                      user guide, section 10), as moe_forward_sigmoid_grouped.
+ *     experts_begin_event, experts_end_event  NULL, or cudaEvent_t handles
+ *                      recorded on `stream` right before the first and right
+ *                      after the last expert GEMM launch, so a caller can time
+ *                      the expert GEMMs inside the one-call forward. A
+ *                      recorded event stops the kernel after it from starting
+ *                      early, so calls with events run slightly slower.
+ *   workspace  moe_forward_workspace_size_ex(T, H, I, E, top_k, dtype,
+ *              logits_dtype, flags) bytes.
+ */
+#define MOE_FORWARD_DETERMINISTIC 1u
+
+typedef struct moe_sigmoid_grouped_routing {
+    const float *bias;          /* [E] FP32 correction or NULL */
+    int groups;
+    int selected_groups;
+    int group_top_two;
+    float scale;
+} moe_sigmoid_grouped_routing;
+
+typedef struct moe_forward_options {
+    unsigned flags;
+    const moe_sigmoid_grouped_routing *sigmoid_grouped;
+    void *experts_begin_event;
+    void *experts_end_event;
+} moe_forward_options;
+
+size_t moe_forward_workspace_size_ex(int64_t T, int64_t H, int64_t I, int64_t E, int top_k,
+                                     int dtype, int logits_dtype, unsigned flags);
+int moe_forward_ex(const void *x, int dtype, const void *logits, int logits_dtype,
+                   const void *gate, const void *up, const void *down, int64_t T, int64_t H,
+                   int64_t I, int64_t E, int top_k, int renormalize, void *y, void *workspace,
+                   size_t workspace_bytes, const moe_forward_options *options, void *stream);
+
+/*
+ * moe_forward_workspace_layout -- where the one-call forward keeps its
+ * routing plan and dispatch map inside the workspace (ruDNN user guide,
+ * section 5: dispatch produces a saved map that combine and backward reuse).
+ * For the arguments of moe_forward_workspace_size_ex, writes byte offsets
+ * from the workspace start; after a moe_forward / moe_forward_ex call with
+ * these sizes and flags has run, the workspace holds there:
+ *   expert_indices [T, top_k] uint32, weights [T, top_k] in logits_dtype (as
+ *   moe_route or moe_route_sigmoid_grouped write them), counts [E] int32,
+ *   offsets [E + 1] int32, row_of and src_of [T * top_k] int32, x_disp
+ *   [T * top_k, H] in dtype (as moe_dispatch writes them);
+ * total is the workspace size. The layout depends only on the arguments.
+ * Errors: MOE_ERR_NULL (layout), MOE_ERR_SHAPE, MOE_ERR_DTYPE, MOE_ERR_VALUE
+ * (unknown flag).
+ */
+typedef struct moe_forward_layout {
+    size_t expert_indices;
+    size_t weights;
+    size_t counts;
+    size_t offsets;
+    size_t row_of;
+    size_t src_of;
+    size_t x_disp;
+    size_t total;
+} moe_forward_layout;
+
+int moe_forward_workspace_layout(int64_t T, int64_t H, int64_t I, int64_t E, int top_k,
+                                 int dtype, int logits_dtype, unsigned flags,
+                                 moe_forward_layout *layout);
+
 /* ======================================================================
  * First-order training.
  * ruDNN user guide, section 12 "MoE first-order training": the weights of a
@@ -571,6 +652,47 @@ int moe_experts_backward(const void *x_disp, const int32_t *offsets, int64_t row
  * for illegal indices: NaN rows, no out-of-bounds read, no host sync.)
  */
 int moe_device_status(void *stream, int clear);
+
+/*
+ * moe_set_wait_limit_ns -- how long a bounded device wait may last before it
+ * gives up (the error convention of the ruDNN user guide, section 3: a
+ * MoeError instead of a hang). Every spin-wait inside the tcgen05 expert
+ * GEMMs (pipeline barriers, and the per-expert readiness counters of the
+ * one-call forward) stops after this many nanoseconds, records
+ * MOE_ERR_DEVICE_TIMEOUT in the status word, drains its own copies and MMAs
+ * and lets the kernel exit. Process-wide; read when a kernel is launched
+ * (a captured graph keeps the value of its capture). 0 restores the
+ * default of 2 s; more than 60 s gives MOE_ERR_VALUE. Meant for tests of the
+ * failure path, which shorten it so an expiry costs milliseconds.
+ * moe_wait_limit_ns returns the limit in force.
+ */
+int moe_set_wait_limit_ns(uint64_t limit_ns);
+uint64_t moe_wait_limit_ns(void);
+
+/*
+ * moe_selftest_wait_expiry -- runs the failure path of the bounded waits on
+ * the GPU, without a fault. It launches the second expert GEMM of the
+ * one-call forward on its own (BF16, combine folded into y_acc, top_k 1,
+ * E experts of rows_per_expert rows each, all data zero) with per-expert
+ * readiness counters that no first GEMM ever raises: each of its producers
+ * waits the bounded time, gives up, records MOE_ERR_DEVICE_TIMEOUT, and the
+ * kernel drains and exits without touching y_acc. The pages have no
+ * counterpart; it exists so a test can check that a wait that can never be
+ * satisfied ends in a status rather than a hang.
+ *
+ *   y_acc      [E * rows_per_expert, H] FP32 (16-byte aligned): not written.
+ *   workspace  moe_selftest_wait_expiry_workspace_size(...) bytes, 256-byte
+ *              aligned (offsets, map, routing weights, counters, h, down).
+ *   1 <= E <= 1024, 1 <= rows_per_expert <= 4096, H and I multiples of 8 in
+ *   [8, 8192]. Afterwards moe_device_status() reports the timeout.
+ * Errors: MOE_ERR_SHAPE, MOE_ERR_NULL, MOE_ERR_ALIGN, MOE_ERR_WORKSPACE,
+ * MOE_ERR_CUDA.
+ */
+size_t moe_selftest_wait_expiry_workspace_size(int64_t E, int64_t rows_per_expert, int64_t H,
+                                               int64_t I);
+int moe_selftest_wait_expiry(int64_t E, int64_t rows_per_expert, int64_t H, int64_t I,
+                             float *y_acc, void *workspace, size_t workspace_bytes,
+                             void *stream);
 
 #ifdef __cplusplus
 }

@@ -48,7 +48,11 @@ EXPORTED = ["moe_status_string", "moe_abi_version", "moe_last_error_detail",
             "moe_router_weights", "moe_router_backward", "moe_combine_backward",
             "moe_dispatch_backward", "moe_experts_training_cache_size",
             "moe_experts_forward_training", "moe_experts_backward_workspace_size",
-            "moe_experts_backward"]
+            "moe_experts_backward", "moe_forward_workspace_size_ex", "moe_forward_ex",
+            "moe_forward_workspace_layout", "moe_set_wait_limit_ns", "moe_wait_limit_ns",
+            "moe_selftest_wait_expiry_workspace_size", "moe_selftest_wait_expiry"]
+
+MOE_FORWARD_DETERMINISTIC = 1
 
 MOE_SCORING_SOFTMAX, MOE_SCORING_SIGMOID = 0, 1
 SCORING_CODES = {"softmax": MOE_SCORING_SOFTMAX, "sigmoid": MOE_SCORING_SIGMOID}
@@ -71,6 +75,25 @@ class CombineExtras(ctypes.Structure):
                 ("const_alpha1", ctypes.c_void_p), ("const_alpha2", ctypes.c_void_p),
                 ("const_v", ctypes.c_void_p), ("shared_expert_x", ctypes.c_void_p),
                 ("active_mask", ctypes.c_void_p), ("active_mask_dims", ctypes.c_int)]
+
+
+class SigmoidGroupedRouting(ctypes.Structure):
+    """Mirror of ``moe_sigmoid_grouped_routing`` (include/moe.h)."""
+    _fields_ = [("bias", ctypes.c_void_p), ("groups", ctypes.c_int),
+                ("selected_groups", ctypes.c_int), ("group_top_two", ctypes.c_int),
+                ("scale", ctypes.c_float)]
+
+
+class ForwardOptions(ctypes.Structure):
+    """Mirror of ``moe_forward_options`` (include/moe.h)."""
+    _fields_ = [("flags", ctypes.c_uint), ("sigmoid_grouped", ctypes.POINTER(SigmoidGroupedRouting)),
+                ("experts_begin_event", ctypes.c_void_p), ("experts_end_event", ctypes.c_void_p)]
+
+
+class ForwardLayout(ctypes.Structure):
+    """Mirror of ``moe_forward_layout`` (include/moe.h)."""
+    _fields_ = [(n, ctypes.c_size_t) for n in ("expert_indices", "weights", "counts", "offsets",
+                                               "row_of", "src_of", "x_disp", "total")]
 
 
 class MoeError(RuntimeError):
@@ -127,6 +150,16 @@ def _bind(lib):
         "moe_experts_backward_workspace_size": ([_I64, _I64, _I64, _I64, _INT], _SZ),
         "moe_experts_backward": ([_P, _P, _I64, _P, _P, _P, _I64, _I64, _I64, _INT, _P, _P,
                                   _P, _P, _P, _P, _P, _SZ, _P], _INT),
+        "moe_forward_workspace_size_ex": ([_I64, _I64, _I64, _I64, _INT, _INT, _INT,
+                                           ctypes.c_uint], _SZ),
+        "moe_forward_ex": ([_P, _INT, _P, _INT, _P, _P, _P, _I64, _I64, _I64, _I64, _INT, _INT,
+                            _P, _P, _SZ, ctypes.POINTER(ForwardOptions), _P], _INT),
+        "moe_forward_workspace_layout": ([_I64, _I64, _I64, _I64, _INT, _INT, _INT,
+                                          ctypes.c_uint, ctypes.POINTER(ForwardLayout)], _INT),
+        "moe_set_wait_limit_ns": ([ctypes.c_uint64], _INT),
+        "moe_wait_limit_ns": ([], ctypes.c_uint64),
+        "moe_selftest_wait_expiry_workspace_size": ([_I64, _I64, _I64, _I64], _SZ),
+        "moe_selftest_wait_expiry": ([_I64, _I64, _I64, _I64, _P, _P, _SZ, _P], _INT),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -439,9 +472,67 @@ def moe_rmsnorm(x: torch.Tensor, gamma: torch.Tensor, eps: float, y=None, rstd=N
 
 
 def moe_forward_workspace_size(T: int, H: int, I: int, E: int, top_k: int,
-                               dtype: torch.dtype, logits_dtype: torch.dtype) -> int:
-    return int(load_library().moe_forward_workspace_size(
-        T, H, I, E, top_k, _code(dtype), _code(logits_dtype)))
+                               dtype: torch.dtype, logits_dtype: torch.dtype,
+                               deterministic: bool = False) -> int:
+    flags = MOE_FORWARD_DETERMINISTIC if deterministic else 0
+    return int(load_library().moe_forward_workspace_size_ex(
+        T, H, I, E, top_k, _code(dtype), _code(logits_dtype), flags))
+
+
+def moe_forward_workspace_layout(T: int, H: int, I: int, E: int, top_k: int,
+                                 dtype: torch.dtype, logits_dtype: torch.dtype,
+                                 deterministic: bool = False) -> dict:
+    """Byte offsets of the routing plan and dispatch map inside the one-call
+    forward's workspace (``moe_forward_layout``)."""
+    lay = ForwardLayout()
+    flags = MOE_FORWARD_DETERMINISTIC if deterministic else 0
+    rc = load_library().moe_forward_workspace_layout(T, H, I, E, top_k, _code(dtype),
+                                                     _code(logits_dtype), flags,
+                                                     ctypes.byref(lay))
+    _check(rc, "moe_forward_workspace_layout")
+    return {n: int(getattr(lay, n)) for n, _ in ForwardLayout._fields_}
+
+
+def _event_handle(ev) -> ctypes.c_void_p:
+    return ctypes.c_void_p(None) if ev is None else ctypes.c_void_p(ev.cuda_event)
+
+
+def moe_forward_ex(x: torch.Tensor, logits: torch.Tensor, gate: torch.Tensor, up: torch.Tensor,
+                   down: torch.Tensor, top_k: int, renormalize: bool, deterministic: bool = False,
+                   sigmoid_grouped: dict | None = None, experts_begin_event=None,
+                   experts_end_event=None, y=None, workspace=None,
+                   stream=None) -> torch.Tensor:
+    """The whole local forward with ``moe_forward_options``: a deterministic
+    combine, group-limited sigmoid routing (``sigmoid_grouped``: bias, groups,
+    selected_groups, group_top_two, scale) and torch.cuda.Event objects (created
+    with enable_timing) recorded around the expert GEMMs."""
+    T, H = x.shape
+    E, I, _ = gate.shape
+    dev = x.device
+    y = y if y is not None else torch.empty((T, H), dtype=x.dtype, device=dev)
+    ws = _workspace(moe_forward_workspace_size(T, H, I, E, top_k, x.dtype, logits.dtype,
+                                               deterministic), dev, workspace)
+    opt = ForwardOptions()
+    opt.flags = MOE_FORWARD_DETERMINISTIC if deterministic else 0
+    sg = None
+    if sigmoid_grouped is not None:
+        bias = sigmoid_grouped.get("bias")
+        if bias is not None and (bias.dtype != torch.float32 or tuple(bias.shape) != (E,)):
+            raise ValueError("bias must be float32 of shape [E]")
+        sg = SigmoidGroupedRouting(None if bias is None else _ptr(bias).value,
+                                   int(sigmoid_grouped["groups"]),
+                                   int(sigmoid_grouped["selected_groups"]),
+                                   int(bool(sigmoid_grouped["group_top_two"])),
+                                   float(sigmoid_grouped.get("scale", 1.0)))
+        opt.sigmoid_grouped = ctypes.pointer(sg)
+    opt.experts_begin_event = _event_handle(experts_begin_event)
+    opt.experts_end_event = _event_handle(experts_end_event)
+    rc = load_library().moe_forward_ex(
+        _ptr(x), _code(x.dtype), _ptr(logits), _code(logits.dtype), _ptr(gate),
+        _ptr(up), _ptr(down), T, H, I, E, int(top_k), int(bool(renormalize)),
+        _ptr(y), _ptr(ws), _nbytes(ws), ctypes.byref(opt), _stream(stream))
+    _check(rc, "moe_forward_ex")
+    return y
 
 
 def moe_forward(x: torch.Tensor, logits: torch.Tensor, gate: torch.Tensor,
@@ -484,6 +575,26 @@ def moe_forward_sigmoid_grouped(x: torch.Tensor, logits: torch.Tensor, bias: tor
         int(bool(renormalize)), float(scale), _ptr(y), _ptr(ws), _nbytes(ws), _stream(stream))
     _check(rc, "moe_forward_sigmoid_grouped")
     return y
+
+
+def moe_set_wait_limit_ns(limit_ns: int) -> None:
+    """Limit of every bounded device wait (0: the default 2 s)."""
+    _check(load_library().moe_set_wait_limit_ns(int(limit_ns)), "moe_set_wait_limit_ns")
+
+
+def moe_wait_limit_ns() -> int:
+    return int(load_library().moe_wait_limit_ns())
+
+
+def moe_selftest_wait_expiry(E: int, rows_per_expert: int, H: int, I: int,
+                             y_acc: torch.Tensor, workspace=None, stream=None) -> None:
+    """Run the bounded waits' failure path (see include/moe.h)."""
+    lib = load_library()
+    ws = _workspace(int(lib.moe_selftest_wait_expiry_workspace_size(E, rows_per_expert, H, I)),
+                    y_acc.device, workspace)
+    rc = lib.moe_selftest_wait_expiry(E, rows_per_expert, H, I, _ptr(y_acc), _ptr(ws),
+                                      _nbytes(ws), _stream(stream))
+    _check(rc, "moe_selftest_wait_expiry")
 
 
 def moe_device_status(stream=None, clear: bool = True) -> int:

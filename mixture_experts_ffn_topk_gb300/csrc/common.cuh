@@ -117,8 +117,15 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
-// Every spin-wait in this library gives up after this long, sets
-// ST_TIMEOUT in the status word and lets the kernel wind down.
+// Host-side per-device caches (SM counts, symbol addresses, attribute
+// opt-ins) cover device ordinals below this bound; higher ordinals skip the
+// cache and look the value up on every call.
+constexpr int kCachedDevices = 64;
+
+// Every spin-wait in this library gives up after a bounded time (2 s unless
+// moe_set_wait_limit_ns() chose another), sets ST_TIMEOUT in the status word
+// and lets the kernel wind down. Kernels receive the limit as an argument,
+// taken from wait_limit_ns() at launch.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 }  // namespace moe

@@ -51,7 +51,7 @@
 // that GEMM1's persistent CTAs leave, so they work on finished experts during
 // GEMM1's last, partly filled round of units.
 //
-// Every wait is bounded (kWaitLimitNs); on expiry the kernel sets ST_TIMEOUT,
+// Every wait is bounded (wait_ns); on expiry the kernel sets ST_TIMEOUT,
 // stops issuing work, drains its own TMA copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -219,7 +219,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB1h,
                        const int32_t *__restrict__ offsets, int E, int N, int K,
                        int n_tiles, void *__restrict__ out, unsigned *status,
-                       CombineInto comb)
+                       CombineInto comb, uint64_t wait_ns)
 {
     using P = Pipe<CG>;
     constexpr int STAGES = P::STAGES;
@@ -302,14 +302,14 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             bool ok = true;
             if (!SWIGLU && comb.ready != nullptr && e != ready_e) {
                 const unsigned need = (unsigned)(m_units<CG>(S.offs[e + 1] - S.offs[e]) * comb.nt1 * 4 * CG);
-                if (!wait_counter(comb.ready + e, need, abort_flag, status, kWaitLimitNs)) break;
+                if (!wait_counter(comb.ready + e, need, abort_flag, status, wait_ns)) break;
                 // the h tiles were written through the generic proxy; the TMA
                 // reads below go through the async proxy
                 asm volatile("fence.proxy.async.global;" ::: "memory");
                 ready_e = e;
             }
             for (int kb = 0; kb < num_kb; ++kb) {
-                if (!mbar_wait<CG>(&S.empty[stage], phase ^ 1u, abort_flag, status, kWaitLimitNs)) { ok = false; break; }
+                if (!mbar_wait<CG>(&S.empty[stage], phase ^ 1u, abort_flag, status, wait_ns)) { ok = false; break; }
                 uint8_t *sa = S.stage[stage];
                 uint8_t *sb = sa + A_BYTES;
                 if constexpr (CG == 2) {
@@ -371,11 +371,11 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             bool half;
             decode_unit<CG>(S, E, tile, e, n, j, half);
             const uint32_t idesc = half ? idesc_half : idesc_full;
-            if (!mbar_wait<CG>(&S.acc_empty[acc], acc_phase ^ 1u, abort_flag, status, kWaitLimitNs)) { ok = false; break; }
+            if (!mbar_wait<CG>(&S.acc_empty[acc], acc_phase ^ 1u, abort_flag, status, wait_ns)) { ok = false; break; }
             tc_fence_after();
             const uint32_t d = tmem_base + (uint32_t)(acc * ACC_COLS);
             for (int kb = 0; kb < num_kb; ++kb) {
-                if (!mbar_wait<CG>(&S.full[stage], phase, abort_flag, status, kWaitLimitNs)) { ok = false; break; }
+                if (!mbar_wait<CG>(&S.full[stage], phase, abort_flag, status, wait_ns)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t a0 = smem_u32(S.stage[stage]);
                 const uint32_t b0 = a0 + A_BYTES;
@@ -442,7 +442,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
             // every lane waits; the warp leaves together if any lane gave up,
             // since tcgen05.ld below needs the whole warp converged
-            const bool ready = mbar_wait<CG>(&S.acc_full[acc], acc_phase, abort_flag, status, kWaitLimitNs);
+            const bool ready = mbar_wait<CG>(&S.acc_full[acc], acc_phase, abort_flag, status, wait_ns);
             if (!__all_sync(0xffffffffu, ready)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
@@ -562,6 +562,11 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
 
     // ------------------------------------------------------------ teardown
     __syncthreads();
+    // GEMM2 with per-expert readiness skipped the grid-level wait at entry;
+    // waiting here, once its own work is done, restores the usual guarantee
+    // for whatever the stream runs next: when GEMM2 has completed, GEMM1 has
+    // too (its h, counters and every other write are done and visible)
+    if (!SWIGLU && comb.ready != nullptr) pdl_wait();
     if (*abort_flag && warp == 0 && lane == 0) {
         if (CG == 1 || leader) {
             // let the outstanding TMA copies land before shared memory goes
@@ -597,8 +602,8 @@ cudaError_t ensure_smem_attr()
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    const uint64_t bit = 1ull << (dev & 63);
-    if (done_mask.load() & bit) return cudaSuccess;
+    const uint64_t bit = dev >= 0 && dev < kCachedDevices ? 1ull << dev : 0ull;
+    if (bit != 0 && (done_mask.load() & bit)) return cudaSuccess;
     err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<DT, SWIGLU, OUT, CG>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes<CG>);
     if (err == cudaSuccess) done_mask.fetch_or(bit);
@@ -625,11 +630,12 @@ cudaError_t grid_size(int64_t units, int *grid)
         *grid = (int)(units < sms ? units : sms);
         return cudaSuccess;
     } else {
-        static std::atomic<int> cached[64];
+        static std::atomic<int> cached[kCachedDevices];
         int dev = 0;
         cudaError_t err = cudaGetDevice(&dev);
         if (err != cudaSuccess) return err;
-        int pairs = cached[dev & 63].load();
+        const bool use_cache = dev >= 0 && dev < kCachedDevices;
+        int pairs = use_cache ? cached[dev].load() : 0;
         if (pairs == 0) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3((unsigned)(sms & ~int64_t(1)));
@@ -645,19 +651,21 @@ cudaError_t grid_size(int64_t units, int *grid)
             err = cudaOccupancyMaxActiveClusters(&pairs, grouped_gemm_tc_kernel<DT, SWIGLU, OUT, CG>, &cfg);
             if (err != cudaSuccess) return err;
             if (pairs < 1) return cudaErrorInvalidConfiguration;
-            cached[dev & 63].store(pairs);
+            if (use_cache) cached[dev].store(pairs);
         }
         *grid = 2 * (int)(units < pairs ? units : pairs);
         return cudaSuccess;
     }
 }
 
-// Programmatic dependent launch, in clusters of CG CTAs.
+// Programmatic dependent launch (unless pdl is false: plain stream order),
+// in clusters of CG CTAs.
 template <int DT, bool SWIGLU, int OUT, int CG>
 cudaError_t launch_gemm(int64_t units, cudaStream_t s, const CUtensorMap &ta, const CUtensorMap &tah,
                         const CUtensorMap &tb0, const CUtensorMap &tb1, const CUtensorMap &tb0h,
                         const CUtensorMap &tb1h, const int32_t *offsets, int E, int N, int K,
-                        int n_tiles, void *out, unsigned *status, const CombineInto &comb)
+                        int n_tiles, void *out, unsigned *status, const CombineInto &comb,
+                        bool pdl = true)
 {
     cudaError_t err = ensure_smem_attr<DT, SWIGLU, OUT, CG>();
     if (err != cudaSuccess) return err;
@@ -671,7 +679,7 @@ cudaError_t launch_gemm(int64_t units, cudaStream_t s, const CUtensorMap &ta, co
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     attr[1].id = cudaLaunchAttributeClusterDimension;
     attr[1].val.clusterDim.x = CG;
     attr[1].val.clusterDim.y = 1;
@@ -679,7 +687,8 @@ cudaError_t launch_gemm(int64_t units, cudaStream_t s, const CUtensorMap &ta, co
     cfg.attrs = attr;
     cfg.numAttrs = CG == 2 ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<DT, SWIGLU, OUT, CG>, ta, tah, tb0, tb1,
-                              tb0h, tb1h, offsets, E, N, K, n_tiles, out, status, comb);
+                              tb0h, tb1h, offsets, E, N, K, n_tiles, out, status, comb,
+                              wait_limit_ns());
 }
 
 // CTA pairs pay when experts average at least two M-tiles: a pair's second
@@ -730,6 +739,42 @@ cudaError_t launch_tc_cg(const void *x_disp, const int32_t *offsets, int64_t row
                                                  (int)H, (int)I, nt2, out, status, comb);
 }
 
+// GEMM2 of the one-call forward on its own: h [rows, I] times down, each row
+// weighted and reduced into y_acc, starting on expert e once ready[e] counts
+// all of its h tiles (as GEMM1 would publish them).
+template <int DT, int CG>
+cudaError_t launch_down_combine_cg(const int32_t *offsets, int64_t rows, const void *down, int E,
+                                   int64_t H, int64_t I, const void *h, const CombineInto &comb,
+                                   float *y_acc, unsigned *status, cudaStream_t s)
+{
+    const CUtensorMapDataType tdt =
+        DT == DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUtensorMap mh, md;
+    if (!encode_2d(&mh, tdt, h, (uint64_t)I, (uint64_t)rows, BK, BM) ||
+        !encode_3d(&md, tdt, down, (uint64_t)I, (uint64_t)H, (uint64_t)E, BK, BN / CG))
+        return cudaErrorInvalidValue;
+    CUtensorMap mhh = mh;
+    if (CG == 2 && !encode_2d(&mhh, tdt, h, (uint64_t)I, (uint64_t)rows, BK, BM / 2))
+        return cudaErrorInvalidValue;
+    const int nt2 = (int)((H + BN - 1) / BN);
+    // plain stream order: this GEMM reads the offsets before any grid-level
+    // wait, so they must be complete when it starts
+    return launch_gemm<DT, false, kOutCombine, CG>(tc_unit_upper_bound(rows, E, nt2, CG), s, mh,
+                                                   mhh, md, md, md, md, offsets, E, (int)H,
+                                                   (int)I, nt2, y_acc, status, comb, false);
+}
+
+// offsets[e] = e * rows_per_expert (e <= E), src_of[r] = r: the dispatch map
+// of one token per row and top_k = 1
+__global__ void selftest_map_kernel(int32_t *offsets, int32_t *src_of, int E, int rows_per_expert)
+{
+    const int rows = E * rows_per_expert;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i <= rows; i += gridDim.x * blockDim.x) {
+        if (i <= E) offsets[i] = i * rows_per_expert;
+        if (i < rows) src_of[i] = i;
+    }
+}
+
 template <int DT>
 cudaError_t launch_tc_dt(const void *x_disp, const int32_t *offsets, int64_t rows,
                          const void *gate, const void *up, const void *down, int E,
@@ -759,6 +804,47 @@ cudaError_t launch_experts_tc(int dt, const void *x_disp, const int32_t *offsets
                                      out_disp, mode, none, status, s);
     return launch_tc_dt<DT_F16>(x_disp, offsets, rows, gate, up, down, E, H, I, h_ws, out_disp,
                                 mode, none, status, s);
+}
+
+size_t selftest_wait_workspace_bytes(int E, int rows_per_expert, int64_t H, int64_t I)
+{
+    const size_t rows = (size_t)E * (size_t)rows_per_expert;
+    auto r = [](size_t v) { return (v + 255) / 256 * 256; };
+    return r((size_t)(E + 1) * 4) + r(rows * 4) + r(rows * 4) + r((size_t)E * 4) +
+           r(rows * (size_t)I * 2) + r((size_t)E * (size_t)H * (size_t)I * 2);
+}
+
+cudaError_t launch_selftest_wait_expiry(int E, int rows_per_expert, int64_t H, int64_t I,
+                                        void *ws, float *y_acc, unsigned *status, cudaStream_t s)
+{
+    const int64_t rows = (int64_t)E * rows_per_expert;
+    auto r = [](size_t v) { return (v + 255) / 256 * 256; };
+    uint8_t *p = static_cast<uint8_t *>(ws);
+    int32_t *offsets = reinterpret_cast<int32_t *>(p);
+    p += r((size_t)(E + 1) * 4);
+    int32_t *src_of = reinterpret_cast<int32_t *>(p);
+    p += r((size_t)rows * 4);
+    float *w = reinterpret_cast<float *>(p);
+    p += r((size_t)rows * 4);
+    unsigned *ready = reinterpret_cast<unsigned *>(p);
+    p += r((size_t)E * 4);
+    void *h = p;
+    p += r((size_t)rows * (size_t)I * 2);
+    void *down = p;
+    // zero h, the weights, the routing weights and the readiness counters
+    cudaError_t err = cudaMemsetAsync(ws, 0, selftest_wait_workspace_bytes(E, rows_per_expert, H, I), s);
+    if (err != cudaSuccess) return err;
+    selftest_map_kernel<<<(unsigned)((rows + 256) / 256), 256, 0, s>>>(offsets, src_of, E,
+                                                                          rows_per_expert);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    const CombineInto comb{src_of, w, DT_F32, 1, nullptr, nullptr, ready,
+                           (int)((I + BN / 2 - 1) / (BN / 2))};
+    if (rows >= kPairMinRowsPerExpert * E)
+        return launch_down_combine_cg<DT_BF16, 2>(offsets, rows, down, E, H, I, h, comb, y_acc,
+                                                  status, s);
+    return launch_down_combine_cg<DT_BF16, 1>(offsets, rows, down, E, H, I, h, comb, y_acc,
+                                              status, s);
 }
 
 cudaError_t launch_experts_tc_training(int dt, const void *x_disp, const int32_t *offsets,

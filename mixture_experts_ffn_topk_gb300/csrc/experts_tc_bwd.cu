@@ -38,7 +38,7 @@
 // then zero-fills the rows past the segment by itself, and a NaN row of
 // another expert never enters a sum.
 //
-// Every wait is bounded (kWaitLimitNs); on expiry the kernel sets ST_TIMEOUT,
+// Every wait is bounded (p.wait_ns); on expiry the kernel sets ST_TIMEOUT,
 // stops issuing work, drains its own copies and MMAs, frees TMEM and exits.
 #include <atomic>
 
@@ -108,6 +108,7 @@ struct BwdParams {
     const uint8_t *emaps;               // WG: per-expert tensor maps, maps_per_expert each
     int maps_per_expert;                // WG: nprob A maps, then the B map
     unsigned *status;
+    uint64_t wait_ns;                   // limit of every bounded wait
 };
 
 // Tile id -> (expert, m, n, problem). DH / DX: m-tiles of an expert's rows,
@@ -300,7 +301,7 @@ bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant_
                 }
             }
             for (int kb = 0; kb < nkb; ++kb) {
-                if (!mbar_wait(&S.empty[stage], phase ^ 1u, abort_flag, status, kWaitLimitNs)) { ok = false; break; }
+                if (!mbar_wait(&S.empty[stage], phase ^ 1u, abort_flag, status, p.wait_ns)) { ok = false; break; }
                 uint64_t *bar = &S.full[stage];
                 uint8_t *sa = S.stage[stage];
                 uint8_t *sb = sa + A_BYTES;
@@ -348,11 +349,11 @@ bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant_
             const int nkb = k_blocks<MODE>(S, p, e);
             const int acc = it & 1;
             const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
-            if (!mbar_wait(&S.acc_empty[acc], acc_phase ^ 1u, abort_flag, status, kWaitLimitNs)) { ok = false; break; }
+            if (!mbar_wait(&S.acc_empty[acc], acc_phase ^ 1u, abort_flag, status, p.wait_ns)) { ok = false; break; }
             tc_fence_after();
             const uint32_t d = tmem_base + (uint32_t)(acc * ACC_COLS);
             for (int kb = 0; kb < nkb; ++kb) {
-                if (!mbar_wait(&S.full[stage], phase, abort_flag, status, kWaitLimitNs)) { ok = false; break; }
+                if (!mbar_wait(&S.full[stage], phase, abort_flag, status, p.wait_ns)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t a0 = smem_u32(S.stage[stage]);
                 const uint32_t b0 = a0 + A_BYTES;
@@ -384,7 +385,7 @@ bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant_
             decode<MODE>(S, p, tile, e, m, n, prob);
             const int acc = it & 1;
             const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
-            const bool ready = mbar_wait(&S.acc_full[acc], acc_phase, abort_flag, status, kWaitLimitNs);
+            const bool ready = mbar_wait(&S.acc_full[acc], acc_phase, abort_flag, status, p.wait_ns);
             if (!__all_sync(0xffffffffu, ready)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
@@ -521,8 +522,8 @@ cudaError_t launch_step(int64_t units, const CUtensorMap &a0, const CUtensorMap 
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    const uint64_t bit = 1ull << (dev & 63);
-    if (!(done_mask.load() & bit)) {
+    const uint64_t bit = dev >= 0 && dev < kCachedDevices ? 1ull << dev : 0ull;
+    if (bit == 0 || !(done_mask.load() & bit)) {
         err = cudaFuncSetAttribute(bwd_gemm_kernel<DT, MODE>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    (int)kBwdSmemBytes<MODE>);
@@ -592,6 +593,7 @@ cudaError_t launch_backward(const void *x_disp, const int32_t *offsets, int64_t 
     p.offsets = offsets;
     p.E = E;
     p.status = status;
+    p.wait_ns = wait_limit_ns();
     if (rows > 0) {
         const int64_t mt = rows / BM + (rows < E ? rows : E);     // M-tiles, upper bound
         // DH: dh, then dg / du into dgu

@@ -14,6 +14,18 @@ int device_sm_count();
 // and returns `code`.
 int report_error(int code, const char *what);
 
+// Host-side argument checks of moe_dispatch_special (moe_dispatch with
+// special_experts = 0) short of the workspace: MOE_OK or the status the call
+// returns, with the detail recorded.
+int check_dispatch_args(const uint32_t *expert_indices, int64_t T, int top_k, int64_t E,
+                        int64_t special_experts, const void *x, int x_dtype, int64_t H,
+                        const int32_t *counts, const int32_t *offsets, const int32_t *row_of,
+                        const int32_t *src_of, const void *x_disp);
+
+// Limit of every bounded device wait, passed to the kernels at launch
+// (kWaitLimitNs unless moe_set_wait_limit_ns() set another).
+uint64_t wait_limit_ns();
+
 // Softmax top-k routing, warp per token. E <= 1024.
 cudaError_t launch_route(const void *logits, int ldt, int64_t T, int E,
                          int top_k, int renormalize, uint32_t *idx, void *w,
@@ -178,6 +190,15 @@ cudaError_t launch_experts_tc_backward(int dt, const void *x_disp, const int32_t
                                        const void *cache, const void *dout, void *dgu_ws,
                                        void *maps_ws, void *dx, float *dgate, float *dup,
                                        float *ddown, unsigned *status, cudaStream_t s);
+
+// The library's test of its bounded waits: GEMM2 of the one-call forward
+// (BF16, combine folded into y_acc [E * rows_per_expert, H] FP32, top_k 1,
+// per-expert readiness) launched on its own over zeroed data, with readiness
+// counters that nothing raises; ws holds selftest_wait_workspace_bytes(...)
+// (offsets, map, routing weights, counters, h, down).
+size_t selftest_wait_workspace_bytes(int E, int rows_per_expert, int64_t H, int64_t I);
+cudaError_t launch_selftest_wait_expiry(int E, int rows_per_expert, int64_t H, int64_t I,
+                                        void *ws, float *y_acc, unsigned *status, cudaStream_t s);
 
 // y = y_acc rounded to ydt ([T, H], H % 8 == 0).
 cudaError_t launch_finalize(const float *y_acc, int64_t T, int64_t H, void *y, int ydt,

@@ -10,6 +10,8 @@
 #include <atomic>
 #include <initializer_list>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/moe.h"
 #include "common.cuh"
 #include "kernels.h"
@@ -21,19 +23,35 @@ __device__ unsigned g_moe_status = 0u;
 
 int device_sm_count()
 {
-    static std::atomic<int> cache[64];
+    static std::atomic<int> cache[kCachedDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-    const int slot = dev & 63;
-    int v = cache[slot].load();
+    const bool cached = dev >= 0 && dev < kCachedDevices;
+    int v = cached ? cache[dev].load() : 0;
     if (v > 0) return v;
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
         v = 1;
-    cache[slot].store(v);
+    if (cached) cache[dev].store(v);
     return v;
 }
 
 namespace {
+std::atomic<uint64_t> g_wait_limit_ns{kWaitLimitNs};
+}
+
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(); }
+
+namespace {
+
+// An NVTX range around each compute entry point, so a profiler's timeline
+// shows which library call enqueued which kernels (header-only NVTX: without
+// an attached tool each push / pop is a check of a null function pointer).
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
 
 thread_local char g_detail[256] = "";
 
@@ -51,14 +69,15 @@ int cuda_fail(cudaError_t err, const char *where)
 
 unsigned *status_ptr()
 {
-    static std::atomic<unsigned *> cache[64];
+    static std::atomic<unsigned *> cache[kCachedDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
-    unsigned *p = cache[dev & 63].load();
+    const bool cached = dev >= 0 && dev < kCachedDevices;
+    unsigned *p = cached ? cache[dev].load() : nullptr;
     if (p != nullptr) return p;
     void *q = nullptr;
     if (cudaGetSymbolAddress(&q, g_moe_status) != cudaSuccess) return nullptr;
-    cache[dev & 63].store(static_cast<unsigned *>(q));
+    if (cached) cache[dev].store(static_cast<unsigned *>(q));
     return static_cast<unsigned *>(q);
 }
 
@@ -68,6 +87,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 constexpr int64_t kMaxE = 1024;
+constexpr uint64_t kMaxWaitLimitNs = 60ull * 1000000000ull;   // moe_set_wait_limit_ns bound
 constexpr int64_t kMaxRows = 0x7fffffff;   // dispatched rows are int32
 
 // Vector width rule shared by the experts and combine kernels: rows are moved
@@ -147,8 +167,15 @@ struct ForwardLayout {
     size_t idx, w, counts, offsets, row_of, src_of, disp_ws, x_disp, h, out_disp, total;
 };
 
+// The one-call forward folds the combine into GEMM2 unless the caller asked
+// for the deterministic (slot-order) combine.
+bool forward_folds(int64_t T, int64_t H, int dt, unsigned flags)
+{
+    return (flags & MOE_FORWARD_DETERMINISTIC) == 0 && fold_combine(T, H, dt);
+}
+
 ForwardLayout forward_layout(int64_t T, int64_t H, int64_t I, int64_t E, int top_k,
-                             int dt, int ldt)
+                             int dt, int ldt, unsigned flags)
 {
     const size_t A = (size_t)(T * top_k), eb = elem_bytes(dt);
     ForwardLayout L;
@@ -168,8 +195,9 @@ ForwardLayout forward_layout(int64_t T, int64_t H, int64_t I, int64_t E, int top
     // (folded: y_acc, then 256 bytes whose first word counts the CTAs of the
     // fused routing kernel, then the experts' h-readiness counters [E]; one
     // memset clears them all)
-    L.out_disp = take(fold_combine(T, H, dt) ? fold_acc_bytes(T, H) + 256 + round_up((size_t)E * 4, 256)
-                                             : A * (size_t)H * 4);
+    L.out_disp = take(forward_folds(T, H, dt, flags)
+                          ? fold_acc_bytes(T, H) + 256 + round_up((size_t)E * 4, 256)
+                          : A * (size_t)H * 4);
     L.total = off;
     return L;
 }
@@ -211,8 +239,12 @@ template <typename RouteFn>
 int forward_impl(const char *name, const void *x, int dtype, const void *logits,
                  int logits_dtype, const void *gate, const void *up, const void *down,
                  int64_t T, int64_t H, int64_t I, int64_t E, int top_k, void *y,
-                 void *workspace, size_t workspace_bytes, void *stream, RouteFn route)
+                 void *workspace, size_t workspace_bytes, const moe_forward_options *opt,
+                 void *stream, RouteFn route)
 {
+    const unsigned flags = opt != nullptr ? opt->flags : 0u;
+    if (flags & ~(unsigned)MOE_FORWARD_DETERMINISTIC)
+        return fail(MOE_ERR_VALUE, "unknown moe_forward_options flag");
     if (!valid_dtype(logits_dtype)) return fail(MOE_ERR_DTYPE, "logits dtype must be F32, BF16 or F16");
     int rc = check_experts_args(T * (int64_t)(top_k > 0 ? top_k : 1), E, H, I, dtype);
     if (rc != MOE_OK) return rc;
@@ -224,7 +256,7 @@ int forward_impl(const char *name, const void *x, int dtype, const void *logits,
     if (!aligned16(x) || !aligned16(logits) || !aligned16(gate) || !aligned16(up) ||
         !aligned16(down) || !aligned16(y))
         return fail(MOE_ERR_ALIGN, "tensors must be 16-byte aligned");
-    const ForwardLayout L = forward_layout(T, H, I, E, top_k, dtype, logits_dtype);
+    const ForwardLayout L = forward_layout(T, H, I, E, top_k, dtype, logits_dtype, flags);
     if (workspace_bytes < L.total || !workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return fail(MOE_ERR_WORKSPACE, "workspace too small or not 256-byte aligned");
     unsigned *st = status_ptr();
@@ -240,7 +272,9 @@ int forward_impl(const char *name, const void *x, int dtype, const void *logits,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t A = T * top_k;
 
-    const bool fused_combine = fold_combine(T, H, dtype);
+    const bool fused_combine = forward_folds(T, H, dtype, flags);
+    cudaEvent_t ev_begin = opt != nullptr ? static_cast<cudaEvent_t>(opt->experts_begin_event) : nullptr;
+    cudaEvent_t ev_end = opt != nullptr ? static_cast<cudaEvent_t>(opt->experts_end_event) : nullptr;
     cudaError_t err = cudaSuccess;
     unsigned *zeroed = nullptr, *ready = nullptr;
     if (fused_combine) {
@@ -253,6 +287,8 @@ int forward_impl(const char *name, const void *x, int dtype, const void *logits,
     const DispatchOut d{counts, offsets, row_of, src_of, x_disp, ws + L.disp_ws, zeroed, st};
     err = route(idx, w, d, s);
     if (err != cudaSuccess) return cuda_fail(err, "forward/route+dispatch");
+    if (ev_begin != nullptr && (err = cudaEventRecord(ev_begin, s)) != cudaSuccess)
+        return cuda_fail(err, "forward/experts_begin_event");
     if (fused_combine) {
         err = launch_experts_tc_combine(dtype, x_disp, offsets, A, gate, up, down, (int)E, H, I,
                                         h, src_of, w, logits_dtype, top_k,
@@ -260,11 +296,15 @@ int forward_impl(const char *name, const void *x, int dtype, const void *logits,
         if (err == cudaErrorInvalidValue)
             return fail(MOE_ERR_ALIGN, "TMA descriptor rejected (pointer alignment or shape)");
         if (err != cudaSuccess) return cuda_fail(err, "forward/experts");
+        if (ev_end != nullptr && (err = cudaEventRecord(ev_end, s)) != cudaSuccess)
+            return cuda_fail(err, "forward/experts_end_event");
         err = launch_finalize(static_cast<const float *>(out_disp), T, H, y, dtype, s);
         return err == cudaSuccess ? MOE_OK : cuda_fail(err, "forward/finalize");
     }
     rc = run_experts(x_disp, offsets, A, gate, up, down, E, H, I, dtype, h, out_disp, MOE_F32, s);
     if (rc != MOE_OK) return rc;
+    if (ev_end != nullptr && (err = cudaEventRecord(ev_end, s)) != cudaSuccess)
+        return cuda_fail(err, "forward/experts_end_event");
     err = launch_combine(out_disp, MOE_F32, w, logits_dtype, row_of, nullptr, nullptr, MOE_F32,
                          1.0f, T, top_k, H, y, dtype, nullptr, nullptr, s);
     return err == cudaSuccess ? MOE_OK : cuda_fail(err, "forward/combine");
@@ -297,13 +337,14 @@ const char *moe_status_string(int status)
     }
 }
 
-int moe_abi_version(void) { return 100; }
+int moe_abi_version(void) { return 101; }
 
 const char *moe_last_error_detail(void) { return g_detail; }
 
 int moe_route(const void *logits, int logits_dtype, int64_t T, int64_t E, int top_k,
               int renormalize, uint32_t *expert_indices, void *weights, void *stream)
 {
+    const NvtxRange nvtx("moe_route");
     int rc = check_route_args(logits, logits_dtype, T, E, top_k, expert_indices, weights);
     if (rc != MOE_OK || T == 0) return rc;
     cudaError_t err = launch_route(logits, logits_dtype, T, (int)E, top_k, renormalize,
@@ -316,6 +357,7 @@ int moe_route_sigmoid_grouped(const void *logits, int logits_dtype, int64_t T, i
                               int group_top_two, int renormalize, float scale,
                               uint32_t *expert_indices, void *weights, void *stream)
 {
+    const NvtxRange nvtx("moe_route_sigmoid_grouped");
     int rc = check_route_args(logits, logits_dtype, T, E, top_k, expert_indices, weights);
     if (rc != MOE_OK) return rc;
     rc = check_sigmoid_grouped_args(E, bias, top_k, groups, selected_groups, group_top_two, scale);
@@ -333,11 +375,14 @@ size_t moe_dispatch_workspace_size(int64_t T, int top_k, int64_t E)
     return round_up(dispatch_workspace_bytes(T * top_k, (int)E), 256);
 }
 
-int moe_dispatch_special(const uint32_t *expert_indices, int64_t T, int top_k, int64_t E,
-                         int64_t special_experts,
-                 const void *x, int x_dtype, int64_t H, int32_t *counts, int32_t *offsets,
-                 int32_t *row_of, int32_t *src_of, void *x_disp, void *workspace,
-                 size_t workspace_bytes, void *stream)
+}  // extern "C"
+
+namespace moe {
+
+int check_dispatch_args(const uint32_t *expert_indices, int64_t T, int top_k, int64_t E,
+                        int64_t special_experts, const void *x, int x_dtype, int64_t H,
+                        const int32_t *counts, const int32_t *offsets, const int32_t *row_of,
+                        const int32_t *src_of, const void *x_disp)
 {
     if (!valid_dtype(x_dtype)) return fail(MOE_ERR_DTYPE, "x dtype must be F32, BF16 or F16");
     if (T < 0 || E < 1 || E > kMaxE || top_k < 1 || H < 1 || T * top_k > kMaxRows)
@@ -350,6 +395,23 @@ int moe_dispatch_special(const uint32_t *expert_indices, int64_t T, int top_k, i
     if (!aligned16(expert_indices) || !aligned16(x) || !aligned16(counts) || !aligned16(offsets) ||
         !aligned16(row_of) || !aligned16(src_of) || !aligned16(x_disp))
         return fail(MOE_ERR_ALIGN, "moe_dispatch: tensors must be 16-byte aligned");
+    return MOE_OK;
+}
+
+}  // namespace moe
+
+extern "C" {
+
+int moe_dispatch_special(const uint32_t *expert_indices, int64_t T, int top_k, int64_t E,
+                         int64_t special_experts,
+                 const void *x, int x_dtype, int64_t H, int32_t *counts, int32_t *offsets,
+                 int32_t *row_of, int32_t *src_of, void *x_disp, void *workspace,
+                 size_t workspace_bytes, void *stream)
+{
+    const NvtxRange nvtx("moe_dispatch");
+    const int rc = check_dispatch_args(expert_indices, T, top_k, E, special_experts, x, x_dtype,
+                                       H, counts, offsets, row_of, src_of, x_disp);
+    if (rc != MOE_OK || T == 0) return rc;
     const size_t need = moe_dispatch_workspace_size(T, top_k, E);
     if (workspace_bytes < need || (need && !workspace) ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u))
@@ -384,6 +446,7 @@ int moe_experts_forward(const void *x_disp, const int32_t *offsets, int64_t rows
                         int64_t H, int64_t I, int dtype, void *out_disp, int out_dtype,
                         void *workspace, size_t workspace_bytes, void *stream)
 {
+    const NvtxRange nvtx("moe_experts_forward");
     int rc = check_experts_args(rows, E, H, I, dtype);
     if (rc != MOE_OK) return rc;
     if (out_dtype != dtype && out_dtype != MOE_F32)
@@ -405,6 +468,7 @@ int moe_combine(const void *out_disp, int out_dtype, const void *weights, int we
                 const int32_t *row_of, int64_t T, int top_k, int64_t H, void *y, int dtype,
                 void *stream)
 {
+    const NvtxRange nvtx("moe_combine");
     int rc = check_combine_args(out_dtype, weights_dtype, dtype, T, top_k, H, false);
     if (rc != MOE_OK || T == 0) return rc;
     if (!out_disp || !weights || !row_of || !y) return fail(MOE_ERR_NULL, "moe_combine: NULL tensor");
@@ -422,6 +486,7 @@ int moe_combine_add_rmsnorm(const void *out_disp, int out_dtype, const void *wei
                             int top_k, int64_t H, void *y, void *x_out, float *rstd,
                             void *stream)
 {
+    const NvtxRange nvtx("moe_combine_add_rmsnorm");
     int rc = check_combine_args(out_dtype, weights_dtype, dtype, T, top_k, H, true);
     if (rc != MOE_OK) return rc;
     if (!valid_dtype(gamma_dtype)) return fail(MOE_ERR_DTYPE, "gamma dtype must be F32, BF16 or F16");
@@ -444,6 +509,7 @@ int moe_combine_v2(const void *out_disp, int out_dtype, const void *weights, int
                    int64_t T, int top_k, int64_t H, void *y, int dtype, void *x_out,
                    float *rstd, void *stream)
 {
+    const NvtxRange nvtx("moe_combine_v2");
     const bool norm = residual != nullptr;
     int rc = check_combine_args(out_dtype, weights_dtype, dtype, T, top_k, H, norm);
     if (rc != MOE_OK) return rc;
@@ -499,6 +565,7 @@ int moe_combine_v2(const void *out_disp, int out_dtype, const void *weights, int
 int moe_rmsnorm(const void *x, int dtype, const void *gamma, int gamma_dtype, float eps,
                 int64_t rows, int64_t H, void *y, float *rstd, void *stream)
 {
+    const NvtxRange nvtx("moe_rmsnorm");
     if (!valid_dtype(dtype)) return fail(MOE_ERR_DTYPE, "x dtype must be F32, BF16 or F16");
     if (gamma_dtype != MOE_F32 && gamma_dtype != dtype)
         return fail(MOE_ERR_DTYPE, "gamma dtype must be F32 or the input dtype");
@@ -514,13 +581,82 @@ int moe_rmsnorm(const void *x, int dtype, const void *gamma, int gamma_dtype, fl
     return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_rmsnorm");
 }
 
+size_t moe_forward_workspace_size_ex(int64_t T, int64_t H, int64_t I, int64_t E, int top_k,
+                                     int dtype, int logits_dtype, unsigned flags)
+{
+    if (T <= 0 || H < 1 || I < 1 || E < 1 || E > kMaxE || top_k < 1 || top_k > E ||
+        !valid_dtype(dtype) || !valid_dtype(logits_dtype) ||
+        (flags & ~(unsigned)MOE_FORWARD_DETERMINISTIC))
+        return 0;
+    return forward_layout(T, H, I, E, top_k, dtype, logits_dtype, flags).total;
+}
+
 size_t moe_forward_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E, int top_k,
                                   int dtype, int logits_dtype)
 {
+    return moe_forward_workspace_size_ex(T, H, I, E, top_k, dtype, logits_dtype, 0u);
+}
+
+int moe_forward_workspace_layout(int64_t T, int64_t H, int64_t I, int64_t E, int top_k,
+                                 int dtype, int logits_dtype, unsigned flags,
+                                 moe_forward_layout *layout)
+{
+    if (layout == nullptr) return fail(MOE_ERR_NULL, "moe_forward_workspace_layout: NULL layout");
+    if (!valid_dtype(dtype) || !valid_dtype(logits_dtype))
+        return fail(MOE_ERR_DTYPE, "dtype must be F32, BF16 or F16");
+    if (flags & ~(unsigned)MOE_FORWARD_DETERMINISTIC)
+        return fail(MOE_ERR_VALUE, "unknown moe_forward_options flag");
     if (T <= 0 || H < 1 || I < 1 || E < 1 || E > kMaxE || top_k < 1 || top_k > E ||
-        !valid_dtype(dtype) || !valid_dtype(logits_dtype))
-        return 0;
-    return forward_layout(T, H, I, E, top_k, dtype, logits_dtype).total;
+        T * top_k > kMaxRows)
+        return fail(MOE_ERR_SHAPE, "need T >= 1, H, I >= 1, 1 <= E <= 1024, 1 <= top_k <= E");
+    const ForwardLayout L = forward_layout(T, H, I, E, top_k, dtype, logits_dtype, flags);
+    layout->expert_indices = L.idx;
+    layout->weights = L.w;
+    layout->counts = L.counts;
+    layout->offsets = L.offsets;
+    layout->row_of = L.row_of;
+    layout->src_of = L.src_of;
+    layout->x_disp = L.x_disp;
+    layout->total = L.total;
+    return MOE_OK;
+}
+
+int moe_forward_ex(const void *x, int dtype, const void *logits, int logits_dtype,
+                   const void *gate, const void *up, const void *down, int64_t T, int64_t H,
+                   int64_t I, int64_t E, int top_k, int renormalize, void *y, void *workspace,
+                   size_t workspace_bytes, const moe_forward_options *options, void *stream)
+{
+    const NvtxRange nvtx("moe_forward_ex");
+    const moe_sigmoid_grouped_routing *sg = options != nullptr ? options->sigmoid_grouped : nullptr;
+    if (sg == nullptr)
+        return forward_impl("moe_forward: NULL tensor", x, dtype, logits, logits_dtype, gate, up,
+                            down, T, H, I, E, top_k, y, workspace, workspace_bytes, options,
+                            stream,
+                            [&](uint32_t *idx, void *w, const DispatchOut &d, cudaStream_t s) {
+                                return launch_route_dispatch(
+                                    logits, logits_dtype, T, (int)E, top_k, renormalize, idx, w,
+                                    x, dtype, H, d.counts, d.offsets, d.row_of, d.src_of,
+                                    d.x_disp, d.ws, d.zeroed, d.status, s);
+                            });
+    if (E >= 1 && E <= kMaxE && top_k >= 1) {
+        const int rc = check_sigmoid_grouped_args(E, sg->bias, top_k, sg->groups,
+                                                  sg->selected_groups, sg->group_top_two,
+                                                  sg->scale);
+        if (rc != MOE_OK) return rc;
+    }
+    return forward_impl("moe_forward_sigmoid_grouped: NULL tensor", x, dtype, logits,
+                        logits_dtype, gate, up, down, T, H, I, E, top_k, y, workspace,
+                        workspace_bytes, options, stream,
+                        [&](uint32_t *idx, void *w, const DispatchOut &d, cudaStream_t s) {
+                            cudaError_t err = launch_route_sigmoid_grouped(
+                                logits, logits_dtype, T, (int)E, sg->bias, top_k, sg->groups,
+                                sg->selected_groups, sg->group_top_two, renormalize, sg->scale,
+                                idx, w, s);
+                            if (err != cudaSuccess) return err;
+                            return launch_dispatch(idx, T, top_k, (int)E, 0, x, dtype, H,
+                                                   d.counts, d.offsets, d.row_of, d.src_of,
+                                                   d.x_disp, d.ws, d.status, s);
+                        });
 }
 
 int moe_forward(const void *x, int dtype, const void *logits, int logits_dtype, const void *gate,
@@ -528,14 +664,8 @@ int moe_forward(const void *x, int dtype, const void *logits, int logits_dtype, 
                 int top_k, int renormalize, void *y, void *workspace, size_t workspace_bytes,
                 void *stream)
 {
-    return forward_impl("moe_forward: NULL tensor", x, dtype, logits, logits_dtype, gate, up,
-                        down, T, H, I, E, top_k, y, workspace, workspace_bytes, stream,
-                        [&](uint32_t *idx, void *w, const DispatchOut &d, cudaStream_t s) {
-                            return launch_route_dispatch(logits, logits_dtype, T, (int)E, top_k,
-                                                         renormalize, idx, w, x, dtype, H,
-                                                         d.counts, d.offsets, d.row_of, d.src_of,
-                                                         d.x_disp, d.ws, d.zeroed, d.status, s);
-                        });
+    return moe_forward_ex(x, dtype, logits, logits_dtype, gate, up, down, T, H, I, E, top_k,
+                          renormalize, y, workspace, workspace_bytes, nullptr, stream);
 }
 
 int moe_forward_sigmoid_grouped(const void *x, int dtype, const void *logits, int logits_dtype,
@@ -545,23 +675,52 @@ int moe_forward_sigmoid_grouped(const void *x, int dtype, const void *logits, in
                                 int renormalize, float scale, void *y, void *workspace,
                                 size_t workspace_bytes, void *stream)
 {
-    if (E >= 1 && E <= kMaxE && top_k >= 1) {
-        const int rc = check_sigmoid_grouped_args(E, bias, top_k, groups, selected_groups,
-                                                  group_top_two, scale);
-        if (rc != MOE_OK) return rc;
-    }
-    return forward_impl("moe_forward_sigmoid_grouped: NULL tensor", x, dtype, logits,
-                        logits_dtype, gate, up, down, T, H, I, E, top_k, y, workspace,
-                        workspace_bytes, stream,
-                        [&](uint32_t *idx, void *w, const DispatchOut &d, cudaStream_t s) {
-                            cudaError_t err = launch_route_sigmoid_grouped(
-                                logits, logits_dtype, T, (int)E, bias, top_k, groups,
-                                selected_groups, group_top_two, renormalize, scale, idx, w, s);
-                            if (err != cudaSuccess) return err;
-                            return launch_dispatch(idx, T, top_k, (int)E, 0, x, dtype, H,
-                                                   d.counts, d.offsets, d.row_of, d.src_of,
-                                                   d.x_disp, d.ws, d.status, s);
-                        });
+    const moe_sigmoid_grouped_routing sg{bias, groups, selected_groups, group_top_two, scale};
+    moe_forward_options opt{};
+    opt.sigmoid_grouped = &sg;
+    return moe_forward_ex(x, dtype, logits, logits_dtype, gate, up, down, T, H, I, E, top_k,
+                          renormalize, y, workspace, workspace_bytes, &opt, stream);
+}
+
+int moe_set_wait_limit_ns(uint64_t limit_ns)
+{
+    if (limit_ns > kMaxWaitLimitNs)
+        return fail(MOE_ERR_VALUE, "moe_set_wait_limit_ns: the limit must be at most 60 s");
+    g_wait_limit_ns.store(limit_ns == 0 ? kWaitLimitNs : limit_ns);
+    return MOE_OK;
+}
+
+uint64_t moe_wait_limit_ns(void) { return wait_limit_ns(); }
+
+size_t moe_selftest_wait_expiry_workspace_size(int64_t E, int64_t rows_per_expert, int64_t H,
+                                               int64_t I)
+{
+    if (E < 1 || E > kMaxE || rows_per_expert < 1 || rows_per_expert > 4096 || H < 8 ||
+        H > 8192 || H % 8 != 0 || I < 8 || I > 8192 || I % 8 != 0)
+        return 0;
+    return selftest_wait_workspace_bytes((int)E, (int)rows_per_expert, H, I);
+}
+
+int moe_selftest_wait_expiry(int64_t E, int64_t rows_per_expert, int64_t H, int64_t I,
+                             float *y_acc, void *workspace, size_t workspace_bytes, void *stream)
+{
+    const NvtxRange nvtx("moe_selftest_wait_expiry");
+    const size_t need = moe_selftest_wait_expiry_workspace_size(E, rows_per_expert, H, I);
+    if (need == 0)
+        return fail(MOE_ERR_SHAPE, "moe_selftest_wait_expiry: need 1 <= E <= 1024, "
+                                   "1 <= rows_per_expert <= 4096, H and I multiples of 8 in [8, 8192]");
+    if (y_acc == nullptr || workspace == nullptr)
+        return fail(MOE_ERR_NULL, "moe_selftest_wait_expiry: NULL y_acc or workspace");
+    if (!aligned16(y_acc)) return fail(MOE_ERR_ALIGN, "moe_selftest_wait_expiry: y_acc must be 16-byte aligned");
+    if (workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return fail(MOE_ERR_WORKSPACE, "moe_selftest_wait_expiry: workspace too small or not 256-byte aligned");
+    unsigned *st = status_ptr();
+    if (!st) return fail(MOE_ERR_CUDA, "cannot resolve the device status word");
+    cudaError_t err = launch_selftest_wait_expiry((int)E, (int)rows_per_expert, H, I, workspace,
+                                                  y_acc, st, static_cast<cudaStream_t>(stream));
+    if (err == cudaErrorInvalidValue)
+        return fail(MOE_ERR_ALIGN, "TMA descriptor rejected (pointer alignment or shape)");
+    return err == cudaSuccess ? MOE_OK : cuda_fail(err, "moe_selftest_wait_expiry");
 }
 
 // ---- first-order training (ruDNN user guide, section 12) ------------------
@@ -610,6 +769,7 @@ int moe_router_weights(const void *logits, int logits_dtype, int64_t T, int64_t 
                        const void *indices, int index_dtype, int top_k, int scoring,
                        int renormalize, float scale, float *weights, void *stream)
 {
+    const NvtxRange nvtx("moe_router_weights");
     int rc = check_router_train_args(logits, logits_dtype, T, E, indices, index_dtype, top_k,
                                      scoring, scale, weights, weights);
     if (rc != MOE_OK || T == 0) return rc;
@@ -626,6 +786,7 @@ int moe_router_backward(const void *logits, int logits_dtype, int64_t T, int64_t
                         const float *grad_weights, int scoring, int renormalize, float scale,
                         void *grad_logits, void *stream)
 {
+    const NvtxRange nvtx("moe_router_backward");
     int rc = check_router_train_args(logits, logits_dtype, T, E, indices, index_dtype, top_k,
                                      scoring, scale, grad_weights, grad_logits);
     if (rc != MOE_OK || T == 0) return rc;
@@ -644,6 +805,7 @@ int moe_combine_backward(const void *out_disp, int out_dtype, const void *weight
                          int64_t T, int top_k, int64_t H, int dtype, void *grad_out_disp,
                          float *grad_weights, void *stream)
 {
+    const NvtxRange nvtx("moe_combine_backward");
     if (!valid_dtype(out_dtype) || !valid_dtype(weights_dtype) || !valid_dtype(dtype))
         return fail(MOE_ERR_DTYPE, "dtype must be F32, BF16 or F16");
     if (out_dtype != dtype && out_dtype != MOE_F32)
@@ -664,6 +826,7 @@ int moe_combine_backward(const void *out_disp, int out_dtype, const void *weight
 int moe_dispatch_backward(const void *grad_x_disp, int dtype, const int32_t *row_of,
                           int64_t T, int top_k, int64_t H, void *grad_x, void *stream)
 {
+    const NvtxRange nvtx("moe_dispatch_backward");
     if (!valid_dtype(dtype)) return fail(MOE_ERR_DTYPE, "dtype must be F32, BF16 or F16");
     if (T < 0 || top_k < 1 || T * top_k > kMaxRows)
         return fail(MOE_ERR_SHAPE, "need T >= 0, top_k >= 1, T*top_k < 2^31");
@@ -688,6 +851,7 @@ int moe_experts_forward_training(const void *x_disp, const int32_t *offsets, int
                                  int64_t H, int64_t I, int dtype, void *out_disp, int out_dtype,
                                  void *cache, size_t cache_bytes, void *stream)
 {
+    const NvtxRange nvtx("moe_experts_forward_training");
     int rc = check_experts_args(rows, E, H, I, dtype);
     if (rc != MOE_OK) return rc;
     if (out_dtype != dtype && out_dtype != MOE_F32)
@@ -745,6 +909,7 @@ int moe_experts_backward(const void *x_disp, const int32_t *offsets, int64_t row
                          float *grad_up, float *grad_down, void *workspace,
                          size_t workspace_bytes, void *stream)
 {
+    const NvtxRange nvtx("moe_experts_backward");
     int rc = check_experts_args(rows, E, H, I, dtype);
     if (rc != MOE_OK) return rc;
     rc = check_experts_ptrs("moe_experts_backward: tensors must be non-NULL and 16-byte aligned",

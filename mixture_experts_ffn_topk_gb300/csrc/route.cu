@@ -477,12 +477,13 @@ cudaError_t launch_route_count(const void *logits, int64_t T, int E, int top_k, 
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    if (!(opted.load() >> (dev & 63) & 1ull)) {
+    const uint64_t bit = dev >= 0 && dev < kCachedDevices ? 1ull << dev : 0ull;
+    if (bit == 0 || !(opted.load() & bit)) {
         err = cudaFuncSetAttribute(route_count_kernel<G, EPL, LDT>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    (int)((1024 + kFusedMaxCounts) * sizeof(int)));
         if (err != cudaSuccess) return err;
-        opted.fetch_or(1ull << (dev & 63));
+        opted.fetch_or(bit);
     }
     return launch_pdl(route_count_kernel<G, EPL, LDT>, dim3((unsigned)nchunks),
                       dim3(route_count_threads<EPL>()), smem, s, logits, T, E, top_k, renorm, idx, w, chunk,

@@ -12,11 +12,19 @@
 // dtype. A row whose corrected scores hold a NaN gets ids 0..k-1 and NaN
 // weights, as in the softmax contract.
 //
-// Scores are FP32 (the kernel's precision): 1 / (1 + expf(-l)). Lane r holds
-// experts r*EPL .. r*EPL+EPL-1 in registers and their corrected scores in a
-// per-warp shared-memory row, from which lanes score the groups (lane g takes
-// groups g, g+32, g+64, g+96). Group and expert picks are rounds of a warp
-// argmax on (score desc, id asc).
+// Scores are FP32, each the sigmoid evaluated in double and rounded once to
+// FP32: 1 / (1 + exp(-l)) with l widened exactly. The double result lies
+// within a few double ulps of the exact sigmoid, so its one rounding to FP32
+// gives the correctly rounded score except when the exact value sits within
+// that distance of an FP32 rounding boundary (about 2^-28 of inputs); every
+// selection decision therefore compares the same FP32 values as any other
+// implementation that rounds the sigmoid once. T * E double evaluations per
+// call are a negligible load at GB300's FP64 rate for the routing shapes.
+//
+// Lane r holds experts r*EPL .. r*EPL+EPL-1 in registers and their corrected
+// scores in a per-warp shared-memory row, from which lanes score the groups
+// (lane g takes groups g, g+32, g+64, g+96). Group and expert picks are
+// rounds of a warp argmax on (score desc, id asc).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -85,7 +93,7 @@ route_sigmoid_grouped_kernel(const void *__restrict__ logits, int64_t T, int E,
             c[i] = -INFINITY;
             if (e < E) {
                 const float l = Elem<LDT>::to_f(L[t * E + e]);
-                s[i] = 1.0f / (1.0f + expf(-l));
+                s[i] = (float)(1.0 / (1.0 + exp(-(double)l)));
                 c[i] = s[i] + b[i];
                 nan |= isnan(c[i]);
                 cs[e] = c[i];

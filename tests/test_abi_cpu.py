@@ -51,7 +51,7 @@ def test_status_strings(lib):
     for code in range(10):
         assert moe.moe_status_string(code)
     assert moe.moe_status_string(99) == "unknown status"
-    assert moe.moe_abi_version() == 100
+    assert moe.moe_abi_version() == 101
 
 
 def P(v):
@@ -126,24 +126,34 @@ def test_forward_sigmoid_grouped_validation(lib):
     assert call(T=0, x=P(None), lg=P(None), y=P(None)) == OK
 
 
-def test_combine_extras_layout_matches_header(tmp_path):
-    """The binding's moe_combine_extras mirror has the C header's layout
-    (field offsets and size as the C compiler lays them out)."""
+def _c_layout(tmp_path, ctype, fields):
+    """sizeof and field offsets of a header struct as the C compiler lays it out."""
     import subprocess
-    fields = [f[0] for f in moe.CombineExtras._fields_]
-    src = tmp_path / "layout.c"
+    src = tmp_path / f"layout_{ctype}.c"
     src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "moe.h"\n'
                    "int main(void) {\n"
-                   '    printf("%zu\\n", sizeof(moe_combine_extras));\n'
-                   + "".join(f'    printf("%zu\\n", offsetof(moe_combine_extras, {n}));\n'
+                   f'    printf("%zu\\n", sizeof({ctype}));\n'
+                   + "".join(f'    printf("%zu\\n", offsetof({ctype}, {n}));\n'
                              for n in fields) + "    return 0;\n}\n")
-    exe = tmp_path / "layout"
+    exe = tmp_path / f"layout_{ctype}"
     subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o",
                     str(exe)], check=True)
-    got = [int(v) for v in subprocess.run([str(exe)], check=True, capture_output=True,
-                                          text=True).stdout.split()]
-    assert got[0] == ctypes.sizeof(moe.CombineExtras)
-    assert got[1:] == [getattr(moe.CombineExtras, n).offset for n in fields]
+    return [int(v) for v in subprocess.run([str(exe)], check=True, capture_output=True,
+                                           text=True).stdout.split()]
+
+
+@pytest.mark.parametrize("ctype,mirror", [("moe_combine_extras", "CombineExtras"),
+                                          ("moe_forward_options", "ForwardOptions"),
+                                          ("moe_sigmoid_grouped_routing", "SigmoidGroupedRouting"),
+                                          ("moe_forward_layout", "ForwardLayout")])
+def test_struct_layouts_match_header(tmp_path, ctype, mirror):
+    """The binding's ctypes mirrors have the C header's layout (field offsets
+    and size as the C compiler lays them out)."""
+    cls = getattr(moe, mirror)
+    fields = [f[0] for f in cls._fields_]
+    got = _c_layout(tmp_path, ctype, fields)
+    assert got[0] == ctypes.sizeof(cls)
+    assert got[1:] == [getattr(cls, n).offset for n in fields]
 
 
 def test_combine_v2_validation(lib):
@@ -411,3 +421,105 @@ def test_training_validation(lib):
     assert bw(gg=P(None)) == NULL
     assert bw(nb=ws - 256) == WORKSPACE
     assert bw(rows=0, ws=P(None), nb=0) == WORKSPACE   # the maps are needed without rows too
+
+
+def test_forward_ex_validation(lib):
+    s = P(None)
+
+    def call(flags=0, **kw):
+        a = dict(x=P(FAKE), dt=BF16, lg=P(FAKE), ldt=BF16, T=32, H=64, I=32, E=8, k=2,
+                 y=P(FAKE), ws=P(FAKE), wsb=1 << 30)
+        a.update(kw)
+        opt = moe.ForwardOptions()
+        opt.flags = flags
+        return lib.moe_forward_ex(a["x"], a["dt"], a["lg"], a["ldt"], P(FAKE), P(FAKE),
+                                  P(FAKE), a["T"], a["H"], a["I"], a["E"], a["k"], 1,
+                                  a["y"], a["ws"], a["wsb"], ctypes.byref(opt), s)
+    assert call(flags=2) == VALUE            # unknown option bit
+    assert call(ldt=3) == DTYPE
+    assert call(k=9) == SHAPE
+    assert call(lg=P(None)) == NULL
+    assert call(y=P(FAKE_ODD)) == ALIGN
+    # the deterministic forward needs the larger workspace
+    need = lib.moe_forward_workspace_size_ex(32, 64, 32, 8, 2, BF16, BF16, 1)
+    assert need > lib.moe_forward_workspace_size_ex(32, 64, 32, 8, 2, BF16, BF16, 0)
+    assert call(flags=1, wsb=lib.moe_forward_workspace_size(32, 64, 32, 8, 2, BF16, BF16)) \
+        == WORKSPACE
+    assert call(flags=1, T=0, x=P(None), lg=P(None), y=P(None)) == OK
+    # sigmoid routing limits through the options
+    sg = moe.SigmoidGroupedRouting(None, 3, 1, 0, 1.0)      # 3 groups do not divide E = 8
+    opt = moe.ForwardOptions()
+    opt.sigmoid_grouped = ctypes.pointer(sg)
+    rc = lib.moe_forward_ex(P(FAKE), BF16, P(FAKE), BF16, P(FAKE), P(FAKE), P(FAKE), 32, 64, 32,
+                            8, 2, 1, P(FAKE), P(FAKE), 1 << 30, ctypes.byref(opt), s)
+    assert rc == SHAPE
+
+
+def test_forward_workspace_layout(lib):
+    """The layout names disjoint, 256-byte aligned regions of the workspace,
+    in the sizes the header gives them, and its total is the workspace size."""
+    for (T, H, I, E, k, dt, ldt) in [(4096, 2048, 1408, 64, 6, BF16, BF16),
+                                     (16384, 4096, 14336, 8, 2, BF16, F32),
+                                     (128, 7168, 2048, 256, 8, BF16, F32),
+                                     (64, 128, 256, 8, 2, F32, F32)]:
+        for flags in (0, 1):
+            lay = moe.ForwardLayout()
+            assert lib.moe_forward_workspace_layout(T, H, I, E, k, dt, ldt, flags,
+                                                    ctypes.byref(lay)) == OK
+            assert lay.total == lib.moe_forward_workspace_size_ex(T, H, I, E, k, dt, ldt, flags)
+            A, eb, lb = T * k, (4 if dt == F32 else 2), (4 if ldt == F32 else 2)
+            regions = sorted([(lay.expert_indices, A * 4), (lay.weights, A * lb),
+                              (lay.counts, E * 4), (lay.offsets, (E + 1) * 4),
+                              (lay.row_of, A * 4), (lay.src_of, A * 4),
+                              (lay.x_disp, A * H * eb)])
+            for (a, n), (b, _) in zip(regions, regions[1:]):
+                assert a % 256 == 0 and a + n <= b
+            assert regions[-1][0] + regions[-1][1] <= lay.total
+    lay = moe.ForwardLayout()
+    assert lib.moe_forward_workspace_layout(8, 64, 32, 8, 2, BF16, BF16, 4,
+                                            ctypes.byref(lay)) == VALUE
+    assert lib.moe_forward_workspace_layout(8, 64, 32, 8, 9, BF16, BF16, 0,
+                                            ctypes.byref(lay)) == SHAPE
+    assert lib.moe_forward_workspace_layout(8, 64, 32, 8, 2, BF16, BF16, 0, None) == NULL
+
+
+def test_wait_limit_setting(lib):
+    assert lib.moe_wait_limit_ns() == 2_000_000_000
+    try:
+        assert lib.moe_set_wait_limit_ns(5_000_000) == OK
+        assert lib.moe_wait_limit_ns() == 5_000_000
+        assert lib.moe_set_wait_limit_ns(61_000_000_000) == VALUE
+        assert lib.moe_wait_limit_ns() == 5_000_000
+    finally:
+        assert lib.moe_set_wait_limit_ns(0) == OK
+    assert lib.moe_wait_limit_ns() == 2_000_000_000
+
+
+def test_selftest_wait_expiry_validation(lib):
+    s = P(None)
+    need = lib.moe_selftest_wait_expiry_workspace_size(2, 300, 256, 128)
+    assert need >= 2 * 256 * 128 * 2 + 600 * 128 * 2
+    assert lib.moe_selftest_wait_expiry_workspace_size(0, 300, 256, 128) == 0
+    assert lib.moe_selftest_wait_expiry(0, 300, 256, 128, P(FAKE), P(FAKE), need, s) == SHAPE
+    assert lib.moe_selftest_wait_expiry(2, 300, 250, 128, P(FAKE), P(FAKE), need, s) == SHAPE
+    assert lib.moe_selftest_wait_expiry(2, 300, 256, 128, P(None), P(FAKE), need, s) == NULL
+    assert lib.moe_selftest_wait_expiry(2, 300, 256, 128, P(FAKE_ODD), P(FAKE), need, s) == ALIGN
+    assert lib.moe_selftest_wait_expiry(2, 300, 256, 128, P(FAKE), P(FAKE), need - 1, s) == WORKSPACE
+
+
+def test_dispatch_noalloc_validation_order(lib):
+    """The no-alloc dispatch checks its arguments as moe_dispatch does before
+    it tests the size against its built-in scratch."""
+    s = P(None)
+    args = lambda **kw: [kw.get("idx", P(FAKE)), kw.get("T", 32768), kw.get("k", 8),
+                         kw.get("E", 1024), kw.get("x", P(FAKE)), kw.get("xdt", BF16),
+                         kw.get("H", 8), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), s]
+    # oversized (about 4 MiB of chunk counts) and a bad dtype / pointer: the
+    # argument's own status comes first
+    assert lib.moe_dispatch_noalloc(*args(xdt=7)) == DTYPE
+    assert lib.moe_dispatch_noalloc(*args(idx=P(None))) == NULL
+    assert lib.moe_dispatch_noalloc(*args(x=P(FAKE_ODD))) == ALIGN
+    assert lib.moe_dispatch_noalloc(*args(E=0)) == SHAPE
+    assert lib.moe_dispatch_workspace_size(32768, 8, 1024) > 256 * 1024
+    assert lib.moe_dispatch_noalloc(*args()) == WORKSPACE
+    assert lib.moe_dispatch_noalloc(*args(T=0, idx=P(None))) == OK

@@ -60,3 +60,17 @@ def test_single_process_needs_no_group(monkeypatch):
     assert (r, w, local, d) == (0, 1, 0, None)
     assert bench.reduce_max(None, 3.5, torch.device("cpu")) == 3.5
     assert bench.aggregate(0.5, 100, 1) == 200
+
+
+def test_gpus_flag_is_never_ignored():
+    """--gpus N > 1 without torchrun relaunches N ranks; inside a torchrun job
+    WORLD_SIZE must equal N; N < 1 is refused."""
+    import bench
+    assert bench.launch_plan(1, {}) == "single"
+    assert bench.launch_plan(4, {}) == "spawn"
+    assert bench.launch_plan(2, {"WORLD_SIZE": "2"}) == "rank"
+    assert bench.launch_plan(1, {"WORLD_SIZE": "1"}) == "single"
+    with pytest.raises(SystemExit):
+        bench.launch_plan(8, {"WORLD_SIZE": "2"})
+    with pytest.raises(SystemExit):
+        bench.launch_plan(0, {})

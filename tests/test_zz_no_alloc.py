@@ -83,7 +83,10 @@ def test_noalloc_matches_dispatch_on_two_calls(lib):
 
 def test_noalloc_refuses_sizes_beyond_its_scratch(lib):
     dev = torch.device("cuda:0")
-    T, k, E, H = 32768, 8, 1024, 8      # 128 chunks x 1024 experts > 65536 counters
+    T, k, E, H = 32768, 8, 1024, 8
+    # the dispatch workspace of this shape (per-chunk counts of 1024 experts,
+    # about 4 MiB on a 152-SM GPU) is far beyond the 256 KiB array
+    assert lib.moe_dispatch_workspace_size(T, k, E) > 256 * 1024
     idx = torch.zeros((T, k), dtype=torch.int32, device=dev)
     x = torch.zeros((T, H), dtype=torch.bfloat16, device=dev)
     out = _outputs(T, k, E, H, x.dtype, dev)
@@ -93,5 +96,11 @@ def test_noalloc_refuses_sizes_beyond_its_scratch(lib):
                                   _p(out["x_disp"]), s)
     assert rc == 6                       # MOE_ERR_WORKSPACE
     assert b"256 KiB" in lib.moe_last_error_detail()
+    # a bad argument is reported as moe_dispatch would report it, before the
+    # size test
+    rc = lib.moe_dispatch_noalloc(_p(idx), T, k, E, _p(x), 7, H, _p(out["counts"]),
+                                  _p(out["offsets"]), _p(out["row_of"]), _p(out["src_of"]),
+                                  _p(out["x_disp"]), s)
+    assert rc == 3                       # MOE_ERR_DTYPE
     torch.cuda.synchronize()
     assert torch.all(out["counts"] == -7)   # nothing was enqueued
