@@ -525,6 +525,16 @@ def moe_forward_ex(x: torch.Tensor, logits: torch.Tensor, gate: torch.Tensor, up
                                    int(bool(sigmoid_grouped["group_top_two"])),
                                    float(sigmoid_grouped.get("scale", 1.0)))
         opt.sigmoid_grouped = ctypes.pointer(sg)
+    # torch creates an event's handle on its first record and only then lets
+    # elapsed_time() read it: record both here first; the library records
+    # them again, later on the same stream, around the expert GEMMs
+    if experts_begin_event is not None or experts_end_event is not None:
+        ts = (torch.cuda.current_stream(dev) if stream is None else
+              stream if isinstance(stream, torch.cuda.Stream) else
+              torch.cuda.ExternalStream(int(stream)))
+        for ev in (experts_begin_event, experts_end_event):
+            if ev is not None:
+                ev.record(ts)
     opt.experts_begin_event = _event_handle(experts_begin_event)
     opt.experts_end_event = _event_handle(experts_end_event)
     rc = load_library().moe_forward_ex(
