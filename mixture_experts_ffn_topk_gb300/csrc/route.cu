@@ -343,6 +343,231 @@ route_thread_kernel(const void *__restrict__ logits, int64_t T, int E, int top_k
     }
 }
 
+// ---- one thread per token, 16-bit logits on packed pairs ----------------------
+//
+// BF16 / F16 logits whose rows are whole 16-byte vectors (E % 8 == 0): the
+// thread keeps its row as E/2 packed 32-bit words and works on pairs where it
+// can, which cuts the instructions per token about fourfold:
+//   * the row maximum is a NaN-propagating packed max, so one look at it
+//     tells an invalid row (a NaN, a +inf, or every logit -inf);
+//   * each logit becomes a 32-bit selection key: its order-preserving 16-bit
+//     code in the high half (-0 and +0 share one code, so they tie) and
+//     63 - id in the low half, so one integer max compares the logits and
+//     breaks ties toward the lower id; the keys of a group of 8 experts are
+//     stored with two 16-byte writes, and the round's rescan reads them back
+//     with two 16-byte reads;
+//   * the softmax sum takes one FFMA and one ex2 per logit.
+// The selected probabilities are recomputed from their keys' codes (the same
+// FP32 operations as in the sum).
+
+// Order-preserving codes of the two 16-bit floats in w (IEEE sign-magnitude,
+// BF16 or F16): a positive value h maps to h + 0x8000, a negative one to
+// 0x8000 - |h|, so -0 and +0 share 0x8000, larger values get larger codes and
+// no code is 0. Per 16-bit lane with no carry or borrow across lanes.
+__device__ __forceinline__ uint32_t order_codes2(uint32_t w)
+{
+    const uint32_t sgn = (w >> 15) & 0x00010001u;     // 1 in each negative lane
+    const uint32_t neg = sgn * 0xffffu;               // 0xffff in each negative lane
+    const uint32_t mag = w & 0x7fff7fffu;
+    return 0x80008000u + (mag & ~neg) - (mag & neg);
+}
+
+// The 16-bit float bits of a code (the inverse of order_codes2; -0 comes
+// back as +0).
+__device__ __forceinline__ uint32_t code_to_bits16(uint32_t code)
+{
+    return code >= 0x8000u ? code - 0x8000u : (0x8000u | (0x8000u - code));
+}
+
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+template <int LDT>
+__device__ __forceinline__ float half_lo(uint32_t w)
+{
+    if constexpr (LDT == DT_BF16) return __uint_as_float(w << 16);
+    else return __half2float(__ushort_as_half((unsigned short)(w & 0xffffu)));
+}
+template <int LDT>
+__device__ __forceinline__ float half_hi(uint32_t w)
+{
+    if constexpr (LDT == DT_BF16) return __uint_as_float(w & 0xffff0000u);
+    else return __half2float(__ushort_as_half((unsigned short)(w >> 16)));
+}
+template <int LDT>
+__device__ __forceinline__ uint32_t max2_nan(uint32_t a, uint32_t b)
+{
+    if constexpr (LDT == DT_BF16) {
+        const __nv_bfloat162 r = __hmax2_nan(*reinterpret_cast<const __nv_bfloat162 *>(&a),
+                                             *reinterpret_cast<const __nv_bfloat162 *>(&b));
+        return *reinterpret_cast<const uint32_t *>(&r);
+    } else {
+        const __half2 r = __hmax2_nan(*reinterpret_cast<const __half2 *>(&a),
+                                      *reinterpret_cast<const __half2 *>(&b));
+        return *reinterpret_cast<const uint32_t *>(&r);
+    }
+}
+
+constexpr int kKeyPad = 4;                 // words after each thread's key row (bank spread)
+
+template <int EPL, int LDT>
+__global__ void __launch_bounds__(kThreadRouteThreads)
+route_thread16_kernel(const void *__restrict__ logits, int64_t T, int E, int top_k,
+                      int renormalize, uint32_t *__restrict__ idx_out,
+                      void *__restrict__ w_out)
+{
+    static_assert(EPL % 8 == 0 && EPL <= 64, "rows of whole 16-byte vectors, ids below 64");
+    constexpr int NW = EPL / 2;                       // packed words per row
+    constexpr int NG = EPL / 8;                       // groups of 8 experts
+    constexpr int ROW = EPL + kKeyPad;                // key words per thread
+    constexpr uint32_t kNegInf2 = LDT == DT_BF16 ? 0xff80ff80u : 0xfc00fc00u;
+    using ET = typename Elem<LDT>::T;
+    const uint4 *L = static_cast<const uint4 *>(logits);
+    ET *W = static_cast<ET *>(w_out);
+    extern __shared__ uint4 key_smem[];               // [threads][ROW] words
+    uint32_t *kr = reinterpret_cast<uint32_t *>(key_smem) + threadIdx.x * ROW;
+    const int vecs = E / 8;                           // 16-byte vectors per row
+    pdl_wait();
+    pdl_launch_dependents();
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < T;
+         t += (int64_t)gridDim.x * blockDim.x) {
+        uint32_t w[NW];
+        const uint4 *row = L + t * vecs;
+#pragma unroll
+        for (int c = 0; c < EPL / 8; ++c) {
+            uint4 v = make_uint4(kNegInf2, kNegInf2, kNegInf2, kNegInf2);
+            if (c < vecs) v = row[c];
+            w[4 * c] = v.x;
+            w[4 * c + 1] = v.y;
+            w[4 * c + 2] = v.z;
+            w[4 * c + 3] = v.w;
+        }
+        // row maximum, NaN-propagating: NaN if any logit is NaN
+        uint32_t mp = w[0];
+#pragma unroll
+        for (int i = 1; i < NW; ++i) mp = max2_nan<LDT>(mp, w[i]);
+        const float ma = half_lo<LDT>(mp), mb = half_hi<LDT>(mp);
+        const float m = (isnan(ma) || isnan(mb)) ? __int_as_float(0x7fc00000) : fmaxf(ma, mb);
+        const bool invalid = !(fabsf(m) < INFINITY);  // NaN, +inf, or every logit -inf
+
+        // FP32 softmax sum, exp(l - m) = 2^(l log2e - m log2e) with one FFMA
+        // per logit; where m log2e would overflow FP32 (|m| near the format's
+        // largest values), 2^((l - m) log2e) instead
+        constexpr float kLog2e = 1.4426950408889634f;
+        const bool big = !(fabsf(m) < 1.0e30f);
+        const float mb2 = big ? 0.0f : -m * kLog2e;
+        auto arg = [&](float l) { return big ? (l - m) * kLog2e : fmaf(l, kLog2e, mb2); };
+        float s = 0.0f;
+        if (!invalid) {
+            if (!big) {
+#pragma unroll
+                for (int i = 0; i < NW; ++i) {
+                    s += ex2_approx(fmaf(half_lo<LDT>(w[i]), kLog2e, mb2));
+                    s += ex2_approx(fmaf(half_hi<LDT>(w[i]), kLog2e, mb2));
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < NW; ++i) {
+                    s += ex2_approx((half_lo<LDT>(w[i]) - m) * kLog2e);
+                    s += ex2_approx((half_hi<LDT>(w[i]) - m) * kLog2e);
+                }
+            }
+        }
+        const float inv_s = 1.0f / s;
+
+        // keys (code << 16 | 63 - id), stored per group of 8; group bests kept
+        uint32_t gk[NG];
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+            uint32_t k8[8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t code = order_codes2(w[4 * g + q]);
+                const int id = 8 * g + 2 * q;
+                k8[2 * q] = (code << 16) | (uint32_t)(63 - id);
+                k8[2 * q + 1] = (code & 0xffff0000u) | (uint32_t)(62 - id);
+            }
+            reinterpret_cast<uint4 *>(kr + 8 * g)[0] = make_uint4(k8[0], k8[1], k8[2], k8[3]);
+            reinterpret_cast<uint4 *>(kr + 8 * g)[1] = make_uint4(k8[4], k8[5], k8[6], k8[7]);
+            uint32_t b = k8[0];
+#pragma unroll
+            for (int q = 1; q < 8; ++q) b = max(b, k8[q]);
+            gk[g] = b;
+        }
+
+        float p[kMaxThreadTopK];
+        int id[kMaxThreadTopK];
+        float z = 0.0f;
+#pragma unroll
+        for (int j = 0; j < kMaxThreadTopK; ++j) {
+            p[j] = 0.0f;
+            id[j] = j;
+            if (j < top_k && !invalid) {
+                uint32_t best = gk[0];
+#pragma unroll
+                for (int g = 1; g < NG; ++g) best = max(best, gk[g]);
+                const int e = 63 - (int)(best & 0xffffu);
+                id[j] = e;
+                const uint32_t bits = code_to_bits16(best >> 16);
+                const float l = LDT == DT_BF16 ? __uint_as_float(bits << 16)
+                                               : __half2float(__ushort_as_half((unsigned short)bits));
+                p[j] = ex2_approx(arg(l)) * inv_s;
+                z += p[j];
+                // take it, rescan its group
+                kr[e] = 0u;
+                const int g0 = e & ~7;
+                const uint4 a = reinterpret_cast<const uint4 *>(kr + g0)[0];
+                const uint4 b = reinterpret_cast<const uint4 *>(kr + g0)[1];
+                const uint32_t nk = max(max(max(a.x, a.y), max(a.z, a.w)),
+                                        max(max(b.x, b.y), max(b.z, b.w)));
+#pragma unroll
+                for (int g = 0; g < NG; ++g)
+                    if (gk[g] == best) gk[g] = nk;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kMaxThreadTopK; ++j) {
+            if (j < top_k) {
+                if (invalid) {
+                    idx_out[t * top_k + j] = (uint32_t)j;
+                    W[t * top_k + j] = Elem<LDT>::from_f(__int_as_float(0x7fc00000));
+                } else {
+                    idx_out[t * top_k + j] = (uint32_t)id[j];
+                    W[t * top_k + j] = Elem<LDT>::from_f(renormalize ? p[j] / z : p[j]);
+                }
+            }
+        }
+    }
+}
+
+template <int EPL, int LDT>
+cudaError_t launch_route_thread16(const void *logits, int64_t T, int E, int top_k, int renorm,
+                                  uint32_t *idx, void *w, cudaStream_t s)
+{
+    constexpr int kThreads = kThreadRouteThreads;
+    const size_t smem = (size_t)kThreads * (EPL + kKeyPad) * sizeof(uint32_t);
+    static std::atomic<uint64_t> opted{0};       // the > 48 KiB opt-in, per device
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    const uint64_t bit = dev >= 0 && dev < kCachedDevices ? 1ull << dev : 0ull;
+    if (smem > 48 * 1024 && (bit == 0 || !(opted.load() & bit))) {
+        err = cudaFuncSetAttribute(route_thread16_kernel<EPL, LDT>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
+        opted.fetch_or(bit);
+    }
+    int64_t blocks = (T + kThreads - 1) / kThreads;
+    const int64_t cap = (int64_t)device_sm_count() * 16;
+    if (blocks > cap) blocks = cap;
+    return launch_pdl(route_thread16_kernel<EPL, LDT>, dim3((unsigned)blocks), dim3(kThreads),
+                      smem, s, logits, T, E, top_k, renorm, idx, w);
+}
+
 template <int EPL, int LDT>
 cudaError_t launch_route_thread(const void *logits, int64_t T, int E, int top_k, int renorm,
                                 uint32_t *idx, void *w, cudaStream_t s)
@@ -382,6 +607,12 @@ cudaError_t launch_route_dt(const void *logits, int64_t T, int E, int top_k,
                             int renorm, uint32_t *idx, void *w, cudaStream_t s)
 {
     if (thread_route_fits(T, E, top_k)) {
+        if (LDT != DT_F32 && E % 8 == 0 && reinterpret_cast<uintptr_t>(logits) % 16 == 0) {
+            if (E <= 8) return launch_route_thread16<8, LDT>(logits, T, E, top_k, renorm, idx, w, s);
+            if (E <= 16) return launch_route_thread16<16, LDT>(logits, T, E, top_k, renorm, idx, w, s);
+            if (E <= 32) return launch_route_thread16<32, LDT>(logits, T, E, top_k, renorm, idx, w, s);
+            return launch_route_thread16<64, LDT>(logits, T, E, top_k, renorm, idx, w, s);
+        }
         if (E <= 8) return launch_route_thread<8, LDT>(logits, T, E, top_k, renorm, idx, w, s);
         if (E <= 16) return launch_route_thread<16, LDT>(logits, T, E, top_k, renorm, idx, w, s);
         if (E <= 32) return launch_route_thread<32, LDT>(logits, T, E, top_k, renorm, idx, w, s);
@@ -402,7 +633,8 @@ cudaError_t launch_route_dt(const void *logits, int64_t T, int E, int top_k,
 // CTA c routes the tokens of assignment chunk c ([c * chunk, (c + 1) * chunk)
 // of the A = T * top_k assignments; a token on a chunk edge is routed by both
 // neighbours, with identical results), counts the chunk's assignments per
-// expert in shared memory and stores the counts in chunk_counts[c][E]. The
+// expert in shared memory and stores the counts in chunk_counts[E][nchunks]
+// (each expert's counts contiguous, as the dispatch passes keep them). The
 // last CTA to finish (a completion counter it resets afterwards) turns every
 // expert's column of counts into the first row each chunk may use inside the
 // expert and writes the expert totals: what the rank/scatter kernel reads.
@@ -438,7 +670,7 @@ route_count_kernel(const void *__restrict__ logits, int64_t T, int E, int top_k,
         if (e < (uint32_t)E) atomicAdd(&hist[e], 1);
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += NT) chunk_counts[c * E + e] = hist[e];
+    for (int e = threadIdx.x; e < E; e += NT) chunk_counts[(int64_t)e * nchunks + c] = hist[e];
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) is_last = atomicAdd(done, 1u) == (unsigned)(nchunks - 1);
@@ -448,15 +680,15 @@ route_count_kernel(const void *__restrict__ logits, int64_t T, int E, int top_k,
     // every CTA's counts into shared memory with all threads' loads in flight
     // (a column walk in global memory would wait for each load in turn), then
     // one thread per expert scans its column there
-    int *cc = hist + E;                                // [nchunks][E]
+    int *cc = hist + E;                                // [E][nchunks]
     const int n = (int)(nchunks * E);
     for (int i = threadIdx.x; i < n; i += NT) cc[i] = __ldcg(chunk_counts + i);
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += NT) {
         int run = 0;
         for (int k = 0; k < (int)nchunks; ++k) {
-            const int v = cc[k * E + e];
-            chunk_counts[(int64_t)k * E + e] = run;
+            const int v = cc[e * (int)nchunks + k];
+            chunk_counts[(int64_t)e * nchunks + k] = run;
             run += v;
         }
         counts[e] = run;

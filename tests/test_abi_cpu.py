@@ -511,15 +511,16 @@ def test_dispatch_noalloc_validation_order(lib):
     """The no-alloc dispatch checks its arguments as moe_dispatch does before
     it tests the size against its built-in scratch."""
     s = P(None)
-    args = lambda **kw: [kw.get("idx", P(FAKE)), kw.get("T", 32768), kw.get("k", 8),
+    args = lambda **kw: [kw.get("idx", P(FAKE)), kw.get("T", 262144), kw.get("k", 8),
                          kw.get("E", 1024), kw.get("x", P(FAKE)), kw.get("xdt", BF16),
                          kw.get("H", 8), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), s]
-    # oversized (about 4 MiB of chunk counts) and a bad dtype / pointer: the
-    # argument's own status comes first
+    # oversized (1-2 MiB of chunk counts, depending on the SM count the chunk
+    # size follows) and a bad dtype / pointer: the argument's own status
+    # comes first
     assert lib.moe_dispatch_noalloc(*args(xdt=7)) == DTYPE
     assert lib.moe_dispatch_noalloc(*args(idx=P(None))) == NULL
     assert lib.moe_dispatch_noalloc(*args(x=P(FAKE_ODD))) == ALIGN
     assert lib.moe_dispatch_noalloc(*args(E=0)) == SHAPE
-    assert lib.moe_dispatch_workspace_size(32768, 8, 1024) > 256 * 1024
+    assert lib.moe_dispatch_workspace_size(262144, 8, 1024) > 256 * 1024
     assert lib.moe_dispatch_noalloc(*args()) == WORKSPACE
     assert lib.moe_dispatch_noalloc(*args(T=0, idx=P(None))) == OK

@@ -97,6 +97,14 @@ ROUTE_CASES = [
     (80000, 24, 8, True, "bf16", "ties"),
     (100000, 64, 8, True, "f32", "specials"),
     (12000, 40, 3, False, "bf16", "ties"),
+    # 16-bit logits with E % 8 == 0 at that T: the packed-pair kernel (rows
+    # padded to 8 / 16 / 32 / 64 logits with -inf where E is smaller)
+    (60000, 64, 8, True, "bf16", "specials"),
+    (50000, 16, 4, False, "f16", "specials"),
+    (40000, 48, 6, True, "f16", "ties"),
+    (30000, 8, 1, True, "bf16", "ties"),
+    (20000, 64, 6, False, "bf16", "extremes"),
+    (20000, 32, 5, True, "f16", "extremes"),
 ]
 
 
@@ -106,6 +114,14 @@ def _route_logits(T, E, ldt, kind, seed):
         l = torch.randint(-2, 3, (T, E), generator=g).float() * 0.5
     else:
         l = torch.randn((T, E), generator=g)
+    if kind == "extremes":
+        # rows near the dtype's largest values (BF16 ~3.4e38: exp(l - m) of
+        # such rows; F16 turns them into +-inf rows) and rows of subnormals
+        # (BF16 keeps 1e-39-scale values and their order; F16 makes them 0)
+        l[0::4] *= 1.0e38
+        l[1::4] *= 1.0e-39
+        l[2::4, ::2] *= 1.0e38
+        l[2::4, 1::2] *= 1.0e-39
     if kind == "specials":
         l[0, 3] = float("nan")
         l[1, :] = float("-inf")
