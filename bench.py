@@ -226,7 +226,7 @@ def run_ours(args, rank, world, local, dist):
     if args.workload in TRAINING_WORKLOADS:
         return run_training(args, rank, world, local, dist, dev, peaks, flush)
 
-    cfg = W.CONFIGS[args.workload]
+    cfg = forward_config(args.workload)
     d = W.moe_inputs(cfg, device=dev, seed=cfg.seed + 1000 * rank)
     T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.top_k
     A = T * k
@@ -406,6 +406,27 @@ def run_ours(args, rank, world, local, dist):
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, d, args.cpu_seconds)
     return line
+
+
+# Smaller cases of the forward workloads with the same per-expert shapes
+# (H, I) and routing, for profiler captures that must hold a few GB at most:
+# name -> (workload, overrides). The coarse prefill with 4 experts and 4096
+# tokens keeps about 2048 rows per expert; the decode shapes with 32 experts
+# keep the Zipf-skewed, weight-streaming decode GEMMs.
+SCALED_WORKLOADS = {
+    "coarse_prefill_e4_bf16": ("coarse_prefill_bf16", {"T": 4096, "E": 4}),
+    "decode_e32_bf16": ("decode_bf16", {"E": 32}),
+    "sigmoid_grouped_decode_e32_bf16": ("sigmoid_grouped_decode_bf16", {"E": 32}),
+}
+
+
+def forward_config(name):
+    """The MoeConfig of a forward workload or of one of its scaled cases."""
+    from mixture_experts_ffn_topk_gb300 import workloads as W
+    if name in SCALED_WORKLOADS:
+        base, overrides = SCALED_WORKLOADS[name]
+        return W.CONFIGS[base].scaled(name=name, **overrides)
+    return W.CONFIGS[name]
 
 
 def fold_combine(T, H, x):
@@ -992,11 +1013,11 @@ def run_reference(args, rank, world):
         return None
     import numpy as np
     from mixture_experts_ffn_topk_gb300 import workloads as W
-    if args.workload not in W.CONFIGS:
+    if args.workload not in W.CONFIGS and args.workload not in SCALED_WORKLOADS:
         return {"impl": "reference",
                 "unavailable": "the oracle reference arm times the one-call forward workloads "
                                f"only, not {args.workload}"}
-    cfg = W.CONFIGS[args.workload]
+    cfg = forward_config(args.workload)
     d = W.moe_inputs(cfg, device="cpu")
     host = host_inputs(cfg, d)
     threads = os.cpu_count() or 1

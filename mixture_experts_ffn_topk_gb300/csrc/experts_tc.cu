@@ -86,6 +86,10 @@ constexpr int TMEM_COLS = 2 * ACC_COLS;
 constexpr int THREADS = 192;
 constexpr int MAX_E = 1024;
 constexpr uint64_t kDrainLimitNs = 100000000ull;   // 100 ms per teardown drain
+// Bytes of A rows one m-block of an expert may cover (see decode_unit): well
+// inside the 129 MB L2, which also carries the streamed weights and the
+// outputs.
+constexpr int64_t kMBlockBytes = 48ll << 20;
 
 constexpr int EPI_ROW_BYTES = 128;           // epilogue staging: 32 rows x 128 B per warp
 
@@ -146,9 +150,15 @@ __device__ __forceinline__ int m_units(int seg_rows)
 // [256 j, 256 j + 256) of the expert's segment; when at most 128 of them
 // remain (`half`), the pair computes an M = 128 tile instead (64 rows per
 // CTA), so no CTA works on rows past the segment for nothing.
+// An expert's units run in m-blocks of up to `mblock` m-units: all n-tiles
+// of one m-block, the m-unit fastest, then the next m-block. The A rows of an
+// m-block (mblock x rows x K) are sized to stay in L2 while the block's
+// n-tiles stream the weights past them; without the blocks, an expert whose
+// A rows outgrow L2 (thousands of rows at K in the thousands) has them
+// re-read from DRAM for every round of n-tiles.
 template <int CG, typename SS>
-__device__ __forceinline__ void decode_unit(const SS &S, int E, int tile, int &e, int &n,
-                                            int &j, bool &half)
+__device__ __forceinline__ void decode_unit(const SS &S, int E, int tile, int n_tiles,
+                                            int mblock, int &e, int &n, int &j, bool &half)
 {
     int lo = 0, hi = E - 1;
     while (lo < hi) {
@@ -159,8 +169,12 @@ __device__ __forceinline__ void decode_unit(const SS &S, int E, int tile, int &e
     const int seg = S.offs[e + 1] - S.offs[e];
     const int mu = m_units<CG>(seg);
     const int local = tile - S.prefix[e];
-    n = local / mu;
-    j = local % mu;
+    const int span = mblock * n_tiles;            // units of one full m-block
+    const int b = local / span;
+    const int mb = mu - b * mblock < mblock ? mu - b * mblock : mblock;
+    const int rem = local - b * span;
+    n = rem / mb;
+    j = b * mblock + rem % mb;
     half = CG == 2 && seg - j * (BM * CG) <= BM;
 }
 
@@ -218,7 +232,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB0h,
                        const __grid_constant__ CUtensorMap tmB1h,
                        const int32_t *__restrict__ offsets, int E, int N, int K,
-                       int n_tiles, void *__restrict__ out, unsigned *status,
+                       int n_tiles, int mblock, void *__restrict__ out, unsigned *status,
                        CombineInto comb, uint64_t wait_ns)
 {
     using P = Pipe<CG>;
@@ -297,7 +311,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         for (int tile = unit0; tile < total_tiles; tile += unit_step) {
             int e, n, j;
             bool half;
-            decode_unit<CG>(S, E, tile, e, n, j, half);
+            decode_unit<CG>(S, E, tile, n_tiles, mblock, e, n, j, half);
             const int row0 = S.offs[e] + unit_row0<CG>(j, rank, half);
             bool ok = true;
             if (!SWIGLU && comb.ready != nullptr && e != ready_e) {
@@ -369,7 +383,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
             int e, n, j;
             bool half;
-            decode_unit<CG>(S, E, tile, e, n, j, half);
+            decode_unit<CG>(S, E, tile, n_tiles, mblock, e, n, j, half);
             const uint32_t idesc = half ? idesc_half : idesc_full;
             if (!mbar_wait<CG>(&S.acc_empty[acc], acc_phase ^ 1u, abort_flag, status, wait_ns)) { ok = false; break; }
             tc_fence_after();
@@ -417,7 +431,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         for (int tile = unit0; tile < total_tiles; tile += unit_step, ++it) {
             int e, n, j;
             bool half;
-            decode_unit<CG>(S, E, tile, e, n, j, half);
+            decode_unit<CG>(S, E, tile, n_tiles, mblock, e, n, j, half);
             const int seg_rows = S.offs[e + 1] - S.offs[e];
             // this warp's first row in the segment and first output column of
             // the tile: an M = 128 pair tile keeps a CTA's 64 rows in lanes
@@ -686,9 +700,12 @@ cudaError_t launch_gemm(int64_t units, cudaStream_t s, const CUtensorMap &ta, co
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = CG == 2 ? 2 : 1;
+    // m-blocks whose A rows take at most kMBlockBytes (see decode_unit)
+    int64_t mblock = kMBlockBytes / ((int64_t)BM * CG * K * 2);
+    mblock = mblock < 1 ? 1 : (mblock > (1 << 20) ? (1 << 20) : mblock);
     return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<DT, SWIGLU, OUT, CG>, ta, tah, tb0, tb1,
-                              tb0h, tb1h, offsets, E, N, K, n_tiles, out, status, comb,
-                              wait_limit_ns());
+                              tb0h, tb1h, offsets, E, N, K, n_tiles, (int)mblock, out, status,
+                              comb, wait_limit_ns());
 }
 
 // CTA pairs pay when experts average at least two M-tiles: a pair's second
