@@ -63,7 +63,10 @@ typedef enum moe_status {
     MOE_ERR_WORKSPACE = 6,      /* workspace too small or misaligned */
     MOE_ERR_CUDA = 7,           /* the CUDA runtime reported an error */
     MOE_ERR_DEVICE_TIMEOUT = 8, /* device status: a bounded wait gave up */
-    MOE_ERR_BAD_INDEX = 9       /* device status: an expert index >= E */
+    MOE_ERR_BAD_INDEX = 9,      /* device status: an expert index >= E */
+    MOE_ERR_BOUNDS = 10         /* device status (bounds-checking build only): an
+                                   index read from a buffer lay outside the buffer it
+                                   addresses; the access was skipped */
 } moe_status;
 
 /* Human-readable text of a status code; never NULL. */
@@ -248,7 +251,8 @@ int moe_experts_forward(const void *x_disp, const int32_t *offsets,
  *
  * y[t] = sum over j < top_k, in slot order, of weights[t,j] *
  * out_disp[row_of[t*top_k + j]], accumulated in FP32, rounded once to dtype.
- * A slot with row_of < 0 makes the token's row NaN. Needs H % 8 == 0.
+ * A slot with row_of < 0 or >= T * top_k (no row inside out_disp) makes the
+ * token's row NaN. Needs H % 8 == 0.
  * Errors: MOE_ERR_NULL, MOE_ERR_SHAPE, MOE_ERR_DTYPE, MOE_ERR_ALIGN,
  * MOE_ERR_CUDA.
  */
@@ -645,9 +649,20 @@ int moe_experts_backward(const void *x_disp, const int32_t *offsets, int64_t row
 
 /*
  * moe_device_status -- read the current device's status word.
- * Synchronises `stream`, then returns MOE_OK, MOE_ERR_BAD_INDEX or
- * MOE_ERR_DEVICE_TIMEOUT (the latter wins when both are set). If clear != 0
- * the word is reset to zero afterwards. MOE_ERR_CUDA if the read fails.
+ * Synchronises `stream`, then returns MOE_OK, MOE_ERR_BAD_INDEX,
+ * MOE_ERR_BOUNDS or MOE_ERR_DEVICE_TIMEOUT (when several are set, the
+ * timeout wins, then the bounds check). If clear != 0 the word is reset to
+ * zero afterwards. MOE_ERR_CUDA if the read fails.
+ *
+ * The bounds-checking build of the library (the same ABI, built with
+ * MOE_DEBUG_BOUNDS=1; the Python binding loads it when the environment
+ * variable MOE_DEBUG_BOUNDS is 1) also checks, on the device, the indices
+ * the kernels read from buffers before using them: the expert offsets given
+ * to the expert GEMMs (they must start at 0 and never fall), the rows the
+ * dispatch ranks (inside the expert's segment) and the map entries the
+ * gather follows (below T * top_k). A failed check skips the access and
+ * records MOE_ERR_BOUNDS. It is meant for tests and debugging, in place of
+ * a memory checker.
  * (Router training in the ruDNN user guide, section 12, fixes the same rule
  * for illegal indices: NaN rows, no out-of-bounds read, no host sync.)
  */

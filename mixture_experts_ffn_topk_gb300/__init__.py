@@ -28,6 +28,21 @@ import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_lib", "libmoe_gb300.so")
+LIB_PATH_DEBUG = os.path.join(_PKG, "_lib", "libmoe_gb300_debug.so")
+_DEFAULT_LIB_PATH = LIB_PATH
+
+
+def library_path(env=None) -> str:
+    """The library the binding loads: the bounds-checking build when the
+    environment variable MOE_DEBUG_BOUNDS is 1, the normal one when it is
+    unset, empty or 0; any other value is an error."""
+    env = os.environ if env is None else env
+    flag = env.get("MOE_DEBUG_BOUNDS", "")
+    if flag in ("", "0"):
+        return LIB_PATH
+    if flag == "1":
+        return LIB_PATH_DEBUG
+    raise ValueError(f"MOE_DEBUG_BOUNDS must be unset, 0 or 1, not {flag!r}")
 
 MOE_F32, MOE_BF16, MOE_F16 = 0, 1, 2
 DTYPE_CODES = {torch.float32: MOE_F32, torch.bfloat16: MOE_BF16,
@@ -36,7 +51,7 @@ DTYPE_CODES = {torch.float32: MOE_F32, torch.bfloat16: MOE_BF16,
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_NULL", 2: "MOE_ERR_SHAPE",
                 3: "MOE_ERR_DTYPE", 4: "MOE_ERR_VALUE", 5: "MOE_ERR_ALIGN",
                 6: "MOE_ERR_WORKSPACE", 7: "MOE_ERR_CUDA",
-                8: "MOE_ERR_DEVICE_TIMEOUT", 9: "MOE_ERR_BAD_INDEX"}
+                8: "MOE_ERR_DEVICE_TIMEOUT", 9: "MOE_ERR_BAD_INDEX", 10: "MOE_ERR_BOUNDS"}
 
 EXPORTED = ["moe_status_string", "moe_abi_version", "moe_last_error_detail",
             "moe_route", "moe_route_sigmoid_grouped", "moe_dispatch_workspace_size",
@@ -173,7 +188,8 @@ def load_library(path: str | None = None):
     global _lib
     with _lock:
         if _lib is None or path is not None:
-            p = path or LIB_PATH
+            # a LIB_PATH reassigned by the caller wins over the environment
+            p = path or (LIB_PATH if LIB_PATH != _DEFAULT_LIB_PATH else library_path())
             if not os.path.exists(p):
                 raise RuntimeError(
                     f"CUDA extension not built: {p} is missing; run "

@@ -132,7 +132,7 @@ combine_kernel(const void *__restrict__ out_disp, const void *__restrict__ w, in
                     const int64_t a = t * top_k + j;
                     const float wj = load_as_float(w, wdt, a);
                     const int32_t r = row_of[a];
-                    if (r < 0) { nan_row = true; continue; }
+                    if (r < 0 || (int64_t)r >= T * top_k) { nan_row = true; continue; }
                     const void *src = static_cast<const uint8_t *>(out_disp) + (int64_t)r * H * elem_o;
 #pragma unroll
                     for (int v = 0; v < V; ++v) {
@@ -173,7 +173,7 @@ combine_kernel(const void *__restrict__ out_disp, const void *__restrict__ w, in
                             wv = load_as_float(w, wdt, a);
                             if (k2 == kRouted) {
                                 const int32_t r = row_of[a];
-                                if (r < 0) k2 = kBad;
+                                if (r < 0 || (int64_t)r >= T * top_k) k2 = kBad;
                                 else off = (int64_t)r * H * elem_o;
                             }
                         }

@@ -14,7 +14,20 @@ enum : int { DT_F32 = 0, DT_BF16 = 1, DT_F16 = 2 };
 enum : int { IDX_U32 = 0, IDX_I32 = 1, IDX_I64 = 2 };
 
 // Bits of the per-device status word (see moe_device_status in moe.h).
-enum : unsigned { ST_BAD_INDEX = 1u, ST_TIMEOUT = 2u };
+enum : unsigned { ST_BAD_INDEX = 1u, ST_TIMEOUT = 2u, ST_BOUNDS = 4u };
+
+// Checks of the bounds-checking build (MOE_DEBUG_BOUNDS=1 at compile time):
+// MOE_BOUNDS_OK(cond, status) is true when cond holds; when it does not, it
+// records ST_BOUNDS in the status word and is false, so the caller skips the
+// access. In the normal build it is `true` and costs nothing.
+#ifndef MOE_DEBUG_BOUNDS
+#define MOE_DEBUG_BOUNDS 0
+#endif
+#if MOE_DEBUG_BOUNDS
+#define MOE_BOUNDS_OK(cond, status) ((cond) ? true : (atomicOr((status), ST_BOUNDS), false))
+#else
+#define MOE_BOUNDS_OK(cond, status) true
+#endif
 
 // Element access by dtype code. 16-bit types are loaded as raw words.
 template <int DT> struct Elem;

@@ -176,8 +176,9 @@ dispatch_rank_kernel(const uint32_t *__restrict__ idx, int64_t A, int E, int64_t
                      int64_t nchunks,
                      const int *__restrict__ chunk_base, const int32_t *__restrict__ counts,
                      int32_t *__restrict__ offsets, int32_t *__restrict__ row_of,
-                     int32_t *__restrict__ src_of)
+                     int32_t *__restrict__ src_of, unsigned *status)
 {
+    (void)status;
     extern __shared__ int smem[];
     const int nw = (int)(blockDim.x / 32);
     int *off = smem;                        // [E + 1] expert offsets
@@ -270,7 +271,9 @@ dispatch_rank_kernel(const uint32_t *__restrict__ idx, int64_t A, int E, int64_t
         int row = -1;
         if (ok) {
             row = mine[e] + __popc(peers & lt);
-            src_of[row] = (int32_t)a;
+            // bounds-checking build: the row lies inside the expert's segment
+            if (MOE_BOUNDS_OK(row >= off[e] && row < off[e + 1], status)) src_of[row] = (int32_t)a;
+            else row = -1;
         }
         if (act) row_of[a] = row;
         __syncwarp();
@@ -286,8 +289,9 @@ dispatch_rank_kernel(const uint32_t *__restrict__ idx, int64_t A, int E, int64_t
 __global__ void __launch_bounds__(256)
 dispatch_gather_rows_kernel(const uint4 *__restrict__ x, int64_t rows, int64_t per_row,
                             int top_k, const int32_t *__restrict__ src_of,
-                            uint4 *__restrict__ x_disp)
+                            uint4 *__restrict__ x_disp, unsigned *status)
 {
+    (void)status;
     // the next kernel (the first expert GEMM) is not let in before this
     // copy ends: its resident CTAs would take registers from the copy
     pdl_wait();
@@ -297,6 +301,7 @@ dispatch_gather_rows_kernel(const uint4 *__restrict__ x, int64_t rows, int64_t p
          r += warps) {
         const int32_t a = src_of[r];
         if (a < 0) continue;
+        if (!MOE_BOUNDS_OK((int64_t)a < rows, status)) continue;
         const uint4 *src = x + (int64_t)(a / top_k) * per_row;
         uint4 *dst = x_disp + r * per_row;
 #pragma unroll 4
@@ -310,8 +315,10 @@ dispatch_gather_rows_kernel(const uint4 *__restrict__ x, int64_t rows, int64_t p
 template <int PER>
 __global__ void __launch_bounds__(256)
 dispatch_gather_narrow_kernel(const uint4 *__restrict__ x, int64_t rows, int top_k,
-                              const int32_t *__restrict__ src_of, uint4 *__restrict__ x_disp)
+                              const int32_t *__restrict__ src_of, uint4 *__restrict__ x_disp,
+                              unsigned *status)
 {
+    (void)status;
     constexpr int U = 4;
     pdl_wait();
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -322,6 +329,7 @@ dispatch_gather_narrow_kernel(const uint4 *__restrict__ x, int64_t rows, int top
         for (int u = 0; u < U; ++u) {
             const int64_t r = r0 + u * stride;
             a[u] = r < rows ? src_of[r] : -1;
+            if (a[u] >= 0 && !MOE_BOUNDS_OK((int64_t)a[u] < rows, status)) a[u] = -1;
         }
         uint4 v[U][PER];
 #pragma unroll
@@ -344,14 +352,14 @@ dispatch_gather_narrow_kernel(const uint4 *__restrict__ x, int64_t rows, int top
 
 template <int PER>
 cudaError_t launch_gather_narrow(const uint4 *x, int64_t rows, int top_k, const int32_t *src_of,
-                                 uint4 *x_disp, cudaStream_t s)
+                                 uint4 *x_disp, unsigned *status, cudaStream_t s)
 {
     int64_t blocks = (rows + 1023) / 1024;
     const int64_t cap = (int64_t)device_sm_count() * 16;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     return launch_pdl(dispatch_gather_narrow_kernel<PER>, dim3((unsigned)blocks), dim3(256), 0, s,
-                      x, rows, top_k, src_of, x_disp);
+                      x, rows, top_k, src_of, x_disp, status);
 }
 
 template <bool VEC>
@@ -359,8 +367,9 @@ __global__ void __launch_bounds__(256)
 dispatch_gather_kernel(const uint8_t *__restrict__ x, int64_t rows,
                        int64_t row_bytes, int top_k,
                        const int32_t *__restrict__ src_of,
-                       uint8_t *__restrict__ x_disp)
+                       uint8_t *__restrict__ x_disp, unsigned *status)
 {
+    (void)status;
     pdl_wait();
     const int64_t unit = VEC ? 16 : 1;
     const int64_t per_row = row_bytes / unit;
@@ -370,6 +379,7 @@ dispatch_gather_kernel(const uint8_t *__restrict__ x, int64_t rows,
         const int64_t r = i / per_row, v = i - r * per_row;
         const int32_t a = src_of[r];
         if (a < 0) continue;
+        if (!MOE_BOUNDS_OK((int64_t)a < rows, status)) continue;
         const int64_t t = a / top_k;
         if (VEC)
             reinterpret_cast<uint4 *>(x_disp + r * row_bytes)[v] =
@@ -426,13 +436,13 @@ cudaError_t launch_dispatch(const uint32_t *idx, int64_t T, int top_k, int E, in
                      nchunks, E, counts);
     if (err != cudaSuccess) return err;
     return launch_dispatch_rank_gather(idx, T, top_k, E, x, xdt, H, counts, offsets, row_of,
-                                       src_of, x_disp, ws, s);
+                                       src_of, x_disp, ws, status, s);
 }
 
 cudaError_t launch_dispatch_rank_gather(const uint32_t *idx, int64_t T, int top_k, int E,
                                         const void *x, int xdt, int64_t H, const int32_t *counts,
                                         int32_t *offsets, int32_t *row_of, int32_t *src_of,
-                                        void *x_disp, void *ws, cudaStream_t s)
+                                        void *x_disp, void *ws, unsigned *status, cudaStream_t s)
 {
     const int64_t A = T * top_k;
     if (A == 0) return cudaSuccess;
@@ -461,8 +471,7 @@ cudaError_t launch_dispatch_rank_gather(const uint32_t *idx, int64_t T, int top_
     }
     err = launch_pdl(dispatch_rank_kernel, dim3((unsigned)nchunks), dim3(nw * 32), rank_bytes, s, idx,
                      A, E, chunk_len, nchunks, (const int *)chunk, (const int32_t *)counts,
-                     offsets, row_of,
-                     src_of);
+                     offsets, row_of, src_of, status);
     if (err != cudaSuccess) return err;
     const int64_t row_bytes = H * (xdt == DT_F32 ? 4 : 2);
     const bool vec = row_bytes % 16 == 0 && reinterpret_cast<uintptr_t>(x) % 16 == 0 &&
@@ -476,31 +485,31 @@ cudaError_t launch_dispatch_rank_gather(const uint32_t *idx, int64_t T, int top_
     const int32_t *so = src_of;
     if (vec && vpr <= 8) {
         switch (vpr) {
-        case 1: err = launch_gather_narrow<1>(xv, A, top_k, so, xdv, s); break;
-        case 2: err = launch_gather_narrow<2>(xv, A, top_k, so, xdv, s); break;
-        case 3: err = launch_gather_narrow<3>(xv, A, top_k, so, xdv, s); break;
-        case 4: err = launch_gather_narrow<4>(xv, A, top_k, so, xdv, s); break;
-        case 5: err = launch_gather_narrow<5>(xv, A, top_k, so, xdv, s); break;
-        case 6: err = launch_gather_narrow<6>(xv, A, top_k, so, xdv, s); break;
-        case 7: err = launch_gather_narrow<7>(xv, A, top_k, so, xdv, s); break;
-        default: err = launch_gather_narrow<8>(xv, A, top_k, so, xdv, s); break;
+        case 1: err = launch_gather_narrow<1>(xv, A, top_k, so, xdv, status, s); break;
+        case 2: err = launch_gather_narrow<2>(xv, A, top_k, so, xdv, status, s); break;
+        case 3: err = launch_gather_narrow<3>(xv, A, top_k, so, xdv, status, s); break;
+        case 4: err = launch_gather_narrow<4>(xv, A, top_k, so, xdv, status, s); break;
+        case 5: err = launch_gather_narrow<5>(xv, A, top_k, so, xdv, status, s); break;
+        case 6: err = launch_gather_narrow<6>(xv, A, top_k, so, xdv, status, s); break;
+        case 7: err = launch_gather_narrow<7>(xv, A, top_k, so, xdv, status, s); break;
+        default: err = launch_gather_narrow<8>(xv, A, top_k, so, xdv, status, s); break;
         }
     } else if (vec && row_bytes / 16 >= 32) {
         int64_t gblocks = (A + 7) / 8;
         if (gblocks > cap) gblocks = cap;
         err = launch_pdl(dispatch_gather_rows_kernel, dim3((unsigned)gblocks), dim3(256), 0, s,
                          reinterpret_cast<const uint4 *>(xb), A, row_bytes / 16, top_k,
-                         (const int32_t *)src_of, reinterpret_cast<uint4 *>(xd));
+                         (const int32_t *)src_of, reinterpret_cast<uint4 *>(xd), status);
     } else {
         const int64_t units = A * (vec ? row_bytes / 16 : row_bytes);
         int64_t gblocks = (units + 255) / 256;
         if (gblocks > cap) gblocks = cap;
         if (vec)
             err = launch_pdl(dispatch_gather_kernel<true>, dim3((unsigned)gblocks), dim3(256), 0,
-                             s, xb, A, row_bytes, top_k, (const int32_t *)src_of, xd);
+                             s, xb, A, row_bytes, top_k, (const int32_t *)src_of, xd, status);
         else
             err = launch_pdl(dispatch_gather_kernel<false>, dim3((unsigned)gblocks), dim3(256),
-                             0, s, xb, A, row_bytes, top_k, (const int32_t *)src_of, xd);
+                             0, s, xb, A, row_bytes, top_k, (const int32_t *)src_of, xd, status);
     }
     if (err != cudaSuccess) return err;
     return cudaGetLastError();

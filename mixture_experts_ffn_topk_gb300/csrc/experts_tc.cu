@@ -270,6 +270,20 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     // grid-level wait, so no line may come from a stale L1)
     for (int i = threadIdx.x; i <= E; i += THREADS) S.offs[i] = __ldcg(offsets + i);
     __syncthreads();
+#if MOE_DEBUG_BOUNDS
+    // bounds-checking build: the caller's offsets start at 0 and never fall;
+    // otherwise the launch records ST_BOUNDS and computes nothing
+    {
+        int bad = 0;
+        for (int i = threadIdx.x; i < E; i += THREADS) bad |= S.offs[i + 1] < S.offs[i];
+        bad |= S.offs[0] != 0;
+        if (__syncthreads_or(bad)) {
+            if (threadIdx.x == 0) atomicOr(status, ST_BOUNDS);
+            for (int i = threadIdx.x; i <= E; i += THREADS) S.offs[i] = 0;
+            __syncthreads();
+        }
+    }
+#endif
     if (warp == 0) {
         // prefix[e] = tiles of experts < e; lane l owns a contiguous run of experts
         const int per = (E + 31) / 32, e0 = lane * per;

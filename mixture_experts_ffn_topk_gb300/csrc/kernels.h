@@ -54,7 +54,7 @@ unsigned *dispatch_done_counter(void *ws, int64_t A, int E);
 cudaError_t launch_dispatch_rank_gather(const uint32_t *idx, int64_t T, int top_k, int E,
                                         const void *x, int xdt, int64_t H, const int32_t *counts,
                                         int32_t *offsets, int32_t *row_of, int32_t *src_of,
-                                        void *x_disp, void *ws, cudaStream_t s);
+                                        void *x_disp, void *ws, unsigned *status, cudaStream_t s);
 // Routing fused with the dispatch's chunk counts and their scan (one kernel:
 // each CTA routes the tokens of one assignment chunk and counts them; the
 // last CTA to finish scans the counts), then the rank/scatter and the gather:

@@ -333,6 +333,7 @@ const char *moe_status_string(int status)
     case MOE_ERR_CUDA: return "CUDA runtime error";
     case MOE_ERR_DEVICE_TIMEOUT: return "a bounded device wait gave up";
     case MOE_ERR_BAD_INDEX: return "an expert index >= E reached dispatch";
+    case MOE_ERR_BOUNDS: return "a device-side bounds check failed (bounds-checking build)";
     default: return "unknown status";
     }
 }
@@ -962,6 +963,7 @@ int moe_device_status(void *stream, int clear)
         if (err != cudaSuccess) return cuda_fail(err, "moe_device_status/clear");
     }
     if (v & ST_TIMEOUT) return MOE_ERR_DEVICE_TIMEOUT;
+    if (v & ST_BOUNDS) return MOE_ERR_BOUNDS;
     if (v & ST_BAD_INDEX) return MOE_ERR_BAD_INDEX;
     return MOE_OK;
 }

@@ -770,7 +770,7 @@ cudaError_t launch_route_dispatch(const void *logits, int ldt, int64_t T, int E,
     }
     if (err != cudaSuccess) return err;
     return launch_dispatch_rank_gather(idx, T, top_k, E, x, xdt, H, counts, offsets, row_of,
-                                       src_of, x_disp, ws, s);
+                                       src_of, x_disp, ws, status, s);
 }
 
 cudaError_t launch_route(const void *logits, int ldt, int64_t T, int E,

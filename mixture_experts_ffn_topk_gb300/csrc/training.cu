@@ -275,7 +275,7 @@ combine_backward_kernel(const void *__restrict__ out_disp, const void *__restric
     const int64_t ob = ODT == DT_F32 ? 4 : 2, eb = DT == DT_F32 ? 4 : 2;
     for (int64_t a = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5); a < A; a += nwarps) {
         const int64_t r = row_of[a];
-        if (r < 0) {
+        if (r < 0 || r >= A) {             // no row (or none inside out_disp)
             if (lane == 0) dw[a] = __int_as_float(0x7fc00000);
             continue;
         }
@@ -326,7 +326,7 @@ dispatch_backward_kernel(const void *__restrict__ d, const int32_t *__restrict__
                 const int n = k - j0 < 32 ? k - j0 : 32;
                 for (int j = 0; j < n; ++j) {
                     const int64_t r = __shfl_sync(0xffffffffu, rj, j);
-                    if (r < 0 || !on) continue;
+                    if (r < 0 || r >= T * k || !on) continue;
                     float v[8];
                     load8<DT>(static_cast<const uint8_t *>(d) + r * H * eb, c, v);
 #pragma unroll

@@ -48,7 +48,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(10):
+    for code in range(11):
         assert moe.moe_status_string(code)
     assert moe.moe_status_string(99) == "unknown status"
     assert moe.moe_abi_version() == 101
@@ -524,3 +524,22 @@ def test_dispatch_noalloc_validation_order(lib):
     assert lib.moe_dispatch_workspace_size(262144, 8, 1024) > 256 * 1024
     assert lib.moe_dispatch_noalloc(*args()) == WORKSPACE
     assert lib.moe_dispatch_noalloc(*args(T=0, idx=P(None))) == OK
+
+
+def test_bounds_build_flag_rule():
+    """MOE_DEBUG_BOUNDS: unset, empty or 0 loads the normal library, 1 the
+    bounds-checking one, anything else is an error."""
+    assert moe.library_path({}) == moe.LIB_PATH
+    assert moe.library_path({"MOE_DEBUG_BOUNDS": "0"}) == moe.LIB_PATH
+    assert moe.library_path({"MOE_DEBUG_BOUNDS": ""}) == moe.LIB_PATH
+    assert moe.library_path({"MOE_DEBUG_BOUNDS": "1"}) == moe.LIB_PATH_DEBUG
+    for bad in ("2", "yes", "true", " 1"):
+        with pytest.raises(ValueError):
+            moe.library_path({"MOE_DEBUG_BOUNDS": bad})
+
+
+def test_bounds_build_exports_the_same_abi():
+    path = build.build(debug_bounds=True)
+    raw = ctypes.CDLL(path)
+    for name in declared_functions():
+        assert hasattr(raw, name), name
