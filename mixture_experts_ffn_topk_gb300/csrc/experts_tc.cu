@@ -27,7 +27,10 @@
 // own 128 x rows and HALF of the 256 weight rows (the MMA reads the other
 // half from the peer's shared memory), so a stage is 32 KiB per CTA instead
 // of 48 and six stages fit: the load pipeline covers 2.5x more MMA time,
-// which the load-latency-bound prefill GEMMs need. The even CTA issues the
+// which the load-latency-bound prefill GEMMs need. For experts with many
+// rows (long, L2-fed, MMA-bound units) the pair runs the same shared memory
+// as three stages of two k-blocks, each operand's two k-blocks fetched by
+// one TMA box of a [K / 64][rows][64] view. The even CTA issues the
 // MMAs and commits them to both CTAs' barriers; both CTAs' TMA copies
 // complete on the even CTA's stage barrier; both CTAs' epilogues read their
 // own TMEM and release the accumulator on the even CTA's barrier.
@@ -74,12 +77,16 @@ constexpr int BN = 256;                      // B rows per tile (UMMA N)
 constexpr int A_BYTES = BM * BK * 2;         // 16 KiB
 
 // Per-CTA pipeline shape for one CTA per tile (CG = 1) or a CTA pair (CG = 2).
+// A pair may run its ring as three stages of two k-blocks each (kps = 2):
+// half as many barrier round trips and commits per unit, for the long,
+// L2-fed units of experts with many rows; short units fed from DRAM keep
+// six single-k-block stages (the finer ring hides more load latency).
 template <int CG>
 struct Pipe {
     static constexpr int B_ROWS = BN / CG;                     // weight rows this CTA loads
-    static constexpr int B_BYTES = B_ROWS * BK * 2;            // 32 / 16 KiB
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;      // 48 / 32 KiB
-    static constexpr int STAGES = CG == 2 ? 6 : 4;
+    static constexpr int B_BYTES = B_ROWS * BK * 2;            // per k-block: 32 / 16 KiB
+    static constexpr int SLOT_BYTES = A_BYTES + B_BYTES;       // 48 / 32 KiB
+    static constexpr int SLOTS = CG == 2 ? 6 : 4;              // single-k-block stages
 };
 constexpr int ACC_COLS = 256;                // fp32 columns per accumulator
 constexpr int TMEM_COLS = 2 * ACC_COLS;
@@ -122,10 +129,12 @@ struct CombineInto {
 
 template <int CG>
 struct __align__(1024) SharedStorage {
-    uint8_t stage[Pipe<CG>::STAGES][Pipe<CG>::STAGE_BYTES];   // each stage 1024-byte aligned
+    // the stage ring: stage i of a kps-k-block ring starts at slot i * kps
+    // and holds the A tiles of its k-blocks, then their B tiles
+    uint8_t slot[Pipe<CG>::SLOTS][Pipe<CG>::SLOT_BYTES];      // each 1024-byte aligned
     uint8_t epi[4][32 * EPI_ROW_BYTES];      // per epilogue warp, 16-byte chunks swizzled
-    uint64_t full[Pipe<CG>::STAGES];
-    uint64_t empty[Pipe<CG>::STAGES];
+    uint64_t full[Pipe<CG>::SLOTS];
+    uint64_t empty[Pipe<CG>::SLOTS];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t drain;
@@ -223,7 +232,7 @@ __device__ __forceinline__ bool wait_counter(const unsigned *c, unsigned need,
 
 // ---- the kernel -------------------------------------------------------------
 
-template <int DT, bool SWIGLU, int OUT, int CG>
+template <int DT, bool SWIGLU, int OUT, int CG, int KPS>
 __global__ void __launch_bounds__(THREADS, 1)
 grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmAh,
@@ -233,16 +242,23 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB1h,
                        const int32_t *__restrict__ offsets, int E, int N, int K,
                        int n_tiles, int mblock, void *__restrict__ out, unsigned *status,
-                       CombineInto comb, uint64_t wait_ns)
+                       CombineInto comb, uint64_t wait_ns, int kbox)
 {
+    // KPS: k-blocks per pipeline stage (1, or 2 on a pair); kbox: the A and
+    // B maps (not the M = 128 SwiGLU weight maps) give boxes of KPS
+    // k-blocks (else one box per k-block)
+    static_assert(KPS == 1 || (KPS == 2 && CG == 2), "two k-blocks per stage on pairs only");
     using P = Pipe<CG>;
-    constexpr int STAGES = P::STAGES;
+    constexpr int kps = KPS;
+    constexpr int n_stages = P::SLOTS / KPS;
+    if (CG == 1) (void)kbox;
     extern __shared__ uint8_t smem_raw[];
     SharedStorage<CG> &S = *reinterpret_cast<SharedStorage<CG> *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr int N_OUT = SWIGLU ? BN / 2 : BN;      // output columns per tile
     const int num_kb = (K + BK - 1) / BK;
+    const int num_ks = (num_kb + kps - 1) / kps;    // pipeline stages per unit
     // CTA pair: rank 0 issues the MMAs and owns the stage and accumulator
     // barriers that both CTAs' copies and epilogues signal
     const int rank = CG == 2 ? (int)cluster_ctarank() : 0;
@@ -250,7 +266,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     const int unit0 = (int)blockIdx.x / CG, unit_step = (int)gridDim.x / CG;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) { mbar_init(&S.full[s], 1); mbar_init(&S.empty[s], 1); }
+        for (int s = 0; s < n_stages; ++s) { mbar_init(&S.full[s], 1); mbar_init(&S.empty[s], 1); }
         for (int a = 0; a < 2; ++a) { mbar_init(&S.acc_full[a], 1); mbar_init(&S.acc_empty[a], 4 * CG); }
         mbar_init(&S.drain, 1);
         S.abort = 0;
@@ -336,51 +352,67 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                 asm volatile("fence.proxy.async.global;" ::: "memory");
                 ready_e = e;
             }
-            for (int kb = 0; kb < num_kb; ++kb) {
+            for (int ks = 0; ks < num_ks; ++ks) {
                 if (!mbar_wait<CG>(&S.empty[stage], phase ^ 1u, abort_flag, status, wait_ns)) { ok = false; break; }
-                uint8_t *sa = S.stage[stage];
-                uint8_t *sb = sa + A_BYTES;
+                uint8_t *sa = S.slot[stage * kps];
+                uint8_t *sb = sa + kps * A_BYTES;
+                const int kb0 = ks * kps;
+                // k-blocks of this stage inside K (the last stage of an odd count
+                // with kps = 2 has one)
+                const int nkb = num_kb - kb0 < kps ? num_kb - kb0 : kps;
                 if constexpr (CG == 2) {
+                    const int a_kb = half ? A_BYTES / 2 : A_BYTES;      // A bytes per k-block
+                    // a box of kps k-blocks always lands whole (zero fill past
+                    // K); one-k-block boxes are issued inside K only
+                    const int a_bytes = (kbox ? kps : nkb) * a_kb;
+                    const int b_bytes = ((half && SWIGLU) || !kbox ? nkb : kps) * P::B_BYTES;
                     // the leader's barrier expects both CTAs' bytes; a peer's
                     // copy may land before the leader arms it (the phase
                     // cannot complete while the leader's arrival is pending)
-                    if (leader)
-                        mbar_arrive_expect_tx(&S.full[stage],
-                                              2 * (half ? P::STAGE_BYTES - A_BYTES / 2 : P::STAGE_BYTES));
+                    if (leader) mbar_arrive_expect_tx(&S.full[stage], 2 * (a_bytes + b_bytes));
                     const uint32_t bar = mapa_shared(smem_u32(&S.full[stage]), 0);
-                    if (half) {
-                        // 64 rows of A per CTA; for SwiGLU each CTA holds 64 gate
-                        // rows over the same 64 up rows, so each TMEM lane half
-                        // of the M = 128 tile sees both factors of 64 h columns
-                        tma_load_2d_pair(sa, &tmAh, bar, kb * BK, row0);
-                        if (SWIGLU) {
-                            const int c1 = n * (BN / 2) + rank * (BN / 4);
-                            tma_load_3d_pair(sb, &tmB0h, bar, kb * BK, c1, e);
-                            tma_load_3d_pair(sb + P::B_BYTES / 2, &tmB1h, bar, kb * BK, c1, e);
-                        } else {
-                            tma_load_3d_pair(sb, &tmB0, bar, kb * BK, n * BN + rank * (BN / 2), e);
+                    const CUtensorMap *ma = half ? &tmAh : &tmA;
+                    if (kbox) {
+                        tma_load_3d_pair(sa, ma, bar, 0, row0, kb0);
+                    } else {
+                        for (int q = 0; q < nkb; ++q)
+                            tma_load_2d_pair(sa + q * a_kb, ma, bar, (kb0 + q) * BK, row0);
+                    }
+                    if (half && SWIGLU) {
+                        // 64 rows of A per CTA; each CTA holds 64 gate rows over
+                        // the same 64 up rows, so each TMEM lane half of the
+                        // M = 128 tile sees both factors of 64 h columns
+                        const int c1 = n * (BN / 2) + rank * (BN / 4);
+                        for (int q = 0; q < nkb; ++q) {
+                            uint8_t *dq = sb + q * P::B_BYTES;
+                            tma_load_3d_pair(dq, &tmB0h, bar, (kb0 + q) * BK, c1, e);
+                            tma_load_3d_pair(dq + P::B_BYTES / 2, &tmB1h, bar, (kb0 + q) * BK, c1, e);
                         }
                     } else {
-                        tma_load_2d_pair(sa, &tmA, bar, kb * BK, row0);
-                        if (SWIGLU)      // CTA 0 holds the gate rows, CTA 1 the up rows
-                            tma_load_3d_pair(sb, rank == 0 ? &tmB0 : &tmB1, bar, kb * BK, n * (BN / 2), e);
-                        else
-                            tma_load_3d_pair(sb, &tmB0, bar, kb * BK, n * BN + rank * (BN / 2), e);
+                        // SwiGLU: CTA 0 holds the gate rows, CTA 1 the up rows
+                        const CUtensorMap *mb = SWIGLU && rank == 1 ? &tmB1 : &tmB0;
+                        const int nrow = SWIGLU ? n * (BN / 2) : n * BN + rank * (BN / 2);
+                        if (kbox) {
+                            tma_load_4d_pair(sb, mb, bar, 0, nrow, kb0, e);
+                        } else {
+                            for (int q = 0; q < nkb; ++q)
+                                tma_load_3d_pair(sb + q * P::B_BYTES, mb, bar, (kb0 + q) * BK, nrow, e);
+                        }
                     }
                 } else {
-                    (void)half;
-                    mbar_arrive_expect_tx(&S.full[stage], P::STAGE_BYTES);
-                    tma_load_2d(sa, &tmA, &S.full[stage], kb * BK, row0);
+                    (void)half; (void)nkb;
+                    mbar_arrive_expect_tx(&S.full[stage], P::SLOT_BYTES);
+                    tma_load_2d(sa, &tmA, &S.full[stage], kb0 * BK, row0);
                     if (SWIGLU) {
-                        tma_load_3d(sb, &tmB0, &S.full[stage], kb * BK, n * (BN / 2), e);
-                        tma_load_3d(sb + P::B_BYTES / 2, &tmB1, &S.full[stage], kb * BK, n * (BN / 2), e);
+                        tma_load_3d(sb, &tmB0, &S.full[stage], kb0 * BK, n * (BN / 2), e);
+                        tma_load_3d(sb + P::B_BYTES / 2, &tmB1, &S.full[stage], kb0 * BK, n * (BN / 2), e);
                     } else {
-                        tma_load_3d(sb, &tmB0, &S.full[stage], kb * BK, n * BN, e);
+                        tma_load_3d(sb, &tmB0, &S.full[stage], kb0 * BK, n * BN, e);
                     }
                 }
                 filled_mask |= 1u << stage;
                 filled_parity = (filled_parity & ~(1u << stage)) | (phase << stage);
-                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                if (++stage == n_stages) { stage = 0; phase ^= 1u; }
             }
             if (!ok) break;
         }
@@ -402,18 +434,26 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             if (!mbar_wait<CG>(&S.acc_empty[acc], acc_phase ^ 1u, abort_flag, status, wait_ns)) { ok = false; break; }
             tc_fence_after();
             const uint32_t d = tmem_base + (uint32_t)(acc * ACC_COLS);
-            for (int kb = 0; kb < num_kb; ++kb) {
+            const uint32_t a_kb = half ? A_BYTES / 2 : A_BYTES;     // A bytes per k-block
+            for (int ks = 0; ks < num_ks; ++ks) {
                 if (!mbar_wait<CG>(&S.full[stage], phase, abort_flag, status, wait_ns)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t a0 = smem_u32(S.stage[stage]);
-                const uint32_t b0 = a0 + A_BYTES;
+                const uint32_t a0 = smem_u32(S.slot[stage * kps]);
+                const uint32_t b0 = a0 + (uint32_t)(kps * A_BYTES);
+                const int nkb = num_kb - ks * kps < kps ? num_kb - ks * kps : kps;
 #pragma unroll
-                for (int k = 0; k < BK / UK; ++k)
-                    umma_f16<CG>(d, sdesc_k_sw128(a0 + k * UK * 2), sdesc_k_sw128(b0 + k * UK * 2),
-                                 idesc, (kb | k) != 0 ? 1u : 0u);
+                for (int q = 0; q < KPS; ++q) {
+                    if (q < nkb) {
+#pragma unroll
+                        for (int k = 0; k < BK / UK; ++k)
+                            umma_f16<CG>(d, sdesc_k_sw128(a0 + q * a_kb + k * UK * 2),
+                                         sdesc_k_sw128(b0 + q * P::B_BYTES + k * UK * 2),
+                                         idesc, (ks | q | k) != 0 ? 1u : 0u);
+                    }
+                }
                 if constexpr (CG == 2) umma_commit_pair(&S.empty[stage]);
                 else umma_commit<CG>(&S.empty[stage]);
-                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                if (++stage == n_stages) { stage = 0; phase ^= 1u; }
             }
             if (ok) {
                 if constexpr (CG == 2) umma_commit_pair(&S.acc_full[acc]);
@@ -598,7 +638,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     if (*abort_flag && warp == 0 && lane == 0) {
         if (CG == 1 || leader) {
             // let the outstanding TMA copies land before shared memory goes
-            for (int s = 0; s < STAGES; ++s)
+            for (int s = 0; s < n_stages; ++s)
                 if (filled_mask >> s & 1u)
                     mbar_wait(&S.full[s], filled_parity >> s & 1u, nullptr, status, kDrainLimitNs);
         } else {
@@ -623,7 +663,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
 
 
 // The dynamic shared-memory opt-in is per device and per kernel instance.
-template <int DT, bool SWIGLU, int OUT, int CG>
+template <int DT, bool SWIGLU, int OUT, int CG, int KPS>
 cudaError_t ensure_smem_attr()
 {
     static std::atomic<uint64_t> done_mask{0};
@@ -632,7 +672,7 @@ cudaError_t ensure_smem_attr()
     if (err != cudaSuccess) return err;
     const uint64_t bit = dev >= 0 && dev < kCachedDevices ? 1ull << dev : 0ull;
     if (bit != 0 && (done_mask.load() & bit)) return cudaSuccess;
-    err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<DT, SWIGLU, OUT, CG>,
+    err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<DT, SWIGLU, OUT, CG, KPS>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes<CG>);
     if (err == cudaSuccess) done_mask.fetch_or(bit);
     return err;
@@ -650,7 +690,7 @@ int64_t tc_unit_upper_bound(int64_t rows, int E, int64_t n_tiles, int cg)
 // CTAs to launch: one per SM for CG = 1; for CG = 2 twice the number of
 // pairs the GPU holds at once (cluster placement can leave SMs unpaired), so
 // the persistent grid is always a single wave.
-template <int DT, bool SWIGLU, int OUT, int CG>
+template <int DT, bool SWIGLU, int OUT, int CG, int KPS>
 cudaError_t grid_size(int64_t units, int *grid)
 {
     const int64_t sms = device_sm_count();
@@ -676,7 +716,8 @@ cudaError_t grid_size(int64_t units, int *grid)
             attr[0].val.clusterDim.z = 1;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
-            err = cudaOccupancyMaxActiveClusters(&pairs, grouped_gemm_tc_kernel<DT, SWIGLU, OUT, CG>, &cfg);
+            err = cudaOccupancyMaxActiveClusters(&pairs, grouped_gemm_tc_kernel<DT, SWIGLU, OUT, CG, KPS>,
+                                                 &cfg);
             if (err != cudaSuccess) return err;
             if (pairs < 1) return cudaErrorInvalidConfiguration;
             if (use_cache) cached[dev].store(pairs);
@@ -688,17 +729,17 @@ cudaError_t grid_size(int64_t units, int *grid)
 
 // Programmatic dependent launch (unless pdl is false: plain stream order),
 // in clusters of CG CTAs.
-template <int DT, bool SWIGLU, int OUT, int CG>
+template <int DT, bool SWIGLU, int OUT, int CG, int KPS>
 cudaError_t launch_gemm(int64_t units, cudaStream_t s, const CUtensorMap &ta, const CUtensorMap &tah,
                         const CUtensorMap &tb0, const CUtensorMap &tb1, const CUtensorMap &tb0h,
                         const CUtensorMap &tb1h, const int32_t *offsets, int E, int N, int K,
                         int n_tiles, void *out, unsigned *status, const CombineInto &comb,
-                        bool pdl = true)
+                        int kbox = 0, bool pdl = true)
 {
-    cudaError_t err = ensure_smem_attr<DT, SWIGLU, OUT, CG>();
+    cudaError_t err = ensure_smem_attr<DT, SWIGLU, OUT, CG, KPS>();
     if (err != cudaSuccess) return err;
     int grid = 0;
-    err = grid_size<DT, SWIGLU, OUT, CG>(units, &grid);
+    err = grid_size<DT, SWIGLU, OUT, CG, KPS>(units, &grid);
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
@@ -717,14 +758,60 @@ cudaError_t launch_gemm(int64_t units, cudaStream_t s, const CUtensorMap &ta, co
     // m-blocks whose A rows take at most kMBlockBytes (see decode_unit)
     int64_t mblock = kMBlockBytes / ((int64_t)BM * CG * K * 2);
     mblock = mblock < 1 ? 1 : (mblock > (1 << 20) ? (1 << 20) : mblock);
-    return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<DT, SWIGLU, OUT, CG>, ta, tah, tb0, tb1,
+    return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<DT, SWIGLU, OUT, CG, KPS>, ta, tah, tb0, tb1,
                               tb0h, tb1h, offsets, E, N, K, n_tiles, (int)mblock, out, status,
-                              comb, wait_limit_ns());
+                              comb, wait_limit_ns(), kbox);
 }
 
 // CTA pairs pay when experts average at least two M-tiles: a pair's second
 // M-tile past an expert's rows is computed for nothing.
 constexpr int64_t kPairMinRowsPerExpert = 2 * BM;
+// Two k-blocks per stage pay when experts average at least 2048 rows (each
+// weight tile then serves eight or more pair units from L2, and the
+// launches are bound by the MMAs, not by load latency): on the coarse
+// prefill shapes (4096 rows per expert) GEMM1 4.43 -> 4.23 ms; with 384
+// rows per expert (weights streamed from DRAM) both GEMMs were 3-4 % slower.
+constexpr int64_t kTwoKbMinRowsPerExpert = 2048;
+
+// Tensor maps of both GEMMs (x / h rows, gate / up / down weights, the
+// M = 128 pair tile's boxes) and whether their A / B maps give two-k-block
+// boxes.
+struct TcMaps {
+    CUtensorMap mx, mxh, mg, mu, mgh, muh, mh, mhh, md;
+    int kbox1, kbox2;
+};
+
+// GEMM1 (SwiGLU into h_ws) then GEMM2 (out_mode) with KPS k-blocks per stage.
+template <int DT, int CG, int KPS>
+cudaError_t launch_gemm_pair(const TcMaps &m, const int32_t *offsets, int64_t rows, int E,
+                             int64_t H, int64_t I, void *h_ws, void *out, int out_mode,
+                             const CombineInto &comb, unsigned *status, cudaStream_t s)
+{
+    const int nt1 = (int)((I + BN / 2 - 1) / (BN / 2));
+    const int nt2 = (int)((H + BN - 1) / BN);
+    const int64_t u1 = tc_unit_upper_bound(rows, E, nt1, CG);
+    const int64_t u2 = tc_unit_upper_bound(rows, E, nt2, CG);
+    cudaError_t err =
+        comb.g_out != nullptr
+            ? launch_gemm<DT, true, kOutSaveGU, CG, KPS>(u1, s, m.mx, m.mxh, m.mg, m.mu, m.mgh,
+                                                        m.muh, offsets, E, (int)I, (int)H, nt1,
+                                                        h_ws, status, comb, m.kbox1)
+            : launch_gemm<DT, true, kOutDtype, CG, KPS>(u1, s, m.mx, m.mxh, m.mg, m.mu, m.mgh,
+                                                       m.muh, offsets, E, (int)I, (int)H, nt1,
+                                                       h_ws, status, comb, m.kbox1);
+    if (err != cudaSuccess) return err;
+    if (out_mode == kOutF32)
+        return launch_gemm<DT, false, kOutF32, CG, KPS>(u2, s, m.mh, m.mhh, m.md, m.md, m.md,
+                                                        m.md, offsets, E, (int)H, (int)I, nt2,
+                                                        out, status, comb, m.kbox2);
+    if (out_mode == kOutCombine)
+        return launch_gemm<DT, false, kOutCombine, CG, KPS>(u2, s, m.mh, m.mhh, m.md, m.md, m.md,
+                                                            m.md, offsets, E, (int)H, (int)I, nt2,
+                                                            out, status, comb, m.kbox2);
+    return launch_gemm<DT, false, kOutDtype, CG, KPS>(u2, s, m.mh, m.mhh, m.md, m.md, m.md, m.md,
+                                                      offsets, E, (int)H, (int)I, nt2, out,
+                                                      status, comb, m.kbox2);
+}
 
 template <int DT, int CG>
 cudaError_t launch_tc_cg(const void *x_disp, const int32_t *offsets, int64_t rows,
@@ -749,25 +836,32 @@ cudaError_t launch_tc_cg(const void *x_disp, const int32_t *offsets, int64_t row
          !encode_3d(&mgh, tdt, gate, (uint64_t)H, (uint64_t)I, (uint64_t)E, BK, BN / 4) ||
          !encode_3d(&muh, tdt, up, (uint64_t)H, (uint64_t)I, (uint64_t)E, BK, BN / 4)))
         return cudaErrorInvalidValue;
-    const int nt1 = (int)((I + BN / 2 - 1) / (BN / 2));
-    const int nt2 = (int)((H + BN - 1) / BN);
-    const int64_t u1 = tc_unit_upper_bound(rows, E, nt1, CG);
-    const int64_t u2 = tc_unit_upper_bound(rows, E, nt2, CG);
-    cudaError_t err =
-        comb.g_out != nullptr
-            ? launch_gemm<DT, true, kOutSaveGU, CG>(u1, s, mx, mxh, mg, mu, mgh, muh, offsets, E,
-                                                   (int)I, (int)H, nt1, h_ws, status, comb)
-            : launch_gemm<DT, true, kOutDtype, CG>(u1, s, mx, mxh, mg, mu, mgh, muh, offsets, E,
-                                                  (int)I, (int)H, nt1, h_ws, status, comb);
-    if (err != cudaSuccess) return err;
-    if (out_mode == kOutF32)
-        return launch_gemm<DT, false, kOutF32, CG>(u2, s, mh, mhh, md, md, md, md, offsets, E,
-                                                   (int)H, (int)I, nt2, out, status, comb);
-    if (out_mode == kOutCombine)
-        return launch_gemm<DT, false, kOutCombine, CG>(u2, s, mh, mhh, md, md, md, md, offsets, E,
-                                                       (int)H, (int)I, nt2, out, status, comb);
-    return launch_gemm<DT, false, kOutDtype, CG>(u2, s, mh, mhh, md, md, md, md, offsets, E,
-                                                 (int)H, (int)I, nt2, out, status, comb);
+    // Experts with many rows: two k-blocks per stage, in boxes of two
+    // k-blocks where K is a whole number of them
+    const int kps = CG == 2 && rows >= kTwoKbMinRowsPerExpert * E ? 2 : 1;
+    int kbox1 = 0, kbox2 = 0;
+    if (kps == 2) {
+        CUtensorMap t0, t1, t2, t3;
+        if (encode_kblocks(&t0, tdt, x_disp, (uint64_t)H, (uint64_t)rows, BM, 2) &&
+            encode_kblocks(&t1, tdt, x_disp, (uint64_t)H, (uint64_t)rows, BM / 2, 2) &&
+            encode_kblocks_e(&t2, tdt, gate, (uint64_t)H, (uint64_t)I, (uint64_t)E, BN / 2, 2) &&
+            encode_kblocks_e(&t3, tdt, up, (uint64_t)H, (uint64_t)I, (uint64_t)E, BN / 2, 2)) {
+            mx = t0; mxh = t1; mg = t2; mu = t3; kbox1 = 1;
+        }
+        if (encode_kblocks(&t0, tdt, h_ws, (uint64_t)I, (uint64_t)rows, BM, 2) &&
+            encode_kblocks(&t1, tdt, h_ws, (uint64_t)I, (uint64_t)rows, BM / 2, 2) &&
+            encode_kblocks_e(&t2, tdt, down, (uint64_t)I, (uint64_t)H, (uint64_t)E, BN / CG, 2)) {
+            mh = t0; mhh = t1; md = t2; kbox2 = 1;
+        }
+    }
+    const TcMaps m{mx, mxh, mg, mu, mgh, muh, mh, mhh, md, kbox1, kbox2};
+    if constexpr (CG == 2) {
+        if (kps == 2)
+            return launch_gemm_pair<DT, CG, 2>(m, offsets, rows, E, H, I, h_ws, out, out_mode,
+                                               comb, status, s);
+    }
+    return launch_gemm_pair<DT, CG, 1>(m, offsets, rows, E, H, I, h_ws, out, out_mode, comb,
+                                       status, s);
 }
 
 // GEMM2 of the one-call forward on its own: h [rows, I] times down, each row
@@ -790,9 +884,9 @@ cudaError_t launch_down_combine_cg(const int32_t *offsets, int64_t rows, const v
     const int nt2 = (int)((H + BN - 1) / BN);
     // plain stream order: this GEMM reads the offsets before any grid-level
     // wait, so they must be complete when it starts
-    return launch_gemm<DT, false, kOutCombine, CG>(tc_unit_upper_bound(rows, E, nt2, CG), s, mh,
+    return launch_gemm<DT, false, kOutCombine, CG, 1>(tc_unit_upper_bound(rows, E, nt2, CG), s, mh,
                                                    mhh, md, md, md, md, offsets, E, (int)H,
-                                                   (int)I, nt2, y_acc, status, comb, false);
+                                                   (int)I, nt2, y_acc, status, comb, 0, false);
 }
 
 // offsets[e] = e * rows_per_expert (e <= E), src_of[r] = r: the dispatch map

@@ -160,6 +160,18 @@ __device__ __forceinline__ void tma_load_3d_pair(void *dst, const CUtensorMap *m
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d_pair(void *dst, const CUtensorMap *map,
+                                                 uint32_t bar_cluster, int c0, int c1, int c2,
+                                                 int c3)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2),
+        "r"(c3)
+        : "memory");
+}
+
 // Tensor-memory allocation; with CG = 2 one warp of each CTA of the pair
 // performs it together, and both CTAs get the same columns.
 template <int CG>
@@ -404,6 +416,41 @@ bool encode_3d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_
     cuuint32_t box[3] = {box0, box1, 1};
     cuuint32_t es[3] = {1, 1, 1};
     return fn(m, dt, 3, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// A row-major [rows, K] 16-bit matrix seen as [K / 64][rows][64] (strides:
+// a row K * 2 bytes, a 64-element k-block 128 bytes): one box of box_rows
+// rows and kbs consecutive k-blocks lands as kbs 128-byte-swizzled
+// [box_rows][64] tiles one after another, each where a one-k-block box
+// would put it. Needs K % 64 == 0.
+bool encode_kblocks(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t K,
+                    uint64_t rows, uint32_t box_rows, uint32_t kbs)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr || K % 64 != 0) return false;
+    cuuint64_t dims[3] = {64, rows, K / 64};
+    cuuint64_t strides[2] = {K * 2, 128};
+    cuuint32_t box[3] = {64, box_rows, kbs};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, dt, 3, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The same for a row-major [E, rows, K] weight tensor, seen as
+// [E][K / 64][rows][64]; a box holds one expert.
+bool encode_kblocks_e(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t K,
+                      uint64_t rows, uint64_t E, uint32_t box_rows, uint32_t kbs)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr || K % 64 != 0) return false;
+    cuuint64_t dims[4] = {64, rows, K / 64, E};
+    cuuint64_t strides[3] = {K * 2, 128, rows * K * 2};
+    cuuint32_t box[4] = {64, box_rows, kbs, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return fn(m, dt, 4, const_cast<void *>(base), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

@@ -60,6 +60,12 @@ SMALL = [
               dtype="bf16", logits_dtype="bf16", logit_bias="zipf", bias_param=1.0),
     cfg_small("pair_f16", T=640, H=384, I=320, E=4, top_k=2, renormalize=True,
               dtype="f16", logits_dtype="f32"),
+    # at least 2048 rows per expert on average: pairs with two k-blocks per
+    # pipeline stage (H = 256: four k-blocks, I = 192: three, the last stage
+    # of each GEMM2 unit half past K); in the one-call forward the folded
+    # combine's per-expert handoff runs in this mode too
+    cfg_small("pair_two_kb_bf16", T=4400, H=256, I=192, E=2, top_k=1, renormalize=True,
+              dtype="bf16", logits_dtype="f32", logit_bias="normal", bias_param=0.5),
 ]
 PAIR = [c for c in SMALL if c.name.startswith("pair_")]
 
@@ -337,6 +343,48 @@ def test_experts_pair_unit_edges(dev, dt):
     assert_close(to_f64(gu_c[0]), rg, name, "cached g")
     assert_close(to_f64(gu_c[1]), ru, name, "cached u")
     assert_close(to_f64(h_c), rh, name, "cached h")
+
+
+# Experts averaging >= 2048 rows run their CTA pairs with two k-blocks per
+# pipeline stage. Counts: 8 full units + a unit with one row on its second
+# CTA (2177), 15 full units + an M = 128 tile of 60 rows (3900), exactly one
+# M = 128 tile (128). (H, I) = (192, 320): odd k-block counts, two-k-block
+# boxes with the second k-block past K in each unit's last stage;
+# (200, 136): K tails, so one box per k-block in two-k-block stages.
+TWO_KB_COUNTS = [2177, 3900, 128]
+
+
+@pytest.mark.parametrize("H,I", [(192, 320), (200, 136)], ids=["boxes", "k_tails"])
+def test_experts_two_kblock_stages(dev, H, I):
+    dt = torch.bfloat16
+    E = len(TWO_KB_COUNTS)
+    offsets = np.concatenate([[0], np.cumsum(TWO_KB_COUNTS)]).astype(np.int32)
+    rows = int(offsets[-1])
+    assert rows >= 2048 * E
+    g = torch.Generator().manual_seed(13)
+    x = torch.randn((rows, H), generator=g).to(dt)
+    gate = (torch.randn((E, I, H), generator=g) * H ** -0.5).to(dt)
+    up = (torch.randn((E, I, H), generator=g) * H ** -0.5).to(dt)
+    down = (torch.randn((E, H, I), generator=g) * I ** -0.5).to(dt)
+    off = torch.from_numpy(offsets).to(dev)
+    on = [t.to(dev) for t in (x, gate, up, down)]
+    out16 = moe.moe_experts_forward(*on[:1], off, *on[1:])
+    out_t, cache = moe.moe_experts_forward_training(*on[:1], off, *on[1:],
+                                                    out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert moe.moe_device_status() == 0
+    ref = oracle.experts_dispatched(np_of(x), "bf16", offsets, np_of(gate), np_of(up),
+                                    np_of(down))
+    assert_close(to_f64(out16), ref, "bf16", "expert outputs (dtype)")
+    assert_close(to_f64(out_t), ref, "bf16", "expert outputs (FP32, training)")
+    hb = rows * I * 2
+    h_c = cache[:hb].view(dt).view(rows, I)
+    gu_c = cache[hb: hb + 2 * rows * I * 4].view(torch.float32).view(2, rows, I)
+    rg, ru, rh = oracle.experts_cache_dispatched(np_of(x), "bf16", offsets, np_of(gate),
+                                                 np_of(up))
+    assert_close(to_f64(gu_c[0]), rg, "bf16", "cached g")
+    assert_close(to_f64(gu_c[1]), ru, "bf16", "cached u")
+    assert_close(to_f64(h_c), rh, "bf16", "cached h")
 
 
 # ---------------------------------------------------------------- combine
