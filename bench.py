@@ -442,7 +442,10 @@ def fold_combine(T, H, x):
 # for full profiler captures of the backward kernels
 TRAINING_WORKLOADS = {"train_fine_prefill_bf16": ("fine_prefill_bf16", {}),
                       "train_coarse_prefill_bf16": ("coarse_prefill_bf16", {}),
-                      "train_fine_prefill_half_bf16": ("fine_prefill_bf16", {"T": 2048, "E": 32})}
+                      "train_fine_prefill_half_bf16": ("fine_prefill_bf16", {"T": 2048, "E": 32}),
+                      # the coarse prefill's per-expert shapes, 4 experts of about
+                      # 2048 rows: small enough for multi-pass profiler captures
+                      "train_coarse_prefill_e4_bf16": ("coarse_prefill_bf16", {"T": 4096, "E": 4})}
 
 
 def run_training(args, rank, world, local, dist, dev, peaks, flush):
