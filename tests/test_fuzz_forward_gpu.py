@@ -145,3 +145,60 @@ def test_forward_random_shapes(dev, cfg):
         assert_close(got, ref["y"], cfg.dtype, f"{cfg.name} y")
     # else the rounding of h alone comes within reach of the bar: the first
     # check holds the GPU to that arithmetic
+
+
+# ---------------------------------------------------------------- routing plan
+
+def draw_plan_case(i: int) -> W.MoeConfig:
+    """Shapes for the routing plan alone: token counts up to 40000, up to
+    1024 experts and top_k up to 16, so every front end of the one-call
+    forward runs (fused routing + counts, one thread per token, the packed
+    16-bit kernel, the separate count and scan passes); tiny experts."""
+    r = np.random.default_rng(9000 + i)
+    E = int(r.choice([1, 3, 8, 16, 24, 33, 64, 100, 256, 1024]))
+    k = int(r.integers(1, min(E, 16) + 1))
+    T = int(r.choice([int(r.integers(1, 600)), int(r.integers(600, 12000)),
+                      int(r.integers(12000, 40000))]))
+    ldt = str(r.choice(["f32", "bf16", "f16"]))
+    bias = str(r.choice(["none", "normal", "zipf"]))
+    return W.MoeConfig(f"plan{i}_{ldt}_T{T}_E{E}_k{k}_{bias}", 300 + i, T=T, H=16, I=16, E=E,
+                       top_k=k, renormalize=bool(r.integers(0, 2)), dtype="bf16",
+                       logits_dtype=ldt, logit_bias=bias,
+                       bias_param=float(r.uniform(0.2, 2.0)))
+
+
+PLAN_CASES = [draw_plan_case(i) for i in range(40)]
+
+
+@pytest.mark.parametrize("cfg", PLAN_CASES, ids=lambda c: c.name)
+def test_forward_plan_random_shapes(dev, cfg):
+    """The routing plan and dispatch map the forward leaves in its workspace
+    equal the oracle's, bit for bit (ruDNN user guide, sections 4 and 5)."""
+    cpu = W.moe_inputs(cfg, device="cpu")
+    g = {n: v.to(dev) for n, v in cpu.items()}
+    T, k, E = cfg.T, cfg.top_k, cfg.E
+    lay = moe.moe_forward_workspace_layout(T, cfg.H, cfg.I, E, k, g["x"].dtype,
+                                           g["logits"].dtype)
+    ws = torch.empty(lay["total"], dtype=torch.uint8, device=dev)
+    moe.moe_forward_ex(g["x"], g["logits"], g["gate"], g["up"], g["down"], k, cfg.renormalize,
+                       workspace=ws)
+    torch.cuda.synchronize()
+    assert moe.moe_device_status(clear=True) == 0
+
+    def tview(name, n, dt):
+        off = lay[name]
+        return ws[off:off + n * torch.tensor([], dtype=dt).element_size()].view(dt).cpu()
+
+    def view(name, n, dt):
+        return tview(name, n, dt).numpy()
+    A = T * k
+    idx_ref, w_ref, _ = oracle.route(np_of(cpu["logits"]), cfg.logits_dtype, k, cfg.renormalize)
+    counts, offsets, row_of, src_of, _ = oracle.dispatch(idx_ref, E)
+    assert np.array_equal(view("expert_indices", A, torch.int32).view(np.uint32),
+                          idx_ref.reshape(-1)), "ids"
+    assert np.array_equal(view("counts", E, torch.int32), counts), "counts"
+    assert np.array_equal(view("offsets", E + 1, torch.int32), offsets), "offsets"
+    assert np.array_equal(view("row_of", A, torch.int32), row_of), "row_of"
+    assert np.array_equal(view("src_of", A, torch.int32), src_of), "src_of"
+    w = tview("weights", A, g["logits"].dtype).reshape(T, k)
+    assert_close(to_f64(w), oracle.to_f64(w_ref, cfg.logits_dtype), cfg.logits_dtype, "weights")
