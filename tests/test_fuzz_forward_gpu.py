@@ -9,7 +9,9 @@ few experts, which selects CTA pairs and, past 2048 rows per expert on
 average, two k-blocks per pipeline stage. Each case's oracle work is bounded
 so the whole file runs in seconds.
 
-Two checks per BF16 / F16 case:
+Every call writes into y and a workspace with 4 KiB bands of a fill byte on
+both sides, which must come back untouched. Two checks per BF16 / F16
+case:
 * against the arithmetic this library documents for the path -- FP32 (here
   FP64) products, h = SiLU(g) * u rounded once to the activation dtype
   between the two GEMMs, y rounded once at the end -- written out below in
@@ -115,6 +117,40 @@ def excess_over_half_ulp(got, ref, dt):
     return np.abs(got[m] - ref[m]) - half_ulp_of(ref[m], dt)
 
 
+GUARD = 4096          # bytes of fill on each side of y and of the workspace
+GUARD_BYTE = 0x5A
+
+
+def guarded(nbytes: int, dev):
+    """(whole, interior): nbytes between two GUARD-byte bands of GUARD_BYTE;
+    the interior keeps the 256-byte alignment of the allocation."""
+    whole = torch.full((nbytes + 2 * GUARD,), GUARD_BYTE, dtype=torch.uint8, device=dev)
+    return whole, whole[GUARD:GUARD + nbytes]
+
+
+def bands_intact(whole: torch.Tensor) -> bool:
+    return bool(torch.all(whole[:GUARD] == GUARD_BYTE)) and \
+        bool(torch.all(whole[-GUARD:] == GUARD_BYTE))
+
+
+def forward_guarded(g, cfg, deterministic, dev):
+    """moe_forward_ex into guarded y and workspace buffers; returns y, and
+    asserts nothing was written outside them."""
+    dt = g["x"].dtype
+    lay = moe.moe_forward_workspace_layout(cfg.T, cfg.H, cfg.I, cfg.E, cfg.top_k, dt,
+                                           g["logits"].dtype, deterministic)
+    ws_whole, ws = guarded(lay["total"], dev)
+    y_whole, yb = guarded(cfg.T * cfg.H * g["x"].element_size(), dev)
+    y = yb.view(dt).view(cfg.T, cfg.H)
+    moe.moe_forward_ex(g["x"], g["logits"], g["gate"], g["up"], g["down"], cfg.top_k,
+                       cfg.renormalize, deterministic=deterministic, y=y, workspace=ws)
+    torch.cuda.synchronize()
+    assert moe.moe_device_status(clear=True) == 0
+    assert bands_intact(ws_whole), f"{cfg.name}: written outside the workspace"
+    assert bands_intact(y_whole), f"{cfg.name}: written outside y"
+    return y, ws, lay
+
+
 @pytest.mark.parametrize("cfg", CASES, ids=lambda c: c.name)
 def test_forward_random_shapes(dev, cfg):
     cpu = W.moe_inputs(cfg, device="cpu")
@@ -122,11 +158,7 @@ def test_forward_random_shapes(dev, cfg):
     o = {n: np_of(v) for n, v in cpu.items()}
     ref = oracle.forward(o["x"], cfg.dtype, o["logits"], cfg.logits_dtype, o["gate"], o["up"],
                          o["down"], cfg.top_k, cfg.renormalize)
-    deterministic = cfg.number % 2 == 1
-    y = moe.moe_forward_ex(g["x"], g["logits"], g["gate"], g["up"], g["down"], cfg.top_k,
-                           cfg.renormalize, deterministic=deterministic)
-    torch.cuda.synchronize()
-    assert moe.moe_device_status(clear=True) == 0
+    y, _, _ = forward_guarded(g, cfg, cfg.number % 2 == 1, dev)
     got = to_f64(y)
     if cfg.dtype == "f32":
         assert_close(got, ref["y"], "f32", f"{cfg.name} y")
@@ -177,13 +209,7 @@ def test_forward_plan_random_shapes(dev, cfg):
     cpu = W.moe_inputs(cfg, device="cpu")
     g = {n: v.to(dev) for n, v in cpu.items()}
     T, k, E = cfg.T, cfg.top_k, cfg.E
-    lay = moe.moe_forward_workspace_layout(T, cfg.H, cfg.I, E, k, g["x"].dtype,
-                                           g["logits"].dtype)
-    ws = torch.empty(lay["total"], dtype=torch.uint8, device=dev)
-    moe.moe_forward_ex(g["x"], g["logits"], g["gate"], g["up"], g["down"], k, cfg.renormalize,
-                       workspace=ws)
-    torch.cuda.synchronize()
-    assert moe.moe_device_status(clear=True) == 0
+    _, ws, lay = forward_guarded(g, cfg, False, dev)
 
     def tview(name, n, dt):
         off = lay[name]
