@@ -828,6 +828,26 @@ def run_routing_sweep(args, world, dist, dev, peaks, flush):
                          "route_frac_hbm": r_bytes / (r_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
                          "dispatch_us": d_ms * 1e3,
                          "dispatch_frac_hbm": d_bytes / (d_ms / 1e3) / 1e9 / peaks["hbm_gbs"]})
+        # the same dispatch at T = 2^20 moving the fine prefill's 4 KiB rows
+        # (H = 2048): the regime of a real gather, where the rows dominate
+        # the bytes (idx and logits as above; x drawn on the device)
+        T, Hw = 1 << 20, base.H
+        A = T * k
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(base.seed)
+        xw = torch.randn((T, Hw), generator=gen, device=dev).to(torch.bfloat16)
+        wide = {"counts": torch.empty(E, dtype=torch.int32, device=dev),
+                "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
+                "row_of": torch.empty(A, dtype=torch.int32, device=dev),
+                "src_of": torch.empty(A, dtype=torch.int32, device=dev),
+                "x_disp": torch.empty((A, Hw), dtype=torch.bfloat16, device=dev),
+                "workspace": torch.empty(moe.moe_dispatch_workspace_size(T, k, E),
+                                         dtype=torch.uint8, device=dev)}
+        dw_ms = timed_loop(lambda: moe.moe_dispatch(idx, xw, E, **wide), args, stream, flush)
+        dw_bytes = A * 12 + E * 8 + T * Hw * 2 + A * Hw * 2
+        wide_row = {"T": T, "H": Hw, "dispatch_us": dw_ms * 1e3, "bytes": dw_bytes,
+                    "dispatch_frac_hbm": dw_bytes / (dw_ms / 1e3) / 1e9 / peaks["hbm_gbs"]}
+        del xw, wide
     if moe.moe_device_status() != 0:
         raise RuntimeError("device status error in the routing sweep")
     big = rows[-1]
@@ -840,13 +860,14 @@ def run_routing_sweep(args, world, dist, dev, peaks, flush):
             "config": {"workload": "routing_sweep", "E": E, "top_k": k, "logits_dtype": "bf16",
                        "l2": "flushed between steps (256 MiB write)"},
             "sweep": rows,
+            "dispatch_wide_rows": wide_row,
             "roofline": {"bound": "hbm", "kernel": "route (T = 2^20)",
                          "achieved": big["route_frac_hbm"] * peaks["hbm_gbs"],
                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": big["route_frac_hbm"],
                          "frac_nominal": big["route_frac_hbm"] * peaks["hbm_gbs"] / NOMINAL_HBM_GBS,
                          "peak_source": peaks["source"], "traffic": None},
-            "gpu_launches": 5 * len(rows) * (args.steps + max(1, args.warmup)),
+            "gpu_launches": (5 * len(rows) + 4) * (args.steps + max(1, args.warmup)),
             "clocks": clk.summary()}
 
 

@@ -42,6 +42,12 @@ constexpr int kMaxChunkWarps = (int)(kMaxChunk / kRun);
 constexpr int kCountThreads = 512;
 constexpr int kCountIds = 16;           // ids per count thread per step (four 16-byte reads)
 constexpr int kScanThreads = 256;
+#ifndef MOE_TOKEN_GATHER_MIN_BYTES
+#define MOE_TOKEN_GATHER_MIN_BYTES (32ll << 20)
+#endif
+// Rows of at least 512 bytes are gathered in token order once x passes this
+// size (a fair share of L2); below it the row-order gather's reads of x hit L2.
+constexpr int64_t kTokenGatherMinBytes = MOE_TOKEN_GATHER_MIN_BYTES;
 
 // About four chunks per SM, a power of two of at least 256 assignments (so
 // every chunk starts on a 16-byte boundary of the ids).
@@ -350,6 +356,54 @@ dispatch_gather_narrow_kernel(const uint4 *__restrict__ x, int64_t rows, int top
     pdl_launch_dependents();
 }
 
+// Token order: x_disp[row_of[t * top_k + j]] = x[t] for every slot j. A warp
+// per token reads its row once, in chunks of 32 lanes x V 16-byte vectors,
+// and writes each chunk to the token's dispatched rows; x is then read from
+// DRAM once even where it outgrows L2 (the row-order gather reads a token's
+// row once per slot). Slots without a row (row_of < 0) are skipped.
+template <int V>
+__global__ void __launch_bounds__(256)
+dispatch_gather_tokens_kernel(const uint4 *__restrict__ x, int64_t T, int64_t per_row,
+                              int top_k, int64_t rows, const int32_t *__restrict__ row_of,
+                              uint4 *__restrict__ x_disp, unsigned *status)
+{
+    (void)status;
+    (void)rows;
+    pdl_wait();
+    const int lane = (int)lane_id();
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
+    for (int64_t t = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; t < T;
+         t += warps) {
+        const uint4 *src = x + t * per_row;
+        const int32_t *slots = row_of + t * top_k;
+        // the rows of the first 32 slots, one per lane (most top_k fit)
+        const int32_t first = lane < top_k ? slots[lane] : -1;
+        for (int64_t c0 = 0; c0 < per_row; c0 += 32 * V) {
+            uint4 buf[V];
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                const int64_t c = c0 + lane + 32 * v;
+                if (c < per_row) buf[v] = __ldg(src + c);
+            }
+            for (int j0 = 0; j0 < top_k; j0 += 32) {
+                const int jn = top_k - j0 < 32 ? top_k - j0 : 32;
+                const int32_t mine = j0 == 0 ? first : (lane < jn ? slots[j0 + lane] : -1);
+                for (int j = 0; j < jn; ++j) {
+                    const int32_t r = __shfl_sync(kFull, mine, j);
+                    if (r < 0 || !MOE_BOUNDS_OK((int64_t)r < rows, status)) continue;
+                    uint4 *dst = x_disp + (int64_t)r * per_row;
+#pragma unroll
+                    for (int v = 0; v < V; ++v) {
+                        const int64_t c = c0 + lane + 32 * v;
+                        if (c < per_row) dst[c] = buf[v];
+                    }
+                }
+            }
+        }
+    }
+    pdl_launch_dependents();
+}
+
 template <int PER>
 cudaError_t launch_gather_narrow(const uint4 *x, int64_t rows, int top_k, const int32_t *src_of,
                                  uint4 *x_disp, unsigned *status, cudaStream_t s)
@@ -494,6 +548,12 @@ cudaError_t launch_dispatch_rank_gather(const uint32_t *idx, int64_t T, int top_
         case 7: err = launch_gather_narrow<7>(xv, A, top_k, so, xdv, status, s); break;
         default: err = launch_gather_narrow<8>(xv, A, top_k, so, xdv, status, s); break;
         }
+    } else if (vec && row_bytes / 16 >= 32 && T * row_bytes > kTokenGatherMinBytes) {
+        int64_t gblocks = (T + 7) / 8;
+        if (gblocks > cap) gblocks = cap;
+        err = launch_pdl(dispatch_gather_tokens_kernel<8>, dim3((unsigned)gblocks), dim3(256), 0,
+                         s, reinterpret_cast<const uint4 *>(xb), T, row_bytes / 16, top_k, A,
+                         (const int32_t *)row_of, reinterpret_cast<uint4 *>(xd), status);
     } else if (vec && row_bytes / 16 >= 32) {
         int64_t gblocks = (A + 7) / 8;
         if (gblocks > cap) gblocks = cap;

@@ -200,7 +200,11 @@ def _check_dispatch(d, idx_np, x_np, E, k, dt):
 DISPATCH_CASES = [(4096, 6, 64, 2048, "bf16"), (8192, 8, 256, 64, "bf16"),
                   (16384, 2, 8, 64, "f32"), (128, 8, 256, 7168, "bf16"),
                   (37, 3, 5, 24, "f16"), (1, 1, 1, 8, "f32"), (500, 4, 1024, 8, "bf16"),
-                  (3000, 1, 4, 40, "bf16")]
+                  (3000, 1, 4, 40, "bf16"),
+                  # x past 32 MiB with rows of >= 512 bytes: the token-order gather
+                  # (k = 40 reads the slots' rows in two groups of 32 lanes)
+                  (9000, 3, 16, 2048, "bf16"), (5000, 40, 64, 1792, "f32"),
+                  (8200, 2, 8, 4096, "f16")]
 
 
 @pytest.mark.parametrize("T,k,E,H,dt", DISPATCH_CASES)
