@@ -353,9 +353,10 @@ route_thread_kernel(const void *__restrict__ logits, int64_t T, int E, int top_k
 //   * each logit becomes a 32-bit selection key: its order-preserving 16-bit
 //     code in the high half (-0 and +0 share one code, so they tie) and
 //     63 - id in the low half, so one integer max compares the logits and
-//     breaks ties toward the lower id; the keys of a group of 8 experts are
-//     stored with two 16-byte writes, and the round's rescan reads them back
-//     with two 16-byte reads;
+//     breaks ties toward the lower id; shared memory keeps only the codes
+//     (the id is the position), a group of 8 experts in one 16-byte word,
+//     and a round's rescan rebuilds that group's keys from one 16-byte read
+//     (half the bytes of stored keys, so more threads fit an SM);
 //   * the softmax sum takes one FFMA and one ex2 per logit.
 // The selected probabilities are recomputed from their keys' codes (the same
 // FP32 operations as in the sum).
@@ -412,7 +413,7 @@ __device__ __forceinline__ uint32_t max2_nan(uint32_t a, uint32_t b)
     }
 }
 
-constexpr int kKeyPad = 4;                 // words after each thread's key row (bank spread)
+constexpr int kKeyPad = 4;                 // words after each thread's code row (bank spread)
 
 template <int EPL, int LDT>
 __global__ void __launch_bounds__(kThreadRouteThreads)
@@ -423,7 +424,7 @@ route_thread16_kernel(const void *__restrict__ logits, int64_t T, int E, int top
     static_assert(EPL % 8 == 0 && EPL <= 64, "rows of whole 16-byte vectors, ids below 64");
     constexpr int NW = EPL / 2;                       // packed words per row
     constexpr int NG = EPL / 8;                       // groups of 8 experts
-    constexpr int ROW = EPL + kKeyPad;                // key words per thread
+    constexpr int ROW = EPL / 2 + kKeyPad;            // code words per thread
     constexpr uint32_t kNegInf2 = LDT == DT_BF16 ? 0xff80ff80u : 0xfc00fc00u;
     using ET = typename Elem<LDT>::T;
     const uint4 *L = static_cast<const uint4 *>(logits);
@@ -491,8 +492,9 @@ route_thread16_kernel(const void *__restrict__ logits, int64_t T, int E, int top
                 k8[2 * q] = (code << 16) | (uint32_t)(63 - id);
                 k8[2 * q + 1] = (code & 0xffff0000u) | (uint32_t)(62 - id);
             }
-            reinterpret_cast<uint4 *>(kr + 8 * g)[0] = make_uint4(k8[0], k8[1], k8[2], k8[3]);
-            reinterpret_cast<uint4 *>(kr + 8 * g)[1] = make_uint4(k8[4], k8[5], k8[6], k8[7]);
+            reinterpret_cast<uint4 *>(kr + 4 * g)[0] =
+                make_uint4(order_codes2(w[4 * g]), order_codes2(w[4 * g + 1]),
+                           order_codes2(w[4 * g + 2]), order_codes2(w[4 * g + 3]));
             uint32_t b = k8[0];
 #pragma unroll
             for (int q = 1; q < 8; ++q) b = max(b, k8[q]);
@@ -517,13 +519,19 @@ route_thread16_kernel(const void *__restrict__ logits, int64_t T, int E, int top
                                                : __half2float(__ushort_as_half((unsigned short)bits));
                 p[j] = ex2_approx(arg(l)) * inv_s;
                 z += p[j];
-                // take it, rescan its group
-                kr[e] = 0u;
+                // take it (code 0: its rebuilt key, 63 - id, is below every
+                // untaken key), then rescan its group's codes
                 const int g0 = e & ~7;
-                const uint4 a = reinterpret_cast<const uint4 *>(kr + g0)[0];
-                const uint4 b = reinterpret_cast<const uint4 *>(kr + g0)[1];
-                const uint32_t nk = max(max(max(a.x, a.y), max(a.z, a.w)),
-                                        max(max(b.x, b.y), max(b.z, b.w)));
+                reinterpret_cast<unsigned short *>(kr)[e] = 0;
+                const uint4 a = reinterpret_cast<const uint4 *>(kr + g0 / 2)[0];
+                const uint32_t cw[4] = {a.x, a.y, a.z, a.w};
+                uint32_t nk = 0u;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int id0 = g0 + 2 * q;
+                    nk = max(nk, (cw[q] << 16) | (uint32_t)(63 - id0));
+                    nk = max(nk, (cw[q] & 0xffff0000u) | (uint32_t)(62 - id0));
+                }
 #pragma unroll
                 for (int g = 0; g < NG; ++g)
                     if (gk[g] == best) gk[g] = nk;
@@ -549,7 +557,7 @@ cudaError_t launch_route_thread16(const void *logits, int64_t T, int E, int top_
                                   uint32_t *idx, void *w, cudaStream_t s)
 {
     constexpr int kThreads = kThreadRouteThreads;
-    const size_t smem = (size_t)kThreads * (EPL + kKeyPad) * sizeof(uint32_t);
+    const size_t smem = (size_t)kThreads * (EPL / 2 + kKeyPad) * sizeof(uint32_t);
     static std::atomic<uint64_t> opted{0};       // the > 48 KiB opt-in, per device
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
