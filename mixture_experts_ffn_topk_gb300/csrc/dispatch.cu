@@ -162,21 +162,30 @@ dispatch_scan_kernel(int *__restrict__ chunk_counts, int64_t nchunks, int E,
 // nbits bits of the ballot of that bit (or of its complement). Ballots run
 // on the integer pipes; __match_any_sync, which computes the same mask, runs
 // on the address-divergence unit and was what held this pass back.
-__device__ __forceinline__ unsigned peers_of(uint32_t key, int nbits)
+template <int NBITS>
+__device__ __forceinline__ unsigned peers_of(uint32_t key)
 {
     unsigned peers = kFull;
 #pragma unroll
-    for (int b = 0; b < 11; ++b) {
-        if (b < nbits) {
-            const bool bit = (key >> b) & 1u;
-            const unsigned on = __ballot_sync(kFull, bit);
-            peers &= bit ? on : ~on;
-        }
+    for (int b = 0; b < NBITS; ++b) {
+        const bool bit = (key >> b) & 1u;
+        const unsigned on = __ballot_sync(kFull, bit);
+        peers &= bit ? on : ~on;
     }
     return peers;
 }
 
+// Bits of the rank keys: expert ids 0..E-1 and the key 2^NBITS - 1 of ids
+// that get no row, above every expert.
+int rank_key_bits(int E)
+{
+    int nbits = 1;
+    while ((1 << nbits) <= E) ++nbits;
+    return nbits;
+}
+
 // CTA c ranks chunk c: warp w owns assignments [a0 + w * kRun, ...) of it.
+template <int NBITS>
 __global__ void __launch_bounds__(kMaxChunkWarps * 32)
 dispatch_rank_kernel(const uint32_t *__restrict__ idx, int64_t A, int E, int64_t chunk,
                      int64_t nchunks,
@@ -261,10 +270,8 @@ dispatch_rank_kernel(const uint32_t *__restrict__ idx, int64_t A, int E, int64_t
     // walk the run in order, 32 assignments at a time: equal experts of a
     // batch take consecutive rows in lane order, so rows inside an expert
     // follow the assignment order (deterministic); ids that get no row share
-    // the key 2^nbits - 1, above every expert
-    int nbits = 1;
-    while ((1 << nbits) <= E) ++nbits;
-    const uint32_t none = (1u << nbits) - 1u;
+    // the key 2^NBITS - 1, above every expert
+    const uint32_t none = (1u << NBITS) - 1u;
     const unsigned lt = (1u << lane) - 1u;
 #pragma unroll
     for (int b = 0; b < kRunBatches; ++b) {
@@ -273,7 +280,7 @@ dispatch_rank_kernel(const uint32_t *__restrict__ idx, int64_t A, int E, int64_t
         const bool act = a < r1;
         const uint32_t e = ev[b];
         const bool ok = act && e < (uint32_t)E;
-        const unsigned peers = peers_of(ok ? e : none, nbits);
+        const unsigned peers = peers_of<NBITS>(ok ? e : none);
         int row = -1;
         if (ok) {
             row = mine[e] + __popc(peers & lt);
@@ -493,6 +500,37 @@ cudaError_t launch_dispatch(const uint32_t *idx, int64_t T, int top_k, int E, in
                                        src_of, x_disp, ws, status, s);
 }
 
+namespace {
+
+template <int NB>
+cudaError_t launch_rank(const uint32_t *idx, int64_t A, int E, int64_t chunk_len,
+                        int64_t nchunks, const int *chunk, const int32_t *counts,
+                        int32_t *offsets, int32_t *row_of, int32_t *src_of, int nw,
+                        size_t rank_bytes, unsigned *status, cudaStream_t s)
+{
+    if (rank_bytes > 48 * 1024) {
+        // up to 16 warps x 1024 experts of counts: past the default 48 KiB
+        static std::atomic<uint64_t> opted{0};
+        int dev = 0;
+        cudaError_t err = cudaGetDevice(&dev);
+        if (err != cudaSuccess) return err;
+        const uint64_t bit = dev >= 0 && dev < kCachedDevices ? 1ull << dev : 0ull;
+        if (bit == 0 || !(opted.load() & bit)) {
+            err = cudaFuncSetAttribute(dispatch_rank_kernel<NB>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)(((size_t)1025 + (size_t)kMaxChunkWarps * 1024) *
+                                             sizeof(int)));
+            if (err != cudaSuccess) return err;
+            opted.fetch_or(bit);
+        }
+    }
+    return launch_pdl(dispatch_rank_kernel<NB>, dim3((unsigned)nchunks), dim3(nw * 32),
+                      rank_bytes, s, idx, A, E, chunk_len, nchunks, chunk, counts, offsets,
+                      row_of, src_of, status);
+}
+
+}  // namespace
+
 cudaError_t launch_dispatch_rank_gather(const uint32_t *idx, int64_t T, int top_k, int E,
                                         const void *x, int xdt, int64_t H, const int32_t *counts,
                                         int32_t *offsets, int32_t *row_of, int32_t *src_of,
@@ -507,25 +545,16 @@ cudaError_t launch_dispatch_rank_gather(const uint32_t *idx, int64_t T, int top_
     cudaError_t err = cudaSuccess;
     // offsets and the per-warp rows of every expert
     const size_t rank_bytes = ((size_t)E + 1 + (size_t)nw * E) * sizeof(int);
-    if (rank_bytes > 48 * 1024) {
-        // up to 16 warps x 1024 experts of counts: past the default 48 KiB
-        static std::atomic<uint64_t> opted{0};
-        int dev = 0;
-        err = cudaGetDevice(&dev);
-        if (err != cudaSuccess) return err;
-        const uint64_t bit = dev >= 0 && dev < kCachedDevices ? 1ull << dev : 0ull;
-        if (bit == 0 || !(opted.load() & bit)) {
-            err = cudaFuncSetAttribute(dispatch_rank_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)(((size_t)1025 + (size_t)kMaxChunkWarps * 1024) *
-                                             sizeof(int)));
-            if (err != cudaSuccess) return err;
-            opted.fetch_or(bit);
-        }
+    switch (rank_key_bits(E)) {
+#define MOE_RANK(NB)                                                                          \
+    case NB: err = launch_rank<NB>(idx, A, E, chunk_len, nchunks, chunk, counts, offsets,     \
+                                   row_of, src_of, nw, rank_bytes, status, s); break;
+    MOE_RANK(1) MOE_RANK(2) MOE_RANK(3) MOE_RANK(4) MOE_RANK(5) MOE_RANK(6)
+    MOE_RANK(7) MOE_RANK(8) MOE_RANK(9) MOE_RANK(10)
+#undef MOE_RANK
+    default: err = launch_rank<11>(idx, A, E, chunk_len, nchunks, chunk, counts, offsets, row_of,
+                                   src_of, nw, rank_bytes, status, s); break;
     }
-    err = launch_pdl(dispatch_rank_kernel, dim3((unsigned)nchunks), dim3(nw * 32), rank_bytes, s, idx,
-                     A, E, chunk_len, nchunks, (const int *)chunk, (const int32_t *)counts,
-                     offsets, row_of, src_of, status);
     if (err != cudaSuccess) return err;
     const int64_t row_bytes = H * (xdt == DT_F32 ? 4 : 2);
     const bool vec = row_bytes % 16 == 0 && reinterpret_cast<uintptr_t>(x) % 16 == 0 &&
