@@ -204,7 +204,11 @@ DISPATCH_CASES = [(4096, 6, 64, 2048, "bf16"), (8192, 8, 256, 64, "bf16"),
                   # x past 32 MiB with rows of >= 512 bytes: the token-order gather
                   # (k = 40 reads the slots' rows in two groups of 32 lanes)
                   (9000, 3, 16, 2048, "bf16"), (5000, 40, 64, 1792, "f32"),
-                  (8200, 2, 8, 4096, "f16")]
+                  (8200, 2, 8, 4096, "f16"),
+                  # rank counters in registers (E <= 64: experts lane and lane + 32)
+                  # around their edges, and E = 100 (seven key bits, shared memory)
+                  (20000, 6, 33, 8, "bf16"), (30000, 8, 64, 16, "f16"),
+                  (5000, 5, 32, 8, "f32"), (20000, 4, 100, 8, "bf16")]
 
 
 @pytest.mark.parametrize("T,k,E,H,dt", DISPATCH_CASES)
@@ -220,6 +224,22 @@ def test_dispatch_parity(dev, T, k, E, H, dt):
     torch.cuda.synchronize()
     _check_dispatch(d, idx.numpy().view(np.uint32), np_of(x), E, k, dt)
     assert moe.moe_device_status() == 0
+
+
+@pytest.mark.parametrize("E", [33, 64, 100])
+def test_dispatch_bad_indices_many_experts(dev, E):
+    """Ids >= E among many experts get no row and are flagged; the rows of the
+    others stay bit-exact (rank counters in registers up to 64 experts)."""
+    T, k, H = 20000, 4, 8
+    g = torch.Generator().manual_seed(E)
+    idx = torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(T)]).int()
+    bad = torch.randint(0, T, (50,), generator=g)
+    idx[bad, 1] = E + torch.randint(0, 1000, (50,), generator=g).int()
+    x = torch.randn((T, H), generator=g).to(torch.bfloat16)
+    assert moe.moe_device_status(clear=True) == 0
+    d = moe.moe_dispatch(idx.to(dev), x.to(dev), E)
+    assert moe.moe_device_status(clear=True) == 9        # MOE_ERR_BAD_INDEX
+    _check_dispatch(d, idx.numpy().view(np.uint32), np_of(x), E, k, "bf16")
 
 
 def test_dispatch_bad_index_flags_and_nans(dev):
