@@ -111,6 +111,12 @@ ROUTE_CASES = [
     (30000, 8, 1, True, "bf16", "ties"),
     (20000, 64, 6, False, "bf16", "extremes"),
     (20000, 32, 5, True, "f16", "extremes"),
+    # E = 64: TMA-fed tiles of 128 rows, several tiles per CTA through the
+    # slot ring at the larger T, one ragged tile at the smallest
+    (9729, 64, 1, False, "f16", "specials"),
+    (40000, 64, 7, True, "f16", "extremes"),
+    (400000, 64, 8, True, "f16", "ties"),
+    (700001, 64, 6, False, "bf16", "normal"),
 ]
 
 
