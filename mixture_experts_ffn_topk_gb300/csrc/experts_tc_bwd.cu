@@ -18,6 +18,11 @@
 //   warp 0     TMA producer, stages of 48 KiB (A 128 x 64, B 256 x 64);
 //   warp 1     tcgen05.mma issuer, M=128 N=256 K=16, two TMEM accumulators;
 //   warps 2-5  epilogue (tcgen05.ld, math, swizzled staging, line stores).
+// Where experts average thousands of rows the same kernel runs on CTA pairs
+// (tcgen05 cta_group::2): M = 256 over the two CTAs' 128 rows each, each CTA
+// loading its A rows and half of B into 32 KiB stages, so a CTA holds six
+// stages (dh five) instead of four (three) and more of the copies' latency
+// is covered; the leader issues the MMAs and owns the stage barriers.
 // DH's epilogue reads 256 KiB of cached FP32 g / u per tile, one row per lane;
 // with four warps those loads, not the MMA, set its pace, so DH runs eight
 // epilogue warps (two per TMEM lane quadrant, 128 columns each, 16 columns
@@ -58,7 +63,9 @@ constexpr int BOX = 64;                  // MN-major box: 64 elements x 64 k-row
 constexpr int BOX_BYTES = BOX * BK * 2;  // 8 KiB
 constexpr int A_BYTES = BM * BK * 2;     // 16 KiB
 constexpr int B_BYTES = BN * BK * 2;     // 32 KiB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+// a stage: this CTA's A tile and its share of B (all of it, or half on a pair)
+template <int CG>
+__host__ __device__ constexpr int stage_bytes() { return A_BYTES + B_BYTES / CG; }
 constexpr int ACC_COLS = 256;
 constexpr int TMEM_COLS = 2 * ACC_COLS;
 constexpr int MAX_E = 1024;
@@ -68,17 +75,20 @@ constexpr uint64_t kDrainLimitNs = 100000000ull;
 
 enum Mode : int { kDH = 0, kDX = 1, kWG = 2 };
 
-template <int MODE>
-__host__ __device__ constexpr int stages_of() { return MODE == kDH ? 3 : 4; }
+template <int MODE, int CG>
+__host__ __device__ constexpr int stages_of()
+{
+    return CG == 2 ? (MODE == kDH ? 5 : 6) : (MODE == kDH ? 3 : 4);
+}
 template <int MODE>
 __host__ __device__ constexpr int epi_warps_of() { return MODE == kDH ? 8 : 4; }
 template <int MODE>
 __host__ __device__ constexpr int threads_of() { return 32 * (2 + epi_warps_of<MODE>()); }
 
-template <int MODE>
+template <int MODE, int CG>
 struct __align__(1024) BwdSmem {
-    static constexpr int STAGES = stages_of<MODE>();
-    uint8_t stage[STAGES][STAGE_BYTES];
+    static constexpr int STAGES = stages_of<MODE, CG>();
+    uint8_t stage[STAGES][stage_bytes<CG>()];
     uint8_t epi[epi_warps_of<MODE>()][32 * EPI_ROW_BYTES];
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
@@ -90,8 +100,8 @@ struct __align__(1024) BwdSmem {
     int prefix[MAX_E + 1];
     int offs[MAX_E + 1];
 };
-template <int MODE>
-constexpr size_t kBwdSmemBytes = sizeof(BwdSmem<MODE>) + 1024;
+template <int MODE, int CG>
+constexpr size_t kBwdSmemBytes = sizeof(BwdSmem<MODE, CG>) + 1024;
 
 struct BwdParams {
     const int32_t *offsets;
@@ -111,15 +121,16 @@ struct BwdParams {
     uint64_t wait_ns;                   // limit of every bounded wait
 };
 
-// Tile id -> (expert, m, n, problem). DH / DX: m-tiles of an expert's rows,
+// Unit id -> (expert, m, n, problem). An m-unit is BM * CG rows (a pair
+// computes M = 256, 128 rows per CTA). DH / DX: m-units of an expert's rows,
 // m fastest (weight tiles shared through L2). WG: expert slowest, then
-// weight-row tile m, then column tile n.
-template <int MODE>
-__device__ __forceinline__ void decode(const BwdSmem<MODE> &S, const BwdParams &p, int tile, int &e,
-                                       int &m, int &n, int &prob)
+// weight-row unit m, then column tile n.
+template <int MODE, int CG>
+__device__ __forceinline__ void decode(const BwdSmem<MODE, CG> &S, const BwdParams &p, int tile,
+                                       int &e, int &m, int &n, int &prob)
 {
     if constexpr (MODE == kWG) {
-        const int mt = (p.M + BM - 1) / BM, per = mt * p.n_tiles;
+        const int mt = (p.M + BM * CG - 1) / (BM * CG), per = mt * p.n_tiles;
         prob = tile / (p.E * per);
         const int rem = tile - prob * p.E * per;
         e = rem / per;
@@ -133,7 +144,7 @@ __device__ __forceinline__ void decode(const BwdSmem<MODE> &S, const BwdParams &
             if (S.prefix[mid] <= tile) lo = mid; else hi = mid - 1;
         }
         e = lo;
-        const int mu = (S.offs[e + 1] - S.offs[e] + BM - 1) / BM;
+        const int mu = (S.offs[e + 1] - S.offs[e] + BM * CG - 1) / (BM * CG);
         const int local = tile - S.prefix[e];
         n = local / mu;
         m = local - n * mu;
@@ -141,8 +152,8 @@ __device__ __forceinline__ void decode(const BwdSmem<MODE> &S, const BwdParams &
     }
 }
 
-template <int MODE>
-__device__ __forceinline__ int k_blocks(const BwdSmem<MODE> &S, const BwdParams &p, int e)
+template <int MODE, int CG>
+__device__ __forceinline__ int k_blocks(const BwdSmem<MODE, CG> &S, const BwdParams &p, int e)
 {
     if constexpr (MODE == kDH) return (p.num_k + BK - 1) / BK;
     else if constexpr (MODE == kDX) return 2 * ((p.num_k + BK - 1) / BK);
@@ -218,45 +229,53 @@ expert_maps_kernel(const __grid_constant__ CUtensorMap base0, const __grid_const
     pdl_launch_dependents();
 }
 
-template <int DT, int MODE>
+template <int DT, int MODE, int CG>
 __global__ void __launch_bounds__(threads_of<MODE>(), 1)
 bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                 const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                 const BwdParams p)
 {
-    constexpr int STAGES = stages_of<MODE>();
+    constexpr int STAGES = stages_of<MODE, CG>();
+    constexpr int STAGE_BYTES = stage_bytes<CG>();
+    constexpr int B_BOXES = BN / BOX / CG;          // MN-major B boxes this CTA loads per stage
     constexpr int EPI_WARPS = epi_warps_of<MODE>();
     constexpr int THREADS = threads_of<MODE>();
+    constexpr int MU = BM * CG;                     // rows of an m-unit
     extern __shared__ uint8_t smem_raw[];
-    BwdSmem<MODE> &S = *reinterpret_cast<BwdSmem<MODE> *>(
+    BwdSmem<MODE, CG> &S = *reinterpret_cast<BwdSmem<MODE, CG> *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     unsigned *status = p.status;
+    // CTA pair: rank 0 issues the MMAs (M = 256 over both CTAs' A rows and
+    // B halves) and owns the stage barriers both CTAs' copies complete on
+    const int rank = CG == 2 ? (int)cluster_ctarank() : 0;
+    const bool leader = rank == 0;
+    const int unit0 = (int)blockIdx.x / CG, unit_step = (int)gridDim.x / CG;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) { mbar_init(&S.full[s], 1); mbar_init(&S.empty[s], 1); }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&S.acc_full[a], 1);
-            mbar_init(&S.acc_empty[a], EPI_WARPS);
+            mbar_init(&S.acc_empty[a], EPI_WARPS * CG);
         }
         mbar_init(&S.drain, 1);
         S.abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
-        tmem_alloc<1>(&S.tmem_base, TMEM_COLS);
-        tmem_relinquish<1>();
+        tmem_alloc<CG>(&S.tmem_base, TMEM_COLS);
+        tmem_relinquish<CG>();
     }
     pdl_wait();
     pdl_launch_dependents();
     for (int i = threadIdx.x; i <= p.E; i += THREADS) S.offs[i] = p.offsets[i];
     __syncthreads();
     if (MODE != kWG && warp == 0) {
-        // prefix[e] = tiles of experts < e (lane l owns a contiguous run)
+        // prefix[e] = units of experts < e (lane l owns a contiguous run)
         const int per = (p.E + 31) / 32, e0 = lane * per;
         int local = 0;
         for (int e = e0; e < e0 + per && e < p.E; ++e)
-            local += (S.offs[e + 1] - S.offs[e] + BM - 1) / BM * p.n_tiles;
+            local += (S.offs[e + 1] - S.offs[e] + MU - 1) / MU * p.n_tiles;
         int incl = local;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -266,16 +285,19 @@ bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant_
         int run = incl - local;
         for (int e = e0; e < e0 + per && e < p.E; ++e) {
             S.prefix[e] = run;
-            run += (S.offs[e + 1] - S.offs[e] + BM - 1) / BM * p.n_tiles;
+            run += (S.offs[e + 1] - S.offs[e] + MU - 1) / MU * p.n_tiles;
         }
         if (lane == 31) S.prefix[p.E] = incl;
     }
     tc_fence_before();
-    __syncthreads();
+    // a pair also makes each CTA's barrier initialisation visible to the
+    // other before any copy or arrival targets it
+    if constexpr (CG == 2) cluster_sync();
+    else __syncthreads();
     tc_fence_after();
 
     const uint32_t tmem_base = S.tmem_base;
-    const int total_tiles = MODE == kWG ? p.nprob * p.E * ((p.M + BM - 1) / BM) * p.n_tiles
+    const int total_tiles = MODE == kWG ? p.nprob * p.E * ((p.M + MU - 1) / MU) * p.n_tiles
                                         : S.prefix[p.E];
     volatile int *abort_flag = &S.abort;
     uint32_t filled_mask = 0, filled_parity = 0;       // producer: stages in flight
@@ -285,11 +307,13 @@ bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant_
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+        for (int tile = unit0; tile < total_tiles && ok; tile += unit_step) {
             int e, m, n, prob;
-            decode<MODE>(S, p, tile, e, m, n, prob);
-            const int nkb = k_blocks<MODE>(S, p, e);
+            decode<MODE, CG>(S, p, tile, e, m, n, prob);
+            const int nkb = k_blocks<MODE, CG>(S, p, e);
             const int seg0 = S.offs[e];
+            const int a_row = m * MU + rank * BM;               // this CTA's first A row / M element
+            const int b_col = n * BN + rank * (BN / CG);        // this CTA's first B column
             const CUtensorMap *wa = nullptr, *wb = nullptr;
             if constexpr (MODE == kWG) {
                 const uint8_t *maps = p.emaps + (size_t)e * p.maps_per_expert * MAP_BYTES;
@@ -301,59 +325,70 @@ bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant_
                 }
             }
             for (int kb = 0; kb < nkb; ++kb) {
-                if (!mbar_wait(&S.empty[stage], phase ^ 1u, abort_flag, status, p.wait_ns)) { ok = false; break; }
-                uint64_t *bar = &S.full[stage];
+                if (!mbar_wait<CG>(&S.empty[stage], phase ^ 1u, abort_flag, status, p.wait_ns)) { ok = false; break; }
                 uint8_t *sa = S.stage[stage];
                 uint8_t *sb = sa + A_BYTES;
-                mbar_arrive_expect_tx(bar, STAGE_BYTES);
+                // both CTAs' copies complete on the leader's barrier, which
+                // expects both; a peer's copy may land before the leader arms
+                // it (the phase cannot complete while the leader's arrival is
+                // pending)
+                if (leader) mbar_arrive_expect_tx(&S.full[stage], CG * STAGE_BYTES);
+                const uint32_t bar = CG == 2 ? mapa_shared(smem_u32(&S.full[stage]), 0)
+                                             : smem_u32(&S.full[stage]);
+                auto load2 = [&](void *dst, const CUtensorMap *map, int c0, int c1) {
+                    if constexpr (CG == 2) tma_load_2d_pair(dst, map, bar, c0, c1);
+                    else tma_load_2d(dst, map, &S.full[stage], c0, c1);
+                };
+                auto load3 = [&](void *dst, const CUtensorMap *map, int c0, int c1, int c2) {
+                    if constexpr (CG == 2) tma_load_3d_pair(dst, map, bar, c0, c1, c2);
+                    else tma_load_3d(dst, map, &S.full[stage], c0, c1, c2);
+                };
                 if constexpr (MODE == kDH) {
-                    const int row0 = seg0 + m * BM;
-                    tma_load_2d(sa, &tmA0, bar, kb * BK, row0);
+                    load2(sa, &tmA0, kb * BK, seg0 + a_row);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        tma_load_3d(sb + j * BOX_BYTES, &tmB0, bar, n * BN + j * BOX, kb * BK, e);
+                    for (int j = 0; j < B_BOXES; ++j)
+                        load3(sb + j * BOX_BYTES, &tmB0, b_col + j * BOX, kb * BK, e);
                 } else if constexpr (MODE == kDX) {
-                    const int row0 = seg0 + m * BM;
                     const int half = (p.num_k + BK - 1) / BK;
                     const bool second = kb >= half;
                     const int kk = (second ? kb - half : kb) * BK;
-                    tma_load_2d(sa, second ? &tmA1 : &tmA0, bar, kk, row0);
+                    load2(sa, second ? &tmA1 : &tmA0, kk, seg0 + a_row);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        tma_load_3d(sb + j * BOX_BYTES, second ? &tmB1 : &tmB0, bar, n * BN + j * BOX, kk, e);
+                    for (int j = 0; j < B_BOXES; ++j)
+                        load3(sb + j * BOX_BYTES, second ? &tmB1 : &tmB0, b_col + j * BOX, kk, e);
                 } else {
                     // rows relative to the expert's own maps: past its last row
                     // the TMA fills zeros
 #pragma unroll
                     for (int j = 0; j < 2; ++j)
-                        tma_load_2d(sa + j * BOX_BYTES, wa, bar, m * BM + j * BOX, kb * BK);
+                        load2(sa + j * BOX_BYTES, wa, a_row + j * BOX, kb * BK);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        tma_load_2d(sb + j * BOX_BYTES, wb, bar, n * BN + j * BOX, kb * BK);
+                    for (int j = 0; j < B_BOXES; ++j)
+                        load2(sb + j * BOX_BYTES, wb, b_col + j * BOX, kb * BK);
                 }
                 filled_mask |= 1u << stage;
                 filled_parity = (filled_parity & ~(1u << stage)) | (phase << stage);
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
         }
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1 && lane == 0 && leader) {
         // ------------------------------------------------------ MMA issuer
-        constexpr uint32_t idesc = idesc_f16_major<DT>(BM, BN, MODE == kWG, true);
+        constexpr uint32_t idesc = idesc_f16_major<DT>(BM * CG, BN, MODE == kWG, true);
         int stage = 0;
         uint32_t phase = 0;
         int it = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++it) {
+        for (int tile = unit0; tile < total_tiles && ok; tile += unit_step, ++it) {
             int e, m, n, prob;
-            decode<MODE>(S, p, tile, e, m, n, prob);
-            const int nkb = k_blocks<MODE>(S, p, e);
+            decode<MODE, CG>(S, p, tile, e, m, n, prob);
+            const int nkb = k_blocks<MODE, CG>(S, p, e);
             const int acc = it & 1;
             const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
-            if (!mbar_wait(&S.acc_empty[acc], acc_phase ^ 1u, abort_flag, status, p.wait_ns)) { ok = false; break; }
+            if (!mbar_wait<CG>(&S.acc_empty[acc], acc_phase ^ 1u, abort_flag, status, p.wait_ns)) { ok = false; break; }
             tc_fence_after();
             const uint32_t d = tmem_base + (uint32_t)(acc * ACC_COLS);
             for (int kb = 0; kb < nkb; ++kb) {
-                if (!mbar_wait(&S.full[stage], phase, abort_flag, status, p.wait_ns)) { ok = false; break; }
+                if (!mbar_wait<CG>(&S.full[stage], phase, abort_flag, status, p.wait_ns)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t a0 = smem_u32(S.stage[stage]);
                 const uint32_t b0 = a0 + A_BYTES;
@@ -362,16 +397,21 @@ bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant_
                     const uint64_t ad = MODE == kWG ? sdesc_mn_sw128(a0 + k * UK * 128, BOX_BYTES)
                                                     : sdesc_k_sw128(a0 + k * UK * 2);
                     const uint64_t bd = sdesc_mn_sw128(b0 + k * UK * 128, BOX_BYTES);
-                    umma_f16<1>(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                    umma_f16<CG>(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
                 }
-                umma_commit<1>(&S.empty[stage]);
+                if constexpr (CG == 2) umma_commit_pair(&S.empty[stage]);
+                else umma_commit<1>(&S.empty[stage]);
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
             // (an expert without rows commits with no MMA: its epilogue writes zeros)
-            if (ok) umma_commit<1>(&S.acc_full[acc]);
+            if (ok) {
+                if constexpr (CG == 2) umma_commit_pair(&S.acc_full[acc]);
+                else umma_commit<1>(&S.acc_full[acc]);
+            }
         }
         if (*abort_flag) {
-            umma_commit<1>(&S.drain);
+            // every MMA issued so far must finish before TMEM is released
+            umma_commit<CG>(&S.drain);
             mbar_wait(&S.drain, 0, nullptr, status, kDrainLimitNs);
         }
     } else if (warp >= 2) {
@@ -380,20 +420,20 @@ bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant_
         static_assert(MODE == kDH || EPI_WARPS == 4, "only DH splits columns over two warps");
         uint8_t *stg = S.epi[warp - 2];
         int it = 0;
-        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++it) {
+        for (int tile = unit0; tile < total_tiles; tile += unit_step, ++it) {
             int e, m, n, prob;
-            decode<MODE>(S, p, tile, e, m, n, prob);
+            decode<MODE, CG>(S, p, tile, e, m, n, prob);
             const int acc = it & 1;
             const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
-            const bool ready = mbar_wait(&S.acc_full[acc], acc_phase, abort_flag, status, p.wait_ns);
+            const bool ready = mbar_wait<CG>(&S.acc_full[acc], acc_phase, abort_flag, status, p.wait_ns);
             if (!__all_sync(0xffffffffu, ready)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
             if constexpr (MODE == kWG) {
-                // rows: weight rows m*128 + q*32 + r; FP32, 32 columns per round;
-                // the next round's tensor-memory load is in flight while the
-                // current one is stored
-                const int row0 = m * BM + q * 32;
+                // rows: weight rows m*MU + rank*128 + q*32 + r; FP32, 32 columns
+                // per round; the next round's tensor-memory load is in flight
+                // while the current one is stored
+                const int row0 = m * MU + rank * BM + q * 32;
                 const int rows_valid = p.M - row0;
                 const bool empty_expert = S.offs[e + 1] == S.offs[e];
                 uint8_t *W = (prob ? p.out1 : p.out0) + ((int64_t)e * p.M + row0) * p.out_row_bytes;
@@ -421,7 +461,7 @@ bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant_
                 }
             } else {
                 const int seg_rows = S.offs[e + 1] - S.offs[e];
-                const int r_seg = m * BM + q * 32;                      // warp's first row in the segment
+                const int r_seg = m * MU + rank * BM + q * 32;          // warp's first row in the segment
                 const int rows_valid = seg_rows - r_seg;
                 const int64_t grow0 = (int64_t)S.offs[e] + r_seg;       // its dispatched row
                 uint8_t *ob = p.out0 + grow0 * p.out_row_bytes;
@@ -492,48 +532,121 @@ bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant_
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&S.acc_empty[acc]);
+            if (lane == 0) {
+                if (CG == 2 && !leader) mbar_arrive_cluster(mapa_shared(smem_u32(&S.acc_empty[acc]), 0));
+                else mbar_arrive(&S.acc_empty[acc]);
+            }
         }
     }
 
     // ------------------------------------------------------------ teardown
     __syncthreads();
     if (*abort_flag && warp == 0 && lane == 0) {
-        for (int s = 0; s < STAGES; ++s)
-            if (filled_mask >> s & 1u)
-                mbar_wait(&S.full[s], filled_parity >> s & 1u, nullptr, status, kDrainLimitNs);
+        if (CG == 1 || leader) {
+            // let the outstanding TMA copies land before shared memory goes
+            for (int s = 0; s < STAGES; ++s)
+                if (filled_mask >> s & 1u)
+                    mbar_wait(&S.full[s], filled_parity >> s & 1u, nullptr, status, kDrainLimitNs);
+        } else {
+            // a peer's copies complete on the leader's barriers, which it
+            // cannot wait on: give them the same bounded time to land
+            const uint64_t t0 = global_timer_ns();
+            while (global_timer_ns() - t0 < kDrainLimitNs) { }
+        }
     }
-    __syncthreads();
+    // a pair keeps both CTAs (their shared memory is read by the leader's
+    // MMAs and signalled by its commits) until both are done
+    if constexpr (CG == 2) cluster_sync();
+    else __syncthreads();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc<1>(tmem_base, TMEM_COLS);
+        tmem_dealloc<CG>(tmem_base, TMEM_COLS);
     }
 }
 
 // ---- host side ---------------------------------------------------------------
 
-template <int DT, int MODE>
-cudaError_t launch_step(int64_t units, const CUtensorMap &a0, const CUtensorMap &a1,
-                        const CUtensorMap &b0, const CUtensorMap &b1, const BwdParams &p,
-                        cudaStream_t s)
+// Experts averaging at least this many rows run the backward GEMMs on CTA
+// pairs: a CTA then holds 32 KiB stages instead of 48, so six fit (five
+// beside dh's eight staging buffers), and more of the copies' latency is
+// covered. With a few hundred rows per expert (weight gradients reducing over
+// K = 384) the pairs measured slower.
+#ifndef MOE_BWD_PAIR_MIN_ROWS
+#define MOE_BWD_PAIR_MIN_ROWS 2048
+#endif
+// Which launches may pair (bit 0: dh, bit 1: dx, bit 2: weight gradients).
+#ifndef MOE_BWD_PAIR_MODES
+#define MOE_BWD_PAIR_MODES 7
+#endif
+
+template <int DT, int MODE, int CG>
+cudaError_t launch_step_cg(int64_t units, const CUtensorMap &a0, const CUtensorMap &a1,
+                           const CUtensorMap &b0, const CUtensorMap &b1, const BwdParams &p,
+                           cudaStream_t s)
 {
     static std::atomic<uint64_t> done_mask{0};
+    static std::atomic<int> pairs_cached[kCachedDevices];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    const uint64_t bit = dev >= 0 && dev < kCachedDevices ? 1ull << dev : 0ull;
+    const bool use_cache = dev >= 0 && dev < kCachedDevices;
+    const uint64_t bit = use_cache ? 1ull << dev : 0ull;
     if (bit == 0 || !(done_mask.load() & bit)) {
-        err = cudaFuncSetAttribute(bwd_gemm_kernel<DT, MODE>,
+        err = cudaFuncSetAttribute(bwd_gemm_kernel<DT, MODE, CG>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)kBwdSmemBytes<MODE>);
+                                   (int)kBwdSmemBytes<MODE, CG>);
         if (err != cudaSuccess) return err;
         done_mask.fetch_or(bit);
     }
     const int64_t sms = device_sm_count();
-    const int grid = (int)(units < sms ? (units < 1 ? 1 : units) : sms);
-    return launch_pdl(bwd_gemm_kernel<DT, MODE>, dim3((unsigned)grid), dim3(threads_of<MODE>()),
-                      kBwdSmemBytes<MODE>, s, a0, a1, b0, b1, p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(threads_of<MODE>());
+    cfg.dynamicSmemBytes = kBwdSmemBytes<MODE, CG>;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = CG;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    int grid = 0;
+    if constexpr (CG == 1) {
+        grid = (int)(units < sms ? (units < 1 ? 1 : units) : sms);
+        cfg.numAttrs = 1;
+    } else {
+        // one wave of pairs: as many as the GPU holds at once (cluster
+        // placement can leave SMs unpaired)
+        int pairs = use_cache ? pairs_cached[dev].load() : 0;
+        if (pairs == 0) {
+            cudaLaunchConfig_t q = cfg;
+            q.gridDim = dim3((unsigned)(sms & ~int64_t(1)));
+            q.attrs = &attr[1];
+            q.numAttrs = 1;
+            err = cudaOccupancyMaxActiveClusters(&pairs, bwd_gemm_kernel<DT, MODE, CG>, &q);
+            if (err != cudaSuccess) return err;
+            if (pairs < 1) return cudaErrorInvalidConfiguration;
+            if (use_cache) pairs_cached[dev].store(pairs);
+        }
+        grid = 2 * (int)(units < pairs ? (units < 1 ? 1 : units) : pairs);
+        cfg.numAttrs = 2;
+    }
+    cfg.gridDim = dim3((unsigned)grid);
+    return cudaLaunchKernelEx(&cfg, bwd_gemm_kernel<DT, MODE, CG>, a0, a1, b0, b1, p);
+}
+
+// units1 / units2: upper bounds on the launch's work units with m-units of
+// 128 rows (single CTAs) and of 256 (pairs)
+template <int DT, int MODE>
+cudaError_t launch_step(bool pair, int64_t units1, int64_t units2, const CUtensorMap &a0,
+                        const CUtensorMap &a1, const CUtensorMap &b0, const CUtensorMap &b1,
+                        const BwdParams &p, cudaStream_t s)
+{
+    if (pair && (MOE_BWD_PAIR_MODES >> MODE & 1))
+        return launch_step_cg<DT, MODE, 2>(units2, a0, a1, b0, b1, p, s);
+    return launch_step_cg<DT, MODE, 1>(units1, a0, a1, b0, b1, p, s);
 }
 
 template <int DT>
@@ -589,6 +702,7 @@ cudaError_t launch_backward(const void *x_disp, const int32_t *offsets, int64_t 
                      offsets, maps_gu);
     if (err != cudaSuccess) return err;
 
+    const bool pair = rows >= (int64_t)MOE_BWD_PAIR_MIN_ROWS * E;
     BwdParams p{};
     p.offsets = offsets;
     p.E = E;
@@ -596,6 +710,7 @@ cudaError_t launch_backward(const void *x_disp, const int32_t *offsets, int64_t 
     p.wait_ns = wait_limit_ns();
     if (rows > 0) {
         const int64_t mt = rows / BM + (rows < E ? rows : E);     // M-tiles, upper bound
+        const int64_t mt2 = rows / (2 * BM) + (rows < E ? rows : E);   // pair m-units
         // DH: dh, then dg / du into dgu
         p.n_tiles = (int)((I + BN - 1) / BN);
         p.num_k = (int)H;
@@ -605,7 +720,7 @@ cudaError_t launch_backward(const void *x_disp, const int32_t *offsets, int64_t 
         p.out0 = static_cast<uint8_t *>(dgu);
         p.out_row_bytes = 4 * I;
         p.du_col_bytes = 2 * I;
-        err = launch_step<DT, kDH>(mt * p.n_tiles, dh_a, dh_a, dh_b, dh_b, p, s);
+        err = launch_step<DT, kDH>(pair, mt * p.n_tiles, mt2 * p.n_tiles, dh_a, dh_a, dh_b, dh_b, p, s);
         if (err != cudaSuccess) return err;
         // DX
         p.n_tiles = (int)((H + BN - 1) / BN);
@@ -613,7 +728,7 @@ cudaError_t launch_backward(const void *x_disp, const int32_t *offsets, int64_t 
         p.N = (int)H;
         p.out0 = static_cast<uint8_t *>(dx);
         p.out_row_bytes = 2 * H;
-        err = launch_step<DT, kDX>(mt * p.n_tiles, dx_a0, dx_a1, dx_b0, dx_b1, p, s);
+        err = launch_step<DT, kDX>(pair, mt * p.n_tiles, mt2 * p.n_tiles, dx_a0, dx_a1, dx_b0, dx_b1, p, s);
         if (err != cudaSuccess) return err;
     }
     // WG: dWd (M = H rows of Wd, N = I)
@@ -626,8 +741,9 @@ cudaError_t launch_backward(const void *x_disp, const int32_t *offsets, int64_t 
     p.out_row_bytes = 4 * I;
     p.emaps = maps_d;
     p.maps_per_expert = 2;
-    err = launch_step<DT, kWG>((int64_t)E * ((H + BM - 1) / BM) * p.n_tiles, wd_a, wd_a, wd_b,
-                               wd_b, p, s);
+    err = launch_step<DT, kWG>(pair, (int64_t)E * ((H + BM - 1) / BM) * p.n_tiles,
+                               (int64_t)E * ((H + 2 * BM - 1) / (2 * BM)) * p.n_tiles, wd_a, wd_a,
+                               wd_b, wd_b, p, s);
     if (err != cudaSuccess) return err;
     // WG: dWg, dWu (M = I rows, N = H)
     p.M = (int)I;
@@ -639,8 +755,9 @@ cudaError_t launch_backward(const void *x_disp, const int32_t *offsets, int64_t 
     p.out_row_bytes = 4 * H;
     p.emaps = maps_gu;
     p.maps_per_expert = 3;
-    return launch_step<DT, kWG>(2 * (int64_t)E * ((I + BM - 1) / BM) * p.n_tiles, wgu_a0, wgu_a1,
-                                wgu_b, wgu_b, p, s);
+    return launch_step<DT, kWG>(pair, 2 * (int64_t)E * ((I + BM - 1) / BM) * p.n_tiles,
+                                2 * (int64_t)E * ((I + 2 * BM - 1) / (2 * BM)) * p.n_tiles, wgu_a0,
+                                wgu_a1, wgu_b, wgu_b, p, s);
 }
 
 }  // namespace

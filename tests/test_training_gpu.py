@@ -207,6 +207,13 @@ EXPERT_CASES = [
     # leave K and N tails
     ("pair_skewed_bf16", 900, 200, 200, 3, 1, torch.bfloat16, 1.0),
     ("pair_f16", 640, 384, 320, 4, 2, torch.float16, 0.0),
+    # at least 2048 rows per expert on average: the backward GEMMs run on CTA
+    # pairs as well (M = 256; weight gradients reduce over thousands of rows);
+    # K / N / M tails, one expert, and a skewed split where one expert holds
+    # few rows
+    ("bwd_pairs_bf16", 4500, 200, 328, 2, 1, torch.bfloat16, 0.8),
+    ("bwd_pairs_one_expert_f16", 5200, 264, 136, 1, 1, torch.float16, 0.0),
+    ("bwd_pairs_skewed_bf16", 6400, 136, 200, 3, 1, torch.bfloat16, 3.0),
 ]
 
 
