@@ -388,3 +388,33 @@ def check_swiglu_cache_matches_forward(lib):
         down = np.zeros((E, H, I)); down[:, 0, i] = 1.0
         out = oracle.experts_dispatched(x, "f64", offsets.astype(np.int32), gate, up, down, lib)
         assert np.allclose(out[:, 0], h[:, i], rtol=1e-14, atol=0)
+
+
+def check_swiglu_backward_column_restriction(lib):
+    """The full-size training test reads an expert's weight gradients at a few
+    intermediate columns from the backward of the expert restricted to those
+    columns (rows of Wg / Wu, columns of Wd). In a SwiGLU FFN column i
+    touches only row i of Wg / Wu and column i of Wd, so the restricted
+    backward's weight gradients equal the full one's at those columns, bit for
+    bit, for any input dtype."""
+    rng = np.random.default_rng(23)
+    H, I, n = 24, 20, 11
+    cols = [0, 7, 19]
+    for dt in ("f64", "bf16"):
+        x = rng.standard_normal((n, H))
+        gate = rng.standard_normal((1, I, H)) / 4
+        up = rng.standard_normal((1, I, H)) / 4
+        down = rng.standard_normal((1, H, I)) / 3
+        dout = rng.standard_normal((n, H))
+        if dt == "bf16":
+            x, gate, up, down = (oracle.convert(a.astype(np.float32), "f32", "bf16", lib)
+                                 for a in (x, gate, up, down))
+        eor = np.zeros(n, np.int32)
+        _, dg, du, dd = oracle.swiglu_backward_rows(x, dt, eor, gate, up, down, dout, "f64", lib)
+        gs = np.ascontiguousarray(gate[:, cols, :])
+        us = np.ascontiguousarray(up[:, cols, :])
+        ds = np.ascontiguousarray(down[:, :, cols])
+        _, dgs, dus, dds = oracle.swiglu_backward_rows(x, dt, eor, gs, us, ds, dout, "f64", lib)
+        assert np.array_equal(dgs[0], dg[0][cols, :]), f"{dt}: gate gradient rows"
+        assert np.array_equal(dus[0], du[0][cols, :]), f"{dt}: up gradient rows"
+        assert np.array_equal(dds[0], dd[0][:, cols]), f"{dt}: down gradient columns"
