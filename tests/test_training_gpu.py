@@ -214,6 +214,9 @@ EXPERT_CASES = [
     ("bwd_pairs_bf16", 4500, 200, 328, 2, 1, torch.bfloat16, 0.8),
     ("bwd_pairs_one_expert_f16", 5200, 264, 136, 1, 1, torch.float16, 0.0),
     ("bwd_pairs_skewed_bf16", 6400, 136, 200, 3, 1, torch.bfloat16, 3.0),
+    # two experts without rows (their weight gradients written as zeros) and
+    # one of 13 rows beside one of 8987
+    ("bwd_pairs_empty_experts_bf16", 9000, 136, 200, 4, 1, torch.bfloat16, 6.0),
 ]
 
 
