@@ -196,13 +196,19 @@ __device__ __forceinline__ void tensormap_acquire(const void *map)
 // Per-expert tensor maps for the weight-gradient GEMMs: for expert e and map
 // j, a copy of base[j] whose base address is the expert's first row and whose
 // row count is the expert's (at least 1), at out + (e * nmaps + j) * 128.
-// One warp per expert; lanes 8j..8j+7 copy map j, lane j rewrites it.
+// One warp per expert builds its maps in shared memory (lanes 8j..8j+7 copy
+// map j, lane j rewrites its address and row count there), then the warp
+// publishes each whole 128-byte map with one tensormap.cp_fenceproxy copy,
+// which releases it to the tensormap proxy that the consumers' TMA copies
+// read it through (after their acquire fence): no map is ever visible in
+// global memory half old and half new.
 __global__ void __launch_bounds__(32)
 expert_maps_kernel(const __grid_constant__ CUtensorMap base0, const __grid_constant__ CUtensorMap base1,
                    const __grid_constant__ CUtensorMap base2, uint64_t addr0, uint64_t addr1,
                    uint64_t addr2, int64_t stride0, int64_t stride1, int64_t stride2, int nmaps,
                    const int32_t *__restrict__ offsets, uint8_t *__restrict__ out)
 {
+    __shared__ __align__(128) uint8_t sm[3 * MAP_BYTES];
     pdl_wait();
     const int e = blockIdx.x, lane = threadIdx.x;
     const int r0 = offsets[e], rows = offsets[e + 1] - r0;
@@ -210,22 +216,25 @@ expert_maps_kernel(const __grid_constant__ CUtensorMap base0, const __grid_const
     if (lane < 8 * nmaps) {
         const int j = lane >> 3, c = lane & 7;
         const CUtensorMap *src = j == 0 ? &base0 : j == 1 ? &base1 : &base2;
-        reinterpret_cast<uint4 *>(slot + j * MAP_BYTES)[c] =
-            reinterpret_cast<const uint4 *>(src)[c];
+        reinterpret_cast<uint4 *>(sm + j * MAP_BYTES)[c] = reinterpret_cast<const uint4 *>(src)[c];
     }
     __syncwarp();
     if (lane < nmaps) {
         const uint64_t a = lane == 0 ? addr0 : lane == 1 ? addr1 : addr2;
         const int64_t st = lane == 0 ? stride0 : lane == 1 ? stride1 : stride2;
-        uint8_t *map = slot + lane * MAP_BYTES;
+        const uint32_t map = smem_u32(sm + lane * MAP_BYTES);
         const uint64_t first = a + (uint64_t)((int64_t)r0 * st);
         const uint32_t n = (uint32_t)(rows > 0 ? rows : 1);
-        asm volatile("tensormap.replace.tile.global_address.global.b1024.b64 [%0], %1;"
-                     ::"l"(map), "l"(first) : "memory");
-        asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 1, %1;"
-                     ::"l"(map), "r"(n) : "memory");
-        asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+        asm volatile("tensormap.replace.tile.global_address.shared::cta.b1024.b64 [%0], %1;"
+                     ::"r"(map), "l"(first) : "memory");
+        asm volatile("tensormap.replace.tile.global_dim.shared::cta.b1024.b32 [%0], 1, %1;"
+                     ::"r"(map), "r"(n) : "memory");
     }
+    __syncwarp();
+    for (int j = 0; j < nmaps; ++j)
+        asm volatile("tensormap.cp_fenceproxy.global.shared::cta.tensormap::generic.release.gpu"
+                     ".sync.aligned [%0], [%1], 128;"
+                     ::"l"(slot + j * MAP_BYTES), "r"(smem_u32(sm + j * MAP_BYTES)) : "memory");
     pdl_launch_dependents();
 }
 
